@@ -1,0 +1,468 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Every check here compares the oracle with something other than itself: the
+tutorial's worked chain, library routines (scipy logsumexp, numpy sorts),
+closed forms, brute-force enumeration on tiny trees, an independent
+sequence-based attention, and exact probabilities of the acceptance rule.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+from scipy.special import logsumexp
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _run_tree(cfg, logits, prefix_len=None, root_token=None):
+    """Oracle stages 1-4 on draft logits [B, D, k, V]."""
+    t = oracle.Tree(cfg)
+    for s in range(cfg.depth):
+        t.expand(s, np.ascontiguousarray(logits[:, s]))
+    t.rerank()
+    B = cfg.batch
+    pl = np.zeros(B, np.int32) if prefix_len is None else prefix_len
+    rt = np.zeros(B, np.int32) if root_token is None else root_token
+    return t, t.build_tree(pl, rt)
+
+
+# ------------------------------------------------------------ worked chain ---
+
+def test_worked_chain_sum_of_values():
+    g = json.load(open(os.path.join(GOLDEN, "worked_chain.json")))
+    vals = g["path_values"]
+    D = len(vals)
+    conf = [vals[0]] + [vals[i] / vals[i - 1] for i in range(1, D)]
+    V, k = 2, 1
+    cfg = oracle.TreeCfg(batch=1, vocab=V, top_k=k, depth=D, node_budget=D)
+    logits = np.zeros((1, D, k, V), np.float32)
+    for s, c in enumerate(conf):
+        logits[0, s, 0] = [math.log(c), math.log(1.0 - c)]
+    t, tr = _run_tree(cfg, logits)
+    kept_vals = np.exp(t.logv[0][t.kept[0] == 1].astype(np.float64))
+    np.testing.assert_allclose(np.sort(kept_vals)[::-1], vals, atol=1e-6)
+    assert abs(t.value_sum(0) - g["expected_accepted"]) < 1e-6
+    assert tr["n_tree"][0] == D + 1
+    assert list(tr["parent"][0]) == [-1, 0, 1, 2, 3]
+
+
+# ----------------------------------------------------------------- stage 1 ---
+
+@pytest.mark.parametrize("dtype", [synth.F32, synth.BF16])
+def test_row_lse_matches_scipy(dtype):
+    V = 4099
+    rows = synth.normal4((6, V), dtype, 2.5, seed=3, stream=synth.STREAM_DRAFT)
+    for r in range(rows.shape[0]):
+        row = rows[r]
+        x = row.astype(np.float64) if dtype == synth.F32 else synth.bf16_to_f32(row).astype(np.float64)
+        lse64, lse32, _ = oracle.row_stats(row, 5)
+        assert abs(lse64 - logsumexp(x)) <= 1e-12 * abs(lse64) + 1e-12
+        assert lse32 == np.float32(lse64)
+
+
+def test_row_lse_closed_forms():
+    V = 1000
+    row = np.full(V, 0.75, np.float32)
+    lse64, _, top = oracle.row_stats(row, 4)
+    assert abs(lse64 - (0.75 + math.log(V))) < 1e-12
+    assert list(top) == [0, 1, 2, 3]  # all equal: lowest ids first
+    row = np.full(V, -300.0, np.float32)
+    row[417] = 5.0
+    lse64, lse32, top = oracle.row_stats(row, 1)
+    assert lse32 == np.float32(5.0) and top[0] == 417
+
+
+@pytest.mark.parametrize("dtype", [synth.F32, synth.BF16])
+def test_topk_matches_lexsort_with_ties(dtype):
+    V, k = 2048, 10
+    rows = synth.normal4((8, V), dtype, 1.0, seed=11, stream=synth.STREAM_DRAFT)
+    # plant exact ties at the top of some rows
+    rows[0, [5, 900, 77]] = rows[0].max() if dtype == synth.F32 else rows[0, np.argmax(synth.bf16_to_f32(rows[0]))]
+    rows[1, :] = rows[1, 0]
+    for r in range(rows.shape[0]):
+        row = np.ascontiguousarray(rows[r])
+        x = row if dtype == synth.F32 else synth.bf16_to_f32(row)
+        want = np.lexsort((np.arange(V), -x.astype(np.float64)))[:k]
+        _, _, top = oracle.row_stats(row, k)
+        assert list(top) == list(want)
+
+
+def test_dexp_accuracy():
+    z = np.concatenate([np.linspace(-32.0, 0.0, 200001, dtype=np.float32),
+                        np.array([0.0, -1e-8, -0.5, -0.34657359, -0.34657360, -31.999, -32.0], np.float32)])
+    worst = 0.0
+    for v in z[::7]:
+        got = oracle.dexp(float(v))
+        ref = math.exp(float(v))
+        worst = max(worst, abs(got - ref) / ref)
+    assert worst < 4 * 2.0 ** -23, worst
+    assert oracle.dexp(0.0) == 1.0
+    assert oracle.dexp(-32.5) == 0.0
+
+
+# ------------------------------------------------------- stage 2: threshold ---
+
+def test_threshold_stops_expansion():
+    V, k = 4, 2
+    cfg = oracle.TreeCfg(batch=1, vocab=V, top_k=k, depth=3, node_budget=6, threshold=0.4)
+    logits = np.full((1, 3, k, V), -30.0, np.float32)
+    logits[0, 0, 0] = np.log([0.5, 0.3, 0.15, 0.05])
+    logits[0, 1, 0] = np.log([0.9, 0.05, 0.03, 0.02])
+    logits[0, 2, 0] = np.log([0.25, 0.25, 0.25, 0.25])
+    t = oracle.Tree(cfg)
+    tok0, cnt0 = t.expand(0, np.ascontiguousarray(logits[:, 0]))
+    assert cnt0[0] == 1 and tok0[0, 0] == 0 and tok0[0, 1] == -1  # 0.3 < 0.4 is not expanded
+    tok1, cnt1 = t.expand(1, np.ascontiguousarray(logits[:, 1]))
+    assert cnt1[0] == 1 and tok1[0, 0] == 0  # 0.45 >= 0.4, 0.025 < 0.4
+    vals = np.exp(t.logv[0, :k + k * k].astype(np.float64))
+    np.testing.assert_allclose(vals[:2], [0.5, 0.3], rtol=1e-6)
+    np.testing.assert_allclose(vals[2:4], [0.45, 0.025], rtol=1e-6)
+    assert not t.valid[0, 4:6].any()  # frontier slot 1 of step 1 did not exist
+    t.expand(2, np.ascontiguousarray(logits[:, 2]))
+    t.rerank()
+    # nodes below the threshold stay candidates for the rerank
+    kept_vals = sorted(np.exp(t.logv[0][t.kept[0] == 1].astype(np.float64)), reverse=True)
+    np.testing.assert_allclose(kept_vals[:3], [0.5, 0.45, 0.3], rtol=1e-6)
+
+
+def test_figure_parameters_config():
+    g = json.load(open(os.path.join(GOLDEN, "expand_rerank_params.json")))
+    k, N, thr = g["top_k"], g["node_budget"], g["threshold"]
+    cfg = oracle.TreeCfg(batch=16, vocab=64, top_k=k, depth=3, node_budget=N, threshold=thr)
+    logits = synth.normal4((16, 3, k, 64), synth.F32, 2.5, seed=5, stream=synth.STREAM_DRAFT)
+    t = oracle.Tree(cfg)
+    for s in range(3):
+        base = oracle.step_base(s, k)
+        F = t.fcount.copy()
+        t.expand(s, np.ascontiguousarray(logits[:, s]))
+        for b in range(16):
+            ids = np.arange(base, base + F[b] * k)
+            v = t.logv[b, ids]
+            elig = ids[v >= np.float32(math.log(thr))]
+            order = elig[np.lexsort((elig, -t.logv[b, elig].astype(np.float64)))][:k]
+            assert t.fcount[b] == len(order)
+            assert list(t.fnode[b, :len(order)]) == list(order)
+    t.rerank()
+    tr = t.build_tree(np.zeros(16, np.int32), np.zeros(16, np.int32))
+    assert (tr["n_tree"] <= N + 1).all()
+
+
+# ---------------------------------------------------- stage 3: brute force ---
+
+def _ancestor_closed(sub, parent):
+    s = set(sub)
+    return all(parent[i] < 0 or parent[i] in s for i in sub)
+
+
+@pytest.mark.parametrize("k,D,N", [(2, 3, 3), (2, 3, 5), (3, 2, 4), (3, 2, 7), (2, 2, 2)])
+def test_rerank_maximises_value_over_connected_subtrees(k, D, N):
+    V = 16
+    B = 12
+    cfg = oracle.TreeCfg(batch=B, vocab=V, top_k=k, depth=D, node_budget=N)
+    logits = synth.normal4((B, D, k, V), synth.F32, 1.7, seed=100 + k * 10 + D + N, stream=synth.STREAM_DRAFT)
+    t, tr = _run_tree(cfg, logits)
+    for b in range(B):
+        valid = [i for i in range(cfg.C) if t.valid[b, i]]
+        val = np.exp(t.logv[b].astype(np.float64))
+        n = min(N, len(valid))
+        best = -1.0
+        best_set = None
+        for sub in itertools.combinations(valid, n):
+            if not _ancestor_closed(sub, t.parent[b]):
+                continue
+            s = float(sum(val[list(sub)]))
+            if s > best:
+                best, best_set = s, set(sub)
+        kept = set(np.nonzero(t.kept[b])[0].tolist())
+        assert _ancestor_closed(kept, t.parent[b])
+        assert abs(sum(val[list(kept)]) - best) <= 1e-12 * best
+        assert kept == best_set
+
+
+def test_rerank_tie_keeps_shallower():
+    # A child with confidence exactly 1 in fp32 (lp == 0) ties with its parent.
+    V, k = 8, 1
+    cfg = oracle.TreeCfg(batch=1, vocab=V, top_k=k, depth=2, node_budget=1)
+    logits = np.full((1, 2, k, V), -200.0, np.float32)
+    logits[0, 0, 0, 3] = 1.0
+    logits[0, 0, 0, 4] = 0.5
+    logits[0, 1, 0, 6] = 0.0
+    t, tr = _run_tree(cfg, logits)
+    assert t.logv[0, 0] == t.logv[0, 1]
+    assert t.kept[0].tolist() == [1, 0]
+    assert tr["tokens"][0, :2].tolist() == [0, 3]
+
+
+# ----------------------------------------------------- stage 4: emission ---
+
+def test_mask_positions_closed_form():
+    B, V, k, D, N = 10, 32, 3, 4, 12
+    cfg = oracle.TreeCfg(batch=B, vocab=V, top_k=k, depth=D, node_budget=N)
+    logits = synth.normal4((B, D, k, V), synth.F32, 2.0, seed=9, stream=synth.STREAM_DRAFT)
+    L = np.arange(B, dtype=np.int32) * 7 + 3
+    t, tr = _run_tree(cfg, logits, prefix_len=L, root_token=np.arange(B, dtype=np.int32) + 100)
+    for b in range(B):
+        n = tr["n_tree"][b]
+        assert n == 1 + t.n_kept[b]
+        assert tr["tokens"][b, 0] == 100 + b
+        for i in range(cfg.T):
+            bits = {j for j in range(cfg.T) if tr["mask"][b, i, j // 32] >> (j % 32) & 1}
+            if i >= n:
+                assert not bits and tr["tokens"][b, i] == -1 and tr["parent"][b, i] == -1
+                continue
+            anc, j = {i}, i
+            while tr["parent"][b, j] >= 0:
+                assert tr["parent"][b, j] < j
+                j = tr["parent"][b, j]
+                anc.add(j)
+            assert bits == anc
+            assert tr["depth"][b, i] == len(anc) - 1
+            assert tr["pos"][b, i] == L[b] + tr["depth"][b, i]
+        ids = np.nonzero(t.kept[b])[0]
+        assert list(tr["tokens"][b, 1:n]) == list(t.token[b, ids])  # id (BFS) order
+
+
+# --------------------------------------------------- stage 5: attention ---
+
+def _tiny_attention_case(dtype, B=2, T=9, Hq=4, Hkv=2, d=16, seed=21):
+    V, k, D = 32, 2, 3
+    cfg = oracle.TreeCfg(batch=B, vocab=V, top_k=k, depth=D, node_budget=T - 1)
+    logits = synth.normal4((B, D, k, V), synth.F32, 2.0, seed=seed, stream=synth.STREAM_DRAFT)
+    L = np.array([5, 12][:B], np.int32)
+    _, tr = _run_tree(cfg, logits, prefix_len=L)
+    Lmax = int(L.max()) + T
+    q = synth.normal4((B, T, Hq, d), dtype, 1.0, seed=seed, stream=synth.STREAM_Q)
+    npdt = np.float32 if dtype == synth.F32 else np.uint16
+    kc = np.zeros((B, Lmax, Hkv, d), npdt)
+    vc = np.zeros((B, Lmax, Hkv, d), npdt)
+    for b in range(B):
+        synth.kv_region(kc, dtype, b * Lmax * Hkv * d, Hkv * d, Hkv, d, 0, int(L[b]) + T, 0, b, seed, synth.STREAM_K)
+        synth.kv_region(vc, dtype, b * Lmax * Hkv * d, Hkv * d, Hkv, d, 0, int(L[b]) + T, 0, b, seed, synth.STREAM_V)
+    return tr, L, q, kc, vc, Lmax
+
+
+def _widen(a, dtype):
+    return a.astype(np.float64) if dtype == synth.F32 else synth.bf16_to_f32(a).astype(np.float64)
+
+
+@pytest.mark.parametrize("dtype", [synth.F32, synth.BF16])
+def test_tree_attention_equals_per_path_causal(dtype):
+    B, T, Hq, Hkv, d = 2, 9, 4, 2, 16
+    tr, L, q, kc, vc, Lmax = _tiny_attention_case(dtype, B, T, Hq, Hkv, d)
+    out = oracle.attention(q, kc, vc, Lmax * Hkv * d, Hkv * d, L, tr["mask"], tr["n_tree"], Hkv)
+    qf, kf, vf = _widen(q, dtype), _widen(kc, dtype), _widen(vc, dtype)
+    for b in range(B):
+        for i in range(T):
+            if i >= tr["n_tree"][b]:
+                assert not out[b, i].any()
+                continue
+            path, j = [], i
+            while j >= 0:
+                path.append(j)
+                j = tr["parent"][b, j]
+            seq_pos = list(range(L[b])) + [L[b] + s for s in reversed(path)]  # prefix ++ root..i
+            for h in range(Hq):
+                g = h // (Hq // Hkv)
+                K = kf[b, seq_pos, g]
+                Vv = vf[b, seq_pos, g]
+                # causal attention of the last position of the sequence
+                s = K @ qf[b, i, h] / math.sqrt(d)
+                w = np.exp(s - s.max())
+                want = (w / w.sum()) @ Vv
+                np.testing.assert_allclose(out[b, i, h], want, rtol=1e-10, atol=1e-12)
+
+
+def test_chain_tree_attention_is_causal_attention():
+    # k = 1: the tree is a chain, the mask is lower-triangular; textbook causal attention.
+    B, V, D, d, Hq = 1, 16, 5, 8, 2
+    T = D + 1
+    cfg = oracle.TreeCfg(batch=B, vocab=V, top_k=1, depth=D, node_budget=D)
+    logits = synth.normal4((B, D, 1, V), synth.F32, 1.0, seed=2, stream=synth.STREAM_DRAFT)
+    L = np.array([4], np.int32)
+    _, tr = _run_tree(cfg, logits, prefix_len=L)
+    S = int(L[0]) + T
+    q = synth.normal4((B, T, Hq, d), synth.F32, 1.0, seed=2, stream=synth.STREAM_Q)
+    kc = synth.normal4((B, S, Hq, d), synth.F32, 1.0, seed=2, stream=synth.STREAM_K)
+    vc = synth.normal4((B, S, Hq, d), synth.F32, 1.0, seed=2, stream=synth.STREAM_V)
+    out = oracle.attention(q, kc, vc, S * Hq * d, Hq * d, L, tr["mask"], tr["n_tree"], Hq)
+    # full causal attention over S positions; queries are the last T positions
+    for h in range(Hq):
+        Qf = np.zeros((S, d))
+        Qf[L[0]:] = q[0, :, h]
+        scores = Qf @ kc[0, :, h].T.astype(np.float64) / math.sqrt(d)
+        scores = np.where(np.tril(np.ones((S, S), bool)), scores, -np.inf)
+        w = np.exp(scores - scores.max(axis=1, keepdims=True))
+        w /= w.sum(axis=1, keepdims=True)
+        want = w @ vc[0, :, h].astype(np.float64)
+        np.testing.assert_allclose(out[0, :, h], want[L[0]:], rtol=1e-10, atol=1e-12)
+
+
+# ------------------------------------------------------ stage 6: verify ---
+
+def _tree_and_target(B, V, k, D, N, seed, plant_frac=0.8):
+    cfg = oracle.TreeCfg(batch=B, vocab=V, top_k=k, depth=D, node_budget=N)
+    logits = synth.normal4((B, D, k, V), synth.F32, 2.0, seed=seed, stream=synth.STREAM_DRAFT)
+    _, tr = _run_tree(cfg, logits)
+    T = cfg.T
+    target = synth.normal4((B, T, V), synth.F32, 1.0, seed=seed, stream=synth.STREAM_TARGET)
+    # make the target agree with some child of each slot so paths get accepted
+    rng = np.random.default_rng(seed)
+    for b in range(B):
+        for t in range(tr["n_tree"][b]):
+            kids = [c for c in range(T) if tr["parent"][b, c] == t]
+            if kids and rng.random() < plant_frac:
+                target[b, t, tr["tokens"][b, rng.choice(kids)]] = 50.0
+    return cfg, tr, target
+
+
+def test_greedy_verify_bruteforce():
+    B, V, k, D, N = 24, 16, 3, 4, 10
+    cfg, tr, target = _tree_and_target(B, V, k, D, N, seed=31)
+    a, slots, toks, am = oracle.verify_greedy(target, tr["tokens"], tr["parent"], tr["n_tree"], D)
+    assert (a > 0).any() and (a >= 2).any()
+    for b in range(B):
+        n = tr["n_tree"][b]
+        g = [int(np.argmax(target[b, t])) for t in range(n)]
+        path, cur = [0], 0
+        while True:
+            nxt = [c for c in range(n) if tr["parent"][b, c] == cur and tr["tokens"][b, c] == g[cur]]
+            assert len(nxt) <= 1
+            if not nxt:
+                break
+            cur = nxt[0]
+            path.append(cur)
+        assert a[b] == len(path) - 1
+        assert list(slots[b, :a[b] + 1]) == path
+        assert list(toks[b, :a[b] + 1]) == [tr["tokens"][b, s] for s in path[1:]] + [g[cur]]
+        assert (slots[b, a[b] + 1:] == -1).all() and (toks[b, a[b] + 1:] == -1).all()
+
+
+def test_greedy_chain_equals_chain_speculative_decoding():
+    # k = 1 chain: accept draft token j while it equals the target's greedy choice at j-1.
+    B, V, D = 40, 8, 5
+    cfg, tr, target = _tree_and_target(B, V, 1, D, D, seed=7, plant_frac=0.7)
+    a, _, toks, _ = oracle.verify_greedy(target, tr["tokens"], tr["parent"], tr["n_tree"], D)
+    for b in range(B):
+        draft = tr["tokens"][b, 1:tr["n_tree"][b]]
+        tgt = target[b].argmax(axis=1)
+        n_acc = 0
+        while n_acc < len(draft) and draft[n_acc] == tgt[n_acc]:
+            n_acc += 1
+        assert a[b] == n_acc
+        assert list(toks[b, :n_acc + 1]) == list(draft[:n_acc]) + [tgt[n_acc]]
+
+
+def _softmax(x):
+    x = x.astype(np.float64)
+    e = np.exp(x - x.max())
+    return e / e.sum()
+
+
+def test_lossless_single_child_accept_probability_is_p():
+    # The proposal of a deterministic top-k child is a point mass, so min(1, p/q) = p(x).
+    V, T = 8, 2
+    row = np.array([1.0, 0.2, -0.5, 2.0, 0.0, -1.0, 0.7, 0.1], np.float32)
+    target = np.zeros((1, T, V), np.float32)
+    target[0, 0] = row
+    tokens = np.array([[0, 6]], np.int32)
+    parent = np.array([[-1, 0]], np.int32)
+    p = _softmax(row)[6]
+    n = 4096
+    U = np.zeros((n, T + 2), np.uint32)
+    U[:, 1] = (np.arange(n, dtype=np.uint64) * (2 ** 32 // n)).astype(np.uint32)
+    a, _, _ = oracle.verify_lossless(np.repeat(target, n, 0), np.repeat(tokens, n, 0), np.repeat(parent, n, 0),
+                                     np.full(n, 2, np.int32), U, depth=1)
+    assert abs(a.mean() - p) <= 1.0 / n + 1e-6
+
+
+def test_lossless_output_distribution_equals_target():
+    # Root with 3 kept children (two of them with kept children). The first two
+    # emitted tokens must follow the target's own autoregressive distribution.
+    V, T = 6, 6
+    tokens = np.array([[9, 2, 0, 5, 1, 4]], np.int32)
+    parent = np.array([[-1, 0, 0, 0, 1, 2]], np.int32)
+    rows = np.array([[0.3, -0.2, 1.1, 0.0, -1.0, 0.6],
+                     [1.5, 0.1, -0.3, 0.2, 0.9, -2.0],
+                     [0.0, 0.4, 0.1, -0.5, 1.2, 0.3],
+                     [0.2, 0.2, 0.2, 0.2, 0.2, 0.2],
+                     [-1.0, 0.0, 1.0, 0.5, 0.5, 0.1],
+                     [0.3, 0.1, 0.0, 2.0, -0.4, 0.2]], np.float32)
+    n = 200000
+    target = np.repeat(rows[None], n, 0)
+    U = synth.words(n, T + 2, c2=0, seed=77)
+    a, slots, toks = oracle.verify_lossless(target, np.repeat(tokens, n, 0), np.repeat(parent, n, 0),
+                                            np.full(n, T, np.int32), U, depth=2)
+    p0 = _softmax(rows[0])
+    emp0 = np.bincount(toks[:, 0], minlength=V) / n
+    sigma = np.sqrt(p0 * (1 - p0) / n)
+    assert (np.abs(emp0 - p0) < 5 * sigma + 1e-9).all(), (emp0, p0)
+    # joint of the first two tokens where the first lands on a tree node
+    slot_of_tok = {int(tokens[0, c]): c for c in range(1, T) if parent[0, c] == 0}
+    for x, c in slot_of_tok.items():
+        pc = _softmax(rows[c])
+        sel = toks[:, 0] == x
+        emp = np.bincount(toks[sel, 1], minlength=V) / sel.sum()
+        sig = np.sqrt(pc * (1 - pc) / sel.sum())
+        assert (np.abs(emp - pc) < 5 * sig + 1e-9).all(), (x, emp, pc)
+    assert (a <= 2).all() and (a >= 0).all()
+
+
+def test_lossless_row_mass_is_exact_integer_sum():
+    V, T = 300, 3
+    target = synth.normal4((1, T, V), synth.BF16, 2.5, seed=4, stream=synth.STREAM_TARGET)
+    U = synth.words(1, T + 2, c2=0, seed=4)
+    tokens = np.array([[1, 2, 3]], np.int32)
+    parent = np.array([[-1, 0, 0]], np.int32)
+    _, _, _, rmax, rmass = oracle.verify_lossless(target, tokens, parent, np.array([T], np.int32), U, depth=1,
+                                                  row_stats_out=True)
+    for t in range(T):
+        x = synth.bf16_to_f32(target[0, t])
+        assert rmax[0, t] == x.max()
+        want = sum(int(np.float32(oracle.dexp(float(np.float32(v - x.max())))) * np.float32(2.0 ** 40)) for v in x)
+        assert int(rmass[0, t]) == want
+        # and the integer masses follow softmax to fp32 precision
+        assert abs(want / 2.0 ** 40 - np.exp(x.astype(np.float64) - x.max()).sum()) < 1e-5 * want / 2.0 ** 40
+
+
+# ------------------------------------------------------ stage 6b: compact ---
+
+def test_kv_compact_moves_path_kv():
+    B, layers, Hkv, d, Lmax, D = 3, 2, 2, 8, 40, 4
+    L = np.array([5, 17, 0], np.int32)
+    a = np.array([3, 0, 4], np.int32)
+    slots = np.array([[0, 2, 5, 7, -1], [0, -1, -1, -1, -1], [0, 1, 3, 4, 8]], np.int32)
+    pos_stride = Hkv * d
+    kv_stride = Lmax * pos_stride
+    layer_stride = 2 * kv_stride
+    seq_stride = layers * layer_stride
+    cache = np.zeros(B * seq_stride, np.uint16)
+    for b in range(B):
+        for l in range(layers):
+            for kv in range(2):
+                synth.kv_region(cache, synth.BF16, b * seq_stride + l * layer_stride + kv * kv_stride, pos_stride,
+                                Hkv, d, 0, Lmax, l, b, 13, synth.STREAM_K + kv)
+    before = cache.copy()
+    new_len = oracle.kv_compact(cache, B, layers, Hkv, d, seq_stride, layer_stride, kv_stride, pos_stride, L, a,
+                                slots)
+    assert list(new_len) == list(L + a + 1)
+    c4 = cache.reshape(B, layers, 2, Lmax, Hkv, d)
+    b4 = before.reshape(B, layers, 2, Lmax, Hkv, d)
+    for b in range(B):
+        for l in range(layers):
+            for kv in range(2):
+                # destination L+j holds what the generator wrote for position L+s_j
+                for j in range(1, a[b] + 1):
+                    regen = np.zeros(Lmax * pos_stride, np.uint16)
+                    synth.kv_region(regen, synth.BF16, 0, pos_stride, Hkv, d, L[b] + slots[b, j],
+                                    L[b] + slots[b, j] + 1, l, b, 13, synth.STREAM_K + kv)
+                    want = regen.reshape(Lmax, Hkv, d)[L[b] + slots[b, j]]
+                    assert (c4[b, l, kv, L[b] + j] == want).all()
+                # everything else is untouched
+                others = [p for p in range(Lmax) if not (L[b] + 1 <= p <= L[b] + a[b])]
+                assert (c4[b, l, kv, others] == b4[b, l, kv, others]).all()
