@@ -1,0 +1,250 @@
+/*
+ * libeagle: the per-cycle dynamic draft-tree pipeline of EAGLE-2 speculative
+ * decoding as hand-written CUDA kernels for sm_103a, behind a C ABI.
+ *
+ * Sources (page title and section):
+ *   [summary]  "EAGLE-2: Faster Inference of Language Models with Dynamic
+ *              Draft Trees" (paperlayer summary of arXiv 2406.16858v2),
+ *              2.1 Speculative Sampling, 4.1 Expansion Phase, 4.2 Reranking
+ *              Phase, App. A Implementation Details.
+ *   [tutorial] "EAGLE-2: Dynamic Draft Trees" (stable-lab), "Value of a Node
+ *              = Its Path Product", "Common misconception".
+ *   [notes]    "EAGLE" (garden.houmin.site), EAGLE 方法 (TopK drafting, tree
+ *              attention) and EAGLE 2 方法 (Expand with a threshold, ReRank
+ *              with the shallower-node tie rule).
+ *
+ * One cycle, in call order:
+ *   eagle_tree_init                       reset the tree state in `ws`
+ *   eagle_expand(step = 0 .. depth-1)     stages 1+2, one call per draft step
+ *   eagle_rerank                          stage 3
+ *   eagle_build_tree                      stage 4
+ *   eagle_tree_attention                  stage 5 (one layer per call)
+ *   eagle_verify                          stage 6
+ *   eagle_kv_compact                      stage 6b
+ *
+ * Conventions for every call:
+ *   - Pointers named in the signatures are device pointers owned by the
+ *     caller unless stated; the library allocates nothing and keeps no state
+ *     outside the caller's workspace, apart from cached device attributes.
+ *   - Every call enqueues work on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and returns without synchronising; a whole cycle can be
+ *     captured in a CUDA graph once each entry point has been called once
+ *     outside capture (first calls set kernel attributes).
+ *   - Argument checks run on the host before any launch; a failed check
+ *     returns a negative eagle_status and launches nothing.
+ *   - Faults found on the device (non-finite rows, out-of-range tokens or
+ *     lengths, a bounded wait that gave up) set a status word in `ws`: the
+ *     first error of the cycle wins, later kernels keep running, and outputs
+ *     are undefined until eagle_status_fetch reports 0.
+ *   - Rows of logits are contiguous; row starts must be 16-byte aligned
+ *     (vocab * element size a multiple of 16, base pointer 16-byte aligned).
+ *   - Calls on distinct workspaces may run concurrently.
+ */
+#ifndef EAGLE_H_
+#define EAGLE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    EAGLE_OK = 0,
+    EAGLE_ERR_INVALID_ARG = -1, /* a host-side argument check failed */
+    EAGLE_ERR_UNSUPPORTED = -2, /* valid but outside what the kernels support */
+    EAGLE_ERR_LAUNCH = -3,      /* a CUDA launch or runtime call failed */
+    EAGLE_ERR_WORKSPACE = -4,   /* workspace missing, misaligned or too small */
+    EAGLE_ERR_DEVICE = -5,      /* eagle_status_fetch: the device raised an error */
+    EAGLE_ERR_TIMEOUT = -6      /* eagle_status_fetch: a bounded device wait gave up */
+} eagle_status;
+
+typedef enum { EAGLE_F32 = 0, EAGLE_BF16 = 1 } eagle_dtype;
+
+typedef enum { EAGLE_VERIFY_GREEDY = 0, EAGLE_VERIFY_LOSSLESS = 1 } eagle_verify_mode;
+
+/* Draft-tree problem [summary 4.1, 4.2, App. A; notes EAGLE 2 方法]. */
+typedef struct {
+    int batch;       /* B, independent sequences */
+    int vocab;       /* V, entries per logit row */
+    int top_k;       /* k: children per expanded node and nodes expanded per step, 1..16 */
+    int depth;       /* D: expansion steps = maximum draft depth, 1..16 */
+    int node_budget; /* N: draft nodes kept by the rerank; tree slots T = N + 1 (root + N), T <= 256 */
+    float threshold; /* path-value threshold below which a node is not expanded; <= 0 disables */
+    int logit_dtype; /* eagle_dtype of the draft and target logits */
+} eagle_tree_cfg;
+
+/*
+ * KV cache geometry (elements, not bytes). Element (b, layer, kv, pos, h, e)
+ * with kv = 0 for K and 1 for V lives at
+ *   b*seq_stride + layer*layer_stride + kv*kv_stride + pos*pos_stride + h*head_dim + e.
+ * Tree slot j of sequence b is stored at position prefix_len[b] + j.
+ */
+typedef struct {
+    int batch, n_q_heads, n_kv_heads, head_dim;
+    int layers;  /* layers moved by eagle_kv_compact */
+    int max_len; /* positions available per (sequence, layer, K|V) region */
+    int dtype;   /* eagle_dtype of Q, K, V and the attention output */
+    int64_t seq_stride, layer_stride, kv_stride, pos_stride;
+} eagle_kv_cfg;
+
+/* Candidate capacity C = k + (D-1) k^2 must be <= 1024. */
+
+/* Bytes of the tree workspace for `cfg` (0 if cfg is invalid). The workspace
+ * is device memory owned by the caller, 256-byte aligned, and must not be
+ * shared by two cycles in flight. Its contents are opaque. */
+size_t eagle_workspace_bytes(const eagle_tree_cfg* cfg);
+
+/* Reset the per-cycle tree state: the root (depth 0) is the only frontier
+ * node of step 0; no candidates. Clears nothing else. */
+int eagle_tree_init(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Stages 1+2, draft step `step` (0-based) [notes EAGLE 方法: TopK drafting;
+ * summary 4.1; tutorial "Value of a Node"; notes EAGLE 2 方法, Expand].
+ *   draft_logits    [B, k, V] row f = the draft distribution of frontier slot f
+ *                   of this step (step 0: only row 0, the root, is read; rows
+ *                   f >= frontier count are never read).
+ *   row_lse_in      [B, k] fp32 in, or NULL: the log-sum-exp of each row when
+ *                   an upstream kernel already has it (e.g. an LM-head
+ *                   epilogue); NULL = computed here (fp32, within 1e-5 of the
+ *                   exact value at V = 128K).
+ *   row_lse         [B, D, k] fp32 out: log-sum-exp used for each row read,
+ *                   at [b, step, f]; NaN for rows not read.
+ *   frontier_tokens [B, k] int32 out: tokens of the nodes to expand at step+1,
+ *                   best value first, -1 padding (input of the next draft forward).
+ *   frontier_count  [B] int32 out.
+ * Per row: lse = max + log(sum exp(x - max)); the k largest logits (equal
+ * logits: lower token id) become children with value
+ * logv = logv(parent) + (x - lse) in fp32, logv(root) = 0. The next frontier
+ * is the k highest-value children of this step among those with
+ * logv >= log(threshold) (equal values: lower node id).
+ */
+int eagle_expand(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int step, const void* draft_logits,
+                 const float* row_lse_in, float* row_lse, int32_t* frontier_tokens, int32_t* frontier_count,
+                 void* stream);
+
+/*
+ * Stage 3 [summary 4.2; tutorial "Value of a Node"; notes EAGLE 2 方法,
+ * ReRank]: keep the min(N, #candidates) candidates with the largest value;
+ * equal values keep the shallower node, then the lower node id. The kept set
+ * is connected (every kept node's parent is kept or is the root). State stays
+ * in `ws`.
+ */
+int eagle_rerank(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Stage 4 [summary 4.2: flattened sequence with a branch-separating mask].
+ *   prefix_len [B] int32 in: verified tokens already in the KV cache (L_b).
+ *   root_token [B] int32 in: last verified token (slot 0, depth 0).
+ *   tokens, parent, depth, pos_ids [B, T] int32 out: slot 0 = root, slots
+ *     1..n_tree-1 = kept nodes in node-id order (depth-major, so parents come
+ *     first); parent = slot of the parent (-1 for the root); pos = L_b + depth;
+ *     unused slots -1.
+ *   mask [B, T, W] uint32 out, W = ceil(T/32): bit j of row i (word j/32,
+ *     LSB first) is set iff slot j is an ancestor of slot i or i itself;
+ *     unused rows are 0. The prefix is always visible and is not in the mask.
+ *   n_tree [B] int32 out: 1 + kept nodes.
+ */
+int eagle_build_tree(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, const int32_t* prefix_len,
+                     const int32_t* root_token, int32_t* tokens, int32_t* parent, int32_t* depth,
+                     int32_t* pos_ids, uint32_t* mask, int32_t* n_tree, void* stream);
+
+/* Scratch bytes for eagle_tree_attention with this geometry and T slots. */
+size_t eagle_attention_workspace_bytes(const eagle_kv_cfg* kv, int T);
+
+/*
+ * Stage 5 [notes EAGLE 方法: tree attention verifies all branches at once;
+ * summary 4.2]. For every sequence b, slot i < n_tree[b] and query head h:
+ *   out[b,i,h,:] = sum_j softmax_j(q.k_j / sqrt(d)) v_j
+ * over keys j in the prefix [0, L_b) and the tree slots set in mask row i
+ * (cache position L_b + slot), KV head h / (Hq/Hkv). fp32 softmax and
+ * accumulation; output in kv->dtype (bf16 rounds to nearest even). Rows
+ * i >= n_tree[b] are written as zeros.
+ *   q   [B, T, Hq, d] in, out [B, T, Hq, d] out, contiguous.
+ *   kv_cache: base of the cache described by kv; `layer` selects the layer.
+ *   ws/ws_bytes: attention scratch (eagle_attention_workspace_bytes), may
+ *   alias nothing else in flight. Requires prefix_len[b] + T <= max_len.
+ *   bf16 needs head_dim 128 (tensor-core path); fp32 supports head_dim <= 128.
+ */
+int eagle_tree_attention(const eagle_kv_cfg* kv, int T, const void* q, const void* kv_cache, int layer,
+                         const int32_t* prefix_len, const uint32_t* mask, const int32_t* n_tree, void* out,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Stage 6 [summary 2.1: target verification, tokens accepted sequentially by
+ * the probability ratio; abstract: the output distribution is unchanged].
+ *   target_logits [B, T, V] in: the target's distribution at each slot.
+ *   tokens, parent [B, T], n_tree [B] in: the tree from eagle_build_tree.
+ *   uniforms [B, T+2] uint32 in (lossless only, else may be NULL): word c
+ *     tests the child at slot c (U24 = word >> 8); words T and T+1 form
+ *     U64 = w[T+1] * 2^32 + w[T] for the final draw. Counter-based in the
+ *     bundled generator; any source of independent uniform words works.
+ *   accept_len [B] out: accepted draft tokens a_b (0..D).
+ *   accepted_slots [B, D+1] out: slots of the accepted path, root first, -1 pad.
+ *   out_tokens [B, D+1] out: the a_b accepted tokens then the bonus token, -1 pad.
+ * GREEDY: the target's choice at slot t is argmax of row t (equal logits:
+ *   lower id); walk from the root into the child carrying that choice.
+ * LOSSLESS (temperature > 0): integer probabilities
+ *   P_t[x] = floor(dexp((x - max_t) / temperature) * 2^40), dexp a fixed-order
+ *   exp (Cody-Waite reduction, degree-7 Taylor, fp32 mul/add); at node u the
+ *   kept children are tested in slot order and child x is accepted iff
+ *   U24 * S < 2^24 * P_u[x] (S = remaining mass); a rejection removes x. With
+ *   no child accepted the bonus is the smallest token y (not removed) whose
+ *   running mass exceeds floor(U64 * S / 2^64).
+ */
+int eagle_verify(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int mode, float temperature,
+                 const void* target_logits, const int32_t* tokens, const int32_t* parent, const int32_t* n_tree,
+                 const uint32_t* uniforms, int32_t* accept_len, int32_t* accepted_slots, int32_t* out_tokens,
+                 void* stream);
+
+/*
+ * Stage 6b: move the accepted path's KV into place. For every layer in
+ * [0, kv->layers), for K and V and j = 1..a_b:
+ *   position L_b + j  <-  what position L_b + accepted_slots[b, j] held,
+ * all sources read before any destination is written; positions outside
+ * [L_b + 1, L_b + a_b] are untouched. new_len[b] = L_b + a_b + 1.
+ *   accepted_slots [B, slots_stride] int32 (slots_stride >= max a_b + 1).
+ *   ws: any eagle workspace whose status word receives device faults
+ *   (a_b > 16, a slot s_j < j, or a position beyond max_len: that sequence
+ *   is left untouched and new_len is not written); may be NULL.
+ * Needs head_dim * n_kv_heads * element size and pos_stride * element size
+ * to be multiples of 16 bytes.
+ */
+int eagle_kv_compact(const eagle_kv_cfg* kv, void* kv_cache, const int32_t* prefix_len, const int32_t* accept_len,
+                     const int32_t* accepted_slots, int slots_stride, int32_t* new_len, void* ws, void* stream);
+
+/* Synchronise `stream`, read the device status word of a workspace (the tree
+ * workspace or the attention scratch: the word is the first 4 bytes of
+ * either) into *device_status (0 = no fault, 1 non-finite row, 2 wait gave
+ * up, 3 index out of range, 4 table overflow), clear it, and return EAGLE_OK,
+ * EAGLE_ERR_DEVICE or EAGLE_ERR_TIMEOUT accordingly. */
+int eagle_status_fetch(void* ws, int* device_status, void* stream);
+
+/* ---------------------------------------------- inspection (tests, tools) --- */
+
+/* Copy the candidate table and rerank result out of `ws` (device to device,
+ * on `stream`): cand_* [B, C], kept [B, C] uint8, n_kept [B]. Any pointer may
+ * be NULL. */
+int eagle_tree_export(const eagle_tree_cfg* cfg, const void* ws, size_t ws_bytes, int32_t* cand_token,
+                      int32_t* cand_parent, int32_t* cand_depth, float* cand_logv, uint8_t* cand_valid,
+                      uint8_t* kept, int32_t* n_kept, void* stream);
+
+/* Copy the per-row target statistics of the last eagle_verify: row maximum
+ * [B, T] fp32, argmax [B, T] int32, integer mass sum_x P_t[x] [B, T] uint64
+ * (lossless only). Rows t >= n_tree are unspecified. */
+int eagle_verify_export(const eagle_tree_cfg* cfg, const void* ws, size_t ws_bytes, float* row_max,
+                        int32_t* row_argmax, uint64_t* row_mass, void* stream);
+
+/* Kernels launched by this library since it was loaded (host-side count). */
+uint64_t eagle_kernel_launches(void);
+
+/* Human-readable message for an eagle_status value. */
+const char* eagle_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EAGLE_H_ */

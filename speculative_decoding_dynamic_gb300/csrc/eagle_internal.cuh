@@ -1,0 +1,148 @@
+// Internal device helpers of libeagle (sm_103a). Not part of the public ABI.
+#pragma once
+
+#include <cooperative_groups.h>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace eagle {
+
+namespace cg = cooperative_groups;
+
+// ------------------------------------------------------------- status word ---
+// Device-detected faults: the first error of a cycle wins (atomicCAS on 0).
+enum DeviceError : int {
+    kDevOk = 0,
+    kDevNonFinite = 1,   // a logit row has a non-finite log-sum-exp / maximum
+    kDevTimeout = 2,     // a bounded wait on an mbarrier gave up
+    kDevBadIndex = 3,    // a token / slot / length out of range
+    kDevOverflow = 4,    // a candidate or tree table would overflow
+};
+
+__device__ __forceinline__ void raise_status(int* status, int code) {
+    if (status != nullptr) atomicCAS(status, 0, code);
+}
+
+// --------------------------------------------------------------- sort keys ---
+// Float -> unsigned with the same order (-0 and +0 are one value).
+__device__ __forceinline__ uint32_t f2o(float f) {
+    uint32_t b = __float_as_uint(f);
+    if ((b & 0x7fffffffu) == 0u) b = 0u;
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float o2f(uint32_t o) {
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+// 64-bit key: larger value first, then lower id. Unique per id.
+__device__ __forceinline__ uint64_t make_key(float v, uint32_t id) {
+    return (static_cast<uint64_t>(f2o(v)) << 32) | static_cast<uint32_t>(0xffffffffu - id);
+}
+__device__ __forceinline__ uint32_t key_id(uint64_t k) { return 0xffffffffu - static_cast<uint32_t>(k); }
+__device__ __forceinline__ float key_val(uint64_t k) { return o2f(static_cast<uint32_t>(k >> 32)); }
+
+__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m) {
+    uint32_t lo = static_cast<uint32_t>(v), hi = static_cast<uint32_t>(v >> 32);
+    lo = __shfl_xor_sync(0xffffffffu, lo, m);
+    hi = __shfl_xor_sync(0xffffffffu, hi, m);
+    return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) {
+        uint64_t o = shfl_xor_u64(v, m);
+        v = o > v ? o : v;
+    }
+    return v;
+}
+__device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) v += shfl_xor_u64(v, m);
+    return v;
+}
+
+// Top-k of n unique keys held in shared memory, by one warp: k rounds of warp
+// argmax, each round taking the largest key below the previous one. Writes
+// out[0..k) (0 = no key). Cost O(k * n / 32) per lane; used for n <= a few
+// hundred.
+__device__ __forceinline__ void warp_topk_smem(const uint64_t* keys, int n, int k, uint64_t* out) {
+    const int lane = threadIdx.x & 31;
+    uint64_t prev = ~0ull;
+    for (int r = 0; r < k; ++r) {
+        uint64_t best = 0;
+        for (int i = lane; i < n; i += 32) {
+            uint64_t v = keys[i];
+            if (v < prev && v > best) best = v;
+        }
+        best = warp_max_u64(best);
+        if (lane == 0) out[r] = best;
+        prev = best;
+        if (best == 0) {
+            for (int q = r + 1 + lane; q < k; q += 32) out[q] = 0;
+            break;
+        }
+    }
+    __syncwarp();
+}
+
+// -------------------------------------------------------------- fast exp2 ---
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// --------------------------------------------------- mbarrier + bulk copies ---
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait on an mbarrier phase. Returns false after ~max_iter polls
+// (each poll may suspend the thread for a hardware-chosen time).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t max_iter = (1u << 21)) {
+    for (uint32_t i = 0; i < max_iter; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+// Bulk (non-tensor) copy global -> this CTA's shared memory; completion is
+// signalled on `bar` as transaction bytes. Both addresses 16-byte aligned,
+// bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Global loads that bypass L1 (data written by other CTAs of the same launch).
+__device__ __forceinline__ int ld_cg_i32(const int* p) { return __ldcg(p); }
+__device__ __forceinline__ float ld_cg_f32(const float* p) { return __ldcg(p); }
+
+// ------------------------------------------------------------- host side ---
+// Dynamic shared memory opt-in and launch helpers live in the launcher files.
+
+}  // namespace eagle

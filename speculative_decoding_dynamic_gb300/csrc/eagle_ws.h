@@ -1,0 +1,120 @@
+// Workspace layout and launcher declarations shared by the host entry points
+// and the kernel files of libeagle. Internal; not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace eagle {
+
+constexpr int kMaxTopK = 16;
+constexpr int kMaxDepth = 16;
+constexpr int kMaxSlots = 256;       // T = N + 1
+constexpr int kMaxCandidates = 1024;  // C = k + (D-1) k^2
+constexpr int kMaxChunks = 8;        // CTAs per logit row (one thread-block cluster)
+
+// Resolved problem description passed by value to kernels.
+struct TreeDims {
+    int B, V, k, D, N, T, W, C;
+    float log_thr;  // -inf disables the threshold
+    int dtype;      // 0 fp32, 1 bf16
+};
+
+// Pointers into the caller's workspace. Layout computed by ws_layout(). The
+// status word is always the first word of a workspace (tree or attention).
+struct TreeWs {
+    int* status;            // [1] first-error-wins device status
+    int* expand_ticket;     // [B] arrivals of row clusters in the current expand step
+    int* verify_ticket;     // [B] arrivals of row clusters in verify
+    int32_t* cand_token;    // [B, C]
+    int32_t* cand_parent;   // [B, C] node id of the parent, -1 = root
+    int32_t* cand_depth;    // [B, C]
+    float* cand_logv;       // [B, C] log path value
+    uint8_t* cand_valid;    // [B, C]
+    int32_t* fnode;         // [D+1, B, k] frontier node ids per step (-1 = root)
+    int32_t* fcount;        // [D+1, B]
+    uint8_t* kept;          // [B, C]
+    int32_t* n_kept;        // [B]
+    int32_t* slot_of;       // [B, C] tree slot of a kept node, -1 otherwise
+    float* row_max;         // [B, T] verify row maximum
+    int32_t* row_arg;       // [B, T] verify row argmax
+    uint64_t* row_mass;     // [B, T] verify integer mass
+    uint64_t* chunk_mass;   // [B, T, kMaxChunks] verify integer mass per row chunk
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Computes the layout; returns total bytes. If base != nullptr fills ws.
+inline size_t ws_layout(const TreeDims& d, void* base, TreeWs* ws) {
+    size_t off = 0;
+    char* p = static_cast<char*>(base);
+    auto take = [&](size_t bytes) -> void* {
+        off = align_up(off, 256);
+        void* r = p ? static_cast<void*>(p + off) : nullptr;
+        off += bytes;
+        return r;
+    };
+    const size_t B = d.B, C = d.C, k = d.k, D = d.D, T = d.T;
+    TreeWs w{};
+    w.status = static_cast<int*>(take(sizeof(int)));
+    w.expand_ticket = static_cast<int*>(take(B * sizeof(int)));
+    w.verify_ticket = static_cast<int*>(take(B * sizeof(int)));
+    w.cand_token = static_cast<int32_t*>(take(B * C * 4));
+    w.cand_parent = static_cast<int32_t*>(take(B * C * 4));
+    w.cand_depth = static_cast<int32_t*>(take(B * C * 4));
+    w.cand_logv = static_cast<float*>(take(B * C * 4));
+    w.cand_valid = static_cast<uint8_t*>(take(B * C));
+    w.fnode = static_cast<int32_t*>(take((D + 1) * B * k * 4));
+    w.fcount = static_cast<int32_t*>(take((D + 1) * B * 4));
+    w.kept = static_cast<uint8_t*>(take(B * C));
+    w.n_kept = static_cast<int32_t*>(take(B * 4));
+    w.slot_of = static_cast<int32_t*>(take(B * C * 4));
+    w.row_max = static_cast<float*>(take(B * T * 4));
+    w.row_arg = static_cast<int32_t*>(take(B * T * 4));
+    w.row_mass = static_cast<uint64_t*>(take(B * T * 8));
+    w.chunk_mass = static_cast<uint64_t*>(take(B * T * kMaxChunks * 8));
+    if (ws) *ws = w;
+    return align_up(off, 256);
+}
+
+// How a logit row is split over a thread-block cluster.
+struct RowSplit {
+    int cpr;          // CTAs per row (cluster size), power of two <= kMaxChunks
+    int chunk;        // elements per CTA (multiple of 16 bytes), last CTA may get fewer
+    int smem_bytes;   // dynamic shared memory per CTA
+};
+RowSplit choose_row_split(int V, int esize);
+
+// ----------------------------------------------------------- launchers ---
+// Each returns cudaSuccess or the launch error. All enqueue on `stream`.
+cudaError_t launch_tree_init(const TreeDims& d, const TreeWs& ws, cudaStream_t stream);
+cudaError_t launch_expand(const TreeDims& d, const TreeWs& ws, int step, const void* logits, const float* lse_in,
+                          float* row_lse, int32_t* ftok, int32_t* fcount_out, cudaStream_t stream);
+cudaError_t launch_rerank(const TreeDims& d, const TreeWs& ws, cudaStream_t stream);
+cudaError_t launch_build_tree(const TreeDims& d, const TreeWs& ws, const int32_t* prefix_len,
+                              const int32_t* root_token, int32_t* tokens, int32_t* parent, int32_t* depth,
+                              int32_t* pos, uint32_t* mask, int32_t* n_tree, cudaStream_t stream);
+cudaError_t launch_verify(const TreeDims& d, const TreeWs& ws, int mode, float inv_temp, const void* target,
+                          const int32_t* tokens, const int32_t* parent, const int32_t* n_tree,
+                          const uint32_t* uniforms, int32_t* accept_len, int32_t* slots, int32_t* out_tokens,
+                          cudaStream_t stream);
+
+struct KvDims {
+    int B, Hq, Hkv, d, layers, max_len, dtype;
+    int64_t seq_stride, layer_stride, kv_stride, pos_stride;
+};
+cudaError_t launch_kv_compact(const KvDims& kv, void* cache, const int32_t* prefix_len, const int32_t* accept_len,
+                              const int32_t* slots, int slots_stride, int32_t* new_len, int* status,
+                              cudaStream_t stream);
+
+size_t attention_ws_bytes(const KvDims& kv, int T);
+cudaError_t launch_attention(const KvDims& kv, int T, const void* q, const void* cache, int layer,
+                             const int32_t* prefix_len, const uint32_t* mask, const int32_t* n_tree, void* out,
+                             void* ws, size_t ws_bytes, int* status, cudaStream_t stream);
+
+// Host-side launch counter (incremented by every launcher).
+void count_launch(int n = 1);
+
+}  // namespace eagle

@@ -1,0 +1,722 @@
+// Vocabulary-row kernels of the draft-tree cycle (sm_103a):
+//   expand_kernel  stages 1+2: per frontier row softmax statistics + top-k,
+//                  child values, then (last row of a sequence) the next frontier.
+//   verify_kernel  stage 6: per target row max/argmax (+ integer mass), then
+//                  (last row of a sequence) the acceptance walk.
+//
+// Layout of the work: one logit row is split over a thread-block cluster of
+// `cpr` CTAs. Each CTA stages its contiguous chunk of the row in shared memory
+// with one bulk asynchronous copy (TMA engine, completion on an mbarrier), so
+// HBM is read exactly once and the reductions re-read shared memory. Partial
+// results are merged through distributed shared memory inside the cluster.
+// The per-sequence tail (frontier selection / acceptance walk) runs in the
+// cluster leader that arrives last on a per-sequence ticket: an atomic add
+// after a device-scope fence, no spin-wait anywhere.
+//
+// Sources (page title and section): "EAGLE" notes (garden.houmin.site),
+// EAGLE 方法 (TopK drafting) and EAGLE 2 方法 (Expand, threshold);
+// "EAGLE-2: Faster Inference ..." summary, 2.1 Speculative Sampling and 4.1
+// Expansion Phase; "EAGLE-2: Dynamic Draft Trees" tutorial, "Value of a Node =
+// Its Path Product".
+
+#include <cuda_bf16.h>
+
+#include <cmath>
+#include <cstdio>
+
+#include "eagle_internal.cuh"
+#include "eagle_ws.h"
+
+namespace eagle {
+
+constexpr int kRowThreads = 256;
+constexpr int kRowWarps = kRowThreads / 32;
+constexpr int kCandCap = 128;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ------------------------------------------------------------ row staging ---
+
+struct RowChunk {
+    int c0;   // first token id of this CTA's chunk
+    int n;    // tokens in the chunk (may be 0)
+    int epv;  // elements per 16-byte vector (8 bf16 / 4 fp32)
+};
+
+// Element e of 16-byte vector v of the staged chunk, widened to fp32.
+template <int DT>
+__device__ __forceinline__ void unpack16(const uint4& u, float* x) {
+    if (DT == 1) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x[2 * i] = __uint_as_float(w[i] << 16);
+            x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    } else {
+        x[0] = __uint_as_float(u.x);
+        x[1] = __uint_as_float(u.y);
+        x[2] = __uint_as_float(u.z);
+        x[3] = __uint_as_float(u.w);
+    }
+}
+
+// Issue the bulk copy of this CTA's chunk into `buf` and wait for it.
+// Returns false if the bounded wait gave up (status already raised).
+__device__ __forceinline__ bool stage_chunk(void* buf, const char* row_base, const RowChunk& ch, int esize,
+                                            uint64_t* bar, int* status) {
+    const uint32_t bytes = static_cast<uint32_t>(ch.n) * esize;
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (bytes == 0) return true;
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_g2s(buf, row_base + static_cast<size_t>(ch.c0) * esize, bytes, bar);
+    }
+    if (!mbar_wait(bar, 0)) {
+        raise_status(status, kDevTimeout);
+        return false;
+    }
+    return true;
+}
+
+// Thread-local maximum (lowest id among equal values) of the staged chunk.
+template <int DT>
+__device__ __forceinline__ void chunk_thread_max(const uint4* buf, const RowChunk& ch, float* tmax, int* targ) {
+    constexpr int EPV = DT == 1 ? 8 : 4;
+    const int nvec = ch.n / EPV;
+    float m = -INFINITY;
+    int a = -1;
+    for (int v = threadIdx.x; v < nvec; v += kRowThreads) {
+        float x[EPV];
+        unpack16<DT>(buf[v], x);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+            if (a < 0 || x[e] > m) {
+                m = x[e];
+                a = ch.c0 + v * EPV + e;
+            }
+        }
+    }
+    *tmax = m;
+    *targ = a;
+}
+
+// ------------------------------------------------------------ expand kernel ---
+
+struct ExpandSmem {
+    uint64_t bar;
+    uint64_t tkeys[kRowThreads];
+    uint64_t cand[kCandCap];
+    uint64_t sel[kMaxTopK * kMaxTopK];  // frontier candidates / cluster merge buffer
+    uint64_t cta_top[kMaxTopK];
+    uint64_t top[kMaxTopK];
+    float wm[kRowWarps];
+    float ws[kRowWarps];
+    float cta_m, cta_s;
+    int n_cand;
+    int last;
+};
+
+template <int DT>
+__global__ void __launch_bounds__(kRowThreads) expand_kernel(TreeDims d, TreeWs w, int step, int chunk,
+                                                              const void* __restrict__ logits,
+                                                              const float* __restrict__ lse_in,
+                                                              float* __restrict__ row_lse,
+                                                              int32_t* __restrict__ ftok_out,
+                                                              int32_t* __restrict__ fcount_out) {
+    extern __shared__ __align__(128) unsigned char dyn_smem[];
+    __shared__ ExpandSmem sm;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int cpr = static_cast<int>(cluster.num_blocks());
+    const int row = blockIdx.y;
+    const int b = row / d.k, f = row % d.k;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int F = w.fcount[step * d.B + b];
+    constexpr int ES = DT == 1 ? 2 : 4;
+
+    if (f >= F) {  // this frontier slot holds no node in this step
+        if (rank == 0 && tid == 0) {
+            row_lse[(static_cast<size_t>(b) * d.D + step) * d.k + f] = __int_as_float(0x7fc00000);
+            if (f == 0) {  // F == 0: nothing to expand, the next frontier is empty
+                fcount_out[b] = 0;
+                for (int j = 0; j < d.k; ++j) ftok_out[b * d.k + j] = -1;
+            }
+        }
+        return;
+    }
+
+    RowChunk ch;
+    ch.c0 = rank * chunk;
+    ch.n = max(0, min(chunk, d.V - ch.c0));
+    ch.epv = 16 / ES;
+    const char* row_base = static_cast<const char*>(logits) + static_cast<size_t>(b * d.k + f) * d.V * ES;
+    const uint4* buf = reinterpret_cast<const uint4*>(dyn_smem);
+    stage_chunk(dyn_smem, row_base, ch, ES, &sm.bar, w.status);
+
+    // Pass 1: thread maximum (value, lowest id) -> thread key.
+    float tmax;
+    int targ;
+    chunk_thread_max<DT>(buf, ch, &tmax, &targ);
+    const uint64_t tkey = targ < 0 ? 0ull : make_key(tmax, static_cast<uint32_t>(targ));
+    sm.tkeys[tid] = tkey;
+
+    // Pass 2: thread sum of exp(x - tmax).
+    constexpr int EPV = DT == 1 ? 8 : 4;
+    const int nvec = ch.n / EPV;
+    float ts = 0.0f;
+    if (lse_in == nullptr && targ >= 0 && tmax > -INFINITY) {
+        const float mb = tmax * kLog2e;
+        for (int v = tid; v < nvec; v += kRowThreads) {
+            float x[EPV];
+            unpack16<DT>(buf[v], x);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) ts += ex2_approx(fmaf(x[e], kLog2e, -mb));
+        }
+    }
+    // Block reduction of (max, sum) with rescaling.
+    float wm = (targ >= 0) ? tmax : -INFINITY;
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, m));
+    float sc = (targ >= 0 && tmax > -INFINITY) ? ts * ex2_approx((tmax - wm) * kLog2e) : 0.0f;
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, m);
+    if (lane == 0) {
+        sm.wm[warp] = wm;
+        sm.ws[warp] = sc;
+    }
+    if (tid == 0) sm.n_cand = 0;
+    __syncthreads();
+
+    // tau = k-th largest thread key: at least k elements have key >= tau.
+    if (warp == 0) {
+        warp_topk_smem(sm.tkeys, kRowThreads, d.k, sm.top);
+        if (lane == 0) {
+            float M = -INFINITY;
+            for (int i = 0; i < kRowWarps; ++i) M = fmaxf(M, sm.wm[i]);
+            float S = 0.0f;
+            if (M > -INFINITY)
+                for (int i = 0; i < kRowWarps; ++i)
+                    if (sm.wm[i] > -INFINITY) S += sm.ws[i] * ex2_approx((sm.wm[i] - M) * kLog2e);
+            sm.cta_m = M;
+            sm.cta_s = S;
+        }
+    }
+    __syncthreads();
+    const uint64_t tau = sm.top[d.k - 1];
+
+    // Pass 3: gather the candidates (key >= tau).
+    for (int v = tid; v < nvec; v += kRowThreads) {
+        float x[EPV];
+        unpack16<DT>(buf[v], x);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+            const uint64_t key = make_key(x[e], static_cast<uint32_t>(ch.c0 + v * EPV + e));
+            if (key >= tau) {
+                const int at = atomicAdd(&sm.n_cand, 1);
+                if (at < kCandCap) sm.cand[at] = key;
+            }
+        }
+    }
+    __syncthreads();
+    const int n_cand = sm.n_cand;
+    if (n_cand <= kCandCap) {
+        if (warp == 0) warp_topk_smem(sm.cand, n_cand, d.k, sm.cta_top);
+    } else {
+        // Many equal values at the top: exact k rounds over the whole chunk.
+        uint64_t prev = ~0ull;
+        for (int r = 0; r < d.k; ++r) {
+            uint64_t best = 0;
+            for (int v = tid; v < nvec; v += kRowThreads) {
+                float x[EPV];
+                unpack16<DT>(buf[v], x);
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) {
+                    const uint64_t key = make_key(x[e], static_cast<uint32_t>(ch.c0 + v * EPV + e));
+                    if (key < prev && key > best) best = key;
+                }
+            }
+            best = warp_max_u64(best);
+            if (lane == 0) sm.tkeys[warp] = best;
+            __syncthreads();
+            if (tid == 0) {
+                uint64_t m = 0;
+                for (int i = 0; i < kRowWarps; ++i) m = sm.tkeys[i] > m ? sm.tkeys[i] : m;
+                sm.cta_top[r] = m;
+            }
+            __syncthreads();
+            prev = sm.cta_top[r];
+        }
+    }
+
+    // Cluster merge: the leader gathers every CTA's (max, sum, top-k).
+    cluster.sync();
+    if (rank == 0 && warp == 0) {
+        float M = -INFINITY;
+        for (int r = 0; r < cpr; ++r) {
+            const ExpandSmem* rs = cluster.map_shared_rank(&sm, r);
+            M = fmaxf(M, rs->cta_m);
+            for (int j = lane; j < d.k; j += 32) sm.sel[r * d.k + j] = rs->cta_top[j];
+        }
+        float S = 0.0f;
+        if (lane == 0 && M > -INFINITY)
+            for (int r = 0; r < cpr; ++r) {
+                const ExpandSmem* rs = cluster.map_shared_rank(&sm, r);
+                if (rs->cta_m > -INFINITY) S += rs->cta_s * ex2_approx((rs->cta_m - M) * kLog2e);
+            }
+        __syncwarp();
+        warp_topk_smem(sm.sel, cpr * d.k, d.k, sm.top);
+        if (lane == 0) {
+            sm.cta_m = M;
+            sm.cta_s = S;
+        }
+    }
+    cluster.sync();  // remote shared memory may be released after this point
+    if (rank != 0) return;
+
+    // Children of this frontier node.
+    const float lse = lse_in != nullptr ? lse_in[b * d.k + f] : sm.cta_m + logf(sm.cta_s);
+    const int parent = w.fnode[(step * d.B + b) * d.k + f];
+    const float plogv = parent < 0 ? 0.0f : w.cand_logv[static_cast<size_t>(b) * d.C + parent];
+    const int base = step == 0 ? 0 : d.k + (step - 1) * d.k * d.k;
+    if (tid < d.k) {
+        const uint64_t key = sm.top[tid];
+        const int id = base + f * d.k + tid;
+        const size_t at = static_cast<size_t>(b) * d.C + id;
+        if (key != 0) {
+            const float x = key_val(key);
+            const float lp = __fsub_rn(x, lse);
+            w.cand_token[at] = static_cast<int32_t>(key_id(key));
+            w.cand_parent[at] = parent;
+            w.cand_depth[at] = step + 1;
+            w.cand_logv[at] = __fadd_rn(plogv, lp);
+            w.cand_valid[at] = 1;
+        }
+    }
+    if (tid == 0) {
+        row_lse[(static_cast<size_t>(b) * d.D + step) * d.k + f] = lse;
+        if (!isfinite(lse)) raise_status(w.status, kDevNonFinite);
+    }
+    __syncthreads();
+
+    // Per-sequence ticket: the last row of this sequence picks the next frontier.
+    if (tid == 0) {
+        __threadfence();
+        const int prev = atomicAdd(&w.expand_ticket[b], 1);
+        sm.last = (prev == F - 1);
+    }
+    __syncthreads();
+    if (!sm.last) return;
+    __threadfence();
+    if (warp == 0) {
+        const int n = F * d.k;
+        for (int i = lane; i < n; i += 32) {
+            const int id = base + i;
+            const size_t at = static_cast<size_t>(b) * d.C + id;
+            const bool valid = __ldcg(reinterpret_cast<const unsigned char*>(&w.cand_valid[at])) != 0;
+            const float lv = __ldcg(&w.cand_logv[at]);
+            sm.sel[i] = (valid && lv >= d.log_thr) ? make_key(lv, static_cast<uint32_t>(id)) : 0ull;
+        }
+        __syncwarp();
+        warp_topk_smem(sm.sel, n, d.k, sm.top);
+        int cnt = 0;
+        for (int j = 0; j < d.k; ++j) cnt += sm.top[j] != 0;
+        if (lane < d.k) {
+            const uint64_t key = sm.top[lane];
+            const int id = key ? static_cast<int>(key_id(key)) : -1;
+            w.fnode[((step + 1) * d.B + b) * d.k + lane] = id;
+            ftok_out[b * d.k + lane] = id >= 0 ? __ldcg(&w.cand_token[static_cast<size_t>(b) * d.C + id]) : -1;
+        }
+        if (lane == 0) {
+            w.fcount[(step + 1) * d.B + b] = cnt;
+            fcount_out[b] = cnt;
+            w.expand_ticket[b] = 0;
+        }
+    }
+}
+
+// ------------------------------------------------------------ verify kernel ---
+
+// Fixed-order exp for lossless verification (contract in eagle.h): Cody-Waite
+// reduction with ln2 = 0x1.62e4p-1 + 0x1.7f7d1cp-20, degree-7 Taylor series of
+// exp(r) in Horner form, exact scaling by 2^n; every step one correctly
+// rounded fp32 multiply or add. z <= 0; returns 0 below -32.
+__device__ __forceinline__ float dexp_fixed(float z) {
+    if (!(z >= -32.0f)) return 0.0f;
+    const float n = rintf(__fmul_rn(z, 0x1.715476p+0f));
+    float r = __fsub_rn(z, __fmul_rn(n, 0x1.62e4p-1f));
+    r = __fsub_rn(r, __fmul_rn(n, 0x1.7f7d1cp-20f));
+    float p = 0x1.a01a02p-13f;                           // 1/7!
+    p = __fadd_rn(__fmul_rn(p, r), 0x1.6c16c2p-10f);     // 1/6!
+    p = __fadd_rn(__fmul_rn(p, r), 0x1.111112p-7f);      // 1/5!
+    p = __fadd_rn(__fmul_rn(p, r), 0x1.555556p-5f);      // 1/4!
+    p = __fadd_rn(__fmul_rn(p, r), 0x1.555556p-3f);      // 1/3!
+    p = __fadd_rn(__fmul_rn(p, r), 0.5f);                // 1/2!
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f);                // 1/1!
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f);                // 1/0!
+    const float scale = __int_as_float((static_cast<int>(n) + 127) << 23);
+    return __fmul_rn(p, scale);
+}
+
+// Integer mass floor(dexp((x - m) * inv_t) * 2^40).
+__device__ __forceinline__ uint64_t fixed_mass(float x, float m, float inv_t) {
+    const float e = dexp_fixed(__fmul_rn(__fsub_rn(x, m), inv_t));
+    return __float2ull_rz(__fmul_rn(e, 0x1p40f));
+}
+
+struct VerifySmem {
+    uint64_t bar;
+    uint64_t wkey[kRowWarps];
+    uint64_t wmass[kRowWarps];
+    uint64_t cta_key;
+    uint64_t cta_mass;
+    int last;
+    // walk state (last-arriving CTA of a sequence)
+    int tok[kMaxSlots];
+    int par[kMaxSlots];
+    int arg[kMaxSlots];
+    float rmax[kMaxSlots];
+    unsigned long long rmass[kMaxSlots];
+    unsigned long long pmass[kMaxSlots];  // mass of slot c's token in its parent's row
+    int path[kMaxDepth + 1];
+    int removed_tok[kMaxSlots];
+    unsigned long long removed_mass[kMaxSlots];
+    unsigned long long scan[kRowThreads];
+    int n_removed, a, cur, sample_chunk, bonus;
+    unsigned long long sample_t;
+};
+
+template <int DT>
+__global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs w, int mode, float inv_t, int chunk,
+                                                              const void* __restrict__ target,
+                                                              const int32_t* __restrict__ tokens,
+                                                              const int32_t* __restrict__ parent,
+                                                              const int32_t* __restrict__ n_tree,
+                                                              const uint32_t* __restrict__ uniforms,
+                                                              int32_t* __restrict__ accept_len,
+                                                              int32_t* __restrict__ slots_out,
+                                                              int32_t* __restrict__ tokens_out) {
+    extern __shared__ __align__(128) unsigned char dyn_smem[];
+    __shared__ VerifySmem sm;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int cpr = static_cast<int>(cluster.num_blocks());
+    const int row = blockIdx.y;
+    const int b = row / d.T, t = row % d.T;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int ES = DT == 1 ? 2 : 4;
+    constexpr int EPV = DT == 1 ? 8 : 4;
+    const int n = n_tree[b];
+    if (n < 1 || n > d.T) {
+        if (rank == 0 && t == 0 && tid == 0) raise_status(w.status, kDevBadIndex);
+        return;
+    }
+    if (t >= n) return;
+
+    RowChunk ch;
+    ch.c0 = rank * chunk;
+    ch.n = max(0, min(chunk, d.V - ch.c0));
+    ch.epv = EPV;
+    const char* row_base = static_cast<const char*>(target) + static_cast<size_t>(b * d.T + t) * d.V * ES;
+    const uint4* buf = reinterpret_cast<const uint4*>(dyn_smem);
+    stage_chunk(dyn_smem, row_base, ch, ES, &sm.bar, w.status);
+
+    float tmax;
+    int targ;
+    chunk_thread_max<DT>(buf, ch, &tmax, &targ);
+    uint64_t key = targ < 0 ? 0ull : make_key(tmax, static_cast<uint32_t>(targ));
+    key = warp_max_u64(key);
+    if (lane == 0) sm.wkey[warp] = key;
+    __syncthreads();
+    if (tid == 0) {
+        uint64_t m = 0;
+        for (int i = 0; i < kRowWarps; ++i) m = sm.wkey[i] > m ? sm.wkey[i] : m;
+        sm.cta_key = m;
+    }
+    cluster.sync();
+    uint64_t gkey = 0;
+    for (int r = 0; r < cpr; ++r) {
+        const uint64_t k2 = cluster.map_shared_rank(&sm, r)->cta_key;
+        gkey = k2 > gkey ? k2 : gkey;
+    }
+    const float M = key_val(gkey);
+    const size_t rt = static_cast<size_t>(b) * d.T + t;
+    if (mode == 1) {
+        const int nvec = ch.n / EPV;
+        uint64_t s = 0;
+        for (int v = tid; v < nvec; v += kRowThreads) {
+            float x[EPV];
+            unpack16<DT>(buf[v], x);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) s += fixed_mass(x[e], M, inv_t);
+        }
+        s = warp_sum_u64(s);
+        if (lane == 0) sm.wmass[warp] = s;
+        __syncthreads();
+        if (tid == 0) {
+            uint64_t tot = 0;
+            for (int i = 0; i < kRowWarps; ++i) tot += sm.wmass[i];
+            w.chunk_mass[rt * kMaxChunks + rank] = tot;
+        }
+    }
+    cluster.sync();  // remote reads done; chunk masses of the cluster are visible
+    if (rank != 0) return;
+    if (tid == 0) {
+        uint64_t mass = 0;
+        if (mode == 1)
+            for (int r = 0; r < cpr; ++r) mass += __ldcg(&w.chunk_mass[rt * kMaxChunks + r]);
+        w.row_max[rt] = M;
+        w.row_arg[rt] = static_cast<int32_t>(key_id(gkey));
+        w.row_mass[rt] = mass;
+        if (!isfinite(M)) raise_status(w.status, kDevNonFinite);
+        __threadfence();
+        const int prev = atomicAdd(&w.verify_ticket[b], 1);
+        sm.last = (prev == n - 1);
+    }
+    __syncthreads();
+    if (!sm.last) return;
+    __threadfence();
+
+    // ---- acceptance walk for sequence b (one CTA) ----
+    const int T = d.T;
+    for (int c = tid; c < T; c += kRowThreads) {
+        sm.tok[c] = c < n ? tokens[static_cast<size_t>(b) * T + c] : -1;
+        sm.par[c] = c < n ? parent[static_cast<size_t>(b) * T + c] : -1;
+        if (c < n) {
+            sm.arg[c] = __ldcg(&w.row_arg[static_cast<size_t>(b) * T + c]);
+            sm.rmax[c] = __ldcg(&w.row_max[static_cast<size_t>(b) * T + c]);
+            sm.rmass[c] = __ldcg(&w.row_mass[static_cast<size_t>(b) * T + c]);
+        }
+    }
+    __syncthreads();
+    bool bad = false;
+    for (int c = 1 + tid; c < n; c += kRowThreads) {
+        const int tk = sm.tok[c], p = sm.par[c];
+        if (tk < 0 || tk >= d.V || p < 0 || p >= c) {
+            bad = true;
+            sm.pmass[c] = 0;
+            continue;
+        }
+        if (mode == 1) {
+            const char* prow = static_cast<const char*>(target) + (static_cast<size_t>(b) * T + p) * d.V * ES;
+            float x;
+            if (DT == 1)
+                x = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(prow)[tk]) << 16);
+            else
+                x = reinterpret_cast<const float*>(prow)[tk];
+            sm.pmass[c] = fixed_mass(x, sm.rmax[p], inv_t);
+        }
+    }
+    if (bad) raise_status(w.status, kDevBadIndex);
+    __syncthreads();
+
+    if (tid == 0) {
+        int cur = 0, a = 0;
+        sm.path[0] = 0;
+        sm.n_removed = 0;
+        unsigned long long S = mode == 1 ? sm.rmass[0] : 0ull;
+        const uint32_t* u = mode == 1 ? uniforms + static_cast<size_t>(b) * (T + 2) : nullptr;
+        for (;;) {
+            int next = -1;
+            if (a < d.D) {
+                for (int c = cur + 1; c < n; ++c) {
+                    if (sm.par[c] != cur) continue;
+                    if (mode == 0) {
+                        if (sm.tok[c] == sm.arg[cur]) {
+                            next = c;
+                            break;
+                        }
+                    } else {
+                        const unsigned __int128 lhs = static_cast<unsigned __int128>(u[c] >> 8) * S;
+                        const unsigned __int128 rhs = static_cast<unsigned __int128>(sm.pmass[c]) << 24;
+                        if (lhs < rhs) {
+                            next = c;
+                            break;
+                        }
+                        S -= sm.pmass[c];
+                        sm.removed_tok[sm.n_removed] = sm.tok[c];
+                        sm.removed_mass[sm.n_removed] = sm.pmass[c];
+                        sm.n_removed++;
+                    }
+                }
+            }
+            if (next < 0) break;
+            sm.path[++a] = next;
+            cur = next;
+            if (mode == 1) {
+                S = sm.rmass[cur];
+                sm.n_removed = 0;
+            }
+        }
+        sm.a = a;
+        sm.cur = cur;
+        sm.bonus = mode == 0 ? sm.arg[cur] : -1;
+        if (mode == 1) {
+            // choose the chunk of row `cur` that holds the draw
+            const uint64_t U64 = (static_cast<uint64_t>(u[T + 1]) << 32) | u[T];
+            const unsigned long long tdraw =
+                static_cast<unsigned long long>((static_cast<unsigned __int128>(U64) * S) >> 64);
+            const size_t rc = static_cast<size_t>(b) * T + cur;
+            unsigned long long run = 0;
+            int chosen = cpr - 1;
+            unsigned long long tin = 0;
+            for (int r = 0; r < cpr; ++r) {
+                unsigned long long cm = __ldcg(&w.chunk_mass[rc * kMaxChunks + r]);
+                const int lo = r * chunk, hi = min(d.V, lo + chunk);
+                for (int q = 0; q < sm.n_removed; ++q)
+                    if (sm.removed_tok[q] >= lo && sm.removed_tok[q] < hi) cm -= sm.removed_mass[q];
+                if (run + cm > tdraw) {
+                    chosen = r;
+                    tin = tdraw - run;
+                    break;
+                }
+                run += cm;
+            }
+            sm.sample_chunk = chosen;
+            sm.sample_t = tin;
+        }
+    }
+    __syncthreads();
+
+    if (mode == 1) {
+        // Scan the chosen chunk of row `cur`: smallest y (not removed) whose
+        // running mass exceeds the draw. Each thread owns a contiguous range.
+        const int cur = sm.cur;
+        const int lo = sm.sample_chunk * chunk, hi = min(d.V, lo + chunk);
+        const int len = max(0, hi - lo);
+        const int per = (len + kRowThreads - 1) / kRowThreads;
+        const int a0 = lo + tid * per, a1 = min(hi, a0 + per);
+        const char* crow = static_cast<const char*>(target) + (static_cast<size_t>(b) * T + cur) * d.V * ES;
+        const float m = sm.rmax[cur];
+        const int nrem = sm.n_removed;
+        auto mass_at = [&](int y) -> unsigned long long {
+            for (int q = 0; q < nrem; ++q)
+                if (sm.removed_tok[q] == y) return 0ull;
+            float x;
+            if (DT == 1)
+                x = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(crow)[y]) << 16);
+            else
+                x = reinterpret_cast<const float*>(crow)[y];
+            return fixed_mass(x, m, inv_t);
+        };
+        unsigned long long mine = 0;
+        for (int y = a0; y < a1; ++y) mine += mass_at(y);
+        sm.scan[tid] = mine;
+        __syncthreads();
+        if (tid == 0) {  // exclusive prefix (256 entries)
+            unsigned long long run = 0;
+            for (int i = 0; i < kRowThreads; ++i) {
+                const unsigned long long v = sm.scan[i];
+                sm.scan[i] = run;
+                run += v;
+            }
+        }
+        __syncthreads();
+        const unsigned long long tin = sm.sample_t;
+        const unsigned long long ex = sm.scan[tid];
+        if (mine > 0 && ex <= tin && tin < ex + mine) {
+            unsigned long long run = ex;
+            for (int y = a0; y < a1; ++y) {
+                run += mass_at(y);
+                if (run > tin) {
+                    sm.bonus = y;
+                    break;
+                }
+            }
+        }
+        __syncthreads();
+    }
+
+    if (tid == 0) {
+        const int a = sm.a;
+        const int Dp1 = d.D + 1;
+        accept_len[b] = a;
+        for (int j = 0; j < Dp1; ++j) {
+            slots_out[b * Dp1 + j] = j <= a ? sm.path[j] : -1;
+            tokens_out[b * Dp1 + j] = j < a ? sm.tok[sm.path[j + 1]] : (j == a ? sm.bonus : -1);
+        }
+        if (sm.bonus < 0) raise_status(w.status, kDevBadIndex);
+        w.verify_ticket[b] = 0;
+    }
+}
+
+// -------------------------------------------------------------- launchers ---
+
+RowSplit choose_row_split(int V, int esize) {
+    RowSplit s;
+    const long row_bytes = static_cast<long>(V) * esize;
+    int cpr = 1;
+    while (cpr < kMaxChunks && row_bytes > static_cast<long>(cpr) * 32 * 1024) cpr *= 2;
+    const int epv = 16 / esize;
+    int chunk = (V + cpr - 1) / cpr;
+    chunk = (chunk + epv - 1) / epv * epv;
+    s.cpr = cpr;
+    s.chunk = chunk;
+    s.smem_bytes = static_cast<int>(align_up(static_cast<size_t>(chunk) * esize, 128));
+    return s;
+}
+
+template <typename K>
+static cudaError_t launch_rows(K kernel, dim3 grid, int cpr, int smem, cudaStream_t stream, void** args) {
+    static_assert(sizeof(K) > 0, "");
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kRowThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cpr;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    count_launch();
+    return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(kernel), args);
+}
+
+cudaError_t launch_expand(const TreeDims& d, const TreeWs& ws, int step, const void* logits, const float* lse_in,
+                          float* row_lse, int32_t* ftok, int32_t* fcount_out, cudaStream_t stream) {
+    const RowSplit s = choose_row_split(d.V, d.dtype == 1 ? 2 : 4);
+    dim3 grid(s.cpr, d.B * d.k, 1);
+    TreeDims dd = d;
+    TreeWs ww = ws;
+    int chunk = s.chunk;
+    void* args[] = {&dd,          &ww,      &step, &chunk, const_cast<void**>(&logits), const_cast<float**>(&lse_in),
+                    &row_lse,     &ftok,    &fcount_out};
+    return d.dtype == 1 ? launch_rows(expand_kernel<1>, grid, s.cpr, s.smem_bytes, stream, args)
+                        : launch_rows(expand_kernel<0>, grid, s.cpr, s.smem_bytes, stream, args);
+}
+
+cudaError_t launch_verify(const TreeDims& d, const TreeWs& ws, int mode, float inv_temp, const void* target,
+                          const int32_t* tokens, const int32_t* parent, const int32_t* n_tree,
+                          const uint32_t* uniforms, int32_t* accept_len, int32_t* slots, int32_t* out_tokens,
+                          cudaStream_t stream) {
+    const RowSplit s = choose_row_split(d.V, d.dtype == 1 ? 2 : 4);
+    dim3 grid(s.cpr, d.B * d.T, 1);
+    TreeDims dd = d;
+    TreeWs ww = ws;
+    int chunk = s.chunk;
+    void* args[] = {&dd,
+                    &ww,
+                    &mode,
+                    &inv_temp,
+                    &chunk,
+                    const_cast<void**>(&target),
+                    const_cast<int32_t**>(&tokens),
+                    const_cast<int32_t**>(&parent),
+                    const_cast<int32_t**>(&n_tree),
+                    const_cast<uint32_t**>(&uniforms),
+                    &accept_len,
+                    &slots,
+                    &out_tokens};
+    return d.dtype == 1 ? launch_rows(verify_kernel<1>, grid, s.cpr, s.smem_bytes, stream, args)
+                        : launch_rows(verify_kernel<0>, grid, s.cpr, s.smem_bytes, stream, args);
+}
+
+}  // namespace eagle

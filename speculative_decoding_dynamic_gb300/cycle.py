@@ -1,0 +1,95 @@
+"""One draft-verify cycle on device buffers, in C-ABI call order.
+
+Allocation of the caller-owned workspaces and outputs, then the sequence
+tree_init -> expand x D -> rerank -> build_tree -> tree_attention -> verify ->
+kv_compact. Every step runs in libeagle's kernels; this module only holds
+buffers and passes pointers.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import eagle as E
+
+
+def torch_dtype(code: int) -> torch.dtype:
+    return torch.float32 if code == E.EAGLE_F32 else torch.bfloat16
+
+
+class DeviceCycle:
+    """Buffers for one cycle of a (TreeCfg, KvCfg) problem on one device."""
+
+    def __init__(self, cfg: E.TreeCfg, kv: E.KvCfg, device="cuda"):
+        self.cfg, self.kv = cfg, kv
+        dev = torch.device(device)
+        B, D, k, T, W = cfg.batch, cfg.depth, cfg.top_k, cfg.T, cfg.W
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.ws = E.alloc_workspace(E.eagle_workspace_bytes(cfg), dev)
+        self.attn_ws = E.alloc_workspace(E.eagle_attention_workspace_bytes(kv, T), dev)
+        self.row_lse = torch.empty(B, D, k, dtype=torch.float32, device=dev)
+        self.ftok = torch.empty(B, k, **i32)
+        self.fcount = torch.empty(B, **i32)
+        self.tokens = torch.empty(B, T, **i32)
+        self.parent = torch.empty(B, T, **i32)
+        self.depth = torch.empty(B, T, **i32)
+        self.pos = torch.empty(B, T, **i32)
+        self.mask = torch.empty(B, T, W, **i32)  # uint32 bit rows
+        self.n_tree = torch.empty(B, **i32)
+        self.attn_out = torch.empty(B, T, kv.n_q_heads, kv.head_dim, dtype=torch_dtype(kv.dtype), device=dev)
+        self.accept_len = torch.empty(B, **i32)
+        self.slots = torch.empty(B, D + 1, **i32)
+        self.out_tokens = torch.empty(B, D + 1, **i32)
+        self.new_len = torch.empty(B, **i32)
+
+    # ---- stages -----------------------------------------------------------
+    def draft(self, draft_logits: torch.Tensor, stream=None, steps=None, lse_in=None):
+        """Stages 1-3. draft_logits: [D, B, k, V] (one contiguous block per step);
+        lse_in: optional [D, B, k] row log-sum-exp supplied from upstream."""
+        cfg = self.cfg
+        E.eagle_tree_init(cfg, self.ws, stream)
+        for s in range(cfg.depth if steps is None else steps):
+            E.eagle_expand(cfg, self.ws, s, draft_logits[s], None if lse_in is None else lse_in[s], self.row_lse,
+                           self.ftok, self.fcount, stream)
+        if steps is None:
+            E.eagle_rerank(cfg, self.ws, stream)
+
+    def build(self, prefix_len, root_token, stream=None):
+        E.eagle_build_tree(self.cfg, self.ws, prefix_len, root_token, self.tokens, self.parent, self.depth, self.pos,
+                           self.mask, self.n_tree, stream)
+
+    def attention(self, q, cache, layer, prefix_len, stream=None):
+        E.eagle_tree_attention(self.kv, self.cfg.T, q, cache, layer, prefix_len, self.mask, self.n_tree,
+                               self.attn_out, self.attn_ws, stream)
+
+    def verify(self, mode, temperature, target, uniforms, stream=None):
+        E.eagle_verify(self.cfg, self.ws, mode, temperature, target, self.tokens, self.parent, self.n_tree, uniforms,
+                       self.accept_len, self.slots, self.out_tokens, stream)
+
+    def compact(self, cache, prefix_len, stream=None):
+        E.eagle_kv_compact(self.kv, cache, prefix_len, self.accept_len, self.slots, self.cfg.depth + 1, self.new_len,
+                           self.ws, stream)
+
+    def run(self, draft_logits, prefix_len, root_token, q, cache, layer, target, uniforms, mode, temperature=1.0,
+            compact=True, stream=None):
+        """The whole cycle (all stages) enqueued on `stream`."""
+        self.draft(draft_logits, stream)
+        self.build(prefix_len, root_token, stream)
+        self.attention(q, cache, layer, prefix_len, stream)
+        self.verify(mode, temperature, target, uniforms, stream)
+        if compact:
+            self.compact(cache, prefix_len, stream)
+
+    def status(self, stream=None) -> int:
+        a = E.eagle_status_fetch(self.ws, stream)
+        b = E.eagle_status_fetch(self.attn_ws, stream)
+        return a or b
+
+
+def tree_cfg(batch, vocab, top_k, depth, node_budget, threshold, dtype) -> E.TreeCfg:
+    return E.TreeCfg(batch, vocab, top_k, depth, node_budget, threshold, dtype)
+
+
+def kv_cfg(batch, n_q_heads, n_kv_heads, head_dim, layers, max_len, dtype, seq_stride, layer_stride, kv_stride,
+           pos_stride) -> E.KvCfg:
+    return E.KvCfg(batch, n_q_heads, n_kv_heads, head_dim, layers, max_len, dtype, seq_stride, layer_stride,
+                   kv_stride, pos_stride)

@@ -1,0 +1,192 @@
+"""Python binding of libeagle (ctypes). Argument marshalling only.
+
+Every function has the name of the C entry point it calls (see
+include/eagle.h for the contract). Tensors are torch CUDA tensors; their data
+pointers and the current CUDA stream are passed through. Importing this module
+fails loudly if the CUDA library has not been built: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libeagle.so")
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libeagle.so is missing ({LIB_PATH}); build it with "
+                      "`python -m speculative_decoding_dynamic_gb300.build` (nvcc, sm_103a)")
+_lib = ctypes.CDLL(LIB_PATH)
+
+EAGLE_OK = 0
+EAGLE_F32, EAGLE_BF16 = 0, 1
+GREEDY, LOSSLESS = 0, 1
+MAX_TOPK, MAX_DEPTH, MAX_SLOTS, MAX_CANDIDATES = 16, 16, 256, 1024
+
+
+class EagleError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        msg = _lib.eagle_status_string(code).decode()
+        super().__init__(f"{fn} -> {code} ({msg})")
+        self.code = code
+
+
+class TreeCfg(ctypes.Structure):
+    """eagle_tree_cfg."""
+    _fields_ = [("batch", ctypes.c_int), ("vocab", ctypes.c_int), ("top_k", ctypes.c_int), ("depth", ctypes.c_int),
+                ("node_budget", ctypes.c_int), ("threshold", ctypes.c_float), ("logit_dtype", ctypes.c_int)]
+
+    @property
+    def T(self) -> int:
+        return self.node_budget + 1
+
+    @property
+    def W(self) -> int:
+        return (self.T + 31) // 32
+
+    @property
+    def C(self) -> int:
+        return self.top_k + (self.depth - 1) * self.top_k * self.top_k
+
+
+class KvCfg(ctypes.Structure):
+    """eagle_kv_cfg (strides in elements)."""
+    _fields_ = [("batch", ctypes.c_int), ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("layers", ctypes.c_int), ("max_len", ctypes.c_int),
+                ("dtype", ctypes.c_int), ("seq_stride", ctypes.c_int64), ("layer_stride", ctypes.c_int64),
+                ("kv_stride", ctypes.c_int64), ("pos_stride", ctypes.c_int64)]
+
+
+_p = ctypes.c_void_p
+_i = ctypes.c_int
+_sz = ctypes.c_size_t
+_TP = ctypes.POINTER(TreeCfg)
+_KP = ctypes.POINTER(KvCfg)
+
+_lib.eagle_workspace_bytes.argtypes = [_TP]
+_lib.eagle_workspace_bytes.restype = _sz
+_lib.eagle_tree_init.argtypes = [_TP, _p, _sz, _p]
+_lib.eagle_expand.argtypes = [_TP, _p, _sz, _i, _p, _p, _p, _p, _p, _p]
+_lib.eagle_rerank.argtypes = [_TP, _p, _sz, _p]
+_lib.eagle_build_tree.argtypes = [_TP, _p, _sz, _p, _p, _p, _p, _p, _p, _p, _p, _p]
+_lib.eagle_attention_workspace_bytes.argtypes = [_KP, _i]
+_lib.eagle_attention_workspace_bytes.restype = _sz
+_lib.eagle_tree_attention.argtypes = [_KP, _i, _p, _p, _i, _p, _p, _p, _p, _p, _sz, _p]
+_lib.eagle_verify.argtypes = [_TP, _p, _sz, _i, ctypes.c_float, _p, _p, _p, _p, _p, _p, _p, _p, _p]
+_lib.eagle_kv_compact.argtypes = [_KP, _p, _p, _p, _p, _i, _p, _p, _p]
+_lib.eagle_status_fetch.argtypes = [_p, ctypes.POINTER(ctypes.c_int), _p]
+_lib.eagle_tree_export.argtypes = [_TP, _p, _sz, _p, _p, _p, _p, _p, _p, _p, _p]
+_lib.eagle_verify_export.argtypes = [_TP, _p, _sz, _p, _p, _p, _p]
+_lib.eagle_kernel_launches.restype = ctypes.c_uint64
+_lib.eagle_status_string.argtypes = [_i]
+_lib.eagle_status_string.restype = ctypes.c_char_p
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, rc: int) -> None:
+    if rc != EAGLE_OK:
+        raise EagleError(fn, rc)
+
+
+def _ws(ws) -> tuple[int, int]:
+    return ws.data_ptr(), ws.numel() * ws.element_size()
+
+
+def eagle_workspace_bytes(cfg: TreeCfg) -> int:
+    return int(_lib.eagle_workspace_bytes(ctypes.byref(cfg)))
+
+
+def eagle_attention_workspace_bytes(kv: KvCfg, T: int) -> int:
+    return int(_lib.eagle_attention_workspace_bytes(ctypes.byref(kv), T))
+
+
+def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """A 256-byte aligned uint8 device tensor (torch allocations are 512-byte aligned)."""
+    if nbytes <= 0:
+        raise ValueError("invalid configuration (workspace size 0)")
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device)
+
+
+def eagle_tree_init(cfg, ws, stream=None):
+    _check("eagle_tree_init", _lib.eagle_tree_init(ctypes.byref(cfg), *_ws(ws), _stream(stream)))
+
+
+def eagle_expand(cfg, ws, step, draft_logits, row_lse_in, row_lse, frontier_tokens, frontier_count, stream=None):
+    _check("eagle_expand", _lib.eagle_expand(ctypes.byref(cfg), *_ws(ws), step, _ptr(draft_logits),
+                                             _ptr(row_lse_in), _ptr(row_lse), _ptr(frontier_tokens),
+                                             _ptr(frontier_count), _stream(stream)))
+
+
+def eagle_rerank(cfg, ws, stream=None):
+    _check("eagle_rerank", _lib.eagle_rerank(ctypes.byref(cfg), *_ws(ws), _stream(stream)))
+
+
+def eagle_build_tree(cfg, ws, prefix_len, root_token, tokens, parent, depth, pos_ids, mask, n_tree, stream=None):
+    _check("eagle_build_tree", _lib.eagle_build_tree(ctypes.byref(cfg), *_ws(ws), _ptr(prefix_len), _ptr(root_token),
+                                                     _ptr(tokens), _ptr(parent), _ptr(depth), _ptr(pos_ids),
+                                                     _ptr(mask), _ptr(n_tree), _stream(stream)))
+
+
+def eagle_tree_attention(kv, T, q, kv_cache, layer, prefix_len, mask, n_tree, out, ws, stream=None):
+    _check("eagle_tree_attention", _lib.eagle_tree_attention(ctypes.byref(kv), T, _ptr(q), _ptr(kv_cache), layer,
+                                                             _ptr(prefix_len), _ptr(mask), _ptr(n_tree), _ptr(out),
+                                                             *_ws(ws), _stream(stream)))
+
+
+def eagle_verify(cfg, ws, mode, temperature, target_logits, tokens, parent, n_tree, uniforms, accept_len,
+                 accepted_slots, out_tokens, stream=None):
+    _check("eagle_verify", _lib.eagle_verify(ctypes.byref(cfg), *_ws(ws), mode, float(temperature),
+                                             _ptr(target_logits), _ptr(tokens), _ptr(parent), _ptr(n_tree),
+                                             _ptr(uniforms), _ptr(accept_len), _ptr(accepted_slots),
+                                             _ptr(out_tokens), _stream(stream)))
+
+
+def eagle_kv_compact(kv, kv_cache, prefix_len, accept_len, accepted_slots, slots_stride, new_len, ws=None,
+                     stream=None):
+    _check("eagle_kv_compact", _lib.eagle_kv_compact(ctypes.byref(kv), _ptr(kv_cache), _ptr(prefix_len),
+                                                     _ptr(accept_len), _ptr(accepted_slots), slots_stride,
+                                                     _ptr(new_len), _ptr(ws), _stream(stream)))
+
+
+def eagle_status_fetch(ws, stream=None) -> int:
+    """Synchronises the stream; returns the device status code (0 = no fault) and clears it."""
+    st = ctypes.c_int(0)
+    _lib.eagle_status_fetch(_ptr(ws), ctypes.byref(st), _stream(stream))
+    return int(st.value)
+
+
+def eagle_tree_export(cfg, ws, cand_token=None, cand_parent=None, cand_depth=None, cand_logv=None, cand_valid=None,
+                      kept=None, n_kept=None, stream=None):
+    _check("eagle_tree_export", _lib.eagle_tree_export(ctypes.byref(cfg), *_ws(ws), _ptr(cand_token),
+                                                       _ptr(cand_parent), _ptr(cand_depth), _ptr(cand_logv),
+                                                       _ptr(cand_valid), _ptr(kept), _ptr(n_kept), _stream(stream)))
+
+
+def eagle_verify_export(cfg, ws, row_max=None, row_argmax=None, row_mass=None, stream=None):
+    _check("eagle_verify_export", _lib.eagle_verify_export(ctypes.byref(cfg), *_ws(ws), _ptr(row_max),
+                                                           _ptr(row_argmax), _ptr(row_mass), _stream(stream)))
+
+
+def eagle_kernel_launches() -> int:
+    return int(_lib.eagle_kernel_launches())
+
+
+def raw_call(name: str, *args) -> int:
+    """Call an entry point with raw ctypes arguments and return its status (host-side checks in tests)."""
+    return int(getattr(_lib, name)(*args))
