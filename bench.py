@@ -1,0 +1,549 @@
+#!/usr/bin/env python3
+"""Draft-verify cycles/s of the EAGLE-2 dynamic draft-tree cycle on GB300.
+
+One step = one whole cycle over one batch: tree init, D expand steps, rerank,
+tree emission, tree attention (one layer), verification and KV compaction of
+every layer, all in libeagle's kernels. Inputs (draft and target logits, Q,
+KV cache) are synthetic and resident in HBM before the timed region; R input
+sets larger than L2 in total are rotated between steps. The cycle of each set
+is captured once in a CUDA graph and replayed.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own replica on its own GPU (the
+sequences of a batch are independent: no collective on the data path);
+ranks meet at a barrier, the max time over ranks is taken and rank 0 prints
+one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_BYTES = 129 * 1024 * 1024
+METRIC = "draft-verify cycles/s at Llama-8B shape; HBM GB/s & % roofline per kernel"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama8b_b1")
+    ap.add_argument("--sharpness", type=float, default=None)
+    ap.add_argument("--verify", default=None, choices=[None, "greedy", "lossless"])
+    ap.add_argument("--planted", action="store_true", help="sharp draft rows (deep chains)")
+    ap.add_argument("--sets", type=int, default=0, help="rotating input sets (0 = enough to exceed L2)")
+    ap.add_argument("--seed", type=int, default=42)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel-reps", type=int, default=100)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------- helpers ---
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def workload(args):
+    from synth import workloads as WL
+    w = WL.WORKLOADS[args.workload]
+    kw = {}
+    if args.sharpness is not None:
+        kw["sharpness"] = args.sharpness
+    if args.verify is not None:
+        kw["verify"] = args.verify
+    return w.with_(**kw) if kw else w
+
+
+def start_clocks(idx: int):
+    path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+    q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    try:
+        f = open(path, "w")
+        p = subprocess.Popen(["nvidia-smi", "-i", str(idx), f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                              "-lms", "50"], stdout=f, stderr=subprocess.DEVNULL)
+        return p, f, path
+    except Exception:
+        return None, None, path
+
+
+def stop_clocks(h) -> dict | None:
+    p, f, path = h
+    if p is None:
+        return None
+    p.terminate()
+    try:
+        p.wait(timeout=5)
+    except Exception:
+        p.kill()
+    f.close()
+    sm, mx, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in open(path):
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            sm.append(float(parts[1]))
+            mx.append(float(parts[2]))
+        except ValueError:
+            continue
+        for n, v in zip(names, parts[5:9]):
+            if v.lower() == "active":
+                reasons.add(n)
+    os.unlink(path)
+    if not sm:
+        return None
+    return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
+            "samples": len(sm)}
+
+
+def kernel_src_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_dynamic_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload_name: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was
+    taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        d = json.load(open(path))
+    except Exception:
+        return None
+    e = d.get(workload_name, {}).get(kernel)
+    if not e or e.get("src_hash") != kernel_src_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------ the cycle ---
+
+def build_sets(args, w, R):
+    """Host inputs of R cycles (set r uses attention layer r and uniforms of cycle r)."""
+    from synth import workloads as WL
+    sets = []
+    for r in range(R):
+        seed = args.seed + 1000 * r
+        sets.append(dict(draft=WL.draft_logits(w, seed, planted=args.planted), target=WL.target_logits(w, seed),
+                         q=WL.queries(w, seed), uniforms=WL.uniforms(w, seed, r), layer=r))
+    return sets
+
+
+def to_dev(a):
+    import torch
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+    if a.dtype == np.uint32:
+        return torch.from_numpy(a.view(np.int32)).cuda()
+    return torch.from_numpy(a).cuda()
+
+
+def pinned(a):
+    import torch
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    elif a.dtype == np.uint32:
+        t = torch.from_numpy(a.view(np.int32))
+    else:
+        t = torch.from_numpy(a)
+    return t.pin_memory()
+
+
+def algorithmic_bytes(w, prefix_len, accept_len, layers):
+    """Bytes each stage must move per cycle (reads + writes of its operands)."""
+    es = w.esize
+    B, D, k, V, T = w.batch, w.depth, w.top_k, w.vocab, w.T
+    rows_per_seq = 1 + (D - 1) * k
+    expand = B * rows_per_seq * V * es
+    expand_step = B * k * V * es  # one step with a full frontier
+    verify = B * T * V * es
+    kv_read = int(sum(int(L) + T for L in prefix_len)) * w.n_kv_heads * w.head_dim * 2 * es
+    qo = 2 * B * T * w.n_q_heads * w.head_dim * es
+    attention = kv_read + qo
+    compact = int(2 * sum(int(a) for a in accept_len) * layers * 2 * w.n_kv_heads * w.head_dim * es)
+    return dict(expand=expand, expand_step=expand_step, verify=verify, attention=attention, compact=compact)
+
+
+def oracle_cycle(w, s, prefix_len, root, kh, vh, geo, mode, tree_region, head_stride=1):
+    """One whole cycle in the CPU oracle (the bench's CPU baseline / reference arm).
+
+    Returns the estimated cycle time in seconds: every stage is run in full
+    except that, with head_stride m > 1, tree attention runs on every m-th query
+    head only and its measured time is multiplied by m (attention is ~95% of
+    the oracle's cycle)."""
+    import oracle
+    t0 = time.perf_counter()
+    cfg = oracle.TreeCfg(w.batch, w.vocab, w.top_k, w.depth, w.node_budget, w.threshold)
+    t = oracle.Tree(cfg)
+    for st in range(w.depth):
+        t.expand(st, s["draft"][st])
+    t.rerank()
+    tr = t.build_tree(prefix_len, root)
+    t1 = time.perf_counter()
+    pos_stride = w.n_kv_heads * w.head_dim
+    if head_stride == 1:
+        oracle.attention(s["q"], kh, vh, geo["max_len"] * pos_stride, pos_stride, prefix_len, tr["mask"],
+                         tr["n_tree"], w.n_kv_heads)
+    else:
+        rows = np.array([(b, i, h) for b in range(w.batch) for i in range(w.T)
+                         for h in range(0, w.n_q_heads, head_stride)], np.int32)
+        oracle.attention_rows(rows, s["q"], kh, vh, geo["max_len"] * pos_stride, pos_stride, prefix_len,
+                              tr["mask"], tr["n_tree"], w.n_kv_heads)
+    t2 = time.perf_counter()
+    if mode == "greedy":
+        a, sl, _, _ = oracle.verify_greedy(s["target"], tr["tokens"], tr["parent"], tr["n_tree"], w.depth)
+    else:
+        a, sl, _ = oracle.verify_lossless(s["target"], tr["tokens"], tr["parent"], tr["n_tree"], s["uniforms"],
+                                          w.depth, np.float32(1.0 / w.temperature))
+    reg = tree_region.copy()
+    L = reg.shape[1]
+    oracle.kv_compact(reg.reshape(-1), w.batch, L, w.n_kv_heads, w.head_dim, L * 2 * w.T * pos_stride,
+                      2 * w.T * pos_stride, w.T * pos_stride, pos_stride, np.zeros(w.batch, np.int32), a, sl)
+    t3 = time.perf_counter()
+    return (t1 - t0) + head_stride * (t2 - t1) + (t3 - t2)
+
+
+def host_attention_layer(w, geo, prefix_len, seed, layer):
+    from synth import workloads as WL
+    npdt = np.float32 if w.esize == 4 else np.uint16
+    shape = (w.batch, geo["max_len"], w.n_kv_heads, w.head_dim)
+    K = np.zeros(shape, npdt)
+    Vv = np.zeros(shape, npdt)
+    for b in range(w.batch):
+        for which, arr in ((0, K), (1, Vv)):
+            WL.kv_fill(arr, w, geo, b, layer, which, 0, int(prefix_len[b]) + w.T, seed,
+                       offset=b * geo["seq_stride"] + layer * geo["layer_stride"] + which * geo["kv_stride"]
+                       - b * geo["max_len"] * geo["pos_stride"])
+    return K, Vv
+
+
+def host_tree_region(w, geo, prefix_len, seed, layers):
+    from synth import workloads as WL
+    npdt = np.float32 if w.esize == 4 else np.uint16
+    out = np.zeros((w.batch, layers, 2, w.T, w.n_kv_heads, w.head_dim), npdt)
+    for b in range(w.batch):
+        L = int(prefix_len[b])
+        for layer in range(layers):
+            for which in range(2):
+                sub = np.zeros(w.T * geo["pos_stride"], npdt)
+                base = b * geo["seq_stride"] + layer * geo["layer_stride"] + which * geo["kv_stride"]
+                WL.kv_fill(sub, w, geo, b, layer, which, L, L + w.T, seed, offset=base + L * geo["pos_stride"])
+                out[b, layer, which] = sub.reshape(w.T, w.n_kv_heads, w.head_dim)
+    return out
+
+
+def run_reference(args, w):
+    """The oracle as it stands, timed on the host cores: the bench's reference arm.
+
+    Each step is one oracle cycle of the workload; when K + W full cycles would
+    take more than ~150 s, tree attention (the dominant stage) is sampled on
+    every m-th query head and its time scaled by m."""
+    from synth import workloads as WL
+    import oracle
+    oracle.build()
+    seed = args.seed
+    s = build_sets(args, w, 1)[0]
+    prefix_len = w.prefix_lengths(seed)
+    root = WL.root_tokens(w, seed)
+    geo = WL.kv_geometry(w, seed, w.layers)
+    kh, vh = host_attention_layer(w, geo, prefix_len, seed, 0)
+    region = host_tree_region(w, geo, prefix_len, seed, w.layers)
+    probe = oracle_cycle(w, s, prefix_len, root, kh, vh, geo, w.verify, region, head_stride=w.n_q_heads)
+    full_est = probe  # with one head per group measured and scaled: an estimate of a full cycle
+    m = 1
+    while m < w.n_q_heads and (args.steps + args.warmup) * full_est / m > 150.0:
+        m *= 2
+    while w.n_q_heads % m:
+        m //= 2
+    for _ in range(args.warmup):
+        oracle_cycle(w, s, prefix_len, root, kh, vh, geo, w.verify, region, head_stride=m)
+    tot = 0.0
+    for _ in range(args.steps):
+        tot += oracle_cycle(w, s, prefix_len, root, kh, vh, geo, w.verify, region, head_stride=m)
+    v = args.steps / tot
+    unit = "cycles/s"
+    sample = (f"{args.steps} oracle cycles of {w.name}: every stage in full"
+              + ("" if m == 1 else f" except tree attention on every {m}-th query head, its time scaled by {m}")
+              + f"; one host core")
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": unit, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "vocab": w.vocab, "depth": w.depth,
+                       "top_k": w.top_k, "node_budget": w.node_budget, "verify": w.verify,
+                       "sharpness": w.sharpness if not isinstance(w.sharpness, tuple) else list(w.sharpness)},
+            "cpu_baseline": {"value": v, "unit": unit, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    ws_, rank, local = dist_env()
+    w = workload(args)
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, w)
+        return
+
+    import torch
+    torch.cuda.set_device(local)
+    if ws_ > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from synth import workloads as WL
+    from speculative_decoding_dynamic_gb300 import build as Bld
+    Bld.build()
+    from speculative_decoding_dynamic_gb300 import cycle as C
+    from speculative_decoding_dynamic_gb300 import eagle as E
+
+    seed = args.seed + 7919 * rank
+    per_set = (w.depth * w.batch * w.top_k + w.batch * w.T) * w.vocab * w.esize
+    prefix_len = w.prefix_lengths(seed)
+    geo = WL.kv_geometry(w, seed, w.layers)
+    attn_bytes = int(sum(int(L) + w.T for L in prefix_len)) * w.n_kv_heads * w.head_dim * 2 * w.esize
+    R = args.sets or max(2, int(np.ceil(1.5 * L2_BYTES / (per_set + attn_bytes))))
+    R = min(R, w.layers)
+    # inputs per set
+    host_sets = []
+    for r in range(R):
+        sd = seed + 1000 * r
+        host_sets.append(dict(draft=WL.draft_logits(w, sd, planted=args.planted), target=WL.target_logits(w, sd),
+                              q=WL.queries(w, sd), uniforms=WL.uniforms(w, sd, r)))
+    dev_sets = [{k: to_dev(v) for k, v in s.items()} for s in host_sets]
+    root = WL.root_tokens(w, seed)
+    prefix_d = to_dev(prefix_len)
+    root_d = to_dev(root)
+
+    # KV cache: attention layers 0..R-1 filled over [0, L+T), every layer's tree region.
+    npdt = np.float32 if w.esize == 4 else np.uint16
+    cache = torch.empty(w.batch * geo["seq_stride"], dtype=C.torch_dtype(w.dtype), device="cuda")
+    for b in range(w.batch):
+        L = int(prefix_len[b])
+        for layer in range(w.layers):
+            for which in range(2):
+                p0 = 0 if layer < R else L
+                host = np.zeros((L + w.T - p0) * geo["pos_stride"], npdt)
+                base = b * geo["seq_stride"] + layer * geo["layer_stride"] + which * geo["kv_stride"]
+                WL.kv_fill(host, w, geo, b, layer, which, p0, L + w.T, seed, offset=base + p0 * geo["pos_stride"])
+                lo = base + p0 * geo["pos_stride"]
+                cache[lo:lo + host.size].copy_(to_dev(host).view(-1))
+
+    cfg = E.TreeCfg(w.batch, w.vocab, w.top_k, w.depth, w.node_budget, w.threshold, w.dtype)
+    kv = E.KvCfg(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.layers, geo["max_len"], w.dtype,
+                 geo["seq_stride"], geo["layer_stride"], geo["kv_stride"], geo["pos_stride"])
+    dc = C.DeviceCycle(cfg, kv)
+    mode = E.GREEDY if w.verify == "greedy" else E.LOSSLESS
+
+    def cycle(r, stream=None):
+        s = dev_sets[r]
+        dc.run(s["draft"], prefix_d, root_d, s["q"], cache, r, s["target"], s["uniforms"], mode, w.temperature,
+               compact=True, stream=stream)
+
+    # warm-up outside capture (sets kernel attributes), then one graph per set
+    for r in range(R):
+        cycle(r)
+    torch.cuda.synchronize()
+    assert dc.status() == 0, "device status after warm-up"
+    graphs = []
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    n0 = E.eagle_kernel_launches()
+    for r in range(R):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            cycle(r)
+        graphs.append(g)
+    launches_per_cycle = (E.eagle_kernel_launches() - n0) // R
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+    for i in range(args.warmup):
+        graphs[i % R].replay()
+    torch.cuda.synchronize()
+    if ws_ > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    clk = start_clocks(local) if rank == 0 else None
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        graphs[i % R].replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if ws_ > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+    clocks = stop_clocks(clk) if clk else None
+    ms_per_step = ms / args.steps
+    value = ws_ * args.steps / (ms / 1e3)
+
+    acc = dc.accept_len.cpu().numpy()
+    n_tree = dc.n_tree.cpu().numpy()
+
+    # ---- per-kernel timing: each stage call alone, same launch configuration ----
+    def time_call(fn, reps):
+        for i in range(3):
+            fn(i % R)
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(reps):
+            fn(i % R)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    reps = args.kernel_reps
+    # state for standalone stage calls: a completed cycle on set 0
+    cycle(0)
+    torch.cuda.synchronize()
+    kt = {}
+    kt["expand_step"] = time_call(lambda r: E.eagle_expand(cfg, dc.ws, min(1, w.depth - 1), dev_sets[r]["draft"][
+        min(1, w.depth - 1)], None, dc.row_lse, dc.ftok, dc.fcount), reps)
+    cycle(0)
+    kt["rerank"] = time_call(lambda r: E.eagle_rerank(cfg, dc.ws), reps)
+    kt["build_tree"] = time_call(lambda r: dc.build(prefix_d, root_d), reps)
+    kt["attention"] = time_call(lambda r: dc.attention(dev_sets[r]["q"], cache, r, prefix_d), reps)
+    kt["verify"] = time_call(lambda r: dc.verify(mode, w.temperature, dev_sets[r]["target"], dev_sets[r]["uniforms"]),
+                             reps)
+    cycle(0)
+    kt["compact"] = time_call(lambda r: dc.compact(cache, prefix_d), reps)
+    torch.cuda.synchronize()
+    alg = algorithmic_bytes(w, prefix_len, acc, w.layers)
+    peak = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else None
+    hbm_peak = peak["hbm_gbs"] if peak else 6800.0
+    peak_src = "measured" if peak else "fallback"
+    per_kernel = {}
+    for name, ms_k in kt.items():
+        byt = {"expand_step": alg["expand_step"], "attention": alg["attention"], "verify": alg["verify"],
+               "compact": alg["compact"]}.get(name)
+        e = {"ms": round(ms_k, 5)}
+        if byt is not None:
+            e["bytes"] = int(byt)
+            e["GB_s"] = round(byt / (ms_k * 1e-3) / 1e9, 1)
+            e["frac_hbm"] = round(byt / (ms_k * 1e-3) / 1e9 / hbm_peak, 4)
+        per_kernel[name] = e
+    cyc_share = {"expand_step": kt["expand_step"] * (w.depth - 1), "attention": kt["attention"],
+                 "verify": kt["verify"]}
+    dom = max(cyc_share, key=cyc_share.get)
+    dom_bytes = {"expand_step": alg["expand_step"], "attention": alg["attention"], "verify": alg["verify"]}[dom]
+    achieved = dom_bytes / (kt[dom] * 1e-3) / 1e9
+    kname = {"expand_step": "expand_kernel", "attention": "attention", "verify": "verify_kernel"}[dom]
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(achieved / hbm_peak, 4), "traffic": ncu_traffic(kname, w.name), "kernel": kname,
+                "peak_source": f"{peak_src} hbm_gbs (burst copy)",
+                "bytes_per_launch": int(dom_bytes)}
+
+    # ---- end to end through host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        pin = [{k: pinned(v) for k, v in s.items()} for s in host_sets]
+        out_a = torch.empty(w.batch, dtype=torch.int32).pin_memory()
+        out_t = torch.empty(w.batch, w.depth + 1, dtype=torch.int32).pin_memory()
+        out_n = torch.empty(w.batch, dtype=torch.int32).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in pin[0].values())
+        d2h = (out_a.numel() + out_t.numel() + out_n.numel()) * 4
+
+        def e2e_step(i):
+            r = i % R
+            for k_, v in pin[r].items():
+                dev_sets[r][k_].copy_(v, non_blocking=True)
+            cycle(r)
+            out_a.copy_(dc.accept_len, non_blocking=True)
+            out_t.copy_(dc.out_tokens, non_blocking=True)
+            out_n.copy_(dc.new_len, non_blocking=True)
+
+        for i in range(min(args.warmup, 3)):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        e2e = {"value": round(ws_ * args.steps / dt, 2), "unit": "cycles/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h),
+               "note": "pinned host inputs copied in, C-ABI calls issued per step (no graph), results copied out"}
+
+    # ---- CPU baseline: the oracle as it stands on a bounded sample ----
+    cpu = None
+    if rank == 0 and ws_ == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        kh, vh = host_attention_layer(w, geo, prefix_len, seed, 0)
+        region = host_tree_region(w, geo, prefix_len, seed, w.layers)
+        s0 = dict(host_sets[0])
+        n = 0
+        tot = 0.0
+        t0 = time.perf_counter()
+        while n < 1 or (time.perf_counter() - t0 < 12.0 and n < 50):
+            tot += oracle_cycle(w, s0, prefix_len, root, kh, vh, geo, w.verify, region)
+            n += 1
+        cpu = {"value": round(n / tot, 4), "unit": "cycles/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} whole oracle cycles of {w.name} (every stage, all attention rows) on one host core"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "cycles/s", "n_gpus": ws_, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == E.EAGLE_BF16 else "f32",
+            "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "vocab": w.vocab, "depth": w.depth, "top_k": w.top_k,
+                       "node_budget": w.node_budget, "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads,
+                       "head_dim": w.head_dim, "prefix": w.prefix if not isinstance(w.prefix, tuple) else
+                       list(w.prefix), "sharpness": w.sharpness if not isinstance(w.sharpness, tuple) else
+                       list(w.sharpness), "verify": w.verify, "compact_layers": w.layers, "planted": args.planted,
+                       "l2": f"{R} rotating input sets, {round(R * (per_set + attn_bytes) / 2**20)} MiB > 129 MB L2",
+                       "graph": "one CUDA graph per input set, replayed"},
+            "tokens_of_tree_per_s": round(value * float(np.mean(n_tree)) * w.batch, 1),
+            "accepted_tokens_per_s": round(value * float(np.mean(acc + 1)) * w.batch, 1),
+            "roofline": roofline, "kernels": per_kernel, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": int(launches_per_cycle * args.steps), "launches_per_cycle": int(launches_per_cycle),
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if ws_ > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

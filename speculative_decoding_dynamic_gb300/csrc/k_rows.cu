@@ -23,6 +23,9 @@
 
 #include <cmath>
 #include <cstdio>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "eagle_internal.cuh"
 #include "eagle_ws.h"
@@ -659,10 +662,27 @@ RowSplit choose_row_split(int V, int esize) {
     return s;
 }
 
+// Raise a kernel's dynamic shared memory limit only when a launch needs more
+// than was set before, so that launches inside a CUDA graph capture (after a
+// first call outside it) make no attribute calls.
+static cudaError_t ensure_dyn_smem(const void* kernel, int smem) {
+    static std::mutex mu;
+    static std::map<std::pair<const void*, int>, int> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const std::pair<const void*, int> key(kernel, dev);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = done.find(key);
+    if (it != done.end() && it->second >= smem) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) done[key] = smem;
+    return e;
+}
+
 template <typename K>
 static cudaError_t launch_rows(K kernel, dim3 grid, int cpr, int smem, cudaStream_t stream, void** args) {
-    static_assert(sizeof(K) > 0, "");
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(kernel), smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
