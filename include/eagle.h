@@ -215,6 +215,31 @@ int eagle_verify(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int mode,
 int eagle_kv_compact(const eagle_kv_cfg* kv, void* kv_cache, const int32_t* prefix_len, const int32_t* accept_len,
                      const int32_t* accepted_slots, int slots_stride, int32_t* new_len, void* ws, void* stream);
 
+/*
+ * eagle_verify without a workspace, for callers that may not allocate device
+ * memory (for example a plugin whose host engine plans all GPU memory up
+ * front and forbids later allocations, or a decode loop that must never wait
+ * on the allocator). No counterpart on the pages: it is the same stage 6 as
+ * eagle_verify, with the same arguments and results, minus ws/ws_bytes.
+ *   - Its per-row scratch is one fixed device array inside the library
+ *     (about 324 KB, present on every GPU that loads the library until the
+ *     process exits). It supports batch <= 1024 and batch * (node_budget + 1)
+ *     <= 4096 and returns EAGLE_ERR_UNSUPPORTED beyond that.
+ *   - The first call on a device looks up that array's device address; make
+ *     that first call before any stream capture.
+ *   - Every call uses the same array, so calls that overlap on the GPU (on
+ *     different streams, or from different threads) race and corrupt each
+ *     other; serialise them. The array keeps the last call's contents; the
+ *     call clears what must start at zero.
+ *   - Device-detected faults are not reported (there is no workspace status
+ *     word to read); bounds checks still keep every access in range.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+int eagle_verify_static(const eagle_tree_cfg* cfg, int mode, float temperature, const void* target_logits,
+                        const int32_t* tokens, const int32_t* parent, const int32_t* n_tree,
+                        const uint32_t* uniforms, int32_t* accept_len, int32_t* accepted_slots,
+                        int32_t* out_tokens, void* stream);
+
 /* Synchronise `stream`, read the device status word of a workspace (the tree
  * workspace or the attention scratch: the word is the first 4 bytes of
  * either) into *device_status (0 = no fault, 1 non-finite row, 2 wait gave

@@ -75,6 +75,7 @@ _lib.eagle_attention_workspace_bytes.restype = _sz
 _lib.eagle_tree_attention.argtypes = [_KP, _i, _p, _p, _i, _p, _p, _p, _p, _p, _sz, _p]
 _lib.eagle_verify.argtypes = [_TP, _p, _sz, _i, ctypes.c_float, _p, _p, _p, _p, _p, _p, _p, _p, _p]
 _lib.eagle_kv_compact.argtypes = [_KP, _p, _p, _p, _p, _i, _p, _p, _p]
+_lib.eagle_verify_static.argtypes = [_TP, _i, ctypes.c_float, _p, _p, _p, _p, _p, _p, _p, _p, _p]
 _lib.eagle_status_fetch.argtypes = [_p, ctypes.POINTER(ctypes.c_int), _p]
 _lib.eagle_tree_export.argtypes = [_TP, _p, _sz, _p, _p, _p, _p, _p, _p, _p, _p]
 _lib.eagle_verify_export.argtypes = [_TP, _p, _sz, _p, _p, _p, _p]
@@ -155,6 +156,15 @@ def eagle_verify(cfg, ws, mode, temperature, target_logits, tokens, parent, n_tr
                                              _ptr(target_logits), _ptr(tokens), _ptr(parent), _ptr(n_tree),
                                              _ptr(uniforms), _ptr(accept_len), _ptr(accepted_slots),
                                              _ptr(out_tokens), _stream(stream)))
+
+
+def eagle_verify_static(cfg, mode, temperature, target_logits, tokens, parent, n_tree, uniforms, accept_len,
+                        accepted_slots, out_tokens, stream=None):
+    """eagle_verify for callers that may not allocate: scratch lives in a fixed device array of the library."""
+    _check("eagle_verify_static", _lib.eagle_verify_static(ctypes.byref(cfg), mode, float(temperature),
+                                                           _ptr(target_logits), _ptr(tokens), _ptr(parent),
+                                                           _ptr(n_tree), _ptr(uniforms), _ptr(accept_len),
+                                                           _ptr(accepted_slots), _ptr(out_tokens), _stream(stream)))
 
 
 def eagle_kv_compact(kv, kv_cache, prefix_len, accept_len, accepted_slots, slots_stride, new_len, ws=None,
