@@ -114,6 +114,11 @@ cudaError_t launch_attention(const KvDims& kv, int T, const void* q, const void*
                              const int32_t* prefix_len, const uint32_t* mask, const int32_t* n_tree, void* out,
                              void* ws, size_t ws_bytes, int* status, cudaStream_t stream);
 
+// Raise a kernel's dynamic shared memory limit on the current device when a
+// launch needs more than was set before (no attribute call once set, so that
+// launches inside a stream capture that follow a first call make none).
+cudaError_t ensure_dyn_smem(const void* kernel, int smem);
+
 // Host-side launch counter (incremented by every launcher).
 void count_launch(int n = 1);
 

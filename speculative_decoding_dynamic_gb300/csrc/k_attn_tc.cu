@@ -1,5 +1,34 @@
-// Stage 5 dispatch. The scratch of eagle_tree_attention starts with the
-// status word (256 bytes reserved).
+// Stage 5, tensor-core path (sm_103a): tree-masked GQA attention.
+//
+// For sequence b, KV head hk, the G = Hq/Hkv query heads of every tree slot
+// form M = G*T query rows (row r <-> slot r / G, head hk*G + r % G, matching
+// the [B, T, Hq, d] layout of Q). One CTA owns a 128-row block of them and a
+// range of 128-key tiles of the sequence's keys (prefix [0, L_b) then the
+// tree slots at L_b + j), and runs, per key tile:
+//   S = Q K^T        tcgen05.mma kind::f16, bf16 operands from shared memory,
+//                    fp32 accumulator in tensor memory (TMEM columns 0..127)
+//   P = softmax part one thread per row (TMEM lane = row): scale, tree mask,
+//                    running max in the log2 domain, P written as bf16 to
+//                    shared memory in the 128B-swizzled K-major layout
+//   O_tile = P V     tcgen05.mma into TMEM columns 128..255, V read MN-major
+//   O += ...         rescaled accumulation in registers
+// K/V tiles arrive by TMA (cp.async.bulk.tensor, 128B swizzle) into a
+// two-stage ring; Q once per CTA. Warp 0 issues TMA, one thread of warp 1
+// issues the MMAs, warps 2..5 do the softmax; mbarriers order them, every
+// wait is bounded. Key ranges of one (b, hk, row block) may be split over
+// CTAs (split-KV): each writes (O, max, sum) partials and the last CTA to
+// arrive on a per-unit counter merges them (log-sum-exp combine).
+//
+// Keys of slot i: every prefix position and the tree slots set in mask row i
+// ["EAGLE" notes, EAGLE 方法: Medusa-style tree attention verifies every
+// branch in one pass; "EAGLE-2: Faster Inference ..." summary 4.2].
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include <cmath>
+#include <mutex>
 
 #include "eagle_internal.cuh"
 #include "eagle_ws.h"
@@ -10,12 +39,549 @@ cudaError_t launch_attention_simt(const KvDims& kv, int T, const void* q, const 
                                   const int32_t* prefix_len, const uint32_t* mask, const int32_t* n_tree, void* out,
                                   int* status, cudaStream_t stream);
 
-size_t attention_ws_bytes(const KvDims& /*kv*/, int /*T*/) { return 256; }
+namespace {
+
+constexpr int kBM = 128;                   // query rows per CTA (one MMA M)
+constexpr int kBN = 128;                   // keys per tile (MMA N of QK^T, K of PV)
+constexpr int kHD = 128;                   // head dim (MMA K of QK^T, N of PV)
+constexpr int kTile = kBM * kHD * 2;       // 32 KB: a 128 x 128 bf16 tile
+constexpr int kHalf = kTile / 2;           // 16 KB: 128 rows x 64 columns (one swizzle-128B column block)
+constexpr int kStages = 2;
+constexpr int kThreads = 192;
+constexpr int kSmemQ = 0;
+constexpr int kSmemKV = kTile;             // stage s: K at kSmemKV + s*2*kTile, V at +kTile
+constexpr int kSmemP = kTile * (1 + 2 * kStages);
+constexpr int kSmemBytes = kSmemP + kTile;  // 192 KB
+constexpr int kTmemCols = 256;
+constexpr int kMaxW = kMaxSlots / 32;
+
+struct TcParams {
+    int B, T, Hq, Hkv, G, n_rb, nsplit, tps, max_len, W;
+    const int32_t* prefix_len;
+    const uint32_t* mask;
+    const int32_t* n_tree;
+    __nv_bfloat16* out;
+    float* part_o;   // [units * nsplit, 128, 128]
+    float* part_ml;  // [units * nsplit, 128, 2]
+    int* tickets;    // [units]
+    int* status;
+    float scale_log2;
+};
+
+// ---------------------------------------------------------------- PTX ---
+
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+        "%5}], [%6];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (layout type 2),
+// descriptor version 1 (bit 46). Start address, leading and stride byte
+// offsets are encoded in 16-byte units.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulate (bits 4-5 = 1), A and B
+// bf16 (bits 7-9, 10-12 = 1), A K-major (bit 15 = 0), B major (bit 16),
+// N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(b_mn_major) << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, int accum) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accum)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void named_sync_softmax() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// ------------------------------------------------------------- kernel ---
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, TcParams p) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* smem =
+        reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ uint64_t bar_q, bar_kv_full[kStages], bar_kv_empty[kStages], bar_s_full, bar_p_full, bar_o_full,
+        bar_s_free;
+    __shared__ uint32_t tmem_holder;
+    __shared__ uint32_t mask_sm[kBM][kMaxW];
+    __shared__ int sh_last;
+
+    const int rb = blockIdx.x, split = blockIdx.y;
+    const int b = blockIdx.z / p.Hkv, hk = blockIdx.z % p.Hkv;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int L = p.prefix_len[b];
+    const int n = p.n_tree[b];
+    const bool bad = L < 0 || L + p.T > p.max_len || n < 1 || n > p.T;
+    const int nkeys = bad ? 0 : L + n;
+    const int ntiles = (nkeys + kBN - 1) / kBN;
+    const int nsplit_b = bad ? 1 : (ntiles + p.tps - 1) / p.tps;
+    if (split >= nsplit_b) return;  // uniform over the CTA
+    const int t_begin = split * p.tps, t_end = min(ntiles, t_begin + p.tps);
+    const int n_local = bad ? 0 : t_end - t_begin;
+    const int unit = (b * p.Hkv + hk) * p.n_rb + rb;
+    const int i0 = rb * (kBM / p.G);  // first slot of this row block
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bar_q, 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bar_kv_full[s], 1);
+            mbar_init(&bar_kv_empty[s], 1);
+        }
+        mbar_init(&bar_s_full, 1);
+        mbar_init(&bar_p_full, 128);
+        mbar_init(&bar_o_full, 1);
+        mbar_init(&bar_s_free, 128);
+        fence_mbar_init();
+
+        if (bad) raise_status(p.status, kDevBadIndex);
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_holder)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (warp >= 2) {  // this row's mask words
+        const int r = ((warp & 3) << 5) | lane;
+        const int i = i0 + r / p.G;
+        for (int w = 0; w < kMaxW; ++w)
+            mask_sm[r][w] = (w < p.W && i < p.T && !bad) ? p.mask[(static_cast<size_t>(b) * p.T + i) * p.W + w] : 0u;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_holder;
+    const uint32_t tmem_s = tmem, tmem_o = tmem + 128;
+
+    unsigned char* sQ = smem + kSmemQ;
+    unsigned char* sP = smem + kSmemP;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer ---
+        if (lane == 0 && n_local > 0) {
+            mbar_arrive_expect_tx(&bar_q, kTile);
+            tma_load_4d(sQ, &tm_q, 0, hk * p.G, i0, b, &bar_q);
+            tma_load_4d(sQ + kHalf, &tm_q, 64, hk * p.G, i0, b, &bar_q);
+            for (int jj = 0; jj < n_local; ++jj) {
+                const int st = jj & 1;
+                if (jj >= kStages && !mbar_wait(&bar_kv_empty[st], ((jj >> 1) - 1) & 1)) {
+                    raise_status(p.status, kDevTimeout);
+                    break;
+                }
+                unsigned char* sK = smem + kSmemKV + st * 2 * kTile;
+                unsigned char* sV = sK + kTile;
+                const int key0 = (t_begin + jj) * kBN;
+                mbar_arrive_expect_tx(&bar_kv_full[st], 2 * kTile);
+                tma_load_4d(sK, &tm_k, 0, hk, key0, b, &bar_kv_full[st]);
+                tma_load_4d(sK + kHalf, &tm_k, 64, hk, key0, b, &bar_kv_full[st]);
+                tma_load_4d(sV, &tm_v, 0, hk, key0, b, &bar_kv_full[st]);
+                tma_load_4d(sV + kHalf, &tm_v, 64, hk, key0, b, &bar_kv_full[st]);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------- MMA issuer ---
+        if (lane == 0 && n_local > 0) {
+            constexpr uint32_t id_qk = idesc_bf16(kBM, kBN, 0);
+            constexpr uint32_t id_pv = idesc_bf16(kBM, kHD, 1);
+            bool ok = mbar_wait(&bar_q, 0);
+            for (int jj = 0; ok && jj < n_local; ++jj) {
+                const int st = jj & 1;
+                ok = mbar_wait(&bar_kv_full[st], (jj >> 1) & 1);
+                if (ok && jj > 0) ok = mbar_wait(&bar_s_free, (jj - 1) & 1);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t aK = smem_u32(smem + kSmemKV + st * 2 * kTile);
+                const uint32_t aV = aK + kTile;
+                const uint32_t aQ = smem_u32(sQ);
+#pragma unroll
+                for (int kk = 0; kk < kHD / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+                    mma_bf16(tmem_s, smem_desc(aQ + off, 16, 1024), smem_desc(aK + off, 16, 1024), id_qk, kk > 0);
+                }
+                mma_commit(&bar_s_full);
+                ok = mbar_wait(&bar_p_full, jj & 1);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t aP = smem_u32(sP);
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk) {
+                    const uint32_t offp = (kk >> 2) * kHalf + (kk & 3) * 32;
+                    mma_bf16(tmem_o, smem_desc(aP + offp, 16, 1024), smem_desc(aV + kk * 2048, kHalf, 1024), id_pv,
+                             kk > 0);
+                }
+                mma_commit(&bar_o_full);
+                mma_commit(&bar_kv_empty[st]);
+            }
+            if (!ok) {
+                raise_status(p.status, kDevTimeout);
+            }
+        }
+    } else {
+        // ------------------------------------------------------ softmax ---
+        const int q4 = warp & 3;
+        const int r = (q4 << 5) | lane;                  // row of the block = TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+        const int grow = rb * kBM + r;                   // row within the (b, hk) problem
+        const int i = i0 + r / p.G;                      // tree slot of the row
+        const int g = r % p.G;
+        float acc[kHD];
+#pragma unroll
+        for (int e = 0; e < kHD; ++e) acc[e] = 0.0f;
+        float m = -INFINITY, l = 0.0f;
+        bool ok = true;
+        for (int jj = 0; jj < n_local; ++jj) {
+            const int st = jj & 1;
+            const int key0 = (t_begin + jj) * kBN;
+            if (!mbar_wait(&bar_s_full, jj & 1)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const bool prefix_only = key0 + kBN <= L;
+            // pass 1: row maximum over the visible keys of this tile
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float v[32];
+                tmem_ld32(tmem_s + lane_off + c * 32, v);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int key = key0 + c * 32 + e;
+                    bool vis = true;
+                    if (!prefix_only) {
+                        const int j = key - L;
+                        vis = key < L || (j < n && ((mask_sm[r][j >> 5] >> (j & 31)) & 1u));
+                    }
+                    if (vis) mx = fmaxf(mx, v[e] * p.scale_log2);
+                }
+            }
+            const float m_new = fmaxf(m, mx);
+            const float m_use = m_new == -INFINITY ? 0.0f : m_new;
+            const float alpha = ex2_approx(m - m_use);
+            // pass 2: probabilities -> bf16 P (swizzled K-major), row sum
+            float sum = 0.0f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float v[32];
+                tmem_ld32(tmem_s + lane_off + c * 32, v);
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float pr[2];
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        const int key = key0 + c * 32 + e + t;
+                        bool vis = true;
+                        if (!prefix_only) {
+                            const int j = key - L;
+                            vis = key < L || (j < n && ((mask_sm[r][j >> 5] >> (j & 31)) & 1u));
+                        }
+                        pr[t] = vis ? ex2_approx(v[e + t] * p.scale_log2 - m_use) : 0.0f;
+                        sum += pr[t];
+                    }
+                    pk[e >> 1] = pack_bf16(pr[0], pr[1]);
+                }
+                // 32 keys = 4 chunks of 16 bytes; chunk index within the 64-key block
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int chunk = c * 4 + q;            // 0..15 over 128 keys
+                    const int blk = chunk >> 3, cin = chunk & 7;
+                    unsigned char* dst = sP + blk * kHalf + r * 128 + ((cin ^ (r & 7)) << 4);
+                    *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                }
+            }
+            l = l * alpha + sum;
+            // V rows of keys that no row can see may hold anything (even NaN):
+            // zero them so that 0 * V stays 0 in the MMA.
+            if (key0 + kBN > nkeys) {
+                if (!mbar_wait(&bar_kv_full[st], (jj >> 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                if (key0 + r >= nkeys) {
+                    unsigned char* sV = smem + kSmemKV + st * 2 * kTile + kTile;
+                    uint4* z0 = reinterpret_cast<uint4*>(sV + r * 128);
+                    uint4* z1 = reinterpret_cast<uint4*>(sV + kHalf + r * 128);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        z0[q] = make_uint4(0, 0, 0, 0);
+                        z1[q] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bar_p_full);
+            if (!mbar_wait(&bar_o_full, jj & 1)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float v[32];
+                tmem_ld32(tmem_o + lane_off + c * 32, v);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) acc[c * 32 + e] = acc[c * 32 + e] * alpha + v[e];
+            }
+            tc_fence_before();
+            mbar_arrive(&bar_s_free);
+            m = m_new;
+        }
+        if (!ok) {
+            raise_status(p.status, kDevTimeout);
+        }
+        // ------------------------------------------------------- epilogue ---
+        const bool row_live = grow < p.G * p.T;
+        __nv_bfloat16* orow =
+            p.out + ((static_cast<size_t>(b) * p.T + i) * p.Hq + static_cast<size_t>(hk) * p.G + g) * kHD;
+        if (nsplit_b == 1) {
+            if (row_live) {
+                const bool live = i < n && l > 0.0f;  // rows of unused slots are written as zeros
+                const float inv = live ? 1.0f / l : 0.0f;
+#pragma unroll
+                for (int c = 0; c < kHD; c += 8) {
+                    uint4 u = make_uint4(0u, 0u, 0u, 0u);
+                    if (live)
+                        u = make_uint4(pack_bf16(acc[c] * inv, acc[c + 1] * inv),
+                                       pack_bf16(acc[c + 2] * inv, acc[c + 3] * inv),
+                                       pack_bf16(acc[c + 4] * inv, acc[c + 5] * inv),
+                                       pack_bf16(acc[c + 6] * inv, acc[c + 7] * inv));
+                    *reinterpret_cast<uint4*>(orow + c) = u;
+                }
+            }
+        } else {
+            const size_t slot = static_cast<size_t>(unit) * p.nsplit + split;
+            float* po = p.part_o + (slot * kBM + r) * kHD;
+#pragma unroll
+            for (int c = 0; c < kHD; c += 4)
+                *reinterpret_cast<float4*>(po + c) = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+            p.part_ml[(slot * kBM + r) * 2] = m;
+            p.part_ml[(slot * kBM + r) * 2 + 1] = l;
+            __threadfence();
+            named_sync_softmax();
+            if (r == 0) {
+                const int prev = atomicAdd(&p.tickets[unit], 1);
+                sh_last = prev == nsplit_b - 1;
+            }
+            named_sync_softmax();
+            if (sh_last) {
+                __threadfence();
+                if (row_live) {
+                    float M = -INFINITY;
+                    for (int s = 0; s < nsplit_b; ++s) {
+                        const size_t sl = static_cast<size_t>(unit) * p.nsplit + s;
+                        M = fmaxf(M, __ldcg(&p.part_ml[(sl * kBM + r) * 2]));
+                    }
+                    const float Mu = M == -INFINITY ? 0.0f : M;
+                    float Ls = 0.0f;
+                    float o[kHD];
+#pragma unroll
+                    for (int e = 0; e < kHD; ++e) o[e] = 0.0f;
+                    for (int s = 0; s < nsplit_b; ++s) {
+                        const size_t sl = static_cast<size_t>(unit) * p.nsplit + s;
+                        const float ms = __ldcg(&p.part_ml[(sl * kBM + r) * 2]);
+                        const float w = ex2_approx(ms - Mu);
+                        Ls += __ldcg(&p.part_ml[(sl * kBM + r) * 2 + 1]) * w;
+                        const float* ps = p.part_o + (sl * kBM + r) * kHD;
+#pragma unroll
+                        for (int e = 0; e < kHD; e += 4) {
+                            const float4 v = __ldcg(reinterpret_cast<const float4*>(ps + e));
+                            o[e] += v.x * w;
+                            o[e + 1] += v.y * w;
+                            o[e + 2] += v.z * w;
+                            o[e + 3] += v.w * w;
+                        }
+                    }
+                    const bool live = i < n && Ls > 0.0f;
+                    const float inv = live ? 1.0f / Ls : 0.0f;
+#pragma unroll
+                    for (int c = 0; c < kHD; c += 8) {
+                        uint4 u = make_uint4(0u, 0u, 0u, 0u);
+                        if (live)
+                            u = make_uint4(pack_bf16(o[c] * inv, o[c + 1] * inv),
+                                           pack_bf16(o[c + 2] * inv, o[c + 3] * inv),
+                                           pack_bf16(o[c + 4] * inv, o[c + 5] * inv),
+                                           pack_bf16(o[c + 6] * inv, o[c + 7] * inv));
+                        *reinterpret_cast<uint4*>(orow + c) = u;
+                    }
+                }
+                if (r == 0) p.tickets[unit] = 0;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+}
+
+// ------------------------------------------------------------- host side ---
+
+struct Plan {
+    int G, n_rb, nsplit, tps, units;
+    size_t off_tickets, off_ml, off_o, bytes;
+};
+
+Plan make_plan(const KvDims& kv, int T) {
+    Plan pl{};
+    pl.G = kv.Hq / kv.Hkv;
+    const int rows = pl.G * T;
+    pl.n_rb = (rows + kBM - 1) / kBM;
+    pl.units = kv.B * kv.Hkv * pl.n_rb;
+    const int max_tiles = (kv.max_len + kBN - 1) / kBN;
+    int want = (8 * 152 + pl.units - 1) / pl.units;  // aim at ~8 waves of CTAs
+    int cap = max_tiles / 2 > 0 ? max_tiles / 2 : 1;  // at least two tiles per split
+    int nsplit = want < 1 ? 1 : (want > cap ? cap : want);
+    pl.tps = (max_tiles + nsplit - 1) / nsplit;
+    pl.nsplit = (max_tiles + pl.tps - 1) / pl.tps;
+    pl.off_tickets = 256;
+    pl.off_ml = align_up(pl.off_tickets + static_cast<size_t>(pl.units) * sizeof(int), 256);
+    const size_t slots = pl.nsplit > 1 ? static_cast<size_t>(pl.units) * pl.nsplit : 0;
+    pl.off_o = align_up(pl.off_ml + slots * kBM * 2 * sizeof(float), 256);
+    pl.bytes = align_up(pl.off_o + slots * kBM * kHD * sizeof(float), 256);
+    return pl;
+}
+
+bool tc_supported(const KvDims& kv, int T) {
+    const int G = kv.Hq / kv.Hkv;
+    return kv.dtype == 1 && kv.d == kHD && G >= 1 && G <= kBM && (kBM % G) == 0 && T <= kMaxSlots &&
+           (kv.pos_stride * 2) % 16 == 0 && (kv.seq_stride * 2) % 16 == 0 && (kv.layer_stride * 2) % 16 == 0 &&
+           (kv.kv_stride * 2) % 16 == 0;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, const cuuint64_t dims[4], const cuuint64_t strides_bytes[3],
+              const cuuint32_t box[4]) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint32_t estride[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides_bytes, box, estride,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+size_t attention_ws_bytes(const KvDims& kv, int T) {
+    if (!tc_supported(kv, T)) return 256;
+    return make_plan(kv, T).bytes;
+}
 
 cudaError_t launch_attention(const KvDims& kv, int T, const void* q, const void* cache, int layer,
                              const int32_t* prefix_len, const uint32_t* mask, const int32_t* n_tree, void* out,
-                             void* /*ws*/, size_t /*ws_bytes*/, int* status, cudaStream_t stream) {
-    return launch_attention_simt(kv, T, q, cache, layer, prefix_len, mask, n_tree, out, status, stream);
+                             void* ws, size_t ws_bytes, int* status, cudaStream_t stream) {
+    if (!tc_supported(kv, T))
+        return launch_attention_simt(kv, T, q, cache, layer, prefix_len, mask, n_tree, out, status, stream);
+    const Plan pl = make_plan(kv, T);
+    if (ws_bytes < pl.bytes) return cudaErrorInvalidValue;
+    char* w = static_cast<char*>(ws);
+    const char* kbase = static_cast<const char*>(cache) + static_cast<int64_t>(layer) * kv.layer_stride * 2;
+    const char* vbase = kbase + kv.kv_stride * 2;
+    CUtensorMap tq, tk, tv;
+    {
+        const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHD), static_cast<cuuint64_t>(kv.Hq),
+                                    static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(kv.B)};
+        const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kHD) * 2, static_cast<cuuint64_t>(kv.Hq) * kHD * 2,
+                                       static_cast<cuuint64_t>(T) * kv.Hq * kHD * 2};
+        const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(pl.G), static_cast<cuuint32_t>(kBM / pl.G), 1};
+        if (!make_map(&tq, q, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHD), static_cast<cuuint64_t>(kv.Hkv),
+                                    static_cast<cuuint64_t>(kv.max_len), static_cast<cuuint64_t>(kv.B)};
+        const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kHD) * 2, static_cast<cuuint64_t>(kv.pos_stride) * 2,
+                                       static_cast<cuuint64_t>(kv.seq_stride) * 2};
+        const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kBN), 1};
+        if (!make_map(&tk, kbase, dims, strides, box)) return cudaErrorInvalidValue;
+        if (!make_map(&tv, vbase, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    TcParams prm{};
+    prm.B = kv.B;
+    prm.T = T;
+    prm.Hq = kv.Hq;
+    prm.Hkv = kv.Hkv;
+    prm.G = pl.G;
+    prm.n_rb = pl.n_rb;
+    prm.nsplit = pl.nsplit;
+    prm.tps = pl.tps;
+    prm.max_len = kv.max_len;
+    prm.W = (T + 31) / 32;
+    prm.prefix_len = prefix_len;
+    prm.mask = mask;
+    prm.n_tree = n_tree;
+    prm.out = static_cast<__nv_bfloat16*>(out);
+    prm.tickets = reinterpret_cast<int*>(w + pl.off_tickets);
+    prm.part_ml = reinterpret_cast<float*>(w + pl.off_ml);
+    prm.part_o = reinterpret_cast<float*>(w + pl.off_o);
+    prm.status = status;
+    prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kHD)));
+    if (pl.nsplit > 1) {
+        cudaError_t e = cudaMemsetAsync(prm.tickets, 0, static_cast<size_t>(pl.units) * sizeof(int), stream);
+        if (e != cudaSuccess) return e;
+    }
+    cudaError_t ae = ensure_dyn_smem(reinterpret_cast<const void*>(attn_tc_kernel), kSmemBytes + 1024);
+    if (ae != cudaSuccess) return ae;
+    dim3 grid(pl.n_rb, pl.nsplit, kv.B * kv.Hkv);
+    count_launch();
+    attn_tc_kernel<<<grid, kThreads, kSmemBytes + 1024, stream>>>(tq, tk, tv, prm);
+    return cudaGetLastError();
 }
 
 }  // namespace eagle

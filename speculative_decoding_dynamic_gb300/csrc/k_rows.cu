@@ -665,7 +665,7 @@ RowSplit choose_row_split(int V, int esize) {
 // Raise a kernel's dynamic shared memory limit only when a launch needs more
 // than was set before, so that launches inside a CUDA graph capture (after a
 // first call outside it) make no attribute calls.
-static cudaError_t ensure_dyn_smem(const void* kernel, int smem) {
+cudaError_t ensure_dyn_smem(const void* kernel, int smem) {
     static std::mutex mu;
     static std::map<std::pair<const void*, int>, int> done;
     int dev = 0;
