@@ -418,14 +418,21 @@ def main():
 
     # ---- per-kernel timing: each stage call alone, same launch configuration ----
     def time_call(fn, reps):
+        """Average device time of one stage call: `reps` calls on rotating inputs
+        captured in a CUDA graph, replayed once untimed and once timed."""
         for i in range(3):
             fn(i % R)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for i in range(reps):
+                fn(i % R)
+        g.replay()
         torch.cuda.synchronize()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for i in range(reps):
-            fn(i % R)
+        g.replay()
         b.record(stream)
         torch.cuda.synchronize()
         return a.elapsed_time(b) / reps

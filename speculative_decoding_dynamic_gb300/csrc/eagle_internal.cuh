@@ -46,6 +46,12 @@ __device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m) {
     hi = __shfl_xor_sync(0xffffffffu, hi, m);
     return (static_cast<uint64_t>(hi) << 32) | lo;
 }
+__device__ __forceinline__ uint64_t shfl_u64(uint64_t v, int src) {
+    uint32_t lo = static_cast<uint32_t>(v), hi = static_cast<uint32_t>(v >> 32);
+    lo = __shfl_sync(0xffffffffu, lo, src);
+    hi = __shfl_sync(0xffffffffu, hi, src);
+    return (static_cast<uint64_t>(hi) << 32) | lo;
+}
 __device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
 #pragma unroll
     for (int m = 16; m > 0; m >>= 1) {

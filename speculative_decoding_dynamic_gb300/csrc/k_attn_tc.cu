@@ -8,10 +8,14 @@
 //   S = Q K^T        tcgen05.mma kind::f16, bf16 operands from shared memory,
 //                    fp32 accumulator in tensor memory (TMEM columns 0..127)
 //   P = softmax part one thread per row (TMEM lane = row): scale, tree mask,
-//                    running max in the log2 domain, P written as bf16 to
-//                    shared memory in the 128B-swizzled K-major layout
-//   O_tile = P V     tcgen05.mma into TMEM columns 128..255, V read MN-major
-//   O += ...         rescaled accumulation in registers
+//                    exponentials in the log2 domain against a reference
+//                    maximum, P written as bf16 to shared memory in the
+//                    128B-swizzled K-major layout
+//   O += P V         tcgen05.mma accumulating in TMEM columns 128..255, V read
+//                    MN-major; the reference maximum is raised (O and the row
+//                    sum rescaled in place) only when a tile's maximum exceeds
+//                    it by more than 2^8, so exponentials stay below 256
+// PV of tile j and QK^T of tile j+1 are issued back to back.
 // K/V tiles arrive by TMA (cp.async.bulk.tensor, 128B swizzle) into a
 // two-stage ring; Q once per CTA. Warp 0 issues TMA, one thread of warp 1
 // issues the MMAs, warps 2..5 do the softmax; mbarriers order them, every
@@ -111,20 +115,39 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 32 consecutive fp32 columns of this thread's TMEM lane.
+// 32 / 64 consecutive fp32 columns of this thread's TMEM lane; the load and
+// its completion wait are one asm statement so no use can move above the wait.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
     uint32_t r[32];
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
+    uint32_t r[64];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
+        "tcgen05.wait::st.sync.aligned;"
+        :
+        : "r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])), "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])), "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])), "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -142,8 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t bar_q, bar_kv_full[kStages], bar_kv_empty[kStages], bar_s_full, bar_p_full, bar_o_full,
-        bar_s_free;
+    __shared__ uint64_t bar_q, bar_kv_full[kStages], bar_kv_empty[kStages], bar_s_full, bar_p_full, bar_o_full;
     __shared__ uint32_t tmem_holder;
     __shared__ uint32_t mask_sm[kBM][kMaxW];
     __shared__ int sh_last;
@@ -172,7 +194,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bar_s_full, 1);
         mbar_init(&bar_p_full, 128);
         mbar_init(&bar_o_full, 1);
-        mbar_init(&bar_s_free, 128);
         fence_mbar_init();
 
         if (bad) raise_status(p.status, kDevBadIndex);
@@ -222,54 +243,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ---------------------------------------------------- MMA issuer ---
+        // Per tile j: once the softmax has written P(j-1) (so S is free),
+        // QK(j) is issued into S and committed, then PV(j-1) accumulates into O.
         if (lane == 0 && n_local > 0) {
             constexpr uint32_t id_qk = idesc_bf16(kBM, kBN, 0);
             constexpr uint32_t id_pv = idesc_bf16(kBM, kHD, 1);
+            const uint32_t aQ = smem_u32(sQ);
+            const uint32_t aP = smem_u32(sP);
             bool ok = mbar_wait(&bar_q, 0);
+            auto issue_pv = [&](int jp) {
+                const int sp = jp & 1;
+                const uint32_t aV = smem_u32(smem + kSmemKV + sp * 2 * kTile + kTile);
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk) {
+                    const uint32_t offp = (kk >> 2) * kHalf + (kk & 3) * 32;
+                    mma_bf16(tmem_o, smem_desc(aP + offp, 16, 1024), smem_desc(aV + kk * 2048, kHalf, 1024), id_pv,
+                             (jp > 0 || kk > 0) ? 1 : 0);
+                }
+                mma_commit(&bar_kv_empty[sp]);
+                mma_commit(&bar_o_full);
+            };
             for (int jj = 0; ok && jj < n_local; ++jj) {
                 const int st = jj & 1;
                 ok = mbar_wait(&bar_kv_full[st], (jj >> 1) & 1);
-                if (ok && jj > 0) ok = mbar_wait(&bar_s_free, (jj - 1) & 1);
+                if (ok && jj > 0) ok = mbar_wait(&bar_p_full, (jj - 1) & 1);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t aK = smem_u32(smem + kSmemKV + st * 2 * kTile);
-                const uint32_t aV = aK + kTile;
-                const uint32_t aQ = smem_u32(sQ);
 #pragma unroll
                 for (int kk = 0; kk < kHD / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
                     mma_bf16(tmem_s, smem_desc(aQ + off, 16, 1024), smem_desc(aK + off, 16, 1024), id_qk, kk > 0);
                 }
-                mma_commit(&bar_s_full);
-                ok = mbar_wait(&bar_p_full, jj & 1);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t aP = smem_u32(sP);
-#pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    const uint32_t offp = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    mma_bf16(tmem_o, smem_desc(aP + offp, 16, 1024), smem_desc(aV + kk * 2048, kHalf, 1024), id_pv,
-                             kk > 0);
-                }
-                mma_commit(&bar_o_full);
-                mma_commit(&bar_kv_empty[st]);
+                mma_commit(&bar_s_full);  // S(j) ready does not wait for PV(j-1)
+                if (jj > 0) issue_pv(jj - 1);
             }
-            if (!ok) {
+            if (ok) ok = mbar_wait(&bar_p_full, (n_local - 1) & 1);
+            if (ok) {
+                tc_fence_after();
+                issue_pv(n_local - 1);
+            } else {
                 raise_status(p.status, kDevTimeout);
             }
         }
     } else {
         // ------------------------------------------------------ softmax ---
+        // One thread per query row (TMEM lane). O accumulates in TMEM; the
+        // exponentials use a reference maximum m_use that is raised (and O, l
+        // rescaled) only when a tile's maximum exceeds it by more than 2^8.
         const int q4 = warp & 3;
         const int r = (q4 << 5) | lane;                  // row of the block = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
         const int grow = rb * kBM + r;                   // row within the (b, hk) problem
         const int i = i0 + r / p.G;                      // tree slot of the row
         const int g = r % p.G;
-        float acc[kHD];
-#pragma unroll
-        for (int e = 0; e < kHD; ++e) acc[e] = 0.0f;
-        float m = -INFINITY, l = 0.0f;
+        float m_use = 0.0f, l = 0.0f;
+        bool seen = false;
         bool ok = true;
         for (int jj = 0; jj < n_local; ++jj) {
             const int st = jj & 1;
@@ -279,60 +308,88 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            const bool prefix_only = key0 + kBN <= L;
-            // pass 1: row maximum over the visible keys of this tile
+            float sv[kBN];
+            tmem_ld64(tmem_s + lane_off, sv);
+            tmem_ld64(tmem_s + lane_off + 64, sv + 64);
+            // visibility of the tile's keys: prefix keys, then tree slots in mask row i
+            uint32_t vis[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int kb = key0 + 32 * c;  // first key of this group of 32
+                uint32_t pre = 0u;
+                const int npre = L - kb;       // keys of the group inside the prefix
+                if (npre >= 32) pre = 0xffffffffu;
+                else if (npre > 0) pre = (1u << npre) - 1u;
+                uint32_t tree = 0u;
+                if (npre < 32) {
+                    const int j0 = kb - L;     // slot of the group's first key (may be negative)
+                    const int lo = j0 < 0 ? 0 : j0;
+                    const int w0 = lo >> 5, sh = lo & 31;
+                    uint32_t win = mask_sm[r][w0 & (kMaxW - 1)] >> sh;
+                    if (sh && w0 + 1 < kMaxW) win |= mask_sm[r][w0 + 1] << (32 - sh);
+                    if (w0 >= kMaxW) win = 0u;
+                    const int limit = n - lo;  // slots j >= n are never visible
+                    if (limit <= 0) win = 0u;
+                    else if (limit < 32) win &= (1u << limit) - 1u;
+                    tree = j0 < 0 ? (win << (-j0)) : win;
+                    if (j0 <= -32) tree = 0u;
+                }
+                vis[c] = pre | tree;
+            }
             float mx = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float v[32];
-                tmem_ld32(tmem_s + lane_off + c * 32, v);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int key = key0 + c * 32 + e;
-                    bool vis = true;
-                    if (!prefix_only) {
-                        const int j = key - L;
-                        vis = key < L || (j < n && ((mask_sm[r][j >> 5] >> (j & 31)) & 1u));
-                    }
-                    if (vis) mx = fmaxf(mx, v[e] * p.scale_log2);
+            for (int e = 0; e < kBN; ++e) {
+                sv[e] *= p.scale_log2;
+                if ((vis[e >> 5] >> (e & 31)) & 1u) mx = fmaxf(mx, sv[e]);
+            }
+            bool rescale = false;
+            float alpha = 1.0f;
+            if (mx > -INFINITY) {
+                if (!seen) {
+                    m_use = mx;  // O and l are still zero
+                    seen = true;
+                } else if (mx > m_use + 8.0f) {
+                    alpha = ex2_approx(m_use - mx);
+                    m_use = mx;
+                    rescale = true;
+                    l *= alpha;
                 }
             }
-            const float m_new = fmaxf(m, mx);
-            const float m_use = m_new == -INFINITY ? 0.0f : m_new;
-            const float alpha = ex2_approx(m - m_use);
-            // pass 2: probabilities -> bf16 P (swizzled K-major), row sum
             float sum = 0.0f;
+            uint32_t pk[kBN / 2];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float v[32];
-                tmem_ld32(tmem_s + lane_off + c * 32, v);
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float pr[2];
-#pragma unroll
-                    for (int t = 0; t < 2; ++t) {
-                        const int key = key0 + c * 32 + e + t;
-                        bool vis = true;
-                        if (!prefix_only) {
-                            const int j = key - L;
-                            vis = key < L || (j < n && ((mask_sm[r][j >> 5] >> (j & 31)) & 1u));
-                        }
-                        pr[t] = vis ? ex2_approx(v[e + t] * p.scale_log2 - m_use) : 0.0f;
-                        sum += pr[t];
-                    }
-                    pk[e >> 1] = pack_bf16(pr[0], pr[1]);
+            for (int e = 0; e < kBN; e += 2) {
+                const float p0 = ((vis[e >> 5] >> (e & 31)) & 1u) ? ex2_approx(sv[e] - m_use) : 0.0f;
+                const float p1 = ((vis[(e + 1) >> 5] >> ((e + 1) & 31)) & 1u) ? ex2_approx(sv[e + 1] - m_use) : 0.0f;
+                sum += p0 + p1;
+                pk[e >> 1] = pack_bf16(p0, p1);
+            }
+            l += sum;
+            if (jj > 0) {  // PV(j-1) done: P buffer free, O stable
+                if (!mbar_wait(&bar_o_full, (jj - 1) & 1)) {
+                    ok = false;
+                    break;
                 }
-                // 32 keys = 4 chunks of 16 bytes; chunk index within the 64-key block
+                tc_fence_after();
+                // tcgen05.ld/st are warp-collective: rescale if any row of the warp needs it
+                // (alpha = 1 for the others).
+                if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        float o[32];
+                        tmem_ld32(tmem_o + lane_off + c * 32, o);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int chunk = c * 4 + q;            // 0..15 over 128 keys
-                    const int blk = chunk >> 3, cin = chunk & 7;
-                    unsigned char* dst = sP + blk * kHalf + r * 128 + ((cin ^ (r & 7)) << 4);
-                    *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                        tmem_st32(tmem_o + lane_off + c * 32, o);
+                    }
                 }
             }
-            l = l * alpha + sum;
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {  // 16 chunks of 8 keys, 128B-swizzled K-major rows
+                const int blk = q >> 3, cin = q & 7;
+                unsigned char* dst = sP + blk * kHalf + r * 128 + ((cin ^ (r & 7)) << 4);
+                *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            }
             // V rows of keys that no row can see may hold anything (even NaN):
             // zero them so that 0 * V stays 0 in the MMA.
             if (key0 + kBN > nkeys) {
@@ -354,51 +411,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&bar_p_full);
-            if (!mbar_wait(&bar_o_full, jj & 1)) {
-                ok = false;
-                break;
-            }
+        }
+        if (ok && n_local > 0) {
+            ok = mbar_wait(&bar_o_full, (n_local - 1) & 1);
             tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float v[32];
-                tmem_ld32(tmem_o + lane_off + c * 32, v);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) acc[c * 32 + e] = acc[c * 32 + e] * alpha + v[e];
-            }
-            tc_fence_before();
-            mbar_arrive(&bar_s_free);
-            m = m_new;
         }
-        if (!ok) {
-            raise_status(p.status, kDevTimeout);
-        }
+        if (!ok) raise_status(p.status, kDevTimeout);
         // ------------------------------------------------------- epilogue ---
         const bool row_live = grow < p.G * p.T;
         __nv_bfloat16* orow =
             p.out + ((static_cast<size_t>(b) * p.T + i) * p.Hq + static_cast<size_t>(hk) * p.G + g) * kHD;
         if (nsplit_b == 1) {
-            if (row_live) {
-                const bool live = i < n && l > 0.0f;  // rows of unused slots are written as zeros
-                const float inv = live ? 1.0f / l : 0.0f;
+            const bool live = row_live && i < n && l > 0.0f && ok;  // rows of unused slots are zeros
+            const float inv = live ? 1.0f / l : 0.0f;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                float o[32];
+                if (n_local > 0) tmem_ld32(tmem_o + lane_off + c * 32, o);
+                if (row_live) {
 #pragma unroll
-                for (int c = 0; c < kHD; c += 8) {
-                    uint4 u = make_uint4(0u, 0u, 0u, 0u);
-                    if (live)
-                        u = make_uint4(pack_bf16(acc[c] * inv, acc[c + 1] * inv),
-                                       pack_bf16(acc[c + 2] * inv, acc[c + 3] * inv),
-                                       pack_bf16(acc[c + 4] * inv, acc[c + 5] * inv),
-                                       pack_bf16(acc[c + 6] * inv, acc[c + 7] * inv));
-                    *reinterpret_cast<uint4*>(orow + c) = u;
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 u = make_uint4(0u, 0u, 0u, 0u);
+                        if (live)
+                            u = make_uint4(pack_bf16(o[8 * q] * inv, o[8 * q + 1] * inv),
+                                           pack_bf16(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
+                                           pack_bf16(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
+                                           pack_bf16(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
+                        *reinterpret_cast<uint4*>(orow + c * 32 + 8 * q) = u;
+                    }
                 }
             }
         } else {
             const size_t slot = static_cast<size_t>(unit) * p.nsplit + split;
             float* po = p.part_o + (slot * kBM + r) * kHD;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                float o[32];
+                tmem_ld32(tmem_o + lane_off + c * 32, o);
 #pragma unroll
-            for (int c = 0; c < kHD; c += 4)
-                *reinterpret_cast<float4*>(po + c) = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
-            p.part_ml[(slot * kBM + r) * 2] = m;
+                for (int q = 0; q < 8; ++q)
+                    *reinterpret_cast<float4*>(po + c * 32 + 4 * q) =
+                        make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+            }
+            p.part_ml[(slot * kBM + r) * 2] = (seen && l > 0.0f) ? m_use : -INFINITY;
             p.part_ml[(slot * kBM + r) * 2 + 1] = l;
             __threadfence();
             named_sync_softmax();
@@ -410,42 +465,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (sh_last) {
                 __threadfence();
                 if (row_live) {
+                    const size_t s0 = static_cast<size_t>(unit) * p.nsplit;
                     float M = -INFINITY;
-                    for (int s = 0; s < nsplit_b; ++s) {
-                        const size_t sl = static_cast<size_t>(unit) * p.nsplit + s;
-                        M = fmaxf(M, __ldcg(&p.part_ml[(sl * kBM + r) * 2]));
-                    }
-                    const float Mu = M == -INFINITY ? 0.0f : M;
+                    for (int s = 0; s < nsplit_b; ++s) M = fmaxf(M, __ldcg(&p.part_ml[((s0 + s) * kBM + r) * 2]));
                     float Ls = 0.0f;
-                    float o[kHD];
-#pragma unroll
-                    for (int e = 0; e < kHD; ++e) o[e] = 0.0f;
                     for (int s = 0; s < nsplit_b; ++s) {
-                        const size_t sl = static_cast<size_t>(unit) * p.nsplit + s;
-                        const float ms = __ldcg(&p.part_ml[(sl * kBM + r) * 2]);
-                        const float w = ex2_approx(ms - Mu);
-                        Ls += __ldcg(&p.part_ml[(sl * kBM + r) * 2 + 1]) * w;
-                        const float* ps = p.part_o + (sl * kBM + r) * kHD;
-#pragma unroll
-                        for (int e = 0; e < kHD; e += 4) {
-                            const float4 v = __ldcg(reinterpret_cast<const float4*>(ps + e));
-                            o[e] += v.x * w;
-                            o[e + 1] += v.y * w;
-                            o[e + 2] += v.z * w;
-                            o[e + 3] += v.w * w;
-                        }
+                        const float ms = __ldcg(&p.part_ml[((s0 + s) * kBM + r) * 2]);
+                        if (ms > -INFINITY) Ls += __ldcg(&p.part_ml[((s0 + s) * kBM + r) * 2 + 1]) * ex2_approx(ms - M);
                     }
                     const bool live = i < n && Ls > 0.0f;
                     const float inv = live ? 1.0f / Ls : 0.0f;
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        float o[32];
 #pragma unroll
-                    for (int c = 0; c < kHD; c += 8) {
-                        uint4 u = make_uint4(0u, 0u, 0u, 0u);
-                        if (live)
-                            u = make_uint4(pack_bf16(o[c] * inv, o[c + 1] * inv),
-                                           pack_bf16(o[c + 2] * inv, o[c + 3] * inv),
-                                           pack_bf16(o[c + 4] * inv, o[c + 5] * inv),
-                                           pack_bf16(o[c + 6] * inv, o[c + 7] * inv));
-                        *reinterpret_cast<uint4*>(orow + c) = u;
+                        for (int e = 0; e < 32; ++e) o[e] = 0.0f;
+                        for (int s = 0; s < nsplit_b; ++s) {
+                            const float ms = __ldcg(&p.part_ml[((s0 + s) * kBM + r) * 2]);
+                            if (!(ms > -INFINITY)) continue;
+                            const float w = ex2_approx(ms - M) * inv;
+                            const float* ps = p.part_o + ((s0 + s) * kBM + r) * kHD + c * 32;
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                const float4 v = __ldcg(reinterpret_cast<const float4*>(ps + 4 * q));
+                                o[4 * q] += v.x * w;
+                                o[4 * q + 1] += v.y * w;
+                                o[4 * q + 2] += v.z * w;
+                                o[4 * q + 3] += v.w * w;
+                            }
+                        }
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint4 u = make_uint4(0u, 0u, 0u, 0u);
+                            if (live)
+                                u = make_uint4(pack_bf16(o[8 * q], o[8 * q + 1]), pack_bf16(o[8 * q + 2], o[8 * q + 3]),
+                                               pack_bf16(o[8 * q + 4], o[8 * q + 5]),
+                                               pack_bf16(o[8 * q + 6], o[8 * q + 7]));
+                            *reinterpret_cast<uint4*>(orow + c * 32 + 8 * q) = u;
+                        }
                     }
                 }
                 if (r == 0) p.tickets[unit] = 0;

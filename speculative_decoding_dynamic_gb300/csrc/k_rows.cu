@@ -7,11 +7,18 @@
 // Layout of the work: one logit row is split over a thread-block cluster of
 // `cpr` CTAs. Each CTA stages its contiguous chunk of the row in shared memory
 // with one bulk asynchronous copy (TMA engine, completion on an mbarrier), so
-// HBM is read exactly once and the reductions re-read shared memory. Partial
-// results are merged through distributed shared memory inside the cluster.
-// The per-sequence tail (frontier selection / acceptance walk) runs in the
-// cluster leader that arrives last on a per-sequence ticket: an atomic add
-// after a device-scope fence, no spin-wait anywhere.
+// HBM is read exactly once; each warp then owns a contiguous part of the
+// chunk and reduces it without block-wide barriers. Partial results are
+// pushed into the cluster leader's shared memory with remote stores before a
+// single cluster barrier. The per-sequence tail (frontier selection /
+// acceptance walk) runs in the cluster leader that arrives last on a
+// per-sequence ticket: an atomic add after a device-scope fence, no spin-wait.
+//
+// Top-k of a warp's part: with key = (value, -id) unique per element, let tau
+// be the k-th largest of the 32 lane maxima. The k lane maxima >= tau are k
+// distinct elements, so every element of the part's top-k has key >= tau; the
+// few elements >= tau are gathered and sorted. The union of the warps' top-k
+// contains the chunk's top-k, and so on up the cluster.
 //
 // Sources (page title and section): "EAGLE" notes (garden.houmin.site),
 // EAGLE 方法 (TopK drafting) and EAGLE 2 方法 (Expand, threshold);
@@ -21,6 +28,7 @@
 
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <map>
@@ -34,18 +42,16 @@ namespace eagle {
 
 constexpr int kRowThreads = 256;
 constexpr int kRowWarps = kRowThreads / 32;
-constexpr int kCandCap = 128;
+constexpr int kWarpCand = 64;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// ------------------------------------------------------------ row staging ---
+// ------------------------------------------------------------ helpers ---
 
 struct RowChunk {
-    int c0;   // first token id of this CTA's chunk
-    int n;    // tokens in the chunk (may be 0)
-    int epv;  // elements per 16-byte vector (8 bf16 / 4 fp32)
+    int c0;  // first token id of this CTA's chunk
+    int n;   // tokens in the chunk (may be 0)
 };
 
-// Element e of 16-byte vector v of the staged chunk, widened to fp32.
 template <int DT>
 __device__ __forceinline__ void unpack16(const uint4& u, float* x) {
     if (DT == 1) {
@@ -64,7 +70,6 @@ __device__ __forceinline__ void unpack16(const uint4& u, float* x) {
 }
 
 // Issue the bulk copy of this CTA's chunk into `buf` and wait for it.
-// Returns false if the bounded wait gave up (status already raised).
 __device__ __forceinline__ bool stage_chunk(void* buf, const char* row_base, const RowChunk& ch, int esize,
                                             uint64_t* bar, int* status) {
     const uint32_t bytes = static_cast<uint32_t>(ch.n) * esize;
@@ -85,41 +90,80 @@ __device__ __forceinline__ bool stage_chunk(void* buf, const char* row_base, con
     return true;
 }
 
-// Thread-local maximum (lowest id among equal values) of the staged chunk.
-template <int DT>
-__device__ __forceinline__ void chunk_thread_max(const uint4* buf, const RowChunk& ch, float* tmax, int* targ) {
-    constexpr int EPV = DT == 1 ? 8 : 4;
-    const int nvec = ch.n / EPV;
-    float m = -INFINITY;
-    int a = -1;
-    for (int v = threadIdx.x; v < nvec; v += kRowThreads) {
-        float x[EPV];
-        unpack16<DT>(buf[v], x);
+// Descending bitonic sort of 32*E keys held by one warp, E per lane
+// (element e = lane*E + j).
+template <int E>
+__device__ __forceinline__ void warp_sort_desc(uint64_t (&v)[E]) {
+    const int lane = threadIdx.x & 31;
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-            if (a < 0 || x[e] > m) {
-                m = x[e];
-                a = ch.c0 + v * EPV + e;
+    for (int size = 2; size <= 32 * E; size <<= 1) {
+#pragma unroll
+        for (int s = size >> 1; s > 0; s >>= 1) {
+            if (s < E) {
+#pragma unroll
+                for (int j = 0; j < E; ++j) {
+                    const int pj = j ^ s;
+                    if (pj > j) {
+                        const int e = lane * E + j;
+                        const bool desc = (e & size) == 0;
+                        const uint64_t a = v[j], c = v[pj];
+                        if ((a < c) == desc) {
+                            v[j] = c;
+                            v[pj] = a;
+                        }
+                    }
+                }
+            } else {
+                const int ls = s / E;
+#pragma unroll
+                for (int j = 0; j < E; ++j) {
+                    const uint64_t o = shfl_xor_u64(v[j], ls);
+                    const int e = lane * E + j;
+                    const bool desc = (e & size) == 0;
+                    const bool lower = (e & s) == 0;
+                    const bool keep_max = lower == desc;
+                    v[j] = keep_max ? (o > v[j] ? o : v[j]) : (o < v[j] ? o : v[j]);
+                }
             }
         }
     }
-    *tmax = m;
-    *targ = a;
+}
+
+// Top-k (k <= 16) of n <= 32*E keys in shared memory by one warp; writes
+// out[0..k), 0 = no key.
+template <int E>
+__device__ __forceinline__ void warp_topk_sorted(const uint64_t* keys, int n, int k, uint64_t* out) {
+    const int lane = threadIdx.x & 31;
+    uint64_t v[E];
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+        const int e = lane * E + j;
+        v[j] = e < n ? keys[e] : 0ull;
+    }
+    warp_sort_desc<E>(v);
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+        const int e = lane * E + j;
+        if (e < k) out[e] = v[j];
+    }
+    __syncwarp();
 }
 
 // ------------------------------------------------------------ expand kernel ---
 
 struct ExpandSmem {
     uint64_t bar;
-    uint64_t tkeys[kRowThreads];
-    uint64_t cand[kCandCap];
-    uint64_t sel[kMaxTopK * kMaxTopK];  // frontier candidates / cluster merge buffer
-    uint64_t cta_top[kMaxTopK];
-    uint64_t top[kMaxTopK];
+    uint64_t wcand[kRowWarps][kWarpCand];
+    int wcount[kRowWarps];
+    uint64_t wtop[kRowWarps * kMaxTopK];
     float wm[kRowWarps];
     float ws[kRowWarps];
-    float cta_m, cta_s;
-    int n_cand;
+    // filled by every CTA of the cluster in the leader's copy (remote stores)
+    uint64_t rtop[kMaxChunks * kMaxTopK];
+    float rm[kMaxChunks];
+    float rs[kMaxChunks];
+    uint64_t top[kMaxTopK];
+    uint64_t sel[kMaxTopK * kMaxTopK];
     int last;
 };
 
@@ -140,6 +184,8 @@ __global__ void __launch_bounds__(kRowThreads) expand_kernel(TreeDims d, TreeWs 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int F = w.fcount[step * d.B + b];
     constexpr int ES = DT == 1 ? 2 : 4;
+    constexpr int EPV = 16 / ES;
+    const int k = d.k;
 
     if (f >= F) {  // this frontier slot holds no node in this step
         if (rank == 0 && tid == 0) {
@@ -155,85 +201,60 @@ __global__ void __launch_bounds__(kRowThreads) expand_kernel(TreeDims d, TreeWs 
     RowChunk ch;
     ch.c0 = rank * chunk;
     ch.n = max(0, min(chunk, d.V - ch.c0));
-    ch.epv = 16 / ES;
     const char* row_base = static_cast<const char*>(logits) + static_cast<size_t>(b * d.k + f) * d.V * ES;
     const uint4* buf = reinterpret_cast<const uint4*>(dyn_smem);
+    if (tid < kRowWarps) sm.wcount[tid] = 0;
     stage_chunk(dyn_smem, row_base, ch, ES, &sm.bar, w.status);
 
-    // Pass 1: thread maximum (value, lowest id) -> thread key.
-    float tmax;
-    int targ;
-    chunk_thread_max<DT>(buf, ch, &tmax, &targ);
-    const uint64_t tkey = targ < 0 ? 0ull : make_key(tmax, static_cast<uint32_t>(targ));
-    sm.tkeys[tid] = tkey;
-
-    // Pass 2: thread sum of exp(x - tmax).
-    constexpr int EPV = DT == 1 ? 8 : 4;
+    // ---- per warp: a contiguous part of the chunk ----
     const int nvec = ch.n / EPV;
-    float ts = 0.0f;
-    if (lse_in == nullptr && targ >= 0 && tmax > -INFINITY) {
-        const float mb = tmax * kLog2e;
-        for (int v = tid; v < nvec; v += kRowThreads) {
-            float x[EPV];
-            unpack16<DT>(buf[v], x);
+    const int vpw = (nvec + kRowWarps - 1) / kRowWarps;
+    const int v0 = warp * vpw, v1 = min(nvec, v0 + vpw);
+    float lmax = -INFINITY;
+    int larg = -1;
+    for (int v = v0 + lane; v < v1; v += 32) {
+        float x[EPV];
+        unpack16<DT>(buf[v], x);
 #pragma unroll
-            for (int e = 0; e < EPV; ++e) ts += ex2_approx(fmaf(x[e], kLog2e, -mb));
-        }
+        for (int e = 0; e < EPV; ++e)
+            if (larg < 0 || x[e] > lmax) {
+                lmax = x[e];
+                larg = ch.c0 + v * EPV + e;
+            }
     }
-    // Block reduction of (max, sum) with rescaling.
-    float wm = (targ >= 0) ? tmax : -INFINITY;
-#pragma unroll
-    for (int m = 16; m > 0; m >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, m));
-    float sc = (targ >= 0 && tmax > -INFINITY) ? ts * ex2_approx((tmax - wm) * kLog2e) : 0.0f;
-#pragma unroll
-    for (int m = 16; m > 0; m >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, m);
-    if (lane == 0) {
-        sm.wm[warp] = wm;
-        sm.ws[warp] = sc;
-    }
-    if (tid == 0) sm.n_cand = 0;
-    __syncthreads();
-
-    // tau = k-th largest thread key: at least k elements have key >= tau.
-    if (warp == 0) {
-        warp_topk_smem(sm.tkeys, kRowThreads, d.k, sm.top);
-        if (lane == 0) {
-            float M = -INFINITY;
-            for (int i = 0; i < kRowWarps; ++i) M = fmaxf(M, sm.wm[i]);
-            float S = 0.0f;
-            if (M > -INFINITY)
-                for (int i = 0; i < kRowWarps; ++i)
-                    if (sm.wm[i] > -INFINITY) S += sm.ws[i] * ex2_approx((sm.wm[i] - M) * kLog2e);
-            sm.cta_m = M;
-            sm.cta_s = S;
-        }
-    }
-    __syncthreads();
-    const uint64_t tau = sm.top[d.k - 1];
-
-    // Pass 3: gather the candidates (key >= tau).
-    for (int v = tid; v < nvec; v += kRowThreads) {
+    uint64_t lk[1] = {larg < 0 ? 0ull : make_key(lmax, static_cast<uint32_t>(larg))};
+    warp_sort_desc<1>(lk);
+    const uint64_t tau = shfl_u64(lk[0], k - 1);  // k-th largest lane maximum (0 if fewer)
+    const uint64_t wtopkey = shfl_u64(lk[0], 0);
+    const float wmax = wtopkey ? key_val(wtopkey) : -INFINITY;
+    float s = 0.0f;
+    const bool do_sum = lse_in == nullptr && wmax > -INFINITY;
+    const float mb = wmax * kLog2e;
+    for (int v = v0 + lane; v < v1; v += 32) {
         float x[EPV];
         unpack16<DT>(buf[v], x);
 #pragma unroll
         for (int e = 0; e < EPV; ++e) {
+            if (do_sum) s += ex2_approx(fmaf(x[e], kLog2e, -mb));
             const uint64_t key = make_key(x[e], static_cast<uint32_t>(ch.c0 + v * EPV + e));
             if (key >= tau) {
-                const int at = atomicAdd(&sm.n_cand, 1);
-                if (at < kCandCap) sm.cand[at] = key;
+                const int at = atomicAdd(&sm.wcount[warp], 1);
+                if (at < kWarpCand) sm.wcand[warp][at] = key;
             }
         }
     }
-    __syncthreads();
-    const int n_cand = sm.n_cand;
-    if (n_cand <= kCandCap) {
-        if (warp == 0) warp_topk_smem(sm.cand, n_cand, d.k, sm.cta_top);
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
+    __syncwarp();
+    const int cnt = sm.wcount[warp];
+    if (cnt <= kWarpCand) {
+        warp_topk_sorted<2>(sm.wcand[warp], cnt, k, &sm.wtop[warp * kMaxTopK]);
     } else {
-        // Many equal values at the top: exact k rounds over the whole chunk.
+        // Many equal values at the top: k exact rounds over the warp's part.
         uint64_t prev = ~0ull;
-        for (int r = 0; r < d.k; ++r) {
+        for (int r = 0; r < k; ++r) {
             uint64_t best = 0;
-            for (int v = tid; v < nvec; v += kRowThreads) {
+            for (int v = v0 + lane; v < v1; v += 32) {
                 float x[EPV];
                 unpack16<DT>(buf[v], x);
 #pragma unroll
@@ -243,45 +264,78 @@ __global__ void __launch_bounds__(kRowThreads) expand_kernel(TreeDims d, TreeWs 
                 }
             }
             best = warp_max_u64(best);
-            if (lane == 0) sm.tkeys[warp] = best;
-            __syncthreads();
-            if (tid == 0) {
-                uint64_t m = 0;
-                for (int i = 0; i < kRowWarps; ++i) m = sm.tkeys[i] > m ? sm.tkeys[i] : m;
-                sm.cta_top[r] = m;
-            }
-            __syncthreads();
-            prev = sm.cta_top[r];
+            if (lane == 0) sm.wtop[warp * kMaxTopK + r] = best;
+            prev = best;
         }
-    }
-
-    // Cluster merge: the leader gathers every CTA's (max, sum, top-k).
-    cluster.sync();
-    if (rank == 0 && warp == 0) {
-        float M = -INFINITY;
-        for (int r = 0; r < cpr; ++r) {
-            const ExpandSmem* rs = cluster.map_shared_rank(&sm, r);
-            M = fmaxf(M, rs->cta_m);
-            for (int j = lane; j < d.k; j += 32) sm.sel[r * d.k + j] = rs->cta_top[j];
-        }
-        float S = 0.0f;
-        if (lane == 0 && M > -INFINITY)
-            for (int r = 0; r < cpr; ++r) {
-                const ExpandSmem* rs = cluster.map_shared_rank(&sm, r);
-                if (rs->cta_m > -INFINITY) S += rs->cta_s * ex2_approx((rs->cta_m - M) * kLog2e);
-            }
         __syncwarp();
-        warp_topk_smem(sm.sel, cpr * d.k, d.k, sm.top);
+    }
+    if (lane == 0) {
+        sm.wm[warp] = wmax;
+        sm.ws[warp] = s;
+    }
+    __syncthreads();
+
+    // ---- CTA: merge the warps, push to the cluster leader ----
+    ExpandSmem* leader = cluster.map_shared_rank(&sm, 0);
+    if (warp == 0) {
+        // the 8 warps' top-k: k <= 16, so 8 * 16 = 128 slots, 4 per lane
+        uint64_t v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int e = lane * 4 + j;  // e = warp_index * 16 + r
+            const int wi = e >> 4, r = e & 15;
+            v[j] = r < k ? sm.wtop[wi * kMaxTopK + r] : 0ull;
+        }
+        warp_sort_desc<4>(v);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int e = lane * 4 + j;
+            if (e < k) leader->rtop[rank * kMaxTopK + e] = v[j];
+        }
         if (lane == 0) {
-            sm.cta_m = M;
-            sm.cta_s = S;
+            float M = -INFINITY;
+            for (int i = 0; i < kRowWarps; ++i) M = fmaxf(M, sm.wm[i]);
+            float S = 0.0f;
+            if (M > -INFINITY)
+                for (int i = 0; i < kRowWarps; ++i)
+                    if (sm.wm[i] > -INFINITY) S += sm.ws[i] * ex2_approx((sm.wm[i] - M) * kLog2e);
+            leader->rm[rank] = M;
+            leader->rs[rank] = S;
         }
     }
-    cluster.sync();  // remote shared memory may be released after this point
+    cluster.sync();
     if (rank != 0) return;
 
+    // ---- leader: row top-k and lse ----
+    if (warp == 0) {
+        uint64_t v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int e = lane * 4 + j;  // e = rank_index * 16 + r
+            const int ri = e >> 4, r = e & 15;
+            v[j] = (ri < cpr && r < k) ? sm.rtop[ri * kMaxTopK + r] : 0ull;
+        }
+        warp_sort_desc<4>(v);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int e = lane * 4 + j;
+            if (e < k) sm.top[e] = v[j];
+        }
+        if (lane == 0) {
+            float M = -INFINITY;
+            for (int r = 0; r < cpr; ++r) M = fmaxf(M, sm.rm[r]);
+            float S = 0.0f;
+            if (M > -INFINITY)
+                for (int r = 0; r < cpr; ++r)
+                    if (sm.rm[r] > -INFINITY) S += sm.rs[r] * ex2_approx((sm.rm[r] - M) * kLog2e);
+            sm.wm[0] = M;
+            sm.ws[0] = S;
+        }
+    }
+    __syncthreads();
+
     // Children of this frontier node.
-    const float lse = lse_in != nullptr ? lse_in[b * d.k + f] : sm.cta_m + logf(sm.cta_s);
+    const float lse = lse_in != nullptr ? lse_in[b * d.k + f] : sm.wm[0] + logf(sm.ws[0]);
     const int parent = w.fnode[(step * d.B + b) * d.k + f];
     const float plogv = parent < 0 ? 0.0f : w.cand_logv[static_cast<size_t>(b) * d.C + parent];
     const int base = step == 0 ? 0 : d.k + (step - 1) * d.k * d.k;
@@ -374,21 +428,22 @@ struct VerifySmem {
     uint64_t bar;
     uint64_t wkey[kRowWarps];
     uint64_t wmass[kRowWarps];
-    uint64_t cta_key;
-    uint64_t cta_mass;
+    uint64_t rkey[kMaxChunks];   // every rank's chunk maximum (pushed to every rank)
+    uint64_t rmass[kMaxChunks];  // every rank's chunk mass (pushed to the leader)
     int last;
     // walk state (last-arriving CTA of a sequence)
     int tok[kMaxSlots];
     int par[kMaxSlots];
     int arg[kMaxSlots];
     float rmax[kMaxSlots];
-    unsigned long long rmass[kMaxSlots];
+    unsigned long long rowmass[kMaxSlots];
     unsigned long long pmass[kMaxSlots];  // mass of slot c's token in its parent's row
+    uint32_t uni[kMaxSlots + 2];
     int path[kMaxDepth + 1];
     int removed_tok[kMaxSlots];
     unsigned long long removed_mass[kMaxSlots];
-    unsigned long long scan[kRowThreads];
-    int n_removed, a, cur, sample_chunk, bonus;
+    unsigned long long wscan[kRowWarps];
+    int n_removed, a, cur, sample_chunk, bonus, bad, found;
     unsigned long long sample_t;
 };
 
@@ -411,7 +466,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
     const int b = row / d.T, t = row % d.T;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int ES = DT == 1 ? 2 : 4;
-    constexpr int EPV = DT == 1 ? 8 : 4;
+    constexpr int EPV = 16 / ES;
     const int n = n_tree[b];
     if (n < 1 || n > d.T) {
         if (rank == 0 && t == 0 && tid == 0) raise_status(w.status, kDevBadIndex);
@@ -422,35 +477,44 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
     RowChunk ch;
     ch.c0 = rank * chunk;
     ch.n = max(0, min(chunk, d.V - ch.c0));
-    ch.epv = EPV;
     const char* row_base = static_cast<const char*>(target) + static_cast<size_t>(b * d.T + t) * d.V * ES;
     const uint4* buf = reinterpret_cast<const uint4*>(dyn_smem);
     stage_chunk(dyn_smem, row_base, ch, ES, &sm.bar, w.status);
 
-    float tmax;
-    int targ;
-    chunk_thread_max<DT>(buf, ch, &tmax, &targ);
-    uint64_t key = targ < 0 ? 0ull : make_key(tmax, static_cast<uint32_t>(targ));
+    // ---- pass 1: maximum (lowest id among equal values) ----
+    const int nvec = ch.n / EPV;
+    const int vpw = (nvec + kRowWarps - 1) / kRowWarps;
+    const int v0 = warp * vpw, v1 = min(nvec, v0 + vpw);
+    float lmax = -INFINITY;
+    int larg = -1;
+    for (int v = v0 + lane; v < v1; v += 32) {
+        float x[EPV];
+        unpack16<DT>(buf[v], x);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e)
+            if (larg < 0 || x[e] > lmax) {
+                lmax = x[e];
+                larg = ch.c0 + v * EPV + e;
+            }
+    }
+    uint64_t key = larg < 0 ? 0ull : make_key(lmax, static_cast<uint32_t>(larg));
     key = warp_max_u64(key);
     if (lane == 0) sm.wkey[warp] = key;
     __syncthreads();
-    if (tid == 0) {
-        uint64_t m = 0;
-        for (int i = 0; i < kRowWarps; ++i) m = sm.wkey[i] > m ? sm.wkey[i] : m;
-        sm.cta_key = m;
+    if (warp == 0) {
+        uint64_t m = lane < kRowWarps ? sm.wkey[lane] : 0ull;
+        m = warp_max_u64(m);
+        if (lane < cpr) cluster.map_shared_rank(&sm, lane)->rkey[rank] = m;  // to every rank
     }
     cluster.sync();
     uint64_t gkey = 0;
-    for (int r = 0; r < cpr; ++r) {
-        const uint64_t k2 = cluster.map_shared_rank(&sm, r)->cta_key;
-        gkey = k2 > gkey ? k2 : gkey;
-    }
+    for (int r = 0; r < cpr; ++r) gkey = sm.rkey[r] > gkey ? sm.rkey[r] : gkey;
     const float M = key_val(gkey);
     const size_t rt = static_cast<size_t>(b) * d.T + t;
     if (mode == 1) {
-        const int nvec = ch.n / EPV;
+        // ---- pass 2: integer mass of the chunk ----
         uint64_t s = 0;
-        for (int v = tid; v < nvec; v += kRowThreads) {
+        for (int v = v0 + lane; v < v1; v += 32) {
             float x[EPV];
             unpack16<DT>(buf[v], x);
 #pragma unroll
@@ -459,18 +523,21 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
         s = warp_sum_u64(s);
         if (lane == 0) sm.wmass[warp] = s;
         __syncthreads();
-        if (tid == 0) {
-            uint64_t tot = 0;
-            for (int i = 0; i < kRowWarps; ++i) tot += sm.wmass[i];
-            w.chunk_mass[rt * kMaxChunks + rank] = tot;
+        if (warp == 0) {
+            uint64_t tot = lane < kRowWarps ? sm.wmass[lane] : 0ull;
+            tot = warp_sum_u64(tot);
+            if (lane == 0) {
+                w.chunk_mass[rt * kMaxChunks + rank] = tot;
+                cluster.map_shared_rank(&sm, 0)->rmass[rank] = tot;
+            }
         }
+        cluster.sync();
     }
-    cluster.sync();  // remote reads done; chunk masses of the cluster are visible
     if (rank != 0) return;
     if (tid == 0) {
         uint64_t mass = 0;
         if (mode == 1)
-            for (int r = 0; r < cpr; ++r) mass += __ldcg(&w.chunk_mass[rt * kMaxChunks + r]);
+            for (int r = 0; r < cpr; ++r) mass += sm.rmass[r];
         w.row_max[rt] = M;
         w.row_arg[rt] = static_cast<int32_t>(key_id(gkey));
         w.row_mass[rt] = mass;
@@ -485,22 +552,29 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
 
     // ---- acceptance walk for sequence b (one CTA) ----
     const int T = d.T;
+    if (tid == 0) sm.bad = 0;
     for (int c = tid; c < T; c += kRowThreads) {
         sm.tok[c] = c < n ? tokens[static_cast<size_t>(b) * T + c] : -1;
         sm.par[c] = c < n ? parent[static_cast<size_t>(b) * T + c] : -1;
         if (c < n) {
             sm.arg[c] = __ldcg(&w.row_arg[static_cast<size_t>(b) * T + c]);
             sm.rmax[c] = __ldcg(&w.row_max[static_cast<size_t>(b) * T + c]);
-            sm.rmass[c] = __ldcg(&w.row_mass[static_cast<size_t>(b) * T + c]);
+            sm.rowmass[c] = __ldcg(&w.row_mass[static_cast<size_t>(b) * T + c]);
         }
     }
+    // chunk masses of every row of the sequence, in the (now idle) chunk buffer
+    unsigned long long* cmass = reinterpret_cast<unsigned long long*>(dyn_smem);
+    if (mode == 1) {
+        for (int c = tid; c < T + 2; c += kRowThreads) sm.uni[c] = uniforms[static_cast<size_t>(b) * (T + 2) + c];
+        for (int q = tid; q < n * cpr; q += kRowThreads)
+            cmass[q] = __ldcg(&w.chunk_mass[(static_cast<size_t>(b) * T + q / cpr) * kMaxChunks + q % cpr]);
+    }
     __syncthreads();
-    bool bad = false;
     for (int c = 1 + tid; c < n; c += kRowThreads) {
         const int tk = sm.tok[c], p = sm.par[c];
+        sm.pmass[c] = 0;
         if (tk < 0 || tk >= d.V || p < 0 || p >= c) {
-            bad = true;
-            sm.pmass[c] = 0;
+            sm.bad = 1;
             continue;
         }
         if (mode == 1) {
@@ -513,15 +587,14 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
             sm.pmass[c] = fixed_mass(x, sm.rmax[p], inv_t);
         }
     }
-    if (bad) raise_status(w.status, kDevBadIndex);
     __syncthreads();
+    if (tid == 0 && sm.bad) raise_status(w.status, kDevBadIndex);
 
     if (tid == 0) {
         int cur = 0, a = 0;
         sm.path[0] = 0;
         sm.n_removed = 0;
-        unsigned long long S = mode == 1 ? sm.rmass[0] : 0ull;
-        const uint32_t* u = mode == 1 ? uniforms + static_cast<size_t>(b) * (T + 2) : nullptr;
+        unsigned long long S = mode == 1 ? sm.rowmass[0] : 0ull;
         for (;;) {
             int next = -1;
             if (a < d.D) {
@@ -533,7 +606,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
                             break;
                         }
                     } else {
-                        const unsigned __int128 lhs = static_cast<unsigned __int128>(u[c] >> 8) * S;
+                        const unsigned __int128 lhs = static_cast<unsigned __int128>(sm.uni[c] >> 8) * S;
                         const unsigned __int128 rhs = static_cast<unsigned __int128>(sm.pmass[c]) << 24;
                         if (lhs < rhs) {
                             next = c;
@@ -550,7 +623,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
             sm.path[++a] = next;
             cur = next;
             if (mode == 1) {
-                S = sm.rmass[cur];
+                S = sm.rowmass[cur];
                 sm.n_removed = 0;
             }
         }
@@ -559,15 +632,14 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
         sm.bonus = mode == 0 ? sm.arg[cur] : -1;
         if (mode == 1) {
             // choose the chunk of row `cur` that holds the draw
-            const uint64_t U64 = (static_cast<uint64_t>(u[T + 1]) << 32) | u[T];
+            const uint64_t U64 = (static_cast<uint64_t>(sm.uni[T + 1]) << 32) | sm.uni[T];
             const unsigned long long tdraw =
                 static_cast<unsigned long long>((static_cast<unsigned __int128>(U64) * S) >> 64);
-            const size_t rc = static_cast<size_t>(b) * T + cur;
             unsigned long long run = 0;
             int chosen = cpr - 1;
             unsigned long long tin = 0;
             for (int r = 0; r < cpr; ++r) {
-                unsigned long long cm = __ldcg(&w.chunk_mass[rc * kMaxChunks + r]);
+                unsigned long long cm = cmass[cur * cpr + r];
                 const int lo = r * chunk, hi = min(d.V, lo + chunk);
                 for (int q = 0; q < sm.n_removed; ++q)
                     if (sm.removed_tok[q] >= lo && sm.removed_tok[q] < hi) cm -= sm.removed_mass[q];
@@ -585,50 +657,81 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
     __syncthreads();
 
     if (mode == 1) {
-        // Scan the chosen chunk of row `cur`: smallest y (not removed) whose
-        // running mass exceeds the draw. Each thread owns a contiguous range.
+        // Smallest y (not removed) of the chosen chunk of row `cur` whose
+        // running mass exceeds the draw. The chunk is staged in shared memory
+        // (second phase of the CTA's mbarrier) and walked in id order in
+        // rounds of 256 vectors, one vector per thread, with a block scan per
+        // round.
         const int cur = sm.cur;
         const int lo = sm.sample_chunk * chunk, hi = min(d.V, lo + chunk);
         const int len = max(0, hi - lo);
-        const int per = (len + kRowThreads - 1) / kRowThreads;
-        const int a0 = lo + tid * per, a1 = min(hi, a0 + per);
         const char* crow = static_cast<const char*>(target) + (static_cast<size_t>(b) * T + cur) * d.V * ES;
-        const float m = sm.rmax[cur];
-        const int nrem = sm.n_removed;
-        auto mass_at = [&](int y) -> unsigned long long {
-            for (int q = 0; q < nrem; ++q)
-                if (sm.removed_tok[q] == y) return 0ull;
-            float x;
-            if (DT == 1)
-                x = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(crow)[y]) << 16);
-            else
-                x = reinterpret_cast<const float*>(crow)[y];
-            return fixed_mass(x, m, inv_t);
-        };
-        unsigned long long mine = 0;
-        for (int y = a0; y < a1; ++y) mine += mass_at(y);
-        sm.scan[tid] = mine;
+        fence_proxy_async_smem();  // earlier generic reads of the buffer before the async-proxy rewrite
         __syncthreads();
-        if (tid == 0) {  // exclusive prefix (256 entries)
-            unsigned long long run = 0;
-            for (int i = 0; i < kRowThreads; ++i) {
-                const unsigned long long v = sm.scan[i];
-                sm.scan[i] = run;
-                run += v;
+        if (tid == 0) {
+            sm.found = 0;
+            if (len > 0) {
+                mbar_arrive_expect_tx(&sm.bar, static_cast<uint32_t>(len) * ES);
+                bulk_g2s(dyn_smem, crow + static_cast<size_t>(lo) * ES, static_cast<uint32_t>(len) * ES, &sm.bar);
             }
         }
+        if (len > 0 && !mbar_wait(&sm.bar, 1)) raise_status(w.status, kDevTimeout);
         __syncthreads();
-        const unsigned long long tin = sm.sample_t;
-        const unsigned long long ex = sm.scan[tid];
-        if (mine > 0 && ex <= tin && tin < ex + mine) {
-            unsigned long long run = ex;
-            for (int y = a0; y < a1; ++y) {
-                run += mass_at(y);
-                if (run > tin) {
-                    sm.bonus = y;
-                    break;
+        const float m = sm.rmax[cur];
+        const int nrem = sm.n_removed;
+        const int nv = len / EPV;
+        unsigned long long tin = sm.sample_t;
+        for (int base = 0; base < nv; base += kRowThreads) {
+            const int v = base + tid;
+            unsigned long long em[EPV];
+            unsigned long long mv = 0;
+            if (v < nv) {
+                float x[EPV];
+                unpack16<DT>(buf[v], x);
+                const int y0 = lo + v * EPV;
+                bool has_removed = false;
+                for (int q = 0; q < nrem; ++q)
+                    has_removed |= static_cast<unsigned>(sm.removed_tok[q] - y0) < static_cast<unsigned>(EPV);
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) {
+                    em[e] = fixed_mass(x[e], m, inv_t);
+                    if (has_removed)
+                        for (int q = 0; q < nrem; ++q)
+                            if (sm.removed_tok[q] == y0 + e) em[e] = 0;
+                    mv += em[e];
                 }
             }
+            // block exclusive scan of mv
+            unsigned long long incl = mv;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t lo32 = __shfl_up_sync(0xffffffffu, static_cast<uint32_t>(incl), o);
+                const uint32_t hi32 = __shfl_up_sync(0xffffffffu, static_cast<uint32_t>(incl >> 32), o);
+                if (lane >= o) incl += (static_cast<unsigned long long>(hi32) << 32) | lo32;
+            }
+            if (lane == 31) sm.wscan[warp] = incl;
+            __syncthreads();
+            unsigned long long wbase = 0, total = 0;
+            for (int i = 0; i < kRowWarps; ++i) {
+                if (i < warp) wbase += sm.wscan[i];
+                total += sm.wscan[i];
+            }
+            const unsigned long long ex = wbase + incl - mv;
+            if (mv > 0 && ex <= tin && tin < ex + mv) {
+                unsigned long long run = ex;
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) {
+                    run += em[e];
+                    if (run > tin) {
+                        sm.bonus = lo + v * EPV + e;
+                        break;
+                    }
+                }
+                sm.found = 1;
+            }
+            __syncthreads();
+            if (sm.found) break;
+            tin -= total;
         }
         __syncthreads();
     }
@@ -662,9 +765,6 @@ RowSplit choose_row_split(int V, int esize) {
     return s;
 }
 
-// Raise a kernel's dynamic shared memory limit only when a launch needs more
-// than was set before, so that launches inside a CUDA graph capture (after a
-// first call outside it) make no attribute calls.
 cudaError_t ensure_dyn_smem(const void* kernel, int smem) {
     static std::mutex mu;
     static std::map<std::pair<const void*, int>, int> done;
@@ -707,8 +807,8 @@ cudaError_t launch_expand(const TreeDims& d, const TreeWs& ws, int step, const v
     TreeDims dd = d;
     TreeWs ww = ws;
     int chunk = s.chunk;
-    void* args[] = {&dd,          &ww,      &step, &chunk, const_cast<void**>(&logits), const_cast<float**>(&lse_in),
-                    &row_lse,     &ftok,    &fcount_out};
+    void* args[] = {&dd,      &ww,   &step,       &chunk, const_cast<void**>(&logits), const_cast<float**>(&lse_in),
+                    &row_lse, &ftok, &fcount_out};
     return d.dtype == 1 ? launch_rows(expand_kernel<1>, grid, s.cpr, s.smem_bytes, stream, args)
                         : launch_rows(expand_kernel<0>, grid, s.cpr, s.smem_bytes, stream, args);
 }
@@ -719,6 +819,8 @@ cudaError_t launch_verify(const TreeDims& d, const TreeWs& ws, int mode, float i
                           cudaStream_t stream) {
     const RowSplit s = choose_row_split(d.V, d.dtype == 1 ? 2 : 4);
     dim3 grid(s.cpr, d.B * d.T, 1);
+    // the acceptance walk keeps the chunk masses of all T rows in the chunk buffer
+    const int smem = static_cast<int>(std::max<size_t>(s.smem_bytes, align_up(static_cast<size_t>(d.T) * s.cpr * 8, 128)));
     TreeDims dd = d;
     TreeWs ww = ws;
     int chunk = s.chunk;
@@ -735,8 +837,8 @@ cudaError_t launch_verify(const TreeDims& d, const TreeWs& ws, int mode, float i
                     &accept_len,
                     &slots,
                     &out_tokens};
-    return d.dtype == 1 ? launch_rows(verify_kernel<1>, grid, s.cpr, s.smem_bytes, stream, args)
-                        : launch_rows(verify_kernel<0>, grid, s.cpr, s.smem_bytes, stream, args);
+    return d.dtype == 1 ? launch_rows(verify_kernel<1>, grid, s.cpr, smem, stream, args)
+                        : launch_rows(verify_kernel<0>, grid, s.cpr, smem, stream, args);
 }
 
 }  // namespace eagle
