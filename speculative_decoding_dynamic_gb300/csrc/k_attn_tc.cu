@@ -165,7 +165,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t bar_q, bar_kv_full[kStages], bar_kv_empty[kStages], bar_s_full, bar_p_full, bar_o_full;
+    __shared__ uint64_t bar_q, bar_kv_full[kStages], bar_kv_empty[kStages], bar_s_full, bar_p_full, bar_o_full,
+        bar_comb;
     __shared__ uint32_t tmem_holder;
     __shared__ uint32_t mask_sm[kBM][kMaxW];
     __shared__ int sh_last;
@@ -194,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bar_s_full, 1);
         mbar_init(&bar_p_full, 128);
         mbar_init(&bar_o_full, 1);
+        mbar_init(&bar_comb, 1);
         fence_mbar_init();
 
         if (bad) raise_status(p.status, kDevBadIndex);
@@ -303,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int jj = 0; jj < n_local; ++jj) {
             const int st = jj & 1;
             const int key0 = (t_begin + jj) * kBN;
-            if (!mbar_wait(&bar_s_full, jj & 1)) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&bar_s_full, jj & 1))) {  // warp-uniform exit
                 ok = false;
                 break;
             }
@@ -366,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             l += sum;
             if (jj > 0) {  // PV(j-1) done: P buffer free, O stable
-                if (!mbar_wait(&bar_o_full, (jj - 1) & 1)) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&bar_o_full, (jj - 1) & 1))) {
                     ok = false;
                     break;
                 }
@@ -393,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // V rows of keys that no row can see may hold anything (even NaN):
             // zero them so that 0 * V stays 0 in the MMA.
             if (key0 + kBN > nkeys) {
-                if (!mbar_wait(&bar_kv_full[st], (jj >> 1) & 1)) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&bar_kv_full[st], (jj >> 1) & 1))) {
                     ok = false;
                     break;
                 }
@@ -413,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&bar_p_full);
         }
         if (ok && n_local > 0) {
-            ok = mbar_wait(&bar_o_full, (n_local - 1) & 1);
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar_o_full, (n_local - 1) & 1));
             tc_fence_after();
         }
         if (!ok) raise_status(p.status, kDevTimeout);
@@ -442,19 +444,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         } else {
-            const size_t slot = static_cast<size_t>(unit) * p.nsplit + split;
-            float* po = p.part_o + (slot * kBM + r) * kHD;
+            // Split partial: unnormalised O row (float4 q of each 32-column
+            // chunk stored at position q ^ (row & 7)), reference max and sum.
+            const size_t s0 = static_cast<size_t>(unit) * p.nsplit;
+            float* po = p.part_o + ((s0 + split) * kBM + r) * kHD;
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 float o[32];
                 tmem_ld32(tmem_o + lane_off + c * 32, o);
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
-                    *reinterpret_cast<float4*>(po + c * 32 + 4 * q) =
+                    *reinterpret_cast<float4*>(po + c * 32 + ((q ^ (r & 7)) << 2)) =
                         make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
             }
-            p.part_ml[(slot * kBM + r) * 2] = (seen && l > 0.0f) ? m_use : -INFINITY;
-            p.part_ml[(slot * kBM + r) * 2 + 1] = l;
+            const float m_own = (seen && l > 0.0f) ? m_use : -INFINITY;
+            p.part_ml[((s0 + split) * kBM + r) * 2] = m_own;
+            p.part_ml[((s0 + split) * kBM + r) * 2 + 1] = l;
             __threadfence();
             named_sync_softmax();
             if (r == 0) {
@@ -463,37 +468,76 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             named_sync_softmax();
             if (sh_last) {
+                // Merge: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s, accumulated
+                // in this CTA's TMEM; the other splits' partials are bulk-copied
+                // into the idle K/V buffers, two per round.
                 __threadfence();
-                if (row_live) {
-                    const size_t s0 = static_cast<size_t>(unit) * p.nsplit;
-                    float M = -INFINITY;
-                    for (int s = 0; s < nsplit_b; ++s) M = fmaxf(M, __ldcg(&p.part_ml[((s0 + s) * kBM + r) * 2]));
-                    float Ls = 0.0f;
-                    for (int s = 0; s < nsplit_b; ++s) {
-                        const float ms = __ldcg(&p.part_ml[((s0 + s) * kBM + r) * 2]);
-                        if (ms > -INFINITY) Ls += __ldcg(&p.part_ml[((s0 + s) * kBM + r) * 2 + 1]) * ex2_approx(ms - M);
-                    }
-                    const bool live = i < n && Ls > 0.0f;
-                    const float inv = live ? 1.0f / Ls : 0.0f;
+                float M = -INFINITY;
+                for (int s = 0; s < nsplit_b; ++s) M = fmaxf(M, __ldcg(&p.part_ml[((s0 + s) * kBM + r) * 2]));
+                float Ls = 0.0f;
+                for (int s = 0; s < nsplit_b; ++s) {
+                    const float ms = __ldcg(&p.part_ml[((s0 + s) * kBM + r) * 2]);
+                    if (ms > -INFINITY) Ls += __ldcg(&p.part_ml[((s0 + s) * kBM + r) * 2 + 1]) * ex2_approx(ms - M);
+                }
+                const bool live = row_live && i < n && Ls > 0.0f;
+                const float inv = live ? 1.0f / Ls : 0.0f;
+                const float w_own = m_own > -INFINITY ? ex2_approx(m_own - M) * inv : 0.0f;
 #pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        float o[32];
+                for (int c = 0; c < 4; ++c) {
+                    float o[32];
+                    tmem_ld32(tmem_o + lane_off + c * 32, o);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = 0.0f;
-                        for (int s = 0; s < nsplit_b; ++s) {
-                            const float ms = __ldcg(&p.part_ml[((s0 + s) * kBM + r) * 2]);
-                            if (!(ms > -INFINITY)) continue;
-                            const float w = ex2_approx(ms - M) * inv;
-                            const float* ps = p.part_o + ((s0 + s) * kBM + r) * kHD + c * 32;
+                    for (int e = 0; e < 32; ++e) o[e] *= w_own;
+                    tmem_st32(tmem_o + lane_off + c * 32, o);
+                }
+                constexpr int kPart = kBM * kHD * 4;  // 64 KB: one split's partial block
+                unsigned char* area = smem + kSmemKV;  // 128 KB of K/V stages, idle now
+                int round = 0;
+                for (int s = 0; s < nsplit_b;) {
+                    int lst[2];
+                    int cnt = 0;
+                    while (s < nsplit_b && cnt < 2) {
+                        if (s != split) lst[cnt++] = s;
+                        ++s;
+                    }
+                    if (cnt == 0) break;
+                    if (r == 0) {
+                        fence_proxy_async_smem();
+                        mbar_arrive_expect_tx(&bar_comb, cnt * kPart);
+                        for (int q = 0; q < cnt; ++q)
+                            bulk_g2s(area + q * kPart, p.part_o + (s0 + lst[q]) * kBM * kHD, kPart, &bar_comb);
+                    }
+                    // on a timeout keep taking part in the named barrier below (no early exit)
+                    const bool landed = __all_sync(0xffffffffu, mbar_wait(&bar_comb, round & 1));
+                    if (!landed) raise_status(p.status, kDevTimeout);
+                    for (int q = 0; landed && q < cnt; ++q) {
+                        const float ms = __ldcg(&p.part_ml[((s0 + lst[q]) * kBM + r) * 2]);
+                        const float wq = ms > -INFINITY ? ex2_approx(ms - M) * inv : 0.0f;
+                        const float* rowp = reinterpret_cast<const float*>(area + q * kPart) + r * kHD;
+#pragma unroll 1
+                        for (int c = 0; c < 4; ++c) {
+                            float o[32];
+                            tmem_ld32(tmem_o + lane_off + c * 32, o);
 #pragma unroll
-                            for (int q = 0; q < 8; ++q) {
-                                const float4 v = __ldcg(reinterpret_cast<const float4*>(ps + 4 * q));
-                                o[4 * q] += v.x * w;
-                                o[4 * q + 1] += v.y * w;
-                                o[4 * q + 2] += v.z * w;
-                                o[4 * q + 3] += v.w * w;
+                            for (int q4 = 0; q4 < 8; ++q4) {
+                                const float4 v =
+                                    *reinterpret_cast<const float4*>(rowp + c * 32 + ((q4 ^ (r & 7)) << 2));
+                                o[4 * q4] += wq * v.x;
+                                o[4 * q4 + 1] += wq * v.y;
+                                o[4 * q4 + 2] += wq * v.z;
+                                o[4 * q4 + 3] += wq * v.w;
                             }
+                            tmem_st32(tmem_o + lane_off + c * 32, o);
                         }
+                    }
+                    named_sync_softmax();  // every row has read the slots before they are refilled
+                    ++round;
+                }
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    float o[32];
+                    tmem_ld32(tmem_o + lane_off + c * 32, o);
+                    if (row_live) {
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             uint4 u = make_uint4(0u, 0u, 0u, 0u);
