@@ -51,7 +51,7 @@ constexpr int kHD = 128;                   // head dim (MMA K of QK^T, N of PV)
 constexpr int kTile = kBM * kHD * 2;       // 32 KB: a 128 x 128 bf16 tile
 constexpr int kHalf = kTile / 2;           // 16 KB: 128 rows x 64 columns (one swizzle-128B column block)
 constexpr int kStages = 2;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2..9 softmax (two column halves)
 constexpr int kSmemQ = 0;
 constexpr int kSmemKV = kTile;             // stage s: K at kSmemKV + s*2*kTile, V at +kTile
 constexpr int kSmemP = kTile * (1 + 2 * kStages);
@@ -155,7 +155,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-__device__ __forceinline__ void named_sync_softmax() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void named_sync_softmax() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 // ------------------------------------------------------------- kernel ---
 
@@ -170,6 +170,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ uint32_t tmem_holder;
     __shared__ uint32_t mask_sm[kBM][kMaxW];
     __shared__ int sh_last;
+    __shared__ float xch[2][2][kBM];  // per-tile row maxima exchanged between the two column halves
+    __shared__ float xsum[2][kBM];    // final row sums of the two halves
 
     const int rb = blockIdx.x, split = blockIdx.y;
     const int b = blockIdx.z / p.Hkv, hk = blockIdx.z % p.Hkv;
@@ -193,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bar_kv_empty[s], 1);
         }
         mbar_init(&bar_s_full, 1);
-        mbar_init(&bar_p_full, 128);
+        mbar_init(&bar_p_full, 256);
         mbar_init(&bar_o_full, 1);
         mbar_init(&bar_comb, 1);
         fence_mbar_init();
@@ -206,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    if (warp >= 2) {  // this row's mask words
+    if (warp >= 2 && warp < 6) {  // this row's mask words
         const int r = ((warp & 3) << 5) | lane;
         const int i = i0 + r / p.G;
         for (int w = 0; w < kMaxW; ++w)
@@ -290,47 +292,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------ softmax ---
-        // One thread per query row (TMEM lane). O accumulates in TMEM; the
-        // exponentials use a reference maximum m_use that is raised (and O, l
-        // rescaled) only when a tile's maximum exceeds it by more than 2^8.
+        // Two threads per query row (TMEM lane): warps 2..5 own key/output
+        // columns 0..63, warps 6..9 columns 64..127 (same lane quarters).
+        // Row maxima and sums are exchanged through shared memory. O
+        // accumulates in TMEM; the exponentials use a reference maximum m_use
+        // that is raised (O, l rescaled) only when a tile's maximum exceeds it
+        // by more than 2^8.
+        const int half = (warp - 2) >> 2;
+        const int cb = half * 64;                        // first column of this half
         const int q4 = warp & 3;
         const int r = (q4 << 5) | lane;                  // row of the block = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
         const int grow = rb * kBM + r;                   // row within the (b, hk) problem
         const int i = i0 + r / p.G;                      // tree slot of the row
         const int g = r % p.G;
-        float m_use = 0.0f, l = 0.0f;
+        float m_use = 0.0f, lh = 0.0f;                   // lh: this half's share of the row sum
         bool seen = false;
         bool ok = true;
         for (int jj = 0; jj < n_local; ++jj) {
             const int st = jj & 1;
             const int key0 = (t_begin + jj) * kBN;
-            if (!__all_sync(0xffffffffu, mbar_wait(&bar_s_full, jj & 1))) {  // warp-uniform exit
-                ok = false;
-                break;
-            }
+            // After a timed-out wait a warp skips the work of the remaining tiles
+            // but still takes every named barrier, so the other half never waits
+            // for it without bound.
+            if (ok && !__all_sync(0xffffffffu, mbar_wait(&bar_s_full, jj & 1))) ok = false;
             tc_fence_after();
-            float sv[kBN];
-            tmem_ld64(tmem_s + lane_off, sv);
-            tmem_ld64(tmem_s + lane_off + 64, sv + 64);
-            // visibility of the tile's keys: prefix keys, then tree slots in mask row i
-            uint32_t vis[4];
+            float sv[64];
+            if (ok) tmem_ld64(tmem_s + lane_off + cb, sv);
+            else
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int kb = key0 + 32 * c;  // first key of this group of 32
+                for (int e = 0; e < 64; ++e) sv[e] = -INFINITY;
+            // visibility of this half's keys: prefix keys, then tree slots in mask row i
+            uint32_t vis[2];
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int kb = key0 + cb + 32 * c;  // first key of this group of 32
                 uint32_t pre = 0u;
-                const int npre = L - kb;       // keys of the group inside the prefix
+                const int npre = L - kb;             // keys of the group inside the prefix
                 if (npre >= 32) pre = 0xffffffffu;
                 else if (npre > 0) pre = (1u << npre) - 1u;
                 uint32_t tree = 0u;
                 if (npre < 32) {
-                    const int j0 = kb - L;     // slot of the group's first key (may be negative)
+                    const int j0 = kb - L;           // slot of the group's first key (may be negative)
                     const int lo = j0 < 0 ? 0 : j0;
                     const int w0 = lo >> 5, sh = lo & 31;
                     uint32_t win = mask_sm[r][w0 & (kMaxW - 1)] >> sh;
                     if (sh && w0 + 1 < kMaxW) win |= mask_sm[r][w0 + 1] << (32 - sh);
                     if (w0 >= kMaxW) win = 0u;
-                    const int limit = n - lo;  // slots j >= n are never visible
+                    const int limit = n - lo;        // slots j >= n are never visible
                     if (limit <= 0) win = 0u;
                     else if (limit < 32) win &= (1u << limit) - 1u;
                     tree = j0 < 0 ? (win << (-j0)) : win;
@@ -340,10 +349,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             float mx = -INFINITY;
 #pragma unroll
-            for (int e = 0; e < kBN; ++e) {
+            for (int e = 0; e < 64; ++e) {
                 sv[e] *= p.scale_log2;
                 if ((vis[e >> 5] >> (e & 31)) & 1u) mx = fmaxf(mx, sv[e]);
             }
+            xch[jj & 1][half][r] = mx;
+            named_sync_softmax();
+            mx = fmaxf(mx, xch[jj & 1][half ^ 1][r]);
             bool rescale = false;
             float alpha = 1.0f;
             if (mx > -INFINITY) {
@@ -354,42 +366,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                     alpha = ex2_approx(m_use - mx);
                     m_use = mx;
                     rescale = true;
-                    l *= alpha;
+                    lh *= alpha;
                 }
             }
             float sum = 0.0f;
-            uint32_t pk[kBN / 2];
+            uint32_t pk[32];
 #pragma unroll
-            for (int e = 0; e < kBN; e += 2) {
+            for (int e = 0; e < 64; e += 2) {
                 const float p0 = ((vis[e >> 5] >> (e & 31)) & 1u) ? ex2_approx(sv[e] - m_use) : 0.0f;
                 const float p1 = ((vis[(e + 1) >> 5] >> ((e + 1) & 31)) & 1u) ? ex2_approx(sv[e + 1] - m_use) : 0.0f;
                 sum += p0 + p1;
                 pk[e >> 1] = pack_bf16(p0, p1);
             }
-            l += sum;
+            lh += sum;
+            if (!ok) continue;
             if (jj > 0) {  // PV(j-1) done: P buffer free, O stable
                 if (!__all_sync(0xffffffffu, mbar_wait(&bar_o_full, (jj - 1) & 1))) {
                     ok = false;
-                    break;
+                    continue;
                 }
                 tc_fence_after();
                 // tcgen05.ld/st are warp-collective: rescale if any row of the warp needs it
                 // (alpha = 1 for the others).
                 if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < 2; ++c) {
                         float o[32];
-                        tmem_ld32(tmem_o + lane_off + c * 32, o);
+                        tmem_ld32(tmem_o + lane_off + cb + c * 32, o);
 #pragma unroll
                         for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                        tmem_st32(tmem_o + lane_off + c * 32, o);
+                        tmem_st32(tmem_o + lane_off + cb + c * 32, o);
                     }
                 }
             }
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {  // 16 chunks of 8 keys, 128B-swizzled K-major rows
-                const int blk = q >> 3, cin = q & 7;
-                unsigned char* dst = sP + blk * kHalf + r * 128 + ((cin ^ (r & 7)) << 4);
+            for (int q = 0; q < 8; ++q) {  // 8 chunks of 8 keys = this half's 64-key block
+                unsigned char* dst = sP + half * kHalf + r * 128 + ((q ^ (r & 7)) << 4);
                 *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
             }
             // V rows of keys that no row can see may hold anything (even NaN):
@@ -397,17 +409,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (key0 + kBN > nkeys) {
                 if (!__all_sync(0xffffffffu, mbar_wait(&bar_kv_full[st], (jj >> 1) & 1))) {
                     ok = false;
-                    break;
+                    continue;
                 }
                 if (key0 + r >= nkeys) {
-                    unsigned char* sV = smem + kSmemKV + st * 2 * kTile + kTile;
-                    uint4* z0 = reinterpret_cast<uint4*>(sV + r * 128);
-                    uint4* z1 = reinterpret_cast<uint4*>(sV + kHalf + r * 128);
+                    unsigned char* sV = smem + kSmemKV + st * 2 * kTile + kTile + half * kHalf;
+                    uint4* z = reinterpret_cast<uint4*>(sV + r * 128);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        z0[q] = make_uint4(0, 0, 0, 0);
-                        z1[q] = make_uint4(0, 0, 0, 0);
-                    }
+                    for (int q = 0; q < 8; ++q) z[q] = make_uint4(0, 0, 0, 0);
                 }
             }
             fence_proxy_async_smem();
@@ -419,6 +427,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
         }
         if (!ok) raise_status(p.status, kDevTimeout);
+        // row sum of both halves
+        xsum[half][r] = lh;
+        named_sync_softmax();
+        const float l = lh + xsum[half ^ 1][r];
         // ------------------------------------------------------- epilogue ---
         const bool row_live = grow < p.G * p.T;
         __nv_bfloat16* orow =
@@ -427,9 +439,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool live = row_live && i < n && l > 0.0f && ok;  // rows of unused slots are zeros
             const float inv = live ? 1.0f / l : 0.0f;
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 float o[32];
-                if (n_local > 0) tmem_ld32(tmem_o + lane_off + c * 32, o);
+                if (n_local > 0) tmem_ld32(tmem_o + lane_off + cb + c * 32, o);
                 if (row_live) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -439,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                            pack_bf16(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
                                            pack_bf16(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
                                            pack_bf16(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
-                        *reinterpret_cast<uint4*>(orow + c * 32 + 8 * q) = u;
+                        *reinterpret_cast<uint4*>(orow + cb + c * 32 + 8 * q) = u;
                     }
                 }
             }
@@ -449,20 +461,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             const size_t s0 = static_cast<size_t>(unit) * p.nsplit;
             float* po = p.part_o + ((s0 + split) * kBM + r) * kHD;
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 float o[32];
-                tmem_ld32(tmem_o + lane_off + c * 32, o);
+                tmem_ld32(tmem_o + lane_off + cb + c * 32, o);
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
-                    *reinterpret_cast<float4*>(po + c * 32 + ((q ^ (r & 7)) << 2)) =
+                    *reinterpret_cast<float4*>(po + cb + c * 32 + ((q ^ (r & 7)) << 2)) =
                         make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
             }
             const float m_own = (seen && l > 0.0f) ? m_use : -INFINITY;
-            p.part_ml[((s0 + split) * kBM + r) * 2] = m_own;
-            p.part_ml[((s0 + split) * kBM + r) * 2 + 1] = l;
+            if (half == 0) {
+                p.part_ml[((s0 + split) * kBM + r) * 2] = m_own;
+                p.part_ml[((s0 + split) * kBM + r) * 2 + 1] = l;
+            }
             __threadfence();
             named_sync_softmax();
-            if (r == 0) {
+            if (r == 0 && half == 0) {
                 const int prev = atomicAdd(&p.tickets[unit], 1);
                 sh_last = prev == nsplit_b - 1;
             }
@@ -483,12 +497,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float inv = live ? 1.0f / Ls : 0.0f;
                 const float w_own = m_own > -INFINITY ? ex2_approx(m_own - M) * inv : 0.0f;
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < 2; ++c) {
                     float o[32];
-                    tmem_ld32(tmem_o + lane_off + c * 32, o);
+                    tmem_ld32(tmem_o + lane_off + cb + c * 32, o);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] *= w_own;
-                    tmem_st32(tmem_o + lane_off + c * 32, o);
+                    tmem_st32(tmem_o + lane_off + cb + c * 32, o);
                 }
                 constexpr int kPart = kBM * kHD * 4;  // 64 KB: one split's partial block
                 unsigned char* area = smem + kSmemKV;  // 128 KB of K/V stages, idle now
@@ -501,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ++s;
                     }
                     if (cnt == 0) break;
-                    if (r == 0) {
+                    if (r == 0 && half == 0) {
                         fence_proxy_async_smem();
                         mbar_arrive_expect_tx(&bar_comb, cnt * kPart);
                         for (int q = 0; q < cnt; ++q)
@@ -513,30 +527,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int q = 0; landed && q < cnt; ++q) {
                         const float ms = __ldcg(&p.part_ml[((s0 + lst[q]) * kBM + r) * 2]);
                         const float wq = ms > -INFINITY ? ex2_approx(ms - M) * inv : 0.0f;
-                        const float* rowp = reinterpret_cast<const float*>(area + q * kPart) + r * kHD;
+                        const float* rowp = reinterpret_cast<const float*>(area + q * kPart) + r * kHD + cb;
 #pragma unroll 1
-                        for (int c = 0; c < 4; ++c) {
+                        for (int c = 0; c < 2; ++c) {
                             float o[32];
-                            tmem_ld32(tmem_o + lane_off + c * 32, o);
+                            tmem_ld32(tmem_o + lane_off + cb + c * 32, o);
 #pragma unroll
-                            for (int q4 = 0; q4 < 8; ++q4) {
+                            for (int q4b = 0; q4b < 8; ++q4b) {
                                 const float4 v =
-                                    *reinterpret_cast<const float4*>(rowp + c * 32 + ((q4 ^ (r & 7)) << 2));
-                                o[4 * q4] += wq * v.x;
-                                o[4 * q4 + 1] += wq * v.y;
-                                o[4 * q4 + 2] += wq * v.z;
-                                o[4 * q4 + 3] += wq * v.w;
+                                    *reinterpret_cast<const float4*>(rowp + c * 32 + ((q4b ^ (r & 7)) << 2));
+                                o[4 * q4b] += wq * v.x;
+                                o[4 * q4b + 1] += wq * v.y;
+                                o[4 * q4b + 2] += wq * v.z;
+                                o[4 * q4b + 3] += wq * v.w;
                             }
-                            tmem_st32(tmem_o + lane_off + c * 32, o);
+                            tmem_st32(tmem_o + lane_off + cb + c * 32, o);
                         }
                     }
                     named_sync_softmax();  // every row has read the slots before they are refilled
                     ++round;
                 }
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < 2; ++c) {
                     float o[32];
-                    tmem_ld32(tmem_o + lane_off + c * 32, o);
+                    tmem_ld32(tmem_o + lane_off + cb + c * 32, o);
                     if (row_live) {
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
@@ -545,11 +559,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 u = make_uint4(pack_bf16(o[8 * q], o[8 * q + 1]), pack_bf16(o[8 * q + 2], o[8 * q + 3]),
                                                pack_bf16(o[8 * q + 4], o[8 * q + 5]),
                                                pack_bf16(o[8 * q + 6], o[8 * q + 7]));
-                            *reinterpret_cast<uint4*>(orow + c * 32 + 8 * q) = u;
+                            *reinterpret_cast<uint4*>(orow + cb + c * 32 + 8 * q) = u;
                         }
                     }
                 }
-                if (r == 0) p.tickets[unit] = 0;
+                if (r == 0 && half == 0) p.tickets[unit] = 0;
             }
         }
     }
