@@ -9,6 +9,14 @@ namespace eagle {
 
 namespace cg = cooperative_groups;
 
+// ------------------------------------------- programmatic dependent launch ---
+// Every kernel of the cycle is launched with programmatic stream
+// serialisation: it lets the next kernel launch at once and waits for the
+// previous one only where it first reads that kernel's results. Both are
+// no-ops for a launch without the attribute.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_prior() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------- status word ---
 // Device-detected faults: the first error of a cycle wins (atomicCAS on 0).
 enum DeviceError : int {

@@ -34,6 +34,8 @@ __global__ void __launch_bounds__(kSimtWarps * 32) attn_simt_kernel(KvDims kv, i
                                                                      void* __restrict__ out, float scale_log2,
                                                                      int* status) {
     const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    pdl_launch_dependents();
+    pdl_wait_prior();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int d = kv.d;
     const int W = (T + 31) / 32;
@@ -132,22 +134,19 @@ cudaError_t launch_attention_simt(const KvDims& kv, int T, const void* q, const 
                                   int* status, cudaStream_t stream) {
     dim3 grid(T, kv.Hq, kv.B);
     const float scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kv.d)));
-    count_launch();
     const int epl = kv.d <= 32 ? 1 : (kv.d <= 64 ? 2 : 4);
-#define EAGLE_SIMT_LAUNCH(DT, E)                                                                              \
-    attn_simt_kernel<DT, E><<<grid, kSimtWarps * 32, 0, stream>>>(kv, T, q, cache, layer, prefix_len, mask, \
-                                                                   n_tree, out, scale_log2, status)
+#define EAGLE_SIMT_LAUNCH(DT, E)                                                                               \
+    return launch_pdl(attn_simt_kernel<DT, E>, grid, dim3(kSimtWarps * 32), 0, stream, kv, T, q, cache, layer, \
+                      prefix_len, mask, n_tree, out, scale_log2, status)
     if (kv.dtype == 1) {
         if (epl == 1) EAGLE_SIMT_LAUNCH(1, 1);
-        else if (epl == 2) EAGLE_SIMT_LAUNCH(1, 2);
-        else EAGLE_SIMT_LAUNCH(1, 4);
-    } else {
-        if (epl == 1) EAGLE_SIMT_LAUNCH(0, 1);
-        else if (epl == 2) EAGLE_SIMT_LAUNCH(0, 2);
-        else EAGLE_SIMT_LAUNCH(0, 4);
+        if (epl == 2) EAGLE_SIMT_LAUNCH(1, 2);
+        EAGLE_SIMT_LAUNCH(1, 4);
     }
+    if (epl == 1) EAGLE_SIMT_LAUNCH(0, 1);
+    if (epl == 2) EAGLE_SIMT_LAUNCH(0, 2);
+    EAGLE_SIMT_LAUNCH(0, 4);
 #undef EAGLE_SIMT_LAUNCH
-    return cudaGetLastError();
 }
 
 }  // namespace eagle

@@ -176,6 +176,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rb = blockIdx.x, split = blockIdx.y;
     const int b = blockIdx.z / p.Hkv, hk = blockIdx.z % p.Hkv;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_launch_dependents();
+    pdl_wait_prior();
     const int L = p.prefix_len[b];
     const int n = p.n_tree[b];
     const bool bad = L < 0 || L + p.T > p.max_len || n < 1 || n > p.T;
@@ -694,9 +696,7 @@ cudaError_t launch_attention(const KvDims& kv, int T, const void* q, const void*
     cudaError_t ae = ensure_dyn_smem(reinterpret_cast<const void*>(attn_tc_kernel), kSmemBytes + 1024);
     if (ae != cudaSuccess) return ae;
     dim3 grid(pl.n_rb, pl.nsplit, kv.B * kv.Hkv);
-    count_launch();
-    attn_tc_kernel<<<grid, kThreads, kSmemBytes + 1024, stream>>>(tq, tk, tv, prm);
-    return cudaGetLastError();
+    return launch_pdl(attn_tc_kernel, grid, dim3(kThreads), kSmemBytes + 1024, stream, tq, tk, tv, prm);
 }
 
 }  // namespace eagle

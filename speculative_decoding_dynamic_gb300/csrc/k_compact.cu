@@ -29,6 +29,8 @@ __global__ void __launch_bounds__(kCompactThreads) kv_compact_kernel(KvDims kv, 
     const int lk = blockIdx.y;  // layer * 2 + kv
     const int layer = lk >> 1, which = lk & 1;
     const int col = blockIdx.x * kCompactThreads + threadIdx.x;  // 16-byte column
+    pdl_launch_dependents();
+    pdl_wait_prior();
     const int ncol = kv.Hkv * kv.d * esize / 16;
     const int L = prefix_len[b];
     const int a = accept_len[b];
@@ -67,10 +69,8 @@ cudaError_t launch_kv_compact(const KvDims& kv, void* cache, const int32_t* pref
     const int esize = kv.dtype == 1 ? 2 : 4;
     const int ncol = kv.Hkv * kv.d * esize / 16;
     dim3 grid((ncol + kCompactThreads - 1) / kCompactThreads, kv.layers * 2, kv.B);
-    count_launch();
-    kv_compact_kernel<<<grid, kCompactThreads, 0, stream>>>(kv, static_cast<char*>(cache), esize, prefix_len,
-                                                            accept_len, slots, slots_stride, new_len, status);
-    return cudaGetLastError();
+    return launch_pdl(kv_compact_kernel, grid, dim3(kCompactThreads), 0, stream, kv, static_cast<char*>(cache), esize,
+                      prefix_len, accept_len, slots, slots_stride, new_len, status);
 }
 
 }  // namespace eagle

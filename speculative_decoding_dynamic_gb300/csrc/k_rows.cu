@@ -182,6 +182,8 @@ __global__ void __launch_bounds__(kRowThreads) expand_kernel(TreeDims d, TreeWs 
     const int row = blockIdx.y;
     const int b = row / d.k, f = row % d.k;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_launch_dependents();
+    pdl_wait_prior();
     const int F = w.fcount[step * d.B + b];
     constexpr int ES = DT == 1 ? 2 : 4;
     constexpr int EPV = 16 / ES;
@@ -467,6 +469,8 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int ES = DT == 1 ? 2 : 4;
     constexpr int EPV = 16 / ES;
+    pdl_launch_dependents();
+    pdl_wait_prior();
     const int n = n_tree[b];
     if (n < 1 || n > d.T) {
         if (rank == 0 && t == 0 && tid == 0) raise_status(w.status, kDevBadIndex);
@@ -789,13 +793,15 @@ static cudaError_t launch_rows(K kernel, dim3 grid, int cpr, int smem, cudaStrea
     cfg.blockDim = dim3(kRowThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = cpr;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     count_launch();
     return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(kernel), args);
 }

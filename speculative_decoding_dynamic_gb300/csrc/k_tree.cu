@@ -19,6 +19,8 @@ namespace eagle {
 // ------------------------------------------------------------ tree init ---
 
 __global__ void tree_init_kernel(TreeDims d, TreeWs w) {
+    pdl_launch_dependents();
+    pdl_wait_prior();
     const size_t BC = static_cast<size_t>(d.B) * d.C;
     const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
     for (size_t i = blockIdx.x * blockDim.x + threadIdx.x; i < BC; i += stride) {
@@ -54,6 +56,8 @@ __global__ void __launch_bounds__(kSortThreads) rerank_kernel(TreeDims d, TreeWs
     __shared__ int n_valid;
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
+    pdl_launch_dependents();
+    pdl_wait_prior();
     if (tid == 0) n_valid = 0;
     __syncthreads();
     int local = 0;
@@ -115,6 +119,8 @@ __global__ void __launch_bounds__(kBuildThreads) build_tree_kernel(TreeDims d, T
     const int b = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int T = d.T, W = d.W;
+    pdl_launch_dependents();
+    pdl_wait_prior();
     const int L = prefix_len[b];
     if (tid == 0 && L < 0) raise_status(w.status, kDevBadIndex);
 
@@ -200,26 +206,20 @@ cudaError_t launch_tree_init(const TreeDims& d, const TreeWs& ws, cudaStream_t s
     const size_t work = static_cast<size_t>(d.B) * d.C;
     int blocks = static_cast<int>((work + 255) / 256);
     blocks = blocks < 1 ? 1 : (blocks > 1216 ? 1216 : blocks);
-    count_launch();
-    tree_init_kernel<<<blocks, 256, 0, stream>>>(d, ws);
-    return cudaGetLastError();
+    return launch_pdl(tree_init_kernel, dim3(blocks), dim3(256), 0, stream, d, ws);
 }
 
 cudaError_t launch_rerank(const TreeDims& d, const TreeWs& ws, cudaStream_t stream) {
     int P = 2;
     while (P < d.C) P <<= 1;
-    count_launch();
-    rerank_kernel<<<d.B, kSortThreads, 0, stream>>>(d, ws, P);
-    return cudaGetLastError();
+    return launch_pdl(rerank_kernel, dim3(d.B), dim3(kSortThreads), 0, stream, d, ws, P);
 }
 
 cudaError_t launch_build_tree(const TreeDims& d, const TreeWs& ws, const int32_t* prefix_len,
                               const int32_t* root_token, int32_t* tokens, int32_t* parent, int32_t* depth,
                               int32_t* pos, uint32_t* mask, int32_t* n_tree, cudaStream_t stream) {
-    count_launch();
-    build_tree_kernel<<<d.B, kBuildThreads, 0, stream>>>(d, ws, prefix_len, root_token, tokens, parent, depth, pos,
-                                                        mask, n_tree);
-    return cudaGetLastError();
+    return launch_pdl(build_tree_kernel, dim3(d.B), dim3(kBuildThreads), 0, stream, d, ws, prefix_len, root_token,
+                      tokens, parent, depth, pos, mask, n_tree);
 }
 
 }  // namespace eagle
