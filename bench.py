@@ -62,6 +62,28 @@ def dist_env():
     return ws, rank, local
 
 
+def rank_seed(seed: int, rank: int) -> int:
+    """Seed of a rank's replica: ranks draw different (independent) sequences."""
+    return seed + 7919 * rank
+
+
+def max_over_ranks(ms: float, device=None) -> float:
+    """Largest timing over the ranks of the default process group (identity when
+    there is none); the slowest replica sets the whole-job time."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, steps: int, ms: float) -> float:
+    """Cycles per second of the whole job: every rank ran `steps` cycles in at most `ms`."""
+    return world * steps / (ms / 1e3)
+
+
 def workload(args):
     from synth import workloads as WL
     w = WL.WORKLOADS[args.workload]
@@ -326,7 +348,7 @@ def main():
     from speculative_decoding_dynamic_gb300 import cycle as C
     from speculative_decoding_dynamic_gb300 import eagle as E
 
-    seed = args.seed + 7919 * rank
+    seed = rank_seed(args.seed, rank)
     per_set = (w.depth * w.batch * w.top_k + w.batch * w.T) * w.vocab * w.esize
     prefix_len = w.prefix_lengths(seed)
     geo = WL.kv_geometry(w, seed, w.layers)
@@ -402,16 +424,13 @@ def main():
         graphs[i % R].replay()
     e1.record(stream)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
+    ms = max_over_ranks(e0.elapsed_time(e1), device="cuda")
     if ws_ > 1:
         import torch.distributed as dist
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
         dist.barrier()
     clocks = stop_clocks(clk) if clk else None
     ms_per_step = ms / args.steps
-    value = ws_ * args.steps / (ms / 1e3)
+    value = job_throughput(ws_, args.steps, ms)
 
     acc = dc.accept_len.cpu().numpy()
     n_tree = dc.n_tree.cpu().numpy()

@@ -69,6 +69,38 @@ __device__ __forceinline__ void unpack16(const uint4& u, float* x) {
     }
 }
 
+// Largest element of a 16-byte vector (NaN elements are ignored).
+template <int DT>
+__device__ __forceinline__ float vec_max(const uint4& u) {
+    if (DT == 1) {
+        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
+        const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&u.z);
+        const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&u.w);
+        const __nv_bfloat162 m = __hmax2(__hmax2(a, b), __hmax2(c, d));
+        return fmaxf(__low2float(m), __high2float(m));
+    } else {
+        return fmaxf(fmaxf(__uint_as_float(u.x), __uint_as_float(u.y)),
+                     fmaxf(__uint_as_float(u.z), __uint_as_float(u.w)));
+    }
+}
+
+// Descending bitonic sort of 32 unsigned values, one per lane.
+__device__ __forceinline__ uint32_t warp_sort_desc_u32(uint32_t v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int s = size >> 1; s > 0; s >>= 1) {
+            const uint32_t o = __shfl_xor_sync(0xffffffffu, v, s);
+            const bool desc = (lane & size) == 0;
+            const bool lower = (lane & s) == 0;
+            v = (lower == desc) ? max(o, v) : min(o, v);
+        }
+    }
+    return v;
+}
+
 // Issue the bulk copy of this CTA's chunk into `buf` and wait for it.
 __device__ __forceinline__ bool stage_chunk(void* buf, const char* row_base, const RowChunk& ch, int esize,
                                             uint64_t* bar, int* status) {
@@ -212,37 +244,40 @@ __global__ void __launch_bounds__(kRowThreads) expand_kernel(TreeDims d, TreeWs 
     const int nvec = ch.n / EPV;
     const int vpw = (nvec + kRowWarps - 1) / kRowWarps;
     const int v0 = warp * vpw, v1 = min(nvec, v0 + vpw);
+    // pass 1: lane maximum (packed compares for bf16)
     float lmax = -INFINITY;
-    int larg = -1;
+    bool lhas = false;
     for (int v = v0 + lane; v < v1; v += 32) {
-        float x[EPV];
-        unpack16<DT>(buf[v], x);
-#pragma unroll
-        for (int e = 0; e < EPV; ++e)
-            if (larg < 0 || x[e] > lmax) {
-                lmax = x[e];
-                larg = ch.c0 + v * EPV + e;
-            }
+        lmax = fmaxf(lmax, vec_max<DT>(buf[v]));
+        lhas = true;
     }
-    uint64_t lk[1] = {larg < 0 ? 0ull : make_key(lmax, static_cast<uint32_t>(larg))};
-    warp_sort_desc<1>(lk);
-    const uint64_t tau = shfl_u64(lk[0], k - 1);  // k-th largest lane maximum (0 if fewer)
-    const uint64_t wtopkey = shfl_u64(lk[0], 0);
-    const float wmax = wtopkey ? key_val(wtopkey) : -INFINITY;
+    // tau = k-th largest lane maximum: at least k elements of the part are
+    // >= tau, so its top-k all are (0 bits: fewer than k lanes with elements)
+    const uint32_t lo = warp_sort_desc_u32(lhas ? f2o(lmax) : 0u);
+    const uint32_t tau_o = __shfl_sync(0xffffffffu, lo, k - 1);
+    const uint32_t wmax_o = __shfl_sync(0xffffffffu, lo, 0);
+    const bool take_all = tau_o == 0u;
+    const float tau = o2f(tau_o);
+    const float wmax = wmax_o ? o2f(wmax_o) : -INFINITY;
+    // pass 2: exp-sum (fp32) and candidates >= tau
     float s = 0.0f;
     const bool do_sum = lse_in == nullptr && wmax > -INFINITY;
     const float mb = wmax * kLog2e;
     for (int v = v0 + lane; v < v1; v += 32) {
+        const uint4 u = buf[v];
         float x[EPV];
-        unpack16<DT>(buf[v], x);
+        unpack16<DT>(u, x);
+        if (do_sum) {
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-            if (do_sum) s += ex2_approx(fmaf(x[e], kLog2e, -mb));
-            const uint64_t key = make_key(x[e], static_cast<uint32_t>(ch.c0 + v * EPV + e));
-            if (key >= tau) {
-                const int at = atomicAdd(&sm.wcount[warp], 1);
-                if (at < kWarpCand) sm.wcand[warp][at] = key;
-            }
+            for (int e = 0; e < EPV; ++e) s += ex2_approx(fmaf(x[e], kLog2e, -mb));
+        }
+        if (take_all || vec_max<DT>(u) >= tau) {
+#pragma unroll
+            for (int e = 0; e < EPV; ++e)
+                if (take_all || x[e] >= tau) {
+                    const int at = atomicAdd(&sm.wcount[warp], 1);
+                    if (at < kWarpCand) sm.wcand[warp][at] = make_key(x[e], static_cast<uint32_t>(ch.c0 + v * EPV + e));
+                }
         }
     }
 #pragma unroll
@@ -492,14 +527,18 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
     float lmax = -INFINITY;
     int larg = -1;
     for (int v = v0 + lane; v < v1; v += 32) {
-        float x[EPV];
-        unpack16<DT>(buf[v], x);
+        const uint4 u = buf[v];
+        const float m8 = vec_max<DT>(u);
+        if (larg < 0 || m8 > lmax) {  // first element equal to the vector maximum: lowest id
+            float x[EPV];
+            unpack16<DT>(u, x);
+            int e0 = 0;
 #pragma unroll
-        for (int e = 0; e < EPV; ++e)
-            if (larg < 0 || x[e] > lmax) {
-                lmax = x[e];
-                larg = ch.c0 + v * EPV + e;
-            }
+            for (int e = EPV - 1; e >= 0; --e)
+                if (x[e] == m8) e0 = e;
+            lmax = m8;
+            larg = ch.c0 + v * EPV + e0;
+        }
     }
     uint64_t key = larg < 0 ? 0ull : make_key(lmax, static_cast<uint32_t>(larg));
     key = warp_max_u64(key);
