@@ -50,6 +50,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel-reps", type=int, default=100)
+    ap.add_argument("--layers", type=int, default=None, help="KV layers moved by compaction (memory cap)")
     return ap.parse_args()
 
 
@@ -92,6 +93,8 @@ def workload(args):
         kw["sharpness"] = args.sharpness
     if args.verify is not None:
         kw["verify"] = args.verify
+    if args.layers is not None:
+        kw["layers"] = args.layers
     return w.with_(**kw) if kw else w
 
 

@@ -38,6 +38,9 @@
  *     are undefined until eagle_status_fetch reports 0.
  *   - Rows of logits are contiguous; row starts must be 16-byte aligned
  *     (vocab * element size a multiple of 16, base pointer 16-byte aligned).
+ *     A row holds at most 512 KB (vocab <= 262144 in bf16, 131072 in fp32):
+ *     lossless verification keeps a whole row in the shared memory of one
+ *     thread-block cluster.
  *   - Calls on distinct workspaces may run concurrently.
  */
 #ifndef EAGLE_H_
@@ -222,9 +225,11 @@ int eagle_kv_compact(const eagle_kv_cfg* kv, void* kv_cache, const int32_t* pref
  * on the allocator). No counterpart on the pages: it is the same stage 6 as
  * eagle_verify, with the same arguments and results, minus ws/ws_bytes.
  *   - Its per-row scratch is one fixed device array inside the library
- *     (about 324 KB, present on every GPU that loads the library until the
- *     process exits). It supports batch <= 1024 and batch * (node_budget + 1)
- *     <= 4096 and returns EAGLE_ERR_UNSUPPORTED beyond that.
+ *     (about 4.3 MB, present on every GPU that loads the library until the
+ *     process exits). It supports batch <= 1024, batch * (node_budget + 1)
+ *     <= 4096 rows and rows * mass pieces <= 4096 * 128 (a row has 128
+ *     pieces at a 128256-entry bf16 vocabulary, 64 * ceil(vocab * element
+ *     size / 131072) in general) and returns EAGLE_ERR_UNSUPPORTED beyond.
  *   - The first call on a device looks up that array's device address; make
  *     that first call before any stream capture.
  *   - Every call uses the same array, so calls that overlap on the GPU (on

@@ -39,8 +39,8 @@ int resolve(const eagle_tree_cfg* cfg, TreeDims* d) {
     if (C > kMaxCandidates || T > kMaxSlots) return EAGLE_ERR_UNSUPPORTED;
     const int esize = cfg->logit_dtype == EAGLE_BF16 ? 2 : 4;
     if ((static_cast<long>(V) * esize) % 16 != 0) return EAGLE_ERR_UNSUPPORTED;
-    const RowSplit s = choose_row_split(V, esize);
-    if (s.smem_bytes > 160 * 1024) return EAGLE_ERR_UNSUPPORTED;
+    // lossless verification keeps a row resident over one cluster: V * esize <= 8 * 4 * 16 KB
+    if (row_chunks(row_seg_elems(V, esize, kMaxChunks), esize) > kRowStages) return EAGLE_ERR_UNSUPPORTED;
     if (static_cast<long>(B) * (T > k ? T : k) > 65535) return EAGLE_ERR_UNSUPPORTED;  // grid.y
     d->B = B;
     d->V = V;

@@ -141,6 +141,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
+// Bounded wait that lets the hardware suspend the thread (up to `hint_ns` per
+// poll, woken early when the phase completes) instead of spinning: for
+// waits that may be long, so that idle warps leave issue slots to the others.
+// Returns false after max_iter polls.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t max_iter = (1u << 16),
+                                                uint32_t hint_ns = 20000u) {
+    for (uint32_t i = 0; i < max_iter; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+            : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
 // Bulk (non-tensor) copy global -> this CTA's shared memory; completion is
 // signalled on `bar` as transaction bytes. Both addresses 16-byte aligned,
 // bytes a multiple of 16.

@@ -16,6 +16,27 @@ constexpr int kMaxSlots = 256;       // T = N + 1
 constexpr int kMaxCandidates = 1024;  // C = k + (D-1) k^2
 constexpr int kMaxChunks = 8;        // CTAs per logit row (one thread-block cluster)
 
+// Row kernels: a CTA's segment of a logit row moves through shared memory in
+// chunks of kRowChunkBytes (one bulk copy each), at most kRowStages chunks
+// resident at once; kRowWarpsPerCta consumer warps each own 1/8 of a chunk.
+constexpr int kRowChunkBytes = 16384;
+constexpr int kRowStages = 4;
+constexpr int kRowWarpsPerCta = 8;
+
+// Elements of a row segment when the row is split over `cpr` CTAs (a multiple
+// of 16 bytes, so every segment starts on a 16-byte boundary).
+inline int row_seg_elems(int V, int esize, int cpr) {
+    const int epv = 16 / esize;
+    const int seg = (V + cpr - 1) / cpr;
+    return (seg + epv - 1) / epv * epv;
+}
+inline int row_chunks(int seg, int esize) { return (seg * esize + kRowChunkBytes - 1) / kRowChunkBytes; }
+// Lossless verification keeps a row's segments resident (cpr = kMaxChunks) and
+// records one integer mass per (chunk, warp) piece of the row.
+inline int verify_mass_slots(int V, int esize) {
+    return kMaxChunks * row_chunks(row_seg_elems(V, esize, kMaxChunks), esize) * kRowWarpsPerCta;
+}
+
 // Resolved problem description passed by value to kernels.
 struct TreeDims {
     int B, V, k, D, N, T, W, C;
@@ -42,7 +63,7 @@ struct TreeWs {
     float* row_max;         // [B, T] verify row maximum
     int32_t* row_arg;       // [B, T] verify row argmax
     uint64_t* row_mass;     // [B, T] verify integer mass
-    uint64_t* chunk_mass;   // [B, T, kMaxChunks] verify integer mass per row chunk
+    uint64_t* chunk_mass;   // [B, T, verify_mass_slots] verify integer mass per row piece
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -75,18 +96,23 @@ inline size_t ws_layout(const TreeDims& d, void* base, TreeWs* ws) {
     w.row_max = static_cast<float*>(take(B * T * 4));
     w.row_arg = static_cast<int32_t*>(take(B * T * 4));
     w.row_mass = static_cast<uint64_t*>(take(B * T * 8));
-    w.chunk_mass = static_cast<uint64_t*>(take(B * T * kMaxChunks * 8));
+    w.chunk_mass = static_cast<uint64_t*>(take(B * T * verify_mass_slots(d.V, d.dtype == 1 ? 2 : 4) * 8));
     if (ws) *ws = w;
     return align_up(off, 256);
 }
 
-// How a logit row is split over a thread-block cluster.
-struct RowSplit {
-    int cpr;          // CTAs per row (cluster size), power of two <= kMaxChunks
-    int chunk;        // elements per CTA (multiple of 16 bytes), last CTA may get fewer
-    int smem_bytes;   // dynamic shared memory per CTA
+// How a logit row is split over a thread-block cluster and streamed.
+struct RowPlan {
+    int cpr;     // CTAs per row (cluster size), power of two <= kMaxChunks
+    int seg;     // elements per CTA (row_seg_elems); the last CTA may get fewer
+    int nch;     // chunks per full segment
+    int stages;  // shared-memory stages (all nch when the segment stays resident)
+    int smem;    // dynamic shared memory per CTA
+    int slots;   // integer-mass pieces per row (resident plans)
 };
-RowSplit choose_row_split(int V, int esize);
+// rows = logit rows of the launch; resident = the whole segment stays in
+// shared memory (needed by the second pass of lossless verification).
+RowPlan plan_rows(int V, int esize, long rows, bool resident);
 
 // ----------------------------------------------------------- launchers ---
 // Each returns cudaSuccess or the launch error. All enqueue on `stream`.

@@ -4,21 +4,30 @@
 //   verify_kernel  stage 6: per target row max/argmax (+ integer mass), then
 //                  (last row of a sequence) the acceptance walk.
 //
-// Layout of the work: one logit row is split over a thread-block cluster of
-// `cpr` CTAs. Each CTA stages its contiguous chunk of the row in shared memory
-// with one bulk asynchronous copy (TMA engine, completion on an mbarrier), so
-// HBM is read exactly once; each warp then owns a contiguous part of the
-// chunk and reduces it without block-wide barriers. Partial results are
-// pushed into the cluster leader's shared memory with remote stores before a
-// single cluster barrier. The per-sequence tail (frontier selection /
-// acceptance walk) runs in the cluster leader that arrives last on a
-// per-sequence ticket: an atomic add after a device-scope fence, no spin-wait.
+// Layout of the work. A logit row is split into `cpr` contiguous segments,
+// one per CTA of a thread-block cluster; cpr (1..8) is chosen per launch so
+// that the grid holds about two waves of CTAs. Each CTA runs eight consumer
+// warps and one producer warp. The producer streams the segment through a
+// ring of 16 KB shared-memory stages with bulk asynchronous copies (TMA
+// engine): a "full" mbarrier per stage counts the bytes, an "empty" mbarrier
+// counts the consumer warps that are done with it, so HBM is read once and
+// the copies of later chunks overlap the arithmetic on earlier ones. Within a
+// chunk every consumer warp owns 128 consecutive 16-byte vectors, four per
+// lane, and keeps its running statistics in registers across chunks.
 //
-// Top-k of a warp's part: with key = (value, -id) unique per element, let tau
-// be the k-th largest of the 32 lane maxima. The k lane maxima >= tau are k
-// distinct elements, so every element of the part's top-k has key >= tau; the
-// few elements >= tau are gathered and sorted. The union of the warps' top-k
-// contains the chunk's top-k, and so on up the cluster.
+// Expansion, one pass over the data: per lane a running maximum and a
+// rescaled exp-sum (online normaliser); per warp a buffer of top-k candidates
+// admitted by a key threshold tau. tau starts at the k-th largest lane
+// maximum of the first chunk (k distinct elements reach it, so every element
+// of the row's top-k does), is shared across the CTA through an atomic
+// maximum in shared memory, and rises to the k-th best buffered key whenever
+// a warp compacts its full buffer. Keys are (value, -id): unique, so ties go
+// to the lower token id. Warp, CTA and cluster results are merged by rank
+// selection (each key counts the keys above it). Partial results are pushed
+// into the cluster leader's shared memory before one cluster barrier. The
+// per-sequence tail (frontier selection / acceptance walk) runs in the
+// cluster leader that arrives last on a per-sequence ticket: an atomic add
+// after a device-scope fence, no spin-wait.
 //
 // Sources (page title and section): "EAGLE" notes (garden.houmin.site),
 // EAGLE 方法 (TopK drafting) and EAGLE 2 方法 (Expand, threshold);
@@ -30,7 +39,6 @@
 
 #include <algorithm>
 #include <cmath>
-#include <cstdio>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -40,17 +48,16 @@
 
 namespace eagle {
 
-constexpr int kRowThreads = 256;
-constexpr int kRowWarps = kRowThreads / 32;
-constexpr int kWarpCand = 64;
+constexpr int kConsumerWarps = kRowWarpsPerCta;
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kRowThreads = (kConsumerWarps + 1) * 32;
+constexpr int kVecPerLane = 4;
+constexpr int kVecPerWarp = 32 * kVecPerLane;
+static_assert(kVecPerWarp * kConsumerWarps * 16 == kRowChunkBytes, "chunk geometry");
+constexpr int kWarpCap = 64;  // candidate buffer per consumer warp
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ------------------------------------------------------------ helpers ---
-
-struct RowChunk {
-    int c0;  // first token id of this CTA's chunk
-    int n;   // tokens in the chunk (may be 0)
-};
 
 template <int DT>
 __device__ __forceinline__ void unpack16(const uint4& u, float* x) {
@@ -69,19 +76,39 @@ __device__ __forceinline__ void unpack16(const uint4& u, float* x) {
     }
 }
 
+// A vector of -inf elements (fills the lanes past the end of a chunk).
+template <int DT>
+__device__ __forceinline__ uint4 neg_inf_vec() {
+    const uint32_t w = DT == 1 ? 0xff80ff80u : 0xff800000u;
+    return make_uint4(w, w, w, w);
+}
+
+__device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t w) { return *reinterpret_cast<const __nv_bfloat162*>(&w); }
+
 // Largest element of a 16-byte vector (NaN elements are ignored).
 template <int DT>
 __device__ __forceinline__ float vec_max(const uint4& u) {
     if (DT == 1) {
-        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
-        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
-        const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&u.z);
-        const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&u.w);
-        const __nv_bfloat162 m = __hmax2(__hmax2(a, b), __hmax2(c, d));
+        const __nv_bfloat162 m = __hmax2(__hmax2(as_bf2(u.x), as_bf2(u.y)), __hmax2(as_bf2(u.z), as_bf2(u.w)));
         return fmaxf(__low2float(m), __high2float(m));
     } else {
         return fmaxf(fmaxf(__uint_as_float(u.x), __uint_as_float(u.y)),
                      fmaxf(__uint_as_float(u.z), __uint_as_float(u.w)));
+    }
+}
+
+// Largest element of a lane's four vectors (packed compares for bf16).
+template <int DT>
+__device__ __forceinline__ float lane_max4(const uint4 (&u)[kVecPerLane]) {
+    if (DT == 1) {
+        __nv_bfloat162 m[kVecPerLane];
+#pragma unroll
+        for (int j = 0; j < kVecPerLane; ++j)
+            m[j] = __hmax2(__hmax2(as_bf2(u[j].x), as_bf2(u[j].y)), __hmax2(as_bf2(u[j].z), as_bf2(u[j].w)));
+        const __nv_bfloat162 a = __hmax2(__hmax2(m[0], m[1]), __hmax2(m[2], m[3]));
+        return fmaxf(__low2float(a), __high2float(a));
+    } else {
+        return fmaxf(fmaxf(vec_max<DT>(u[0]), vec_max<DT>(u[1])), fmaxf(vec_max<DT>(u[2]), vec_max<DT>(u[3])));
     }
 }
 
@@ -101,31 +128,13 @@ __device__ __forceinline__ uint32_t warp_sort_desc_u32(uint32_t v) {
     return v;
 }
 
-// Issue the bulk copy of this CTA's chunk into `buf` and wait for it.
-__device__ __forceinline__ bool stage_chunk(void* buf, const char* row_base, const RowChunk& ch, int esize,
-                                            uint64_t* bar, int* status) {
-    const uint32_t bytes = static_cast<uint32_t>(ch.n) * esize;
-    if (threadIdx.x == 0) {
-        mbar_init(bar, 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-    if (bytes == 0) return true;
-    if (threadIdx.x == 0) {
-        mbar_arrive_expect_tx(bar, bytes);
-        bulk_g2s(buf, row_base + static_cast<size_t>(ch.c0) * esize, bytes, bar);
-    }
-    if (!mbar_wait(bar, 0)) {
-        raise_status(status, kDevTimeout);
-        return false;
-    }
-    return true;
-}
+__device__ __forceinline__ uint32_t shfl_xor_key(uint32_t v, int m) { return __shfl_xor_sync(0xffffffffu, v, m); }
+__device__ __forceinline__ uint64_t shfl_xor_key(uint64_t v, int m) { return shfl_xor_u64(v, m); }
 
 // Descending bitonic sort of 32*E keys held by one warp, E per lane
 // (element e = lane*E + j).
-template <int E>
-__device__ __forceinline__ void warp_sort_desc(uint64_t (&v)[E]) {
+template <int E, typename K>
+__device__ __forceinline__ void warp_sort_desc(K (&v)[E]) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int size = 2; size <= 32 * E; size <<= 1) {
@@ -138,7 +147,7 @@ __device__ __forceinline__ void warp_sort_desc(uint64_t (&v)[E]) {
                     if (pj > j) {
                         const int e = lane * E + j;
                         const bool desc = (e & size) == 0;
-                        const uint64_t a = v[j], c = v[pj];
+                        const K a = v[j], c = v[pj];
                         if ((a < c) == desc) {
                             v[j] = c;
                             v[pj] = a;
@@ -149,7 +158,7 @@ __device__ __forceinline__ void warp_sort_desc(uint64_t (&v)[E]) {
                 const int ls = s / E;
 #pragma unroll
                 for (int j = 0; j < E; ++j) {
-                    const uint64_t o = shfl_xor_u64(v[j], ls);
+                    const K o = shfl_xor_key(v[j], ls);
                     const int e = lane * E + j;
                     const bool desc = (e & size) == 0;
                     const bool lower = (e & s) == 0;
@@ -161,37 +170,107 @@ __device__ __forceinline__ void warp_sort_desc(uint64_t (&v)[E]) {
     }
 }
 
-// Top-k (k <= 16) of n <= 32*E keys in shared memory by one warp; writes
-// out[0..k), 0 = no key.
-template <int E>
-__device__ __forceinline__ void warp_topk_sorted(const uint64_t* keys, int n, int k, uint64_t* out) {
-    const int lane = threadIdx.x & 31;
-    uint64_t v[E];
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Rank of `key` among n lists of kMaxTopK keys (zeros = empty): how many
+// keys are larger. Every list is read whole (zero padding counts nothing).
+__device__ __forceinline__ int rank_in_lists(const uint64_t* lists, int n, uint64_t key) {
+    int r = 0;
+    for (int l = 0; l < n; ++l) {
+        const ulonglong2* p = reinterpret_cast<const ulonglong2*>(lists + l * kMaxTopK);
 #pragma unroll
-    for (int j = 0; j < E; ++j) {
-        const int e = lane * E + j;
-        v[j] = e < n ? keys[e] : 0ull;
+        for (int q = 0; q < kMaxTopK / 2; ++q) {
+            const ulonglong2 a = p[q];
+            r += (a.x > key) + (a.y > key);
+        }
     }
-    warp_sort_desc<E>(v);
-#pragma unroll
-    for (int j = 0; j < E; ++j) {
-        const int e = lane * E + j;
-        if (e < k) out[e] = v[j];
+    return r;
+}
+
+// --------------------------------------------------------- the chunk ring ---
+
+struct RowRing {
+    uint64_t full[kRowStages];
+    uint64_t empty[kRowStages];
+};
+
+__device__ __forceinline__ void ring_init(RowRing& r, int ns) {
+    for (int s = 0; s < ns; ++s) {
+        mbar_init(&r.full[s], 1);
+        mbar_init(&r.empty[s], kConsumerWarps);
     }
+    fence_mbar_init();
+}
+
+// Producer (one thread): chunk c of the segment goes to stage c % ns once the
+// consumers have released that stage's previous chunk.
+__device__ __forceinline__ void ring_produce(RowRing& r, unsigned char* stages, const char* src, int seg_bytes,
+                                             int nch, int ns, int* status) {
+    for (int c = 0; c < nch; ++c) {
+        const int s = c % ns;
+        if (c >= ns && !mbar_wait_sleep(&r.empty[s], ((c / ns) - 1) & 1)) {
+            raise_status(status, kDevTimeout);
+            return;
+        }
+        const uint32_t bytes = static_cast<uint32_t>(min(kRowChunkBytes, seg_bytes - c * kRowChunkBytes));
+        mbar_arrive_expect_tx(&r.full[s], bytes);
+        bulk_g2s(stages + s * kRowChunkBytes, src + static_cast<size_t>(c) * kRowChunkBytes, bytes, &r.full[s]);
+    }
+}
+
+// Consumer warp: wait (bounded) until chunk c has landed. After a first
+// timeout later waits are short, so a failed launch still ends promptly.
+__device__ __forceinline__ bool ring_wait(RowRing& r, int c, int ns, bool& failed, int* status) {
+    bool ok = mbar_wait_sleep(&r.full[c % ns], (c / ns) & 1, failed ? 16u : (1u << 16));
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) {
+        failed = true;
+        if ((threadIdx.x & 31) == 0) raise_status(status, kDevTimeout);
+    }
+    return ok;
+}
+
+// Consumer warp: done reading chunk c (its vectors are in registers).
+__device__ __forceinline__ void ring_release(RowRing& r, int c, int ns) {
     __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&r.empty[c % ns]);
+}
+
+// This lane's four vectors of a chunk (-inf past the end of the chunk).
+template <int DT>
+__device__ __forceinline__ void load_lane(const unsigned char* stage, int nvec, int warp, int lane,
+                                          uint4 (&u)[kVecPerLane]) {
+    const uint4* vb = reinterpret_cast<const uint4*>(stage) + warp * kVecPerWarp + lane;
+    if (nvec == kVecPerWarp * kConsumerWarps) {  // a full chunk
+#pragma unroll
+        for (int j = 0; j < kVecPerLane; ++j) u[j] = vb[j * 32];
+        return;
+    }
+#pragma unroll
+    for (int j = 0; j < kVecPerLane; ++j) {
+        const int v = warp * kVecPerWarp + j * 32 + lane;
+        u[j] = v < nvec ? vb[j * 32] : neg_inf_vec<DT>();
+    }
 }
 
 // ------------------------------------------------------------ expand kernel ---
 
 struct ExpandSmem {
-    uint64_t bar;
-    uint64_t wcand[kRowWarps][kWarpCand];
-    int wcount[kRowWarps];
-    uint64_t wtop[kRowWarps * kMaxTopK];
-    float wm[kRowWarps];
-    float ws[kRowWarps];
+    RowRing ring;
+    unsigned long long tau;  // CTA-wide admission key (atomic maximum)
+    alignas(16) uint64_t wbuf[kConsumerWarps][kWarpCap];
+    int wcnt[kConsumerWarps];           // keys appended to a warp's buffer (may pass kWarpCap)
+    uint64_t wtau[kConsumerWarps];      // a warp's admission key
+    uint32_t boot[kConsumerWarps][kMaxTopK];  // the k largest lane maxima of each warp, first chunk
+    float wm[kConsumerWarps];
+    float ws[kConsumerWarps];
+    uint64_t ctop[kMaxTopK];
     // filled by every CTA of the cluster in the leader's copy (remote stores)
-    uint64_t rtop[kMaxChunks * kMaxTopK];
+    alignas(16) uint64_t rtop[kMaxChunks * kMaxTopK];
     float rm[kMaxChunks];
     float rs[kMaxChunks];
     uint64_t top[kMaxTopK];
@@ -199,8 +278,94 @@ struct ExpandSmem {
     int last;
 };
 
+constexpr int kCompactAt = 40;  // compact a warp's buffer once it holds this many keys
+
+// The k largest keys of a warp's buffer, sorted, in buf[0..kMaxTopK) with
+// zeros past the k-th (the form the CTA merge reads). One sort of 32 keys.
+__device__ __forceinline__ void warp_final_small(uint64_t* buf, int cnt, int k) {
+    const int lane = threadIdx.x & 31;
+    uint64_t v[1] = {lane < cnt ? buf[lane] : 0ull};
+    warp_sort_desc<1>(v);
+    __syncwarp();
+    if (lane < kMaxTopK) buf[lane] = lane < k ? v[0] : 0ull;
+    __syncwarp();
+}
+
+// Keep the k largest keys of a warp's buffer, sorted, in buf[0..kMaxTopK)
+// (zeros past the k-th); raise the warp's admission key to the k-th when the
+// buffer held at least k, and publish it to the CTA. Called by a whole warp.
+__device__ __forceinline__ void warp_compact(uint64_t* buf, int* cnt_p, uint64_t* wtau, int k,
+                                          unsigned long long* tau_cta) {
+    const int lane = threadIdx.x & 31;
+    __syncwarp();
+    const int cnt = min(*cnt_p, kWarpCap);
+    uint64_t v[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int e = lane * 2 + j;
+        v[j] = e < cnt ? buf[e] : 0ull;
+    }
+    warp_sort_desc<2>(v);
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int e = lane * 2 + j;
+        if (e < kMaxTopK) buf[e] = e < k ? v[j] : 0ull;
+    }
+    if (cnt >= k) {
+        const uint64_t kth = shfl_u64(v[(k - 1) & 1], (k - 1) >> 1);
+        if (lane == 0) {
+            if (kth > *wtau) *wtau = kth;
+            if (tau_cta != nullptr) atomicMax(tau_cta, static_cast<unsigned long long>(*wtau));
+        }
+    }
+    if (lane == 0) *cnt_p = min(cnt, k);
+    __syncwarp();
+}
+
+// Exact admission of one chunk's elements when the fast path overflowed the
+// buffer (many keys at or above the admission key: ties, tiny rows): the
+// chunk's appends are discarded and its elements re-admitted one slice of 32
+// at a time, compacting whenever a slice might not fit. Called by a whole warp.
 template <int DT>
-__global__ void __launch_bounds__(kRowThreads) expand_kernel(TreeDims d, TreeWs w, int step, int chunk,
+__device__ __noinline__ void admit_exact(const unsigned char* stage, int nvec, int id0, int cnt_before,
+                                         uint64_t* buf, int* cnt_p, uint64_t* wtau, int k,
+                                         unsigned long long* tau_cta) {
+    constexpr int EPV = DT == 1 ? 8 : 4;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    __syncwarp();
+    if (lane == 0) *cnt_p = cnt_before;
+    warp_compact(buf, cnt_p, wtau, k, tau_cta);
+#pragma unroll 1
+    for (int j = 0; j < kVecPerLane; ++j) {
+        const int v = warp * kVecPerWarp + j * 32 + lane;
+        float x[EPV];
+        unpack16<DT>(v < nvec ? reinterpret_cast<const uint4*>(stage)[v] : neg_inf_vec<DT>(), x);
+#pragma unroll 1
+        for (int e = 0; e < EPV; ++e) {
+            const uint64_t tau = *wtau;
+            const uint64_t key = make_key(x[e], static_cast<uint32_t>(id0 + v * EPV + e));
+            bool p = v < nvec && x[e] == x[e] && key >= tau;
+            unsigned bal = __ballot_sync(0xffffffffu, p);
+            if (bal == 0u) continue;
+            if (*cnt_p + __popc(bal) > kWarpCap) {
+                warp_compact(buf, cnt_p, wtau, k, tau_cta);
+                p = p && key >= *wtau;
+                bal = __ballot_sync(0xffffffffu, p);
+            }
+            const int cnt = *cnt_p;
+            if (p) buf[cnt + __popc(bal & lanemask_lt())] = key;
+            __syncwarp();
+            if (lane == 0) *cnt_p = cnt + __popc(bal);
+            __syncwarp();
+        }
+    }
+}
+
+__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory"); }
+
+template <int DT>
+__global__ void __launch_bounds__(kRowThreads, 3) expand_kernel(TreeDims d, TreeWs w, int step, int seg, int ns,
                                                               const void* __restrict__ logits,
                                                               const float* __restrict__ lse_in,
                                                               float* __restrict__ row_lse,
@@ -219,6 +384,7 @@ __global__ void __launch_bounds__(kRowThreads) expand_kernel(TreeDims d, TreeWs 
     const int F = w.fcount[step * d.B + b];
     constexpr int ES = DT == 1 ? 2 : 4;
     constexpr int EPV = 16 / ES;
+    constexpr int CE = kRowChunkBytes / ES;  // elements per chunk
     const int k = d.k;
 
     if (f >= F) {  // this frontier slot holds no node in this step
@@ -232,142 +398,212 @@ __global__ void __launch_bounds__(kRowThreads) expand_kernel(TreeDims d, TreeWs 
         return;
     }
 
-    RowChunk ch;
-    ch.c0 = rank * chunk;
-    ch.n = max(0, min(chunk, d.V - ch.c0));
+    const int c0 = rank * seg;
+    const int n = max(0, min(seg, d.V - c0));
+    const int nch = (n * ES + kRowChunkBytes - 1) / kRowChunkBytes;
     const char* row_base = static_cast<const char*>(logits) + static_cast<size_t>(b * d.k + f) * d.V * ES;
-    const uint4* buf = reinterpret_cast<const uint4*>(dyn_smem);
-    if (tid < kRowWarps) sm.wcount[tid] = 0;
-    stage_chunk(dyn_smem, row_base, ch, ES, &sm.bar, w.status);
-
-    // ---- per warp: a contiguous part of the chunk ----
-    const int nvec = ch.n / EPV;
-    const int vpw = (nvec + kRowWarps - 1) / kRowWarps;
-    const int v0 = warp * vpw, v1 = min(nvec, v0 + vpw);
-    // pass 1: lane maximum (packed compares for bf16)
-    float lmax = -INFINITY;
-    bool lhas = false;
-    for (int v = v0 + lane; v < v1; v += 32) {
-        lmax = fmaxf(lmax, vec_max<DT>(buf[v]));
-        lhas = true;
+    if (tid == 0) {
+        ring_init(sm.ring, ns);
+        sm.tau = 0ull;
     }
-    // tau = k-th largest lane maximum: at least k elements of the part are
-    // >= tau, so its top-k all are (0 bits: fewer than k lanes with elements)
-    const uint32_t lo = warp_sort_desc_u32(lhas ? f2o(lmax) : 0u);
-    const uint32_t tau_o = __shfl_sync(0xffffffffu, lo, k - 1);
-    const uint32_t wmax_o = __shfl_sync(0xffffffffu, lo, 0);
-    const bool take_all = tau_o == 0u;
-    const float tau = o2f(tau_o);
-    const float wmax = wmax_o ? o2f(wmax_o) : -INFINITY;
-    // pass 2: exp-sum (fp32) and candidates >= tau
-    float s = 0.0f;
-    const bool do_sum = lse_in == nullptr && wmax > -INFINITY;
-    const float mb = wmax * kLog2e;
-    for (int v = v0 + lane; v < v1; v += 32) {
-        const uint4 u = buf[v];
-        float x[EPV];
-        unpack16<DT>(u, x);
-        if (do_sum) {
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) s += ex2_approx(fmaf(x[e], kLog2e, -mb));
-        }
-        if (take_all || vec_max<DT>(u) >= tau) {
-#pragma unroll
-            for (int e = 0; e < EPV; ++e)
-                if (take_all || x[e] >= tau) {
-                    const int at = atomicAdd(&sm.wcount[warp], 1);
-                    if (at < kWarpCand) sm.wcand[warp][at] = make_key(x[e], static_cast<uint32_t>(ch.c0 + v * EPV + e));
-                }
-        }
-    }
-#pragma unroll
-    for (int m = 16; m > 0; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
-    __syncwarp();
-    const int cnt = sm.wcount[warp];
-    if (cnt <= kWarpCand) {
-        warp_topk_sorted<2>(sm.wcand[warp], cnt, k, &sm.wtop[warp * kMaxTopK]);
-    } else {
-        // Many equal values at the top: k exact rounds over the warp's part.
-        uint64_t prev = ~0ull;
-        for (int r = 0; r < k; ++r) {
-            uint64_t best = 0;
-            for (int v = v0 + lane; v < v1; v += 32) {
-                float x[EPV];
-                unpack16<DT>(buf[v], x);
-#pragma unroll
-                for (int e = 0; e < EPV; ++e) {
-                    const uint64_t key = make_key(x[e], static_cast<uint32_t>(ch.c0 + v * EPV + e));
-                    if (key < prev && key > best) best = key;
-                }
-            }
-            best = warp_max_u64(best);
-            if (lane == 0) sm.wtop[warp * kMaxTopK + r] = best;
-            prev = best;
-        }
-        __syncwarp();
-    }
-    if (lane == 0) {
-        sm.wm[warp] = wmax;
-        sm.ws[warp] = s;
+    if (tid < kMaxTopK) {
+        sm.ctop[tid] = 0ull;
+        sm.top[tid] = 0ull;
     }
     __syncthreads();
 
-    // ---- CTA: merge the warps, push to the cluster leader ----
-    ExpandSmem* leader = cluster.map_shared_rank(&sm, 0);
-    if (warp == 0) {
-        // the 8 warps' top-k: k <= 16, so 8 * 16 = 128 slots, 4 per lane
-        uint64_t v[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int e = lane * 4 + j;  // e = warp_index * 16 + r
-            const int wi = e >> 4, r = e & 15;
-            v[j] = r < k ? sm.wtop[wi * kMaxTopK + r] : 0ull;
+    if (warp == kProducerWarp) {
+        if (lane == 0 && nch > 0)
+            ring_produce(sm.ring, dyn_smem, row_base + static_cast<size_t>(c0) * ES, n * ES, nch, ns, w.status);
+        __syncwarp();
+    } else {
+        const bool do_sum = lse_in == nullptr;
+        float m_l = -INFINITY, s_l = 0.0f;  // lane: running max and sum of exp(x - m_l)
+        uint64_t tau = 0ull;                // warp: admission key (0 = admit all)
+        bool failed = false;
+        uint64_t* buf = sm.wbuf[warp];
+        if (lane == 0) {
+            sm.wcnt[warp] = 0;
+            sm.wtau[warp] = 0ull;
         }
-        warp_sort_desc<4>(v);
+        __syncwarp();
+        if (nch > 0) {
+            // tau from the k-th largest of the CTA's lane maxima over the first
+            // chunk: k distinct elements reach it, so every element of the
+            // row's top-k does. Warp 0 selects it from the warps' k largest.
+            const bool ok0 = ring_wait(sm.ring, 0, ns, failed, w.status);
+            uint4 u[kVecPerLane];
+            load_lane<DT>(dyn_smem, ok0 ? min(CE, n) / EPV : 0, warp, lane, u);
+            const float cm = lane_max4<DT>(u);
+            const uint32_t lo = warp_sort_desc_u32(cm > -INFINITY ? f2o(cm) : 0u);
+            if (lane < k) sm.boot[warp][lane] = lo;
+            consumer_bar();
+            if (warp == 0) {
+                uint32_t bv[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int e = lane * 4 + j;
-            if (e < k) leader->rtop[rank * kMaxTopK + e] = v[j];
+                for (int j = 0; j < 4; ++j) {
+                    const int e = lane * 4 + j;
+                    bv[j] = e < kConsumerWarps * k ? sm.boot[e / k][e % k] : 0u;
+                }
+                warp_sort_desc<4>(bv);
+                const uint32_t kth = __shfl_sync(0xffffffffu, bv[(k - 1) & 3], (k - 1) >> 2);
+                if (lane == 0) sm.tau = kth != 0u ? static_cast<unsigned long long>(kth) << 32 : 0ull;
+            }
+            consumer_bar();
+            tau = sm.tau;
+            if (lane == 0) sm.wtau[warp] = tau;
+        }
+        for (int c = 0; c < nch; ++c) {
+            const bool ok = c == 0 ? !failed : ring_wait(sm.ring, c, ns, failed, w.status);
+            const int nvec = ok ? min(CE, n - c * CE) / EPV : 0;
+            const unsigned char* stage = dyn_smem + (c % ns) * kRowChunkBytes;
+            uint4 u[kVecPerLane];
+            load_lane<DT>(stage, nvec, warp, lane, u);
+            const float cm = lane_max4<DT>(u);
+            if (c > 0) {
+                const uint64_t t2 = *reinterpret_cast<volatile unsigned long long*>(&sm.tau);
+                if (t2 > tau) tau = t2;
+            }
+            if (!ok) {
+                ring_release(sm.ring, c, ns);
+                continue;
+            }
+            if (do_sum) {
+                if (cm > m_l) {
+                    s_l = m_l > -INFINITY ? s_l * ex2_approx((m_l - cm) * kLog2e) : 0.0f;
+                    m_l = cm;
+                }
+                if (m_l > -INFINITY) {
+                    const float mb = m_l * kLog2e;
+                    float sa = 0.0f, sb = 0.0f;
+#pragma unroll
+                    for (int j = 0; j < kVecPerLane; ++j) {
+                        float x[EPV];
+                        unpack16<DT>(u[j], x);
+#pragma unroll
+                        for (int e = 0; e < EPV; e += 2) {
+                            sa += ex2_approx(fmaf(x[e], kLog2e, -mb));
+                            sb += ex2_approx(fmaf(x[e + 1], kLog2e, -mb));
+                        }
+                    }
+                    s_l += sa + sb;
+                }
+            }
+            // candidates: keys >= tau, appended lane by lane
+            const bool take_all = tau == 0ull;
+            const float tv = key_val(tau);
+            const bool lane_hot = take_all || cm >= tv;
+            if (__any_sync(0xffffffffu, lane_hot)) {
+                const int id0 = c0 + c * CE;
+                const int cnt_before = sm.wcnt[warp];
+                __syncwarp();
+                if (lane_hot) {
+#pragma unroll
+                    for (int j = 0; j < kVecPerLane; ++j) {
+                        const int v = warp * kVecPerWarp + j * 32 + lane;
+                        if (v >= nvec || !(take_all || vec_max<DT>(u[j]) >= tv)) continue;
+                        float x[EPV];
+                        unpack16<DT>(u[j], x);
+#pragma unroll
+                        for (int e = 0; e < EPV; ++e) {
+                            if (!(take_all || x[e] >= tv)) continue;  // NaN fails too
+                            const uint64_t key = make_key(x[e], static_cast<uint32_t>(id0 + v * EPV + e));
+                            if (x[e] == x[e] && key >= tau) {
+                                const int at = atomicAdd(&sm.wcnt[warp], 1);
+                                if (at < kWarpCap) buf[at] = key;
+                            }
+                        }
+                    }
+                }
+                __syncwarp();
+                const int cnt = *reinterpret_cast<volatile int*>(&sm.wcnt[warp]);
+                if (cnt >= kCompactAt && lane == 0) sm.wtau[warp] = tau;
+                if (cnt > kWarpCap) {
+                    admit_exact<DT>(stage, nvec, id0, cnt_before, buf, &sm.wcnt[warp], &sm.wtau[warp], k, &sm.tau);
+                    tau = sm.wtau[warp];
+                } else if (cnt >= kCompactAt) {
+                    warp_compact(buf, &sm.wcnt[warp], &sm.wtau[warp], k, &sm.tau);
+                    tau = sm.wtau[warp];
+                }
+            }
+            ring_release(sm.ring, c, ns);
+        }
+        // the warp's top-k, sorted, in buf[0..kMaxTopK) (zeros past the k-th)
+        const int cnt_end = sm.wcnt[warp];
+        __syncwarp();
+        if (cnt_end <= 32)
+            warp_final_small(buf, cnt_end, k);
+        else
+            warp_compact(buf, &sm.wcnt[warp], &sm.wtau[warp], k, nullptr);
+        // the warp's (max, sum)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float mo = __shfl_xor_sync(0xffffffffu, m_l, o);
+            const float so = __shfl_xor_sync(0xffffffffu, s_l, o);
+            const float M = fmaxf(m_l, mo);
+            float s = 0.0f;
+            if (m_l > -INFINITY) s += s_l * ex2_approx((m_l - M) * kLog2e);
+            if (mo > -INFINITY) s += so * ex2_approx((mo - M) * kLog2e);
+            m_l = M;
+            s_l = s;
         }
         if (lane == 0) {
-            float M = -INFINITY;
-            for (int i = 0; i < kRowWarps; ++i) M = fmaxf(M, sm.wm[i]);
-            float S = 0.0f;
-            if (M > -INFINITY)
-                for (int i = 0; i < kRowWarps; ++i)
-                    if (sm.wm[i] > -INFINITY) S += sm.ws[i] * ex2_approx((sm.wm[i] - M) * kLog2e);
-            leader->rm[rank] = M;
-            leader->rs[rank] = S;
+            sm.wm[warp] = m_l;
+            sm.ws[warp] = s_l;
         }
+    }
+    __syncthreads();
+
+    // ---- CTA: merge the warps' lists, push to the cluster leader ----
+    if (tid < kConsumerWarps * k) {
+        const uint64_t key = sm.wbuf[tid / k][tid % k];
+        if (key != 0ull) {
+            int r = 0;
+#pragma unroll
+            for (int wi = 0; wi < kConsumerWarps; ++wi) {
+                const ulonglong2* p = reinterpret_cast<const ulonglong2*>(sm.wbuf[wi]);
+#pragma unroll
+                for (int q = 0; q < kMaxTopK / 2; ++q) {
+                    const ulonglong2 a = p[q];
+                    r += (a.x > key) + (a.y > key);
+                }
+            }
+            if (r < k) sm.ctop[r] = key;
+        }
+    }
+    __syncthreads();
+    ExpandSmem* leader = cluster.map_shared_rank(&sm, 0);
+    if (tid < kMaxTopK) leader->rtop[rank * kMaxTopK + tid] = sm.ctop[tid];
+    if (tid == 0) {
+        float M = -INFINITY;
+        for (int i = 0; i < kConsumerWarps; ++i) M = fmaxf(M, sm.wm[i]);
+        float S = 0.0f;
+        if (M > -INFINITY)
+            for (int i = 0; i < kConsumerWarps; ++i)
+                if (sm.wm[i] > -INFINITY) S += sm.ws[i] * ex2_approx((sm.wm[i] - M) * kLog2e);
+        leader->rm[rank] = M;
+        leader->rs[rank] = S;
     }
     cluster.sync();
     if (rank != 0) return;
 
     // ---- leader: row top-k and lse ----
-    if (warp == 0) {
-        uint64_t v[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int e = lane * 4 + j;  // e = rank_index * 16 + r
-            const int ri = e >> 4, r = e & 15;
-            v[j] = (ri < cpr && r < k) ? sm.rtop[ri * kMaxTopK + r] : 0ull;
+    if (tid < cpr * k) {
+        const uint64_t key = sm.rtop[(tid / k) * kMaxTopK + tid % k];
+        if (key != 0ull) {
+            const int r = rank_in_lists(sm.rtop, cpr, key);
+            if (r < k) sm.top[r] = key;
         }
-        warp_sort_desc<4>(v);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int e = lane * 4 + j;
-            if (e < k) sm.top[e] = v[j];
-        }
-        if (lane == 0) {
-            float M = -INFINITY;
-            for (int r = 0; r < cpr; ++r) M = fmaxf(M, sm.rm[r]);
-            float S = 0.0f;
-            if (M > -INFINITY)
-                for (int r = 0; r < cpr; ++r)
-                    if (sm.rm[r] > -INFINITY) S += sm.rs[r] * ex2_approx((sm.rm[r] - M) * kLog2e);
-            sm.wm[0] = M;
-            sm.ws[0] = S;
-        }
+    }
+    if (tid == kRowThreads - 1) {
+        float M = -INFINITY;
+        for (int r = 0; r < cpr; ++r) M = fmaxf(M, sm.rm[r]);
+        float S = 0.0f;
+        if (M > -INFINITY)
+            for (int r = 0; r < cpr; ++r)
+                if (sm.rm[r] > -INFINITY) S += sm.rs[r] * ex2_approx((sm.rm[r] - M) * kLog2e);
+        sm.wm[0] = M;
+        sm.ws[0] = S;
     }
     __syncthreads();
 
@@ -405,30 +641,36 @@ __global__ void __launch_bounds__(kRowThreads) expand_kernel(TreeDims d, TreeWs 
     __syncthreads();
     if (!sm.last) return;
     __threadfence();
-    if (warp == 0) {
-        const int n = F * d.k;
-        for (int i = lane; i < n; i += 32) {
-            const int id = base + i;
-            const size_t at = static_cast<size_t>(b) * d.C + id;
-            const bool valid = __ldcg(reinterpret_cast<const unsigned char*>(&w.cand_valid[at])) != 0;
-            const float lv = __ldcg(&w.cand_logv[at]);
-            sm.sel[i] = (valid && lv >= d.log_thr) ? make_key(lv, static_cast<uint32_t>(id)) : 0ull;
-        }
-        __syncwarp();
-        warp_topk_smem(sm.sel, n, d.k, sm.top);
+    const int nsel = F * d.k;
+    for (int i = tid; i < nsel; i += kRowThreads) {
+        const int id = base + i;
+        const size_t at = static_cast<size_t>(b) * d.C + id;
+        const bool valid = __ldcg(reinterpret_cast<const unsigned char*>(&w.cand_valid[at])) != 0;
+        const float lv = __ldcg(&w.cand_logv[at]);
+        sm.sel[i] = (valid && lv >= d.log_thr) ? make_key(lv, static_cast<uint32_t>(id)) : 0ull;
+    }
+    if (tid < kMaxTopK) sm.top[tid] = 0ull;
+    __syncthreads();
+    for (int i = tid; i < nsel; i += kRowThreads) {
+        const uint64_t key = sm.sel[i];
+        if (key == 0ull) continue;
+        int r = 0;
+        for (int j = 0; j < nsel; ++j) r += sm.sel[j] > key;
+        if (r < d.k) sm.top[r] = key;
+    }
+    __syncthreads();
+    if (tid < d.k) {
+        const uint64_t key = sm.top[tid];
+        const int id = key ? static_cast<int>(key_id(key)) : -1;
+        w.fnode[((step + 1) * d.B + b) * d.k + tid] = id;
+        ftok_out[b * d.k + tid] = id >= 0 ? __ldcg(&w.cand_token[static_cast<size_t>(b) * d.C + id]) : -1;
+    }
+    if (tid == 0) {
         int cnt = 0;
-        for (int j = 0; j < d.k; ++j) cnt += sm.top[j] != 0;
-        if (lane < d.k) {
-            const uint64_t key = sm.top[lane];
-            const int id = key ? static_cast<int>(key_id(key)) : -1;
-            w.fnode[((step + 1) * d.B + b) * d.k + lane] = id;
-            ftok_out[b * d.k + lane] = id >= 0 ? __ldcg(&w.cand_token[static_cast<size_t>(b) * d.C + id]) : -1;
-        }
-        if (lane == 0) {
-            w.fcount[(step + 1) * d.B + b] = cnt;
-            fcount_out[b] = cnt;
-            w.expand_ticket[b] = 0;
-        }
+        for (int j = 0; j < d.k; ++j) cnt += sm.top[j] != 0ull;
+        w.fcount[(step + 1) * d.B + b] = cnt;
+        fcount_out[b] = cnt;
+        w.expand_ticket[b] = 0;
     }
 }
 
@@ -462,13 +704,17 @@ __device__ __forceinline__ uint64_t fixed_mass(float x, float m, float inv_t) {
 }
 
 struct VerifySmem {
-    uint64_t bar;
-    uint64_t wkey[kRowWarps];
-    uint64_t wmass[kRowWarps];
-    uint64_t rkey[kMaxChunks];   // every rank's chunk maximum (pushed to every rank)
-    uint64_t rmass[kMaxChunks];  // every rank's chunk mass (pushed to the leader)
+    RowRing ring;
+    uint64_t wkey[kConsumerWarps];
+    unsigned long long wmass[kConsumerWarps];
+    uint64_t rkey[kMaxChunks];   // every rank's segment maximum
+    uint64_t rmass[kMaxChunks];  // every rank's segment mass (pushed to the leader)
     int last;
-    // walk state (last-arriving CTA of a sequence)
+};
+
+// Acceptance-walk state of the last-arriving CTA of a sequence; it lives in
+// the (then idle) dynamic shared memory of the chunk ring.
+struct WalkSmem {
     int tok[kMaxSlots];
     int par[kMaxSlots];
     int arg[kMaxSlots];
@@ -477,16 +723,30 @@ struct VerifySmem {
     unsigned long long pmass[kMaxSlots];  // mass of slot c's token in its parent's row
     uint32_t uni[kMaxSlots + 2];
     int path[kMaxDepth + 1];
-    int removed_tok[kMaxSlots];
-    unsigned long long removed_mass[kMaxSlots];
-    unsigned long long wscan[kRowWarps];
-    int n_removed, a, cur, sample_chunk, bonus, bad, found;
-    unsigned long long sample_t;
+    int child[kMaxTopK];
+    int removed_tok[kMaxTopK];
+    unsigned long long removed_mass[kMaxTopK];
+    unsigned long long scan[4];
+    unsigned long long t_in;
+    int n_removed, a, cur, bonus, bad, piece;
 };
 
-template <int DT>
-__global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs w, int mode, float inv_t, int chunk,
-                                                              const void* __restrict__ target,
+// Element range [lo, hi) of integer-mass piece q of a row: piece (rank, chunk,
+// warp) of a resident plan with `nch` chunks per segment of `seg` elements.
+__device__ __forceinline__ void piece_range(int q, int nch, int seg, int V, int CE, int EPV, int& lo, int& hi) {
+    const int r = q / (nch * kConsumerWarps);
+    const int c = (q / kConsumerWarps) % nch;
+    const int wq = q % kConsumerWarps;
+    const int s_end = min(V, (r + 1) * seg);
+    const int cs = r * seg + c * CE;
+    const int ce = min(cs + CE, s_end);
+    lo = cs + wq * kVecPerWarp * EPV;
+    hi = max(lo, min(lo + kVecPerWarp * EPV, ce));
+}
+
+template <int DT, int MODE>
+__global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs w, float inv_t, int seg, int ns,
+                                                              int nslot, const void* __restrict__ target,
                                                               const int32_t* __restrict__ tokens,
                                                               const int32_t* __restrict__ parent,
                                                               const int32_t* __restrict__ n_tree,
@@ -504,6 +764,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int ES = DT == 1 ? 2 : 4;
     constexpr int EPV = 16 / ES;
+    constexpr int CE = kRowChunkBytes / ES;
     pdl_launch_dependents();
     pdl_wait_prior();
     const int n = n_tree[b];
@@ -513,73 +774,107 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
     }
     if (t >= n) return;
 
-    RowChunk ch;
-    ch.c0 = rank * chunk;
-    ch.n = max(0, min(chunk, d.V - ch.c0));
+    const int c0 = rank * seg;
+    const int len = max(0, min(seg, d.V - c0));
+    const int nch = (len * ES + kRowChunkBytes - 1) / kRowChunkBytes;
     const char* row_base = static_cast<const char*>(target) + static_cast<size_t>(b * d.T + t) * d.V * ES;
-    const uint4* buf = reinterpret_cast<const uint4*>(dyn_smem);
-    stage_chunk(dyn_smem, row_base, ch, ES, &sm.bar, w.status);
+    if (tid == 0) ring_init(sm.ring, ns);
+    __syncthreads();
 
-    // ---- pass 1: maximum (lowest id among equal values) ----
-    const int nvec = ch.n / EPV;
-    const int vpw = (nvec + kRowWarps - 1) / kRowWarps;
-    const int v0 = warp * vpw, v1 = min(nvec, v0 + vpw);
-    float lmax = -INFINITY;
-    int larg = -1;
-    for (int v = v0 + lane; v < v1; v += 32) {
-        const uint4 u = buf[v];
-        const float m8 = vec_max<DT>(u);
-        if (larg < 0 || m8 > lmax) {  // first element equal to the vector maximum: lowest id
-            float x[EPV];
-            unpack16<DT>(u, x);
-            int e0 = 0;
+    bool failed = false;
+    if (warp == kProducerWarp) {
+        if (lane == 0 && nch > 0)
+            ring_produce(sm.ring, dyn_smem, row_base + static_cast<size_t>(c0) * ES, len * ES, nch, ns, w.status);
+        __syncwarp();
+    } else {
+        // ---- pass 1: maximum, lowest id among equal values ----
+        float lm = -INFINITY;
+        int larg = -1;
+        for (int c = 0; c < nch; ++c) {
+            if (!ring_wait(sm.ring, c, ns, failed, w.status)) {
+                ring_release(sm.ring, c, ns);
+                continue;
+            }
+            const int nvec = min(CE, len - c * CE) / EPV;
+            uint4 u[kVecPerLane];
+            load_lane<DT>(dyn_smem + (c % ns) * kRowChunkBytes, nvec, warp, lane, u);
+            ring_release(sm.ring, c, ns);
+            if (larg >= 0 && !(lane_max4<DT>(u) > lm)) continue;  // nothing above the lane maximum
 #pragma unroll
-            for (int e = EPV - 1; e >= 0; --e)
-                if (x[e] == m8) e0 = e;
-            lmax = m8;
-            larg = ch.c0 + v * EPV + e0;
+            for (int j = 0; j < kVecPerLane; ++j) {
+                const int v = warp * kVecPerWarp + j * 32 + lane;
+                if (v >= nvec) continue;
+                const float m8 = vec_max<DT>(u[j]);
+                if (larg < 0 || m8 > lm) {  // first element equal to the vector maximum: lowest id
+                    float x[EPV];
+                    unpack16<DT>(u[j], x);
+                    int e0 = 0;
+#pragma unroll
+                    for (int e = EPV - 1; e >= 0; --e)
+                        if (x[e] == m8) e0 = e;
+                    lm = m8;
+                    larg = c0 + c * CE + v * EPV + e0;
+                }
+            }
         }
+        uint64_t key = larg < 0 ? 0ull : make_key(lm, static_cast<uint32_t>(larg));
+        key = warp_max_u64(key);
+        if (lane == 0) sm.wkey[warp] = key;
     }
-    uint64_t key = larg < 0 ? 0ull : make_key(lmax, static_cast<uint32_t>(larg));
-    key = warp_max_u64(key);
-    if (lane == 0) sm.wkey[warp] = key;
     __syncthreads();
     if (warp == 0) {
-        uint64_t m = lane < kRowWarps ? sm.wkey[lane] : 0ull;
+        uint64_t m = lane < kConsumerWarps ? sm.wkey[lane] : 0ull;
         m = warp_max_u64(m);
-        if (lane < cpr) cluster.map_shared_rank(&sm, lane)->rkey[rank] = m;  // to every rank
+        if (MODE == 1) {
+            if (lane < cpr) cluster.map_shared_rank(&sm, lane)->rkey[rank] = m;  // to every rank
+        } else if (lane == 0) {
+            cluster.map_shared_rank(&sm, 0)->rkey[rank] = m;
+        }
     }
     cluster.sync();
+    if (MODE == 0 && rank != 0) return;
     uint64_t gkey = 0;
     for (int r = 0; r < cpr; ++r) gkey = sm.rkey[r] > gkey ? sm.rkey[r] : gkey;
     const float M = key_val(gkey);
     const size_t rt = static_cast<size_t>(b) * d.T + t;
-    if (mode == 1) {
-        // ---- pass 2: integer mass of the chunk ----
-        uint64_t s = 0;
-        for (int v = v0 + lane; v < v1; v += 32) {
-            float x[EPV];
-            unpack16<DT>(buf[v], x);
+    if (MODE == 1) {
+        // ---- pass 2: integer masses of the resident segment, one per (chunk, warp) ----
+        const int nch_full = nslot / (cpr * kConsumerWarps);
+        unsigned long long wtot = 0;
+        if (warp < kConsumerWarps) {
+            for (int c = 0; c < nch_full; ++c) {
+                unsigned long long s = 0;
+                if (c < nch && !failed) {
+                    const int nvec = min(CE, len - c * CE) / EPV;
+                    const uint4* vb = reinterpret_cast<const uint4*>(dyn_smem + c * kRowChunkBytes);
 #pragma unroll
-            for (int e = 0; e < EPV; ++e) s += fixed_mass(x[e], M, inv_t);
-        }
-        s = warp_sum_u64(s);
-        if (lane == 0) sm.wmass[warp] = s;
-        __syncthreads();
-        if (warp == 0) {
-            uint64_t tot = lane < kRowWarps ? sm.wmass[lane] : 0ull;
-            tot = warp_sum_u64(tot);
-            if (lane == 0) {
-                w.chunk_mass[rt * kMaxChunks + rank] = tot;
-                cluster.map_shared_rank(&sm, 0)->rmass[rank] = tot;
+                    for (int j = 0; j < kVecPerLane; ++j) {
+                        const int v = warp * kVecPerWarp + j * 32 + lane;
+                        if (v >= nvec) continue;
+                        float x[EPV];
+                        unpack16<DT>(vb[v], x);
+#pragma unroll
+                        for (int e = 0; e < EPV; ++e) s += fixed_mass(x[e], M, inv_t);
+                    }
+                }
+                s = warp_sum_u64(s);
+                if (lane == 0) w.chunk_mass[rt * nslot + (rank * nch_full + c) * kConsumerWarps + warp] = s;
+                wtot += s;
             }
+            if (lane == 0) sm.wmass[warp] = wtot;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            unsigned long long tot = 0;
+            for (int i = 0; i < kConsumerWarps; ++i) tot += sm.wmass[i];
+            cluster.map_shared_rank(&sm, 0)->rmass[rank] = tot;
         }
         cluster.sync();
+        if (rank != 0) return;
     }
-    if (rank != 0) return;
     if (tid == 0) {
         uint64_t mass = 0;
-        if (mode == 1)
+        if (MODE == 1)
             for (int r = 0; r < cpr; ++r) mass += sm.rmass[r];
         w.row_max[rt] = M;
         w.row_arg[rt] = static_cast<int32_t>(key_id(gkey));
@@ -594,218 +889,252 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
     __threadfence();
 
     // ---- acceptance walk for sequence b (one CTA) ----
+    WalkSmem& ws = *reinterpret_cast<WalkSmem*>(dyn_smem);
     const int T = d.T;
-    if (tid == 0) sm.bad = 0;
+    if (tid == 0) {
+        ws.bad = 0;
+        ws.piece = -1;
+        ws.n_removed = 0;
+    }
     for (int c = tid; c < T; c += kRowThreads) {
-        sm.tok[c] = c < n ? tokens[static_cast<size_t>(b) * T + c] : -1;
-        sm.par[c] = c < n ? parent[static_cast<size_t>(b) * T + c] : -1;
+        ws.tok[c] = c < n ? tokens[static_cast<size_t>(b) * T + c] : -1;
+        ws.par[c] = c < n ? parent[static_cast<size_t>(b) * T + c] : -1;
         if (c < n) {
-            sm.arg[c] = __ldcg(&w.row_arg[static_cast<size_t>(b) * T + c]);
-            sm.rmax[c] = __ldcg(&w.row_max[static_cast<size_t>(b) * T + c]);
-            sm.rowmass[c] = __ldcg(&w.row_mass[static_cast<size_t>(b) * T + c]);
+            ws.arg[c] = __ldcg(&w.row_arg[static_cast<size_t>(b) * T + c]);
+            ws.rmax[c] = __ldcg(&w.row_max[static_cast<size_t>(b) * T + c]);
+            ws.rowmass[c] = __ldcg(&w.row_mass[static_cast<size_t>(b) * T + c]);
         }
     }
-    // chunk masses of every row of the sequence, in the (now idle) chunk buffer
-    unsigned long long* cmass = reinterpret_cast<unsigned long long*>(dyn_smem);
-    if (mode == 1) {
-        for (int c = tid; c < T + 2; c += kRowThreads) sm.uni[c] = uniforms[static_cast<size_t>(b) * (T + 2) + c];
-        for (int q = tid; q < n * cpr; q += kRowThreads)
-            cmass[q] = __ldcg(&w.chunk_mass[(static_cast<size_t>(b) * T + q / cpr) * kMaxChunks + q % cpr]);
-    }
+    if (MODE == 1)
+        for (int c = tid; c < T + 2; c += kRowThreads) ws.uni[c] = uniforms[static_cast<size_t>(b) * (T + 2) + c];
     __syncthreads();
     for (int c = 1 + tid; c < n; c += kRowThreads) {
-        const int tk = sm.tok[c], p = sm.par[c];
-        sm.pmass[c] = 0;
+        const int tk = ws.tok[c], p = ws.par[c];
+        ws.pmass[c] = 0;
         if (tk < 0 || tk >= d.V || p < 0 || p >= c) {
-            sm.bad = 1;
+            ws.bad = 1;
             continue;
         }
-        if (mode == 1) {
+        if (MODE == 1) {
             const char* prow = static_cast<const char*>(target) + (static_cast<size_t>(b) * T + p) * d.V * ES;
             float x;
             if (DT == 1)
                 x = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(prow)[tk]) << 16);
             else
                 x = reinterpret_cast<const float*>(prow)[tk];
-            sm.pmass[c] = fixed_mass(x, sm.rmax[p], inv_t);
+            ws.pmass[c] = fixed_mass(x, ws.rmax[p], inv_t);
         }
     }
     __syncthreads();
-    if (tid == 0 && sm.bad) raise_status(w.status, kDevBadIndex);
+    const bool bad = ws.bad != 0;
+    if (tid == 0 && bad) raise_status(w.status, kDevBadIndex);
 
-    if (tid == 0) {
+    if (warp == 0) {
+        // One warp walks the tree; at each node its children (contiguous in
+        // slot order) are tested together, lane j on child j.
         int cur = 0, a = 0;
-        sm.path[0] = 0;
-        sm.n_removed = 0;
-        unsigned long long S = mode == 1 ? sm.rowmass[0] : 0ull;
-        for (;;) {
+        unsigned long long S = MODE == 1 ? ws.rowmass[0] : 0ull;
+        if (lane == 0) ws.path[0] = 0;
+        while (a < d.D && !bad) {
+            int nchild = 0;
+            for (int c0w = cur + 1; c0w < n; c0w += 32) {
+                const int c = c0w + lane;
+                const bool is = c < n && ws.par[c] == cur;
+                const unsigned bal = __ballot_sync(0xffffffffu, is);
+                if (is) {
+                    const int pos = nchild + __popc(bal & lanemask_lt());
+                    if (pos < kMaxTopK) ws.child[pos] = c;
+                }
+                nchild += __popc(bal);
+            }
+            __syncwarp();
+            nchild = min(nchild, kMaxTopK);
+            if (nchild == 0) break;
+            const int c = lane < nchild ? ws.child[lane] : -1;
             int next = -1;
-            if (a < d.D) {
-                for (int c = cur + 1; c < n; ++c) {
-                    if (sm.par[c] != cur) continue;
-                    if (mode == 0) {
-                        if (sm.tok[c] == sm.arg[cur]) {
-                            next = c;
-                            break;
-                        }
-                    } else {
-                        const unsigned __int128 lhs = static_cast<unsigned __int128>(sm.uni[c] >> 8) * S;
-                        const unsigned __int128 rhs = static_cast<unsigned __int128>(sm.pmass[c]) << 24;
-                        if (lhs < rhs) {
-                            next = c;
-                            break;
-                        }
-                        S -= sm.pmass[c];
-                        sm.removed_tok[sm.n_removed] = sm.tok[c];
-                        sm.removed_mass[sm.n_removed] = sm.pmass[c];
-                        sm.n_removed++;
+            if (MODE == 0) {
+                const unsigned bal = __ballot_sync(0xffffffffu, c >= 0 && ws.tok[c] == ws.arg[cur]);
+                if (bal) next = ws.child[__ffs(bal) - 1];
+            } else {
+                const unsigned long long P = c >= 0 ? ws.pmass[c] : 0ull;
+                unsigned long long incl = P;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned long long y = shfl_u64(incl, max(lane - o, 0));
+                    if (lane >= o) incl += y;
+                }
+                const unsigned long long Sj = S - (incl - P);  // after the earlier children's removal
+                const bool acc = c >= 0 && static_cast<unsigned __int128>(ws.uni[c] >> 8) * Sj <
+                                               (static_cast<unsigned __int128>(P) << 24);
+                const unsigned bal = __ballot_sync(0xffffffffu, acc);
+                if (bal) {
+                    next = ws.child[__ffs(bal) - 1];
+                } else {
+                    S -= shfl_u64(incl, 31);  // every child rejected: their tokens leave the residual
+                    if (c >= 0) {
+                        ws.removed_tok[lane] = ws.tok[c];
+                        ws.removed_mass[lane] = P;
                     }
+                    if (lane == 0) ws.n_removed = nchild;
                 }
             }
             if (next < 0) break;
-            sm.path[++a] = next;
+            ++a;
+            if (lane == 0) ws.path[a] = next;
             cur = next;
-            if (mode == 1) {
-                S = sm.rowmass[cur];
-                sm.n_removed = 0;
-            }
+            if (MODE == 1) S = ws.rowmass[cur];
         }
-        sm.a = a;
-        sm.cur = cur;
-        sm.bonus = mode == 0 ? sm.arg[cur] : -1;
-        if (mode == 1) {
-            // choose the chunk of row `cur` that holds the draw
-            const uint64_t U64 = (static_cast<uint64_t>(sm.uni[T + 1]) << 32) | sm.uni[T];
+        __syncwarp();
+        if (lane == 0) {
+            ws.a = a;
+            ws.cur = cur;
+            ws.bonus = MODE == 0 ? ws.arg[cur] : -1;
+        }
+        if (MODE == 1 && !bad) {
+            // the piece of row `cur` that holds the draw t = floor(U64 * S / 2^64)
+            const uint64_t U64 = (static_cast<uint64_t>(ws.uni[T + 1]) << 32) | ws.uni[T];
             const unsigned long long tdraw =
                 static_cast<unsigned long long>((static_cast<unsigned __int128>(U64) * S) >> 64);
-            unsigned long long run = 0;
-            int chosen = cpr - 1;
-            unsigned long long tin = 0;
-            for (int r = 0; r < cpr; ++r) {
-                unsigned long long cm = cmass[cur * cpr + r];
-                const int lo = r * chunk, hi = min(d.V, lo + chunk);
-                for (int q = 0; q < sm.n_removed; ++q)
-                    if (sm.removed_tok[q] >= lo && sm.removed_tok[q] < hi) cm -= sm.removed_mass[q];
-                if (run + cm > tdraw) {
-                    chosen = r;
-                    tin = tdraw - run;
-                    break;
-                }
-                run += cm;
+            const int nrem = ws.n_removed;
+            const int nch_full = nslot / (cpr * kConsumerWarps);
+            const uint64_t* pm = w.chunk_mass + (static_cast<size_t>(b) * T + cur) * nslot;
+            const int per = (nslot + 31) / 32;
+            auto piece_mass = [&](int q) -> unsigned long long {
+                unsigned long long m = __ldcg(pm + q);
+                int lo, hi;
+                piece_range(q, nch_full, seg, d.V, CE, EPV, lo, hi);
+                for (int r = 0; r < nrem; ++r)
+                    if (ws.removed_tok[r] >= lo && ws.removed_tok[r] < hi) m -= ws.removed_mass[r];
+                return m;
+            };
+            unsigned long long loc = 0;
+            for (int i = 0; i < per; ++i) {
+                const int q = lane * per + i;
+                if (q < nslot) loc += piece_mass(q);
             }
-            sm.sample_chunk = chosen;
-            sm.sample_t = tin;
+            unsigned long long incl = loc;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long y = shfl_u64(incl, max(lane - o, 0));
+                if (lane >= o) incl += y;
+            }
+            unsigned long long run = incl - loc;
+            if (loc > 0 && run <= tdraw && tdraw < run + loc) {
+                for (int i = 0; i < per; ++i) {
+                    const int q = lane * per + i;
+                    if (q >= nslot) break;
+                    const unsigned long long m = piece_mass(q);
+                    if (run + m > tdraw) {
+                        ws.piece = q;
+                        ws.t_in = tdraw - run;
+                        break;
+                    }
+                    run += m;
+                }
+            }
         }
     }
     __syncthreads();
 
-    if (mode == 1) {
-        // Smallest y (not removed) of the chosen chunk of row `cur` whose
-        // running mass exceeds the draw. The chunk is staged in shared memory
-        // (second phase of the CTA's mbarrier) and walked in id order in
-        // rounds of 256 vectors, one vector per thread, with a block scan per
-        // round.
-        const int cur = sm.cur;
-        const int lo = sm.sample_chunk * chunk, hi = min(d.V, lo + chunk);
-        const int len = max(0, hi - lo);
-        const char* crow = static_cast<const char*>(target) + (static_cast<size_t>(b) * T + cur) * d.V * ES;
-        fence_proxy_async_smem();  // earlier generic reads of the buffer before the async-proxy rewrite
-        __syncthreads();
-        if (tid == 0) {
-            sm.found = 0;
-            if (len > 0) {
-                mbar_arrive_expect_tx(&sm.bar, static_cast<uint32_t>(len) * ES);
-                bulk_g2s(dyn_smem, crow + static_cast<size_t>(lo) * ES, static_cast<uint32_t>(len) * ES, &sm.bar);
+    if (MODE == 1) {
+        // Smallest y of the chosen piece (not removed) whose running mass
+        // exceeds the draw: one 16-byte vector per thread, block scan.
+        const int q = ws.piece;
+        const int cur = ws.cur;
+        const int nch_full = nslot / (cpr * kConsumerWarps);
+        int lo = 0, hi = 0;
+        if (q >= 0) piece_range(q, nch_full, seg, d.V, CE, EPV, lo, hi);
+        const int nrem = ws.n_removed;
+        const float m = ws.rmax[cur];
+        unsigned long long em[EPV];
+        unsigned long long mv = 0;
+        const int y0 = lo + tid * EPV;
+        if (tid < kVecPerWarp && y0 < hi) {
+            const char* crow = static_cast<const char*>(target) + (static_cast<size_t>(b) * T + cur) * d.V * ES;
+            const uint4 u = __ldcg(reinterpret_cast<const uint4*>(crow + static_cast<size_t>(y0) * ES));
+            float x[EPV];
+            unpack16<DT>(u, x);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) {
+                em[e] = fixed_mass(x[e], m, inv_t);
+                for (int r = 0; r < nrem; ++r)
+                    if (ws.removed_tok[r] == y0 + e) em[e] = 0;
+                mv += em[e];
             }
         }
-        if (len > 0 && !mbar_wait(&sm.bar, 1)) raise_status(w.status, kDevTimeout);
+        unsigned long long incl = mv;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = shfl_u64(incl, max(lane - o, 0));
+            if (lane >= o) incl += y;
+        }
+        if (warp < 4 && lane == 31) ws.scan[warp] = incl;
         __syncthreads();
-        const float m = sm.rmax[cur];
-        const int nrem = sm.n_removed;
-        const int nv = len / EPV;
-        unsigned long long tin = sm.sample_t;
-        for (int base = 0; base < nv; base += kRowThreads) {
-            const int v = base + tid;
-            unsigned long long em[EPV];
-            unsigned long long mv = 0;
-            if (v < nv) {
-                float x[EPV];
-                unpack16<DT>(buf[v], x);
-                const int y0 = lo + v * EPV;
-                bool has_removed = false;
-                for (int q = 0; q < nrem; ++q)
-                    has_removed |= static_cast<unsigned>(sm.removed_tok[q] - y0) < static_cast<unsigned>(EPV);
-#pragma unroll
-                for (int e = 0; e < EPV; ++e) {
-                    em[e] = fixed_mass(x[e], m, inv_t);
-                    if (has_removed)
-                        for (int q = 0; q < nrem; ++q)
-                            if (sm.removed_tok[q] == y0 + e) em[e] = 0;
-                    mv += em[e];
-                }
-            }
-            // block exclusive scan of mv
-            unsigned long long incl = mv;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t lo32 = __shfl_up_sync(0xffffffffu, static_cast<uint32_t>(incl), o);
-                const uint32_t hi32 = __shfl_up_sync(0xffffffffu, static_cast<uint32_t>(incl >> 32), o);
-                if (lane >= o) incl += (static_cast<unsigned long long>(hi32) << 32) | lo32;
-            }
-            if (lane == 31) sm.wscan[warp] = incl;
-            __syncthreads();
-            unsigned long long wbase = 0, total = 0;
-            for (int i = 0; i < kRowWarps; ++i) {
-                if (i < warp) wbase += sm.wscan[i];
-                total += sm.wscan[i];
-            }
-            const unsigned long long ex = wbase + incl - mv;
+        if (tid < kVecPerWarp && q >= 0) {
+            unsigned long long ex = incl - mv;
+            for (int i = 0; i < warp; ++i) ex += ws.scan[i];
+            const unsigned long long tin = ws.t_in;
             if (mv > 0 && ex <= tin && tin < ex + mv) {
                 unsigned long long run = ex;
 #pragma unroll
                 for (int e = 0; e < EPV; ++e) {
                     run += em[e];
                     if (run > tin) {
-                        sm.bonus = lo + v * EPV + e;
+                        ws.bonus = y0 + e;
                         break;
                     }
                 }
-                sm.found = 1;
             }
-            __syncthreads();
-            if (sm.found) break;
-            tin -= total;
         }
         __syncthreads();
     }
 
     if (tid == 0) {
-        const int a = sm.a;
+        const int a = ws.a;
         const int Dp1 = d.D + 1;
         accept_len[b] = a;
         for (int j = 0; j < Dp1; ++j) {
-            slots_out[b * Dp1 + j] = j <= a ? sm.path[j] : -1;
-            tokens_out[b * Dp1 + j] = j < a ? sm.tok[sm.path[j + 1]] : (j == a ? sm.bonus : -1);
+            slots_out[b * Dp1 + j] = j <= a ? ws.path[j] : -1;
+            tokens_out[b * Dp1 + j] = j < a ? ws.tok[ws.path[j + 1]] : (j == a ? ws.bonus : -1);
         }
-        if (sm.bonus < 0) raise_status(w.status, kDevBadIndex);
+        if (ws.bonus < 0) raise_status(w.status, kDevBadIndex);
         w.verify_ticket[b] = 0;
     }
 }
 
 // -------------------------------------------------------------- launchers ---
 
-RowSplit choose_row_split(int V, int esize) {
-    RowSplit s;
-    const long row_bytes = static_cast<long>(V) * esize;
-    int cpr = 1;
-    while (cpr < kMaxChunks && row_bytes > static_cast<long>(cpr) * 32 * 1024) cpr *= 2;
-    const int epv = 16 / esize;
-    int chunk = (V + cpr - 1) / cpr;
-    chunk = (chunk + epv - 1) / epv * epv;
-    s.cpr = cpr;
-    s.chunk = chunk;
-    s.smem_bytes = static_cast<int>(align_up(static_cast<size_t>(chunk) * esize, 128));
-    return s;
+static int sm_count() {
+    static std::mutex mu;
+    static std::map<int, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(dev);
+    if (it != cache.end()) return it->second;
+    int n = 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+    cache[dev] = n;
+    return n;
+}
+
+RowPlan plan_rows(int V, int esize, long rows, bool resident) {
+    int cpr = kMaxChunks;
+    if (!resident) {
+        // about two waves of CTAs (three resident per SM with a 4-stage ring)
+        const long target = 2L * 3 * sm_count();
+        cpr = 1;
+        while (cpr < kMaxChunks && rows * cpr < target) cpr *= 2;
+    }
+    RowPlan p;
+    p.cpr = cpr;
+    p.seg = row_seg_elems(V, esize, cpr);
+    p.nch = row_chunks(p.seg, esize);
+    p.stages = resident ? p.nch : std::min(p.nch, kRowStages);
+    p.smem = p.nch <= 1 ? static_cast<int>(align_up(static_cast<size_t>(p.seg) * esize, 128))
+                        : p.stages * kRowChunkBytes;
+    p.slots = cpr * p.nch * kConsumerWarps;
+    return p;
 }
 
 cudaError_t ensure_dyn_smem(const void* kernel, int smem) {
@@ -847,33 +1176,36 @@ static cudaError_t launch_rows(K kernel, dim3 grid, int cpr, int smem, cudaStrea
 
 cudaError_t launch_expand(const TreeDims& d, const TreeWs& ws, int step, const void* logits, const float* lse_in,
                           float* row_lse, int32_t* ftok, int32_t* fcount_out, cudaStream_t stream) {
-    const RowSplit s = choose_row_split(d.V, d.dtype == 1 ? 2 : 4);
-    dim3 grid(s.cpr, d.B * d.k, 1);
+    const RowPlan p = plan_rows(d.V, d.dtype == 1 ? 2 : 4, static_cast<long>(d.B) * d.k, false);
+    dim3 grid(p.cpr, d.B * d.k, 1);
     TreeDims dd = d;
     TreeWs ww = ws;
-    int chunk = s.chunk;
-    void* args[] = {&dd,      &ww,   &step,       &chunk, const_cast<void**>(&logits), const_cast<float**>(&lse_in),
+    int seg = p.seg, ns = p.stages;
+    void* args[] = {&dd,   &ww, &step, &seg, &ns, const_cast<void**>(&logits), const_cast<float**>(&lse_in),
                     &row_lse, &ftok, &fcount_out};
-    return d.dtype == 1 ? launch_rows(expand_kernel<1>, grid, s.cpr, s.smem_bytes, stream, args)
-                        : launch_rows(expand_kernel<0>, grid, s.cpr, s.smem_bytes, stream, args);
+    return d.dtype == 1 ? launch_rows(expand_kernel<1>, grid, p.cpr, p.smem, stream, args)
+                        : launch_rows(expand_kernel<0>, grid, p.cpr, p.smem, stream, args);
 }
 
 cudaError_t launch_verify(const TreeDims& d, const TreeWs& ws, int mode, float inv_temp, const void* target,
                           const int32_t* tokens, const int32_t* parent, const int32_t* n_tree,
                           const uint32_t* uniforms, int32_t* accept_len, int32_t* slots, int32_t* out_tokens,
                           cudaStream_t stream) {
-    const RowSplit s = choose_row_split(d.V, d.dtype == 1 ? 2 : 4);
-    dim3 grid(s.cpr, d.B * d.T, 1);
-    // the acceptance walk keeps the chunk masses of all T rows in the chunk buffer
-    const int smem = static_cast<int>(std::max<size_t>(s.smem_bytes, align_up(static_cast<size_t>(d.T) * s.cpr * 8, 128)));
+    const int esize = d.dtype == 1 ? 2 : 4;
+    const RowPlan p = plan_rows(d.V, esize, static_cast<long>(d.B) * d.T, mode == 1);
+    if (mode == 1 && p.stages > kRowStages) return cudaErrorInvalidValue;
+    dim3 grid(p.cpr, d.B * d.T, 1);
+    // the acceptance walk keeps its state in the (then idle) stage memory
+    const int smem = static_cast<int>(std::max<size_t>(p.smem, align_up(sizeof(WalkSmem), 128)));
     TreeDims dd = d;
     TreeWs ww = ws;
-    int chunk = s.chunk;
+    int seg = p.seg, ns = p.stages, nslot = mode == 1 ? p.slots : 0;
     void* args[] = {&dd,
                     &ww,
-                    &mode,
                     &inv_temp,
-                    &chunk,
+                    &seg,
+                    &ns,
+                    &nslot,
                     const_cast<void**>(&target),
                     const_cast<int32_t**>(&tokens),
                     const_cast<int32_t**>(&parent),
@@ -882,8 +1214,11 @@ cudaError_t launch_verify(const TreeDims& d, const TreeWs& ws, int mode, float i
                     &accept_len,
                     &slots,
                     &out_tokens};
-    return d.dtype == 1 ? launch_rows(verify_kernel<1>, grid, s.cpr, smem, stream, args)
-                        : launch_rows(verify_kernel<0>, grid, s.cpr, smem, stream, args);
+    if (d.dtype == 1)
+        return mode == 1 ? launch_rows(verify_kernel<1, 1>, grid, p.cpr, smem, stream, args)
+                         : launch_rows(verify_kernel<1, 0>, grid, p.cpr, smem, stream, args);
+    return mode == 1 ? launch_rows(verify_kernel<0, 1>, grid, p.cpr, smem, stream, args)
+                     : launch_rows(verify_kernel<0, 0>, grid, p.cpr, smem, stream, args);
 }
 
 }  // namespace eagle

@@ -27,6 +27,9 @@ namespace {
 
 constexpr int kMaxRows = 4096;  // batch * T
 constexpr int kMaxSeqs = 1024;  // batch
+// integer-mass pieces of lossless verification: rows * verify_mass_slots(V)
+// (128 per row at a 128256-entry bf16 vocabulary)
+constexpr size_t kMaxPieces = static_cast<size_t>(kMaxRows) * 128;
 
 // Byte offsets inside the fixed scratch array.
 constexpr size_t kOffStatus = 0;
@@ -35,7 +38,7 @@ constexpr size_t kOffRowMax = kOffTicket + kMaxSeqs * sizeof(int);
 constexpr size_t kOffRowArg = kOffRowMax + kMaxRows * sizeof(float);
 constexpr size_t kOffRowMass = kOffRowArg + kMaxRows * sizeof(int32_t);
 constexpr size_t kOffChunkMass = kOffRowMass + kMaxRows * sizeof(uint64_t);
-constexpr size_t kScratchBytes = kOffChunkMass + static_cast<size_t>(kMaxRows) * kMaxChunks * sizeof(uint64_t);
+constexpr size_t kScratchBytes = kOffChunkMass + kMaxPieces * sizeof(uint64_t);
 
 static __device__ __align__(256) unsigned char g_verify_scratch[kScratchBytes];
 
@@ -76,6 +79,8 @@ extern "C" int eagle_verify_static(const eagle_tree_cfg* cfg, int mode, float te
     if (eagle_workspace_bytes(cfg) == 0) return EAGLE_ERR_INVALID_ARG;
     const long rows = static_cast<long>(cfg->batch) * (cfg->node_budget + 1);
     if (cfg->batch > kMaxSeqs || rows > kMaxRows) return EAGLE_ERR_UNSUPPORTED;  // beyond the fixed scratch
+    const int esize = cfg->logit_dtype == EAGLE_BF16 ? 2 : 4;
+    if (static_cast<size_t>(rows) * verify_mass_slots(cfg->vocab, esize) > kMaxPieces) return EAGLE_ERR_UNSUPPORTED;
     if (mode != EAGLE_VERIFY_GREEDY && mode != EAGLE_VERIFY_LOSSLESS) return EAGLE_ERR_INVALID_ARG;
     if (!target_logits || !tokens || !parent || !n_tree || !accept_len || !accepted_slots || !out_tokens)
         return EAGLE_ERR_INVALID_ARG;
