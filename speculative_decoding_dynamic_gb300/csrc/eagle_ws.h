@@ -112,7 +112,7 @@ struct RowPlan {
 };
 // rows = logit rows of the launch; resident = the whole segment stays in
 // shared memory (needed by the second pass of lossless verification).
-RowPlan plan_rows(int V, int esize, long rows, bool resident);
+RowPlan plan_rows(int V, int esize, long rows, bool resident, int max_stages, int max_seg_chunks);
 
 // ----------------------------------------------------------- launchers ---
 // Each returns cudaSuccess or the launch error. All enqueue on `stream`.

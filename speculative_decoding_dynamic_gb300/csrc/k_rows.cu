@@ -54,7 +54,9 @@ constexpr int kRowThreads = (kConsumerWarps + 1) * 32;
 constexpr int kVecPerLane = 4;
 constexpr int kVecPerWarp = 32 * kVecPerLane;
 static_assert(kVecPerWarp * kConsumerWarps * 16 == kRowChunkBytes, "chunk geometry");
-constexpr int kWarpCap = 64;  // candidate buffer per consumer warp
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kMaxSegChunks = 8;  // chunks of one CTA's row segment in expansion
+constexpr int kExpandStages = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ------------------------------------------------------------ helpers ---
@@ -259,13 +261,14 @@ __device__ __forceinline__ void load_lane(const unsigned char* stage, int nvec, 
 
 // ------------------------------------------------------------ expand kernel ---
 
+// Barrier of the eight consumer warps only (the producer warp keeps streaming).
+__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
+
 struct ExpandSmem {
     RowRing ring;
-    unsigned long long tau;  // CTA-wide admission key (atomic maximum)
-    alignas(16) uint64_t wbuf[kConsumerWarps][kWarpCap];
-    int wcnt[kConsumerWarps];           // keys appended to a warp's buffer (may pass kWarpCap)
-    uint64_t wtau[kConsumerWarps];      // a warp's admission key
-    uint32_t boot[kConsumerWarps][kMaxTopK];  // the k largest lane maxima of each warp, first chunk
+    unsigned long long tau;                       // segment admission key (atomic maximum)
+    uint32_t gmax[kMaxSegChunks][kConsumers];     // maximum of each lane group (ordered bits)
+    int ngroups, nkeys;
     float wm[kConsumerWarps];
     float ws[kConsumerWarps];
     uint64_t ctop[kMaxTopK];
@@ -274,103 +277,108 @@ struct ExpandSmem {
     float rm[kMaxChunks];
     float rs[kMaxChunks];
     uint64_t top[kMaxTopK];
-    uint64_t sel[kMaxTopK * kMaxTopK];
     int last;
 };
 
-constexpr int kCompactAt = 40;  // compact a warp's buffer once it holds this many keys
-
-// The k largest keys of a warp's buffer, sorted, in buf[0..kMaxTopK) with
-// zeros past the k-th (the form the CTA merge reads). One sort of 32 keys.
-__device__ __forceinline__ void warp_final_small(uint64_t* buf, int cnt, int k) {
-    const int lane = threadIdx.x & 31;
-    uint64_t v[1] = {lane < cnt ? buf[lane] : 0ull};
-    warp_sort_desc<1>(v);
-    __syncwarp();
-    if (lane < kMaxTopK) buf[lane] = lane < k ? v[0] : 0ull;
-    __syncwarp();
-}
-
-// Keep the k largest keys of a warp's buffer, sorted, in buf[0..kMaxTopK)
-// (zeros past the k-th); raise the warp's admission key to the k-th when the
-// buffer held at least k, and publish it to the CTA. Called by a whole warp.
-__device__ __forceinline__ void warp_compact(uint64_t* buf, int* cnt_p, uint64_t* wtau, int k,
-                                          unsigned long long* tau_cta) {
-    const int lane = threadIdx.x & 31;
-    __syncwarp();
-    const int cnt = min(*cnt_p, kWarpCap);
-    uint64_t v[2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const int e = lane * 2 + j;
-        v[j] = e < cnt ? buf[e] : 0ull;
-    }
-    warp_sort_desc<2>(v);
-    __syncwarp();
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const int e = lane * 2 + j;
-        if (e < kMaxTopK) buf[e] = e < k ? v[j] : 0ull;
-    }
-    if (cnt >= k) {
-        const uint64_t kth = shfl_u64(v[(k - 1) & 1], (k - 1) >> 1);
-        if (lane == 0) {
-            if (kth > *wtau) *wtau = kth;
-            if (tau_cta != nullptr) atomicMax(tau_cta, static_cast<unsigned long long>(*wtau));
-        }
-    }
-    if (lane == 0) *cnt_p = min(cnt, k);
-    __syncwarp();
-}
-
-// Exact admission of one chunk's elements when the fast path overflowed the
-// buffer (many keys at or above the admission key: ties, tiny rows): the
-// chunk's appends are discarded and its elements re-admitted one slice of 32
-// at a time, compacting whenever a slice might not fit. Called by a whole warp.
+// Top-k keys of a CTA's row segment, after the streaming pass (consumer
+// threads only). A lane group is one lane's four vectors of one chunk, and
+// gmax holds each group's maximum. tau = the largest, over the warps, of the
+// warp's k-th largest lane maximum of the whole segment: k distinct elements
+// reach it, so every element of the segment's top-k does, and lies in a group
+// whose maximum reaches it. Those groups are read again (from L2: the row was
+// just streamed), their elements >= tau collected, and the k largest keys
+// found by rank selection into ctop. When the keys do not fit the scratch
+// (many equal values at the top), k block-wide rounds over the candidate
+// groups pick the keys one by one instead.
 template <int DT>
-__device__ __noinline__ void admit_exact(const unsigned char* stage, int nvec, int id0, int cnt_before,
-                                         uint64_t* buf, int* cnt_p, uint64_t* wtau, int k,
-                                         unsigned long long* tau_cta) {
-    constexpr int EPV = DT == 1 ? 8 : 4;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    __syncwarp();
-    if (lane == 0) *cnt_p = cnt_before;
-    warp_compact(buf, cnt_p, wtau, k, tau_cta);
-#pragma unroll 1
-    for (int j = 0; j < kVecPerLane; ++j) {
-        const int v = warp * kVecPerWarp + j * 32 + lane;
-        float x[EPV];
-        unpack16<DT>(v < nvec ? reinterpret_cast<const uint4*>(stage)[v] : neg_inf_vec<DT>(), x);
-#pragma unroll 1
-        for (int e = 0; e < EPV; ++e) {
-            const uint64_t tau = *wtau;
-            const uint64_t key = make_key(x[e], static_cast<uint32_t>(id0 + v * EPV + e));
-            bool p = v < nvec && x[e] == x[e] && key >= tau;
-            unsigned bal = __ballot_sync(0xffffffffu, p);
-            if (bal == 0u) continue;
-            if (*cnt_p + __popc(bal) > kWarpCap) {
-                warp_compact(buf, cnt_p, wtau, k, tau_cta);
-                p = p && key >= *wtau;
-                bal = __ballot_sync(0xffffffffu, p);
-            }
-            const int cnt = *cnt_p;
-            if (p) buf[cnt + __popc(bal & lanemask_lt())] = key;
-            __syncwarp();
-            if (lane == 0) *cnt_p = cnt + __popc(bal);
-            __syncwarp();
+__device__ __noinline__ void segment_topk(ExpandSmem& sm, unsigned char* scratch, int scratch_bytes,
+                                          const char* row_base, int c0, int n, int nch, int k) {
+    constexpr int ES = DT == 1 ? 2 : 4;
+    constexpr int EPV = 16 / ES;
+    constexpr int CE = kRowChunkBytes / ES;
+    constexpr int kGroupElems = kVecPerLane * EPV;
+    const int tid = threadIdx.x;
+    const uint64_t tau = sm.tau;
+    const float tv = key_val(tau);
+    const bool all = tau == 0ull;
+    const uint32_t tau_o = static_cast<uint32_t>(tau >> 32);
+    uint32_t* glist = reinterpret_cast<uint32_t*>(scratch);
+    const int gcap = nch * kConsumers;
+    uint64_t* keys = reinterpret_cast<uint64_t*>(scratch + gcap * sizeof(uint32_t));
+    const int kcap = (scratch_bytes - gcap * static_cast<int>(sizeof(uint32_t))) / static_cast<int>(sizeof(uint64_t));
+    // candidate groups
+    for (int q = tid; q < nch * kConsumers; q += kConsumers) {
+        const uint32_t gm = sm.gmax[q / kConsumers][q % kConsumers];
+        if (gm != 0u && (all || gm >= tau_o)) glist[atomicAdd(&sm.ngroups, 1)] = static_cast<uint32_t>(q);
+    }
+    consumer_bar();
+    const int ng = sm.ngroups;
+    auto group_elem = [&](uint32_t q, int i, float& x, int& id) -> bool {
+        const int c = static_cast<int>(q) / kConsumers, l = static_cast<int>(q) % kConsumers;
+        const int j = i / EPV, e = i % EPV;
+        id = c0 + c * CE + ((l / 32) * kVecPerWarp + j * 32 + (l % 32)) * EPV + e;
+        if (id >= c0 + n) return false;
+        const char* p = row_base + static_cast<size_t>(id) * ES;
+        x = DT == 1 ? __uint_as_float(static_cast<uint32_t>(__ldcg(reinterpret_cast<const unsigned short*>(p))) << 16)
+                    : __ldcg(reinterpret_cast<const float*>(p));
+        return true;
+    };
+    // keys >= tau of the candidate groups: thread t takes element t % 32 of
+    // groups t / 32, t / 32 + 8, ...
+    for (int p = tid; p < ng * kGroupElems; p += kConsumers) {
+        const uint32_t q = glist[p / kGroupElems];
+        float x;
+        int id;
+        if (!group_elem(q, p % kGroupElems, x, id)) continue;
+        if (!(all || x >= tv) || x != x) continue;
+        const uint64_t key = make_key(x, static_cast<uint32_t>(id));
+        if (key < tau) continue;
+        const int at = atomicAdd(&sm.nkeys, 1);
+        if (at < kcap) keys[at] = key;
+    }
+    consumer_bar();
+    const int nk = sm.nkeys;
+    if (nk <= kcap) {
+        for (int i = tid; i < nk; i += kConsumers) {
+            const uint64_t key = keys[i];
+            int r = 0;
+            for (int j = 0; j < nk; ++j) r += keys[j] > key;
+            if (r < k) sm.ctop[r] = key;
         }
+        return;
+    }
+    // many equal values: k rounds, each the largest key below the previous one
+    uint64_t* red = keys;  // one slot per consumer warp
+    const int lane = tid & 31, warp = tid >> 5;
+    uint64_t prev = ~0ull;
+    for (int r = 0; r < k; ++r) {
+        uint64_t best = 0;
+        for (int p = tid; p < ng * kGroupElems; p += kConsumers) {
+            float x;
+            int id;
+            if (!group_elem(glist[p / kGroupElems], p % kGroupElems, x, id) || x != x) continue;
+            const uint64_t key = make_key(x, static_cast<uint32_t>(id));
+            if (key < prev && key > best) best = key;
+        }
+        best = warp_max_u64(best);
+        consumer_bar();
+        if (lane == 0) red[warp] = best;
+        consumer_bar();
+        best = 0;
+        for (int i = 0; i < kConsumerWarps; ++i) best = red[i] > best ? red[i] : best;
+        if (tid == 0) sm.ctop[r] = best;
+        prev = best;
+        if (best == 0) break;
     }
 }
-
-__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory"); }
 
 template <int DT>
 __global__ void __launch_bounds__(kRowThreads, 3) expand_kernel(TreeDims d, TreeWs w, int step, int seg, int ns,
-                                                              const void* __restrict__ logits,
-                                                              const float* __restrict__ lse_in,
-                                                              float* __restrict__ row_lse,
-                                                              int32_t* __restrict__ ftok_out,
-                                                              int32_t* __restrict__ fcount_out) {
+                                                                 int smem_bytes, const void* __restrict__ logits,
+                                                                 const float* __restrict__ lse_in,
+                                                                 float* __restrict__ row_lse,
+                                                                 int32_t* __restrict__ ftok_out,
+                                                                 int32_t* __restrict__ fcount_out) {
     extern __shared__ __align__(128) unsigned char dyn_smem[];
     __shared__ ExpandSmem sm;
     cg::cluster_group cluster = cg::this_cluster();
@@ -400,11 +408,13 @@ __global__ void __launch_bounds__(kRowThreads, 3) expand_kernel(TreeDims d, Tree
 
     const int c0 = rank * seg;
     const int n = max(0, min(seg, d.V - c0));
-    const int nch = (n * ES + kRowChunkBytes - 1) / kRowChunkBytes;
+    const int nch = min(kMaxSegChunks, (n * ES + kRowChunkBytes - 1) / kRowChunkBytes);  // the launcher keeps <= 8
     const char* row_base = static_cast<const char*>(logits) + static_cast<size_t>(b * d.k + f) * d.V * ES;
     if (tid == 0) {
         ring_init(sm.ring, ns);
         sm.tau = 0ull;
+        sm.ngroups = 0;
+        sm.nkeys = 0;
     }
     if (tid < kMaxTopK) {
         sm.ctop[tid] = 0ull;
@@ -417,159 +427,62 @@ __global__ void __launch_bounds__(kRowThreads, 3) expand_kernel(TreeDims d, Tree
             ring_produce(sm.ring, dyn_smem, row_base + static_cast<size_t>(c0) * ES, n * ES, nch, ns, w.status);
         __syncwarp();
     } else {
+        // ---- one pass: lane maxima, online exp-sum, group maxima ----
         const bool do_sum = lse_in == nullptr;
         float m_l = -INFINITY, s_l = 0.0f;  // lane: running max and sum of exp(x - m_l)
-        uint64_t tau = 0ull;                // warp: admission key (0 = admit all)
         bool failed = false;
-        uint64_t* buf = sm.wbuf[warp];
-        if (lane == 0) {
-            sm.wcnt[warp] = 0;
-            sm.wtau[warp] = 0ull;
-        }
-        __syncwarp();
-        if (nch > 0) {
-            // tau from the k-th largest of the CTA's lane maxima over the first
-            // chunk: k distinct elements reach it, so every element of the
-            // row's top-k does. Warp 0 selects it from the warps' k largest.
-            const bool ok0 = ring_wait(sm.ring, 0, ns, failed, w.status);
-            uint4 u[kVecPerLane];
-            load_lane<DT>(dyn_smem, ok0 ? min(CE, n) / EPV : 0, warp, lane, u);
-            const float cm = lane_max4<DT>(u);
-            const uint32_t lo = warp_sort_desc_u32(cm > -INFINITY ? f2o(cm) : 0u);
-            if (lane < k) sm.boot[warp][lane] = lo;
-            consumer_bar();
-            if (warp == 0) {
-                uint32_t bv[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int e = lane * 4 + j;
-                    bv[j] = e < kConsumerWarps * k ? sm.boot[e / k][e % k] : 0u;
-                }
-                warp_sort_desc<4>(bv);
-                const uint32_t kth = __shfl_sync(0xffffffffu, bv[(k - 1) & 3], (k - 1) >> 2);
-                if (lane == 0) sm.tau = kth != 0u ? static_cast<unsigned long long>(kth) << 32 : 0ull;
-            }
-            consumer_bar();
-            tau = sm.tau;
-            if (lane == 0) sm.wtau[warp] = tau;
-        }
         for (int c = 0; c < nch; ++c) {
-            const bool ok = c == 0 ? !failed : ring_wait(sm.ring, c, ns, failed, w.status);
+            const bool ok = ring_wait(sm.ring, c, ns, failed, w.status);
             const int nvec = ok ? min(CE, n - c * CE) / EPV : 0;
-            const unsigned char* stage = dyn_smem + (c % ns) * kRowChunkBytes;
             uint4 u[kVecPerLane];
-            load_lane<DT>(stage, nvec, warp, lane, u);
-            const float cm = lane_max4<DT>(u);
-            if (c > 0) {
-                const uint64_t t2 = *reinterpret_cast<volatile unsigned long long*>(&sm.tau);
-                if (t2 > tau) tau = t2;
-            }
-            if (!ok) {
-                ring_release(sm.ring, c, ns);
-                continue;
-            }
-            if (do_sum) {
-                if (cm > m_l) {
-                    s_l = m_l > -INFINITY ? s_l * ex2_approx((m_l - cm) * kLog2e) : 0.0f;
-                    m_l = cm;
-                }
-                if (m_l > -INFINITY) {
-                    const float mb = m_l * kLog2e;
-                    float sa = 0.0f, sb = 0.0f;
-#pragma unroll
-                    for (int j = 0; j < kVecPerLane; ++j) {
-                        float x[EPV];
-                        unpack16<DT>(u[j], x);
-#pragma unroll
-                        for (int e = 0; e < EPV; e += 2) {
-                            sa += ex2_approx(fmaf(x[e], kLog2e, -mb));
-                            sb += ex2_approx(fmaf(x[e + 1], kLog2e, -mb));
-                        }
-                    }
-                    s_l += sa + sb;
-                }
-            }
-            // candidates: keys >= tau, appended lane by lane
-            const bool take_all = tau == 0ull;
-            const float tv = key_val(tau);
-            const bool lane_hot = take_all || cm >= tv;
-            if (__any_sync(0xffffffffu, lane_hot)) {
-                const int id0 = c0 + c * CE;
-                const int cnt_before = sm.wcnt[warp];
-                __syncwarp();
-                if (lane_hot) {
-#pragma unroll
-                    for (int j = 0; j < kVecPerLane; ++j) {
-                        const int v = warp * kVecPerWarp + j * 32 + lane;
-                        if (v >= nvec || !(take_all || vec_max<DT>(u[j]) >= tv)) continue;
-                        float x[EPV];
-                        unpack16<DT>(u[j], x);
-#pragma unroll
-                        for (int e = 0; e < EPV; ++e) {
-                            if (!(take_all || x[e] >= tv)) continue;  // NaN fails too
-                            const uint64_t key = make_key(x[e], static_cast<uint32_t>(id0 + v * EPV + e));
-                            if (x[e] == x[e] && key >= tau) {
-                                const int at = atomicAdd(&sm.wcnt[warp], 1);
-                                if (at < kWarpCap) buf[at] = key;
-                            }
-                        }
-                    }
-                }
-                __syncwarp();
-                const int cnt = *reinterpret_cast<volatile int*>(&sm.wcnt[warp]);
-                if (cnt >= kCompactAt && lane == 0) sm.wtau[warp] = tau;
-                if (cnt > kWarpCap) {
-                    admit_exact<DT>(stage, nvec, id0, cnt_before, buf, &sm.wcnt[warp], &sm.wtau[warp], k, &sm.tau);
-                    tau = sm.wtau[warp];
-                } else if (cnt >= kCompactAt) {
-                    warp_compact(buf, &sm.wcnt[warp], &sm.wtau[warp], k, &sm.tau);
-                    tau = sm.wtau[warp];
-                }
-            }
+            load_lane<DT>(dyn_smem + (c % ns) * kRowChunkBytes, nvec, warp, lane, u);
             ring_release(sm.ring, c, ns);
+            const float cm = lane_max4<DT>(u);
+            sm.gmax[c][tid] = warp * kVecPerWarp + lane < nvec ? f2o(cm) : 0u;
+            if (cm > m_l) {
+                s_l = (do_sum && m_l > -INFINITY) ? s_l * ex2_approx((m_l - cm) * kLog2e) : 0.0f;
+                m_l = cm;
+            }
+            if (do_sum && m_l > -INFINITY) {
+                const float mb = m_l * kLog2e;
+                float sa = 0.0f, sb = 0.0f;
+#pragma unroll
+                for (int j = 0; j < kVecPerLane; ++j) {
+                    float x[EPV];
+                    unpack16<DT>(u[j], x);
+#pragma unroll
+                    for (int e = 0; e < EPV; e += 2) {
+                        sa += ex2_approx(fmaf(x[e], kLog2e, -mb));
+                        sb += ex2_approx(fmaf(x[e + 1], kLog2e, -mb));
+                    }
+                }
+                s_l += sa + sb;
+            }
         }
-        // the warp's top-k, sorted, in buf[0..kMaxTopK) (zeros past the k-th)
-        const int cnt_end = sm.wcnt[warp];
-        __syncwarp();
-        if (cnt_end <= 32)
-            warp_final_small(buf, cnt_end, k);
-        else
-            warp_compact(buf, &sm.wcnt[warp], &sm.wtau[warp], k, nullptr);
+        // tau: the warp's k-th largest lane maximum (0 bits: fewer than k lanes hold elements)
+        const uint32_t lo = warp_sort_desc_u32(m_l > -INFINITY || (nch > 0 && warp * kVecPerWarp + lane < n / EPV)
+                                                   ? f2o(m_l) : 0u);
+        const uint32_t kth = __shfl_sync(0xffffffffu, lo, k - 1);
+        if (lane == 0 && kth != 0u) atomicMax(&sm.tau, static_cast<unsigned long long>(kth) << 32);
         // the warp's (max, sum)
+        float sw = do_sum ? s_l : 0.0f, mw = m_l;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
-            const float mo = __shfl_xor_sync(0xffffffffu, m_l, o);
-            const float so = __shfl_xor_sync(0xffffffffu, s_l, o);
-            const float M = fmaxf(m_l, mo);
-            float s = 0.0f;
-            if (m_l > -INFINITY) s += s_l * ex2_approx((m_l - M) * kLog2e);
-            if (mo > -INFINITY) s += so * ex2_approx((mo - M) * kLog2e);
-            m_l = M;
-            s_l = s;
+            const float mo = __shfl_xor_sync(0xffffffffu, mw, o);
+            const float so = __shfl_xor_sync(0xffffffffu, sw, o);
+            const float M = fmaxf(mw, mo);
+            float sum = 0.0f;
+            if (mw > -INFINITY) sum += sw * ex2_approx((mw - M) * kLog2e);
+            if (mo > -INFINITY) sum += so * ex2_approx((mo - M) * kLog2e);
+            mw = M;
+            sw = sum;
         }
         if (lane == 0) {
-            sm.wm[warp] = m_l;
-            sm.ws[warp] = s_l;
+            sm.wm[warp] = mw;
+            sm.ws[warp] = sw;
         }
-    }
-    __syncthreads();
-
-    // ---- CTA: merge the warps' lists, push to the cluster leader ----
-    if (tid < kConsumerWarps * k) {
-        const uint64_t key = sm.wbuf[tid / k][tid % k];
-        if (key != 0ull) {
-            int r = 0;
-#pragma unroll
-            for (int wi = 0; wi < kConsumerWarps; ++wi) {
-                const ulonglong2* p = reinterpret_cast<const ulonglong2*>(sm.wbuf[wi]);
-#pragma unroll
-                for (int q = 0; q < kMaxTopK / 2; ++q) {
-                    const ulonglong2 a = p[q];
-                    r += (a.x > key) + (a.y > key);
-                }
-            }
-            if (r < k) sm.ctop[r] = key;
-        }
+        consumer_bar();
+        segment_topk<DT>(sm, dyn_smem, smem_bytes, row_base, c0, n, nch, k);
     }
     __syncthreads();
     ExpandSmem* leader = cluster.map_shared_rank(&sm, 0);
@@ -642,20 +555,21 @@ __global__ void __launch_bounds__(kRowThreads, 3) expand_kernel(TreeDims d, Tree
     if (!sm.last) return;
     __threadfence();
     const int nsel = F * d.k;
+    uint64_t* sel = reinterpret_cast<uint64_t*>(dyn_smem);  // the ring is idle now
     for (int i = tid; i < nsel; i += kRowThreads) {
         const int id = base + i;
         const size_t at = static_cast<size_t>(b) * d.C + id;
         const bool valid = __ldcg(reinterpret_cast<const unsigned char*>(&w.cand_valid[at])) != 0;
         const float lv = __ldcg(&w.cand_logv[at]);
-        sm.sel[i] = (valid && lv >= d.log_thr) ? make_key(lv, static_cast<uint32_t>(id)) : 0ull;
+        sel[i] = (valid && lv >= d.log_thr) ? make_key(lv, static_cast<uint32_t>(id)) : 0ull;
     }
     if (tid < kMaxTopK) sm.top[tid] = 0ull;
     __syncthreads();
     for (int i = tid; i < nsel; i += kRowThreads) {
-        const uint64_t key = sm.sel[i];
+        const uint64_t key = sel[i];
         if (key == 0ull) continue;
         int r = 0;
-        for (int j = 0; j < nsel; ++j) r += sm.sel[j] > key;
+        for (int j = 0; j < nsel; ++j) r += sel[j] > key;
         if (r < d.k) sm.top[r] = key;
     }
     __syncthreads();
@@ -1118,19 +1032,21 @@ static int sm_count() {
     return n;
 }
 
-RowPlan plan_rows(int V, int esize, long rows, bool resident) {
+RowPlan plan_rows(int V, int esize, long rows, bool resident, int max_stages, int max_seg_chunks) {
     int cpr = kMaxChunks;
     if (!resident) {
         // about two waves of CTAs (three resident per SM with a 4-stage ring)
         const long target = 2L * 3 * sm_count();
         cpr = 1;
-        while (cpr < kMaxChunks && rows * cpr < target) cpr *= 2;
+        while (cpr < kMaxChunks &&
+               (rows * cpr < target || row_chunks(row_seg_elems(V, esize, cpr), esize) > max_seg_chunks))
+            cpr *= 2;
     }
     RowPlan p;
     p.cpr = cpr;
     p.seg = row_seg_elems(V, esize, cpr);
     p.nch = row_chunks(p.seg, esize);
-    p.stages = resident ? p.nch : std::min(p.nch, kRowStages);
+    p.stages = resident ? p.nch : std::min(p.nch, max_stages);
     p.smem = p.nch <= 1 ? static_cast<int>(align_up(static_cast<size_t>(p.seg) * esize, 128))
                         : p.stages * kRowChunkBytes;
     p.slots = cpr * p.nch * kConsumerWarps;
@@ -1176,15 +1092,30 @@ static cudaError_t launch_rows(K kernel, dim3 grid, int cpr, int smem, cudaStrea
 
 cudaError_t launch_expand(const TreeDims& d, const TreeWs& ws, int step, const void* logits, const float* lse_in,
                           float* row_lse, int32_t* ftok, int32_t* fcount_out, cudaStream_t stream) {
-    const RowPlan p = plan_rows(d.V, d.dtype == 1 ? 2 : 4, static_cast<long>(d.B) * d.k, false);
+    const RowPlan p =
+        plan_rows(d.V, d.dtype == 1 ? 2 : 4, static_cast<long>(d.B) * d.k, false, kExpandStages, kMaxSegChunks);
+    if (p.nch > kMaxSegChunks) return cudaErrorInvalidValue;
     dim3 grid(p.cpr, d.B * d.k, 1);
     TreeDims dd = d;
     TreeWs ww = ws;
-    int seg = p.seg, ns = p.stages;
-    void* args[] = {&dd,   &ww, &step, &seg, &ns, const_cast<void**>(&logits), const_cast<float**>(&lse_in),
-                    &row_lse, &ftok, &fcount_out};
-    return d.dtype == 1 ? launch_rows(expand_kernel<1>, grid, p.cpr, p.smem, stream, args)
-                        : launch_rows(expand_kernel<0>, grid, p.cpr, p.smem, stream, args);
+    // after the pass the stage memory holds the candidate groups and keys of
+    // the segment's top-k and, in the last CTA of a sequence, the frontier keys
+    const int smem = std::max({p.smem, static_cast<int>(kMaxTopK * kMaxTopK * sizeof(uint64_t)),
+                               p.nch * kConsumers * 4 + 512 * 8});
+    int seg = p.seg, ns = p.stages, smem_bytes = smem;
+    void* args[] = {&dd,
+                    &ww,
+                    &step,
+                    &seg,
+                    &ns,
+                    &smem_bytes,
+                    const_cast<void**>(&logits),
+                    const_cast<float**>(&lse_in),
+                    &row_lse,
+                    &ftok,
+                    &fcount_out};
+    return d.dtype == 1 ? launch_rows(expand_kernel<1>, grid, p.cpr, smem, stream, args)
+                        : launch_rows(expand_kernel<0>, grid, p.cpr, smem, stream, args);
 }
 
 cudaError_t launch_verify(const TreeDims& d, const TreeWs& ws, int mode, float inv_temp, const void* target,
@@ -1192,7 +1123,7 @@ cudaError_t launch_verify(const TreeDims& d, const TreeWs& ws, int mode, float i
                           const uint32_t* uniforms, int32_t* accept_len, int32_t* slots, int32_t* out_tokens,
                           cudaStream_t stream) {
     const int esize = d.dtype == 1 ? 2 : 4;
-    const RowPlan p = plan_rows(d.V, esize, static_cast<long>(d.B) * d.T, mode == 1);
+    const RowPlan p = plan_rows(d.V, esize, static_cast<long>(d.B) * d.T, mode == 1, kRowStages, 1 << 20);
     if (mode == 1 && p.stages > kRowStages) return cudaErrorInvalidValue;
     dim3 grid(p.cpr, d.B * d.T, 1);
     // the acceptance walk keeps its state in the (then idle) stage memory
