@@ -291,13 +291,12 @@ struct ExpandSmem {
 // (many equal values at the top), k block-wide rounds over the candidate
 // groups pick the keys one by one instead.
 template <int DT>
-__device__ __noinline__ void segment_topk(ExpandSmem& sm, unsigned char* scratch, int scratch_bytes,
+__device__ __forceinline__ void segment_topk(ExpandSmem& sm, unsigned char* scratch, int scratch_bytes,
                                           const char* row_base, int c0, int n, int nch, int k) {
     constexpr int ES = DT == 1 ? 2 : 4;
     constexpr int EPV = 16 / ES;
     constexpr int CE = kRowChunkBytes / ES;
-    constexpr int kGroupElems = kVecPerLane * EPV;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint64_t tau = sm.tau;
     const float tv = key_val(tau);
     const bool all = tau == 0ull;
@@ -306,35 +305,44 @@ __device__ __noinline__ void segment_topk(ExpandSmem& sm, unsigned char* scratch
     const int gcap = nch * kConsumers;
     uint64_t* keys = reinterpret_cast<uint64_t*>(scratch + gcap * sizeof(uint32_t));
     const int kcap = (scratch_bytes - gcap * static_cast<int>(sizeof(uint32_t))) / static_cast<int>(sizeof(uint64_t));
-    // candidate groups
-    for (int q = tid; q < nch * kConsumers; q += kConsumers) {
-        const uint32_t gm = sm.gmax[q / kConsumers][q % kConsumers];
-        if (gm != 0u && (all || gm >= tau_o)) glist[atomicAdd(&sm.ngroups, 1)] = static_cast<uint32_t>(q);
+    // candidate groups: this thread's own lane groups, appended warp by warp
+    for (int c = 0; c < nch; ++c) {
+        const uint32_t gm = sm.gmax[c][tid];
+        const bool hot = gm != 0u && (all || gm >= tau_o);
+        const unsigned bal = __ballot_sync(0xffffffffu, hot);
+        if (bal == 0u) continue;
+        int base = 0;
+        if (lane == 0) base = atomicAdd(&sm.ngroups, __popc(bal));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        if (hot) glist[base + __popc(bal & lanemask_lt())] = static_cast<uint32_t>(c * kConsumers + tid);
     }
     consumer_bar();
     const int ng = sm.ngroups;
-    auto group_elem = [&](uint32_t q, int i, float& x, int& id) -> bool {
+    // element id of vector j of candidate group q
+    auto group_vec = [&](uint32_t q, int j) -> int {
         const int c = static_cast<int>(q) / kConsumers, l = static_cast<int>(q) % kConsumers;
-        const int j = i / EPV, e = i % EPV;
-        id = c0 + c * CE + ((l / 32) * kVecPerWarp + j * 32 + (l % 32)) * EPV + e;
-        if (id >= c0 + n) return false;
-        const char* p = row_base + static_cast<size_t>(id) * ES;
-        x = DT == 1 ? __uint_as_float(static_cast<uint32_t>(__ldcg(reinterpret_cast<const unsigned short*>(p))) << 16)
-                    : __ldcg(reinterpret_cast<const float*>(p));
-        return true;
+        return c0 + c * CE + ((l / 32) * kVecPerWarp + j * 32 + (l % 32)) * EPV;
     };
-    // keys >= tau of the candidate groups: thread t takes element t % 32 of
-    // groups t / 32, t / 32 + 8, ...
-    for (int p = tid; p < ng * kGroupElems; p += kConsumers) {
-        const uint32_t q = glist[p / kGroupElems];
-        float x;
-        int id;
-        if (!group_elem(q, p % kGroupElems, x, id)) continue;
-        if (!(all || x >= tv) || x != x) continue;
-        const uint64_t key = make_key(x, static_cast<uint32_t>(id));
-        if (key < tau) continue;
-        const int at = atomicAdd(&sm.nkeys, 1);
-        if (at < kcap) keys[at] = key;
+    // keys >= tau: one 16-byte vector of a candidate group per thread
+    for (int p = tid; p < ng * kVecPerLane; p += kConsumers) {
+        const int id0 = group_vec(glist[p / kVecPerLane], p % kVecPerLane);
+        if (id0 >= c0 + n) continue;
+        float x[EPV];
+        unpack16<DT>(__ldcg(reinterpret_cast<const uint4*>(row_base + static_cast<size_t>(id0) * ES)), x);
+        int mine = 0;
+#pragma unroll
+        for (int e = 0; e < EPV; ++e)
+            mine += (all || x[e] >= tv) && x[e] == x[e] && make_key(x[e], static_cast<uint32_t>(id0 + e)) >= tau;
+        if (mine == 0) continue;
+        int at = atomicAdd(&sm.nkeys, mine);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+            const uint64_t key = make_key(x[e], static_cast<uint32_t>(id0 + e));
+            if ((all || x[e] >= tv) && x[e] == x[e] && key >= tau) {
+                if (at < kcap) keys[at] = key;
+                ++at;
+            }
+        }
     }
     consumer_bar();
     const int nk = sm.nkeys;
@@ -349,16 +357,20 @@ __device__ __noinline__ void segment_topk(ExpandSmem& sm, unsigned char* scratch
     }
     // many equal values: k rounds, each the largest key below the previous one
     uint64_t* red = keys;  // one slot per consumer warp
-    const int lane = tid & 31, warp = tid >> 5;
     uint64_t prev = ~0ull;
     for (int r = 0; r < k; ++r) {
         uint64_t best = 0;
-        for (int p = tid; p < ng * kGroupElems; p += kConsumers) {
-            float x;
-            int id;
-            if (!group_elem(glist[p / kGroupElems], p % kGroupElems, x, id) || x != x) continue;
-            const uint64_t key = make_key(x, static_cast<uint32_t>(id));
-            if (key < prev && key > best) best = key;
+        for (int p = tid; p < ng * kVecPerLane; p += kConsumers) {
+            const int id0 = group_vec(glist[p / kVecPerLane], p % kVecPerLane);
+            if (id0 >= c0 + n) continue;
+            float x[EPV];
+            unpack16<DT>(__ldcg(reinterpret_cast<const uint4*>(row_base + static_cast<size_t>(id0) * ES)), x);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) {
+                if (x[e] != x[e]) continue;
+                const uint64_t key = make_key(x[e], static_cast<uint32_t>(id0 + e));
+                if (key < prev && key > best) best = key;
+            }
         }
         best = warp_max_u64(best);
         consumer_bar();
