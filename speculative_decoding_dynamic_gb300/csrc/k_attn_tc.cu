@@ -51,12 +51,13 @@ constexpr int kHD = 128;                   // head dim (MMA K of QK^T, N of PV)
 constexpr int kTile = kBM * kHD * 2;       // 32 KB: a 128 x 128 bf16 tile
 constexpr int kHalf = kTile / 2;           // 16 KB: 128 rows x 64 columns (one swizzle-128B column block)
 constexpr int kStages = 2;
-constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2..9 softmax (two column halves)
+constexpr int kSoftmaxThreads = 512;
+constexpr int kThreads = 64 + kSoftmaxThreads;  // warp 0 TMA, warp 1 MMA, warps 2..17 softmax (four column quarters)
 constexpr int kSmemQ = 0;
 constexpr int kSmemKV = kTile;             // stage s: K at kSmemKV + s*2*kTile, V at +kTile
 constexpr int kSmemP = kTile * (1 + 2 * kStages);
 constexpr int kSmemBytes = kSmemP + kTile;  // 192 KB
-constexpr int kTmemCols = 256;
+constexpr int kTmemCols = 512;  // S double buffer (2 x 128 columns) + O (128)
 constexpr int kMaxW = kMaxSlots / 32;
 
 struct TcParams {
@@ -115,7 +116,7 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 32 / 64 consecutive fp32 columns of this thread's TMEM lane; the load and
+// 32 consecutive fp32 columns of this thread's TMEM lane; the load and
 // its completion wait are one asm statement so no use can move above the wait.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
     uint32_t r[32];
@@ -127,18 +128,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
         : "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
-    uint32_t r[64];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-        : "r"(taddr)
-        : "memory");
-#pragma unroll
-    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
@@ -155,7 +144,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-__device__ __forceinline__ void named_sync_softmax() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ void named_sync_softmax() { asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory"); }
 
 // ------------------------------------------------------------- kernel ---
 
@@ -165,13 +154,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t bar_q, bar_kv_full[kStages], bar_kv_empty[kStages], bar_s_full, bar_p_full, bar_o_full,
-        bar_comb;
+    __shared__ uint64_t bar_q, bar_k_full[kStages], bar_k_empty[kStages], bar_v_full[kStages], bar_v_empty[kStages],
+        bar_s_full[2], bar_s_free[2], bar_p_full, bar_o_full, bar_comb;
     __shared__ uint32_t tmem_holder;
     __shared__ uint32_t mask_sm[kBM][kMaxW];
     __shared__ int sh_last;
-    __shared__ float xch[2][2][kBM];  // per-tile row maxima exchanged between the two column halves
-    __shared__ float xsum[2][kBM];    // final row sums of the two halves
+    __shared__ float xch[2][4][kBM];  // per-tile row maxima exchanged between the four column quarters
+    __shared__ float xsum[4][kBM];    // final row sums of the four quarters
 
     const int rb = blockIdx.x, split = blockIdx.y;
     const int b = blockIdx.z / p.Hkv, hk = blockIdx.z % p.Hkv;
@@ -193,11 +182,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(&bar_q, 1);
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&bar_kv_full[s], 1);
-            mbar_init(&bar_kv_empty[s], 1);
+            mbar_init(&bar_k_full[s], 1);
+            mbar_init(&bar_k_empty[s], 1);
+            mbar_init(&bar_v_full[s], 1);
+            mbar_init(&bar_v_empty[s], 1);
         }
-        mbar_init(&bar_s_full, 1);
-        mbar_init(&bar_p_full, 256);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bar_s_full[s], 1);
+            mbar_init(&bar_s_free[s], kSoftmaxThreads);
+        }
+        mbar_init(&bar_p_full, kSoftmaxThreads);
         mbar_init(&bar_o_full, 1);
         mbar_init(&bar_comb, 1);
         fence_mbar_init();
@@ -220,45 +214,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_holder;
-    const uint32_t tmem_s = tmem, tmem_o = tmem + 128;
+    const uint32_t tmem_s = tmem, tmem_o = tmem + 256;  // S buffer b at tmem_s + 128 b
 
     unsigned char* sQ = smem + kSmemQ;
     unsigned char* sP = smem + kSmemP;
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer ---
-        if (lane == 0 && n_local > 0) {
-            mbar_arrive_expect_tx(&bar_q, kTile);
-            tma_load_4d(sQ, &tm_q, 0, hk * p.G, i0, b, &bar_q);
-            tma_load_4d(sQ + kHalf, &tm_q, 64, hk * p.G, i0, b, &bar_q);
+        // ------------------------------------------------ TMA producers ---
+        // Lane 0 loads Q and the K tiles, lane 1 the V tiles: a K stage is
+        // free once QK^T of its tile is done, a V stage once PV is, so the K
+        // of the next tiles does not wait behind V.
+        if (lane < 2 && n_local > 0) {
+            const bool is_k = lane == 0;
+            if (is_k) {
+                mbar_arrive_expect_tx(&bar_q, kTile);
+                tma_load_4d(sQ, &tm_q, 0, hk * p.G, i0, b, &bar_q);
+                tma_load_4d(sQ + kHalf, &tm_q, 64, hk * p.G, i0, b, &bar_q);
+            }
+            uint64_t* full = is_k ? bar_k_full : bar_v_full;
+            uint64_t* empty = is_k ? bar_k_empty : bar_v_empty;
+            const CUtensorMap* map = is_k ? &tm_k : &tm_v;
             for (int jj = 0; jj < n_local; ++jj) {
                 const int st = jj & 1;
-                if (jj >= kStages && !mbar_wait(&bar_kv_empty[st], ((jj >> 1) - 1) & 1)) {
+                if (jj >= kStages && !mbar_wait(&empty[st], ((jj >> 1) - 1) & 1)) {
                     raise_status(p.status, kDevTimeout);
                     break;
                 }
-                unsigned char* sK = smem + kSmemKV + st * 2 * kTile;
-                unsigned char* sV = sK + kTile;
+                unsigned char* dst = smem + kSmemKV + st * 2 * kTile + (is_k ? 0 : kTile);
                 const int key0 = (t_begin + jj) * kBN;
-                mbar_arrive_expect_tx(&bar_kv_full[st], 2 * kTile);
-                tma_load_4d(sK, &tm_k, 0, hk, key0, b, &bar_kv_full[st]);
-                tma_load_4d(sK + kHalf, &tm_k, 64, hk, key0, b, &bar_kv_full[st]);
-                tma_load_4d(sV, &tm_v, 0, hk, key0, b, &bar_kv_full[st]);
-                tma_load_4d(sV + kHalf, &tm_v, 64, hk, key0, b, &bar_kv_full[st]);
+                mbar_arrive_expect_tx(&full[st], kTile);
+                tma_load_4d(dst, map, 0, hk, key0, b, &full[st]);
+                tma_load_4d(dst + kHalf, map, 64, hk, key0, b, &full[st]);
             }
         }
+        __syncwarp();
     } else if (warp == 1) {
         // ---------------------------------------------------- MMA issuer ---
-        // Per tile j: once the softmax has written P(j-1) (so S is free),
-        // QK(j) is issued into S and committed, then PV(j-1) accumulates into O.
+        // S is double buffered in TMEM: QK(j) goes into buffer j & 1 as soon
+        // as K(j) has landed and the softmax has read S(j-2) out of it, so it
+        // runs while the softmax works on tile j-1. PV(j-1) follows once the
+        // softmax has written P(j-1).
         if (lane == 0 && n_local > 0) {
             constexpr uint32_t id_qk = idesc_bf16(kBM, kBN, 0);
             constexpr uint32_t id_pv = idesc_bf16(kBM, kHD, 1);
             const uint32_t aQ = smem_u32(sQ);
             const uint32_t aP = smem_u32(sP);
             bool ok = mbar_wait(&bar_q, 0);
-            auto issue_pv = [&](int jp) {
+            auto issue_pv = [&](int jp) -> bool {
                 const int sp = jp & 1;
+                if (!mbar_wait(&bar_p_full, jp & 1) || !mbar_wait(&bar_v_full[sp], (jp >> 1) & 1)) return false;
+                tc_fence_after();
                 const uint32_t aV = smem_u32(smem + kSmemKV + sp * 2 * kTile + kTile);
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk) {
@@ -266,98 +271,100 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_bf16(tmem_o, smem_desc(aP + offp, 16, 1024), smem_desc(aV + kk * 2048, kHalf, 1024), id_pv,
                              (jp > 0 || kk > 0) ? 1 : 0);
                 }
-                mma_commit(&bar_kv_empty[sp]);
+                mma_commit(&bar_v_empty[sp]);
                 mma_commit(&bar_o_full);
+                return true;
             };
             for (int jj = 0; ok && jj < n_local; ++jj) {
                 const int st = jj & 1;
-                ok = mbar_wait(&bar_kv_full[st], (jj >> 1) & 1);
-                if (ok && jj > 0) ok = mbar_wait(&bar_p_full, (jj - 1) & 1);
+                ok = mbar_wait(&bar_k_full[st], (jj >> 1) & 1);
+                if (ok && jj >= 2) ok = mbar_wait(&bar_s_free[st], ((jj >> 1) - 1) & 1);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t aK = smem_u32(smem + kSmemKV + st * 2 * kTile);
 #pragma unroll
                 for (int kk = 0; kk < kHD / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    mma_bf16(tmem_s, smem_desc(aQ + off, 16, 1024), smem_desc(aK + off, 16, 1024), id_qk, kk > 0);
+                    mma_bf16(tmem_s + st * kBN, smem_desc(aQ + off, 16, 1024), smem_desc(aK + off, 16, 1024), id_qk,
+                             kk > 0);
                 }
-                mma_commit(&bar_s_full);  // S(j) ready does not wait for PV(j-1)
-                if (jj > 0) issue_pv(jj - 1);
+                mma_commit(&bar_k_empty[st]);
+                mma_commit(&bar_s_full[st]);
+                if (jj > 0) ok = issue_pv(jj - 1);
             }
-            if (ok) ok = mbar_wait(&bar_p_full, (n_local - 1) & 1);
-            if (ok) {
-                tc_fence_after();
-                issue_pv(n_local - 1);
-            } else {
-                raise_status(p.status, kDevTimeout);
-            }
+            if (ok) ok = issue_pv(n_local - 1);
+            if (!ok) raise_status(p.status, kDevTimeout);
         }
     } else {
         // ------------------------------------------------------ softmax ---
-        // Two threads per query row (TMEM lane): warps 2..5 own key/output
-        // columns 0..63, warps 6..9 columns 64..127 (same lane quarters).
-        // Row maxima and sums are exchanged through shared memory. O
-        // accumulates in TMEM; the exponentials use a reference maximum m_use
-        // that is raised (O, l rescaled) only when a tile's maximum exceeds it
-        // by more than 2^8.
-        const int half = (warp - 2) >> 2;
-        const int cb = half * 64;                        // first column of this half
+        // Four threads per query row (TMEM lane): warp w (2..17) serves the
+        // rows of TMEM lane quarter w % 4 and key/output columns
+        // 32 * ((w - 2) / 4) onwards. Row maxima and sums are exchanged
+        // through shared memory. O accumulates in TMEM; the exponentials use
+        // a reference maximum m_use that is raised (O, l rescaled) only when a
+        // tile's maximum exceeds it by more than 2^8. Tiles wholly inside the
+        // prefix skip the mask.
+        const int cq = (warp - 2) >> 2;                  // column quarter
+        const int cb = cq * 32;                          // first column of this quarter
         const int q4 = warp & 3;
         const int r = (q4 << 5) | lane;                  // row of the block = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
         const int grow = rb * kBM + r;                   // row within the (b, hk) problem
         const int i = i0 + r / p.G;                      // tree slot of the row
         const int g = r % p.G;
-        float m_use = 0.0f, lh = 0.0f;                   // lh: this half's share of the row sum
+        const float sc = p.scale_log2;
+        float m_use = 0.0f, lh = 0.0f;                   // lh: this quarter's share of the row sum
         bool seen = false;
         bool ok = true;
         for (int jj = 0; jj < n_local; ++jj) {
             const int st = jj & 1;
             const int key0 = (t_begin + jj) * kBN;
             // After a timed-out wait a warp skips the work of the remaining tiles
-            // but still takes every named barrier, so the other half never waits
-            // for it without bound.
-            if (ok && !__all_sync(0xffffffffu, mbar_wait(&bar_s_full, jj & 1))) ok = false;
+            // but still takes every named barrier, so the others never wait for
+            // it without bound.
+            if (ok && !__all_sync(0xffffffffu, mbar_wait(&bar_s_full[st], (jj >> 1) & 1))) ok = false;
             tc_fence_after();
-            float sv[64];
-            if (ok) tmem_ld64(tmem_s + lane_off + cb, sv);
+            float sv[32];
+            if (ok) tmem_ld32(tmem_s + st * kBN + lane_off + cb, sv);
             else
 #pragma unroll
-                for (int e = 0; e < 64; ++e) sv[e] = -INFINITY;
-            // visibility of this half's keys: prefix keys, then tree slots in mask row i
-            uint32_t vis[2];
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int kb = key0 + cb + 32 * c;  // first key of this group of 32
-                uint32_t pre = 0u;
-                const int npre = L - kb;             // keys of the group inside the prefix
-                if (npre >= 32) pre = 0xffffffffu;
-                else if (npre > 0) pre = (1u << npre) - 1u;
-                uint32_t tree = 0u;
-                if (npre < 32) {
-                    const int j0 = kb - L;           // slot of the group's first key (may be negative)
-                    const int lo = j0 < 0 ? 0 : j0;
-                    const int w0 = lo >> 5, sh = lo & 31;
-                    uint32_t win = mask_sm[r][w0 & (kMaxW - 1)] >> sh;
-                    if (sh && w0 + 1 < kMaxW) win |= mask_sm[r][w0 + 1] << (32 - sh);
-                    if (w0 >= kMaxW) win = 0u;
-                    const int limit = n - lo;        // slots j >= n are never visible
-                    if (limit <= 0) win = 0u;
-                    else if (limit < 32) win &= (1u << limit) - 1u;
-                    tree = j0 < 0 ? (win << (-j0)) : win;
-                    if (j0 <= -32) tree = 0u;
-                }
-                vis[c] = pre | tree;
+                for (int e = 0; e < 32; ++e) sv[e] = -INFINITY;
+            tc_fence_before();
+            mbar_arrive(&bar_s_free[st]);  // S buffer st may take tile j+2
+            // visibility of this quarter's 32 keys: prefix keys, then tree slots in mask row i
+            const int kb = key0 + cb;
+            uint32_t vis = 0xffffffffu;
+            const int npre = L - kb;  // keys of the quarter inside the prefix
+            if (npre < 32) {
+                uint32_t pre = npre > 0 ? (1u << npre) - 1u : 0u;
+                const int j0 = kb - L;  // slot of the quarter's first key (may be negative)
+                const int lo = j0 < 0 ? 0 : j0;
+                const int w0 = lo >> 5, sh = lo & 31;
+                uint32_t win = mask_sm[r][w0 & (kMaxW - 1)] >> sh;
+                if (sh && w0 + 1 < kMaxW) win |= mask_sm[r][w0 + 1] << (32 - sh);
+                if (w0 >= kMaxW) win = 0u;
+                const int limit = n - lo;  // slots j >= n are never visible
+                if (limit <= 0) win = 0u;
+                else if (limit < 32) win &= (1u << limit) - 1u;
+                uint32_t tree = j0 < 0 ? (win << (-j0)) : win;
+                if (j0 <= -32) tree = 0u;
+                vis = pre | tree;
             }
-            float mx = -INFINITY;
+            const bool full = vis == 0xffffffffu;
+            float mr = -INFINITY;  // raw maximum (the scale is positive)
+            if (full) {
 #pragma unroll
-            for (int e = 0; e < 64; ++e) {
-                sv[e] *= p.scale_log2;
-                if ((vis[e >> 5] >> (e & 31)) & 1u) mx = fmaxf(mx, sv[e]);
+                for (int e = 0; e < 32; ++e) mr = fmaxf(mr, sv[e]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    if ((vis >> e) & 1u) mr = fmaxf(mr, sv[e]);
             }
-            xch[jj & 1][half][r] = mx;
+            float mx = mr * sc;
+            xch[jj & 1][cq][r] = mx;
             named_sync_softmax();
-            mx = fmaxf(mx, xch[jj & 1][half ^ 1][r]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) mx = fmaxf(mx, xch[jj & 1][c][r]);
             bool rescale = false;
             float alpha = 1.0f;
             if (mx > -INFINITY) {
@@ -371,16 +378,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     lh *= alpha;
                 }
             }
-            float sum = 0.0f;
-            uint32_t pk[32];
+            float sa = 0.0f, sb = 0.0f;
+            uint32_t pk[16];
+            if (full) {
 #pragma unroll
-            for (int e = 0; e < 64; e += 2) {
-                const float p0 = ((vis[e >> 5] >> (e & 31)) & 1u) ? ex2_approx(sv[e] - m_use) : 0.0f;
-                const float p1 = ((vis[(e + 1) >> 5] >> ((e + 1) & 31)) & 1u) ? ex2_approx(sv[e + 1] - m_use) : 0.0f;
-                sum += p0 + p1;
-                pk[e >> 1] = pack_bf16(p0, p1);
+                for (int e = 0; e < 32; e += 2) {
+                    const float p0 = ex2_approx(fmaf(sv[e], sc, -m_use));
+                    const float p1 = ex2_approx(fmaf(sv[e + 1], sc, -m_use));
+                    sa += p0;
+                    sb += p1;
+                    pk[e >> 1] = pack_bf16(p0, p1);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const float p0 = ((vis >> e) & 1u) ? ex2_approx(fmaf(sv[e], sc, -m_use)) : 0.0f;
+                    const float p1 = ((vis >> (e + 1)) & 1u) ? ex2_approx(fmaf(sv[e + 1], sc, -m_use)) : 0.0f;
+                    sa += p0;
+                    sb += p1;
+                    pk[e >> 1] = pack_bf16(p0, p1);
+                }
             }
-            lh += sum;
+            lh += sa + sb;
             if (!ok) continue;
             if (jj > 0) {  // PV(j-1) done: P buffer free, O stable
                 if (!__all_sync(0xffffffffu, mbar_wait(&bar_o_full, (jj - 1) & 1))) {
@@ -391,33 +410,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // tcgen05.ld/st are warp-collective: rescale if any row of the warp needs it
                 // (alpha = 1 for the others).
                 if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll 1
-                    for (int c = 0; c < 2; ++c) {
-                        float o[32];
-                        tmem_ld32(tmem_o + lane_off + cb + c * 32, o);
+                    float o[32];
+                    tmem_ld32(tmem_o + lane_off + cb, o);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                        tmem_st32(tmem_o + lane_off + cb + c * 32, o);
-                    }
+                    for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                    tmem_st32(tmem_o + lane_off + cb, o);
                 }
             }
+            // P rows in the 128B-swizzled K-major layout: this quarter's 32 keys
+            // are 16-byte chunks (cq & 1) * 4 .. + 3 of half cq >> 1
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {  // 8 chunks of 8 keys = this half's 64-key block
-                unsigned char* dst = sP + half * kHalf + r * 128 + ((q ^ (r & 7)) << 4);
+            for (int q = 0; q < 4; ++q) {
+                const int chunk = (cq & 1) * 4 + q;
+                unsigned char* dst = sP + (cq >> 1) * kHalf + r * 128 + ((chunk ^ (r & 7)) << 4);
                 *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
             }
             // V rows of keys that no row can see may hold anything (even NaN):
-            // zero them so that 0 * V stays 0 in the MMA.
+            // zero them so that 0 * V stays 0 in the MMA (each V row is 2 x 128
+            // bytes; this thread clears 64 of them).
             if (key0 + kBN > nkeys) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&bar_kv_full[st], (jj >> 1) & 1))) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&bar_v_full[st], (jj >> 1) & 1))) {
                     ok = false;
                     continue;
                 }
                 if (key0 + r >= nkeys) {
-                    unsigned char* sV = smem + kSmemKV + st * 2 * kTile + kTile + half * kHalf;
-                    uint4* z = reinterpret_cast<uint4*>(sV + r * 128);
+                    unsigned char* sV = smem + kSmemKV + st * 2 * kTile + kTile + (cq >> 1) * kHalf;
+                    uint4* z = reinterpret_cast<uint4*>(sV + r * 128 + (cq & 1) * 64);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) z[q] = make_uint4(0, 0, 0, 0);
+                    for (int q = 0; q < 4; ++q) z[q] = make_uint4(0, 0, 0, 0);
                 }
             }
             fence_proxy_async_smem();
@@ -429,10 +449,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
         }
         if (!ok) raise_status(p.status, kDevTimeout);
-        // row sum of both halves
-        xsum[half][r] = lh;
+        // row sum of the four quarters
+        xsum[cq][r] = lh;
         named_sync_softmax();
-        const float l = lh + xsum[half ^ 1][r];
+        const float l = xsum[0][r] + xsum[1][r] + xsum[2][r] + xsum[3][r];
         // ------------------------------------------------------- epilogue ---
         const bool row_live = grow < p.G * p.T;
         __nv_bfloat16* orow =
@@ -440,21 +460,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nsplit_b == 1) {
             const bool live = row_live && i < n && l > 0.0f && ok;  // rows of unused slots are zeros
             const float inv = live ? 1.0f / l : 0.0f;
-#pragma unroll 1
-            for (int c = 0; c < 2; ++c) {
-                float o[32];
-                if (n_local > 0) tmem_ld32(tmem_o + lane_off + cb + c * 32, o);
-                if (row_live) {
+            float o[32];
+            if (n_local > 0) tmem_ld32(tmem_o + lane_off + cb, o);
+            if (row_live) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint4 u = make_uint4(0u, 0u, 0u, 0u);
-                        if (live)
-                            u = make_uint4(pack_bf16(o[8 * q] * inv, o[8 * q + 1] * inv),
-                                           pack_bf16(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
-                                           pack_bf16(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
-                                           pack_bf16(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
-                        *reinterpret_cast<uint4*>(orow + cb + c * 32 + 8 * q) = u;
-                    }
+                for (int q = 0; q < 4; ++q) {
+                    uint4 u = make_uint4(0u, 0u, 0u, 0u);
+                    if (live)
+                        u = make_uint4(pack_bf16(o[8 * q] * inv, o[8 * q + 1] * inv),
+                                       pack_bf16(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
+                                       pack_bf16(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
+                                       pack_bf16(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
+                    *reinterpret_cast<uint4*>(orow + cb + 8 * q) = u;
                 }
             }
         } else {
@@ -462,23 +479,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             // chunk stored at position q ^ (row & 7)), reference max and sum.
             const size_t s0 = static_cast<size_t>(unit) * p.nsplit;
             float* po = p.part_o + ((s0 + split) * kBM + r) * kHD;
-#pragma unroll 1
-            for (int c = 0; c < 2; ++c) {
+            {
                 float o[32];
-                tmem_ld32(tmem_o + lane_off + cb + c * 32, o);
+                tmem_ld32(tmem_o + lane_off + cb, o);
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
-                    *reinterpret_cast<float4*>(po + cb + c * 32 + ((q ^ (r & 7)) << 2)) =
+                    *reinterpret_cast<float4*>(po + cb + ((q ^ (r & 7)) << 2)) =
                         make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
             }
             const float m_own = (seen && l > 0.0f) ? m_use : -INFINITY;
-            if (half == 0) {
+            if (cq == 0) {
                 p.part_ml[((s0 + split) * kBM + r) * 2] = m_own;
                 p.part_ml[((s0 + split) * kBM + r) * 2 + 1] = l;
             }
             __threadfence();
             named_sync_softmax();
-            if (r == 0 && half == 0) {
+            if (r == 0 && cq == 0) {
                 const int prev = atomicAdd(&p.tickets[unit], 1);
                 sh_last = prev == nsplit_b - 1;
             }
@@ -498,13 +514,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool live = row_live && i < n && Ls > 0.0f;
                 const float inv = live ? 1.0f / Ls : 0.0f;
                 const float w_own = m_own > -INFINITY ? ex2_approx(m_own - M) * inv : 0.0f;
-#pragma unroll 1
-                for (int c = 0; c < 2; ++c) {
+                {
                     float o[32];
-                    tmem_ld32(tmem_o + lane_off + cb + c * 32, o);
+                    tmem_ld32(tmem_o + lane_off + cb, o);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] *= w_own;
-                    tmem_st32(tmem_o + lane_off + cb + c * 32, o);
+                    tmem_st32(tmem_o + lane_off + cb, o);
                 }
                 constexpr int kPart = kBM * kHD * 4;  // 64 KB: one split's partial block
                 unsigned char* area = smem + kSmemKV;  // 128 KB of K/V stages, idle now
@@ -517,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ++s;
                     }
                     if (cnt == 0) break;
-                    if (r == 0 && half == 0) {
+                    if (r == 0 && cq == 0) {
                         fence_proxy_async_smem();
                         mbar_arrive_expect_tx(&bar_comb, cnt * kPart);
                         for (int q = 0; q < cnt; ++q)
@@ -530,42 +545,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float ms = __ldcg(&p.part_ml[((s0 + lst[q]) * kBM + r) * 2]);
                         const float wq = ms > -INFINITY ? ex2_approx(ms - M) * inv : 0.0f;
                         const float* rowp = reinterpret_cast<const float*>(area + q * kPart) + r * kHD + cb;
-#pragma unroll 1
-                        for (int c = 0; c < 2; ++c) {
-                            float o[32];
-                            tmem_ld32(tmem_o + lane_off + cb + c * 32, o);
+                        float o[32];
+                        tmem_ld32(tmem_o + lane_off + cb, o);
 #pragma unroll
-                            for (int q4b = 0; q4b < 8; ++q4b) {
-                                const float4 v =
-                                    *reinterpret_cast<const float4*>(rowp + c * 32 + ((q4b ^ (r & 7)) << 2));
-                                o[4 * q4b] += wq * v.x;
-                                o[4 * q4b + 1] += wq * v.y;
-                                o[4 * q4b + 2] += wq * v.z;
-                                o[4 * q4b + 3] += wq * v.w;
-                            }
-                            tmem_st32(tmem_o + lane_off + cb + c * 32, o);
+                        for (int q4b = 0; q4b < 8; ++q4b) {
+                            const float4 v = *reinterpret_cast<const float4*>(rowp + ((q4b ^ (r & 7)) << 2));
+                            o[4 * q4b] += wq * v.x;
+                            o[4 * q4b + 1] += wq * v.y;
+                            o[4 * q4b + 2] += wq * v.z;
+                            o[4 * q4b + 3] += wq * v.w;
                         }
+                        tmem_st32(tmem_o + lane_off + cb, o);
                     }
                     named_sync_softmax();  // every row has read the slots before they are refilled
                     ++round;
                 }
-#pragma unroll 1
-                for (int c = 0; c < 2; ++c) {
-                    float o[32];
-                    tmem_ld32(tmem_o + lane_off + cb + c * 32, o);
-                    if (row_live) {
+                float o[32];
+                tmem_ld32(tmem_o + lane_off + cb, o);
+                if (row_live) {
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint4 u = make_uint4(0u, 0u, 0u, 0u);
-                            if (live)
-                                u = make_uint4(pack_bf16(o[8 * q], o[8 * q + 1]), pack_bf16(o[8 * q + 2], o[8 * q + 3]),
-                                               pack_bf16(o[8 * q + 4], o[8 * q + 5]),
-                                               pack_bf16(o[8 * q + 6], o[8 * q + 7]));
-                            *reinterpret_cast<uint4*>(orow + cb + c * 32 + 8 * q) = u;
-                        }
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 u = make_uint4(0u, 0u, 0u, 0u);
+                        if (live)
+                            u = make_uint4(pack_bf16(o[8 * q], o[8 * q + 1]), pack_bf16(o[8 * q + 2], o[8 * q + 3]),
+                                           pack_bf16(o[8 * q + 4], o[8 * q + 5]), pack_bf16(o[8 * q + 6], o[8 * q + 7]));
+                        *reinterpret_cast<uint4*>(orow + cb + 8 * q) = u;
                     }
                 }
-                if (r == 0 && half == 0) p.tickets[unit] = 0;
+                if (r == 0 && cq == 0) p.tickets[unit] = 0;
             }
         }
     }
@@ -590,7 +597,9 @@ Plan make_plan(const KvDims& kv, int T) {
     pl.n_rb = (rows + kBM - 1) / kBM;
     pl.units = kv.B * kv.Hkv * pl.n_rb;
     const int max_tiles = (kv.max_len + kBN - 1) / kBN;
-    int want = (8 * 152 + pl.units - 1) / pl.units;  // aim at ~8 waves of CTAs
+    // split the keys of a unit over CTAs only when the units alone fill fewer
+    // than three waves (one CTA per SM): partial results cost HBM traffic
+    int want = pl.units >= 3 * 152 ? 1 : (8 * 152 + pl.units - 1) / pl.units;
     int cap = max_tiles / 2 > 0 ? max_tiles / 2 : 1;  // at least two tiles per split
     int nsplit = want < 1 ? 1 : (want > cap ? cap : want);
     pl.tps = (max_tiles + nsplit - 1) / nsplit;
