@@ -145,6 +145,9 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 }
 
 __device__ __forceinline__ void named_sync_softmax() { asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory"); }
+// The four softmax warps that serve one TMEM lane quarter (the rows 32 q4 ..
+// 32 q4 + 31, one warp per column quarter) meet on barrier 2 + q4.
+__device__ __forceinline__ void named_sync_rows(int q4) { asm volatile("bar.sync %0, 128;" ::"r"(2 + q4) : "memory"); }
 
 // ------------------------------------------------------------- kernel ---
 
@@ -236,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const CUtensorMap* map = is_k ? &tm_k : &tm_v;
             for (int jj = 0; jj < n_local; ++jj) {
                 const int st = jj & 1;
-                if (jj >= kStages && !mbar_wait(&empty[st], ((jj >> 1) - 1) & 1)) {
+                if (jj >= kStages && !mbar_wait_sleep(&empty[st], ((jj >> 1) - 1) & 1)) {
                     raise_status(p.status, kDevTimeout);
                     break;
                 }
@@ -259,10 +262,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t id_pv = idesc_bf16(kBM, kHD, 1);
             const uint32_t aQ = smem_u32(sQ);
             const uint32_t aP = smem_u32(sP);
-            bool ok = mbar_wait(&bar_q, 0);
+            bool ok = mbar_wait_sleep(&bar_q, 0);
             auto issue_pv = [&](int jp) -> bool {
                 const int sp = jp & 1;
-                if (!mbar_wait(&bar_p_full, jp & 1) || !mbar_wait(&bar_v_full[sp], (jp >> 1) & 1)) return false;
+                if (!mbar_wait_sleep(&bar_p_full, jp & 1) || !mbar_wait_sleep(&bar_v_full[sp], (jp >> 1) & 1))
+                    return false;
                 tc_fence_after();
                 const uint32_t aV = smem_u32(smem + kSmemKV + sp * 2 * kTile + kTile);
 #pragma unroll
@@ -277,8 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             for (int jj = 0; ok && jj < n_local; ++jj) {
                 const int st = jj & 1;
-                ok = mbar_wait(&bar_k_full[st], (jj >> 1) & 1);
-                if (ok && jj >= 2) ok = mbar_wait(&bar_s_free[st], ((jj >> 1) - 1) & 1);
+                ok = mbar_wait_sleep(&bar_k_full[st], (jj >> 1) & 1);
+                if (ok && jj >= 2) ok = mbar_wait_sleep(&bar_s_free[st], ((jj >> 1) - 1) & 1);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t aK = smem_u32(smem + kSmemKV + st * 2 * kTile);
@@ -322,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // After a timed-out wait a warp skips the work of the remaining tiles
             // but still takes every named barrier, so the others never wait for
             // it without bound.
-            if (ok && !__all_sync(0xffffffffu, mbar_wait(&bar_s_full[st], (jj >> 1) & 1))) ok = false;
+            if (ok && !__all_sync(0xffffffffu, mbar_wait_sleep(&bar_s_full[st], (jj >> 1) & 1))) ok = false;
             tc_fence_after();
             float sv[32];
             if (ok) tmem_ld32(tmem_s + st * kBN + lane_off + cb, sv);
@@ -362,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             float mx = mr * sc;
             xch[jj & 1][cq][r] = mx;
-            named_sync_softmax();
+            named_sync_rows(q4);
 #pragma unroll
             for (int c = 0; c < 4; ++c) mx = fmaxf(mx, xch[jj & 1][c][r]);
             bool rescale = false;
@@ -402,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             lh += sa + sb;
             if (!ok) continue;
             if (jj > 0) {  // PV(j-1) done: P buffer free, O stable
-                if (!__all_sync(0xffffffffu, mbar_wait(&bar_o_full, (jj - 1) & 1))) {
+                if (!__all_sync(0xffffffffu, mbar_wait_sleep(&bar_o_full, (jj - 1) & 1))) {
                     ok = false;
                     continue;
                 }
