@@ -50,14 +50,15 @@ constexpr int kBN = 128;                   // keys per tile (MMA N of QK^T, K of
 constexpr int kHD = 128;                   // head dim (MMA K of QK^T, N of PV)
 constexpr int kTile = kBM * kHD * 2;       // 32 KB: a 128 x 128 bf16 tile
 constexpr int kHalf = kTile / 2;           // 16 KB: 128 rows x 64 columns (one swizzle-128B column block)
-constexpr int kStages = 2;
+constexpr int kKStages = 3;  // K tiles in flight (a stage frees after QK^T)
+constexpr int kVStages = 2;  // V tiles in flight (a stage frees after PV)
 constexpr int kSoftmaxThreads = 512;
 constexpr int kThreads = 64 + kSoftmaxThreads;  // warp 0 TMA, warp 1 MMA, warps 2..17 softmax (four column quarters)
 constexpr int kSmemQ = 0;
-constexpr int kSmemKV = kTile;             // stage s: K at kSmemKV + s*2*kTile, V at +kTile
-constexpr int kSmemP = kTile * (1 + 2 * kStages);
-constexpr int kSmemBytes = kSmemP + kTile;  // 192 KB
-constexpr int kTmemCols = 512;  // S double buffer (2 x 128 columns) + O (128)
+constexpr int kSmemK = kTile;                      // K stage s at kSmemK + s * kTile
+constexpr int kSmemV = kSmemK + kKStages * kTile;  // V stage s at kSmemV + s * kTile
+constexpr int kSmemBytes = kSmemV + kVStages * kTile;  // 192 KB
+constexpr int kTmemCols = 512;  // S double buffer (2 x 128 columns), O (128), P (64: bf16 pairs)
 constexpr int kMaxW = kMaxSlots / 32;
 
 struct TcParams {
@@ -108,6 +109,16 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b
         : "memory");
 }
 
+// The same with operand A (M x K, row = TMEM lane, K packed two bf16 per
+// 32-bit column) read from tensor memory.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc, int accum) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(b), "r"(idesc), "r"(accum)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
@@ -139,6 +150,17 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
         : "memory");
 }
 
+// 16 consecutive 32-bit columns of this thread's TMEM lane (store + wait).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};\n\t"
+        "tcgen05.wait::st.sync.aligned;"
+        :
+        : "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+          "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<const uint32_t*>(&h);
@@ -157,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t bar_q, bar_k_full[kStages], bar_k_empty[kStages], bar_v_full[kStages], bar_v_empty[kStages],
+    __shared__ uint64_t bar_q, bar_k_full[kKStages], bar_k_empty[kKStages], bar_v_full[kVStages], bar_v_empty[kVStages],
         bar_s_full[2], bar_s_free[2], bar_p_full, bar_o_full, bar_comb;
     __shared__ uint32_t tmem_holder;
     __shared__ uint32_t mask_sm[kBM][kMaxW];
@@ -184,9 +206,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&bar_q, 1);
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kKStages; ++s) {
             mbar_init(&bar_k_full[s], 1);
             mbar_init(&bar_k_empty[s], 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
             mbar_init(&bar_v_full[s], 1);
             mbar_init(&bar_v_empty[s], 1);
         }
@@ -218,9 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = tmem_holder;
     const uint32_t tmem_s = tmem, tmem_o = tmem + 256;  // S buffer b at tmem_s + 128 b
+    const uint32_t tmem_p = tmem + 384;                 // P(j): row = lane, keys as bf16 pairs
 
     unsigned char* sQ = smem + kSmemQ;
-    unsigned char* sP = smem + kSmemP;
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producers ---
@@ -237,13 +261,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint64_t* full = is_k ? bar_k_full : bar_v_full;
             uint64_t* empty = is_k ? bar_k_empty : bar_v_empty;
             const CUtensorMap* map = is_k ? &tm_k : &tm_v;
+            const int ns = is_k ? kKStages : kVStages;
             for (int jj = 0; jj < n_local; ++jj) {
-                const int st = jj & 1;
-                if (jj >= kStages && !mbar_wait_sleep(&empty[st], ((jj >> 1) - 1) & 1)) {
+                const int st = jj % ns;
+                if (jj >= ns && !mbar_wait_sleep(&empty[st], ((jj / ns) - 1) & 1)) {
                     raise_status(p.status, kDevTimeout);
                     break;
                 }
-                unsigned char* dst = smem + kSmemKV + st * 2 * kTile + (is_k ? 0 : kTile);
+                unsigned char* dst = smem + (is_k ? kSmemK : kSmemV) + st * kTile;
                 const int key0 = (t_begin + jj) * kBN;
                 mbar_arrive_expect_tx(&full[st], kTile);
                 tma_load_4d(dst, map, 0, hk, key0, b, &full[st]);
@@ -261,39 +286,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t id_qk = idesc_bf16(kBM, kBN, 0);
             constexpr uint32_t id_pv = idesc_bf16(kBM, kHD, 1);
             const uint32_t aQ = smem_u32(sQ);
-            const uint32_t aP = smem_u32(sP);
             bool ok = mbar_wait_sleep(&bar_q, 0);
             auto issue_pv = [&](int jp) -> bool {
-                const int sp = jp & 1;
-                if (!mbar_wait_sleep(&bar_p_full, jp & 1) || !mbar_wait_sleep(&bar_v_full[sp], (jp >> 1) & 1))
+                const int sp = jp % kVStages;
+                if (!mbar_wait_sleep(&bar_p_full, jp & 1) || !mbar_wait_sleep(&bar_v_full[sp], (jp / kVStages) & 1))
                     return false;
                 tc_fence_after();
-                const uint32_t aV = smem_u32(smem + kSmemKV + sp * 2 * kTile + kTile);
+                const uint32_t aV = smem_u32(smem + kSmemV + sp * kTile);
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    const uint32_t offp = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    mma_bf16(tmem_o, smem_desc(aP + offp, 16, 1024), smem_desc(aV + kk * 2048, kHalf, 1024), id_pv,
-                             (jp > 0 || kk > 0) ? 1 : 0);
-                }
+                for (int kk = 0; kk < kBN / 16; ++kk)  // A = P from TMEM: 16 keys = 8 columns per MMA
+                    mma_bf16_ts(tmem_o, tmem_p + kk * 8, smem_desc(aV + kk * 2048, kHalf, 1024), id_pv,
+                                (jp > 0 || kk > 0) ? 1 : 0);
                 mma_commit(&bar_v_empty[sp]);
                 mma_commit(&bar_o_full);
                 return true;
             };
             for (int jj = 0; ok && jj < n_local; ++jj) {
-                const int st = jj & 1;
-                ok = mbar_wait_sleep(&bar_k_full[st], (jj >> 1) & 1);
-                if (ok && jj >= 2) ok = mbar_wait_sleep(&bar_s_free[st], ((jj >> 1) - 1) & 1);
+                const int sb = jj & 1, sk = jj % kKStages;
+                ok = mbar_wait_sleep(&bar_k_full[sk], (jj / kKStages) & 1);
+                if (ok && jj >= 2) ok = mbar_wait_sleep(&bar_s_free[sb], ((jj >> 1) - 1) & 1);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t aK = smem_u32(smem + kSmemKV + st * 2 * kTile);
+                const uint32_t aK = smem_u32(smem + kSmemK + sk * kTile);
 #pragma unroll
                 for (int kk = 0; kk < kHD / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    mma_bf16(tmem_s + st * kBN, smem_desc(aQ + off, 16, 1024), smem_desc(aK + off, 16, 1024), id_qk,
+                    mma_bf16(tmem_s + sb * kBN, smem_desc(aQ + off, 16, 1024), smem_desc(aK + off, 16, 1024), id_qk,
                              kk > 0);
                 }
-                mma_commit(&bar_k_empty[st]);
-                mma_commit(&bar_s_full[st]);
+                mma_commit(&bar_k_empty[sk]);
+                mma_commit(&bar_s_full[sb]);
                 if (jj > 0) ok = issue_pv(jj - 1);
             }
             if (ok) ok = issue_pv(n_local - 1);
@@ -421,24 +443,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st32(tmem_o + lane_off + cb, o);
                 }
             }
-            // P rows in the 128B-swizzled K-major layout: this quarter's 32 keys
-            // are 16-byte chunks (cq & 1) * 4 .. + 3 of half cq >> 1
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int chunk = (cq & 1) * 4 + q;
-                unsigned char* dst = sP + (cq >> 1) * kHalf + r * 128 + ((chunk ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-            }
+            // P into TMEM: row r = lane, this quarter's 32 keys = columns 16 cq .. 16 cq + 15
+            tmem_st16(tmem_p + lane_off + cq * 16, pk);
             // V rows of keys that no row can see may hold anything (even NaN):
             // zero them so that 0 * V stays 0 in the MMA (each V row is 2 x 128
             // bytes; this thread clears 64 of them).
             if (key0 + kBN > nkeys) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&bar_v_full[st], (jj >> 1) & 1))) {
+                const int sv_st = jj % kVStages;
+                if (!__all_sync(0xffffffffu, mbar_wait(&bar_v_full[sv_st], (jj / kVStages) & 1))) {
                     ok = false;
                     continue;
                 }
                 if (key0 + r >= nkeys) {
-                    unsigned char* sV = smem + kSmemKV + st * 2 * kTile + kTile + (cq >> 1) * kHalf;
+                    unsigned char* sV = smem + kSmemV + sv_st * kTile + (cq >> 1) * kHalf;
                     uint4* z = reinterpret_cast<uint4*>(sV + r * 128 + (cq & 1) * 64);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) z[q] = make_uint4(0, 0, 0, 0);
@@ -526,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st32(tmem_o + lane_off + cb, o);
                 }
                 constexpr int kPart = kBM * kHD * 4;  // 64 KB: one split's partial block
-                unsigned char* area = smem + kSmemKV;  // 128 KB of K/V stages, idle now
+                unsigned char* area = smem + kSmemK;  // 160 KB of K/V stages, idle now
                 int round = 0;
                 for (int s = 0; s < nsplit_b;) {
                     int lst[2];
