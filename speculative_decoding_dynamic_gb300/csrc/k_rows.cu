@@ -291,8 +291,9 @@ struct ExpandSmem {
 // (many equal values at the top), k block-wide rounds over the candidate
 // groups pick the keys one by one instead.
 template <int DT>
-__device__ __forceinline__ void segment_topk(ExpandSmem& sm, unsigned char* scratch, int scratch_bytes,
-                                          const char* row_base, int c0, int n, int nch, int k) {
+__device__ __forceinline__ void segment_topk(ExpandSmem& sm, const unsigned char* stages, bool resident,
+                                             unsigned char* scratch, int scratch_bytes, const char* row_base, int c0,
+                                             int n, int nch, int k) {
     constexpr int ES = DT == 1 ? 2 : 4;
     constexpr int EPV = 16 / ES;
     constexpr int CE = kRowChunkBytes / ES;
@@ -325,10 +326,14 @@ __device__ __forceinline__ void segment_topk(ExpandSmem& sm, unsigned char* scra
     };
     // keys >= tau: one 16-byte vector of a candidate group per thread
     for (int p = tid; p < ng * kVecPerLane; p += kConsumers) {
-        const int id0 = group_vec(glist[p / kVecPerLane], p % kVecPerLane);
+        const uint32_t q = glist[p / kVecPerLane];
+        const int id0 = group_vec(q, p % kVecPerLane);
         if (id0 >= c0 + n) continue;
         float x[EPV];
-        unpack16<DT>(__ldcg(reinterpret_cast<const uint4*>(row_base + static_cast<size_t>(id0) * ES)), x);
+        // a resident segment is still in the stages (chunk c in stage c); else read it back from L2
+        const uint4 u = resident ? reinterpret_cast<const uint4*>(stages)[(id0 - c0) / EPV]
+                                 : __ldcg(reinterpret_cast<const uint4*>(row_base + static_cast<size_t>(id0) * ES));
+        unpack16<DT>(u, x);
         int mine = 0;
 #pragma unroll
         for (int e = 0; e < EPV; ++e)
@@ -494,7 +499,11 @@ __global__ void __launch_bounds__(kRowThreads, 3) expand_kernel(TreeDims d, Tree
             sm.ws[warp] = sw;
         }
         consumer_bar();
-        segment_topk<DT>(sm, dyn_smem, smem_bytes, row_base, c0, n, nch, k);
+        // a segment of at most ns chunks stays in the stages; the scratch then follows them
+        const bool resident = nch <= ns;
+        const int scratch_off = resident ? ns * kRowChunkBytes : 0;
+        segment_topk<DT>(sm, dyn_smem, resident, dyn_smem + scratch_off, smem_bytes - scratch_off, row_base, c0, n,
+                         nch, k);
     }
     __syncthreads();
     ExpandSmem* leader = cluster.map_shared_rank(&sm, 0);
@@ -1112,8 +1121,9 @@ cudaError_t launch_expand(const TreeDims& d, const TreeWs& ws, int step, const v
     TreeWs ww = ws;
     // after the pass the stage memory holds the candidate groups and keys of
     // the segment's top-k and, in the last CTA of a sequence, the frontier keys
-    const int smem = std::max({p.smem, static_cast<int>(kMaxTopK * kMaxTopK * sizeof(uint64_t)),
-                               p.nch * kConsumers * 4 + 512 * 8});
+    const int scratch = p.nch * kConsumers * 4 + 512 * 8;  // candidate groups + keys
+    const int smem = std::max(static_cast<int>(kMaxTopK * kMaxTopK * sizeof(uint64_t)),
+                              p.nch <= p.stages ? p.stages * kRowChunkBytes + scratch : std::max(p.smem, scratch));
     int seg = p.seg, ns = p.stages, smem_bytes = smem;
     void* args[] = {&dd,
                     &ww,
