@@ -618,11 +618,21 @@ Plan make_plan(const KvDims& kv, int T) {
     pl.n_rb = (rows + kBM - 1) / kBM;
     pl.units = kv.B * kv.Hkv * pl.n_rb;
     const int max_tiles = (kv.max_len + kBN - 1) / kBN;
-    // split the keys of a unit over CTAs only when the units alone fill fewer
-    // than three waves (one CTA per SM): partial results cost HBM traffic
-    int want = pl.units >= 3 * 152 ? 1 : (8 * 152 + pl.units - 1) / pl.units;
-    int cap = max_tiles / 2 > 0 ? max_tiles / 2 : 1;  // at least two tiles per split
-    int nsplit = want < 1 ? 1 : (want > cap ? cap : want);
+    // Keys of a unit may be split over CTAs (one CTA per SM). Cost model:
+    // waves of CTAs x tiles per CTA, plus a prologue/epilogue of about two
+    // tiles per CTA and a merge of about one tile per extra split.
+    const int sms = 152;
+    int nsplit = 1;
+    double best = 1e30;
+    for (int ns = 1; ns <= std::max(1, max_tiles / 2); ++ns) {
+        const int tps = (max_tiles + ns - 1) / ns;
+        const double waves = std::ceil(static_cast<double>(pl.units) * ns / sms);
+        const double cost = waves * (tps + 2.0 + (ns > 1 ? 1.0 : 0.0));
+        if (cost < best - 1e-9) {
+            best = cost;
+            nsplit = ns;
+        }
+    }
     pl.tps = (max_tiles + nsplit - 1) / nsplit;
     pl.nsplit = (max_tiles + pl.tps - 1) / pl.tps;
     pl.off_tickets = 256;
