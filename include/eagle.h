@@ -191,7 +191,8 @@ int eagle_tree_attention(const eagle_kv_cfg* kv, int T, const void* q, const voi
  *   lower id); walk from the root into the child carrying that choice.
  * LOSSLESS (temperature > 0): integer probabilities
  *   P_t[x] = floor(dexp((x - max_t) / temperature) * 2^40), dexp a fixed-order
- *   exp (Cody-Waite reduction, degree-7 Taylor, fp32 mul/add); at node u the
+ *   exp (Cody-Waite reduction, degree-7 Taylor in Horner form, each step one
+ *   correctly rounded fp32 fused multiply-add); at node u the
  *   kept children are tested in slot order and child x is accepted iff
  *   U24 * S < 2^24 * P_u[x] (S = remaining mass); a rejection removes x. With
  *   no child accepted the bonus is the smallest token y (not removed) whose

@@ -80,24 +80,26 @@ void row_stats(const void* row, int dtype, int V, int k, double* lse64, std::vec
 // same integer probabilities. Written from the mathematics: Cody-Waite
 // reduction z = n ln2 + r with ln2 split into a 16-bit head and a tail, a
 // degree-7 Taylor polynomial of exp(r) in Horner form, then scaling by 2^n.
-// Every operation is one correctly rounded fp32 multiply or add (built with
+// Every step is one correctly rounded fp32 operation: n is z log2(e) rounded
+// to the nearest integer (ties to even) by one fused multiply-add with
+// 1.5 * 2^23, the reduction and each Horner step are fused multiply-adds
+// (std::fma), the scaling is exact. No other contraction (built with
 // -ffp-contract=off). Defined for z <= 0; returns 0 below -32.
 float dexp(float z) {
     if (!(z >= -32.0f)) return 0.0f;
     const float kLog2e = 1.44269502f;             // 0x3FB8AA3B
     const float kLn2Hi = 0.693145751953125f;      // 0x3F317200, 16 significant bits
     const float kLn2Lo = 1.42860677e-06f;         // 0x35BFBE8E = ln2 - kLn2Hi
-    float n = std::nearbyint(z * kLog2e);
-    float r = z - n * kLn2Hi;
-    r = r - n * kLn2Lo;
+    const float kRound = 12582912.0f;             // 1.5 * 2^23
+    const float t = std::fma(z, kLog2e, kRound);  // kRound + nearest integer to z log2(e)
+    const float n = t - kRound;                   // exact
+    float r = std::fma(-n, kLn2Hi, z);
+    r = std::fma(-n, kLn2Lo, r);
     const float c[8] = {1.0f, 1.0f, 0.5f, 1.0f / 6.0f, 1.0f / 24.0f, 1.0f / 120.0f, 1.0f / 720.0f,
                         1.0f / 5040.0f};
     float p = c[7];
-    for (int i = 6; i >= 0; --i) {
-        p = p * r;
-        p = p + c[i];
-    }
-    int e = static_cast<int>(n) + 127;
+    for (int i = 6; i >= 0; --i) p = std::fma(p, r, c[i]);
+    const int e = static_cast<int>(n) + 127;
     uint32_t sb = static_cast<uint32_t>(e) << 23;
     float scale;
     std::memcpy(&scale, &sb, 4);

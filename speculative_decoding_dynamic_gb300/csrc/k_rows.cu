@@ -613,29 +613,39 @@ __global__ void __launch_bounds__(kRowThreads, 3) expand_kernel(TreeDims d, Tree
 
 // Fixed-order exp for lossless verification (contract in eagle.h): Cody-Waite
 // reduction with ln2 = 0x1.62e4p-1 + 0x1.7f7d1cp-20, degree-7 Taylor series of
-// exp(r) in Horner form, exact scaling by 2^n; every step one correctly
-// rounded fp32 multiply or add. z <= 0; returns 0 below -32.
-__device__ __forceinline__ float dexp_fixed(float z) {
-    if (!(z >= -32.0f)) return 0.0f;
-    const float n = rintf(__fmul_rn(z, 0x1.715476p+0f));
-    float r = __fsub_rn(z, __fmul_rn(n, 0x1.62e4p-1f));
-    r = __fsub_rn(r, __fmul_rn(n, 0x1.7f7d1cp-20f));
-    float p = 0x1.a01a02p-13f;                           // 1/7!
-    p = __fadd_rn(__fmul_rn(p, r), 0x1.6c16c2p-10f);     // 1/6!
-    p = __fadd_rn(__fmul_rn(p, r), 0x1.111112p-7f);      // 1/5!
-    p = __fadd_rn(__fmul_rn(p, r), 0x1.555556p-5f);      // 1/4!
-    p = __fadd_rn(__fmul_rn(p, r), 0x1.555556p-3f);      // 1/3!
-    p = __fadd_rn(__fmul_rn(p, r), 0.5f);                // 1/2!
-    p = __fadd_rn(__fmul_rn(p, r), 1.0f);                // 1/1!
-    p = __fadd_rn(__fmul_rn(p, r), 1.0f);                // 1/0!
-    const float scale = __int_as_float((static_cast<int>(n) + 127) << 23);
-    return __fmul_rn(p, scale);
+// exp(r) in Horner form, exact scaling by 2^n. Every step is one correctly
+// rounded fp32 operation: n = z log2(e) rounded to nearest-even by one fused
+// multiply-add with 1.5 * 2^23, then fused multiply-adds for the reduction and
+// each Horner step. z <= 0. Returns p and the exponent n (value p * 2^n),
+// p = 0 below -32.
+__device__ __forceinline__ float dexp_parts(float z, int& n_out) {
+    if (!(z >= -32.0f)) {
+        n_out = 0;
+        return 0.0f;
+    }
+    const float t = __fmaf_rn(z, 0x1.715476p+0f, 12582912.0f);  // 1.5 * 2^23 + nearest integer
+    const float n = __fsub_rn(t, 12582912.0f);
+    n_out = __float_as_int(t) - 0x4B400000;
+    float r = __fmaf_rn(-n, 0x1.62e4p-1f, z);
+    r = __fmaf_rn(-n, 0x1.7f7d1cp-20f, r);
+    float p = 0x1.a01a02p-13f;              // 1/7!
+    p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);  // 1/6!
+    p = __fmaf_rn(p, r, 0x1.111112p-7f);   // 1/5!
+    p = __fmaf_rn(p, r, 0x1.555556p-5f);   // 1/4!
+    p = __fmaf_rn(p, r, 0x1.555556p-3f);   // 1/3!
+    p = __fmaf_rn(p, r, 0.5f);             // 1/2!
+    p = __fmaf_rn(p, r, 1.0f);             // 1/1!
+    p = __fmaf_rn(p, r, 1.0f);             // 1/0!
+    return p;
 }
 
-// Integer mass floor(dexp((x - m) * inv_t) * 2^40).
+// Integer mass floor(dexp((x - m) * inv_t) * 2^40): p * 2^(n + 40), both
+// scalings exact, then truncated.
 __device__ __forceinline__ uint64_t fixed_mass(float x, float m, float inv_t) {
-    const float e = dexp_fixed(__fmul_rn(__fsub_rn(x, m), inv_t));
-    return __float2ull_rz(__fmul_rn(e, 0x1p40f));
+    int n;
+    const float p = dexp_parts(__fmul_rn(__fsub_rn(x, m), inv_t), n);
+    const float scale = __int_as_float((n + 127 + 40) << 23);
+    return __float2ull_rz(__fmul_rn(p, scale));
 }
 
 struct VerifySmem {
