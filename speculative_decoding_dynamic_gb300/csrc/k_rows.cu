@@ -639,13 +639,17 @@ __device__ __forceinline__ float dexp_parts(float z, int& n_out) {
     return p;
 }
 
-// Integer mass floor(dexp((x - m) * inv_t) * 2^40): p * 2^(n + 40), both
-// scalings exact, then truncated.
+// Integer mass floor(dexp((x - m) * inv_t) * 2^40) = floor(p * 2^(n + 40)):
+// p's 24-bit significand shifted by (its exponent + n + 17), an exact
+// integer operation (the float product would be exact as well).
 __device__ __forceinline__ uint64_t fixed_mass(float x, float m, float inv_t) {
     int n;
     const float p = dexp_parts(__fmul_rn(__fsub_rn(x, m), inv_t), n);
-    const float scale = __int_as_float((n + 127 + 40) << 23);
-    return __float2ull_rz(__fmul_rn(p, scale));
+    const uint32_t bits = __float_as_uint(p);
+    const uint32_t sig = (bits & 0x7FFFFFu) | 0x800000u;
+    const int sh = static_cast<int>(bits >> 23) - 127 + n + 17;
+    if (p == 0.0f || sh <= -24) return 0ull;
+    return sh >= 0 ? static_cast<uint64_t>(sig) << sh : static_cast<uint64_t>(sig >> (-sh));
 }
 
 struct VerifySmem {
