@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--sharpness", type=float, default=None)
     ap.add_argument("--verify", default=None, choices=[None, "greedy", "lossless"])
     ap.add_argument("--planted", action="store_true", help="sharp draft rows (deep chains)")
+    ap.add_argument("--aligned", action="store_true",
+                    help="target rows favour each slot's first kept child (deep acceptance; compaction moves KV)")
     ap.add_argument("--sets", type=int, default=0, help="rotating input sets (0 = enough to exceed L2)")
     ap.add_argument("--seed", type=int, default=42)
     ap.add_argument("--no-e2e", action="store_true")
@@ -55,6 +57,23 @@ def parse():
 
 
 # ------------------------------------------------------------- helpers ---
+
+def align_targets(target: np.ndarray, tokens: np.ndarray, parent: np.ndarray, n_tree: np.ndarray, value: float):
+    """Aligned-target variant: in the target row of every tree slot, the token of
+    the slot's first kept child gets the logit `value` (about 0.9 of the row's
+    mass), so verification accepts along first children and compaction has KV
+    to move. Input construction only; changes `target` in place."""
+    B = target.shape[0]
+    bits = np.uint16(np.float32(value).view(np.uint32) >> 16) if target.dtype == np.uint16 else np.float32(value)
+    for b in range(B):
+        n = int(n_tree[b])
+        first = {}
+        for c in range(1, n):
+            p = int(parent[b, c])
+            if p >= 0 and p not in first:
+                first[p] = c
+        for t, c in first.items():
+            target[b, t, int(tokens[b, c])] = bits
 
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
@@ -397,6 +416,12 @@ def main():
     # warm-up outside capture (sets kernel attributes), then one graph per set
     for r in range(R):
         cycle(r)
+        if args.aligned:  # the tree depends on the draft rows only: align this set's targets to it
+            torch.cuda.synchronize()
+            align_targets(host_sets[r]["target"], dc.tokens.cpu().numpy(), dc.parent.cpu().numpy(),
+                          dc.n_tree.cpu().numpy(), WL.plant_value(w, float(np.mean(w.sharpness_per_seq(seed)))))
+            dev_sets[r]["target"].copy_(to_dev(host_sets[r]["target"]).view(dev_sets[r]["target"].shape))
+            cycle(r)
     torch.cuda.synchronize()
     assert dc.status() == 0, "device status after warm-up"
     graphs = []
@@ -435,29 +460,52 @@ def main():
     ms_per_step = ms / args.steps
     value = job_throughput(ws_, args.steps, ms)
 
-    acc = dc.accept_len.cpu().numpy()
+    # accepted lengths of every input set (lossless acceptance differs between sets)
+    accs = []
+    for r in range(R):
+        graphs[r].replay()
+        torch.cuda.synchronize()
+        accs.append(dc.accept_len.cpu().numpy())
+    acc_all = np.stack(accs)               # [R, B]
+    acc = acc_all.mean(axis=0)             # per sequence, averaged over the sets
     n_tree = dc.n_tree.cpu().numpy()
 
     # ---- per-kernel timing: each stage call alone, same launch configuration ----
-    def time_call(fn, reps):
+    flush = None
+
+    def time_call(fn, reps, flush_l2=False):
         """Average device time of one stage call: `reps` calls on rotating inputs
-        captured in a CUDA graph, replayed once untimed and once timed."""
+        captured in a CUDA graph, replayed once untimed and once timed. With
+        flush_l2, every call is preceded by a write of a buffer larger than L2
+        and the time of the writes alone is subtracted (for a stage whose
+        inputs do not rotate, such as compaction of the same cache rows)."""
+        nonlocal flush
+        if flush_l2 and flush is None:
+            flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device="cuda")
         for i in range(3):
             fn(i % R)
         torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=side):
-            for i in range(reps):
-                fn(i % R)
-        g.replay()
-        torch.cuda.synchronize()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        g.replay()
-        b.record(stream)
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) / reps
+
+        def timed(with_fn):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                for i in range(reps):
+                    if flush_l2:
+                        flush.fill_(i)
+                    if with_fn:
+                        fn(i % R)
+            g.replay()
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / reps
+
+        t = timed(True)
+        return max(t - timed(False), 0.0) if flush_l2 else t
 
     reps = args.kernel_reps
     # state for standalone stage calls: a completed cycle on set 0
@@ -473,7 +521,9 @@ def main():
     kt["verify"] = time_call(lambda r: dc.verify(mode, w.temperature, dev_sets[r]["target"], dev_sets[r]["uniforms"]),
                              reps)
     cycle(0)
-    kt["compact"] = time_call(lambda r: dc.compact(cache, prefix_d), reps)
+    torch.cuda.synchronize()
+    acc_compact = dc.accept_len.cpu().numpy()  # the accepted lengths the timed compaction calls move
+    kt["compact"] = time_call(lambda r: dc.compact(cache, prefix_d), reps, flush_l2=True)
     torch.cuda.synchronize()
     alg = algorithmic_bytes(w, prefix_len, acc, w.layers)
     peak = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
@@ -483,7 +533,7 @@ def main():
     per_kernel = {}
     for name, ms_k in kt.items():
         byt = {"expand_step": alg["expand_step"], "attention": alg["attention"], "verify": alg["verify"],
-               "compact": alg["compact"]}.get(name)
+               "compact": algorithmic_bytes(w, prefix_len, acc_compact, w.layers)["compact"]}.get(name)
         e = {"ms": round(ms_k, 5)}
         if byt is not None:
             e["bytes"] = int(byt)
@@ -560,10 +610,12 @@ def main():
                        "head_dim": w.head_dim, "prefix": w.prefix if not isinstance(w.prefix, tuple) else
                        list(w.prefix), "sharpness": w.sharpness if not isinstance(w.sharpness, tuple) else
                        list(w.sharpness), "verify": w.verify, "compact_layers": w.layers, "planted": args.planted,
+                       "aligned": args.aligned,
                        "l2": f"{R} rotating input sets, {round(R * (per_set + attn_bytes) / 2**20)} MiB > 129 MB L2",
                        "graph": "one CUDA graph per input set, replayed"},
             "tokens_of_tree_per_s": round(value * float(np.mean(n_tree)) * w.batch, 1),
             "accepted_tokens_per_s": round(value * float(np.mean(acc + 1)) * w.batch, 1),
+            "mean_accept_len": round(float(np.mean(acc)), 3),
             "roofline": roofline, "kernels": per_kernel, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": int(launches_per_cycle * args.steps), "launches_per_cycle": int(launches_per_cycle),
             "clocks": clocks,
