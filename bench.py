@@ -33,6 +33,7 @@ sys.path.insert(0, ROOT)
 
 L2_BYTES = 129 * 1024 * 1024
 METRIC = "draft-verify cycles/s at Llama-8B shape; HBM GB/s & % roofline per kernel"
+POLICIES = {"dynamic": 0, "confidence": 1, "no_rerank": 2}
 
 
 def parse():
@@ -53,6 +54,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel-reps", type=int, default=100)
     ap.add_argument("--layers", type=int, default=None, help="KV layers moved by compaction (memory cap)")
+    ap.add_argument("--policy", default="dynamic", choices=list(POLICIES),
+                    help="tree policy: EAGLE-2, confidence-ranked frontier, or no rerank (ablations)")
     return ap.parse_args()
 
 
@@ -237,7 +240,7 @@ def algorithmic_bytes(w, prefix_len, accept_len, layers):
     return dict(expand=expand, expand_step=expand_step, verify=verify, attention=attention, compact=compact)
 
 
-def oracle_cycle(w, s, prefix_len, root, kh, vh, geo, mode, tree_region, head_stride=1):
+def oracle_cycle(w, s, prefix_len, root, kh, vh, geo, mode, tree_region, head_stride=1, policy=0):
     """One whole cycle in the CPU oracle (the bench's CPU baseline / reference arm).
 
     Returns the estimated cycle time in seconds: every stage is run in full
@@ -246,7 +249,7 @@ def oracle_cycle(w, s, prefix_len, root, kh, vh, geo, mode, tree_region, head_st
     the oracle's cycle)."""
     import oracle
     t0 = time.perf_counter()
-    cfg = oracle.TreeCfg(w.batch, w.vocab, w.top_k, w.depth, w.node_budget, w.threshold)
+    cfg = oracle.TreeCfg(w.batch, w.vocab, w.top_k, w.depth, w.node_budget, w.threshold, policy)
     t = oracle.Tree(cfg)
     for st in range(w.depth):
         t.expand(st, s["draft"][st])
@@ -321,7 +324,8 @@ def run_reference(args, w):
     geo = WL.kv_geometry(w, seed, w.layers)
     kh, vh = host_attention_layer(w, geo, prefix_len, seed, 0)
     region = host_tree_region(w, geo, prefix_len, seed, w.layers)
-    probe = oracle_cycle(w, s, prefix_len, root, kh, vh, geo, w.verify, region, head_stride=w.n_q_heads)
+    probe = oracle_cycle(w, s, prefix_len, root, kh, vh, geo, w.verify, region, head_stride=w.n_q_heads,
+                         policy=POLICIES[args.policy])
     full_est = probe  # with one head per group measured and scaled: an estimate of a full cycle
     m = 1
     while m < w.n_q_heads and (args.steps + args.warmup) * full_est / m > 150.0:
@@ -329,10 +333,12 @@ def run_reference(args, w):
     while w.n_q_heads % m:
         m //= 2
     for _ in range(args.warmup):
-        oracle_cycle(w, s, prefix_len, root, kh, vh, geo, w.verify, region, head_stride=m)
+        oracle_cycle(w, s, prefix_len, root, kh, vh, geo, w.verify, region, head_stride=m,
+                     policy=POLICIES[args.policy])
     tot = 0.0
     for _ in range(args.steps):
-        tot += oracle_cycle(w, s, prefix_len, root, kh, vh, geo, w.verify, region, head_stride=m)
+        tot += oracle_cycle(w, s, prefix_len, root, kh, vh, geo, w.verify, region, head_stride=m,
+                            policy=POLICIES[args.policy])
     v = args.steps / tot
     unit = "cycles/s"
     sample = (f"{args.steps} oracle cycles of {w.name}: every stage in full"
@@ -344,7 +350,7 @@ def run_reference(args, w):
             "data": "synthetic",
             "config": {"workload": w.name, "batch": w.batch, "vocab": w.vocab, "depth": w.depth,
                        "top_k": w.top_k, "node_budget": w.node_budget, "verify": w.verify,
-                       "sharpness": w.sharpness if not isinstance(w.sharpness, tuple) else list(w.sharpness)},
+                       "policy": args.policy, "sharpness": w.sharpness if not isinstance(w.sharpness, tuple) else list(w.sharpness)},
             "cpu_baseline": {"value": v, "unit": unit, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -402,7 +408,8 @@ def main():
                 lo = base + p0 * geo["pos_stride"]
                 cache[lo:lo + host.size].copy_(to_dev(host).view(-1))
 
-    cfg = E.TreeCfg(w.batch, w.vocab, w.top_k, w.depth, w.node_budget, w.threshold, w.dtype)
+    cfg = E.TreeCfg(w.batch, w.vocab, w.top_k, w.depth, w.node_budget, w.threshold, w.dtype,
+                    POLICIES[args.policy])
     kv = E.KvCfg(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.layers, geo["max_len"], w.dtype,
                  geo["seq_stride"], geo["layer_stride"], geo["kv_stride"], geo["pos_stride"])
     dc = C.DeviceCycle(cfg, kv)
@@ -467,6 +474,14 @@ def main():
         torch.cuda.synchronize()
         accs.append(dc.accept_len.cpu().numpy())
     acc_all = np.stack(accs)               # [R, B]
+    # summed path value of the kept nodes (the tree's expected accepted length), averaged over sets
+    vsum = torch.empty(w.batch, dtype=torch.float32, device="cuda")
+    vals = []
+    for r in range(R):
+        graphs[r].replay()
+        E.eagle_tree_value(cfg, dc.ws, vsum)
+        torch.cuda.synchronize()
+        vals.append(vsum.cpu().numpy())
     acc = acc_all.mean(axis=0)             # per sequence, averaged over the sets
     n_tree = dc.n_tree.cpu().numpy()
 
@@ -594,7 +609,8 @@ def main():
         tot = 0.0
         t0 = time.perf_counter()
         while n < 1 or (time.perf_counter() - t0 < 12.0 and n < 50):
-            tot += oracle_cycle(w, s0, prefix_len, root, kh, vh, geo, w.verify, region)
+            tot += oracle_cycle(w, s0, prefix_len, root, kh, vh, geo, w.verify, region,
+                                policy=POLICIES[args.policy])
             n += 1
         cpu = {"value": round(n / tot, 4), "unit": "cycles/s", "cores": 1, "kind": "oracle",
                "sample": f"{n} whole oracle cycles of {w.name} (every stage, all attention rows) on one host core"}
@@ -610,12 +626,13 @@ def main():
                        "head_dim": w.head_dim, "prefix": w.prefix if not isinstance(w.prefix, tuple) else
                        list(w.prefix), "sharpness": w.sharpness if not isinstance(w.sharpness, tuple) else
                        list(w.sharpness), "verify": w.verify, "compact_layers": w.layers, "planted": args.planted,
-                       "aligned": args.aligned,
+                       "aligned": args.aligned, "policy": args.policy,
                        "l2": f"{R} rotating input sets, {round(R * (per_set + attn_bytes) / 2**20)} MiB > 129 MB L2",
                        "graph": "one CUDA graph per input set, replayed"},
             "tokens_of_tree_per_s": round(value * float(np.mean(n_tree)) * w.batch, 1),
             "accepted_tokens_per_s": round(value * float(np.mean(acc + 1)) * w.batch, 1),
             "mean_accept_len": round(float(np.mean(acc)), 3),
+            "mean_tree_value": round(float(np.mean(vals)), 3),
             "roofline": roofline, "kernels": per_kernel, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": int(launches_per_cycle * args.steps), "launches_per_cycle": int(launches_per_cycle),
             "clocks": clocks,

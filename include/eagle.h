@@ -67,6 +67,19 @@ typedef enum { EAGLE_F32 = 0, EAGLE_BF16 = 1 } eagle_dtype;
 
 typedef enum { EAGLE_VERIFY_GREEDY = 0, EAGLE_VERIFY_LOSSLESS = 1 } eagle_verify_mode;
 
+/* Tree policy [summary 5.2.1, 5.2.2: the ablations of value-based expansion
+ * and of reranking]:
+ *   EAGLE_POLICY_DYNAMIC     EAGLE-2: the frontier of each step is the top-k of
+ *                            its children by path value; the rerank keeps the
+ *                            N most valuable of all drafted nodes.
+ *   EAGLE_POLICY_CONFIDENCE  the frontier is ranked by each child's own
+ *                            confidence (its log-probability) instead of its
+ *                            path value; the rerank is unchanged.
+ *   EAGLE_POLICY_NO_RERANK   no rerank: the kept nodes are the ones the
+ *                            expansion chose, the frontier of every step (k per
+ *                            depth), the N most valuable of them if more. */
+typedef enum { EAGLE_POLICY_DYNAMIC = 0, EAGLE_POLICY_CONFIDENCE = 1, EAGLE_POLICY_NO_RERANK = 2 } eagle_policy;
+
 /* Draft-tree problem [summary 4.1, 4.2, App. A; notes EAGLE 2 方法]. */
 typedef struct {
     int batch;       /* B, independent sequences */
@@ -76,6 +89,7 @@ typedef struct {
     int node_budget; /* N: draft nodes kept by the rerank; tree slots T = N + 1 (root + N), T <= 256 */
     float threshold; /* path-value threshold below which a node is not expanded; <= 0 disables */
     int logit_dtype; /* eagle_dtype of the draft and target logits */
+    int policy;      /* eagle_policy (0 = EAGLE-2) */
 } eagle_tree_cfg;
 
 /*
@@ -153,6 +167,15 @@ int eagle_rerank(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, void* str
 int eagle_build_tree(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, const int32_t* prefix_len,
                      const int32_t* root_token, int32_t* tokens, int32_t* parent, int32_t* depth,
                      int32_t* pos_ids, uint32_t* mask, int32_t* n_tree, void* stream);
+
+/*
+ * Readout of the kept tree [tutorial, "Value of a Node = Its Path Product":
+ * the expected number of accepted tokens of a verify pass is the sum of the
+ * kept nodes' path values]. After eagle_rerank:
+ *   value_sum [B] float out: sum over the kept nodes of exp(log path value),
+ *   accumulated in fp32 in node-id order.
+ */
+int eagle_tree_value(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, float* value_sum, void* stream);
 
 /* Scratch bytes for eagle_tree_attention with this geometry and T slots. */
 size_t eagle_attention_workspace_bytes(const eagle_kv_cfg* kv, int T);

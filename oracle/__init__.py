@@ -40,8 +40,8 @@ def _load():
     lib.oracle_dexp.argtypes = [f32]
     lib.oracle_dexp.restype = f32
     lib.oracle_tree_init.argtypes = [i32, i32, i32, p, p, p, p, p, p, p]
-    lib.oracle_expand.argtypes = [i32, i32, i32, i32, i32, f32, p, p, i32, p, p, p, p, p, p, p, p, p, p]
-    lib.oracle_rerank.argtypes = [i32, i32, i32, p, p, p, p, p]
+    lib.oracle_expand.argtypes = [i32, i32, i32, i32, i32, f32, i32, p, p, i32, p, p, p, p, p, p, p, p, p, p, p]
+    lib.oracle_rerank.argtypes = [i32, i32, i32, i32, i32, i32, p, p, p, p, p, p]
     lib.oracle_build_tree.argtypes = [i32, i32, i32, i32, p, p, p, p, p, p, p, p, p, p, p, p, p]
     lib.oracle_value_sum.argtypes = [i32, p, p]
     lib.oracle_value_sum.restype = f64
@@ -105,6 +105,7 @@ class TreeCfg:
     depth: int
     node_budget: int
     threshold: float = 0.0
+    policy: int = 0  # 0 EAGLE-2, 1 confidence-based expansion, 2 without reranking
 
     @property
     def C(self) -> int:
@@ -134,6 +135,8 @@ class Tree:
         self.fcount = np.zeros(B, np.int32)
         self.kept = np.zeros((B, C), np.uint8)
         self.n_kept = np.zeros(B, np.int32)
+        self.lp = np.full((B, C), -np.inf, np.float32)               # each node's own confidence (log)
+        self.fhist = np.full((cfg.depth + 1, B, k), -1, np.int32)   # frontier node ids of every step
         self.row_lse = np.full((B, cfg.depth, k), np.nan, np.float32)
         _load().oracle_tree_init(B, C, k, _p(self.token), _p(self.parent), _p(self.depth), _p(self.logv),
                                  _p(self.valid), _p(self.fnode), _p(self.fcount))
@@ -149,19 +152,21 @@ class Tree:
         lse_out = np.full((B, k), np.nan, np.float32)
         ftok = np.zeros((B, k), np.int32)
         fcnt = np.zeros(B, np.int32)
-        rc = _load().oracle_expand(B, V, k, step, _dtype_code(logits_s), log_threshold(cfg.threshold),
+        rc = _load().oracle_expand(B, V, k, step, _dtype_code(logits_s), log_threshold(cfg.threshold), cfg.policy,
                                    _p(logits_s), _p(lse_in), cfg.C, _p(self.token), _p(self.parent),
-                                   _p(self.depth), _p(self.logv), _p(self.valid), _p(self.fnode),
+                                   _p(self.depth), _p(self.logv), _p(self.lp), _p(self.valid), _p(self.fnode),
                                    _p(self.fcount), _p(lse_out), _p(ftok), _p(fcnt))
         if rc != 0:
             raise RuntimeError(f"oracle_expand failed: {rc}")
+        self.fhist[step + 1] = self.fnode
         self.row_lse[:, step, :] = lse_out
         return ftok, fcnt
 
     def rerank(self):
         cfg = self.cfg
-        _load().oracle_rerank(cfg.batch, cfg.C, cfg.node_budget, _p(self.depth), _p(self.logv), _p(self.valid),
-                              _p(self.kept), _p(self.n_kept))
+        _load().oracle_rerank(cfg.batch, cfg.C, cfg.node_budget, cfg.policy, cfg.depth, cfg.top_k,
+                              _p(self.fhist), _p(self.depth), _p(self.logv), _p(self.valid), _p(self.kept),
+                              _p(self.n_kept))
         return self.kept, self.n_kept
 
     def build_tree(self, prefix_len: np.ndarray, root_token: np.ndarray):

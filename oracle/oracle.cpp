@@ -175,9 +175,14 @@ void oracle_tree_init(int B, int C, int k, int32_t* cand_token, int32_t* cand_pa
 //
 // lse_in: if non-null, the row lse values [B, k] to use instead of this
 // oracle's own (stage-chained parity runs feed the GPU's fp32 lse here).
-int oracle_expand(int B, int V, int k, int step, int dtype, float log_thr, const void* logits_s,
+//
+// policy 1 (ablation "confidence-based expansion", EAGLE-2 summary 5.2.1:
+// value-based expansion compared with confidence-based): the next frontier is
+// ranked by the child's own confidence lp = x - lse instead of its value; the
+// threshold still applies to the value. cand_lp [B, C] receives lp.
+int oracle_expand(int B, int V, int k, int step, int dtype, float log_thr, int policy, const void* logits_s,
                   const float* lse_in, int C, int32_t* cand_token, int32_t* cand_parent,
-                  int32_t* cand_depth, float* cand_logv, uint8_t* cand_valid, int32_t* fnode,
+                  int32_t* cand_depth, float* cand_logv, float* cand_lp, uint8_t* cand_valid, int32_t* fnode,
                   int32_t* fcount, float* row_lse_out, int32_t* ftok_out, int32_t* fcount_out) {
     const int64_t base = step_base(step, k);
     for (int b = 0; b < B; ++b) {
@@ -204,6 +209,7 @@ int oracle_expand(int B, int V, int k, int step, int dtype, float log_thr, const
                 cand_parent[at] = parent;
                 cand_depth[at] = step + 1;
                 cand_logv[at] = plogv + lp;
+                cand_lp[at] = lp;
                 cand_valid[at] = 1;
             }
         }
@@ -215,9 +221,10 @@ int oracle_expand(int B, int V, int k, int step, int dtype, float log_thr, const
                 int64_t at = static_cast<int64_t>(b) * C + id;
                 if (cand_valid[at] && cand_logv[at] >= log_thr) elig.push_back(id);
             }
+        const float* rank_by = policy == 1 ? cand_lp : cand_logv;
         std::sort(elig.begin(), elig.end(), [&](int a, int c) {
-            float va = cand_logv[static_cast<int64_t>(b) * C + a];
-            float vc = cand_logv[static_cast<int64_t>(b) * C + c];
+            float va = rank_by[static_cast<int64_t>(b) * C + a];
+            float vc = rank_by[static_cast<int64_t>(b) * C + c];
             if (va != vc) return va > vc;
             return a < c;
         });
@@ -239,12 +246,26 @@ int oracle_expand(int B, int V, int k, int step, int dtype, float log_thr, const
 // 4.2: rerank all draft tokens, keep the top m by value; EAGLE notes, EAGLE 2
 // 方法, ReRank: on equal values the shallower node is kept]. Ties beyond depth
 // go to the lower node id (reading). Full sort, then the first min(N, #valid).
-int oracle_rerank(int B, int C, int N, const int32_t* cand_depth, const float* cand_logv,
-                  const uint8_t* cand_valid, uint8_t* kept, int32_t* n_kept) {
+//
+// policy 2 (ablation "without reranking", EAGLE-2 summary 5.2.2): the
+// candidates are only the nodes chosen by the expansion phase, i.e. the
+// frontier of every step 1..D (fhist [D+1, B, k], -1 = none; reading: these
+// are the tokens drafted without a rerank, k per depth), of which the first N
+// by the same order are kept.
+int oracle_rerank(int B, int C, int N, int policy, int D, int k, const int32_t* fhist, const int32_t* cand_depth,
+                  const float* cand_logv, const uint8_t* cand_valid, uint8_t* kept, int32_t* n_kept) {
     for (int b = 0; b < B; ++b) {
         std::vector<int> ids;
-        for (int i = 0; i < C; ++i)
-            if (cand_valid[static_cast<int64_t>(b) * C + i]) ids.push_back(i);
+        if (policy == 2) {
+            for (int s = 1; s <= D; ++s)
+                for (int f = 0; f < k; ++f) {
+                    const int id = fhist[(static_cast<int64_t>(s) * B + b) * k + f];
+                    if (id >= 0 && cand_valid[static_cast<int64_t>(b) * C + id]) ids.push_back(id);
+                }
+        } else {
+            for (int i = 0; i < C; ++i)
+                if (cand_valid[static_cast<int64_t>(b) * C + i]) ids.push_back(i);
+        }
         std::sort(ids.begin(), ids.end(), [&](int a, int c) {
             int64_t ia = static_cast<int64_t>(b) * C + a, ic = static_cast<int64_t>(b) * C + c;
             if (cand_logv[ia] != cand_logv[ic]) return cand_logv[ia] > cand_logv[ic];

@@ -34,6 +34,7 @@ int resolve(const eagle_tree_cfg* cfg, TreeDims* d) {
     if (V < k) return EAGLE_ERR_INVALID_ARG;
     if (cfg->logit_dtype != EAGLE_F32 && cfg->logit_dtype != EAGLE_BF16) return EAGLE_ERR_INVALID_ARG;
     if (std::isnan(cfg->threshold)) return EAGLE_ERR_INVALID_ARG;
+    if (cfg->policy < EAGLE_POLICY_DYNAMIC || cfg->policy > EAGLE_POLICY_NO_RERANK) return EAGLE_ERR_INVALID_ARG;
     const long C = k + static_cast<long>(D - 1) * k * k;
     const int T = N + 1;
     if (C > kMaxCandidates || T > kMaxSlots) return EAGLE_ERR_UNSUPPORTED;
@@ -53,6 +54,7 @@ int resolve(const eagle_tree_cfg* cfg, TreeDims* d) {
     d->log_thr = cfg->threshold > 0.0f ? static_cast<float>(std::log(static_cast<double>(cfg->threshold)))
                                        : -INFINITY;
     d->dtype = cfg->logit_dtype;
+    d->policy = cfg->policy;
     return EAGLE_OK;
 }
 
@@ -131,6 +133,16 @@ int eagle_rerank(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, void* str
     if (rc == EAGLE_OK) rc = bind_ws(d, ws, ws_bytes, &w);
     if (rc != EAGLE_OK) return rc;
     return launch_result(launch_rerank(d, w, static_cast<cudaStream_t>(stream)));
+}
+
+int eagle_tree_value(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, float* value_sum, void* stream) {
+    TreeDims d;
+    TreeWs w;
+    int rc = resolve(cfg, &d);
+    if (rc == EAGLE_OK) rc = bind_ws(d, ws, ws_bytes, &w);
+    if (rc != EAGLE_OK) return rc;
+    if (value_sum == nullptr) return EAGLE_ERR_INVALID_ARG;
+    return launch_result(launch_tree_value(d, w, value_sum, static_cast<cudaStream_t>(stream)));
 }
 
 int eagle_build_tree(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, const int32_t* prefix_len,

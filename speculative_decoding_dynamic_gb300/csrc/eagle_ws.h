@@ -42,6 +42,7 @@ struct TreeDims {
     int B, V, k, D, N, T, W, C;
     float log_thr;  // -inf disables the threshold
     int dtype;      // 0 fp32, 1 bf16
+    int policy;     // 0 EAGLE-2, 1 confidence-based expansion, 2 without rerank
 };
 
 // Pointers into the caller's workspace. Layout computed by ws_layout(). The
@@ -54,6 +55,7 @@ struct TreeWs {
     int32_t* cand_parent;   // [B, C] node id of the parent, -1 = root
     int32_t* cand_depth;    // [B, C]
     float* cand_logv;       // [B, C] log path value
+    float* cand_lp;         // [B, C] the node's own log-probability (confidence)
     uint8_t* cand_valid;    // [B, C]
     int32_t* fnode;         // [D+1, B, k] frontier node ids per step (-1 = root)
     int32_t* fcount;        // [D+1, B]
@@ -87,6 +89,7 @@ inline size_t ws_layout(const TreeDims& d, void* base, TreeWs* ws) {
     w.cand_parent = static_cast<int32_t*>(take(B * C * 4));
     w.cand_depth = static_cast<int32_t*>(take(B * C * 4));
     w.cand_logv = static_cast<float*>(take(B * C * 4));
+    w.cand_lp = static_cast<float*>(take(B * C * 4));
     w.cand_valid = static_cast<uint8_t*>(take(B * C));
     w.fnode = static_cast<int32_t*>(take((D + 1) * B * k * 4));
     w.fcount = static_cast<int32_t*>(take((D + 1) * B * 4));
@@ -120,6 +123,7 @@ cudaError_t launch_tree_init(const TreeDims& d, const TreeWs& ws, cudaStream_t s
 cudaError_t launch_expand(const TreeDims& d, const TreeWs& ws, int step, const void* logits, const float* lse_in,
                           float* row_lse, int32_t* ftok, int32_t* fcount_out, cudaStream_t stream);
 cudaError_t launch_rerank(const TreeDims& d, const TreeWs& ws, cudaStream_t stream);
+cudaError_t launch_tree_value(const TreeDims& d, const TreeWs& ws, float* value_sum, cudaStream_t stream);
 cudaError_t launch_build_tree(const TreeDims& d, const TreeWs& ws, const int32_t* prefix_len,
                               const int32_t* root_token, int32_t* tokens, int32_t* parent, int32_t* depth,
                               int32_t* pos, uint32_t* mask, int32_t* n_tree, cudaStream_t stream);

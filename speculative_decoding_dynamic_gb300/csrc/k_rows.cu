@@ -557,6 +557,7 @@ __global__ void __launch_bounds__(kRowThreads, 3) expand_kernel(TreeDims d, Tree
             w.cand_parent[at] = parent;
             w.cand_depth[at] = step + 1;
             w.cand_logv[at] = __fadd_rn(plogv, lp);
+            w.cand_lp[at] = lp;
             w.cand_valid[at] = 1;
         }
     }
@@ -582,7 +583,9 @@ __global__ void __launch_bounds__(kRowThreads, 3) expand_kernel(TreeDims d, Tree
         const size_t at = static_cast<size_t>(b) * d.C + id;
         const bool valid = __ldcg(reinterpret_cast<const unsigned char*>(&w.cand_valid[at])) != 0;
         const float lv = __ldcg(&w.cand_logv[at]);
-        sel[i] = (valid && lv >= d.log_thr) ? make_key(lv, static_cast<uint32_t>(id)) : 0ull;
+        // ranked by value (EAGLE-2) or by the child's own confidence (policy 1)
+        const float rank_by = d.policy == 1 ? __ldcg(&w.cand_lp[at]) : lv;
+        sel[i] = (valid && lv >= d.log_thr) ? make_key(rank_by, static_cast<uint32_t>(id)) : 0ull;
     }
     if (tid < kMaxTopK) sm.top[tid] = 0ull;
     __syncthreads();

@@ -28,6 +28,7 @@ __global__ void tree_init_kernel(TreeDims d, TreeWs w) {
         w.cand_parent[i] = -1;
         w.cand_depth[i] = -1;
         w.cand_logv[i] = -INFINITY;
+        w.cand_lp[i] = -INFINITY;
         w.cand_valid[i] = 0;
         w.kept[i] = 0;
         w.slot_of[i] = -1;
@@ -50,22 +51,32 @@ constexpr int kSortThreads = 512;
 
 // Key of a candidate: value first (larger), then lower node id. Node ids are
 // depth-major, so for equal values the lower id is also the shallower node.
-// Invalid candidates get key 0 and sort last.
+// Invalid candidates get key 0 and sort last. Without rerank (policy 2) only
+// the nodes the expansion chose (the frontier of steps 1..D) are candidates.
 __global__ void __launch_bounds__(kSortThreads) rerank_kernel(TreeDims d, TreeWs w, int P) {
     __shared__ uint64_t keys[kMaxCandidates];
+    __shared__ uint8_t chosen[kMaxCandidates];
     __shared__ int n_valid;
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
     pdl_launch_dependents();
     pdl_wait_prior();
     if (tid == 0) n_valid = 0;
+    if (d.policy == 2) {
+        for (int i = tid; i < d.C; i += kSortThreads) chosen[i] = 0;
+        __syncthreads();
+        for (int q = tid; q < d.D * d.k; q += kSortThreads) {
+            const int id = w.fnode[((1 + q / d.k) * d.B + b) * d.k + q % d.k];
+            if (id >= 0 && id < d.C) chosen[id] = 1;
+        }
+    }
     __syncthreads();
     int local = 0;
     for (int i = tid; i < P; i += kSortThreads) {
         uint64_t key = 0;
         if (i < d.C) {
             const size_t at = static_cast<size_t>(b) * d.C + i;
-            if (w.cand_valid[at]) {
+            if (w.cand_valid[at] && (d.policy != 2 || chosen[i])) {
                 key = make_key(w.cand_logv[at], static_cast<uint32_t>(i));
                 ++local;
             }
@@ -200,6 +211,24 @@ __global__ void __launch_bounds__(kBuildThreads) build_tree_kernel(TreeDims d, T
     if (tid == 0) n_tree[b] = n;
 }
 
+// ------------------------------------------------------------- tree value ---
+
+// Sum of exp(log value) over the kept nodes of a sequence, in node-id order
+// (one warp per sequence: lane-strided partial sums combined in lane order).
+__global__ void __launch_bounds__(32) tree_value_kernel(TreeDims d, TreeWs w, float* __restrict__ value_sum) {
+    const int b = blockIdx.x, lane = threadIdx.x;
+    pdl_launch_dependents();
+    pdl_wait_prior();
+    float s = 0.0f;
+    for (int i = lane; i < d.C; i += 32) {
+        const size_t at = static_cast<size_t>(b) * d.C + i;
+        if (w.kept[at]) s += expf(w.cand_logv[at]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) value_sum[b] = s;
+}
+
 // -------------------------------------------------------------- launchers ---
 
 cudaError_t launch_tree_init(const TreeDims& d, const TreeWs& ws, cudaStream_t stream) {
@@ -213,6 +242,10 @@ cudaError_t launch_rerank(const TreeDims& d, const TreeWs& ws, cudaStream_t stre
     int P = 2;
     while (P < d.C) P <<= 1;
     return launch_pdl(rerank_kernel, dim3(d.B), dim3(kSortThreads), 0, stream, d, ws, P);
+}
+
+cudaError_t launch_tree_value(const TreeDims& d, const TreeWs& ws, float* value_sum, cudaStream_t stream) {
+    return launch_pdl(tree_value_kernel, dim3(d.B), dim3(32), 0, stream, d, ws, value_sum);
 }
 
 cudaError_t launch_build_tree(const TreeDims& d, const TreeWs& ws, const int32_t* prefix_len,

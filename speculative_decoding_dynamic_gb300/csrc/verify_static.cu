@@ -102,6 +102,7 @@ extern "C" int eagle_verify_static(const eagle_tree_cfg* cfg, int mode, float te
     d.C = cfg->top_k + (cfg->depth - 1) * cfg->top_k * cfg->top_k;
     d.log_thr = -INFINITY;  // not used by verification
     d.dtype = cfg->logit_dtype;
+    d.policy = 0;  // not used by verification
 
     unsigned char* base = nullptr;
     if (scratch_address(&base) != cudaSuccess) return EAGLE_ERR_LAUNCH;

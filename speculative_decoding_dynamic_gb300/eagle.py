@@ -35,7 +35,8 @@ class EagleError(RuntimeError):
 class TreeCfg(ctypes.Structure):
     """eagle_tree_cfg."""
     _fields_ = [("batch", ctypes.c_int), ("vocab", ctypes.c_int), ("top_k", ctypes.c_int), ("depth", ctypes.c_int),
-                ("node_budget", ctypes.c_int), ("threshold", ctypes.c_float), ("logit_dtype", ctypes.c_int)]
+                ("node_budget", ctypes.c_int), ("threshold", ctypes.c_float), ("logit_dtype", ctypes.c_int),
+                ("policy", ctypes.c_int)]
 
     @property
     def T(self) -> int:
@@ -69,6 +70,7 @@ _lib.eagle_workspace_bytes.restype = _sz
 _lib.eagle_tree_init.argtypes = [_TP, _p, _sz, _p]
 _lib.eagle_expand.argtypes = [_TP, _p, _sz, _i, _p, _p, _p, _p, _p, _p]
 _lib.eagle_rerank.argtypes = [_TP, _p, _sz, _p]
+_lib.eagle_tree_value.argtypes = [_TP, _p, _sz, _p, _p]
 _lib.eagle_build_tree.argtypes = [_TP, _p, _sz, _p, _p, _p, _p, _p, _p, _p, _p, _p]
 _lib.eagle_attention_workspace_bytes.argtypes = [_KP, _i]
 _lib.eagle_attention_workspace_bytes.restype = _sz
@@ -136,6 +138,10 @@ def eagle_expand(cfg, ws, step, draft_logits, row_lse_in, row_lse, frontier_toke
 
 def eagle_rerank(cfg, ws, stream=None):
     _check("eagle_rerank", _lib.eagle_rerank(ctypes.byref(cfg), *_ws(ws), _stream(stream)))
+
+
+def eagle_tree_value(cfg, ws, value_sum, stream=None):
+    _check("eagle_tree_value", _lib.eagle_tree_value(ctypes.byref(cfg), *_ws(ws), _ptr(value_sum), _stream(stream)))
 
 
 def eagle_build_tree(cfg, ws, prefix_len, root_token, tokens, parent, depth, pos_ids, mask, n_tree, stream=None):

@@ -28,10 +28,10 @@ class Inputs:
         self.uniforms = WL.uniforms(w, seed, 0)
         self.attn_layer = attn_layer
 
-    def oracle_tree(self, lse_in=None):
+    def oracle_tree(self, lse_in=None, policy: int = 0):
         """Stages 1-4 in the oracle; lse_in: [D, B, k] or None (own lse)."""
         w = self.w
-        cfg = oracle.TreeCfg(w.batch, w.vocab, w.top_k, w.depth, w.node_budget, w.threshold)
+        cfg = oracle.TreeCfg(w.batch, w.vocab, w.top_k, w.depth, w.node_budget, w.threshold, policy)
         t = oracle.Tree(cfg)
         fronts = []
         for s in range(w.depth):
@@ -96,9 +96,9 @@ def device_cycle(w: WL.Workload):
     return C, E
 
 
-def make_cfgs(w: WL.Workload, geo: dict):
+def make_cfgs(w: WL.Workload, geo: dict, policy: int = 0):
     from speculative_decoding_dynamic_gb300 import eagle as E
-    cfg = E.TreeCfg(w.batch, w.vocab, w.top_k, w.depth, w.node_budget, w.threshold, w.dtype)
+    cfg = E.TreeCfg(w.batch, w.vocab, w.top_k, w.depth, w.node_budget, w.threshold, w.dtype, policy)
     kv = E.KvCfg(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, geo["layers"], geo["max_len"], w.dtype,
                  geo["seq_stride"], geo["layer_stride"], geo["kv_stride"], geo["pos_stride"])
     return cfg, kv

@@ -208,3 +208,53 @@ def test_own_lse_end_to_end(case):
         assert (np.abs(gaps) <= H.near_tie_tol(w.depth)).any(), f"sequence {b}: tree differs without a near-tie"
     print(f"{name}: {same}/{w.batch} trees identical, {near} near-tie divergences; lse max err {err:.2e}")
     assert same >= w.batch - max(1, w.batch // 16)
+
+
+POLICY_CASES = [(name, pol) for name in ("tiny", "llama8b_b1", "llama8b_b64") for pol in (0, 1, 2)]
+
+
+@pytest.mark.parametrize("case", POLICY_CASES, ids=[f"{n}-policy{p}" for n, p in POLICY_CASES])
+def test_policy_parity(case):
+    """Stages 2-4 under each tree policy (EAGLE-2, confidence-ranked
+    frontier, no rerank) with identical log-prob inputs: frontiers,
+    candidate tables, kept sets and the emitted tree bit-exact; the summed
+    path value of the kept nodes within fp32 rounding of the oracle's."""
+    import torch
+    from speculative_decoding_dynamic_gb300 import cycle as C
+    from speculative_decoding_dynamic_gb300 import eagle as E
+
+    name, policy = case
+    w = WL.WORKLOADS[name]
+    inp = H.Inputs(w, seed=11, planted=True)
+    lse_o = inp.oracle_lse()
+    ot, otr, ofronts = inp.oracle_tree(lse_o, policy=policy)
+    geo = WL.kv_geometry(w, inp.seed, 1)
+    cfg, kv = H.make_cfgs(w, geo, policy=policy)
+    dc = C.DeviceCycle(cfg, kv)
+    draft = H.to_dev(inp.draft)
+    lse_dev = H.to_dev(lse_o)
+    E.eagle_tree_init(cfg, dc.ws)
+    for s in range(w.depth):
+        E.eagle_expand(cfg, dc.ws, s, draft[s], lse_dev[s], dc.row_lse, dc.ftok, dc.fcount)
+        torch.cuda.synchronize()
+        ft, fc = ofronts[s]
+        assert (H.to_host(dc.fcount) == fc).all(), f"frontier count, step {s}"
+        assert (H.to_host(dc.ftok) == ft).all(), f"frontier tokens, step {s}"
+    E.eagle_rerank(cfg, dc.ws)
+    dc.build(H.to_dev(inp.prefix_len), H.to_dev(inp.root))
+    vs = torch.empty(w.batch, dtype=torch.float32, device="cuda")
+    E.eagle_tree_value(cfg, dc.ws, vs)
+    g = _gpu_tree_tables(E, cfg, dc)
+    v = ot.valid.astype(bool)
+    assert (g["valid"] == ot.valid).all()
+    assert (g["token"][v] == ot.token[v]).all() and (g["parent"][v] == ot.parent[v]).all()
+    assert H.isclose_bits(g["logv"][v], ot.logv[v])
+    assert (g["kept"] == ot.kept).all() and (g["n_kept"] == ot.n_kept).all()
+    for key in ("tokens", "parent", "depth", "pos", "n_tree"):
+        assert (H.to_host(getattr(dc, key)) == otr[key]).all(), key
+    assert (H.to_host(dc.mask).view(np.uint32) == otr["mask"]).all(), "mask"
+    want = np.array([ot.value_sum(b) for b in range(w.batch)])
+    got = H.to_host(vs).astype(np.float64)
+    # fp32 terms each within 2 ulp of exp, summed in fp32: relative 1e-5 of the sum
+    assert np.allclose(got, want, rtol=1e-5, atol=1e-6), np.abs(got - want).max()
+    assert dc.status() == 0

@@ -466,3 +466,81 @@ def test_kv_compact_moves_path_kv():
                 # everything else is untouched
                 others = [p for p in range(Lmax) if not (L[b] + 1 <= p <= L[b] + a[b])]
                 assert (c4[b, l, kv, others] == b4[b, l, kv, others]).all()
+
+
+# ------------------------------------------------- ablation policies (§5.2) ---
+
+def _rows(*probs, V=8):
+    """fp32 logit rows log(p) padded with equal small mass (sums to 1)."""
+    out = []
+    for p in probs:
+        rest = (1.0 - sum(p)) / (V - len(p))
+        out.append(np.log(np.array(list(p) + [rest] * (V - len(p)), np.float64)).astype(np.float32))
+    return np.array(out, np.float32)
+
+
+def _landscape():
+    """Hand-built k = 2, D = 3 landscape (values by hand):
+    root -> A 0.69, B 0.30; A -> A1 .5, A2 .44; B -> B1 .95, B2 .04;
+    A1 -> A1a .9; A2 -> A2a .9. Node ids: A 0, B 1, A1 2, A2 3, B1 4, B2 5,
+    A1a 6, A1b 7, A2a 8, A2b 9."""
+    s0 = np.zeros((1, 2, 8), np.float32)
+    s0[0, 0] = _rows((0.69, 0.30))[0]
+    s1 = _rows((0.5, 0.44), (0.95, 0.04))[None]
+    s2 = _rows((0.9, 0.09), (0.9, 0.09))[None]
+    return [s0, s1, s2]
+
+
+def _run(policy, N, steps):
+    t = oracle.Tree(oracle.TreeCfg(1, 8, 2, 3, N, 0.0, policy))
+    fronts = [t.expand(s, logits) for s, logits in enumerate(steps)]
+    t.rerank()
+    return t, fronts
+
+
+def test_confidence_expansion_ranks_the_frontier_by_own_confidence():
+    # value-based: A1 (.345) and A2 (.3036) lead depth 2; confidence-based:
+    # B1 (.95) and A1 (.5) lead, although B1's value (.285) is lower
+    steps = _landscape()[:2]
+    tv, fv = _run(0, 6, steps)
+    tc, fc = _run(1, 6, steps)
+    assert list(tv.fhist[2, 0]) == [2, 3]
+    assert list(tc.fhist[2, 0]) == [4, 2]
+    assert list(fc[1][0][0]) == [0, 0]  # B1 and A1 are both token 0 of their rows
+    # the threshold and the values themselves do not depend on the policy
+    assert np.array_equal(tv.logv, tc.logv)
+
+
+def test_without_rerank_keeps_the_expanded_nodes():
+    steps = _landscape()
+    t2, _ = _run(2, 6, steps)
+    t0, _ = _run(0, 6, steps)
+    kept2 = set(np.flatnonzero(t2.kept[0]))
+    kept0 = set(np.flatnonzero(t0.kept[0]))
+    assert kept2 == {0, 1, 2, 3, 6, 8}  # the frontier of every step (k per depth)
+    assert kept0 == {0, 1, 2, 3, 4, 6}  # top-6 by value: B1 (.285) beats A2a (.2732)
+    # reranking improves the expected acceptance length [EAGLE-2 summary 5.2.2]
+    v0, v2 = t0.value_sum(0), t2.value_sum(0)
+    assert abs(v0 - (0.69 + 0.345 + 0.3036 + 0.30 + 0.3105 + 0.285)) < 1e-3
+    assert abs(v2 - (0.69 + 0.30 + 0.345 + 0.3036 + 0.3105 + 0.27324)) < 1e-3
+    assert v0 > v2
+
+
+def test_rerank_value_never_below_expansion_only_tree():
+    # rerank keeps the N most valuable candidates, a connected set; the nodes
+    # of the expansion phase are one of the connected sets it chooses among
+    for seed in range(6):
+        B, V, k, D, N = 3, 64, 3, 4, 9
+        logits = synth.normal4((D, B, k, V), synth.F32, 2.5, seed=seed, stream=synth.STREAM_DRAFT)
+        t0 = oracle.Tree(oracle.TreeCfg(B, V, k, D, N, 0.0, 0))
+        t2 = oracle.Tree(oracle.TreeCfg(B, V, k, D, N, 0.0, 2))
+        for s in range(D):
+            t0.expand(s, logits[s])
+            t2.expand(s, logits[s])
+        t0.rerank()
+        t2.rerank()
+        for b in range(B):
+            assert t0.value_sum(b) >= t2.value_sum(b) - 1e-9
+            # the expansion-only tree is connected: every kept node's parent is kept or the root
+            kept = np.flatnonzero(t2.kept[b])
+            assert all(t2.parent[b, i] < 0 or t2.kept[b, t2.parent[b, i]] for i in kept)
