@@ -33,7 +33,7 @@ sys.path.insert(0, ROOT)
 
 L2_BYTES = 129 * 1024 * 1024
 METRIC = "draft-verify cycles/s at Llama-8B shape; HBM GB/s & % roofline per kernel"
-POLICIES = {"dynamic": 0, "confidence": 1, "no_rerank": 2}
+POLICIES = {"dynamic": 0, "confidence": 1, "no_rerank": 2, "static": 3}
 
 
 def parse():

@@ -68,7 +68,8 @@ typedef enum { EAGLE_F32 = 0, EAGLE_BF16 = 1 } eagle_dtype;
 typedef enum { EAGLE_VERIFY_GREEDY = 0, EAGLE_VERIFY_LOSSLESS = 1 } eagle_verify_mode;
 
 /* Tree policy [summary 5.2.1, 5.2.2: the ablations of value-based expansion
- * and of reranking]:
+ * and of reranking; tutorial "Watch the Budget Being Spent": the EAGLE-1
+ * fixed shape against the dynamic tree]:
  *   EAGLE_POLICY_DYNAMIC     EAGLE-2: the frontier of each step is the top-k of
  *                            its children by path value; the rerank keeps the
  *                            N most valuable of all drafted nodes.
@@ -77,8 +78,18 @@ typedef enum { EAGLE_VERIFY_GREEDY = 0, EAGLE_VERIFY_LOSSLESS = 1 } eagle_verify
  *                            path value; the rerank is unchanged.
  *   EAGLE_POLICY_NO_RERANK   no rerank: the kept nodes are the ones the
  *                            expansion chose, the frontier of every step (k per
- *                            depth), the N most valuable of them if more. */
-typedef enum { EAGLE_POLICY_DYNAMIC = 0, EAGLE_POLICY_CONFIDENCE = 1, EAGLE_POLICY_NO_RERANK = 2 } eagle_policy;
+ *                            depth), the N most valuable of them if more.
+ *   EAGLE_POLICY_STATIC      a fixed shape, the same for every input: the
+ *                            frontier is chosen by position (child r of
+ *                            frontier slot f ranked by f + r, then by lower
+ *                            node id), and the kept nodes are the frontiers,
+ *                            the first N by depth, then node id. */
+typedef enum {
+    EAGLE_POLICY_DYNAMIC = 0,
+    EAGLE_POLICY_CONFIDENCE = 1,
+    EAGLE_POLICY_NO_RERANK = 2,
+    EAGLE_POLICY_STATIC = 3
+} eagle_policy;
 
 /* Draft-tree problem [summary 4.1, 4.2, App. A; notes EAGLE 2 方法]. */
 typedef struct {

@@ -105,7 +105,7 @@ class TreeCfg:
     depth: int
     node_budget: int
     threshold: float = 0.0
-    policy: int = 0  # 0 EAGLE-2, 1 confidence-based expansion, 2 without reranking
+    policy: int = 0  # 0 EAGLE-2, 1 confidence-based expansion, 2 without reranking, 3 static shape
 
     @property
     def C(self) -> int:

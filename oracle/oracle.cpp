@@ -180,6 +180,13 @@ void oracle_tree_init(int B, int C, int k, int32_t* cand_token, int32_t* cand_pa
 // value-based expansion compared with confidence-based): the next frontier is
 // ranked by the child's own confidence lp = x - lse instead of its value; the
 // threshold still applies to the value. cand_lp [B, C] receives lp.
+//
+// policy 3 (the EAGLE-1 static shape that the tutorial's widget sets against
+// the dynamic tree, "Watch the Budget Being Spent": the same branching
+// pattern for every context): the next frontier is chosen by position only,
+// child r of frontier slot f ranked by f + r ascending, then by lower node id
+// (reading: a fixed triangular pattern that favours the first children of
+// the first slots, as a hand-shaped tree does).
 int oracle_expand(int B, int V, int k, int step, int dtype, float log_thr, int policy, const void* logits_s,
                   const float* lse_in, int C, int32_t* cand_token, int32_t* cand_parent,
                   int32_t* cand_depth, float* cand_logv, float* cand_lp, uint8_t* cand_valid, int32_t* fnode,
@@ -221,13 +228,24 @@ int oracle_expand(int B, int V, int k, int step, int dtype, float log_thr, int p
                 int64_t at = static_cast<int64_t>(b) * C + id;
                 if (cand_valid[at] && cand_logv[at] >= log_thr) elig.push_back(id);
             }
-        const float* rank_by = policy == 1 ? cand_lp : cand_logv;
-        std::sort(elig.begin(), elig.end(), [&](int a, int c) {
-            float va = rank_by[static_cast<int64_t>(b) * C + a];
-            float vc = rank_by[static_cast<int64_t>(b) * C + c];
-            if (va != vc) return va > vc;
-            return a < c;
-        });
+        if (policy == 3) {
+            auto pos = [&](int id) {
+                const int i = static_cast<int>(id - base);
+                return i / k + i % k;
+            };
+            std::sort(elig.begin(), elig.end(), [&](int a, int c) {
+                if (pos(a) != pos(c)) return pos(a) < pos(c);
+                return a < c;
+            });
+        } else {
+            const float* rank_by = policy == 1 ? cand_lp : cand_logv;
+            std::sort(elig.begin(), elig.end(), [&](int a, int c) {
+                float va = rank_by[static_cast<int64_t>(b) * C + a];
+                float vc = rank_by[static_cast<int64_t>(b) * C + c];
+                if (va != vc) return va > vc;
+                return a < c;
+            });
+        }
         const int nf = std::min<int>(k, static_cast<int>(elig.size()));
         for (int f = 0; f < k; ++f) {
             fnode[b * k + f] = f < nf ? elig[f] : -1;
@@ -252,11 +270,14 @@ int oracle_expand(int B, int V, int k, int step, int dtype, float log_thr, int p
 // frontier of every step 1..D (fhist [D+1, B, k], -1 = none; reading: these
 // are the tokens drafted without a rerank, k per depth), of which the first N
 // by the same order are kept.
+//
+// policy 3 (static shape): the same candidates as policy 2, the first N by
+// depth, then lower node id: a shape that does not depend on the values.
 int oracle_rerank(int B, int C, int N, int policy, int D, int k, const int32_t* fhist, const int32_t* cand_depth,
                   const float* cand_logv, const uint8_t* cand_valid, uint8_t* kept, int32_t* n_kept) {
     for (int b = 0; b < B; ++b) {
         std::vector<int> ids;
-        if (policy == 2) {
+        if (policy == 2 || policy == 3) {
             for (int s = 1; s <= D; ++s)
                 for (int f = 0; f < k; ++f) {
                     const int id = fhist[(static_cast<int64_t>(s) * B + b) * k + f];
@@ -268,7 +289,7 @@ int oracle_rerank(int B, int C, int N, int policy, int D, int k, const int32_t* 
         }
         std::sort(ids.begin(), ids.end(), [&](int a, int c) {
             int64_t ia = static_cast<int64_t>(b) * C + a, ic = static_cast<int64_t>(b) * C + c;
-            if (cand_logv[ia] != cand_logv[ic]) return cand_logv[ia] > cand_logv[ic];
+            if (policy != 3 && cand_logv[ia] != cand_logv[ic]) return cand_logv[ia] > cand_logv[ic];
             if (cand_depth[ia] != cand_depth[ic]) return cand_depth[ia] < cand_depth[ic];
             return a < c;
         });

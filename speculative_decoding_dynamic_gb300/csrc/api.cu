@@ -34,7 +34,7 @@ int resolve(const eagle_tree_cfg* cfg, TreeDims* d) {
     if (V < k) return EAGLE_ERR_INVALID_ARG;
     if (cfg->logit_dtype != EAGLE_F32 && cfg->logit_dtype != EAGLE_BF16) return EAGLE_ERR_INVALID_ARG;
     if (std::isnan(cfg->threshold)) return EAGLE_ERR_INVALID_ARG;
-    if (cfg->policy < EAGLE_POLICY_DYNAMIC || cfg->policy > EAGLE_POLICY_NO_RERANK) return EAGLE_ERR_INVALID_ARG;
+    if (cfg->policy < EAGLE_POLICY_DYNAMIC || cfg->policy > EAGLE_POLICY_STATIC) return EAGLE_ERR_INVALID_ARG;
     const long C = k + static_cast<long>(D - 1) * k * k;
     const int T = N + 1;
     if (C > kMaxCandidates || T > kMaxSlots) return EAGLE_ERR_UNSUPPORTED;

@@ -166,6 +166,39 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// Three-input maximum (NaN operands are dropped, like fmaxf).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Largest of 32 values: a tree of three-input maxima (depth 4).
+__device__ __forceinline__ float max32(const float (&v)[32]) {
+    float t[11];
+#pragma unroll
+    for (int q = 0; q < 10; ++q) t[q] = fmax3(v[3 * q], v[3 * q + 1], v[3 * q + 2]);
+    t[10] = fmaxf(v[30], v[31]);
+    return fmaxf(fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmax3(t[6], t[7], t[8])), fmaxf(t[9], t[10]));
+}
+
+// Packed fp32 pairs: (lo, hi) in one 64-bit register; two results per instruction.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    return (static_cast<uint64_t>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ float f2_lo(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float f2_hi(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 __device__ __forceinline__ void named_sync_softmax() { asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory"); }
 // The four softmax warps that serve one TMEM lane quarter (the rows 32 q4 ..
 // 32 q4 + 31, one warp per column quarter) meet on barrier 2 + q4.
@@ -339,6 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = i0 + r / p.G;                      // tree slot of the row
         const int g = r % p.G;
         const float sc = p.scale_log2;
+        // a lane quarter whose 32 rows are all past the problem's rows does no
+        // arithmetic (it still takes part in every barrier and V clearing)
+        const bool quarter_live = rb * kBM + q4 * 32 < p.G * p.T;
         float m_use = 0.0f, lh = 0.0f;                   // lh: this quarter's share of the row sum
         bool seen = false;
         bool ok = true;
@@ -351,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok && !__all_sync(0xffffffffu, mbar_wait_sleep(&bar_s_full[st], (jj >> 1) & 1))) ok = false;
             tc_fence_after();
             float sv[32];
-            if (ok) tmem_ld32(tmem_s + st * kBN + lane_off + cb, sv);
+            if (ok && quarter_live) tmem_ld32(tmem_s + st * kBN + lane_off + cb, sv);
             else
 #pragma unroll
                 for (int e = 0; e < 32; ++e) sv[e] = -INFINITY;
@@ -376,21 +412,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (j0 <= -32) tree = 0u;
                 vis = pre | tree;
             }
-            const bool full = vis == 0xffffffffu;
-            float mr = -INFINITY;  // raw maximum (the scale is positive)
-            if (full) {
+            if (vis != 0xffffffffu) {  // invisible keys: -inf, so their exponentials are 0
 #pragma unroll
-                for (int e = 0; e < 32; ++e) mr = fmaxf(mr, sv[e]);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    if ((vis >> e) & 1u) mr = fmaxf(mr, sv[e]);
+                for (int e = 0; e < 32; ++e) sv[e] = ((vis >> e) & 1u) ? sv[e] : -INFINITY;
             }
-            float mx = mr * sc;
-            xch[jj & 1][cq][r] = mx;
-            named_sync_rows(q4);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) mx = fmaxf(mx, xch[jj & 1][c][r]);
+            float mx = max32(sv) * sc;  // the scale is positive
+            if (quarter_live) {
+                xch[jj & 1][cq][r] = mx;
+                named_sync_rows(q4);
+                mx = fmaxf(fmaxf(xch[jj & 1][0][r], xch[jj & 1][1][r]), fmaxf(xch[jj & 1][2][r], xch[jj & 1][3][r]));
+            }
             bool rescale = false;
             float alpha = 1.0f;
             if (mx > -INFINITY) {
@@ -404,28 +435,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     lh *= alpha;
                 }
             }
-            float sa = 0.0f, sb = 0.0f;
             uint32_t pk[16];
-            if (full) {
+            if (quarter_live) {
+                // p = 2^(s sc - m_use), two per packed multiply-add; four packed partial sums
+                const uint64_t sc2 = f2_pack(sc, sc), nm2 = f2_pack(-m_use, -m_use);
+                uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    const float p0 = ex2_approx(fmaf(sv[e], sc, -m_use));
-                    const float p1 = ex2_approx(fmaf(sv[e + 1], sc, -m_use));
-                    sa += p0;
-                    sb += p1;
+                    const uint64_t z = f2_fma(f2_pack(sv[e], sv[e + 1]), sc2, nm2);
+                    const float p0 = ex2_approx(f2_lo(z));
+                    const float p1 = ex2_approx(f2_hi(z));
+                    acc[(e >> 1) & 3] = f2_add(acc[(e >> 1) & 3], f2_pack(p0, p1));
                     pk[e >> 1] = pack_bf16(p0, p1);
                 }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const float p0 = ((vis >> e) & 1u) ? ex2_approx(fmaf(sv[e], sc, -m_use)) : 0.0f;
-                    const float p1 = ((vis >> (e + 1)) & 1u) ? ex2_approx(fmaf(sv[e + 1], sc, -m_use)) : 0.0f;
-                    sa += p0;
-                    sb += p1;
-                    pk[e >> 1] = pack_bf16(p0, p1);
-                }
+                const uint64_t s2 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+                lh += f2_lo(s2) + f2_hi(s2);
             }
-            lh += sa + sb;
             if (!ok) continue;
             if (jj > 0) {  // PV(j-1) done: P buffer free, O stable
                 if (!__all_sync(0xffffffffu, mbar_wait_sleep(&bar_o_full, (jj - 1) & 1))) {
@@ -435,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 // tcgen05.ld/st are warp-collective: rescale if any row of the warp needs it
                 // (alpha = 1 for the others).
-                if (__any_sync(0xffffffffu, rescale)) {
+                if (quarter_live && __any_sync(0xffffffffu, rescale)) {
                     float o[32];
                     tmem_ld32(tmem_o + lane_off + cb, o);
 #pragma unroll
@@ -444,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             // P into TMEM: row r = lane, this quarter's 32 keys = columns 16 cq .. 16 cq + 15
-            tmem_st16(tmem_p + lane_off + cq * 16, pk);
+            if (quarter_live) tmem_st16(tmem_p + lane_off + cq * 16, pk);
             // V rows of keys that no row can see may hold anything (even NaN):
             // zero them so that 0 * V stays 0 in the MMA (each V row is 2 x 128
             // bytes; this thread clears 64 of them).

@@ -16,13 +16,14 @@
 // lane, and keeps its running statistics in registers across chunks.
 //
 // Expansion, one pass over the data: per lane a running maximum and a
-// rescaled exp-sum (online normaliser); per warp a buffer of top-k candidates
-// admitted by a key threshold tau. tau starts at the k-th largest lane
-// maximum of the first chunk (k distinct elements reach it, so every element
-// of the row's top-k does), is shared across the CTA through an atomic
-// maximum in shared memory, and rises to the k-th best buffered key whenever
-// a warp compacts its full buffer. Keys are (value, -id): unique, so ties go
-// to the lower token id. Warp, CTA and cluster results are merged by rank
+// rescaled exp-sum (online normaliser), and the maximum of each lane group
+// (the lane's four vectors of one chunk). After the pass, the admission key
+// tau = the largest over the warps of the warp's k-th largest lane maximum
+// (k distinct elements reach it, so every element of the segment's top-k
+// does, and lies in a group whose maximum reaches it). Only those groups are
+// read again (from the stages when the segment stayed resident, else from
+// L2) and their keys >= tau ranked. Keys are (value, -id): unique, so ties go
+// to the lower token id. CTA and cluster results are merged by rank
 // selection (each key counts the keys above it). Partial results are pushed
 // into the cluster leader's shared memory before one cluster barrier. The
 // per-sequence tail (frontier selection / acceptance walk) runs in the
@@ -577,31 +578,46 @@ __global__ void __launch_bounds__(kRowThreads, 3) expand_kernel(TreeDims d, Tree
     if (!sm.last) return;
     __threadfence();
     const int nsel = F * d.k;
-    uint64_t* sel = reinterpret_cast<uint64_t*>(dyn_smem);  // the ring is idle now
+    // the ring is idle now: candidate keys, their tokens, the chosen tokens
+    uint64_t* sel = reinterpret_cast<uint64_t*>(dyn_smem);
+    int32_t* sel_tok = reinterpret_cast<int32_t*>(dyn_smem + kMaxTopK * kMaxTopK * sizeof(uint64_t));
+    int32_t* top_tok = sel_tok + kMaxTopK * kMaxTopK;
     for (int i = tid; i < nsel; i += kRowThreads) {
         const int id = base + i;
         const size_t at = static_cast<size_t>(b) * d.C + id;
         const bool valid = __ldcg(reinterpret_cast<const unsigned char*>(&w.cand_valid[at])) != 0;
         const float lv = __ldcg(&w.cand_logv[at]);
-        // ranked by value (EAGLE-2) or by the child's own confidence (policy 1)
-        const float rank_by = d.policy == 1 ? __ldcg(&w.cand_lp[at]) : lv;
+        // ranked by value (EAGLE-2), by the child's own confidence (policy 1),
+        // or by position f + r within the step (static shape, policy 3)
+        const float rank_by = d.policy == 1   ? __ldcg(&w.cand_lp[at])
+                              : d.policy == 3 ? -static_cast<float>(i / d.k + i % d.k)
+                                              : lv;
+        sel_tok[i] = __ldcg(&w.cand_token[at]);
         sel[i] = (valid && lv >= d.log_thr) ? make_key(rank_by, static_cast<uint32_t>(id)) : 0ull;
     }
+    if (tid == 0 && (nsel & 1)) sel[nsel] = 0ull;  // pad to pairs
     if (tid < kMaxTopK) sm.top[tid] = 0ull;
     __syncthreads();
+    const ulonglong2* sp = reinterpret_cast<const ulonglong2*>(sel);
     for (int i = tid; i < nsel; i += kRowThreads) {
         const uint64_t key = sel[i];
         if (key == 0ull) continue;
         int r = 0;
-        for (int j = 0; j < nsel; ++j) r += sel[j] > key;
-        if (r < d.k) sm.top[r] = key;
+        for (int j = 0; j < (nsel + 1) / 2; ++j) {
+            const ulonglong2 q = sp[j];
+            r += (q.x > key) + (q.y > key);
+        }
+        if (r < d.k) {
+            sm.top[r] = key;
+            top_tok[r] = sel_tok[i];
+        }
     }
     __syncthreads();
     if (tid < d.k) {
         const uint64_t key = sm.top[tid];
         const int id = key ? static_cast<int>(key_id(key)) : -1;
         w.fnode[((step + 1) * d.B + b) * d.k + tid] = id;
-        ftok_out[b * d.k + tid] = id >= 0 ? __ldcg(&w.cand_token[static_cast<size_t>(b) * d.C + id]) : -1;
+        ftok_out[b * d.k + tid] = id >= 0 ? top_tok[tid] : -1;
     }
     if (tid == 0) {
         int cnt = 0;
@@ -1137,10 +1153,11 @@ cudaError_t launch_expand(const TreeDims& d, const TreeWs& ws, int step, const v
     TreeDims dd = d;
     TreeWs ww = ws;
     // after the pass the stage memory holds the candidate groups and keys of
-    // the segment's top-k and, in the last CTA of a sequence, the frontier keys
+    // the segment's top-k and, in the last CTA of a sequence, the frontier
+    // candidates (keys and tokens)
     const int scratch = p.nch * kConsumers * 4 + 512 * 8;  // candidate groups + keys
-    const int smem = std::max(static_cast<int>(kMaxTopK * kMaxTopK * sizeof(uint64_t)),
-                              p.nch <= p.stages ? p.stages * kRowChunkBytes + scratch : std::max(p.smem, scratch));
+    const int pick = kMaxTopK * kMaxTopK * (8 + 4) + kMaxTopK * 4 + 16;
+    const int smem = std::max(pick, p.nch <= p.stages ? p.stages * kRowChunkBytes + scratch : std::max(p.smem, scratch));
     int seg = p.seg, ns = p.stages, smem_bytes = smem;
     void* args[] = {&dd,
                     &ww,

@@ -52,7 +52,9 @@ constexpr int kSortThreads = 512;
 // Key of a candidate: value first (larger), then lower node id. Node ids are
 // depth-major, so for equal values the lower id is also the shallower node.
 // Invalid candidates get key 0 and sort last. Without rerank (policy 2) only
-// the nodes the expansion chose (the frontier of steps 1..D) are candidates.
+// the nodes the expansion chose (the frontier of steps 1..D) are candidates;
+// the static shape (policy 3) takes the same candidates keyed by depth
+// (shallower first), then lower id, so the kept shape ignores the values.
 __global__ void __launch_bounds__(kSortThreads) rerank_kernel(TreeDims d, TreeWs w, int P) {
     __shared__ uint64_t keys[kMaxCandidates];
     __shared__ uint8_t chosen[kMaxCandidates];
@@ -62,7 +64,8 @@ __global__ void __launch_bounds__(kSortThreads) rerank_kernel(TreeDims d, TreeWs
     pdl_launch_dependents();
     pdl_wait_prior();
     if (tid == 0) n_valid = 0;
-    if (d.policy == 2) {
+    const bool frontiers_only = d.policy == 2 || d.policy == 3;
+    if (frontiers_only) {
         for (int i = tid; i < d.C; i += kSortThreads) chosen[i] = 0;
         __syncthreads();
         for (int q = tid; q < d.D * d.k; q += kSortThreads) {
@@ -76,8 +79,10 @@ __global__ void __launch_bounds__(kSortThreads) rerank_kernel(TreeDims d, TreeWs
         uint64_t key = 0;
         if (i < d.C) {
             const size_t at = static_cast<size_t>(b) * d.C + i;
-            if (w.cand_valid[at] && (d.policy != 2 || chosen[i])) {
-                key = make_key(w.cand_logv[at], static_cast<uint32_t>(i));
+            if (w.cand_valid[at] && (!frontiers_only || chosen[i])) {
+                // static shape: by depth (shallower first), not by value
+                const float v = d.policy == 3 ? -static_cast<float>(w.cand_depth[at]) : w.cand_logv[at];
+                key = make_key(v, static_cast<uint32_t>(i));
                 ++local;
             }
             w.kept[at] = 0;

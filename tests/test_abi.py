@@ -56,9 +56,9 @@ def test_workspace_bytes_and_invalid_configs(E):
     assert E.eagle_workspace_bytes(_cfg(E, vocab=1000)) > 0
     assert E.eagle_workspace_bytes(_cfg(E, vocab=3, top_k=4)) == 0
     assert E.eagle_workspace_bytes(_cfg(E, logit_dtype=7)) == 0
-    for pol in (0, 1, 2):
+    for pol in (0, 1, 2, 3):
         assert E.eagle_workspace_bytes(_cfg(E, policy=pol)) > 0
-    assert E.eagle_workspace_bytes(_cfg(E, policy=3)) == 0
+    assert E.eagle_workspace_bytes(_cfg(E, policy=4)) == 0
     assert E.eagle_workspace_bytes(_cfg(E, policy=-1)) == 0
 
 

@@ -210,13 +210,13 @@ def test_own_lse_end_to_end(case):
     assert same >= w.batch - max(1, w.batch // 16)
 
 
-POLICY_CASES = [(name, pol) for name in ("tiny", "llama8b_b1", "llama8b_b64") for pol in (0, 1, 2)]
+POLICY_CASES = [(name, pol) for name in ("tiny", "llama8b_b1", "llama8b_b64") for pol in (0, 1, 2, 3)]
 
 
 @pytest.mark.parametrize("case", POLICY_CASES, ids=[f"{n}-policy{p}" for n, p in POLICY_CASES])
 def test_policy_parity(case):
     """Stages 2-4 under each tree policy (EAGLE-2, confidence-ranked
-    frontier, no rerank) with identical log-prob inputs: frontiers,
+    frontier, no rerank, static shape) with identical log-prob inputs: frontiers,
     candidate tables, kept sets and the emitted tree bit-exact; the summed
     path value of the kept nodes within fp32 rounding of the oracle's."""
     import torch
