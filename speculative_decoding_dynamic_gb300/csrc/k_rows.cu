@@ -671,6 +671,40 @@ __device__ __forceinline__ uint64_t fixed_mass(float x, float m, float inv_t) {
     return sh >= 0 ? static_cast<uint64_t>(sig) << sh : static_cast<uint64_t>(sig >> (-sh));
 }
 
+// The masses of two elements at once: the same fixed-order exp, its fp32
+// operations done as packed pairs (each lane of a pair rounds exactly as the
+// scalar operation), then per element the significand placed 24 bits up and
+// shifted right by 24 - (exponent + n + 17), i.e. floor(p * 2^(n + 40)); an
+// argument below -32 shifts everything out. Equal to fixed_mass(x0) +
+// fixed_mass(x1).
+__device__ __forceinline__ uint64_t pair_mass(float x0, float x1, uint64_t neg_m2, uint64_t inv_t2) {
+    const uint64_t z = f2_mul(f2_add(f2_pack(x0, x1), neg_m2), inv_t2);
+    const uint64_t t = f2_fma(z, f2_pack(0x1.715476p+0f, 0x1.715476p+0f), f2_pack(12582912.0f, 12582912.0f));
+    const uint64_t n = f2_add(t, f2_pack(-12582912.0f, -12582912.0f));
+    uint64_t r = f2_fma(n, f2_pack(-0x1.62e4p-1f, -0x1.62e4p-1f), z);
+    r = f2_fma(n, f2_pack(-0x1.7f7d1cp-20f, -0x1.7f7d1cp-20f), r);
+    uint64_t p = f2_fma(f2_pack(0x1.a01a02p-13f, 0x1.a01a02p-13f), r, f2_pack(0x1.6c16c2p-10f, 0x1.6c16c2p-10f));
+    p = f2_fma(p, r, f2_pack(0x1.111112p-7f, 0x1.111112p-7f));
+    p = f2_fma(p, r, f2_pack(0x1.555556p-5f, 0x1.555556p-5f));
+    p = f2_fma(p, r, f2_pack(0x1.555556p-3f, 0x1.555556p-3f));
+    p = f2_fma(p, r, f2_pack(0.5f, 0.5f));
+    p = f2_fma(p, r, f2_pack(1.0f, 1.0f));
+    p = f2_fma(p, r, f2_pack(1.0f, 1.0f));
+    uint64_t s = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t pb = static_cast<uint32_t>(p >> (32 * h));
+        const uint32_t tb = static_cast<uint32_t>(t >> (32 * h));
+        const float zh = __uint_as_float(static_cast<uint32_t>(z >> (32 * h)));
+        // 24 - sh with sh = (pb >> 23) - 127 + (tb - 0x4B400000) + 17
+        int shr = 134 - static_cast<int>(pb >> 23) - (static_cast<int>(tb) - 0x4B400000);
+        if (!(zh >= -32.0f)) shr = 63;
+        const uint64_t sig48 = static_cast<uint64_t>((pb & 0x7FFFFFu) | 0x800000u) << 24;
+        s += sig48 >> shr;
+    }
+    return s;
+}
+
 struct VerifySmem {
     RowRing ring;
     uint64_t wkey[kConsumerWarps];
@@ -809,6 +843,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
         // ---- pass 2: integer masses of the resident segment, one per (chunk, warp) ----
         const int nch_full = nslot / (cpr * kConsumerWarps);
         unsigned long long wtot = 0;
+        const uint64_t neg_m2 = f2_pack(-M, -M), inv_t2 = f2_pack(inv_t, inv_t);
         if (warp < kConsumerWarps) {
             for (int c = 0; c < nch_full; ++c) {
                 unsigned long long s = 0;
@@ -822,7 +857,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
                         float x[EPV];
                         unpack16<DT>(vb[v], x);
 #pragma unroll
-                        for (int e = 0; e < EPV; ++e) s += fixed_mass(x[e], M, inv_t);
+                        for (int e = 0; e < EPV; e += 2) s += pair_mass(x[e], x[e + 1], neg_m2, inv_t2);
                     }
                 }
                 s = warp_sum_u64(s);
