@@ -4,24 +4,28 @@
 // form M = G*T query rows (row r <-> slot r / G, head hk*G + r % G, matching
 // the [B, T, Hq, d] layout of Q). One CTA owns a 128-row block of them and a
 // range of 128-key tiles of the sequence's keys (prefix [0, L_b) then the
-// tree slots at L_b + j), and runs, per key tile:
+// tree slots at L_b + j), and runs, per key tile j:
 //   S = Q K^T        tcgen05.mma kind::f16, bf16 operands from shared memory,
-//                    fp32 accumulator in tensor memory (TMEM columns 0..127)
-//   P = softmax part one thread per row (TMEM lane = row): scale, tree mask,
-//                    exponentials in the log2 domain against a reference
-//                    maximum, P written as bf16 to shared memory in the
-//                    128B-swizzled K-major layout
-//   O += P V         tcgen05.mma accumulating in TMEM columns 128..255, V read
-//                    MN-major; the reference maximum is raised (O and the row
+//                    fp32 accumulator in tensor memory, double buffered
+//                    (TMEM columns 128 (j & 1) ..), so QK^T of tile j+1 runs
+//                    while the softmax works on tile j
+//   P = softmax part four threads per row (TMEM lane = row, 32 key columns
+//                    each; row maxima exchanged in shared memory): scale,
+//                    tree mask, exponentials in the log2 domain against a
+//                    reference maximum, P written as bf16 pairs into tensor
+//                    memory (double buffered, columns 384 + 64 (j & 1) ..)
+//   O += P V         tcgen05.mma with A = P read from tensor memory, V from
+//                    shared memory (MN-major), accumulating in TMEM columns
+//                    256..383; the reference maximum is raised (O and the row
 //                    sum rescaled in place) only when a tile's maximum exceeds
 //                    it by more than 2^8, so exponentials stay below 256
-// PV of tile j and QK^T of tile j+1 are issued back to back.
-// K/V tiles arrive by TMA (cp.async.bulk.tensor, 128B swizzle) into a
-// two-stage ring; Q once per CTA. Warp 0 issues TMA, one thread of warp 1
-// issues the MMAs, warps 2..5 do the softmax; mbarriers order them, every
-// wait is bounded. Key ranges of one (b, hk, row block) may be split over
-// CTAs (split-KV): each writes (O, max, sum) partials and the last CTA to
-// arrive on a per-unit counter merges them (log-sum-exp combine).
+// K and V tiles arrive by TMA (cp.async.bulk.tensor, 128B swizzle) into
+// their own rings (a K stage frees after QK^T, a V stage after PV), issued
+// by two lanes of warp 0; one thread of warp 1 issues every MMA; warps 2..17
+// do the softmax. mbarriers order them, every wait is bounded. Key ranges of
+// one (b, hk, row block) may be split over CTAs (split-KV): each writes
+// (O, max, sum) partials and the last CTA to arrive on a per-unit counter
+// merges them (log-sum-exp combine).
 //
 // Keys of slot i: every prefix position and the tree slots set in mask row i
 // ["EAGLE" notes, EAGLE 方法: Medusa-style tree attention verifies every
@@ -58,7 +62,7 @@ constexpr int kSmemQ = 0;
 constexpr int kSmemK = kTile;                      // K stage s at kSmemK + s * kTile
 constexpr int kSmemV = kSmemK + kKStages * kTile;  // V stage s at kSmemV + s * kTile
 constexpr int kSmemBytes = kSmemV + kVStages * kTile;  // 192 KB
-constexpr int kTmemCols = 512;  // S double buffer (2 x 128 columns), O (128), P (64: bf16 pairs)
+constexpr int kTmemCols = 512;  // S double buffer (2 x 128 columns), O (128), P double buffer (2 x 64: bf16 pairs)
 constexpr int kMaxW = kMaxSlots / 32;
 
 struct TcParams {
@@ -182,23 +186,6 @@ __device__ __forceinline__ float max32(const float (&v)[32]) {
     return fmaxf(fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmax3(t[6], t[7], t[8])), fmaxf(t[9], t[10]));
 }
 
-// Packed fp32 pairs: (lo, hi) in one 64-bit register; two results per instruction.
-__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
-    return (static_cast<uint64_t>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
-}
-__device__ __forceinline__ float f2_lo(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
-__device__ __forceinline__ float f2_hi(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
 __device__ __forceinline__ void named_sync_softmax() { asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory"); }
 // The four softmax warps that serve one TMEM lane quarter (the rows 32 q4 ..
 // 32 q4 + 31, one warp per column quarter) meet on barrier 2 + q4.
@@ -275,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = tmem_holder;
     const uint32_t tmem_s = tmem, tmem_o = tmem + 256;  // S buffer b at tmem_s + 128 b
-    const uint32_t tmem_p = tmem + 384;                 // P(j): row = lane, keys as bf16 pairs
+    const uint32_t tmem_p = tmem + 384;                 // P(j) at tmem_p + 64 (j & 1): row = lane, bf16 pairs
 
     unsigned char* sQ = smem + kSmemQ;
 
@@ -328,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t aV = smem_u32(smem + kSmemV + sp * kTile);
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)  // A = P from TMEM: 16 keys = 8 columns per MMA
-                    mma_bf16_ts(tmem_o, tmem_p + kk * 8, smem_desc(aV + kk * 2048, kHalf, 1024), id_pv,
+                    mma_bf16_ts(tmem_o, tmem_p + (jp & 1) * 64 + kk * 8, smem_desc(aV + kk * 2048, kHalf, 1024), id_pv,
                                 (jp > 0 || kk > 0) ? 1 : 0);
                 mma_commit(&bar_v_empty[sp]);
                 mma_commit(&bar_o_full);
@@ -452,24 +439,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 lh += f2_lo(s2) + f2_hi(s2);
             }
             if (!ok) continue;
-            if (jj > 0) {  // PV(j-1) done: P buffer free, O stable
+            // P is double buffered: P(j) goes to buffer j & 1, whose last reader
+            // PV(j-2) is complete (it precedes QK(j) on the tensor pipe). O is
+            // waited for only when it must be rescaled: PV(j-1) done, O stable.
+            // tcgen05.ld/st are warp-collective: rescale if any row of the warp
+            // needs it (alpha = 1 for the others).
+            if (jj > 0 && quarter_live && __any_sync(0xffffffffu, rescale)) {
                 if (!__all_sync(0xffffffffu, mbar_wait_sleep(&bar_o_full, (jj - 1) & 1))) {
                     ok = false;
                     continue;
                 }
                 tc_fence_after();
-                // tcgen05.ld/st are warp-collective: rescale if any row of the warp needs it
-                // (alpha = 1 for the others).
-                if (quarter_live && __any_sync(0xffffffffu, rescale)) {
-                    float o[32];
-                    tmem_ld32(tmem_o + lane_off + cb, o);
+                float o[32];
+                tmem_ld32(tmem_o + lane_off + cb, o);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                    tmem_st32(tmem_o + lane_off + cb, o);
-                }
+                for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                tmem_st32(tmem_o + lane_off + cb, o);
             }
             // P into TMEM: row r = lane, this quarter's 32 keys = columns 16 cq .. 16 cq + 15
-            if (quarter_live) tmem_st16(tmem_p + lane_off + cq * 16, pk);
+            if (quarter_live) tmem_st16(tmem_p + (jj & 1) * 64 + lane_off + cq * 16, pk);
             // V rows of keys that no row can see may hold anything (even NaN):
             // zero them so that 0 * V stays 0 in the MMA (each V row is 2 x 128
             // bytes; this thread clears 64 of them).
@@ -484,9 +472,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint4* z = reinterpret_cast<uint4*>(sV + r * 128 + (cq & 1) * 64);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) z[q] = make_uint4(0, 0, 0, 0);
+                    fence_proxy_async_smem();  // the MMA reads V through the async proxy
                 }
             }
-            fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&bar_p_full);
         }
