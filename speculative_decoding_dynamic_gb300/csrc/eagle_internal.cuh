@@ -192,6 +192,21 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
+// Hint: bring [src, src + bytes) into L2 (16-byte aligned, bytes a multiple
+// of 16). Reads nothing into the CTA, so it may be issued before the
+// programmatic-dependency wait: L2 is the point of coherence, a later write
+// by the previous kernel still lands before the copy issued after the wait.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+// The head of a row segment (at most its first two 16 KB chunks: enough to
+// hide the first copies' latency without crowding L2 when many CTAs are in
+// flight), one hint per 16 KB.
+__device__ __forceinline__ void prefetch_l2_segment(const char* src, int bytes) {
+    bytes = min(bytes, 2 * 16384);
+    for (int off = 0; off < bytes; off += 16384) prefetch_l2(src + off, static_cast<uint32_t>(min(16384, bytes - off)));
+}
+
 // Global loads that bypass L1 (data written by other CTAs of the same launch).
 __device__ __forceinline__ int ld_cg_i32(const int* p) { return __ldcg(p); }
 __device__ __forceinline__ float ld_cg_f32(const float* p) { return __ldcg(p); }

@@ -80,6 +80,14 @@ struct TcParams {
 
 // ---------------------------------------------------------------- PTX ---
 
+// Hint: bring one tile of a tensor map into L2 (no shared memory written).
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int c0, int c1, int c2, int c3) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
                                             uint64_t* bar) {
     asm volatile(
@@ -211,6 +219,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int b = blockIdx.z / p.Hkv, hk = blockIdx.z % p.Hkv;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_launch_dependents();
+    // Q and the first K/V tiles of this CTA's key range into L2 while the
+    // previous kernel finishes (hints only; a tile past the sequence's keys
+    // is simply not used)
+    if (warp == 0 && lane < 2) {
+        const int key0 = split * p.tps * kBN;
+        if (lane == 0) {
+            tma_prefetch_4d(&tm_q, 0, hk * p.G, rb * (kBM / p.G), b);
+            tma_prefetch_4d(&tm_q, 64, hk * p.G, rb * (kBM / p.G), b);
+        }
+        const CUtensorMap* map = lane == 0 ? &tm_k : &tm_v;
+        for (int jj = 0; jj < 2 && key0 + jj * kBN < p.max_len; ++jj) {
+            tma_prefetch_4d(map, 0, hk, key0 + jj * kBN, b);
+            tma_prefetch_4d(map, 64, hk, key0 + jj * kBN, b);
+        }
+    }
     pdl_wait_prior();
     const int L = p.prefix_len[b];
     const int n = p.n_tree[b];

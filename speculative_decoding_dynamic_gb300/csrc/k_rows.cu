@@ -57,7 +57,7 @@ constexpr int kVecPerWarp = 32 * kVecPerLane;
 static_assert(kVecPerWarp * kConsumerWarps * 16 == kRowChunkBytes, "chunk geometry");
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kMaxSegChunks = 8;  // chunks of one CTA's row segment in expansion
-constexpr int kExpandStages = 4;
+constexpr int kExpandStages = 2;  // four CTAs per SM (registers and shared memory)
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ------------------------------------------------------------ helpers ---
@@ -391,7 +391,7 @@ __device__ __forceinline__ void segment_topk(ExpandSmem& sm, const unsigned char
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kRowThreads, 3) expand_kernel(TreeDims d, TreeWs w, int step, int seg, int ns,
+__global__ void __launch_bounds__(kRowThreads, 4) expand_kernel(TreeDims d, TreeWs w, int step, int seg, int ns,
                                                                  int smem_bytes, const void* __restrict__ logits,
                                                                  const float* __restrict__ lse_in,
                                                                  float* __restrict__ row_lse,
@@ -405,10 +405,17 @@ __global__ void __launch_bounds__(kRowThreads, 3) expand_kernel(TreeDims d, Tree
     const int row = blockIdx.y;
     const int b = row / d.k, f = row % d.k;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int ES = DT == 1 ? 2 : 4;
     pdl_launch_dependents();
+    // the head of the segment into L2 while the previous kernel finishes (rows
+    // of slots that turn out empty are prefetched too: they are inside the input)
+    if (tid == kProducerWarp * 32) {
+        const int cp = rank * seg;
+        const int np = max(0, min(seg, d.V - cp));
+        prefetch_l2_segment(static_cast<const char*>(logits) + (static_cast<size_t>(row) * d.V + cp) * ES, np * ES);
+    }
     pdl_wait_prior();
     const int F = w.fcount[step * d.B + b];
-    constexpr int ES = DT == 1 ? 2 : 4;
     constexpr int EPV = 16 / ES;
     constexpr int CE = kRowChunkBytes / ES;  // elements per chunk
     const int k = d.k;
@@ -768,6 +775,11 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
     constexpr int EPV = 16 / ES;
     constexpr int CE = kRowChunkBytes / ES;
     pdl_launch_dependents();
+    if (tid == kProducerWarp * 32) {  // the segment's head into L2 while the previous kernel finishes
+        const int cp = rank * seg;
+        const int np = max(0, min(seg, d.V - cp));
+        prefetch_l2_segment(static_cast<const char*>(target) + (static_cast<size_t>(row) * d.V + cp) * ES, np * ES);
+    }
     pdl_wait_prior();
     const int n = n_tree[b];
     if (n < 1 || n > d.T) {
@@ -1124,7 +1136,7 @@ static int sm_count() {
 RowPlan plan_rows(int V, int esize, long rows, bool resident, int max_stages, int max_seg_chunks) {
     int cpr = kMaxChunks;
     if (!resident) {
-        // about two waves of CTAs (three resident per SM with a 4-stage ring)
+        // about two waves of CTAs (three or four resident per SM)
         const long target = 2L * 3 * sm_count();
         cpr = 1;
         while (cpr < kMaxChunks &&
