@@ -305,6 +305,11 @@ int eagle_verify_export(const eagle_tree_cfg* cfg, const void* ws, size_t ws_byt
 /* Kernels launched by this library since it was loaded (host-side count). */
 uint64_t eagle_kernel_launches(void);
 
+/* The cudaError_t of the calling thread's most recent call that returned
+ * EAGLE_ERR_LAUNCH (0 if none), and its CUDA message in *message when
+ * message is not NULL (a static string). */
+int eagle_last_cuda_error(const char** message);
+
 /* Human-readable message for an eagle_status value. */
 const char* eagle_status_string(int status);
 

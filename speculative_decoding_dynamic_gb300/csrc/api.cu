@@ -90,7 +90,14 @@ int resolve_kv(const eagle_kv_cfg* kv, KvDims* k) {
     return EAGLE_OK;
 }
 
-int launch_result(cudaError_t e) { return e == cudaSuccess ? EAGLE_OK : EAGLE_ERR_LAUNCH; }
+// The CUDA error of the calling thread's last failed call (0 = none).
+thread_local int g_last_cuda_error = 0;
+
+int launch_result(cudaError_t e) {
+    if (e == cudaSuccess) return EAGLE_OK;
+    g_last_cuda_error = static_cast<int>(e);
+    return EAGLE_ERR_LAUNCH;
+}
 
 }  // namespace
 
@@ -276,6 +283,12 @@ int eagle_verify_export(const eagle_tree_cfg* cfg, const void* ws, size_t ws_byt
 }
 
 uint64_t eagle_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int eagle_last_cuda_error(const char** message) {
+    const int e = g_last_cuda_error;
+    if (message) *message = e ? cudaGetErrorString(static_cast<cudaError_t>(e)) : "no error";
+    return e;
+}
 
 const char* eagle_status_string(int status) {
     switch (status) {

@@ -57,12 +57,13 @@ constexpr int kHalf = kTile / 2;           // 16 KB: 128 rows x 64 columns (one 
 constexpr int kKStages = 3;  // K tiles in flight (a stage frees after QK^T)
 constexpr int kVStages = 2;  // V tiles in flight (a stage frees after PV)
 constexpr int kSoftmaxThreads = 512;
+constexpr int kGroupThreads = kSoftmaxThreads / 2;  // one softmax group: alternate key tiles
 constexpr int kThreads = 64 + kSoftmaxThreads;  // warp 0 TMA, warp 1 MMA, warps 2..17 softmax (four column quarters)
 constexpr int kSmemQ = 0;
 constexpr int kSmemK = kTile;                      // K stage s at kSmemK + s * kTile
 constexpr int kSmemV = kSmemK + kKStages * kTile;  // V stage s at kSmemV + s * kTile
 constexpr int kSmemBytes = kSmemV + kVStages * kTile;  // 192 KB
-constexpr int kTmemCols = 512;  // S double buffer (2 x 128 columns), O (128), P double buffer (2 x 64: bf16 pairs)
+constexpr int kTmemCols = 512;  // S double buffer (2 x 128 columns; P over S), O per softmax group (2 x 128)
 constexpr int kMaxW = kMaxSlots / 32;
 
 struct TcParams {
@@ -153,6 +154,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 consecutive fp32 columns (load + wait).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
@@ -195,9 +210,12 @@ __device__ __forceinline__ float max32(const float (&v)[32]) {
 }
 
 __device__ __forceinline__ void named_sync_softmax() { asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory"); }
-// The four softmax warps that serve one TMEM lane quarter (the rows 32 q4 ..
-// 32 q4 + 31, one warp per column quarter) meet on barrier 2 + q4.
-__device__ __forceinline__ void named_sync_rows(int q4) { asm volatile("bar.sync %0, 128;" ::"r"(2 + q4) : "memory"); }
+// The two warps of softmax group g that serve one TMEM lane quarter (the
+// rows 32 q4 .. 32 q4 + 31, one warp per column half) meet on barrier
+// 2 + 4 g + q4.
+__device__ __forceinline__ void named_sync_pair(int g, int q4) {
+    asm volatile("bar.sync %0, 64;" ::"r"(2 + 4 * g + q4) : "memory");
+}
 
 // ------------------------------------------------------------- kernel ---
 
@@ -208,12 +226,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char* smem =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ uint64_t bar_q, bar_k_full[kKStages], bar_k_empty[kKStages], bar_v_full[kVStages], bar_v_empty[kVStages],
-        bar_s_full[2], bar_s_free[2], bar_p_full, bar_o_full, bar_comb;
+        bar_s_full[2], bar_p_full[2], bar_o_full[2], bar_comb;
     __shared__ uint32_t tmem_holder;
     __shared__ uint32_t mask_sm[kBM][kMaxW];
     __shared__ int sh_last;
-    __shared__ float xch[2][4][kBM];  // per-tile row maxima exchanged between the four column quarters
-    __shared__ float xsum[4][kBM];    // final row sums of the four quarters
+    __shared__ float xch[2][2][2][kBM];  // [group][tile parity][column half][row]: per-tile row maxima
+    __shared__ float gm[2][kBM];         // [group][row]: reference maximum (-inf: the group saw no key)
+    __shared__ float gl[2][2][kBM];      // [group][column half][row]: row sums
 
     const int rb = blockIdx.x, split = blockIdx.y;
     const int b = blockIdx.z / p.Hkv, hk = blockIdx.z % p.Hkv;
@@ -259,10 +278,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bar_s_full[s], 1);
-            mbar_init(&bar_s_free[s], kSoftmaxThreads);
+            mbar_init(&bar_p_full[s], kGroupThreads);
+            mbar_init(&bar_o_full[s], 1);
         }
-        mbar_init(&bar_p_full, kSoftmaxThreads);
-        mbar_init(&bar_o_full, 1);
         mbar_init(&bar_comb, 1);
         fence_mbar_init();
 
@@ -284,8 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_holder;
-    const uint32_t tmem_s = tmem, tmem_o = tmem + 256;  // S buffer b at tmem_s + 128 b
-    const uint32_t tmem_p = tmem + 384;                 // P(j) at tmem_p + 64 (j & 1): row = lane, bf16 pairs
+    const uint32_t tmem_s = tmem;        // S(j) at tmem_s + 128 (j & 1); P(j) over its first 64 columns
+    const uint32_t tmem_o = tmem + 256;  // O of group g at tmem_o + 128 g
 
     unsigned char* sQ = smem + kSmemQ;
 
@@ -321,33 +339,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ---------------------------------------------------- MMA issuer ---
-        // S is double buffered in TMEM: QK(j) goes into buffer j & 1 as soon
-        // as K(j) has landed and the softmax has read S(j-2) out of it, so it
-        // runs while the softmax works on tile j-1. PV(j-1) follows once the
-        // softmax has written P(j-1).
+        // Tile j belongs to softmax group j & 1. QK(j) goes into S buffer
+        // j & 1, whose previous content P(j-2) was read by PV(j-2), issued
+        // earlier (tcgen05.mma of one thread execute in issue order). PV(j)
+        // reads P(j) from that buffer and accumulates into O of group j & 1.
+        // Issue order QK(0) QK(1) PV(0) QK(2) PV(1) QK(3) ...: while one
+        // group computes its softmax, the tensor pipe serves the other.
         if (lane == 0 && n_local > 0) {
             constexpr uint32_t id_qk = idesc_bf16(kBM, kBN, 0);
             constexpr uint32_t id_pv = idesc_bf16(kBM, kHD, 1);
             const uint32_t aQ = smem_u32(sQ);
             bool ok = mbar_wait_sleep(&bar_q, 0);
             auto issue_pv = [&](int jp) -> bool {
-                const int sp = jp % kVStages;
-                if (!mbar_wait_sleep(&bar_p_full, jp & 1) || !mbar_wait_sleep(&bar_v_full[sp], (jp / kVStages) & 1))
+                const int g = jp & 1, sp = jp % kVStages;
+                if (!mbar_wait_sleep(&bar_p_full[g], (jp >> 1) & 1) ||
+                    !mbar_wait_sleep(&bar_v_full[sp], (jp / kVStages) & 1))
                     return false;
                 tc_fence_after();
                 const uint32_t aV = smem_u32(smem + kSmemV + sp * kTile);
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)  // A = P from TMEM: 16 keys = 8 columns per MMA
-                    mma_bf16_ts(tmem_o, tmem_p + (jp & 1) * 64 + kk * 8, smem_desc(aV + kk * 2048, kHalf, 1024), id_pv,
-                                (jp > 0 || kk > 0) ? 1 : 0);
+                    mma_bf16_ts(tmem_o + g * kHD, tmem_s + g * kBN + kk * 8, smem_desc(aV + kk * 2048, kHalf, 1024),
+                                id_pv, (jp >= 2 || kk > 0) ? 1 : 0);
                 mma_commit(&bar_v_empty[sp]);
-                mma_commit(&bar_o_full);
+                mma_commit(&bar_o_full[g]);
                 return true;
             };
             for (int jj = 0; ok && jj < n_local; ++jj) {
                 const int sb = jj & 1, sk = jj % kKStages;
                 ok = mbar_wait_sleep(&bar_k_full[sk], (jj / kKStages) & 1);
-                if (ok && jj >= 2) ok = mbar_wait_sleep(&bar_s_free[sb], ((jj >> 1) - 1) & 1);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t aK = smem_u32(smem + kSmemK + sk * kTile);
@@ -366,15 +386,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------ softmax ---
-        // Four threads per query row (TMEM lane): warp w (2..17) serves the
-        // rows of TMEM lane quarter w % 4 and key/output columns
-        // 32 * ((w - 2) / 4) onwards. Row maxima and sums are exchanged
-        // through shared memory. O accumulates in TMEM; the exponentials use
-        // a reference maximum m_use that is raised (O, l rescaled) only when a
-        // tile's maximum exceeds it by more than 2^8. Tiles wholly inside the
-        // prefix skip the mask.
-        const int cq = (warp - 2) >> 2;                  // column quarter
-        const int cb = cq * 32;                          // first column of this quarter
+        // Two groups of eight warps take alternate key tiles (group g: tiles
+        // g, g + 2, ...), each with its own reference maximum, row sum and O
+        // accumulator; they are combined at the end. In a group, two threads
+        // serve a query row (TMEM lane): warp w serves lane quarter w % 4 and
+        // key / output columns 64 h onwards, h the warp's column half. The
+        // two halves exchange row maxima through shared memory. The
+        // exponentials use a reference maximum m_use raised (O_g, l rescaled)
+        // only when a tile's maximum exceeds it by more than 2^8.
+        const int gidx = (warp - 2) >> 3;                // softmax group
+        const int ch = ((warp - 2) >> 2) & 1;            // column half
+        const int cb = ch * 64;                          // first key / output column of the half
         const int q4 = warp & 3;
         const int r = (q4 << 5) | lane;                  // row of the block = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
@@ -385,52 +407,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         // a lane quarter whose 32 rows are all past the problem's rows does no
         // arithmetic (it still takes part in every barrier and V clearing)
         const bool quarter_live = rb * kBM + q4 * 32 < p.G * p.T;
-        float m_use = 0.0f, lh = 0.0f;                   // lh: this quarter's share of the row sum
+        const uint32_t s_cols = tmem_s + gidx * kBN;
+        const uint32_t o_cols = tmem_o + gidx * kHD;
+        float m_use = 0.0f, lh = 0.0f;                   // lh: this half's share of the group's row sum
         bool seen = false;
         bool ok = true;
-        for (int jj = 0; jj < n_local; ++jj) {
-            const int st = jj & 1;
+        for (int jj = gidx; jj < n_local; jj += 2) {
+            const int u = jj >> 1;  // the group's own tile count
             const int key0 = (t_begin + jj) * kBN;
             // After a timed-out wait a warp skips the work of the remaining tiles
             // but still takes every named barrier, so the others never wait for
             // it without bound.
-            if (ok && !__all_sync(0xffffffffu, mbar_wait_sleep(&bar_s_full[st], (jj >> 1) & 1))) ok = false;
+            if (ok && !__all_sync(0xffffffffu, mbar_wait_sleep(&bar_s_full[gidx], u & 1))) ok = false;
             tc_fence_after();
-            float sv[32];
-            if (ok && quarter_live) tmem_ld32(tmem_s + st * kBN + lane_off + cb, sv);
-            else
+            float sv[2][32];
+            if (ok && quarter_live) {
+                tmem_ld32(s_cols + lane_off + cb, sv[0]);
+                tmem_ld32(s_cols + lane_off + cb + 32, sv[1]);
+            } else {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) sv[e] = -INFINITY;
-            tc_fence_before();
-            mbar_arrive(&bar_s_free[st]);  // S buffer st may take tile j+2
-            // visibility of this quarter's 32 keys: prefix keys, then tree slots in mask row i
-            const int kb = key0 + cb;
-            uint32_t vis = 0xffffffffu;
-            const int npre = L - kb;  // keys of the quarter inside the prefix
-            if (npre < 32) {
-                uint32_t pre = npre > 0 ? (1u << npre) - 1u : 0u;
-                const int j0 = kb - L;  // slot of the quarter's first key (may be negative)
-                const int lo = j0 < 0 ? 0 : j0;
-                const int w0 = lo >> 5, sh = lo & 31;
-                uint32_t win = mask_sm[r][w0 & (kMaxW - 1)] >> sh;
-                if (sh && w0 + 1 < kMaxW) win |= mask_sm[r][w0 + 1] << (32 - sh);
-                if (w0 >= kMaxW) win = 0u;
-                const int limit = n - lo;  // slots j >= n are never visible
-                if (limit <= 0) win = 0u;
-                else if (limit < 32) win &= (1u << limit) - 1u;
-                uint32_t tree = j0 < 0 ? (win << (-j0)) : win;
-                if (j0 <= -32) tree = 0u;
-                vis = pre | tree;
+                for (int e = 0; e < 32; ++e) sv[0][e] = sv[1][e] = -INFINITY;
             }
-            if (vis != 0xffffffffu) {  // invisible keys: -inf, so their exponentials are 0
+            // visibility of the half's keys, 32 at a time: prefix keys, then tree slots in mask row i
 #pragma unroll
-                for (int e = 0; e < 32; ++e) sv[e] = ((vis >> e) & 1u) ? sv[e] : -INFINITY;
+            for (int hq = 0; hq < 2; ++hq) {
+                const int kb = key0 + cb + 32 * hq;
+                const int npre = L - kb;  // keys of the 32 inside the prefix
+                if (npre < 32) {
+                    const uint32_t pre = npre > 0 ? (1u << npre) - 1u : 0u;
+                    const int j0 = kb - L;  // slot of the first key (may be negative)
+                    const int lo = j0 < 0 ? 0 : j0;
+                    const int w0 = lo >> 5, sh = lo & 31;
+                    uint32_t win = mask_sm[r][w0 & (kMaxW - 1)] >> sh;
+                    if (sh && w0 + 1 < kMaxW) win |= mask_sm[r][w0 + 1] << (32 - sh);
+                    if (w0 >= kMaxW) win = 0u;
+                    const int limit = n - lo;  // slots j >= n are never visible
+                    if (limit <= 0) win = 0u;
+                    else if (limit < 32) win &= (1u << limit) - 1u;
+                    uint32_t tree = j0 < 0 ? (win << (-j0)) : win;
+                    if (j0 <= -32) tree = 0u;
+                    const uint32_t vis = pre | tree;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) sv[hq][e] = ((vis >> e) & 1u) ? sv[hq][e] : -INFINITY;
+                }
             }
-            float mx = max32(sv) * sc;  // the scale is positive
+            float mx = fmaxf(max32(sv[0]), max32(sv[1])) * sc;  // the scale is positive
             if (quarter_live) {
-                xch[jj & 1][cq][r] = mx;
-                named_sync_rows(q4);
-                mx = fmaxf(fmaxf(xch[jj & 1][0][r], xch[jj & 1][1][r]), fmaxf(xch[jj & 1][2][r], xch[jj & 1][3][r]));
+                xch[gidx][u & 1][ch][r] = mx;
+                tc_fence_before();
+                named_sync_pair(gidx, q4);  // also: both halves have read S, so P may overwrite it
+                tc_fence_after();
+                mx = fmaxf(xch[gidx][u & 1][0][r], xch[gidx][u & 1][1][r]);
             }
             bool rescale = false;
             float alpha = 1.0f;
@@ -445,45 +472,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                     lh *= alpha;
                 }
             }
-            uint32_t pk[16];
+            if (!ok) continue;
             if (quarter_live) {
-                // p = 2^(s sc - m_use), two per packed multiply-add; four packed partial sums
+                // p = 2^(s sc - m_use), two per packed multiply-add; packed partial sums.
+                // P(j) as bf16 pairs over S columns 32 h .. 32 h + 31 of this buffer.
                 const uint64_t sc2 = f2_pack(sc, sc), nm2 = f2_pack(-m_use, -m_use);
-                uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+                uint64_t acc[2] = {0ull, 0ull};
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const uint64_t z = f2_fma(f2_pack(sv[e], sv[e + 1]), sc2, nm2);
-                    const float p0 = ex2_approx(f2_lo(z));
-                    const float p1 = ex2_approx(f2_hi(z));
-                    acc[(e >> 1) & 3] = f2_add(acc[(e >> 1) & 3], f2_pack(p0, p1));
-                    pk[e >> 1] = pack_bf16(p0, p1);
+                for (int hq = 0; hq < 2; ++hq) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const uint64_t z = f2_fma(f2_pack(sv[hq][e], sv[hq][e + 1]), sc2, nm2);
+                        const float p0 = ex2_approx(f2_lo(z));
+                        const float p1 = ex2_approx(f2_hi(z));
+                        acc[(e >> 1) & 1] = f2_add(acc[(e >> 1) & 1], f2_pack(p0, p1));
+                        pk[e >> 1] = pack_bf16(p0, p1);
+                    }
+                    tmem_st16(s_cols + lane_off + (cb >> 1) + 16 * hq, pk);
                 }
-                const uint64_t s2 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+                const uint64_t s2 = f2_add(acc[0], acc[1]);
                 lh += f2_lo(s2) + f2_hi(s2);
             }
-            if (!ok) continue;
-            // P is double buffered: P(j) goes to buffer j & 1, whose last reader
-            // PV(j-2) is complete (it precedes QK(j) on the tensor pipe). O is
-            // waited for only when it must be rescaled: PV(j-1) done, O stable.
-            // tcgen05.ld/st are warp-collective: rescale if any row of the warp
-            // needs it (alpha = 1 for the others).
-            if (jj > 0 && quarter_live && __any_sync(0xffffffffu, rescale)) {
-                if (!__all_sync(0xffffffffu, mbar_wait_sleep(&bar_o_full, (jj - 1) & 1))) {
-                    ok = false;
-                    continue;
-                }
-                tc_fence_after();
-                float o[32];
-                tmem_ld32(tmem_o + lane_off + cb, o);
+            // O_g is stable: its last update PV(j-2) preceded QK(j) on the tensor
+            // pipe, and PV(j) waits for this thread's arrival below. tcgen05.ld/st
+            // are warp-collective: rescale if any row of the warp needs it
+            // (alpha = 1 for the others).
+            if (quarter_live && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                tmem_st32(tmem_o + lane_off + cb, o);
+                for (int hq = 0; hq < 2; ++hq) {
+                    float o[32];
+                    tmem_ld32(o_cols + lane_off + cb + 32 * hq, o);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                    tmem_st32(o_cols + lane_off + cb + 32 * hq, o);
+                }
             }
-            // P into TMEM: row r = lane, this quarter's 32 keys = columns 16 cq .. 16 cq + 15
-            if (quarter_live) tmem_st16(tmem_p + (jj & 1) * 64 + lane_off + cq * 16, pk);
             // V rows of keys that no row can see may hold anything (even NaN):
-            // zero them so that 0 * V stays 0 in the MMA (each V row is 2 x 128
-            // bytes; this thread clears 64 of them).
+            // zero them so that 0 * V stays 0 in the MMA (a V row is two 128-byte
+            // halves; thread (row r, column half h) clears half h of row r).
             if (key0 + kBN > nkeys) {
                 const int sv_st = jj % kVStages;
                 if (!__all_sync(0xffffffffu, mbar_wait(&bar_v_full[sv_st], (jj / kVStages) & 1))) {
@@ -491,44 +518,66 @@ __global__ void __launch_bounds__(kThreads, 1)
                     continue;
                 }
                 if (key0 + r >= nkeys) {
-                    unsigned char* sV = smem + kSmemV + sv_st * kTile + (cq >> 1) * kHalf;
-                    uint4* z = reinterpret_cast<uint4*>(sV + r * 128 + (cq & 1) * 64);
+                    uint4* z = reinterpret_cast<uint4*>(smem + kSmemV + sv_st * kTile + ch * kHalf + r * 128);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) z[q] = make_uint4(0, 0, 0, 0);
+                    for (int q = 0; q < 8; ++q) z[q] = make_uint4(0, 0, 0, 0);
                     fence_proxy_async_smem();  // the MMA reads V through the async proxy
                 }
             }
             tc_fence_before();
-            mbar_arrive(&bar_p_full);
+            mbar_arrive(&bar_p_full[gidx]);
         }
-        if (ok && n_local > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&bar_o_full, (n_local - 1) & 1));
-            tc_fence_after();
-        }
+        // both groups' last PV done: O_0 and O_1 final
+        const int last0 = (n_local + 1) / 2 - 1, last1 = n_local / 2 - 1;  // group tile counts - 1
+        if (ok && last0 >= 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar_o_full[0], last0 & 1));
+        if (ok && last1 >= 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar_o_full[1], last1 & 1));
+        tc_fence_after();
         if (!ok) raise_status(p.status, kDevTimeout);
-        // row sum of the four quarters
-        xsum[cq][r] = lh;
+        // per-row statistics of both groups
+        if (ch == 0) gm[gidx][r] = (seen && quarter_live) ? m_use : -INFINITY;
+        gl[gidx][ch][r] = lh;
         named_sync_softmax();
-        const float l = xsum[0][r] + xsum[1][r] + xsum[2][r] + xsum[3][r];
         // ------------------------------------------------------- epilogue ---
+        // Every softmax warp now serves output columns 32 cq .. 32 cq + 31 of
+        // its lane quarter: O = (2^(m0 - M) O_0 + 2^(m1 - M) O_1) with M the
+        // larger reference maximum, l likewise.
+        const int cq = (warp - 2) >> 2;  // output column quarter
+        const int oc = cq * 32;
+        const float m0 = gm[0][r], m1 = gm[1][r];
+        const float M = fmaxf(m0, m1);
+        const float a0 = m0 > -INFINITY ? ex2_approx(m0 - M) : 0.0f;
+        const float a1 = m1 > -INFINITY ? ex2_approx(m1 - M) : 0.0f;
+        const float l = a0 * (gl[0][0][r] + gl[0][1][r]) + a1 * (gl[1][0][r] + gl[1][1][r]);
+        float o[32];
+        // a group that saw no key has weight 0 and its O may be unset: select, not multiply
+        if (last0 >= 0) tmem_ld32(tmem_o + lane_off + oc, o);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = (last0 >= 0 && a0 > 0.0f) ? a0 * o[e] : 0.0f;
+        if (last1 >= 0 && __any_sync(0xffffffffu, a1 > 0.0f)) {
+#pragma unroll
+            for (int hq = 0; hq < 2; ++hq) {
+                float o1[16];
+                tmem_ld16(tmem_o + kHD + lane_off + oc + 16 * hq, o1);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) o[16 * hq + e] += a1 > 0.0f ? a1 * o1[e] : 0.0f;
+            }
+        }
         const bool row_live = grow < p.G * p.T;
         __nv_bfloat16* orow =
             p.out + ((static_cast<size_t>(b) * p.T + i) * p.Hq + static_cast<size_t>(hk) * p.G + g) * kHD;
         if (nsplit_b == 1) {
             const bool live = row_live && i < n && l > 0.0f && ok;  // rows of unused slots are zeros
             const float inv = live ? 1.0f / l : 0.0f;
-            float o[32];
-            if (n_local > 0) tmem_ld32(tmem_o + lane_off + cb, o);
             if (row_live) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    uint4 u = make_uint4(0u, 0u, 0u, 0u);
+                    uint4 uo = make_uint4(0u, 0u, 0u, 0u);
                     if (live)
-                        u = make_uint4(pack_bf16(o[8 * q] * inv, o[8 * q + 1] * inv),
-                                       pack_bf16(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
-                                       pack_bf16(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
-                                       pack_bf16(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
-                    *reinterpret_cast<uint4*>(orow + cb + 8 * q) = u;
+                        uo = make_uint4(pack_bf16(o[8 * q] * inv, o[8 * q + 1] * inv),
+                                        pack_bf16(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
+                                        pack_bf16(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
+                                        pack_bf16(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
+                    *reinterpret_cast<uint4*>(orow + oc + 8 * q) = uo;
                 }
             }
         } else {
@@ -536,15 +585,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // chunk stored at position q ^ (row & 7)), reference max and sum.
             const size_t s0 = static_cast<size_t>(unit) * p.nsplit;
             float* po = p.part_o + ((s0 + split) * kBM + r) * kHD;
-            {
-                float o[32];
-                tmem_ld32(tmem_o + lane_off + cb, o);
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    *reinterpret_cast<float4*>(po + cb + ((q ^ (r & 7)) << 2)) =
-                        make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-            }
-            const float m_own = (seen && l > 0.0f) ? m_use : -INFINITY;
+            for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<float4*>(po + oc + ((q ^ (r & 7)) << 2)) =
+                    make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+            const float m_own = (M > -INFINITY && l > 0.0f) ? M : -INFINITY;
             if (cq == 0) {
                 p.part_ml[((s0 + split) * kBM + r) * 2] = m_own;
                 p.part_ml[((s0 + split) * kBM + r) * 2 + 1] = l;
@@ -557,27 +602,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             named_sync_softmax();
             if (sh_last) {
-                // Merge: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s, accumulated
-                // in this CTA's TMEM; the other splits' partials are bulk-copied
-                // into the idle K/V buffers, two per round.
+                // Merge: O = sum_s 2^(m_s - Mx) O_s / sum_s 2^(m_s - Mx) l_s, accumulated
+                // in registers; the other splits' partials are bulk-copied into the
+                // idle K/V buffers, two per round.
                 __threadfence();
-                float M = -INFINITY;
-                for (int s = 0; s < nsplit_b; ++s) M = fmaxf(M, __ldcg(&p.part_ml[((s0 + s) * kBM + r) * 2]));
+                float Mx = -INFINITY;
+                for (int s = 0; s < nsplit_b; ++s) Mx = fmaxf(Mx, __ldcg(&p.part_ml[((s0 + s) * kBM + r) * 2]));
                 float Ls = 0.0f;
                 for (int s = 0; s < nsplit_b; ++s) {
                     const float ms = __ldcg(&p.part_ml[((s0 + s) * kBM + r) * 2]);
-                    if (ms > -INFINITY) Ls += __ldcg(&p.part_ml[((s0 + s) * kBM + r) * 2 + 1]) * ex2_approx(ms - M);
+                    if (ms > -INFINITY) Ls += __ldcg(&p.part_ml[((s0 + s) * kBM + r) * 2 + 1]) * ex2_approx(ms - Mx);
                 }
                 const bool live = row_live && i < n && Ls > 0.0f;
                 const float inv = live ? 1.0f / Ls : 0.0f;
-                const float w_own = m_own > -INFINITY ? ex2_approx(m_own - M) * inv : 0.0f;
-                {
-                    float o[32];
-                    tmem_ld32(tmem_o + lane_off + cb, o);
+                const float w_own = m_own > -INFINITY ? ex2_approx(m_own - Mx) * inv : 0.0f;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] *= w_own;
-                    tmem_st32(tmem_o + lane_off + cb, o);
-                }
+                for (int e = 0; e < 32; ++e) o[e] = w_own > 0.0f ? o[e] * w_own : 0.0f;
                 constexpr int kPart = kBM * kHD * 4;  // 64 KB: one split's partial block
                 unsigned char* area = smem + kSmemK;  // 160 KB of K/V stages, idle now
                 int round = 0;
@@ -600,10 +640,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!landed) raise_status(p.status, kDevTimeout);
                     for (int q = 0; landed && q < cnt; ++q) {
                         const float ms = __ldcg(&p.part_ml[((s0 + lst[q]) * kBM + r) * 2]);
-                        const float wq = ms > -INFINITY ? ex2_approx(ms - M) * inv : 0.0f;
-                        const float* rowp = reinterpret_cast<const float*>(area + q * kPart) + r * kHD + cb;
-                        float o[32];
-                        tmem_ld32(tmem_o + lane_off + cb, o);
+                        const float wq = ms > -INFINITY ? ex2_approx(ms - Mx) * inv : 0.0f;
+                        if (wq == 0.0f) continue;
+                        const float* rowp = reinterpret_cast<const float*>(area + q * kPart) + r * kHD + oc;
 #pragma unroll
                         for (int q4b = 0; q4b < 8; ++q4b) {
                             const float4 v = *reinterpret_cast<const float4*>(rowp + ((q4b ^ (r & 7)) << 2));
@@ -612,21 +651,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                             o[4 * q4b + 2] += wq * v.z;
                             o[4 * q4b + 3] += wq * v.w;
                         }
-                        tmem_st32(tmem_o + lane_off + cb, o);
                     }
                     named_sync_softmax();  // every row has read the slots before they are refilled
                     ++round;
                 }
-                float o[32];
-                tmem_ld32(tmem_o + lane_off + cb, o);
                 if (row_live) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        uint4 u = make_uint4(0u, 0u, 0u, 0u);
+                        uint4 uo = make_uint4(0u, 0u, 0u, 0u);
                         if (live)
-                            u = make_uint4(pack_bf16(o[8 * q], o[8 * q + 1]), pack_bf16(o[8 * q + 2], o[8 * q + 3]),
-                                           pack_bf16(o[8 * q + 4], o[8 * q + 5]), pack_bf16(o[8 * q + 6], o[8 * q + 7]));
-                        *reinterpret_cast<uint4*>(orow + cb + 8 * q) = u;
+                            uo = make_uint4(pack_bf16(o[8 * q], o[8 * q + 1]), pack_bf16(o[8 * q + 2], o[8 * q + 3]),
+                                            pack_bf16(o[8 * q + 4], o[8 * q + 5]),
+                                            pack_bf16(o[8 * q + 6], o[8 * q + 7]));
+                        *reinterpret_cast<uint4*>(orow + oc + 8 * q) = uo;
                     }
                 }
                 if (r == 0 && cq == 0) p.tickets[unit] = 0;

@@ -28,6 +28,10 @@ MAX_TOPK, MAX_DEPTH, MAX_SLOTS, MAX_CANDIDATES = 16, 16, 256, 1024
 class EagleError(RuntimeError):
     def __init__(self, fn: str, code: int):
         msg = _lib.eagle_status_string(code).decode()
+        if code == -3:  # EAGLE_ERR_LAUNCH: add the CUDA error
+            cmsg = ctypes.c_char_p()
+            cerr = _lib.eagle_last_cuda_error(ctypes.byref(cmsg))
+            msg += f"; CUDA error {cerr}: {cmsg.value.decode() if cmsg.value else ''}"
         super().__init__(f"{fn} -> {code} ({msg})")
         self.code = code
 
@@ -82,6 +86,8 @@ _lib.eagle_status_fetch.argtypes = [_p, ctypes.POINTER(ctypes.c_int), _p]
 _lib.eagle_tree_export.argtypes = [_TP, _p, _sz, _p, _p, _p, _p, _p, _p, _p, _p]
 _lib.eagle_verify_export.argtypes = [_TP, _p, _sz, _p, _p, _p, _p]
 _lib.eagle_kernel_launches.restype = ctypes.c_uint64
+_lib.eagle_last_cuda_error.argtypes = [ctypes.POINTER(ctypes.c_char_p)]
+_lib.eagle_last_cuda_error.restype = _i
 _lib.eagle_status_string.argtypes = [_i]
 _lib.eagle_status_string.restype = ctypes.c_char_p
 
