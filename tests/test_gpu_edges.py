@@ -36,11 +36,11 @@ def _tables(E, cfg, ws):
     return {k: H.to_host(v) for k, v in t.items()}
 
 
-def _run_tree(logits, B, V, k, D, N, thr, dtype, L=None, root=None):
+def _run_tree(logits, B, V, k, D, N, thr, dtype, L=None, root=None, policy=0):
     """Stages 1-4 on both sides with identical log-prob inputs (the oracle's lse)."""
     import torch
     E = _E()
-    cfg_o = oracle.TreeCfg(B, V, k, D, N, thr)
+    cfg_o = oracle.TreeCfg(B, V, k, D, N, thr, policy)
     t = oracle.Tree(cfg_o)
     fronts = []
     for s in range(D):
@@ -54,7 +54,7 @@ def _run_tree(logits, B, V, k, D, N, thr, dtype, L=None, root=None):
         for b in range(B):
             for f in range(k):
                 _, lse[s, b, f], _ = oracle.row_stats(np.ascontiguousarray(logits[s, b, f]), 1)
-    cfg = E.TreeCfg(B, V, k, D, N, thr, dtype)
+    cfg = E.TreeCfg(B, V, k, D, N, thr, dtype, policy)
     ws = E.alloc_workspace(E.eagle_workspace_bytes(cfg))
     i32 = dict(dtype=torch.int32, device="cuda")
     row_lse = torch.empty(B, D, k, dtype=torch.float32, device="cuda")
@@ -103,6 +103,28 @@ def test_tree_edges(B, V, k, D, N, thr, dtype):
     t, tr = _run_tree(logits, B, V, k, D, N, thr, dtype)
     if thr > 0.9:
         assert (t.fcount == 0).all() or (tr["n_tree"] <= 1 + k).all()
+
+
+@pytest.mark.parametrize("policy", [1, 2, 3])
+@pytest.mark.parametrize("B,V,k,D,N,thr,dtype", [
+    (2, 1000, 2, 3, 8, 0.95, synth.F32),        # threshold empties the frontier after step 0
+    (1, 128256, 1, 5, 5, 0.0, synth.BF16),      # k = 1: a chain
+    (2, 2048, 16, 4, 255, 0.0, synth.F32),      # k = 16, T = 256
+    (2, 32000, 10, 6, 60, 0.3, synth.BF16),     # threshold prunes part of every layer
+    (3, 4104, 3, 4, 5, 0.0, synth.BF16),        # budget below the expanded nodes
+])
+def test_policy_edges(B, V, k, D, N, thr, dtype, policy):
+    """The ablation policies (confidence frontier, no rerank, static shape)
+    on the same degenerate inputs: bit-exact tables, kept sets and trees."""
+    logits = synth.normal4((D, B, k, V), dtype, 2.5, seed=V + k + policy, stream=synth.STREAM_DRAFT)
+    synth.plant(logits, dtype, float(np.log(9.0 * V)) + 3.0, seed=V + k, stream=synth.STREAM_DRAFT, frac=0.7)
+    t, tr = _run_tree(logits, B, V, k, D, N, thr, dtype, policy=policy)
+    kept = t.kept.astype(bool)
+    assert (t.n_kept <= N).all() and (kept.sum(1) == t.n_kept).all()
+    if policy in (2, 3):  # only expanded nodes (frontiers) can be kept
+        for b in range(B):
+            fr = set(int(x) for x in t.fhist[1:, b].ravel() if x >= 0)
+            assert set(np.flatnonzero(kept[b])) <= fr
 
 
 def test_equal_logit_rows_use_exact_fallback():
