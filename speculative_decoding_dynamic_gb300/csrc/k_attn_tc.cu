@@ -691,16 +691,18 @@ Plan make_plan(const KvDims& kv, int T) {
     pl.n_rb = (rows + kBM - 1) / kBM;
     pl.units = kv.B * kv.Hkv * pl.n_rb;
     const int max_tiles = (kv.max_len + kBN - 1) / kBN;
-    // Keys of a unit may be split over CTAs (one CTA per SM). Cost model:
-    // waves of CTAs x tiles per CTA, plus a prologue/epilogue of about two
-    // tiles per CTA and a merge of about one tile per extra split.
+    // Keys of a unit may be split over CTAs (one CTA per SM). Cost model, in
+    // tile times: waves of CTAs x (tiles per CTA + a fixed eight for the
+    // prologue, epilogue and partial store of a CTA) + 1.5 per extra split
+    // (the merge). Fitted on GB300: 70B b8 best at 3-4 splits (6 before),
+    // 8B b1 at 3-4, 8B b64 at 1.
     const int sms = 152;
     int nsplit = 1;
     double best = 1e30;
     for (int ns = 1; ns <= std::max(1, max_tiles / 2); ++ns) {
         const int tps = (max_tiles + ns - 1) / ns;
         const double waves = std::ceil(static_cast<double>(pl.units) * ns / sms);
-        const double cost = waves * (tps + 2.0 + (ns > 1 ? 1.0 : 0.0));
+        const double cost = waves * (tps + 8.0) + 1.5 * (ns - 1);
         if (cost < best - 1e-9) {
             best = cost;
             nsplit = ns;
