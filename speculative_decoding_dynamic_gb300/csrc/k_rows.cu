@@ -57,7 +57,7 @@ constexpr int kVecPerWarp = 32 * kVecPerLane;
 static_assert(kVecPerWarp * kConsumerWarps * 16 == kRowChunkBytes, "chunk geometry");
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kMaxSegChunks = 8;  // chunks of one CTA's row segment in expansion
-constexpr int kExpandStages = 2;  // four CTAs per SM (registers and shared memory)
+constexpr int kExpandStages = 2;  // five CTAs per SM (40 registers, ~43 KB shared memory each)
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ------------------------------------------------------------ helpers ---
@@ -391,7 +391,7 @@ __device__ __forceinline__ void segment_topk(ExpandSmem& sm, const unsigned char
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kRowThreads, 4) expand_kernel(TreeDims d, TreeWs w, int step, int seg, int ns,
+__global__ void __launch_bounds__(kRowThreads, 5) expand_kernel(TreeDims d, TreeWs w, int step, int seg, int ns,
                                                                  int smem_bytes, const void* __restrict__ logits,
                                                                  const float* __restrict__ lse_in,
                                                                  float* __restrict__ row_lse,
@@ -1136,7 +1136,7 @@ static int sm_count() {
 RowPlan plan_rows(int V, int esize, long rows, bool resident, int max_stages, int max_seg_chunks) {
     int cpr = kMaxChunks;
     if (!resident) {
-        // about two waves of CTAs (three or four resident per SM)
+        // about two waves of CTAs (three to five resident per SM)
         const long target = 2L * 3 * sm_count();
         cpr = 1;
         while (cpr < kMaxChunks &&
