@@ -90,7 +90,36 @@ __global__ void __launch_bounds__(kSortThreads) rerank_kernel(TreeDims d, TreeWs
         keys[i] = key;
     }
     if (local) atomicAdd(&n_valid, local);
-    // Bitonic sort, descending.
+    if (P <= kSortThreads) {
+        // Bitonic sort, descending, one key per thread in a register: pairs
+        // closer than 32 meet by warp shuffles, farther ones through shared
+        // memory (two buffers alternate, one barrier per such stage).
+        __syncthreads();
+        uint64_t v = tid < P ? keys[tid] : 0ull;
+        int sm_stage = 0;
+        for (int size = 2; size <= kSortThreads; size <<= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                uint64_t o;
+                if (stride >= 32) {
+                    uint64_t* buf = keys + (sm_stage & 1) * kSortThreads;
+                    buf[tid] = v;
+                    __syncthreads();
+                    o = buf[tid ^ stride];
+                    ++sm_stage;
+                } else {
+                    o = shfl_xor_u64(v, stride);
+                }
+                const bool desc = (tid & size) == 0;
+                const bool lower = (tid & stride) == 0;
+                v = (lower == desc) ? (o > v ? o : v) : (o < v ? o : v);
+            }
+        }
+        const int keep = min(d.N, n_valid);
+        if (tid < keep) w.kept[static_cast<size_t>(b) * d.C + key_id(v)] = 1;
+        if (tid == 0) w.n_kept[b] = keep;
+        return;
+    }
+    // Bitonic sort, descending (more than 512 keys: in shared memory).
     for (int size = 2; size <= P; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
             __syncthreads();
@@ -130,6 +159,8 @@ __global__ void __launch_bounds__(kBuildThreads) build_tree_kernel(TreeDims d, T
                                                                     int32_t* __restrict__ n_tree) {
     __shared__ int slot_of[kMaxCandidates];
     __shared__ int par_node[kMaxCandidates];
+    __shared__ int tok_of[kMaxCandidates];  // token and depth of every candidate, loaded with the flags
+    __shared__ int dep_of[kMaxCandidates];
     __shared__ int warp_sum[kBuildThreads / 32];
     __shared__ int node_at[kMaxSlots];
     const int b = blockIdx.x;
@@ -143,7 +174,11 @@ __global__ void __launch_bounds__(kBuildThreads) build_tree_kernel(TreeDims d, T
     // Exclusive scan of the kept flags in node-id order gives each kept node its slot.
     const size_t base = static_cast<size_t>(b) * d.C;
     const int flag = (tid < d.C) ? (w.kept[base + tid] != 0) : 0;
-    if (tid < d.C) par_node[tid] = w.cand_parent[base + tid];
+    if (tid < d.C) {
+        par_node[tid] = w.cand_parent[base + tid];
+        tok_of[tid] = w.cand_token[base + tid];
+        dep_of[tid] = w.cand_depth[base + tid];
+    }
     const unsigned ballot = __ballot_sync(0xffffffffu, flag);
     const int before_in_warp = __popc(ballot & ((1u << lane) - 1u));
     if (lane == 0) warp_sum[warp] = __popc(ballot);
@@ -192,8 +227,8 @@ __global__ void __launch_bounds__(kBuildThreads) build_tree_kernel(TreeDims d, T
             const int pn = par_node[id];
             const int ps = pn < 0 ? 0 : slot_of[pn];
             if (ps < 0) raise_status(w.status, kDevOverflow);  // parent not kept: cannot happen
-            const int dep = w.cand_depth[base + id];
-            tokens[r] = w.cand_token[base + id];
+            const int dep = dep_of[id];
+            tokens[r] = tok_of[id];
             parent[r] = ps;
             depth[r] = dep;
             pos[r] = L + dep;
