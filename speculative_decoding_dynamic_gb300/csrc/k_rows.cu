@@ -353,10 +353,16 @@ __device__ __forceinline__ void segment_topk(ExpandSmem& sm, const unsigned char
     consumer_bar();
     const int nk = sm.nkeys;
     if (nk <= kcap) {
+        // rank = keys above; two keys per 16-byte load (the keys start 16-byte aligned)
+        const ulonglong2* kp = reinterpret_cast<const ulonglong2*>(keys);
         for (int i = tid; i < nk; i += kConsumers) {
             const uint64_t key = keys[i];
             int r = 0;
-            for (int j = 0; j < nk; ++j) r += keys[j] > key;
+            for (int j = 0; j < nk / 2; ++j) {
+                const ulonglong2 q = kp[j];
+                r += (q.x > key) + (q.y > key);
+            }
+            if (nk & 1) r += keys[nk - 1] > key;
             if (r < k) sm.ctop[r] = key;
         }
         return;
