@@ -211,6 +211,17 @@ __device__ __forceinline__ void prefetch_l2_segment(const char* src, int bytes) 
 __device__ __forceinline__ int ld_cg_i32(const int* p) { return __ldcg(p); }
 __device__ __forceinline__ float ld_cg_f32(const float* p) { return __ldcg(p); }
 
+// Per-sequence ticket: add one at device scope with acquire-release
+// semantics. The release covers the caller's writes and, being cumulative,
+// the writes it observed through earlier barriers (its CTA's, its cluster's);
+// the returned count acquires every earlier arrival's. Threads of the CTA
+// that read those writes after a barrier following the call observe them.
+__device__ __forceinline__ int ticket_add(int* p) {
+    int prev;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(prev) : "l"(p) : "memory");
+    return prev;
+}
+
 // ------------------------------------------------------------- host side ---
 // Dynamic shared memory opt-in and launch helpers live in the launcher files.
 

@@ -583,13 +583,11 @@ __global__ void __launch_bounds__(kRowThreads, 5) expand_kernel(TreeDims d, Tree
 
     // Per-sequence ticket: the last row of this sequence picks the next frontier.
     if (tid == 0) {
-        __threadfence();
-        const int prev = atomicAdd(&w.expand_ticket[b], 1);
+        const int prev = ticket_add(&w.expand_ticket[b]);
         sm.last = (prev == F - 1);
     }
     __syncthreads();
     if (!sm.last) return;
-    __threadfence();
     const int nsel = F * d.k;
     // the ring is idle now: candidate keys, their tokens, the chosen tokens
     uint64_t* sel = reinterpret_cast<uint64_t*>(dyn_smem);
@@ -901,13 +899,11 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
         w.row_arg[rt] = static_cast<int32_t>(key_id(gkey));
         w.row_mass[rt] = mass;
         if (!isfinite(M)) raise_status(w.status, kDevNonFinite);
-        __threadfence();
-        const int prev = atomicAdd(&w.verify_ticket[b], 1);
+        const int prev = ticket_add(&w.verify_ticket[b]);
         sm.last = (prev == n - 1);
     }
     __syncthreads();
     if (!sm.last) return;
-    __threadfence();
 
     // ---- acceptance walk for sequence b (one CTA) ----
     WalkSmem& ws = *reinterpret_cast<WalkSmem*>(dyn_smem);
