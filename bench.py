@@ -484,6 +484,14 @@ def main():
         vals.append(vsum.cpu().numpy())
     acc = acc_all.mean(axis=0)             # per sequence, averaged over the sets
     n_tree = dc.n_tree.cpu().numpy()
+    depth_h = dc.depth.cpu().numpy()
+    # attention FLOPs actually computed: QK^T and PV over every live slot's keys
+    # (the prefix plus its ancestors-or-self), 2 FLOP per multiply-add
+    attn_flop = 0
+    for b in range(w.batch):
+        nb = int(n_tree[b])
+        anc = int(sum(int(depth_h[b, i]) + 1 for i in range(nb)))
+        attn_flop += 4 * w.n_q_heads * w.head_dim * (nb * int(prefix_len[b]) + anc)
 
     # ---- per-kernel timing: each stage call alone, same launch configuration ----
     flush = None
@@ -554,6 +562,10 @@ def main():
             e["bytes"] = int(byt)
             e["GB_s"] = round(byt / (ms_k * 1e-3) / 1e9, 1)
             e["frac_hbm"] = round(byt / (ms_k * 1e-3) / 1e9 / hbm_peak, 4)
+        if name == "attention":
+            e["tflops"] = round(attn_flop / (ms_k * 1e-3) / 1e12, 1)
+            if peak:
+                e["frac_tensor"] = round(attn_flop / (ms_k * 1e-3) / 1e12 / peak["bf16_tflops"], 4)
         per_kernel[name] = e
     cyc_share = {"expand_step": kt["expand_step"] * (w.depth - 1), "attention": kt["attention"],
                  "verify": kt["verify"]}
@@ -565,6 +577,14 @@ def main():
                 "frac": round(achieved / hbm_peak, 4), "traffic": ncu_traffic(kname, w.name), "kernel": kname,
                 "peak_source": f"{peak_src} hbm_gbs (burst copy)",
                 "bytes_per_launch": int(dom_bytes)}
+    tensor_peak = peak["bf16_tflops"] if peak else 1900.0
+    if dom == "attention" and attn_flop / (tensor_peak * 1e12) > dom_bytes / (hbm_peak * 1e9):
+        # the attention shape is compute-bound: its roofline is the tensor pipe (bf16 dense)
+        ach_t = attn_flop / (kt[dom] * 1e-3) / 1e12
+        roofline.update({"bound": "tensor", "achieved": round(ach_t, 1), "peak": tensor_peak, "unit": "TFLOP/s",
+                         "frac": round(ach_t / tensor_peak, 4),
+                         "peak_source": f"{peak_src} bf16_tflops (burst cuBLAS GEMM)",
+                         "flop_per_launch": int(attn_flop)})
 
     # ---- end to end through host buffers ----
     e2e = None
