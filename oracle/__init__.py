@@ -50,6 +50,7 @@ def _load():
     lib.oracle_verify_greedy.argtypes = [i32, i32, i32, i32, i32, p, p, p, p, p, p, p, p]
     lib.oracle_verify_lossless.argtypes = [i32, i32, i32, i32, i32, f32, p, p, p, p, p, p, p, p, p, p]
     lib.oracle_kv_compact.argtypes = [i32, i32, i32, i32, i32, p, i64, i64, i64, i64, p, p, p, i32, p]
+    lib.oracle_lmhead_logits.argtypes = [i32, i32, i32, p, p, p]
     _lib = lib
     return lib
 
@@ -269,3 +270,18 @@ def kv_compact(cache: np.ndarray, B: int, layers: int, Hkv: int, d: int, seq_str
                               _p(np.ascontiguousarray(accept_len, np.int32)),
                               _p(np.ascontiguousarray(accepted_slots, np.int32)), Dp1, _p(new_len))
     return new_len
+
+
+def lmhead_logits(hidden: np.ndarray, W: np.ndarray) -> np.ndarray:
+    """LM-head logits of frontier rows: hidden [M, H] and W [V, H] as bf16 bits (uint16);
+    returns fp32 [M, V] (exact dot products rounded once to fp32)."""
+    hidden = np.ascontiguousarray(hidden, np.uint16)
+    W = np.ascontiguousarray(W, np.uint16)
+    M, H = hidden.shape
+    V, H2 = W.shape
+    assert H == H2
+    out = np.empty((M, V), np.float32)
+    rc = _load().oracle_lmhead_logits(M, V, H, _p(hidden), _p(W), _p(out))
+    if rc != 0:
+        raise RuntimeError(f"oracle_lmhead_logits failed: {rc}")
+    return out

@@ -634,4 +634,28 @@ int oracle_kv_compact(int B, int layers, int Hkv, int d, int elem_size, void* ca
     return 0;
 }
 
+
+// ------------------------------------------------ LM head (next row f1) ---
+
+// Logits of M frontier rows through the LM head, the step before stage 1
+// ["EAGLE" notes, EAGLE 方法: the draft model reuses the target's LM head;
+// reading: logits[m, v] = sum_h hidden[m, h] * W[v, h] with bf16 hidden
+// states [M, H] and weights [V, H] (row v holds vocabulary entry v), each
+// product exact in double, summed in double in h order and rounded once to
+// float]. Stage 1 then runs on these fp32 rows.
+int oracle_lmhead_logits(int M, int V, int H, const uint16_t* hidden, const uint16_t* W, float* logits) {
+    if (M < 0 || V < 1 || H < 1) return -1;
+    std::vector<double> hrow(static_cast<size_t>(H));
+    for (int m = 0; m < M; ++m) {
+        for (int h = 0; h < H; ++h) hrow[h] = load_logit(hidden, 1, static_cast<int64_t>(m) * H + h);
+        for (int v = 0; v < V; ++v) {
+            const uint16_t* wr = W + static_cast<int64_t>(v) * H;
+            double s = 0.0;
+            for (int h = 0; h < H; ++h) s += hrow[h] * static_cast<double>(load_logit(wr, 1, h));
+            logits[static_cast<int64_t>(m) * V + v] = static_cast<float>(s);
+        }
+    }
+    return 0;
+}
+
 }  // extern "C"

@@ -589,3 +589,66 @@ def test_dynamic_tree_gains_over_static_shape_on_sharp_landscapes():
     assert d_sharp > 1.08 * s_sharp  # 1.67 vs 1.49 at these seeds
     assert d_flat >= s_flat
     assert (d_flat - s_flat) / s_flat < (d_sharp - s_sharp) / s_sharp
+
+
+# ------------------------------------------------- LM-head logits (f1) ---
+# The draft reuses the target's LM head ("EAGLE" notes, EAGLE 方法): logits of a
+# frontier row are its hidden state times the head's weight rows.
+
+def _lmhead_case(M, V, H, seed):
+    h = synth.normal4((M, H), synth.BF16, 1.0, seed, synth.STREAM_HIDDEN)
+    W = synth.normal4((V, H), synth.BF16, 0.05, seed, synth.STREAM_LMHEAD)
+    return h, W
+
+
+def _f32_ulp(x):
+    x = np.abs(x.astype(np.float32))
+    return np.spacing(x).astype(np.float64)
+
+
+def test_lmhead_one_hot_rows_select_weight_columns():
+    # hidden row m = c_m * e_{h_m} with c_m a power of two: logits row m is
+    # exactly c_m * W[:, h_m] (one exact product per entry)
+    M, V, H = 6, 37, 24
+    _, W = _lmhead_case(M, V, H, 3)
+    h = np.zeros((M, H), np.uint16)
+    cols = [0, 5, 23, 11, 5, 17]
+    scales = [1.0, 2.0, 0.5, -4.0, 0.125, 1.0]
+    for m, (c, s) in enumerate(zip(cols, scales)):
+        h[m, c] = np.array([s], np.float32).view(np.uint32)[0] >> 16
+    got = oracle.lmhead_logits(h, W)
+    Wf = synth.bf16_to_f32(W)
+    for m, (c, s) in enumerate(zip(cols, scales)):
+        assert np.array_equal(got[m], (Wf[:, c] * np.float32(s)).astype(np.float32))
+
+
+def test_lmhead_matches_float64_matmul():
+    # non-square M, V, H so that a transposed operand cannot pass; the double
+    # sums differ from numpy's only in summation order, far below fp32 ulp
+    M, V, H = 5, 203, 96
+    h, W = _lmhead_case(M, V, H, 7)
+    got = oracle.lmhead_logits(h, W)
+    ref = synth.bf16_to_f32(h).astype(np.float64) @ synth.bf16_to_f32(W).astype(np.float64).T
+    err = np.abs(got.astype(np.float64) - ref)
+    assert np.all(err <= 0.5 * _f32_ulp(ref) + 1e-30)
+    assert np.mean(got == ref.astype(np.float32)) > 0.99
+
+
+def test_lmhead_linear_and_order_free():
+    M, V, H = 4, 64, 48
+    h, W = _lmhead_case(M, V, H, 11)
+    base = oracle.lmhead_logits(h, W)
+    # doubling (exponent + 1) and negation (sign bit) are exact on bf16 inputs
+    h2 = (synth.bf16_to_f32(h) * 2).view(np.uint32) >> 16
+    assert np.array_equal(oracle.lmhead_logits(h2.astype(np.uint16), W), 2 * base)
+    hn = h ^ np.uint16(0x8000)
+    assert np.array_equal(oracle.lmhead_logits(hn, W), -base)
+    # permuting the hidden dimension of both operands leaves each sum within rounding
+    perm = np.random.default_rng(0).permutation(H)
+    pp = oracle.lmhead_logits(np.ascontiguousarray(h[:, perm]), np.ascontiguousarray(W[:, perm]))
+    assert np.all(np.abs(pp.astype(np.float64) - base) <= _f32_ulp(base) + 1e-30)
+    # one weight row zeroed: that vocabulary column becomes 0, the others stay
+    Wz = W.copy()
+    Wz[9] = 0
+    z = oracle.lmhead_logits(h, Wz)
+    assert np.all(z[:, 9] == 0) and np.array_equal(np.delete(z, 9, 1), np.delete(base, 9, 1))
