@@ -54,6 +54,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel-reps", type=int, default=100)
     ap.add_argument("--layers", type=int, default=None, help="KV layers moved by compaction (memory cap)")
+    ap.add_argument("--lmhead", action="store_true",
+                    help="each draft step's rows come from the LM head (bf16 tensor-core GEMM of synthetic hidden "
+                         "states against a resident random [V, H] weight)")
     ap.add_argument("--policy", default="dynamic", choices=list(POLICIES),
                     help="tree policy: EAGLE-2, confidence-ranked frontier, or no rerank (ablations)")
     return ap.parse_args()
@@ -389,6 +392,12 @@ def main():
         sd = seed + 1000 * r
         host_sets.append(dict(draft=WL.draft_logits(w, sd, planted=args.planted), target=WL.target_logits(w, sd),
                               q=WL.queries(w, sd), uniforms=WL.uniforms(w, sd, r)))
+    weight_d = lm_out = None
+    if args.lmhead:
+        for r in range(R):
+            host_sets[r]["hidden"] = WL.hidden_states(w, seed + 1000 * r)
+        weight_h = WL.lmhead_weight(w, seed)
+        weight_d = to_dev(weight_h)
     dev_sets = [{k: to_dev(v) for k, v in s.items()} for s in host_sets]
     root = WL.root_tokens(w, seed)
     prefix_d = to_dev(prefix_len)
@@ -414,11 +423,17 @@ def main():
                  geo["seq_stride"], geo["layer_stride"], geo["kv_stride"], geo["pos_stride"])
     dc = C.DeviceCycle(cfg, kv)
     mode = E.GREEDY if w.verify == "greedy" else E.LOSSLESS
+    if args.lmhead:  # the draft rows are an intermediate written by the LM head every step
+        lm_out = torch.empty(w.depth, w.batch, w.top_k, w.vocab, dtype=C.torch_dtype(w.dtype), device="cuda")
 
     def cycle(r, stream=None):
         s = dev_sets[r]
-        dc.run(s["draft"], prefix_d, root_d, s["q"], cache, r, s["target"], s["uniforms"], mode, w.temperature,
-               compact=True, stream=stream)
+        if args.lmhead:
+            dc.run(lm_out, prefix_d, root_d, s["q"], cache, r, s["target"], s["uniforms"], mode, w.temperature,
+                   compact=True, stream=stream, head=(weight_d, s["hidden"]))
+        else:
+            dc.run(s["draft"], prefix_d, root_d, s["q"], cache, r, s["target"], s["uniforms"], mode, w.temperature,
+                   compact=True, stream=stream)
 
     # warm-up outside capture (sets kernel attributes), then one graph per set
     for r in range(R):
@@ -535,6 +550,10 @@ def main():
     cycle(0)
     torch.cuda.synchronize()
     kt = {}
+    if args.lmhead:
+        kt["lmhead"] = time_call(lambda r: E.eagle_lmhead(cfg, dc.ws, w.hidden_size, dev_sets[r]["hidden"][1],
+                                                          weight_d, lm_out[1]), reps)
+        cycle(0)
     kt["expand_step"] = time_call(lambda r: E.eagle_expand(cfg, dc.ws, min(1, w.depth - 1), dev_sets[r]["draft"][
         min(1, w.depth - 1)], None, dc.row_lse, dc.ftok, dc.fcount), reps)
     cycle(0)
@@ -553,43 +572,54 @@ def main():
         os.path.join(ROOT, "MEASURED_PEAKS.json")) else None
     hbm_peak = peak["hbm_gbs"] if peak else 6800.0
     peak_src = "measured" if peak else "fallback"
+    tensor_peak = peak["bf16_tflops"] if peak else 1900.0
+    # LM head of one step: the weight, the hidden rows, the logits written
+    lm_flop = 2 * w.batch * w.top_k * w.vocab * w.hidden_size
+    lm_bytes = (w.vocab + w.batch * w.top_k) * w.hidden_size * 2 + w.batch * w.top_k * w.vocab * w.esize
     per_kernel = {}
     for name, ms_k in kt.items():
         byt = {"expand_step": alg["expand_step"], "attention": alg["attention"], "verify": alg["verify"],
+               "lmhead": lm_bytes,
                "compact": algorithmic_bytes(w, prefix_len, acc_compact, w.layers)["compact"]}.get(name)
         e = {"ms": round(ms_k, 5)}
         if byt is not None:
             e["bytes"] = int(byt)
             e["GB_s"] = round(byt / (ms_k * 1e-3) / 1e9, 1)
             e["frac_hbm"] = round(byt / (ms_k * 1e-3) / 1e9 / hbm_peak, 4)
-        if name == "attention":
-            e["tflops"] = round(attn_flop / (ms_k * 1e-3) / 1e12, 1)
+        flop = {"attention": attn_flop, "lmhead": lm_flop}.get(name)
+        if flop is not None:
+            e["tflops"] = round(flop / (ms_k * 1e-3) / 1e12, 1)
             if peak:
-                e["frac_tensor"] = round(attn_flop / (ms_k * 1e-3) / 1e12 / peak["bf16_tflops"], 4)
+                e["frac_tensor"] = round(flop / (ms_k * 1e-3) / 1e12 / peak["bf16_tflops"], 4)
         per_kernel[name] = e
     cyc_share = {"expand_step": kt["expand_step"] * (w.depth - 1), "attention": kt["attention"],
                  "verify": kt["verify"]}
+    if args.lmhead:
+        cyc_share["lmhead"] = kt["lmhead"] * w.depth
     dom = max(cyc_share, key=cyc_share.get)
-    dom_bytes = {"expand_step": alg["expand_step"], "attention": alg["attention"], "verify": alg["verify"]}[dom]
+    dom_bytes = {"expand_step": alg["expand_step"], "attention": alg["attention"], "verify": alg["verify"],
+                 "lmhead": lm_bytes}[dom]
     achieved = dom_bytes / (kt[dom] * 1e-3) / 1e9
-    kname = {"expand_step": "expand_kernel", "attention": "attention", "verify": "verify_kernel"}[dom]
+    kname = {"expand_step": "expand_kernel", "attention": "attention", "verify": "verify_kernel",
+             "lmhead": "lmhead_kernel"}[dom]
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(achieved / hbm_peak, 4), "traffic": ncu_traffic(kname, w.name), "kernel": kname,
                 "peak_source": f"{peak_src} hbm_gbs (burst copy)",
                 "bytes_per_launch": int(dom_bytes)}
-    tensor_peak = peak["bf16_tflops"] if peak else 1900.0
-    if dom == "attention" and attn_flop / (tensor_peak * 1e12) > dom_bytes / (hbm_peak * 1e9):
-        # the attention shape is compute-bound: its roofline is the tensor pipe (bf16 dense)
-        ach_t = attn_flop / (kt[dom] * 1e-3) / 1e12
+    dom_flop = {"attention": attn_flop, "lmhead": lm_flop}.get(dom, 0)
+    if dom_flop / (tensor_peak * 1e12) > dom_bytes / (hbm_peak * 1e9):
+        # a compute-bound contraction: its roofline is the tensor pipe (bf16 dense)
+        ach_t = dom_flop / (kt[dom] * 1e-3) / 1e12
         roofline.update({"bound": "tensor", "achieved": round(ach_t, 1), "peak": tensor_peak, "unit": "TFLOP/s",
                          "frac": round(ach_t / tensor_peak, 4),
                          "peak_source": f"{peak_src} bf16_tflops (burst cuBLAS GEMM)",
-                         "flop_per_launch": int(attn_flop)})
+                         "flop_per_launch": int(dom_flop)})
 
     # ---- end to end through host buffers ----
     e2e = None
     if not args.no_e2e:
-        pin = [{k: pinned(v) for k, v in s.items()} for s in host_sets]
+        # with the LM head on, the draft rows are not an input (the hidden states are)
+        pin = [{k: pinned(v) for k, v in s.items() if not (args.lmhead and k == "draft")} for s in host_sets]
         out_a = torch.empty(w.batch, dtype=torch.int32).pin_memory()
         out_t = torch.empty(w.batch, w.depth + 1, dtype=torch.int32).pin_memory()
         out_n = torch.empty(w.batch, dtype=torch.int32).pin_memory()
@@ -632,8 +662,20 @@ def main():
             tot += oracle_cycle(w, s0, prefix_len, root, kh, vh, geo, w.verify, region,
                                 policy=POLICIES[args.policy])
             n += 1
-        cpu = {"value": round(n / tot, 4), "unit": "cycles/s", "cores": 1, "kind": "oracle",
-               "sample": f"{n} whole oracle cycles of {w.name} (every stage, all attention rows) on one host core"}
+        sample = f"{n} whole oracle cycles of {w.name} (every stage, all attention rows) on one host core"
+        per_cycle = tot / n
+        if args.lmhead:
+            # the oracle's LM head on one row against 2048 vocabulary rows, scaled to
+            # every row of every step and the whole vocabulary
+            nv = min(w.vocab, 2048)
+            t1 = time.perf_counter()
+            oracle.lmhead_logits(np.ascontiguousarray(host_sets[0]["hidden"][0, :1]), weight_h[:nv])
+            t_lm = time.perf_counter() - t1
+            per_cycle += t_lm * w.depth * w.batch * w.top_k * (w.vocab / nv)
+            sample += (f"; plus the oracle LM head timed on 1 row x {nv} vocabulary rows x {w.hidden_size} and scaled "
+                       f"to {w.depth} steps x {w.batch * w.top_k} rows x {w.vocab} entries")
+        cpu = {"value": round(1.0 / per_cycle, 6), "unit": "cycles/s", "cores": 1, "kind": "oracle",
+               "sample": sample}
 
     if rank == 0:
         line = {
@@ -646,7 +688,8 @@ def main():
                        "head_dim": w.head_dim, "prefix": w.prefix if not isinstance(w.prefix, tuple) else
                        list(w.prefix), "sharpness": w.sharpness if not isinstance(w.sharpness, tuple) else
                        list(w.sharpness), "verify": w.verify, "compact_layers": w.layers, "planted": args.planted,
-                       "aligned": args.aligned, "policy": args.policy,
+                       "aligned": args.aligned, "policy": args.policy, "lmhead": args.lmhead,
+                       "hidden_size": w.hidden_size if args.lmhead else None,
                        "l2": f"{R} rotating input sets, {round(R * (per_set + attn_bytes) / 2**20)} MiB > 129 MB L2",
                        "graph": "one CUDA graph per input set, replayed"},
             "tokens_of_tree_per_s": round(value * float(np.mean(n_tree)) * w.batch, 1),

@@ -15,6 +15,7 @@
  *
  * One cycle, in call order:
  *   eagle_tree_init                       reset the tree state in `ws`
+ *   eagle_lmhead (optional, per step)     LM-head logits of the frontier rows
  *   eagle_expand(step = 0 .. depth-1)     stages 1+2, one call per draft step
  *   eagle_rerank                          stage 3
  *   eagle_build_tree                      stage 4
@@ -152,6 +153,27 @@ int eagle_tree_init(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, void* 
 int eagle_expand(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int step, const void* draft_logits,
                  const float* row_lse_in, float* row_lse, int32_t* frontier_tokens, int32_t* frontier_count,
                  void* stream);
+
+/*
+ * LM head of a draft step, the projection whose rows stages 1+2 read
+ * [notes EAGLE 方法: the draft model reuses the target model's LM head].
+ *   hidden_dim      H, a multiple of 8 (>= 8).
+ *   hidden          [B*k, H] bf16 in: row b*k + f is the draft model's last
+ *                   hidden state for frontier slot f of sequence b (rows of
+ *                   slots past the frontier count may hold anything finite).
+ *   weight          [V, H] bf16 in: row v is vocabulary entry v's weights.
+ *   draft_logits    [B, k, V] out, in cfg->logit_dtype: logits[r, v] =
+ *                   sum_h hidden[r, h] * weight[v, h], accumulated in fp32
+ *                   on the tensor cores (order and rounding of the fp32
+ *                   sums unspecified; within H * 2^-23 * sum_h
+ *                   |hidden[r, h] * weight[v, h]| of the exact sum), then
+ *                   rounded to nearest even for bf16. The buffer
+ *                   is the draft_logits argument of eagle_expand.
+ * All three pointers 16-byte aligned; the weight stays read-only. Uses the
+ * workspace's status word only (a timed-out wait raises it).
+ */
+int eagle_lmhead(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int hidden_dim, const void* hidden,
+                 const void* weight, void* draft_logits, void* stream);
 
 /*
  * Stage 3 [summary 4.2; tutorial "Value of a Node"; notes EAGLE 2 方法,

@@ -133,6 +133,20 @@ int eagle_expand(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int step,
                                        frontier_count, static_cast<cudaStream_t>(stream)));
 }
 
+int eagle_lmhead(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int hidden_dim, const void* hidden,
+                 const void* weight, void* draft_logits, void* stream) {
+    TreeDims d;
+    TreeWs w;
+    int rc = resolve(cfg, &d);
+    if (rc == EAGLE_OK) rc = bind_ws(d, ws, ws_bytes, &w);
+    if (rc != EAGLE_OK) return rc;
+    if (!hidden || !weight || !draft_logits || hidden_dim < 8) return EAGLE_ERR_INVALID_ARG;
+    if (hidden_dim % 8 != 0 || !aligned16(hidden) || !aligned16(weight) || !aligned16(draft_logits))
+        return EAGLE_ERR_UNSUPPORTED;
+    return launch_result(launch_lmhead(d.B * d.k, d.V, hidden_dim, hidden, weight, d.dtype, draft_logits, w.status,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 int eagle_rerank(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, void* stream) {
     TreeDims d;
     TreeWs w;

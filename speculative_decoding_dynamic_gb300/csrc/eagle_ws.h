@@ -141,6 +141,10 @@ cudaError_t launch_kv_compact(const KvDims& kv, void* cache, const int32_t* pref
                               cudaStream_t stream);
 
 size_t attention_ws_bytes(const KvDims& kv, int T);
+// LM-head logits [M, V] (fp32, or bf16 when out_dtype is 1) of hidden [M, H]
+// and weight [V, H] (bf16), on the tensor cores.
+cudaError_t launch_lmhead(int M, int V, int H, const void* hidden, const void* weight, int out_dtype, void* out,
+                          int* status, cudaStream_t stream);
 cudaError_t launch_attention(const KvDims& kv, int T, const void* q, const void* cache, int layer,
                              const int32_t* prefix_len, const uint32_t* mask, const int32_t* n_tree, void* out,
                              void* ws, size_t ws_bytes, int* status, cudaStream_t stream);

@@ -620,7 +620,19 @@ bool tc_supported(const KvDims& kv, int T) {
            (kv.kv_stride * 2) % 16 == 0;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+bool make_map(CUtensorMap* m, const void* base, const cuuint64_t dims[4], const cuuint64_t strides_bytes[3],
+              const cuuint32_t box[4]) {
+    auto fn = tensor_map_encode_fn();
+    if (!fn) return false;
+    const cuuint32_t estride[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides_bytes, box, estride,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
     std::call_once(once, [] {
@@ -633,18 +645,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     });
     return fn;
 }
-
-bool make_map(CUtensorMap* m, const void* base, const cuuint64_t dims[4], const cuuint64_t strides_bytes[3],
-              const cuuint32_t box[4]) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    const cuuint32_t estride[4] = {1, 1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides_bytes, box, estride,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-}  // namespace
 
 size_t attention_ws_bytes(const KvDims& kv, int T) {
     if (!tc_supported(kv, T)) return 256;

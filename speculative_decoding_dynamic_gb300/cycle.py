@@ -42,12 +42,17 @@ class DeviceCycle:
         self.new_len = torch.empty(B, **i32)
 
     # ---- stages -----------------------------------------------------------
-    def draft(self, draft_logits: torch.Tensor, stream=None, steps=None, lse_in=None):
+    def draft(self, draft_logits: torch.Tensor, stream=None, steps=None, lse_in=None, head=None):
         """Stages 1-3. draft_logits: [D, B, k, V] (one contiguous block per step);
-        lse_in: optional [D, B, k] row log-sum-exp supplied from upstream."""
+        lse_in: optional [D, B, k] row log-sum-exp supplied from upstream.
+        head: optional (weight [V, H], hidden [D, B*k, H]), both bf16: each
+        step's rows are then first written into draft_logits[s] by the LM head."""
         cfg = self.cfg
         E.eagle_tree_init(cfg, self.ws, stream)
         for s in range(cfg.depth if steps is None else steps):
+            if head is not None:
+                weight, hidden = head
+                E.eagle_lmhead(cfg, self.ws, hidden.shape[-1], hidden[s], weight, draft_logits[s], stream)
             E.eagle_expand(cfg, self.ws, s, draft_logits[s], None if lse_in is None else lse_in[s], self.row_lse,
                            self.ftok, self.fcount, stream)
         if steps is None:
@@ -70,9 +75,9 @@ class DeviceCycle:
                            self.ws, stream)
 
     def run(self, draft_logits, prefix_len, root_token, q, cache, layer, target, uniforms, mode, temperature=1.0,
-            compact=True, stream=None):
+            compact=True, stream=None, head=None):
         """The whole cycle (all stages) enqueued on `stream`."""
-        self.draft(draft_logits, stream)
+        self.draft(draft_logits, stream, head=head)
         self.build(prefix_len, root_token, stream)
         self.attention(q, cache, layer, prefix_len, stream)
         self.verify(mode, temperature, target, uniforms, stream)

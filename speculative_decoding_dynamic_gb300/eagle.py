@@ -73,6 +73,7 @@ _lib.eagle_workspace_bytes.argtypes = [_TP]
 _lib.eagle_workspace_bytes.restype = _sz
 _lib.eagle_tree_init.argtypes = [_TP, _p, _sz, _p]
 _lib.eagle_expand.argtypes = [_TP, _p, _sz, _i, _p, _p, _p, _p, _p, _p]
+_lib.eagle_lmhead.argtypes = [_TP, _p, _sz, _i, _p, _p, _p, _p]
 _lib.eagle_rerank.argtypes = [_TP, _p, _sz, _p]
 _lib.eagle_tree_value.argtypes = [_TP, _p, _sz, _p, _p]
 _lib.eagle_build_tree.argtypes = [_TP, _p, _sz, _p, _p, _p, _p, _p, _p, _p, _p, _p]
@@ -140,6 +141,11 @@ def eagle_expand(cfg, ws, step, draft_logits, row_lse_in, row_lse, frontier_toke
     _check("eagle_expand", _lib.eagle_expand(ctypes.byref(cfg), *_ws(ws), step, _ptr(draft_logits),
                                              _ptr(row_lse_in), _ptr(row_lse), _ptr(frontier_tokens),
                                              _ptr(frontier_count), _stream(stream)))
+
+
+def eagle_lmhead(cfg, ws, hidden_dim, hidden, weight, draft_logits, stream=None):
+    _check("eagle_lmhead", _lib.eagle_lmhead(ctypes.byref(cfg), *_ws(ws), hidden_dim, _ptr(hidden), _ptr(weight),
+                                             _ptr(draft_logits), _stream(stream)))
 
 
 def eagle_rerank(cfg, ws, stream=None):

@@ -14,8 +14,8 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-from . import BF16, F32, STREAM_DRAFT, STREAM_K, STREAM_Q, STREAM_TARGET, STREAM_V, kv_region, normal4, plant, \
-    seq_params, words
+from . import BF16, F32, STREAM_DRAFT, STREAM_HIDDEN, STREAM_K, STREAM_LMHEAD, STREAM_Q, STREAM_TARGET, STREAM_V, \
+    kv_region, normal4, plant, seq_params, words
 
 
 @dataclass
@@ -37,6 +37,7 @@ class Workload:
     layers: int  # layers moved by compaction (memory-capped for 70B)
     model_layers: int
     temperature: float = 1.0
+    hidden_size: int = 0  # LM-head input width of the model
     notes: str = ""
     extra: dict = field(default_factory=dict)
 
@@ -81,22 +82,23 @@ class Workload:
 WORKLOADS: dict[str, Workload] = {
     "tiny": Workload("tiny", batch=1, vocab=1024, top_k=2, depth=3, node_budget=8, threshold=0.1, dtype=F32,
                      n_q_heads=4, n_kv_heads=4, head_dim=16, prefix=32, sharpness=2.5, verify="greedy", layers=1,
-                     model_layers=1, notes="CPU-checkable cycle; threshold 0.1, k 2, N 8 as in the EAGLE notes' figure"),
+                     model_layers=1, hidden_size=64,
+                     notes="CPU-checkable cycle; threshold 0.1, k 2, N 8 as in the EAGLE notes' figure"),
     "llama8b_b1": Workload("llama8b_b1", batch=1, vocab=128256, top_k=10, depth=6, node_budget=60, threshold=0.0,
                            dtype=BF16, n_q_heads=32, n_kv_heads=8, head_dim=128, prefix=2048, sharpness=2.5,
-                           verify="lossless", layers=32, model_layers=32,
+                           verify="lossless", layers=32, model_layers=32, hidden_size=4096,
                            notes="Llama-3.1-8B shape, batch 1 (sharpness 0.8 and 2.5; greedy and lossless)"),
     "vicuna13b_b1": Workload("vicuna13b_b1", batch=1, vocab=32000, top_k=10, depth=6, node_budget=60, threshold=0.0,
                              dtype=BF16, n_q_heads=40, n_kv_heads=40, head_dim=128, prefix=4096, sharpness=2.5,
-                             verify="lossless", layers=40, model_layers=40,
+                             verify="lossless", layers=40, model_layers=40, hidden_size=5120,
                              notes="Vicuna-13B shape, batch 1, MHA, lossless at temperature 1"),
     "llama8b_b64": Workload("llama8b_b64", batch=64, vocab=128256, top_k=10, depth=6, node_budget=60, threshold=0.0,
                             dtype=BF16, n_q_heads=32, n_kv_heads=8, head_dim=128, prefix=(256, 1793),
-                            sharpness=(0.8, 1.7), verify="greedy", layers=32, model_layers=32,
+                            sharpness=(0.8, 1.7), verify="greedy", layers=32, model_layers=32, hidden_size=4096,
                             notes="Llama-3.1-8B shape, batch 64, prefix U[256,2048], sharpness U[0.8,2.5]"),
     "llama70b_b8": Workload("llama70b_b8", batch=8, vocab=128256, top_k=8, depth=8, node_budget=64, threshold=0.0,
                             dtype=BF16, n_q_heads=64, n_kv_heads=8, head_dim=128, prefix=32768, sharpness=1.5,
-                            verify="lossless", layers=16, model_layers=80,
+                            verify="lossless", layers=16, model_layers=80, hidden_size=8192,
                             notes="Llama-3.3-70B shape, batch 8, 32K prefix; compaction capped at 16 of 80 layers"),
 }
 
@@ -116,6 +118,24 @@ def draft_logits(w: Workload, seed: int, planted: bool = False) -> np.ndarray:
         # one planted token per row, same value for the batch (uses the mean sharpness)
         plant(out, w.dtype, plant_value(w, float(np.mean(s))), seed, STREAM_DRAFT)
     return out
+
+
+LMHEAD_STD = 0.02  # weight scale of the synthetic LM head
+
+
+def lmhead_weight(w: Workload, seed: int) -> np.ndarray:
+    """[V, H] bf16 LM-head weights, 0.02 * N(0,1): element (v, h) at counter (h, v, 0, 0), stream 9."""
+    return normal4((w.vocab, w.hidden_size), BF16, LMHEAD_STD, seed, STREAM_LMHEAD)
+
+
+def hidden_states(w: Workload, seed: int) -> np.ndarray:
+    """[D, B*k, H] bf16 draft hidden states of the frontier rows, one block per
+    draft step, scaled so that logits through ``lmhead_weight`` have standard
+    deviation about the workload's (mean) sharpness: element (s, r, h) at
+    counter (h, r, s, 0), stream 8."""
+    s = float(np.mean(w.sharpness_per_seq(seed)))
+    scale = s / (LMHEAD_STD * math.sqrt(w.hidden_size))
+    return normal4((w.depth, w.batch * w.top_k, w.hidden_size), BF16, scale, seed, STREAM_HIDDEN)
 
 
 def target_logits(w: Workload, seed: int) -> np.ndarray:

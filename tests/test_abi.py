@@ -84,6 +84,11 @@ def test_calls_reject_bad_arguments_before_launch(E):
              ptr, ptr, ptr, None) == -1
     assert r("eagle_verify", ctypes.byref(cfg), fake_ws, ws_bytes, 1, ctypes.c_float(1.0), ptr, ptr, ptr, ptr, None,
              ptr, ptr, ptr, None) == -1
+    assert r("eagle_lmhead", ctypes.byref(cfg), fake_ws, ws_bytes, 4096, None, ptr, ptr, None) == -1
+    assert r("eagle_lmhead", ctypes.byref(cfg), fake_ws, ws_bytes, 0, ptr, ptr, ptr, None) == -1
+    assert r("eagle_lmhead", ctypes.byref(cfg), fake_ws, ws_bytes, 4100, ptr, ptr, ptr, None) == -2  # H % 8
+    assert r("eagle_lmhead", ctypes.byref(cfg), fake_ws, ws_bytes, 4096, ptr, P((1 << 21) + 8), ptr, None) == -2
+    assert r("eagle_lmhead", ctypes.byref(cfg), None, ws_bytes, 4096, ptr, ptr, ptr, None) == -4
     kv = E.KvCfg(2, 8, 3, 64, 4, 100, E.EAGLE_BF16, 0, 0, 0, 192)  # 8 % 3 != 0
     assert r("eagle_tree_attention", ctypes.byref(kv), 9, ptr, ptr, 0, ptr, ptr, ptr, ptr, fake_ws, 4096, None) == -1
     kv = E.KvCfg(2, 8, 2, 64, 4, 100, E.EAGLE_BF16, 4 * 2 * 100 * 128, 2 * 100 * 128, 100 * 128, 128)

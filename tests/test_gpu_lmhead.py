@@ -1,0 +1,132 @@
+"""LM-head logits on the tensor cores against the oracle, and a draft step fed by them.
+
+The draft model reuses the target's LM head ("EAGLE" notes, EAGLE 方法). The
+oracle sums the exact bf16 products in double and rounds once; the kernel
+accumulates in fp32 on the tensor cores in an unspecified order and rounding,
+so each entry must lie within H * 2^-23 * sum_h |hidden[h] W[v, h]| of the
+exact sum (recursive fp32 summation of H terms, round-toward-zero allowed),
+plus half a bf16 ulp when the output is bf16. A dropped or repeated 64-wide
+hidden block, a transposed operand or a wrong vocabulary tile misses that
+bound by orders of magnitude.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+import harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+def _E():
+    from speculative_decoding_dynamic_gb300 import eagle as E
+    return E
+
+
+def _inputs(M, V, Hd, seed):
+    h = synth.normal4((M, Hd), synth.BF16, 1.0, seed, synth.STREAM_HIDDEN)
+    W = synth.normal4((V, Hd), synth.BF16, 0.05, seed, synth.STREAM_LMHEAD)
+    return h, W
+
+
+def _check(got, h, W, dtype):
+    ref = oracle.lmhead_logits(h, W).astype(np.float64)
+    a = np.abs(synth.bf16_to_f32(h)).astype(np.float64)
+    b = np.abs(synth.bf16_to_f32(W)).astype(np.float64)
+    tol = h.shape[1] * 2.0 ** -23 * (a @ b.T) + np.spacing(np.abs(ref).astype(np.float32)).astype(np.float64)
+    if dtype == synth.BF16:
+        tol = tol + 2.0 ** -8 * (np.abs(ref) + tol)
+        g = synth.bf16_to_f32(got).astype(np.float64)
+    else:
+        g = got.astype(np.float64)
+    err = np.abs(g - ref)
+    assert np.all(err <= tol), f"max err {err.max()} at {np.unravel_index(np.argmax(err - tol), err.shape)}"
+    return g
+
+
+def _lmhead(E, cfg, ws, Hd, dh, dW):
+    import torch
+    B, k, V = cfg.batch, cfg.top_k, cfg.vocab
+    dt = torch.float32 if cfg.logit_dtype == synth.F32 else torch.bfloat16
+    out = torch.full((B, k, V), float("nan"), dtype=dt, device="cuda")
+    E.eagle_lmhead(cfg, ws, Hd, dh, dW, out)
+    torch.cuda.synchronize()
+    assert E.eagle_status_fetch(ws) == 0
+    return H.to_host(out).reshape(B * k, V)
+
+
+@pytest.mark.parametrize("B,k,V,Hd,dtype", [
+    (1, 10, 1000, 256, synth.F32),     # 10 rows (one 16-column MMA), ragged last vocabulary tile
+    (1, 10, 1000, 200, synth.BF16),    # hidden size not a multiple of 64: zero-filled last block
+    (30, 10, 2056, 512, synth.F32),    # 300 rows: two row chunks of 160
+    (1, 1, 136, 64, synth.F32),        # one row, one hidden block, 8-row last tile
+    (64, 10, 4096, 128, synth.BF16),   # 640 rows: three chunks of 224 (the last one 192 live)
+    (2, 16, 384, 1024, synth.BF16),    # 32 rows, 16 hidden blocks (the ring wraps)
+])
+def test_lmhead_matches_oracle(B, k, V, Hd, dtype):
+    E = _E()
+    cfg = E.TreeCfg(B, V, k, 1, 1, 0.0, dtype, 0)
+    ws = E.alloc_workspace(E.eagle_workspace_bytes(cfg))
+    h, W = _inputs(B * k, V, Hd, seed=V + Hd)
+    got = _lmhead(E, cfg, ws, Hd, H.to_dev(h), H.to_dev(W))
+    _check(got, h, W, dtype)
+
+
+@pytest.fixture(scope="module")
+def llama8b_head():
+    """Llama-8B-shaped LM head (V = 128256, H = 4096), bf16, on the device."""
+    V, Hd = 128256, 4096
+    W = synth.normal4((V, Hd), synth.BF16, 0.02, 8, synth.STREAM_LMHEAD)
+    return V, Hd, W, H.to_dev(W)
+
+
+@pytest.mark.parametrize("B", [1, 64])
+def test_lmhead_full_size_sampled(llama8b_head, B):
+    """Full vocabulary and hidden size at batch 1 and 64 (k = 10): sampled
+    vocabulary columns (every tile boundary of a few tiles, the last entries
+    and a seeded spread) against the oracle."""
+    E = _E()
+    V, Hd, W, dW = llama8b_head
+    k = 10
+    cfg = E.TreeCfg(B, V, k, 6, 60, 0.0, synth.BF16, 0)
+    ws = E.alloc_workspace(E.eagle_workspace_bytes(cfg))
+    h = synth.normal4((B * k, Hd), synth.BF16, 1.0, B, synth.STREAM_HIDDEN)
+    got = _lmhead(E, cfg, ws, Hd, H.to_dev(h), dW)
+    rng = np.random.default_rng(B)
+    cols = np.unique(np.concatenate([[0, 1, 127, 128, 129, 255, 256, 1001 * 128 - 1, 1001 * 128, V - 2, V - 1],
+                                     rng.integers(0, V, 53)]))
+    _check(np.ascontiguousarray(got[:, cols]), h, np.ascontiguousarray(W[cols]), synth.BF16)
+    assert np.isfinite(synth.bf16_to_f32(got)).all()
+
+
+def test_lmhead_feeds_expand():
+    """One draft step on device logits: the expansion equals the oracle's on
+    the same (device-written) rows and log-sum-exps."""
+    import torch
+    E = _E()
+    B, k, V, Hd = 2, 4, 4104, 256
+    cfg = E.TreeCfg(B, V, k, 1, 4, 0.0, synth.BF16, 0)
+    ws = E.alloc_workspace(E.eagle_workspace_bytes(cfg))
+    h, W = _inputs(B * k, V, Hd, seed=5)
+    E.eagle_tree_init(cfg, ws)
+    out = torch.empty(B, k, V, dtype=torch.bfloat16, device="cuda")
+    E.eagle_lmhead(cfg, ws, Hd, H.to_dev(h), H.to_dev(W), out)
+    torch.cuda.synchronize()
+    lg = H.to_host(out)
+    _check(lg.reshape(B * k, V), h, W, synth.BF16)
+    lse = np.zeros((B, k), np.float32)
+    for b in range(B):
+        for f in range(k):
+            _, lse[b, f], _ = oracle.row_stats(np.ascontiguousarray(lg[b, f]), 1)
+    t = oracle.Tree(oracle.TreeCfg(B, V, k, 1, 4, 0.0, 0))
+    ftok_o, fcnt_o = t.expand(0, lg)[:2]
+    i32 = dict(dtype=torch.int32, device="cuda")
+    row_lse = torch.empty(B, 1, k, dtype=torch.float32, device="cuda")
+    ftok, fcnt = torch.empty(B, k, **i32), torch.empty(B, **i32)
+    E.eagle_expand(cfg, ws, 0, out, H.to_dev(lse), row_lse, ftok, fcnt)
+    torch.cuda.synchronize()
+    assert (H.to_host(fcnt) == fcnt_o).all()
+    assert (H.to_host(ftok) == ftok_o).all()
+    assert E.eagle_status_fetch(ws) == 0
