@@ -582,12 +582,12 @@ def main():
                "lmhead": lm_bytes,
                "compact": algorithmic_bytes(w, prefix_len, acc_compact, w.layers)["compact"]}.get(name)
         e = {"ms": round(ms_k, 5)}
-        if byt is not None:
+        if byt is not None and ms_k > 0:  # (a flushed timing of a tiny call can come out as 0)
             e["bytes"] = int(byt)
             e["GB_s"] = round(byt / (ms_k * 1e-3) / 1e9, 1)
             e["frac_hbm"] = round(byt / (ms_k * 1e-3) / 1e9 / hbm_peak, 4)
         flop = {"attention": attn_flop, "lmhead": lm_flop}.get(name)
-        if flop is not None:
+        if flop is not None and ms_k > 0:
             e["tflops"] = round(flop / (ms_k * 1e-3) / 1e12, 1)
             if peak:
                 e["frac_tensor"] = round(flop / (ms_k * 1e-3) / 1e12 / peak["bf16_tflops"], 4)
