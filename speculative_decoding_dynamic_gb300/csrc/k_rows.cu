@@ -56,7 +56,12 @@ constexpr int kVecPerLane = 4;
 constexpr int kVecPerWarp = 32 * kVecPerLane;
 static_assert(kVecPerWarp * kConsumerWarps * 16 == kRowChunkBytes, "chunk geometry");
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kMaxSegChunks = 8;  // chunks of one CTA's row segment in expansion
+constexpr int kMaxSegChunks = 8;  // chunks of one CTA's row segment in expansion (fp32 rows)
+// bf16 rows: group maxima are bf16 values, whose order-preserving bits are
+// decided by their top half, so 16 bits per group and twice the chunks fit
+constexpr int kMaxSegChunksBf16 = 2 * kMaxSegChunks;
+template <int DT>
+__host__ __device__ constexpr int max_seg_chunks() { return DT == 1 ? kMaxSegChunksBf16 : kMaxSegChunks; }
 constexpr int kExpandStages = 2;  // five CTAs per SM (40 registers, ~43 KB shared memory each)
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -268,7 +273,7 @@ __device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" 
 struct ExpandSmem {
     RowRing ring;
     unsigned long long tau;                       // segment admission key (atomic maximum)
-    uint32_t gmax[kMaxSegChunks][kConsumers];     // maximum of each lane group (ordered bits)
+    uint32_t gmax[kMaxSegChunks][kConsumers];     // maximum of each lane group (ordered bits; see gmax_put)
     int ngroups, nkeys;
     float wm[kConsumerWarps];
     float ws[kConsumerWarps];
@@ -280,6 +285,25 @@ struct ExpandSmem {
     uint64_t top[kMaxTopK];
     int last;
 };
+
+// Group maximum of lane group (chunk c, consumer thread t), as ordered bits.
+// bf16 rows keep the top 16 bits only (exact for bf16 values: equal top
+// halves mean equal values), read back as (top << 16); compare them with
+// gmax_floor(tau). 0 marks a group without elements.
+template <int DT>
+__device__ __forceinline__ void gmax_put(ExpandSmem& sm, int c, int t, uint32_t o) {
+    if (DT == 1)
+        reinterpret_cast<uint16_t*>(&sm.gmax[0][0])[c * kConsumers + t] = static_cast<uint16_t>(o >> 16);
+    else
+        sm.gmax[c][t] = o;
+}
+template <int DT>
+__device__ __forceinline__ uint32_t gmax_get(const ExpandSmem& sm, int c, int t) {
+    if (DT == 1) return static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(&sm.gmax[0][0])[c * kConsumers + t]) << 16;
+    return sm.gmax[c][t];
+}
+template <int DT>
+__device__ __forceinline__ uint32_t gmax_floor(uint32_t o) { return DT == 1 ? (o & 0xFFFF0000u) : o; }
 
 // Top-k keys of a CTA's row segment, after the streaming pass (consumer
 // threads only). A lane group is one lane's four vectors of one chunk, and
@@ -309,8 +333,8 @@ __device__ __forceinline__ void segment_topk(ExpandSmem& sm, const unsigned char
     const int kcap = (scratch_bytes - gcap * static_cast<int>(sizeof(uint32_t))) / static_cast<int>(sizeof(uint64_t));
     // candidate groups: this thread's own lane groups, appended warp by warp
     for (int c = 0; c < nch; ++c) {
-        const uint32_t gm = sm.gmax[c][tid];
-        const bool hot = gm != 0u && (all || gm >= tau_o);
+        const uint32_t gm = gmax_get<DT>(sm, c, tid);
+        const bool hot = gm != 0u && (all || gm >= gmax_floor<DT>(tau_o));
         const unsigned bal = __ballot_sync(0xffffffffu, hot);
         if (bal == 0u) continue;
         int base = 0;
@@ -439,7 +463,7 @@ __global__ void __launch_bounds__(kRowThreads, 5) expand_kernel(TreeDims d, Tree
 
     const int c0 = rank * seg;
     const int n = max(0, min(seg, d.V - c0));
-    const int nch = min(kMaxSegChunks, (n * ES + kRowChunkBytes - 1) / kRowChunkBytes);  // the launcher keeps <= 8
+    const int nch = min(max_seg_chunks<DT>(), (n * ES + kRowChunkBytes - 1) / kRowChunkBytes);  // the launcher keeps within
     const char* row_base = static_cast<const char*>(logits) + static_cast<size_t>(b * d.k + f) * d.V * ES;
     if (tid == 0) {
         ring_init(sm.ring, ns);
@@ -469,7 +493,7 @@ __global__ void __launch_bounds__(kRowThreads, 5) expand_kernel(TreeDims d, Tree
             load_lane<DT>(dyn_smem + (c % ns) * kRowChunkBytes, nvec, warp, lane, u);
             ring_release(sm.ring, c, ns);
             const float cm = lane_max4<DT>(u);
-            sm.gmax[c][tid] = warp * kVecPerWarp + lane < nvec ? f2o(cm) : 0u;
+            gmax_put<DT>(sm, c, tid, warp * kVecPerWarp + lane < nvec ? f2o(cm) : 0u);
             if (cm > m_l) {
                 s_l = (do_sum && m_l > -INFINITY) ? s_l * ex2_approx((m_l - cm) * kLog2e) : 0.0f;
                 m_l = cm;
@@ -1197,7 +1221,24 @@ cudaError_t launch_expand(const TreeDims& d, const TreeWs& ws, int step, const v
                           float* row_lse, int32_t* ftok, int32_t* fcount_out, cudaStream_t stream) {
     const int esize = d.dtype == 1 ? 2 : 4;
     const long rows = static_cast<long>(d.B) * d.k;
+    const int max_seg = esize == 2 ? kMaxSegChunksBf16 : kMaxSegChunks;
     RowPlan p = plan_rows(d.V, esize, rows, false, kExpandStages, kMaxSegChunks);
+    // Rows enough to fill every CTA slot once (three to five per SM, five
+    // resident): one CTA per row in a single wave, no cluster merge, instead
+    // of about two waves of half rows whose per-CTA tails leave HBM idle.
+    if (p.cpr > 1 && rows >= 3L * sm_count() && rows <= 5L * sm_count()) {
+        const int seg1 = row_seg_elems(d.V, esize, 1);
+        const int nch1 = row_chunks(seg1, esize);
+        if (nch1 <= max_seg) {
+            p.cpr = 1;
+            p.seg = seg1;
+            p.nch = nch1;
+            p.stages = std::min(nch1, kExpandStages);
+            p.smem = nch1 <= 1 ? static_cast<int>(align_up(static_cast<size_t>(seg1) * esize, 128))
+                               : p.stages * kRowChunkBytes;
+            p.slots = nch1 * kConsumerWarps;
+        }
+    }
     // With enough rows to fill the SMs at four CTAs per row, four larger
     // resident segments beat eight small ones (fewer tails and cluster
     // members per row; 70B b8: 14.4 -> 13.0 us per step). Few rows keep eight.
@@ -1213,7 +1254,7 @@ cudaError_t launch_expand(const TreeDims& d, const TreeWs& ws, int step, const v
             p.slots = 4 * nch4 * kConsumerWarps;
         }
     }
-    if (p.nch > kMaxSegChunks) return cudaErrorInvalidValue;
+    if (p.nch > max_seg) return cudaErrorInvalidValue;
     dim3 grid(p.cpr, d.B * d.k, 1);
     TreeDims dd = d;
     TreeWs ww = ws;
