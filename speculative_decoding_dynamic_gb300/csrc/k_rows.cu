@@ -499,19 +499,23 @@ __global__ void __launch_bounds__(kRowThreads, 5) expand_kernel(TreeDims d, Tree
                 m_l = cm;
             }
             if (do_sum && m_l > -INFINITY) {
+                // even and odd elements summed apart, as packed fp32 pairs (one
+                // multiply-add and one add per two elements, each lane's result
+                // the scalar operation's)
                 const float mb = m_l * kLog2e;
-                float sa = 0.0f, sb = 0.0f;
+                const uint64_t l2 = f2_pack(kLog2e, kLog2e), nmb = f2_pack(-mb, -mb);
+                uint64_t sab = 0ull;  // (even sum, odd sum)
 #pragma unroll
                 for (int j = 0; j < kVecPerLane; ++j) {
                     float x[EPV];
                     unpack16<DT>(u[j], x);
 #pragma unroll
                     for (int e = 0; e < EPV; e += 2) {
-                        sa += ex2_approx(fmaf(x[e], kLog2e, -mb));
-                        sb += ex2_approx(fmaf(x[e + 1], kLog2e, -mb));
+                        const uint64_t z = f2_fma(f2_pack(x[e], x[e + 1]), l2, nmb);
+                        sab = f2_add(sab, f2_pack(ex2_approx(f2_lo(z)), ex2_approx(f2_hi(z))));
                     }
                 }
-                s_l += sa + sb;
+                s_l += f2_lo(sab) + f2_hi(sab);
             }
         }
         // tau: the warp's k-th largest lane maximum (0 bits: fewer than k lanes hold elements)
