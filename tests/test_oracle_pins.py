@@ -652,3 +652,71 @@ def test_lmhead_linear_and_order_free():
     Wz[9] = 0
     z = oracle.lmhead_logits(h, Wz)
     assert np.all(z[:, 9] == 0) and np.array_equal(np.delete(z, 9, 1), np.delete(base, 9, 1))
+
+
+# ------------------------------------- which verification rule is lossless ---
+# Exact enumeration on one node with two sampled children (no Monte Carlo):
+# children c1, c2 drawn from the draft distribution q without replacement
+# (sequential draws), first emitted token under three tree/verify choices.
+
+def _draws_without_replacement(q):
+    V = len(q)
+    for a in range(V):
+        for b in range(V):
+            if a != b:
+                yield a, b, q[a] * q[b] / (1.0 - q[a])
+
+
+def _residual(p, q):
+    r = np.maximum(p - q, 0.0)
+    return r / r.sum()
+
+
+def _draft_rule_tests(p, q, children):
+    """Emitted-token distribution of min(1, p/q) tests along `children` (the
+    draft distribution loses each rejected child; the target becomes the
+    residual), then a draw from the last residual."""
+    out = np.zeros_like(p)
+    stay = 1.0
+    p_cur, q_cur = p.copy(), q.copy()
+    for x in children:
+        acc = min(1.0, p_cur[x] / q_cur[x])
+        out[x] += stay * acc
+        stay *= 1.0 - acc
+        p_cur = _residual(p_cur, q_cur)
+        q_cur = q_cur.copy()
+        q_cur[x] = 0.0
+        q_cur /= q_cur.sum()
+    return out + stay * p_cur
+
+
+def _onehot_rule_tests(p, children):
+    """Emitted-token distribution of the built rule: accept x with p_cur(x),
+    on rejection remove x from the target and renormalise."""
+    out = np.zeros_like(p)
+    stay = 1.0
+    p_cur = p.copy()
+    for x in children:
+        out[x] += stay * p_cur[x]
+        stay *= 1.0 - p_cur[x]
+        p_cur = p_cur.copy()
+        p_cur[x] = 0.0
+        p_cur /= p_cur.sum()
+    return out + stay * p_cur
+
+
+def test_draft_rule_lossless_only_for_token_independent_shapes():
+    p = np.array([0.1, 0.45, 0.3, 0.15])
+    q = np.array([0.5, 0.2, 0.2, 0.1])
+    both = np.zeros(4)      # every sampled child tested, in sampling order
+    by_value = np.zeros(4)  # only the child of higher draft probability kept (a value-ranked budget of one)
+    onehot = np.zeros(4)    # the same value-ranked child under the built rule
+    for a, b, w in _draws_without_replacement(q):
+        keep = a if (q[a], -a) > (q[b], -b) else b
+        both += w * _draft_rule_tests(p, q, [a, b])
+        by_value += w * _draft_rule_tests(p, q, [keep])
+        onehot += w * _onehot_rule_tests(p, [keep])
+    assert np.allclose(both, p, atol=1e-12)
+    assert np.allclose(onehot, p, atol=1e-12)
+    # the draft-probability rule on a value-selected child is biased
+    assert np.abs(by_value - p).max() > 0.02
