@@ -720,3 +720,31 @@ def test_draft_rule_lossless_only_for_token_independent_shapes():
     assert np.allclose(onehot, p, atol=1e-12)
     # the draft-probability rule on a value-selected child is biased
     assert np.abs(by_value - p).max() > 0.02
+
+
+def test_lmhead_parity_bound_catches_planted_mistakes():
+    """The GPU parity bound for the LM head (H * 2^-23 * sum_h |h w| plus half a
+    bf16 ulp) is tight enough to flag the mistakes a tiled kernel could make:
+    a dropped 64-wide hidden block, a block counted twice, a neighbouring
+    vocabulary row, or operands read transposed. Mistakes are planted in
+    copies of the inputs fed to the oracle."""
+    M, V, Hd = 6, 300, 256
+    h, W = _lmhead_case(M, V, Hd, 13)
+    ref = oracle.lmhead_logits(h, W).astype(np.float64)
+    a = np.abs(synth.bf16_to_f32(h)).astype(np.float64)
+    b = np.abs(synth.bf16_to_f32(W)).astype(np.float64)
+    tol = Hd * 2.0 ** -23 * (a @ b.T)
+    tol = tol + 2.0 ** -8 * (np.abs(ref) + tol)
+
+    def flagged(got):
+        return bool(np.any(np.abs(got.astype(np.float64) - ref) > tol))
+
+    assert not flagged(ref)
+    dropped = h.copy()
+    dropped[:, 64:128] = 0
+    assert flagged(oracle.lmhead_logits(dropped, W))
+    twice = np.concatenate([h, h[:, 128:192]], axis=1)
+    assert flagged(oracle.lmhead_logits(twice, np.concatenate([W, W[:, 128:192]], axis=1)))
+    assert flagged(oracle.lmhead_logits(h, np.roll(W, 1, axis=0)))
+    Wt = np.ascontiguousarray(W.reshape(-1)[: V * Hd].reshape(Hd, V).T)  # the weight read as [H, V]
+    assert flagged(oracle.lmhead_logits(h, Wt))
