@@ -64,6 +64,8 @@ def _lmhead(E, cfg, ws, Hd, dh, dW):
     (1, 1, 136, 64, synth.F32),        # one row, one hidden block, 8-row last tile
     (64, 10, 4096, 128, synth.BF16),   # 640 rows: three chunks of 224 (the last one 192 live)
     (2, 16, 384, 1024, synth.BF16),    # 32 rows, 16 hidden blocks (the ring wraps)
+    (8, 8, 2056, 8192, synth.BF16),    # 70B shape: 64 rows, 128 hidden blocks
+    (1, 10, 32000, 5120, synth.BF16),  # 13B shape: 250 vocabulary tiles, 80 hidden blocks
 ])
 def test_lmhead_matches_oracle(B, k, V, Hd, dtype):
     E = _E()
