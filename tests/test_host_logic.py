@@ -1,0 +1,88 @@
+"""Host-side models of selection rules the CUDA kernels rely on (CPU only).
+
+The expansion kernel finds a row segment's top-k without ranking every
+element: it admits only the lane groups (32 elements) whose maximum reaches
+an admission key tau (the largest over warps of the warp's k-th largest lane
+maximum), and for bf16 rows it keeps just the top 16 order bits of each group
+maximum. This models that rule on the kernel's data layout and checks that
+the admitted keys always contain the exact top-k (value descending, equal
+values by lower id), on random rows, heavy ties, negative rows, -inf entries
+and a ragged tail. It does not run or import any CUDA code.
+"""
+import numpy as np
+import pytest
+
+import synth
+
+CHUNK = 8192          # bf16 elements per 16 KB chunk
+WARPS, J, LANES, E = 8, 4, 32, 8
+
+
+def _f2o(x):
+    b = x.astype(np.float32).view(np.uint32).copy()
+    b[(b & 0x7FFFFFFF) == 0] = 0
+    neg = (b & 0x80000000) != 0
+    return np.where(neg, ~b, b | 0x80000000).astype(np.uint32)
+
+
+def _keys(o, ids):
+    return (o.astype(np.uint64) << np.uint64(32)) | (np.uint64(0xFFFFFFFF) - ids.astype(np.uint64))
+
+
+def _admitted_topk(bits, k):
+    """The kernel's rule on one segment of bf16 bit patterns (uint16)."""
+    n = bits.size
+    nch = (n + CHUNK - 1) // CHUNK
+    x = np.full(nch * CHUNK, -np.inf, np.float32)
+    x[:n] = synth.bf16_to_f32(bits)
+    ids = np.arange(nch * CHUNK, dtype=np.int64)
+    real = ids < n
+    xv = x.reshape(nch, WARPS, J, LANES, E)
+    group_max = xv.max(axis=(2, 4))                          # [chunk, warp, lane]
+    first_vec = (np.arange(WARPS)[:, None] * (J * LANES) + np.arange(LANES)[None, :]) * E
+    has = (np.arange(nch)[:, None, None] * CHUNK + first_vec[None]) < n
+    gm_o = np.where(has, _f2o(group_max), 0).astype(np.uint32)
+    gm16 = (gm_o >> 16).astype(np.uint32)                   # bf16 rows keep 16 bits
+    lane_max = group_max.max(axis=0)                          # [warp, lane]
+    lane_has = has.any(axis=0)
+    lane_o = np.where(lane_has, _f2o(lane_max), 0).astype(np.uint32)
+    kth = np.sort(lane_o, axis=1)[:, ::-1][:, k - 1]           # warp's k-th largest lane maximum
+    tau = int(kth.max())
+    if tau == 0:
+        hot = gm16 != 0
+    else:
+        hot = (gm16 != 0) & ((gm16 << 16) >= (tau & 0xFFFF0000))
+    hot_el = np.broadcast_to(hot[:, :, None, :, None], xv.shape).reshape(-1)
+    keys = _keys(_f2o(x), ids)
+    ok = hot_el & real & ~np.isnan(x) & (keys >= (np.uint64(tau) << np.uint64(32)))
+    cand = np.sort(keys[ok])[::-1][:k]
+    return cand, int(ok.sum())
+
+
+def _true_topk(bits, k):
+    x = synth.bf16_to_f32(bits)
+    ids = np.arange(bits.size)
+    keys = _keys(_f2o(x), ids)
+    return np.sort(keys[~np.isnan(x)])[::-1][:k]
+
+
+def _bf16(a):
+    return (np.asarray(a, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("n", [16 * CHUNK, 128256, 9 * CHUNK + 1000])
+@pytest.mark.parametrize("k", [1, 10, 16])
+def test_admission_key_keeps_the_exact_topk(n, k):
+    rng = np.random.default_rng(n + k)
+    cases = [
+        _bf16(rng.normal(0, 2.5, n)),                            # the workloads' rows
+        _bf16(rng.integers(-3, 3, n).astype(np.float32)),        # six distinct values: ties everywhere
+        _bf16(-np.abs(rng.normal(0, 1, n)) - 1.0),               # every value negative
+        _bf16(np.where(rng.random(n) < 0.9, -np.inf, rng.normal(0, 1, n))),  # mostly -inf
+        _bf16(np.full(n, 0.5, np.float32)),                      # one value
+    ]
+    for bits in cases:
+        got, admitted = _admitted_topk(bits, k)
+        want = _true_topk(bits, k)
+        assert np.array_equal(got, want)
+        assert admitted >= min(k, int((~np.isnan(synth.bf16_to_f32(bits))).sum()))
