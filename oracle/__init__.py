@@ -51,6 +51,11 @@ def _load():
     lib.oracle_verify_lossless.argtypes = [i32, i32, i32, i32, i32, f32, p, p, p, p, p, p, p, p, p, p]
     lib.oracle_kv_compact.argtypes = [i32, i32, i32, i32, i32, p, i64, i64, i64, i64, p, p, p, i32, p]
     lib.oracle_lmhead_logits.argtypes = [i32, i32, i32, p, p, p]
+    lib.oracle_expand_sampled.argtypes = [i32, i32, i32, i32, i32, f32, i32, p, p, p, i32, p, p, p, p, p, p, p, p,
+                                          p, p, p]
+    lib.oracle_dlog.argtypes = [i32, p, p]
+    lib.oracle_gumbel.argtypes = [i32, p, p]
+    lib.oracle_verify_draft.argtypes = [i32, i32, i32, i32, i32, f32, p, p, p, p, p, p, p, p, p, p]
     _lib = lib
     return lib
 
@@ -142,8 +147,11 @@ class Tree:
         _load().oracle_tree_init(B, C, k, _p(self.token), _p(self.parent), _p(self.depth), _p(self.logv),
                                  _p(self.valid), _p(self.fnode), _p(self.fcount))
 
-    def expand(self, step: int, logits_s: np.ndarray, lse_in: np.ndarray | None = None):
-        """Stages 1+2 for step ``step``; logits_s is [B, k, V]. Returns (frontier tokens [B,k], count [B])."""
+    def expand(self, step: int, logits_s: np.ndarray, lse_in: np.ndarray | None = None,
+               words: np.ndarray | None = None):
+        """Stages 1+2 for step ``step``; logits_s is [B, k, V]. Returns (frontier tokens [B,k], count [B]).
+        words: optional uint32 [B, k, V]; the children are then drawn from the row's softmax
+        without replacement (Gumbel-top-k) instead of being its top-k."""
         cfg = self.cfg
         B, k, V = cfg.batch, cfg.top_k, cfg.vocab
         logits_s = np.ascontiguousarray(logits_s)
@@ -153,10 +161,19 @@ class Tree:
         lse_out = np.full((B, k), np.nan, np.float32)
         ftok = np.zeros((B, k), np.int32)
         fcnt = np.zeros(B, np.int32)
-        rc = _load().oracle_expand(B, V, k, step, _dtype_code(logits_s), log_threshold(cfg.threshold), cfg.policy,
-                                   _p(logits_s), _p(lse_in), cfg.C, _p(self.token), _p(self.parent),
-                                   _p(self.depth), _p(self.logv), _p(self.lp), _p(self.valid), _p(self.fnode),
-                                   _p(self.fcount), _p(lse_out), _p(ftok), _p(fcnt))
+        if words is None:
+            rc = _load().oracle_expand(B, V, k, step, _dtype_code(logits_s), log_threshold(cfg.threshold),
+                                       cfg.policy, _p(logits_s), _p(lse_in), cfg.C, _p(self.token), _p(self.parent),
+                                       _p(self.depth), _p(self.logv), _p(self.lp), _p(self.valid), _p(self.fnode),
+                                       _p(self.fcount), _p(lse_out), _p(ftok), _p(fcnt))
+        else:
+            words = np.ascontiguousarray(words, np.uint32)
+            assert words.shape == (B, k, V), words.shape
+            rc = _load().oracle_expand_sampled(B, V, k, step, _dtype_code(logits_s), log_threshold(cfg.threshold),
+                                               cfg.policy, _p(logits_s), _p(lse_in), _p(words), cfg.C,
+                                               _p(self.token), _p(self.parent), _p(self.depth), _p(self.logv),
+                                               _p(self.lp), _p(self.valid), _p(self.fnode), _p(self.fcount),
+                                               _p(lse_out), _p(ftok), _p(fcnt))
         if rc != 0:
             raise RuntimeError(f"oracle_expand failed: {rc}")
         self.fhist[step + 1] = self.fnode
@@ -187,6 +204,23 @@ class Tree:
                                        _p(out["pos"]), _p(out["mask"]), _p(out["n_tree"]), _p(out["slot_of"]))
         if rc != 0:
             raise RuntimeError(f"oracle_build_tree failed: {rc}")
+        return out
+
+    def draft_rows(self, slot_of: np.ndarray, n_tree: np.ndarray) -> np.ndarray:
+        """[B, T] int64: for each tree slot, the row of the draft logits [D, B, k, V]
+        (flattened to [D*B*k, V]) its children were drawn from, -1 if never expanded."""
+        cfg = self.cfg
+        B, T, k, D = cfg.batch, cfg.T, cfg.top_k, cfg.depth
+        out = np.full((B, T), -1, np.int64)
+        for b in range(B):
+            out[b, 0] = (0 * B + b) * k + 0  # the root: step 0, row 0
+            for st in range(1, D):
+                for f in range(k):
+                    nid = int(self.fhist[st, b, f])
+                    if nid >= 0 and self.kept[b, nid]:
+                        sl = int(slot_of[b, nid])
+                        if 0 <= sl < int(n_tree[b]):
+                            out[b, sl] = (st * B + b) * k + f
         return out
 
     def value_sum(self, b: int) -> float:
@@ -285,3 +319,43 @@ def lmhead_logits(hidden: np.ndarray, W: np.ndarray) -> np.ndarray:
     if rc != 0:
         raise RuntimeError(f"oracle_lmhead_logits failed: {rc}")
     return out
+
+
+def dlog(y: np.ndarray) -> np.ndarray:
+    """The oracle's fixed-order fp32 logarithm (positive normal inputs)."""
+    y = np.ascontiguousarray(y, np.float32)
+    out = np.empty_like(y)
+    _load().oracle_dlog(y.size, _p(y), _p(out))
+    return out
+
+
+def gumbel(words: np.ndarray) -> np.ndarray:
+    """Gumbel noise -ln(-ln u) of uint32 words (u = ((w >> 9) + 1/2) 2^-23), fp32."""
+    w = np.ascontiguousarray(words, np.uint32)
+    out = np.empty(w.shape, np.float32)
+    _load().oracle_gumbel(w.size, _p(w), _p(out))
+    return out
+
+
+def verify_draft(target: np.ndarray, draft: np.ndarray, draft_row: np.ndarray, tokens, parent, n_tree, uniforms,
+                 depth: int, inv_temp: float = 1.0):
+    """Stage 6 with the draft-probability rule (children drawn from the draft rows).
+    target [B,T,V]; draft [R,V] (same dtype); draft_row [B,T] int64. Returns (accept_len, slots, out_tokens)."""
+    B, T, V = target.shape
+    Dp1 = depth + 1
+    a = np.zeros(B, np.int32)
+    slots = np.zeros((B, Dp1), np.int32)
+    toks = np.zeros((B, Dp1), np.int32)
+    u = np.ascontiguousarray(uniforms, np.uint32)
+    assert u.shape == (B, T + 2)
+    draft = np.ascontiguousarray(draft)
+    assert draft.dtype == target.dtype and draft.shape[-1] == V
+    rc = _load().oracle_verify_draft(B, T, V, Dp1, _dtype_code(target), ctypes.c_float(inv_temp),
+                                     _p(np.ascontiguousarray(target)), _p(draft),
+                                     _p(np.ascontiguousarray(draft_row, np.int64)),
+                                     _p(np.ascontiguousarray(tokens, np.int32)),
+                                     _p(np.ascontiguousarray(parent, np.int32)),
+                                     _p(np.ascontiguousarray(n_tree, np.int32)), _p(u), _p(a), _p(slots), _p(toks))
+    if rc != 0:
+        raise RuntimeError(f"oracle_verify_draft failed: {rc}")
+    return a, slots, toks

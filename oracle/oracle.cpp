@@ -115,6 +115,71 @@ uint64_t fixed_mass(float x, float m, float inv_t) {
     return static_cast<uint64_t>(e * 1099511627776.0f);  // exact: power-of-two scale, then floor
 }
 
+// Fixed-order natural logarithm of a positive normal float, for the Gumbel
+// keys of sampled drafting; every step is one correctly rounded fp32
+// operation so that another implementation of the same steps reaches the
+// same bits (reading: a sampled child is an integer decided by floating
+// point, so both sides take it in the same precision). Written from the
+// mathematics: y = m 2^e with m in [sqrt(1/2), sqrt(2)) (exact bit
+// operations), s = (m - 1) / (m + 1), ln m = 2 atanh(s) = 2 s (1 + s^2/3 +
+// s^4/5 + s^6/7 + s^8/9 + s^10/11) in Horner form in s^2 by fused
+// multiply-adds (the next term is below 2^-33 relative for |s| <= 0.172),
+// then ln y = e ln2_hi + (e ln2_lo + ln m) with the 16-bit head of ln 2 used
+// by dexp (e ln2_hi exact).
+float dlog(float y) {
+    uint32_t b;
+    std::memcpy(&b, &y, 4);
+    int e = static_cast<int>((b >> 23) & 0xffu) - 127;
+    const uint32_t mb = (b & 0x7fffffu) | 0x3f800000u;
+    float m;
+    std::memcpy(&m, &mb, 4);
+    if (m > 1.41421353816986083984375f) {  // fp32 just below sqrt(2)
+        m = m * 0.5f;
+        e += 1;
+    }
+    const float s = (m - 1.0f) / (m + 1.0f);
+    const float z = s * s;
+    float p = 1.0f / 11.0f;
+    p = std::fmaf(p, z, 1.0f / 9.0f);
+    p = std::fmaf(p, z, 1.0f / 7.0f);
+    p = std::fmaf(p, z, 1.0f / 5.0f);
+    p = std::fmaf(p, z, 1.0f / 3.0f);
+    p = std::fmaf(p, z, 1.0f);
+    float t = s * p;
+    t = t + t;
+    const float ef = static_cast<float>(e);
+    return std::fmaf(ef, 0.693145751953125f, std::fmaf(ef, 1.42860677e-06f, t));
+}
+
+// Gumbel noise of a 32-bit uniform word: u = ((w >> 9) + 1/2) 2^-23, exact in
+// fp32 and strictly inside (0, 1); g = -ln(-ln u) by dlog.
+float gumbel_of_word(uint32_t w) {
+    const float u = (static_cast<float>(w >> 9) + 0.5f) * 0x1p-23f;
+    return -dlog(-dlog(u));
+}
+
+// The k children of one row drawn from q = softmax(row) without replacement,
+// in drawing order: the k largest keys fl(x + g(w_x)) (the Gumbel-top-k
+// identity: perturbing log-probabilities by independent Gumbel noise and
+// sorting gives sequential sampling without replacement); equal keys go to
+// the lower id. NaN entries are never drawn.
+void sampled_topk(const void* row, int dtype, int V, int k, const uint32_t* words, std::vector<int>* out) {
+    std::vector<std::pair<float, int>> keys;
+    keys.reserve(V);
+    for (int x = 0; x < V; ++x) {
+        const float v = load_logit(row, dtype, x);
+        if (v != v) continue;
+        keys.emplace_back(v + gumbel_of_word(words[x]), x);
+    }
+    const int kk = std::min<int>(k, static_cast<int>(keys.size()));
+    std::partial_sort(keys.begin(), keys.begin() + kk, keys.end(), [](const auto& a, const auto& c) {
+        if (a.first != c.first) return a.first > c.first;
+        return a.second < c.second;
+    });
+    out->clear();
+    for (int i = 0; i < kk; ++i) out->push_back(keys[i].second);
+}
+
 }  // namespace
 
 extern "C" {
@@ -188,10 +253,11 @@ void oracle_tree_init(int B, int C, int k, int32_t* cand_token, int32_t* cand_pa
 // child r of frontier slot f ranked by f + r ascending, then by lower node id
 // (reading: a fixed triangular pattern that favours the first children of
 // the first slots, as a hand-shaped tree does).
-int oracle_expand(int B, int V, int k, int step, int dtype, float log_thr, int policy, const void* logits_s,
-                  const float* lse_in, int C, int32_t* cand_token, int32_t* cand_parent,
-                  int32_t* cand_depth, float* cand_logv, float* cand_lp, uint8_t* cand_valid, int32_t* fnode,
-                  int32_t* fcount, float* row_lse_out, int32_t* ftok_out, int32_t* fcount_out) {
+static int expand_impl(int B, int V, int k, int step, int dtype, float log_thr, int policy, const void* logits_s,
+                       const float* lse_in, const uint32_t* words_s, int C, int32_t* cand_token,
+                       int32_t* cand_parent, int32_t* cand_depth, float* cand_logv, float* cand_lp,
+                       uint8_t* cand_valid, int32_t* fnode, int32_t* fcount, float* row_lse_out, int32_t* ftok_out,
+                       int32_t* fcount_out) {
     const int64_t base = step_base(step, k);
     for (int b = 0; b < B; ++b) {
         const int F = fcount[b];
@@ -203,6 +269,7 @@ int oracle_expand(int B, int V, int k, int step, int dtype, float log_thr, int p
             double lse64;
             std::vector<int> topk;
             row_stats(row, dtype, V, k, &lse64, &topk);
+            if (words_s) sampled_topk(row, dtype, V, k, words_s + row_off, &topk);
             float lse = lse_in ? lse_in[b * k + f] : static_cast<float>(lse64);
             if (row_lse_out) row_lse_out[b * k + f] = lse;
             const int parent = fnode[b * k + f];
@@ -256,6 +323,38 @@ int oracle_expand(int B, int V, int k, int step, int dtype, float log_thr, int p
         fcount[b] = nf;
         if (fcount_out) fcount_out[b] = nf;
     }
+    return 0;
+}
+
+int oracle_expand(int B, int V, int k, int step, int dtype, float log_thr, int policy, const void* logits_s,
+                  const float* lse_in, int C, int32_t* cand_token, int32_t* cand_parent,
+                  int32_t* cand_depth, float* cand_logv, float* cand_lp, uint8_t* cand_valid, int32_t* fnode,
+                  int32_t* fcount, float* row_lse_out, int32_t* ftok_out, int32_t* fcount_out) {
+    return expand_impl(B, V, k, step, dtype, log_thr, policy, logits_s, lse_in, nullptr, C, cand_token, cand_parent,
+                       cand_depth, cand_logv, cand_lp, cand_valid, fnode, fcount, row_lse_out, ftok_out, fcount_out);
+}
+
+// Sampled drafting (next row f4: children drawn from the draft distribution
+// instead of its top-k, so that the draft-probability acceptance rule can be
+// used; reading: Gumbel-top-k over per-element uniform words [B, k, V] of
+// the step, values and everything after the draw exactly as oracle_expand).
+int oracle_expand_sampled(int B, int V, int k, int step, int dtype, float log_thr, int policy,
+                          const void* logits_s, const float* lse_in, const uint32_t* words_s, int C,
+                          int32_t* cand_token, int32_t* cand_parent, int32_t* cand_depth, float* cand_logv,
+                          float* cand_lp, uint8_t* cand_valid, int32_t* fnode, int32_t* fcount, float* row_lse_out,
+                          int32_t* ftok_out, int32_t* fcount_out) {
+    if (!words_s) return -1;
+    return expand_impl(B, V, k, step, dtype, log_thr, policy, logits_s, lse_in, words_s, C, cand_token, cand_parent,
+                       cand_depth, cand_logv, cand_lp, cand_valid, fnode, fcount, row_lse_out, ftok_out, fcount_out);
+}
+
+int oracle_dlog(int n, const float* y, float* out) {
+    for (int i = 0; i < n; ++i) out[i] = dlog(y[i]);
+    return 0;
+}
+
+int oracle_gumbel(int n, const uint32_t* w, float* out) {
+    for (int i = 0; i < n; ++i) out[i] = gumbel_of_word(w[i]);
     return 0;
 }
 
@@ -595,6 +694,119 @@ int oracle_verify_lossless(int B, int T, int V, int Dp1, int dtype, float inv_t,
         }
         write_path(b, Dp1, static_cast<int>(path.size()) - 1, path.data(), tk, bonus, accept_len,
                    accepted_slots, out_tokens);
+    }
+    return 0;
+}
+
+// Verification with the draft-probability rule (next row f4) [EAGLE-2
+// summary 2.1: tokens accepted sequentially by the probability ratio]. At
+// node u with target p_cur and draft q_cur (the softmax of the row u's
+// children were drawn from, without replacement and in slot order), child x
+// is accepted with probability min(1, p_cur(x) / q_cur(x)); on rejection
+// p_cur becomes the residual max(0, p_cur - q_cur) renormalised and x leaves
+// q_cur (renormalised: the next child was drawn without it). The first
+// accepted child becomes the new node (p and q reset to its own rows); if
+// none is accepted, or u has no kept child, the bonus token is drawn from
+// p_cur. This is the target distribution exactly when the tested children
+// of every node are its drawn children in drawing order (a token-independent
+// tree shape); a tree kept by draft value is not (reading, pinned by exact
+// enumeration and by sampling in the tests).
+//
+// Integer arithmetic in the style of oracle_verify_lossless: P and Q are
+// fixed_mass integers (2^40 scale) of the target and draft rows, A the
+// current target residual with sum SA, Q with sum SQ. Child x (uniform word
+// u[b, c] of its slot c, U24 = u >> 8) is accepted iff
+// U24 * Q[x] * SA < 2^24 * A[x] * SQ. A rejection sets
+// r(y) = max(0, A[y] * SQ - Q[y] * SA) (the residual scaled by SA * SQ) and
+// A = floor(r / 2^s), s the smallest shift that brings max r to 2^40 or
+// below (A is kept when every r is 0); then SQ -= Q[x], Q[x] = 0. The bonus
+// draw is the lossless one on A: t = floor(U64 * SA / 2^64), the smallest y
+// whose running sum of A exceeds t.
+//   draft      [R, V] draft rows; draft_row [B, T] row of the slot's node
+//              (-1: never expanded, then the node has no kept child).
+int oracle_verify_draft(int B, int T, int V, int Dp1, int dtype, float inv_t, const void* target,
+                        const void* draft, const int64_t* draft_row, const int32_t* tokens, const int32_t* parent,
+                        const int32_t* n_tree, const uint32_t* uniforms, int32_t* accept_len,
+                        int32_t* accepted_slots, int32_t* out_tokens) {
+    typedef unsigned __int128 u128;
+    std::vector<uint64_t> A(V), Q(V);
+    std::vector<u128> r(V);
+    for (int b = 0; b < B; ++b) {
+        const int n = n_tree[b];
+        const int32_t* tk = tokens + static_cast<int64_t>(b) * T;
+        const int32_t* pa = parent + static_cast<int64_t>(b) * T;
+        const uint32_t* u = uniforms + static_cast<int64_t>(b) * (T + 2);
+        std::vector<int> path(1, 0);
+        int cur = 0;
+        int bonus = -1;
+        for (;;) {
+            const void* prow = row_ptr(target, dtype, static_cast<int64_t>(b) * T + cur, V);
+            float m = -INFINITY;
+            for (int x = 0; x < V; ++x) m = std::max(m, load_logit(prow, dtype, x));
+            uint64_t SA = 0;
+            for (int x = 0; x < V; ++x) {
+                A[x] = fixed_mass(load_logit(prow, dtype, x), m, inv_t);
+                SA += A[x];
+            }
+            const int64_t dr = draft_row[static_cast<int64_t>(b) * T + cur];
+            uint64_t SQ = 0;
+            if (dr >= 0) {
+                const void* qrow = row_ptr(draft, dtype, dr, V);
+                float mq = -INFINITY;
+                for (int x = 0; x < V; ++x) mq = std::max(mq, load_logit(qrow, dtype, x));
+                for (int x = 0; x < V; ++x) {
+                    Q[x] = fixed_mass(load_logit(qrow, dtype, x), mq, inv_t);
+                    SQ += Q[x];
+                }
+            }
+            int next = -1;
+            for (int c = 1; c < n && static_cast<int>(path.size()) < Dp1; ++c) {
+                if (pa[c] != cur) continue;
+                if (dr < 0) return -2;  // a kept child of a node that was never expanded
+                const int x = tk[c];
+                const u128 lhs = static_cast<u128>(static_cast<uint64_t>(u[c] >> 8) * Q[x]) * SA;
+                const u128 rhs = (static_cast<u128>(A[x]) * SQ) << 24;
+                if (lhs < rhs) {
+                    next = c;
+                    break;
+                }
+                u128 mx = 0;
+                for (int y = 0; y < V; ++y) {
+                    const u128 pa_ = static_cast<u128>(A[y]) * SQ, qa = static_cast<u128>(Q[y]) * SA;
+                    r[y] = pa_ > qa ? pa_ - qa : 0;
+                    mx = std::max(mx, r[y]);
+                }
+                if (mx > 0) {
+                    int sh = 0;
+                    while ((mx >> sh) > (static_cast<u128>(1) << 40)) ++sh;
+                    SA = 0;
+                    for (int y = 0; y < V; ++y) {
+                        A[y] = static_cast<uint64_t>(r[y] >> sh);
+                        SA += A[y];
+                    }
+                }
+                SQ -= Q[x];
+                Q[x] = 0;
+            }
+            if (next >= 0) {
+                path.push_back(next);
+                cur = next;
+                continue;
+            }
+            const uint64_t U64 = (static_cast<uint64_t>(u[T + 1]) << 32) | u[T];
+            const uint64_t t = static_cast<uint64_t>((static_cast<u128>(U64) * SA) >> 64);
+            uint64_t run = 0;
+            for (int y = 0; y < V; ++y) {
+                run += A[y];
+                if (run > t) {
+                    bonus = y;
+                    break;
+                }
+            }
+            break;
+        }
+        write_path(b, Dp1, static_cast<int>(path.size()) - 1, path.data(), tk, bonus, accept_len, accepted_slots,
+                   out_tokens);
     }
     return 0;
 }

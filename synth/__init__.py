@@ -22,6 +22,7 @@ _lib = None
 F32, BF16 = 0, 1
 STREAM_DRAFT, STREAM_TARGET, STREAM_Q, STREAM_K, STREAM_V, STREAM_SEQ, STREAM_VERIFY = 1, 2, 3, 4, 5, 6, 7
 STREAM_HIDDEN, STREAM_LMHEAD = 8, 9  # frontier hidden states, LM-head weights
+STREAM_GUMBEL = 10  # uniform words of sampled drafting
 
 
 def build(force: bool = False) -> str:

@@ -748,3 +748,119 @@ def test_lmhead_parity_bound_catches_planted_mistakes():
     assert flagged(oracle.lmhead_logits(h, np.roll(W, 1, axis=0)))
     Wt = np.ascontiguousarray(W.reshape(-1)[: V * Hd].reshape(Hd, V).T)  # the weight read as [H, V]
     assert flagged(oracle.lmhead_logits(h, Wt))
+
+
+# ------------------------------------------- sampled drafting (next row f4) ---
+
+def test_dlog_within_three_ulp_of_log():
+    rng = np.random.default_rng(0)
+    y = np.exp2(rng.uniform(-24, 12, 100000)).astype(np.float32)
+    near_one = (1 + rng.uniform(-0.01, 0.01, 50000)).astype(np.float32)
+    edges = np.float32([2.0, 0.5, 1 + 2 ** -23, 1 - 2 ** -24, 2 ** -24, 1.4142135, 1.4142137, 0.70710677, 4096.0])
+    y = np.concatenate([y, near_one, edges])
+    got = oracle.dlog(y).astype(np.float64)
+    ref = np.log(y.astype(np.float64))
+    ulp = np.spacing(np.abs(ref).astype(np.float32)).astype(np.float64)
+    assert np.all(np.abs(got - ref) <= 3 * ulp)
+    assert oracle.dlog(np.float32([1.0]))[0] == 0.0
+
+
+def test_gumbel_noise_quantiles():
+    # g = -ln(-ln u): P(g <= t) = exp(-exp(-t)); u is the word's top 23 bits + 1/2
+    w = np.arange(0, 1 << 32, 1 << 12, dtype=np.uint64).astype(np.uint32)  # 2^20 evenly spaced words
+    g = oracle.gumbel(w).astype(np.float64)
+    for t in (-1.5, -0.5, 0.0, 0.5, 1.0, 2.0, 4.0):
+        assert abs(np.mean(g <= t) - math.exp(-math.exp(-t))) < 1e-5
+    assert np.all(np.diff(g) >= 0)  # monotone in the word
+
+
+def _chi2_sf(counts, probs):
+    from scipy.stats import chi2
+    n = counts.sum()
+    exp = n * probs
+    stat = float(((counts - exp) ** 2 / exp).sum())
+    return chi2.sf(stat, len(probs) - 1)
+
+
+def test_gumbel_topk_draws_without_replacement():
+    """Children of a row drawn by the oracle's sampled expansion: the first is
+    distributed as q = softmax(row), the ordered pair as q(a) q(b) / (1 - q(a))."""
+    V, k, B = 5, 2, 60000
+    x = np.array([1.2, 0.3, -0.5, 0.9, -1.4], np.float32)
+    q = np.exp(x.astype(np.float64) - x.max())
+    q /= q.sum()
+    logits = np.ascontiguousarray(np.broadcast_to(x, (B, k, V)))
+    words = synth.words(B, k * V, 0, 31, synth.STREAM_GUMBEL).reshape(B, k, V)
+    t = oracle.Tree(oracle.TreeCfg(B, V, k, 1, k, 0.0, 0))
+    t.expand(0, logits, words=words)
+    first, second = t.token[:, 0], t.token[:, 1]
+    assert np.all(first != second)
+    assert _chi2_sf(np.bincount(first, minlength=V).astype(float), q) > 1e-4
+    pair = np.zeros((V, V))
+    np.add.at(pair, (first, second), 1.0)
+    probs = np.array([[q[a] * q[b] / (1 - q[a]) if a != b else 0.0 for b in range(V)] for a in range(V)])
+    m = probs > 0
+    assert _chi2_sf(pair[m], probs[m]) > 1e-4
+    # the values stay the unperturbed log-probabilities
+    lse = np.log(np.exp(x.astype(np.float64)).sum())
+    assert np.allclose(t.lp[:, 0], x[first] - lse, atol=1e-6)
+
+
+def _sampled_tree_first_tokens(policy, N, xp, xq, B, seed, draft_equals_target=False, both=False):
+    """One sampled-drafting cycle per sequence (k 2, depth 2, V 6) verified with
+    the draft-probability rule; returns (first emitted tokens, accept lengths)
+    (with both=True, all emitted tokens instead of the first)."""
+    V, k, D = xp.shape[-1], 2, 2
+    cfg = oracle.TreeCfg(B, V, k, D, N, 0.0, policy)
+    draft = np.empty((D, B, k, V), np.float32)
+    draft[0] = xq[0]
+    draft[1] = xq[1]
+    t = oracle.Tree(cfg)
+    for s in range(D):
+        w = synth.words(B, k * V, s, seed, synth.STREAM_GUMBEL).reshape(B, k, V)
+        t.expand(s, np.ascontiguousarray(draft[s]), words=w)
+    t.rerank()
+    tr = t.build_tree(np.zeros(B, np.int32), np.zeros(B, np.int32))
+    T = cfg.T
+    target = np.empty((B, T, V), np.float32)
+    target[:, 0] = xp[0]
+    target[:, 1:] = xp[1]
+    rows = t.draft_rows(tr["slot_of"], tr["n_tree"])
+    uni = synth.words(B, T + 2, 0, seed, synth.STREAM_VERIFY)
+    if draft_equals_target:  # every node's draft row is its own target row
+        flat = np.empty((D * B * k, V), np.float32)
+        flat[:] = xp[1]
+        flat[rows[:, 0]] = xp[0]
+    else:
+        flat = draft.reshape(D * B * k, V)
+    a, _, toks = oracle.verify_draft(target, flat, rows, tr["tokens"], tr["parent"], tr["n_tree"], uni, D)
+    return (toks if both else toks[:, 0]), a
+
+
+XP = np.array([[0.2, 1.5, 1.1, 0.4, -0.3, 0.9], [0.5, -0.2, 1.0, 0.1, 0.7, -1.0]], np.float32)
+XQ = np.array([[1.4, 0.2, 0.9, 1.0, -0.8, 0.3], [-0.4, 0.6, 0.8, 1.1, 0.0, 0.2]], np.float32)
+
+
+def _softmax64(x):
+    e = np.exp(x.astype(np.float64) - x.max())
+    return e / e.sum()
+
+
+def test_draft_rule_with_drawn_children_is_lossless_on_a_static_tree():
+    toks, a = _sampled_tree_first_tokens(3, 6, XP, XQ, B=40000, seed=5, both=True)
+    assert _chi2_sf(np.bincount(toks[:, 0], minlength=6).astype(float), _softmax64(XP[0])) > 1e-4
+    # after an accepted first-level child, the next token follows that child's target row
+    moved = a >= 1
+    assert 0.2 < moved.mean() < 0.95  # both accepts and rejections are exercised
+    assert _chi2_sf(np.bincount(toks[moved, 1], minlength=6).astype(float), _softmax64(XP[1])) > 1e-4
+
+
+def test_draft_rule_on_a_value_ranked_tree_is_biased():
+    # budget 1: the rerank keeps the drawn first-level child of higher draft value
+    first, _ = _sampled_tree_first_tokens(0, 1, XP, XQ, B=40000, seed=6)
+    assert _chi2_sf(np.bincount(first, minlength=6).astype(float), _softmax64(XP[0])) < 1e-9
+
+
+def test_draft_rule_accepts_every_first_child_when_draft_equals_target():
+    _, a = _sampled_tree_first_tokens(3, 6, XP, XQ, B=2000, seed=7, draft_equals_target=True)
+    assert np.all(a == 2)
