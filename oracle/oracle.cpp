@@ -24,9 +24,11 @@
 //
 // Parity status of each function (what pins it is in the CPU test-suite):
 //   row_stats, expand, rerank, build_tree, attention, verify_greedy,
-//   verify_lossless, kv_compact, dexp, value_sum, lmhead_logits: pinned
-//   (closed forms, library routines, brute force, the tutorial's worked
-//   chain, one-hot rows and a float64 matmul for the LM head).
+//   verify_lossless, kv_compact, dexp, value_sum, lmhead_logits,
+//   expand_sampled, dlog, gumbel, verify_draft: pinned (closed forms, library
+//   routines, brute force, the tutorial's worked chain, one-hot rows and a
+//   float64 matmul for the LM head, chi-square against the sampling and
+//   target distributions for sampled drafting).
 
 #include <algorithm>
 #include <cmath>
