@@ -86,3 +86,16 @@ def test_admission_key_keeps_the_exact_topk(n, k):
         want = _true_topk(bits, k)
         assert np.array_equal(got, want)
         assert admitted >= min(k, int((~np.isnan(synth.bf16_to_f32(bits))).sum()))
+
+
+def test_input_generator_philox_known_answers():
+    """The seeded input generator's Philox4x32-10 against the known-answer
+    vectors published with the Random123 library (counter, key -> output)."""
+    kat = [
+        ([0, 0, 0, 0], [0, 0], [0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8]),
+        ([0xFFFFFFFF] * 4, [0xFFFFFFFF] * 2, [0x408F276D, 0x41C83B0E, 0xA20BC7C6, 0x6D5451FD]),
+        ([0x243F6A88, 0x85A308D3, 0x13198A2E, 0x03707344], [0xA4093822, 0x299F31D0],
+         [0xD16CFE09, 0x94FDCCEB, 0x5001E420, 0x24126EA1]),
+    ]
+    for ctr, key, out in kat:
+        assert list(synth.philox(ctr, key)) == out
