@@ -20,6 +20,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import re
 import os
 import subprocess
 import sys
@@ -169,11 +170,21 @@ def stop_clocks(h) -> dict | None:
 
 
 def kernel_src_hash() -> str:
+    """Hash of the sources the library is compiled from: every .cu file of csrc
+    and the csrc headers they include (transitively), in name order."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_dynamic_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    todo = [f for f in os.listdir(csrc) if f.endswith(".cu")]
+    used = set()
+    while todo:
+        f = todo.pop()
+        if f in used or not os.path.exists(os.path.join(csrc, f)):
+            continue
+        used.add(f)
+        for inc in re.findall(r'^\s*#\s*include\s+"([^"/]+)"', open(os.path.join(csrc, f)).read(), re.M):
+            todo.append(inc)
+    for f in sorted(used):
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 

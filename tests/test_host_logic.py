@@ -99,3 +99,59 @@ def test_input_generator_philox_known_answers():
     ]
     for ctr, key, out in kat:
         assert list(synth.philox(ctr, key)) == out
+
+
+# Device arithmetic of sampled drafting, compiled for the host from the same
+# header (every operation an explicit round-to-nearest step, so the host twin
+# reaches the device's bits): bit-exact against the oracle's own logarithm and
+# Gumbel noise, and against the input generator's Philox.
+
+_SHIM = r"""
+#include "sampling.cuh"
+extern "C" void t_log(int n, const float* y, float* o) { for (int i = 0; i < n; ++i) o[i] = eagle::sampling::fixed_log(y[i]); }
+extern "C" void t_gumbel(int n, const unsigned* w, float* o) { for (int i = 0; i < n; ++i) o[i] = eagle::sampling::gumbel_of_word(w[i]); }
+extern "C" void t_philox(const unsigned* c, const unsigned* k, unsigned* o) { eagle::sampling::philox4x32_10(c, k[0], k[1], o); }
+"""
+
+
+@pytest.fixture(scope="module")
+def sampling_host(tmp_path_factory):
+    import ctypes
+    import os
+    import subprocess
+    d = tmp_path_factory.mktemp("sampling")
+    src = d / "shim.cpp"
+    src.write_text(_SHIM)
+    csrc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                        "speculative_decoding_dynamic_gb300", "csrc")
+    lib = d / "shim.so"
+    subprocess.run(["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fPIC", "-shared", "-I", csrc, str(src), "-o",
+                    str(lib)], check=True)
+    return ctypes.CDLL(str(lib))
+
+
+def test_sampling_arithmetic_matches_the_oracle_bit_for_bit(sampling_host):
+    import ctypes
+    import oracle
+    rng = np.random.default_rng(3)
+    y = np.concatenate([np.exp2(rng.uniform(-24, 12, 50000)), 1 + rng.uniform(-0.01, 0.01, 20000)]).astype(np.float32)
+    got = np.empty_like(y)
+    sampling_host.t_log(y.size, y.ctypes.data_as(ctypes.c_void_p), got.ctypes.data_as(ctypes.c_void_p))
+    assert np.array_equal(got.view(np.uint32), oracle.dlog(y).view(np.uint32))
+    w = synth.words(1, 100000, 0, 9, synth.STREAM_GUMBEL).reshape(-1)
+    w = np.concatenate([w, np.uint32([0, 1, 511, 512, 0xFFFFFFFF, 0x80000000])])
+    g = np.empty(w.size, np.float32)
+    sampling_host.t_gumbel(w.size, w.ctypes.data_as(ctypes.c_void_p), g.ctypes.data_as(ctypes.c_void_p))
+    assert np.array_equal(g.view(np.uint32), oracle.gumbel(w).view(np.uint32))
+
+
+def test_sampling_philox_matches_the_input_generator(sampling_host):
+    import ctypes
+    rng = np.random.default_rng(4)
+    for _ in range(200):
+        c = rng.integers(0, 1 << 32, 4, dtype=np.uint64).astype(np.uint32)
+        k = rng.integers(0, 1 << 32, 2, dtype=np.uint64).astype(np.uint32)
+        o = np.zeros(4, np.uint32)
+        sampling_host.t_philox(c.ctypes.data_as(ctypes.c_void_p), k.ctypes.data_as(ctypes.c_void_p),
+                               o.ctypes.data_as(ctypes.c_void_p))
+        assert np.array_equal(o, synth.philox(c, k))
