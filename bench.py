@@ -169,28 +169,45 @@ def stop_clocks(h) -> dict | None:
             "samples": len(sm)}
 
 
-def kernel_src_hash() -> str:
-    """Hash of the sources the library is compiled from: every .cu file of csrc
-    and the csrc headers they include (transitively), in name order."""
+CSRC = os.path.join(ROOT, "speculative_decoding_dynamic_gb300", "csrc")
+# translation unit of each profiled kernel
+KERNEL_TU = {"expand_kernel": "k_rows.cu", "verify_kernel": "k_rows.cu", "attention": "k_attn_tc.cu",
+             "lmhead_kernel": "k_lmhead.cu"}
+
+
+def _src_hash(roots) -> str:
+    """Hash of the csrc files `roots` and the csrc headers they include
+    (transitively), in name order."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "speculative_decoding_dynamic_gb300", "csrc")
-    todo = [f for f in os.listdir(csrc) if f.endswith(".cu")]
+    todo = list(roots)
     used = set()
     while todo:
         f = todo.pop()
-        if f in used or not os.path.exists(os.path.join(csrc, f)):
+        if f in used or not os.path.exists(os.path.join(CSRC, f)):
             continue
         used.add(f)
-        for inc in re.findall(r'^\s*#\s*include\s+"([^"/]+)"', open(os.path.join(csrc, f)).read(), re.M):
+        for inc in re.findall(r'^\s*#\s*include\s+"([^"/]+)"', open(os.path.join(CSRC, f)).read(), re.M):
             todo.append(inc)
     for f in sorted(used):
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        h.update(open(os.path.join(CSRC, f), "rb").read())
     return h.hexdigest()[:16]
+
+
+def kernel_src_hash() -> str:
+    """Hash of the sources the library is compiled from: every .cu file of csrc
+    and the headers they include."""
+    return _src_hash(f for f in os.listdir(CSRC) if f.endswith(".cu"))
+
+
+def tu_src_hash(kernel: str) -> str:
+    """Hash of the sources one profiled kernel is compiled from (its .cu file
+    and the headers it includes)."""
+    return _src_hash([KERNEL_TU[kernel]])
 
 
 def ncu_traffic(kernel: str, workload_name: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was
-    taken on the current kernel sources; else None."""
+    taken on the current sources of that kernel's translation unit; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -199,7 +216,7 @@ def ncu_traffic(kernel: str, workload_name: str):
     except Exception:
         return None
     e = d.get(workload_name, {}).get(kernel)
-    if not e or e.get("src_hash") != kernel_src_hash():
+    if not e or kernel not in KERNEL_TU or e.get("src_hash") != tu_src_hash(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 
