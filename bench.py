@@ -4,11 +4,18 @@
 One step = one whole cycle over one batch: tree init, D expand steps, rerank,
 tree emission, tree attention (one layer), verification and KV compaction of
 every layer, all in libeagle's kernels. Inputs (draft and target logits, Q,
-KV cache) are synthetic and resident in HBM before the timed region; R input
+KV cache) are synthetic and resident in HBM before the timed region; input
 sets larger than L2 in total are rotated between steps. The cycle of each set
 is captured once in a CUDA graph and replayed.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+The JSON line's headline is the Llama-3.1-8B batch-1 cycle (lossless). The
+same run then measures, with the same K and W, the other configurations of
+the workload table (8B batch 64 greedy, with and without aligned targets,
+70B batch 8 lossless, 13B batch 1 lossless, 8B batch 1 greedy) into the
+line's `configs` block (skip with --no-configs). The oracle is timed on the
+host cores: one core, and one process per core on independent cycles.
 
 Under torchrun (N > 1) every rank runs its own replica on its own GPU (the
 sequences of a batch are independent: no collective on the data path);
@@ -20,8 +27,9 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
-import re
 import os
+import platform
+import re
 import subprocess
 import sys
 import tempfile
@@ -36,8 +44,17 @@ L2_BYTES = 129 * 1024 * 1024
 METRIC = "draft-verify cycles/s at Llama-8B shape; HBM GB/s & % roofline per kernel"
 POLICIES = {"dynamic": 0, "confidence": 1, "no_rerank": 2, "static": 3}
 
+# The configurations measured beside the headline: (label, workload, overrides, variant flags).
+EXTRA_CONFIGS = [
+    ("llama8b_b64_greedy", "llama8b_b64", {}, {}),
+    ("llama8b_b64_greedy_aligned", "llama8b_b64", {}, {"aligned": True}),
+    ("llama70b_b8_lossless", "llama70b_b8", {}, {}),
+    ("vicuna13b_b1_lossless", "vicuna13b_b1", {}, {}),
+    ("llama8b_b1_greedy", "llama8b_b1", {"verify": "greedy"}, {}),
+]
 
-def parse():
+
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
@@ -53,14 +70,16 @@ def parse():
     ap.add_argument("--seed", type=int, default=42)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="measure the headline workload only")
+    ap.add_argument("--cpu-seconds", type=float, default=8.0, help="oracle time per CPU-baseline leg")
     ap.add_argument("--kernel-reps", type=int, default=100)
     ap.add_argument("--layers", type=int, default=None, help="KV layers moved by compaction (memory cap)")
     ap.add_argument("--lmhead", action="store_true",
                     help="each draft step's rows come from the LM head (bf16 tensor-core GEMM of synthetic hidden "
                          "states against a resident random [V, H] weight)")
     ap.add_argument("--policy", default="dynamic", choices=list(POLICIES),
-                    help="tree policy: EAGLE-2, confidence-ranked frontier, or no rerank (ablations)")
-    return ap.parse_args()
+                    help="tree policy: EAGLE-2, confidence-ranked frontier, no rerank or static shape (ablations)")
+    return ap.parse_args(argv)
 
 
 # ------------------------------------------------------------- helpers ---
@@ -81,6 +100,7 @@ def align_targets(target: np.ndarray, tokens: np.ndarray, parent: np.ndarray, n_
                 first[p] = c
         for t, c in first.items():
             target[b, t, int(tokens[b, c])] = bits
+
 
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
@@ -138,6 +158,20 @@ def start_clocks(idx: int):
         return None, None, path
 
 
+def wait_first_sample(h, timeout_s: float = 3.0) -> None:
+    """Block until the clock sampler has written its first line (its start-up
+    takes longer than a short timed region)."""
+    p, f, path = h
+    if p is None:
+        return
+    t0 = time.time()
+    while time.time() - t0 < timeout_s:
+        f.flush()
+        if os.path.getsize(path) > 0:
+            return
+        time.sleep(0.02)
+
+
 def stop_clocks(h) -> dict | None:
     p, f, path = h
     if p is None:
@@ -172,12 +206,25 @@ def stop_clocks(h) -> dict | None:
 CSRC = os.path.join(ROOT, "speculative_decoding_dynamic_gb300", "csrc")
 # translation unit of each profiled kernel
 KERNEL_TU = {"expand_kernel": "k_rows.cu", "verify_kernel": "k_rows.cu", "attention": "k_attn_tc.cu",
-             "lmhead_kernel": "k_lmhead.cu"}
+             "lmhead_kernel": "k_lmhead.cu", "kv_compact_kernel": "k_compact.cu"}
+
+
+def _toolchain_id() -> bytes:
+    """The compile flags of the library build and the nvcc release: a change of
+    either changes the generated code."""
+    from speculative_decoding_dynamic_gb300 import build as Bld
+    try:
+        ver = subprocess.run([Bld._nvcc(), "--version"], capture_output=True, text=True).stdout
+        ver = " ".join(re.findall(r"release [0-9.]+, V[0-9.]+", ver))
+    except Exception:
+        ver = "unknown"
+    flags = [f for f in Bld.NVCC_FLAGS if not os.path.isabs(f)]
+    return (" ".join(Bld.ARCH + flags) + " | " + ver).encode()
 
 
 def _src_hash(roots) -> str:
-    """Hash of the csrc files `roots` and the csrc headers they include
-    (transitively), in name order."""
+    """Hash of the csrc files `roots`, the csrc headers they include
+    (transitively, in name order) and the toolchain (flags, nvcc release)."""
     h = hashlib.sha256()
     todo = list(roots)
     used = set()
@@ -190,18 +237,19 @@ def _src_hash(roots) -> str:
             todo.append(inc)
     for f in sorted(used):
         h.update(open(os.path.join(CSRC, f), "rb").read())
+    h.update(_toolchain_id())
     return h.hexdigest()[:16]
 
 
 def kernel_src_hash() -> str:
     """Hash of the sources the library is compiled from: every .cu file of csrc
-    and the headers they include."""
+    and the headers they include, with the toolchain."""
     return _src_hash(f for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
 def tu_src_hash(kernel: str) -> str:
     """Hash of the sources one profiled kernel is compiled from (its .cu file
-    and the headers it includes)."""
+    and the headers it includes, with the toolchain)."""
     return _src_hash([KERNEL_TU[kernel]])
 
 
@@ -221,18 +269,32 @@ def ncu_traffic(kernel: str, workload_name: str):
     return e.get("dram_bytes_per_launch")
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        m = re.search(r"^Model name:\s*(.+)$", out, re.M)
+        if m:
+            return m.group(1).strip()
+    except Exception:
+        pass
+    try:
+        m = re.search(r"^model name\s*:\s*(.+)$", open("/proc/cpuinfo").read(), re.M)
+        if m:
+            return m.group(1).strip()
+    except Exception:
+        pass
+    return platform.processor() or platform.machine()
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
 # ------------------------------------------------------------ the cycle ---
-
-def build_sets(args, w, R):
-    """Host inputs of R cycles (set r uses attention layer r and uniforms of cycle r)."""
-    from synth import workloads as WL
-    sets = []
-    for r in range(R):
-        seed = args.seed + 1000 * r
-        sets.append(dict(draft=WL.draft_logits(w, seed, planted=args.planted), target=WL.target_logits(w, seed),
-                         q=WL.queries(w, seed), uniforms=WL.uniforms(w, seed, r), layer=r))
-    return sets
-
 
 def to_dev(a):
     import torch
@@ -256,6 +318,28 @@ def pinned(a):
     return t.pin_memory()
 
 
+def rotation_sets(w, seed: int, sets: int = 0) -> tuple[int, int, int]:
+    """(R, bytes per set, attention bytes per set): enough rotating input sets that
+    one pass over them exceeds 1.5x L2 (one set when a single set already does)."""
+    per_set = (w.depth * w.batch * w.top_k + w.batch * w.T) * w.vocab * w.esize
+    attn_bytes = int(sum(int(L) + w.T for L in w.prefix_lengths(seed))) * w.n_kv_heads * w.head_dim * 2 * w.esize
+    R = sets or max(1, int(np.ceil(1.5 * L2_BYTES / (per_set + attn_bytes))))
+    return min(R, w.layers), per_set, attn_bytes
+
+
+def config_of(w, args, variant: dict, R: int, per_set: int, attn_bytes: int) -> dict:
+    """The workload description printed by both arms."""
+    return {"workload": w.name, "batch": w.batch, "vocab": w.vocab, "depth": w.depth, "top_k": w.top_k,
+            "node_budget": w.node_budget, "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads,
+            "head_dim": w.head_dim, "prefix": list(w.prefix) if isinstance(w.prefix, tuple) else w.prefix,
+            "sharpness": list(w.sharpness) if isinstance(w.sharpness, tuple) else w.sharpness,
+            "verify": w.verify, "compact_layers": w.layers, "planted": bool(variant.get("planted", False)),
+            "aligned": bool(variant.get("aligned", False)), "policy": args.policy, "lmhead": args.lmhead,
+            "hidden_size": w.hidden_size if args.lmhead else None,
+            "l2": f"{R} rotating input set(s), {round(R * (per_set + attn_bytes) / 2**20)} MiB > 129 MB L2",
+            "graph": "one CUDA graph per input set, replayed"}
+
+
 def algorithmic_bytes(w, prefix_len, accept_len, layers):
     """Bytes each stage must move per cycle (reads + writes of its operands)."""
     es = w.esize
@@ -270,6 +354,8 @@ def algorithmic_bytes(w, prefix_len, accept_len, layers):
     compact = int(2 * sum(int(a) for a in accept_len) * layers * 2 * w.n_kv_heads * w.head_dim * es)
     return dict(expand=expand, expand_step=expand_step, verify=verify, attention=attention, compact=compact)
 
+
+# ------------------------------------------------------------ the oracle ---
 
 def oracle_cycle(w, s, prefix_len, root, kh, vh, geo, mode, tree_region, head_stride=1, policy=0):
     """One whole cycle in the CPU oracle (the bench's CPU baseline / reference arm).
@@ -339,88 +425,128 @@ def host_tree_region(w, geo, prefix_len, seed, layers):
     return out
 
 
-def run_reference(args, w):
-    """The oracle as it stands, timed on the host cores: the bench's reference arm.
+class OracleInputs:
+    """Host inputs of one oracle cycle of a workload (input set `set_index` of `seed`)."""
 
-    Each step is one oracle cycle of the workload; when K + W full cycles would
-    take more than ~150 s, tree attention (the dominant stage) is sampled on
-    every m-th query head and its time scaled by m."""
+    def __init__(self, w, seed: int, set_index: int = 0, planted: bool = False):
+        from synth import workloads as WL
+        sd = seed + 1000 * set_index
+        self.w = w
+        self.s = dict(draft=WL.draft_logits(w, sd, planted=planted), target=WL.target_logits(w, sd),
+                      q=WL.queries(w, sd), uniforms=WL.uniforms(w, sd, set_index))
+        self.prefix_len = w.prefix_lengths(seed)
+        self.root = WL.root_tokens(w, seed)
+        self.geo = WL.kv_geometry(w, seed, w.layers)
+        self.kh, self.vh = host_attention_layer(w, self.geo, self.prefix_len, seed, 0)
+        self.region = host_tree_region(w, self.geo, self.prefix_len, seed, w.layers)
+
+    def cycle(self, head_stride=1, policy=0) -> float:
+        return oracle_cycle(self.w, self.s, self.prefix_len, self.root, self.kh, self.vh, self.geo, self.w.verify,
+                            self.region, head_stride=head_stride, policy=policy)
+
+
+def _oracle_worker_init():
+    # one core per process: the input generator's OpenMP loops stay single-threaded
+    os.environ["OMP_NUM_THREADS"] = "1"
+
+
+def _oracle_worker(job):
+    """One process of the all-cores CPU baseline: builds its own input set, waits
+    for the common start time, then runs oracle cycles for `seconds` (or exactly
+    `cycles` when given). Returns (cycles run, wall seconds, summed cycle estimates)."""
+    name, kw, seed, set_index, policy, head_stride, seconds, cycles, start_at = job
     from synth import workloads as WL
+    w = WL.WORKLOADS[name].with_(**kw)
+    inp = OracleInputs(w, seed, set_index)
+    inp.cycle(head_stride, policy)  # warm (first touch of the inputs, library load)
+    while time.time() < start_at:
+        time.sleep(0.005)
+    t0 = time.perf_counter()
+    n, est = 0, 0.0
+    while (cycles and n < cycles) or (not cycles and (n < 1 or time.perf_counter() - t0 < seconds)):
+        est += inp.cycle(head_stride, policy)
+        n += 1
+    return n, time.perf_counter() - t0, est
+
+
+class OraclePool:
+    """One spawned process per host core, for the oracle on all cores (started
+    with `spawn` so that it is independent of any CUDA state of this process)."""
+
+    def __init__(self, n: int):
+        import multiprocessing as mp
+        self.n = n
+        self.pool = mp.get_context("spawn").Pool(n, initializer=_oracle_worker_init)
+
+    def run(self, w, seed, policy, head_stride=1, seconds=8.0, cycles=0, lead=None):
+        """All processes run independent cycles (input set i in process i) from a
+        common start; returns (total cycles, wall seconds of the slowest, estimates)."""
+        kw = {k: getattr(w, k) for k in ("sharpness", "verify", "layers", "prefix", "batch")}
+        if lead is None:  # input generation and one warm cycle before the common start
+            lead = 15.0 + 3e-8 * (w.depth * w.top_k + w.T) * w.batch * w.vocab
+        start_at = time.time() + lead
+        jobs = [(w.name, kw, seed, i, policy, head_stride, seconds, cycles, start_at) for i in range(self.n)]
+        res = self.pool.map(_oracle_worker, jobs, chunksize=1)
+        return sum(r[0] for r in res), max(r[1] for r in res), sum(r[2] for r in res)
+
+    def close(self):
+        self.pool.terminate()
+        self.pool.join()
+
+
+def cpu_baseline(w, args, seed, pool, lmhead_extra=None):
+    """The oracle as it stands on the host: one core (in this process), and
+    every core (one process per core, independent cycles)."""
     import oracle
     oracle.build()
-    seed = args.seed
-    s = build_sets(args, w, 1)[0]
-    prefix_len = w.prefix_lengths(seed)
-    root = WL.root_tokens(w, seed)
-    geo = WL.kv_geometry(w, seed, w.layers)
-    kh, vh = host_attention_layer(w, geo, prefix_len, seed, 0)
-    region = host_tree_region(w, geo, prefix_len, seed, w.layers)
-    probe = oracle_cycle(w, s, prefix_len, root, kh, vh, geo, w.verify, region, head_stride=w.n_q_heads,
-                         policy=POLICIES[args.policy])
-    full_est = probe  # with one head per group measured and scaled: an estimate of a full cycle
-    m = 1
-    while m < w.n_q_heads and (args.steps + args.warmup) * full_est / m > 150.0:
-        m *= 2
-    while w.n_q_heads % m:
-        m //= 2
-    for _ in range(args.warmup):
-        oracle_cycle(w, s, prefix_len, root, kh, vh, geo, w.verify, region, head_stride=m,
-                     policy=POLICIES[args.policy])
-    tot = 0.0
-    for _ in range(args.steps):
-        tot += oracle_cycle(w, s, prefix_len, root, kh, vh, geo, w.verify, region, head_stride=m,
-                            policy=POLICIES[args.policy])
-    v = args.steps / tot
-    unit = "cycles/s"
-    sample = (f"{args.steps} oracle cycles of {w.name}: every stage in full"
-              + ("" if m == 1 else f" except tree attention on every {m}-th query head, its time scaled by {m}")
-              + f"; one host core")
-    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": unit, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic",
-            "config": {"workload": w.name, "batch": w.batch, "vocab": w.vocab, "depth": w.depth,
-                       "top_k": w.top_k, "node_budget": w.node_budget, "verify": w.verify,
-                       "policy": args.policy, "sharpness": w.sharpness if not isinstance(w.sharpness, tuple) else list(w.sharpness)},
-            "cpu_baseline": {"value": v, "unit": unit, "cores": 1, "kind": "oracle", "sample": sample},
-            "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(line), flush=True)
+    inp = OracleInputs(w, seed, 0, planted=args.planted)
+    n, tot = 0, 0.0
+    t0 = time.perf_counter()
+    while n < 1 or (time.perf_counter() - t0 < args.cpu_seconds and n < 50):
+        tot += inp.cycle(policy=POLICIES[args.policy])
+        n += 1
+    per_cycle = tot / n
+    extra = lmhead_extra(inp) if lmhead_extra else (0.0, "")
+    single = {"value": round(1.0 / (per_cycle + extra[0]), 6), "unit": "cycles/s", "cores": 1,
+              "sample": f"{n} whole oracle cycles of {w.name} (every stage, all attention rows) on one core"
+                        + extra[1]}
+    out = dict(single, kind="oracle", cpu_model=cpu_model(), host_cores=host_cores(), single_core=single)
+    if pool is not None and pool.n > 1:
+        cyc, wall, _ = pool.run(w, seed, POLICIES[args.policy], seconds=args.cpu_seconds)
+        v = cyc / wall
+        if extra[0] > 0:  # the LM head leg is timed on one core and scaled: add it per cycle
+            v = 1.0 / (1.0 / v + extra[0] / pool.n)
+        out.update({"value": round(v, 6), "cores": pool.n,
+                    "sample": f"{cyc} whole oracle cycles of {w.name} (every stage, all attention rows) in "
+                              f"{wall:.1f} s, one process per core ({pool.n} processes), independent input sets"
+                              + extra[1]})
+    return out
 
 
-def main():
-    args = parse()
-    ws_, rank, local = dist_env()
-    w = workload(args)
-    if args.impl == "reference":
-        if rank == 0:
-            run_reference(args, w)
-        return
+# ------------------------------------------------------------ our arm ---
 
+def run_workload(args, w, variant: dict, seed: int, ws_: int, rank: int, local: int, with_e2e: bool,
+                 fill_all_regions: bool = True) -> dict:
+    """Measure one configuration: returns the fields of a bench line (no CPU baseline).
+
+    fill_all_regions: write generator values into every layer's tree region
+    (else only the attention layers are generated; the other layers' regions,
+    which only compaction touches, stay zero: the same bytes are moved)."""
     import torch
-    torch.cuda.set_device(local)
-    if ws_ > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     from synth import workloads as WL
-    from speculative_decoding_dynamic_gb300 import build as Bld
-    Bld.build()
     from speculative_decoding_dynamic_gb300 import cycle as C
     from speculative_decoding_dynamic_gb300 import eagle as E
 
-    seed = rank_seed(args.seed, rank)
-    per_set = (w.depth * w.batch * w.top_k + w.batch * w.T) * w.vocab * w.esize
+    planted, aligned = bool(variant.get("planted", False)), bool(variant.get("aligned", False))
     prefix_len = w.prefix_lengths(seed)
     geo = WL.kv_geometry(w, seed, w.layers)
-    attn_bytes = int(sum(int(L) + w.T for L in prefix_len)) * w.n_kv_heads * w.head_dim * 2 * w.esize
-    R = args.sets or max(2, int(np.ceil(1.5 * L2_BYTES / (per_set + attn_bytes))))
-    R = min(R, w.layers)
-    # inputs per set
+    R, per_set, attn_bytes = rotation_sets(w, seed, args.sets)
     host_sets = []
     for r in range(R):
         sd = seed + 1000 * r
-        host_sets.append(dict(draft=WL.draft_logits(w, sd, planted=args.planted), target=WL.target_logits(w, sd),
-                              q=WL.queries(w, sd), uniforms=WL.uniforms(w, sd, r)))
-    weight_d = lm_out = None
+        host_sets.append(dict(draft=WL.draft_logits(w, sd, planted=planted), target=WL.target_logits(w, sd),
+                              q=WL.queries(w, sd)))
+    weight_d = lm_out = weight_h = None
     if args.lmhead:
         for r in range(R):
             host_sets[r]["hidden"] = WL.hidden_states(w, seed + 1000 * r)
@@ -431,12 +557,12 @@ def main():
     prefix_d = to_dev(prefix_len)
     root_d = to_dev(root)
 
-    # KV cache: attention layers 0..R-1 filled over [0, L+T), every layer's tree region.
+    # KV cache: attention layers 0..R-1 filled over [0, L+T), the other layers' tree regions.
     npdt = np.float32 if w.esize == 4 else np.uint16
-    cache = torch.empty(w.batch * geo["seq_stride"], dtype=C.torch_dtype(w.dtype), device="cuda")
+    cache = torch.zeros(w.batch * geo["seq_stride"], dtype=C.torch_dtype(w.dtype), device="cuda")
     for b in range(w.batch):
         L = int(prefix_len[b])
-        for layer in range(w.layers):
+        for layer in range(w.layers if fill_all_regions else R):
             for which in range(2):
                 p0 = 0 if layer < R else L
                 host = np.zeros((L + w.T - p0) * geo["pos_stride"], npdt)
@@ -457,16 +583,16 @@ def main():
     def cycle(r, stream=None):
         s = dev_sets[r]
         if args.lmhead:
-            dc.run(lm_out, prefix_d, root_d, s["q"], cache, r, s["target"], s["uniforms"], mode, w.temperature,
+            dc.run(lm_out, prefix_d, root_d, s["q"], cache, r, s["target"], seed + 1000 * r, r, mode, w.temperature,
                    compact=True, stream=stream, head=(weight_d, s["hidden"]))
         else:
-            dc.run(s["draft"], prefix_d, root_d, s["q"], cache, r, s["target"], s["uniforms"], mode, w.temperature,
-                   compact=True, stream=stream)
+            dc.run(s["draft"], prefix_d, root_d, s["q"], cache, r, s["target"], seed + 1000 * r, r, mode,
+                   w.temperature, compact=True, stream=stream)
 
     # warm-up outside capture (sets kernel attributes), then one graph per set
     for r in range(R):
         cycle(r)
-        if args.aligned:  # the tree depends on the draft rows only: align this set's targets to it
+        if aligned:  # the tree depends on the draft rows only: align this set's targets to it
             torch.cuda.synchronize()
             align_targets(host_sets[r]["target"], dc.tokens.cpu().numpy(), dc.parent.cpu().numpy(),
                           dc.n_tree.cpu().numpy(), WL.plant_value(w, float(np.mean(w.sharpness_per_seq(seed)))))
@@ -487,13 +613,17 @@ def main():
     torch.cuda.synchronize()
 
     stream = torch.cuda.current_stream()
+    # clocks are sampled from before the warm-up to the end of the per-kernel
+    # timings (the timed region alone can be shorter than one sample period)
+    clk = start_clocks(local) if rank == 0 else None
+    if clk:
+        wait_first_sample(clk)
     for i in range(args.warmup):
         graphs[i % R].replay()
     torch.cuda.synchronize()
     if ws_ > 1:
         import torch.distributed as dist
         dist.barrier()
-    clk = start_clocks(local) if rank == 0 else None
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -506,7 +636,6 @@ def main():
     if ws_ > 1:
         import torch.distributed as dist
         dist.barrier()
-    clocks = stop_clocks(clk) if clk else None
     ms_per_step = ms / args.steps
     value = job_throughput(ws_, args.steps, ms)
 
@@ -588,13 +717,15 @@ def main():
     kt["rerank"] = time_call(lambda r: E.eagle_rerank(cfg, dc.ws), reps)
     kt["build_tree"] = time_call(lambda r: dc.build(prefix_d, root_d), reps)
     kt["attention"] = time_call(lambda r: dc.attention(dev_sets[r]["q"], cache, r, prefix_d), reps)
-    kt["verify"] = time_call(lambda r: dc.verify(mode, w.temperature, dev_sets[r]["target"], dev_sets[r]["uniforms"]),
-                             reps)
+    kt["verify"] = time_call(lambda r: dc.verify(mode, w.temperature, dev_sets[r]["target"], seed + 1000 * r, r), reps)
     cycle(0)
     torch.cuda.synchronize()
     acc_compact = dc.accept_len.cpu().numpy()  # the accepted lengths the timed compaction calls move
     kt["compact"] = time_call(lambda r: dc.compact(cache, prefix_d), reps, flush_l2=True)
     torch.cuda.synchronize()
+    clocks = stop_clocks(clk) if clk else None
+    if clocks:
+        clocks["window"] = "warm-up, timed region and per-kernel timings"
     alg = algorithmic_bytes(w, prefix_len, acc, w.layers)
     peak = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
         os.path.join(ROOT, "MEASURED_PEAKS.json")) else None
@@ -620,6 +751,7 @@ def main():
             if peak:
                 e["frac_tensor"] = round(flop / (ms_k * 1e-3) / 1e12 / peak["bf16_tflops"], 4)
         per_kernel[name] = e
+    per_kernel["compact"]["accept_len_moved"] = round(float(np.mean(acc_compact)), 3)
     cyc_share = {"expand_step": kt["expand_step"] * (w.depth - 1), "attention": kt["attention"],
                  "verify": kt["verify"]}
     if args.lmhead:
@@ -645,7 +777,7 @@ def main():
 
     # ---- end to end through host buffers ----
     e2e = None
-    if not args.no_e2e:
+    if with_e2e:
         # with the LM head on, the draft rows are not an input (the hidden states are)
         pin = [{k: pinned(v) for k, v in s.items() if not (args.lmhead and k == "draft")} for s in host_sets]
         out_a = torch.empty(w.batch, dtype=torch.int32).pin_memory()
@@ -674,59 +806,167 @@ def main():
         e2e = {"value": round(ws_ * args.steps / dt, 2), "unit": "cycles/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h),
                "note": "pinned host inputs copied in, C-ABI calls issued per step (no graph), results copied out"}
+        del pin
 
-    # ---- CPU baseline: the oracle as it stands on a bounded sample ----
+    res = {
+        "value": round(value, 2), "ms_per_step": round(ms_per_step, 5),
+        "config": config_of(w, args, variant, R, per_set, attn_bytes),
+        "tokens_of_tree_per_s": round(value * float(np.mean(n_tree)) * w.batch, 1),
+        "accepted_tokens_per_s": round(value * float(np.mean(acc + 1)) * w.batch, 1),
+        "mean_accept_len": round(float(np.mean(acc)), 3),
+        "mean_tree_value": round(float(np.mean(vals)), 3),
+        "roofline": roofline, "kernels": per_kernel, "e2e": e2e,
+        "gpu_launches": int(launches_per_cycle * args.steps), "launches_per_cycle": int(launches_per_cycle),
+        "clocks": clocks, "dtype": "bf16" if w.dtype == E.EAGLE_BF16 else "f32",
+        "_host": {"weight_h": weight_h, "host_sets": host_sets},
+    }
+    # release the device buffers of this configuration before the next one
+    del graphs, dev_sets, cache, dc, flush, weight_d, lm_out
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def config_summary(r: dict) -> dict:
+    """The compact record of one extra configuration in the `configs` block."""
+    keep = ("value", "ms_per_step", "e2e", "kernels", "roofline", "mean_accept_len", "mean_tree_value",
+            "tokens_of_tree_per_s", "accepted_tokens_per_s", "launches_per_cycle", "clocks", "config")
+    out = {k: r[k] for k in keep}
+    out["unit"] = "cycles/s"
+    if out["e2e"]:
+        out["e2e"] = {k: v for k, v in out["e2e"].items() if k != "note"}
+    return out
+
+
+# ------------------------------------------------------ the reference arm ---
+
+def run_reference(args, w):
+    """The oracle as it stands, timed on the host cores: the bench's reference arm.
+
+    Each step runs one oracle cycle of the workload in every process of a pool
+    (one process per host core, independent input sets, common start); the
+    value is the cycles of all processes over the time of the slowest. When the
+    steps would take more than ~150 s, tree attention (the dominant stage) is
+    sampled on every m-th query head and its time scaled by m."""
+    import oracle
+    oracle.build()
+    seed = args.seed
+    cores = host_cores()
+    pool = OraclePool(cores) if cores > 1 else None
+    probe_inp = OracleInputs(w, seed, 0)
+    probe = probe_inp.cycle(head_stride=w.n_q_heads, policy=POLICIES[args.policy])
+    m = 1
+    while m < w.n_q_heads and (args.steps + args.warmup) * probe / m > 150.0:
+        m *= 2
+    while w.n_q_heads % m:
+        m //= 2
+    if pool is None:
+        for _ in range(args.warmup):
+            probe_inp.cycle(m, POLICIES[args.policy])
+        tot = sum(probe_inp.cycle(m, POLICIES[args.policy]) for _ in range(args.steps))
+        v = args.steps / tot
+        ms_step = 1e3 * tot / args.steps
+        n_proc = 1
+    else:
+        # warm-up cycles run inside the workers before the common start; then K cycles each
+        cyc, wall, est = pool.run(w, seed, POLICIES[args.policy], head_stride=m, cycles=args.steps)
+        # with attention sampled the estimates scale each cycle back to a full one
+        scale = max(1.0, (est / max(cyc, 1)) / (wall / args.steps))
+        v = cyc / (wall * scale)
+        ms_step = 1e3 * wall * scale / args.steps
+        n_proc = pool.n
+        pool.close()
+    unit = "cycles/s"
+    sample = (f"{args.steps} oracle cycles of {w.name} in each of {n_proc} process(es) (one per host core, "
+              f"independent input sets): every stage in full"
+              + ("" if m == 1 else f" except tree attention on every {m}-th query head, its time scaled by {m}"))
+    R, per_set, attn_bytes = rotation_sets(w, seed, args.sets)
+    variant = {"planted": args.planted, "aligned": args.aligned}
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": unit, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(w, args, variant, R, per_set, attn_bytes),
+            "cpu_baseline": {"value": v, "unit": unit, "cores": n_proc, "kind": "oracle", "sample": sample,
+                             "cpu_model": cpu_model()},
+            "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ main ---
+
+def main():
+    args = parse()
+    ws_, rank, local = dist_env()
+    w = workload(args)
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, w)
+        return
+
+    # the all-cores oracle pool is spawned before this process touches the GPU
+    pool = None
+    if rank == 0 and ws_ == 1 and not args.no_cpu_baseline and host_cores() > 1:
+        pool = OraclePool(host_cores())
+
+    import torch
+    torch.cuda.set_device(local)
+    if ws_ > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from synth import workloads as WL
+    from speculative_decoding_dynamic_gb300 import build as Bld
+    Bld.build()
+    from speculative_decoding_dynamic_gb300 import eagle as E  # noqa: F401  (loads libeagle.so)
+
+    seed = rank_seed(args.seed, rank)
+    variant = {"planted": args.planted, "aligned": args.aligned}
+    head = run_workload(args, w, variant, seed, ws_, rank, local, with_e2e=not args.no_e2e)
+    hostd = head.pop("_host")
+
+    configs = None
+    if not args.no_configs and ws_ == 1:
+        configs = {}
+        for label, name, kw, var in EXTRA_CONFIGS:
+            wc = WL.WORKLOADS[name].with_(**kw) if kw else WL.WORKLOADS[name]
+            if wc.name == w.name and wc.verify == w.verify and var.get("aligned", False) == args.aligned:
+                continue  # the headline itself
+            r = run_workload(args, wc, var, seed, ws_, rank, local, with_e2e=not args.no_e2e,
+                             fill_all_regions=False)
+            r.pop("_host")
+            configs[label] = config_summary(r)
+
     cpu = None
     if rank == 0 and ws_ == 1 and not args.no_cpu_baseline:
-        import oracle
-        oracle.build()
-        kh, vh = host_attention_layer(w, geo, prefix_len, seed, 0)
-        region = host_tree_region(w, geo, prefix_len, seed, w.layers)
-        s0 = dict(host_sets[0])
-        n = 0
-        tot = 0.0
-        t0 = time.perf_counter()
-        while n < 1 or (time.perf_counter() - t0 < 12.0 and n < 50):
-            tot += oracle_cycle(w, s0, prefix_len, root, kh, vh, geo, w.verify, region,
-                                policy=POLICIES[args.policy])
-            n += 1
-        sample = f"{n} whole oracle cycles of {w.name} (every stage, all attention rows) on one host core"
-        per_cycle = tot / n
+        lm_extra = None
         if args.lmhead:
-            # the oracle's LM head on one row against 2048 vocabulary rows, scaled to
-            # every row of every step and the whole vocabulary
-            nv = min(w.vocab, 2048)
-            t1 = time.perf_counter()
-            oracle.lmhead_logits(np.ascontiguousarray(host_sets[0]["hidden"][0, :1]), weight_h[:nv])
-            t_lm = time.perf_counter() - t1
-            per_cycle += t_lm * w.depth * w.batch * w.top_k * (w.vocab / nv)
-            sample += (f"; plus the oracle LM head timed on 1 row x {nv} vocabulary rows x {w.hidden_size} and scaled "
-                       f"to {w.depth} steps x {w.batch * w.top_k} rows x {w.vocab} entries")
-        cpu = {"value": round(1.0 / per_cycle, 6), "unit": "cycles/s", "cores": 1, "kind": "oracle",
-               "sample": sample}
+            def lm_extra(inp):
+                # the oracle's LM head on one row against 2048 vocabulary rows, scaled
+                # to every row of every step and the whole vocabulary
+                import oracle
+                nv = min(w.vocab, 2048)
+                t1 = time.perf_counter()
+                oracle.lmhead_logits(np.ascontiguousarray(hostd["host_sets"][0]["hidden"][0, :1]),
+                                     hostd["weight_h"][:nv])
+                t_lm = time.perf_counter() - t1
+                return (t_lm * w.depth * w.batch * w.top_k * (w.vocab / nv),
+                        f"; plus the oracle LM head timed on 1 row x {nv} vocabulary rows x {w.hidden_size} and "
+                        f"scaled to {w.depth} steps x {w.batch * w.top_k} rows x {w.vocab} entries")
+        cpu = cpu_baseline(w, args, seed, pool, lm_extra)
+    if pool is not None:
+        pool.close()
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": round(value, 2), "unit": "cycles/s", "n_gpus": ws_, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == E.EAGLE_BF16 else "f32",
-            "data": "synthetic",
-            "config": {"workload": w.name, "batch": w.batch, "vocab": w.vocab, "depth": w.depth, "top_k": w.top_k,
-                       "node_budget": w.node_budget, "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads,
-                       "head_dim": w.head_dim, "prefix": w.prefix if not isinstance(w.prefix, tuple) else
-                       list(w.prefix), "sharpness": w.sharpness if not isinstance(w.sharpness, tuple) else
-                       list(w.sharpness), "verify": w.verify, "compact_layers": w.layers, "planted": args.planted,
-                       "aligned": args.aligned, "policy": args.policy, "lmhead": args.lmhead,
-                       "hidden_size": w.hidden_size if args.lmhead else None,
-                       "l2": f"{R} rotating input sets, {round(R * (per_set + attn_bytes) / 2**20)} MiB > 129 MB L2",
-                       "graph": "one CUDA graph per input set, replayed"},
-            "tokens_of_tree_per_s": round(value * float(np.mean(n_tree)) * w.batch, 1),
-            "accepted_tokens_per_s": round(value * float(np.mean(acc + 1)) * w.batch, 1),
-            "mean_accept_len": round(float(np.mean(acc)), 3),
-            "mean_tree_value": round(float(np.mean(vals)), 3),
-            "roofline": roofline, "kernels": per_kernel, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": int(launches_per_cycle * args.steps), "launches_per_cycle": int(launches_per_cycle),
-            "clocks": clocks,
+            "metric": METRIC, "value": head["value"], "unit": "cycles/s", "n_gpus": ws_, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"], "data": "synthetic",
+            "config": head["config"],
+            "tokens_of_tree_per_s": head["tokens_of_tree_per_s"],
+            "accepted_tokens_per_s": head["accepted_tokens_per_s"],
+            "mean_accept_len": head["mean_accept_len"], "mean_tree_value": head["mean_tree_value"],
+            "roofline": head["roofline"], "kernels": head["kernels"], "cpu_baseline": cpu, "e2e": head["e2e"],
+            "gpu_launches": head["gpu_launches"], "launches_per_cycle": head["launches_per_cycle"],
+            "clocks": head["clocks"], "configs": configs,
         }
         print(json.dumps(line), flush=True)
     if ws_ > 1:

@@ -234,12 +234,17 @@ int eagle_tree_attention(const eagle_kv_cfg* kv, int T, const void* q, const voi
 /*
  * Stage 6 [summary 2.1: target verification, tokens accepted sequentially by
  * the probability ratio; abstract: the output distribution is unchanged].
+ *   seed, cycle     the uniforms of lossless verification are counter-based:
+ *                   word c of sequence b (c = 0 .. T+1) is word 0 of
+ *                   Philox4x32-10 (Salmon et al., SC'11) at counter
+ *                   (c, b, cycle & 0xffffffff, cycle >> 32) under key
+ *                   (seed & 0xffffffff ^ 7, seed >> 32), drawn on the device.
+ *                   Word c tests the child at slot c (U24 = word >> 8); words T
+ *                   and T+1 form U64 = w[T+1] * 2^32 + w[T] for the final
+ *                   draw. Use a new cycle number per cycle. Unused by GREEDY.
  *   target_logits [B, T, V] in: the target's distribution at each slot.
+ *   draft_logits    reserved for the draft-probability rule; may be NULL.
  *   tokens, parent [B, T], n_tree [B] in: the tree from eagle_build_tree.
- *   uniforms [B, T+2] uint32 in (lossless only, else may be NULL): word c
- *     tests the child at slot c (U24 = word >> 8); words T and T+1 form
- *     U64 = w[T+1] * 2^32 + w[T] for the final draw. Counter-based in the
- *     bundled generator; any source of independent uniform words works.
  *   accept_len [B] out: accepted draft tokens a_b (0..D).
  *   accepted_slots [B, D+1] out: slots of the accepted path, root first, -1 pad.
  *   out_tokens [B, D+1] out: the a_b accepted tokens then the bonus token, -1 pad.
@@ -254,13 +259,15 @@ int eagle_tree_attention(const eagle_kv_cfg* kv, int T, const void* q, const voi
  *   no child accepted the bonus is the smallest token y (not removed) whose
  *   running mass exceeds floor(U64 * S / 2^64).
  */
-int eagle_verify(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int mode, float temperature,
-                 const void* target_logits, const int32_t* tokens, const int32_t* parent, const int32_t* n_tree,
-                 const uint32_t* uniforms, int32_t* accept_len, int32_t* accepted_slots, int32_t* out_tokens,
-                 void* stream);
+int eagle_verify(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int mode, float temperature, uint64_t seed,
+                 uint64_t cycle, const void* target_logits, const void* draft_logits, const int32_t* tokens,
+                 const int32_t* parent, const int32_t* n_tree, int32_t* accept_len, int32_t* accepted_slots,
+                 int32_t* out_tokens, void* stream);
 
 /*
- * Stage 6b: move the accepted path's KV into place. For every layer in
+ * Stage 6b: move the accepted path's KV into place (not on the pages: the
+ * plain reading of compacting the accepted nodes' KV into the contiguous
+ * cache after verification). For every layer in
  * [0, kv->layers), for K and V and j = 1..a_b:
  *   position L_b + j  <-  what position L_b + accepted_slots[b, j] held,
  * all sources read before any destination is written; positions outside
@@ -284,11 +291,14 @@ int eagle_kv_compact(const eagle_kv_cfg* kv, void* kv_cache, const int32_t* pref
  *   - Its per-row scratch is one fixed device array inside the library
  *     (about 4.3 MB, present on every GPU that loads the library until the
  *     process exits). It supports batch <= 1024, batch * (node_budget + 1)
- *     <= 4096 rows and rows * mass pieces <= 4096 * 128 (a row has 128
- *     pieces at a 128256-entry bf16 vocabulary, 64 * ceil(vocab * element
- *     size / 131072) in general) and returns EAGLE_ERR_UNSUPPORTED beyond.
+ *     <= 4096 rows and, in LOSSLESS mode, rows * mass pieces <= 4096 * 128 (a
+ *     row has 128 pieces at a 128256-entry bf16 vocabulary, 64 * ceil(vocab *
+ *     element size / 131072) in general) and returns EAGLE_ERR_UNSUPPORTED
+ *     beyond.
  *   - The first call on a device looks up that array's device address; make
- *     that first call before any stream capture.
+ *     that first call before any stream capture. The address is kept per
+ *     device for the life of the process: do not call this after
+ *     cudaDeviceReset on that device.
  *   - Every call uses the same array, so calls that overlap on the GPU (on
  *     different streams, or from different threads) race and corrupt each
  *     other; serialise them. The array keeps the last call's contents; the
@@ -297,10 +307,10 @@ int eagle_kv_compact(const eagle_kv_cfg* kv, void* kv_cache, const int32_t* pref
  *     word to read); bounds checks still keep every access in range.
  * Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  */
-int eagle_verify_static(const eagle_tree_cfg* cfg, int mode, float temperature, const void* target_logits,
-                        const int32_t* tokens, const int32_t* parent, const int32_t* n_tree,
-                        const uint32_t* uniforms, int32_t* accept_len, int32_t* accepted_slots,
-                        int32_t* out_tokens, void* stream);
+int eagle_verify_static(const eagle_tree_cfg* cfg, int mode, float temperature, uint64_t seed, uint64_t cycle,
+                        const void* target_logits, const int32_t* tokens, const int32_t* parent,
+                        const int32_t* n_tree, int32_t* accept_len, int32_t* accepted_slots, int32_t* out_tokens,
+                        void* stream);
 
 /* Synchronise `stream`, read the device status word of a workspace (the tree
  * workspace or the attention scratch: the word is the first 4 bytes of
@@ -323,6 +333,16 @@ int eagle_tree_export(const eagle_tree_cfg* cfg, const void* ws, size_t ws_bytes
  * (lossless only). Rows t >= n_tree are unspecified. */
 int eagle_verify_export(const eagle_tree_cfg* cfg, const void* ws, size_t ws_bytes, float* row_max,
                         int32_t* row_argmax, uint64_t* row_mass, void* stream);
+
+/* Failure-path test hook: eagle_expand (own lse) with the row kernel's copy
+ * producer switched off, so no copy is ever in flight and every consumer's
+ * bounded wait on the chunk ring gives up (the first after about a second,
+ * later ones at once). The launch completes, its outputs are meaningless and
+ * the workspace's status word reads 2 (eagle_status_fetch returns
+ * EAGLE_ERR_TIMEOUT); the context stays usable. */
+int eagle_test_expand_starved(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int step,
+                              const void* draft_logits, float* row_lse, int32_t* frontier_tokens,
+                              int32_t* frontier_count, void* stream);
 
 /* Kernels launched by this library since it was loaded (host-side count). */
 uint64_t eagle_kernel_launches(void);

@@ -118,9 +118,9 @@ int eagle_tree_init(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, void* 
     return launch_result(launch_tree_init(d, w, static_cast<cudaStream_t>(stream)));
 }
 
-int eagle_expand(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int step, const void* draft_logits,
-                 const float* row_lse_in, float* row_lse, int32_t* frontier_tokens, int32_t* frontier_count,
-                 void* stream) {
+static int expand_call(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int step, const void* draft_logits,
+                       const float* row_lse_in, float* row_lse, int32_t* frontier_tokens, int32_t* frontier_count,
+                       void* stream, bool starve) {
     TreeDims d;
     TreeWs w;
     int rc = resolve(cfg, &d);
@@ -130,7 +130,21 @@ int eagle_expand(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int step,
     if (!draft_logits || !row_lse || !frontier_tokens || !frontier_count) return EAGLE_ERR_INVALID_ARG;
     if (!aligned16(draft_logits)) return EAGLE_ERR_UNSUPPORTED;
     return launch_result(launch_expand(d, w, step, draft_logits, row_lse_in, row_lse, frontier_tokens,
-                                       frontier_count, static_cast<cudaStream_t>(stream)));
+                                       frontier_count, static_cast<cudaStream_t>(stream), starve));
+}
+
+int eagle_expand(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int step, const void* draft_logits,
+                 const float* row_lse_in, float* row_lse, int32_t* frontier_tokens, int32_t* frontier_count,
+                 void* stream) {
+    return expand_call(cfg, ws, ws_bytes, step, draft_logits, row_lse_in, row_lse, frontier_tokens, frontier_count,
+                       stream, false);
+}
+
+int eagle_test_expand_starved(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int step,
+                              const void* draft_logits, float* row_lse, int32_t* frontier_tokens,
+                              int32_t* frontier_count, void* stream) {
+    return expand_call(cfg, ws, ws_bytes, step, draft_logits, nullptr, row_lse, frontier_tokens, frontier_count,
+                       stream, true);
 }
 
 int eagle_lmhead(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int hidden_dim, const void* hidden,
@@ -201,10 +215,10 @@ int eagle_tree_attention(const eagle_kv_cfg* kv, int T, const void* q, const voi
                                           static_cast<int*>(ws), static_cast<cudaStream_t>(stream)));
 }
 
-int eagle_verify(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int mode, float temperature,
-                 const void* target_logits, const int32_t* tokens, const int32_t* parent, const int32_t* n_tree,
-                 const uint32_t* uniforms, int32_t* accept_len, int32_t* accepted_slots, int32_t* out_tokens,
-                 void* stream) {
+int eagle_verify(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int mode, float temperature, uint64_t seed,
+                 uint64_t cycle, const void* target_logits, const void* draft_logits, const int32_t* tokens,
+                 const int32_t* parent, const int32_t* n_tree, int32_t* accept_len, int32_t* accepted_slots,
+                 int32_t* out_tokens, void* stream) {
     TreeDims d;
     TreeWs w;
     int rc = resolve(cfg, &d);
@@ -213,14 +227,16 @@ int eagle_verify(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int mode,
     if (mode != EAGLE_VERIFY_GREEDY && mode != EAGLE_VERIFY_LOSSLESS) return EAGLE_ERR_INVALID_ARG;
     if (!target_logits || !tokens || !parent || !n_tree || !accept_len || !accepted_slots || !out_tokens)
         return EAGLE_ERR_INVALID_ARG;
+    (void)draft_logits;  // read by the draft-probability rule only
     float inv_t = 1.0f;
     if (mode == EAGLE_VERIFY_LOSSLESS) {
-        if (!(temperature > 0.0f) || !std::isfinite(temperature) || uniforms == nullptr) return EAGLE_ERR_INVALID_ARG;
+        if (!(temperature > 0.0f) || !std::isfinite(temperature)) return EAGLE_ERR_INVALID_ARG;
         inv_t = static_cast<float>(1.0 / static_cast<double>(temperature));
     }
     if (!aligned16(target_logits)) return EAGLE_ERR_UNSUPPORTED;
-    return launch_result(launch_verify(d, w, mode, inv_t, target_logits, tokens, parent, n_tree, uniforms, accept_len,
-                                       accepted_slots, out_tokens, static_cast<cudaStream_t>(stream)));
+    return launch_result(launch_verify(d, w, mode, inv_t, target_logits, tokens, parent, n_tree,
+                                       verify_rng(seed, cycle), accept_len, accepted_slots, out_tokens,
+                                       static_cast<cudaStream_t>(stream)));
 }
 
 int eagle_kv_compact(const eagle_kv_cfg* kv, void* kv_cache, const int32_t* prefix_len, const int32_t* accept_len,

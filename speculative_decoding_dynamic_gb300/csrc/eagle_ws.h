@@ -120,17 +120,30 @@ RowPlan plan_rows(int V, int esize, long rows, bool resident, int max_stages, in
 // ----------------------------------------------------------- launchers ---
 // Each returns cudaSuccess or the launch error. All enqueue on `stream`.
 cudaError_t launch_tree_init(const TreeDims& d, const TreeWs& ws, cudaStream_t stream);
+// starve_ring: the failure-path test hook (the row ring's producer issues no
+// copies, so the consumers' bounded waits give up and raise status 2).
 cudaError_t launch_expand(const TreeDims& d, const TreeWs& ws, int step, const void* logits, const float* lse_in,
-                          float* row_lse, int32_t* ftok, int32_t* fcount_out, cudaStream_t stream);
+                          float* row_lse, int32_t* ftok, int32_t* fcount_out, cudaStream_t stream,
+                          bool starve_ring = false);
 cudaError_t launch_rerank(const TreeDims& d, const TreeWs& ws, cudaStream_t stream);
 cudaError_t launch_tree_value(const TreeDims& d, const TreeWs& ws, float* value_sum, cudaStream_t stream);
 cudaError_t launch_build_tree(const TreeDims& d, const TreeWs& ws, const int32_t* prefix_len,
                               const int32_t* root_token, int32_t* tokens, int32_t* parent, int32_t* depth,
                               int32_t* pos, uint32_t* mask, int32_t* n_tree, cudaStream_t stream);
+// Counter-based uniforms of lossless verification: word c of sequence b is
+// word 0 of Philox4x32-10 at counter (c, b, c2, c3) under key (k0, k1), where
+// (k0, k1) = (seed_lo ^ kVerifyStream, seed_hi) and (c2, c3) = (cycle_lo, cycle_hi).
+constexpr uint32_t kVerifyStream = 7;
+struct VerifyRng {
+    uint32_t k0, k1, c2, c3;
+};
+inline VerifyRng verify_rng(uint64_t seed, uint64_t cycle) {
+    return VerifyRng{static_cast<uint32_t>(seed) ^ kVerifyStream, static_cast<uint32_t>(seed >> 32),
+                     static_cast<uint32_t>(cycle), static_cast<uint32_t>(cycle >> 32)};
+}
 cudaError_t launch_verify(const TreeDims& d, const TreeWs& ws, int mode, float inv_temp, const void* target,
-                          const int32_t* tokens, const int32_t* parent, const int32_t* n_tree,
-                          const uint32_t* uniforms, int32_t* accept_len, int32_t* slots, int32_t* out_tokens,
-                          cudaStream_t stream);
+                          const int32_t* tokens, const int32_t* parent, const int32_t* n_tree, VerifyRng rng,
+                          int32_t* accept_len, int32_t* slots, int32_t* out_tokens, cudaStream_t stream);
 
 struct KvDims {
     int B, Hq, Hkv, d, layers, max_len, dtype;

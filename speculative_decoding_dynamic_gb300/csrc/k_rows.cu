@@ -46,6 +46,7 @@
 
 #include "eagle_internal.cuh"
 #include "eagle_ws.h"
+#include "sampling.cuh"
 
 namespace eagle {
 
@@ -426,7 +427,7 @@ __global__ void __launch_bounds__(kRowThreads, 5) expand_kernel(TreeDims d, Tree
                                                                  const float* __restrict__ lse_in,
                                                                  float* __restrict__ row_lse,
                                                                  int32_t* __restrict__ ftok_out,
-                                                                 int32_t* __restrict__ fcount_out) {
+                                                                 int32_t* __restrict__ fcount_out, int starve) {
     extern __shared__ __align__(128) unsigned char dyn_smem[];
     __shared__ ExpandSmem sm;
     cg::cluster_group cluster = cg::this_cluster();
@@ -478,7 +479,8 @@ __global__ void __launch_bounds__(kRowThreads, 5) expand_kernel(TreeDims d, Tree
     __syncthreads();
 
     if (warp == kProducerWarp) {
-        if (lane == 0 && nch > 0)
+        // (starve: the failure-path test hook, no copy is issued and every ring wait gives up)
+        if (lane == 0 && nch > 0 && !starve)
             ring_produce(sm.ring, dyn_smem, row_base + static_cast<size_t>(c0) * ES, n * ES, nch, ns, w.status);
         __syncwarp();
     } else {
@@ -790,8 +792,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
                                                               int nslot, const void* __restrict__ target,
                                                               const int32_t* __restrict__ tokens,
                                                               const int32_t* __restrict__ parent,
-                                                              const int32_t* __restrict__ n_tree,
-                                                              const uint32_t* __restrict__ uniforms,
+                                                              const int32_t* __restrict__ n_tree, VerifyRng rng,
                                                               int32_t* __restrict__ accept_len,
                                                               int32_t* __restrict__ slots_out,
                                                               int32_t* __restrict__ tokens_out) {
@@ -950,8 +951,13 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
             ws.rowmass[c] = __ldcg(&w.row_mass[static_cast<size_t>(b) * T + c]);
         }
     }
-    if (MODE == 1)
-        for (int c = tid; c < T + 2; c += kRowThreads) ws.uni[c] = uniforms[static_cast<size_t>(b) * (T + 2) + c];
+    if (MODE == 1)  // uniform word c of sequence b: Philox4x32-10 at counter (c, b, cycle), word 0
+        for (int c = tid; c < T + 2; c += kRowThreads) {
+            const uint32_t ctr[4] = {static_cast<uint32_t>(c), static_cast<uint32_t>(b), rng.c2, rng.c3};
+            uint32_t out[4];
+            sampling::philox4x32_10(ctr, rng.k0, rng.k1, out);
+            ws.uni[c] = out[0];
+        }
     __syncthreads();
     for (int c = 1 + tid; c < n; c += kRowThreads) {
         const int tk = ws.tok[c], p = ws.par[c];
@@ -1222,7 +1228,7 @@ static cudaError_t launch_rows(K kernel, dim3 grid, int cpr, int smem, cudaStrea
 }
 
 cudaError_t launch_expand(const TreeDims& d, const TreeWs& ws, int step, const void* logits, const float* lse_in,
-                          float* row_lse, int32_t* ftok, int32_t* fcount_out, cudaStream_t stream) {
+                          float* row_lse, int32_t* ftok, int32_t* fcount_out, cudaStream_t stream, bool starve_ring) {
     const int esize = d.dtype == 1 ? 2 : 4;
     const long rows = static_cast<long>(d.B) * d.k;
     const int max_seg = esize == 2 ? kMaxSegChunksBf16 : kMaxSegChunks;
@@ -1268,7 +1274,7 @@ cudaError_t launch_expand(const TreeDims& d, const TreeWs& ws, int step, const v
     const int scratch = p.nch * kConsumers * 4 + 512 * 8;  // candidate groups + keys
     const int pick = kMaxTopK * kMaxTopK * (8 + 4) + kMaxTopK * 4 + 16;
     const int smem = std::max(pick, p.nch <= p.stages ? p.stages * kRowChunkBytes + scratch : std::max(p.smem, scratch));
-    int seg = p.seg, ns = p.stages, smem_bytes = smem;
+    int seg = p.seg, ns = p.stages, smem_bytes = smem, starve = starve_ring ? 1 : 0;
     void* args[] = {&dd,
                     &ww,
                     &step,
@@ -1279,15 +1285,15 @@ cudaError_t launch_expand(const TreeDims& d, const TreeWs& ws, int step, const v
                     const_cast<float**>(&lse_in),
                     &row_lse,
                     &ftok,
-                    &fcount_out};
+                    &fcount_out,
+                    &starve};
     return d.dtype == 1 ? launch_rows(expand_kernel<1>, grid, p.cpr, smem, stream, args)
                         : launch_rows(expand_kernel<0>, grid, p.cpr, smem, stream, args);
 }
 
 cudaError_t launch_verify(const TreeDims& d, const TreeWs& ws, int mode, float inv_temp, const void* target,
-                          const int32_t* tokens, const int32_t* parent, const int32_t* n_tree,
-                          const uint32_t* uniforms, int32_t* accept_len, int32_t* slots, int32_t* out_tokens,
-                          cudaStream_t stream) {
+                          const int32_t* tokens, const int32_t* parent, const int32_t* n_tree, VerifyRng rng,
+                          int32_t* accept_len, int32_t* slots, int32_t* out_tokens, cudaStream_t stream) {
     const int esize = d.dtype == 1 ? 2 : 4;
     const RowPlan p = plan_rows(d.V, esize, static_cast<long>(d.B) * d.T, mode == 1, kRowStages, 1 << 20);
     if (mode == 1 && p.stages > kRowStages) return cudaErrorInvalidValue;
@@ -1307,7 +1313,7 @@ cudaError_t launch_verify(const TreeDims& d, const TreeWs& ws, int mode, float i
                     const_cast<int32_t**>(&tokens),
                     const_cast<int32_t**>(&parent),
                     const_cast<int32_t**>(&n_tree),
-                    const_cast<uint32_t**>(&uniforms),
+                    &rng,
                     &accept_len,
                     &slots,
                     &out_tokens};

@@ -70,23 +70,26 @@ cudaError_t scratch_address(unsigned char** out) {
 
 using namespace eagle;
 
-extern "C" int eagle_verify_static(const eagle_tree_cfg* cfg, int mode, float temperature,
-                                   const void* target_logits, const int32_t* tokens, const int32_t* parent,
-                                   const int32_t* n_tree, const uint32_t* uniforms, int32_t* accept_len,
+extern "C" int eagle_verify_static(const eagle_tree_cfg* cfg, int mode, float temperature, uint64_t seed,
+                                   uint64_t cycle, const void* target_logits, const int32_t* tokens,
+                                   const int32_t* parent, const int32_t* n_tree, int32_t* accept_len,
                                    int32_t* accepted_slots, int32_t* out_tokens, void* stream) {
     if (cfg == nullptr) return EAGLE_ERR_INVALID_ARG;
     // Same checks as eagle_verify, through its public size query.
     if (eagle_workspace_bytes(cfg) == 0) return EAGLE_ERR_INVALID_ARG;
+    if (mode != EAGLE_VERIFY_GREEDY && mode != EAGLE_VERIFY_LOSSLESS) return EAGLE_ERR_INVALID_ARG;
     const long rows = static_cast<long>(cfg->batch) * (cfg->node_budget + 1);
     if (cfg->batch > kMaxSeqs || rows > kMaxRows) return EAGLE_ERR_UNSUPPORTED;  // beyond the fixed scratch
+    // integer-mass pieces are written by lossless verification only
     const int esize = cfg->logit_dtype == EAGLE_BF16 ? 2 : 4;
-    if (static_cast<size_t>(rows) * verify_mass_slots(cfg->vocab, esize) > kMaxPieces) return EAGLE_ERR_UNSUPPORTED;
-    if (mode != EAGLE_VERIFY_GREEDY && mode != EAGLE_VERIFY_LOSSLESS) return EAGLE_ERR_INVALID_ARG;
+    if (mode == EAGLE_VERIFY_LOSSLESS &&
+        static_cast<size_t>(rows) * verify_mass_slots(cfg->vocab, esize) > kMaxPieces)
+        return EAGLE_ERR_UNSUPPORTED;
     if (!target_logits || !tokens || !parent || !n_tree || !accept_len || !accepted_slots || !out_tokens)
         return EAGLE_ERR_INVALID_ARG;
     float inv_t = 1.0f;
     if (mode == EAGLE_VERIFY_LOSSLESS) {
-        if (!(temperature > 0.0f) || !(temperature < INFINITY) || uniforms == nullptr) return EAGLE_ERR_INVALID_ARG;
+        if (!(temperature > 0.0f) || !(temperature < INFINITY)) return EAGLE_ERR_INVALID_ARG;
         inv_t = static_cast<float>(1.0 / static_cast<double>(temperature));
     }
     if ((reinterpret_cast<uintptr_t>(target_logits) & 15u) != 0) return EAGLE_ERR_UNSUPPORTED;
@@ -117,7 +120,7 @@ extern "C" int eagle_verify_static(const eagle_tree_cfg* cfg, int mode, float te
     // is fully written by the kernels before it is read.
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(base, 0, kOffTicket + d.B * sizeof(int), s) != cudaSuccess) return EAGLE_ERR_LAUNCH;
-    const cudaError_t e = launch_verify(d, w, mode, inv_t, target_logits, tokens, parent, n_tree, uniforms,
-                                        accept_len, accepted_slots, out_tokens, s);
+    const cudaError_t e = launch_verify(d, w, mode, inv_t, target_logits, tokens, parent, n_tree,
+                                        verify_rng(seed, cycle), accept_len, accepted_slots, out_tokens, s);
     return e == cudaSuccess ? EAGLE_OK : EAGLE_ERR_LAUNCH;
 }

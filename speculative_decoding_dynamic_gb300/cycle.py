@@ -66,21 +66,22 @@ class DeviceCycle:
         E.eagle_tree_attention(self.kv, self.cfg.T, q, cache, layer, prefix_len, self.mask, self.n_tree,
                                self.attn_out, self.attn_ws, stream)
 
-    def verify(self, mode, temperature, target, uniforms, stream=None):
-        E.eagle_verify(self.cfg, self.ws, mode, temperature, target, self.tokens, self.parent, self.n_tree, uniforms,
-                       self.accept_len, self.slots, self.out_tokens, stream)
+    def verify(self, mode, temperature, target, seed, cycle, stream=None):
+        """Stage 6; lossless uniforms are Philox words of (seed, cycle) drawn on the device."""
+        E.eagle_verify(self.cfg, self.ws, mode, temperature, seed, cycle, target, self.tokens, self.parent,
+                       self.n_tree, self.accept_len, self.slots, self.out_tokens, stream=stream)
 
     def compact(self, cache, prefix_len, stream=None):
         E.eagle_kv_compact(self.kv, cache, prefix_len, self.accept_len, self.slots, self.cfg.depth + 1, self.new_len,
                            self.ws, stream)
 
-    def run(self, draft_logits, prefix_len, root_token, q, cache, layer, target, uniforms, mode, temperature=1.0,
+    def run(self, draft_logits, prefix_len, root_token, q, cache, layer, target, seed, cycle, mode, temperature=1.0,
             compact=True, stream=None, head=None):
         """The whole cycle (all stages) enqueued on `stream`."""
         self.draft(draft_logits, stream, head=head)
         self.build(prefix_len, root_token, stream)
         self.attention(q, cache, layer, prefix_len, stream)
-        self.verify(mode, temperature, target, uniforms, stream)
+        self.verify(mode, temperature, target, seed, cycle, stream)
         if compact:
             self.compact(cache, prefix_len, stream)
 
@@ -89,12 +90,3 @@ class DeviceCycle:
         b = E.eagle_status_fetch(self.attn_ws, stream)
         return a or b
 
-
-def tree_cfg(batch, vocab, top_k, depth, node_budget, threshold, dtype) -> E.TreeCfg:
-    return E.TreeCfg(batch, vocab, top_k, depth, node_budget, threshold, dtype)
-
-
-def kv_cfg(batch, n_q_heads, n_kv_heads, head_dim, layers, max_len, dtype, seq_stride, layer_stride, kv_stride,
-           pos_stride) -> E.KvCfg:
-    return E.KvCfg(batch, n_q_heads, n_kv_heads, head_dim, layers, max_len, dtype, seq_stride, layer_stride,
-                   kv_stride, pos_stride)

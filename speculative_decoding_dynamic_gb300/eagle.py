@@ -73,6 +73,7 @@ _lib.eagle_workspace_bytes.argtypes = [_TP]
 _lib.eagle_workspace_bytes.restype = _sz
 _lib.eagle_tree_init.argtypes = [_TP, _p, _sz, _p]
 _lib.eagle_expand.argtypes = [_TP, _p, _sz, _i, _p, _p, _p, _p, _p, _p]
+_lib.eagle_test_expand_starved.argtypes = [_TP, _p, _sz, _i, _p, _p, _p, _p, _p]
 _lib.eagle_lmhead.argtypes = [_TP, _p, _sz, _i, _p, _p, _p, _p]
 _lib.eagle_rerank.argtypes = [_TP, _p, _sz, _p]
 _lib.eagle_tree_value.argtypes = [_TP, _p, _sz, _p, _p]
@@ -80,9 +81,10 @@ _lib.eagle_build_tree.argtypes = [_TP, _p, _sz, _p, _p, _p, _p, _p, _p, _p, _p, 
 _lib.eagle_attention_workspace_bytes.argtypes = [_KP, _i]
 _lib.eagle_attention_workspace_bytes.restype = _sz
 _lib.eagle_tree_attention.argtypes = [_KP, _i, _p, _p, _i, _p, _p, _p, _p, _p, _sz, _p]
-_lib.eagle_verify.argtypes = [_TP, _p, _sz, _i, ctypes.c_float, _p, _p, _p, _p, _p, _p, _p, _p, _p]
+_u64 = ctypes.c_uint64
+_lib.eagle_verify.argtypes = [_TP, _p, _sz, _i, ctypes.c_float, _u64, _u64, _p, _p, _p, _p, _p, _p, _p, _p, _p]
 _lib.eagle_kv_compact.argtypes = [_KP, _p, _p, _p, _p, _i, _p, _p, _p]
-_lib.eagle_verify_static.argtypes = [_TP, _i, ctypes.c_float, _p, _p, _p, _p, _p, _p, _p, _p, _p]
+_lib.eagle_verify_static.argtypes = [_TP, _i, ctypes.c_float, _u64, _u64, _p, _p, _p, _p, _p, _p, _p, _p]
 _lib.eagle_status_fetch.argtypes = [_p, ctypes.POINTER(ctypes.c_int), _p]
 _lib.eagle_tree_export.argtypes = [_TP, _p, _sz, _p, _p, _p, _p, _p, _p, _p, _p]
 _lib.eagle_verify_export.argtypes = [_TP, _p, _sz, _p, _p, _p, _p]
@@ -143,6 +145,14 @@ def eagle_expand(cfg, ws, step, draft_logits, row_lse_in, row_lse, frontier_toke
                                              _ptr(frontier_count), _stream(stream)))
 
 
+def eagle_test_expand_starved(cfg, ws, step, draft_logits, row_lse, frontier_tokens, frontier_count, stream=None):
+    """Failure-path test hook: expansion whose row ring receives no copies (status 2 expected)."""
+    _check("eagle_test_expand_starved", _lib.eagle_test_expand_starved(ctypes.byref(cfg), *_ws(ws), step,
+                                                                       _ptr(draft_logits), _ptr(row_lse),
+                                                                       _ptr(frontier_tokens), _ptr(frontier_count),
+                                                                       _stream(stream)))
+
+
 def eagle_lmhead(cfg, ws, hidden_dim, hidden, weight, draft_logits, stream=None):
     _check("eagle_lmhead", _lib.eagle_lmhead(ctypes.byref(cfg), *_ws(ws), hidden_dim, _ptr(hidden), _ptr(weight),
                                              _ptr(draft_logits), _stream(stream)))
@@ -168,20 +178,20 @@ def eagle_tree_attention(kv, T, q, kv_cache, layer, prefix_len, mask, n_tree, ou
                                                              *_ws(ws), _stream(stream)))
 
 
-def eagle_verify(cfg, ws, mode, temperature, target_logits, tokens, parent, n_tree, uniforms, accept_len,
-                 accepted_slots, out_tokens, stream=None):
-    _check("eagle_verify", _lib.eagle_verify(ctypes.byref(cfg), *_ws(ws), mode, float(temperature),
-                                             _ptr(target_logits), _ptr(tokens), _ptr(parent), _ptr(n_tree),
-                                             _ptr(uniforms), _ptr(accept_len), _ptr(accepted_slots),
+def eagle_verify(cfg, ws, mode, temperature, seed, cycle, target_logits, tokens, parent, n_tree, accept_len,
+                 accepted_slots, out_tokens, draft_logits=None, stream=None):
+    _check("eagle_verify", _lib.eagle_verify(ctypes.byref(cfg), *_ws(ws), mode, float(temperature), int(seed),
+                                             int(cycle), _ptr(target_logits), _ptr(draft_logits), _ptr(tokens),
+                                             _ptr(parent), _ptr(n_tree), _ptr(accept_len), _ptr(accepted_slots),
                                              _ptr(out_tokens), _stream(stream)))
 
 
-def eagle_verify_static(cfg, mode, temperature, target_logits, tokens, parent, n_tree, uniforms, accept_len,
+def eagle_verify_static(cfg, mode, temperature, seed, cycle, target_logits, tokens, parent, n_tree, accept_len,
                         accepted_slots, out_tokens, stream=None):
     """eagle_verify for callers that may not allocate: scratch lives in a fixed device array of the library."""
-    _check("eagle_verify_static", _lib.eagle_verify_static(ctypes.byref(cfg), mode, float(temperature),
-                                                           _ptr(target_logits), _ptr(tokens), _ptr(parent),
-                                                           _ptr(n_tree), _ptr(uniforms), _ptr(accept_len),
+    _check("eagle_verify_static", _lib.eagle_verify_static(ctypes.byref(cfg), mode, float(temperature), int(seed),
+                                                           int(cycle), _ptr(target_logits), _ptr(tokens),
+                                                           _ptr(parent), _ptr(n_tree), _ptr(accept_len),
                                                            _ptr(accepted_slots), _ptr(out_tokens), _stream(stream)))
 
 

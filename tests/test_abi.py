@@ -78,12 +78,17 @@ def test_calls_reject_bad_arguments_before_launch(E):
     assert r("eagle_expand", ctypes.byref(cfg), fake_ws, ws_bytes, 0, None, None, ptr, ptr, ptr, None) == -1
     assert r("eagle_expand", ctypes.byref(cfg), fake_ws, ws_bytes, 0, P((1 << 21) + 4), None, ptr, ptr, ptr,
              None) == -2
-    assert r("eagle_verify", ctypes.byref(cfg), fake_ws, ws_bytes, 5, ctypes.c_float(1.0), ptr, ptr, ptr, ptr, ptr,
+    u64 = ctypes.c_uint64
+    one = ctypes.c_float(1.0)
+    assert r("eagle_verify", ctypes.byref(cfg), fake_ws, ws_bytes, 5, one, u64(1), u64(0), ptr, None, ptr, ptr, ptr,
              ptr, ptr, ptr, None) == -1
-    assert r("eagle_verify", ctypes.byref(cfg), fake_ws, ws_bytes, 1, ctypes.c_float(0.0), ptr, ptr, ptr, ptr, ptr,
+    assert r("eagle_verify", ctypes.byref(cfg), fake_ws, ws_bytes, 1, ctypes.c_float(0.0), u64(1), u64(0), ptr, None,
+             ptr, ptr, ptr, ptr, ptr, ptr, None) == -1
+    assert r("eagle_verify", ctypes.byref(cfg), fake_ws, ws_bytes, 0, one, u64(1), u64(0), None, None, ptr, ptr, ptr,
              ptr, ptr, ptr, None) == -1
-    assert r("eagle_verify", ctypes.byref(cfg), fake_ws, ws_bytes, 1, ctypes.c_float(1.0), ptr, ptr, ptr, ptr, None,
-             ptr, ptr, ptr, None) == -1
+    assert r("eagle_verify", ctypes.byref(cfg), fake_ws, ws_bytes, 0, one, u64(1), u64(0), P((1 << 21) + 4), None,
+             ptr, ptr, ptr, ptr, ptr, ptr, None) == -2
+    assert r("eagle_test_expand_starved", ctypes.byref(cfg), fake_ws, ws_bytes, 3, ptr, ptr, ptr, ptr, None) == -1
     assert r("eagle_lmhead", ctypes.byref(cfg), fake_ws, ws_bytes, 4096, None, ptr, ptr, None) == -1
     assert r("eagle_lmhead", ctypes.byref(cfg), fake_ws, ws_bytes, 0, ptr, ptr, ptr, None) == -1
     assert r("eagle_lmhead", ctypes.byref(cfg), fake_ws, ws_bytes, 4100, ptr, ptr, ptr, None) == -2  # H % 8
@@ -103,3 +108,25 @@ def test_calls_reject_bad_arguments_before_launch(E):
 def test_status_strings(E):
     for code in range(-6, 1):
         assert E._lib.eagle_status_string(code)
+
+
+def test_static_verify_rejects_what_its_fixed_scratch_cannot_hold(E):
+    """eagle_verify_static's size limits, checked before any CUDA call (the
+    pointers are never dereferenced: every call here is rejected first)."""
+    P = ctypes.c_void_p
+    p = P(1 << 20)
+    u64 = ctypes.c_uint64
+    one = ctypes.c_float(1.0)
+
+    def call(cfg, mode):
+        return E.raw_call("eagle_verify_static", ctypes.byref(cfg), mode, one, u64(1), u64(0), p, p, p, p, p, p, p,
+                          None)
+
+    assert call(E.TreeCfg(80, 1024, 4, 3, 60, 0.0, E.EAGLE_F32), 0) == -2  # 80 * 61 rows > 4096
+    assert call(E.TreeCfg(1025, 1024, 4, 3, 1, 0.0, E.EAGLE_F32), 0) == -2  # batch > 1024
+    # fp32 at a 128256-entry vocabulary: 256 mass pieces per row, so at most 2048 lossless rows
+    assert call(E.TreeCfg(34, 128256, 4, 3, 60, 0.0, E.EAGLE_F32), 1) == -2  # 2074 rows
+    assert call(E.TreeCfg(2, 1024, 4, 3, 10, 0.0, E.EAGLE_F32), 7) == -1  # unknown mode
+    assert call(E.TreeCfg(2, 1024, 0, 3, 10, 0.0, E.EAGLE_F32), 0) == -1  # invalid tree
+    assert E.raw_call("eagle_verify_static", ctypes.byref(E.TreeCfg(2, 1024, 4, 3, 10, 0.0, E.EAGLE_F32)), 1,
+                      ctypes.c_float(0.0), u64(1), u64(0), p, p, p, p, p, p, p, None) == -1  # temperature 0

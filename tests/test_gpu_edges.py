@@ -137,7 +137,7 @@ def test_equal_logit_rows_use_exact_fallback():
     _run_tree(logits, B, V, k, D, N, 0.0, synth.BF16)
 
 
-def _verify_both(target, tokens, parent, n_tree, depth, mode, uniforms=None, V=None):
+def _verify_both(target, tokens, parent, n_tree, depth, mode, seed=0, cycle=0):
     import torch
     E = _E()
     B, T, V = target.shape
@@ -145,13 +145,13 @@ def _verify_both(target, tokens, parent, n_tree, depth, mode, uniforms=None, V=N
     ws = E.alloc_workspace(E.eagle_workspace_bytes(cfg))
     i32 = dict(dtype=torch.int32, device="cuda")
     a, sl, tk = torch.empty(B, **i32), torch.empty(B, depth + 1, **i32), torch.empty(B, depth + 1, **i32)
-    uni = None if uniforms is None else H.to_dev(uniforms)
-    E.eagle_verify(cfg, ws, mode, 1.0, H.to_dev(target), H.to_dev(tokens), H.to_dev(parent), H.to_dev(n_tree), uni,
-                   a, sl, tk)
+    E.eagle_verify(cfg, ws, mode, 1.0, seed, cycle, H.to_dev(target), H.to_dev(tokens), H.to_dev(parent),
+                   H.to_dev(n_tree), a, sl, tk)
     torch.cuda.synchronize()
     if mode == E.GREEDY:
         ra, rs, rt, _ = oracle.verify_greedy(target, tokens, parent, n_tree, depth)
     else:
+        uniforms = synth.words(B, T + 2, cycle, seed=seed, stream=synth.STREAM_VERIFY)
         ra, rs, rt = oracle.verify_lossless(target, tokens, parent, n_tree, uniforms, depth)
     assert (H.to_host(a) == ra).all() and (H.to_host(sl) == rs).all() and (H.to_host(tk) == rt).all()
     assert E.eagle_status_fetch(ws) == 0
@@ -173,8 +173,7 @@ def test_verify_root_only_and_full_chain(mode):
         tokens[1, c] = 100 + c
         parent[1, c] = c - 1
         target[1, c - 1, 100 + c] = np.float32(60.0).view(np.uint32) >> 16
-    U = synth.words(2, T + 2, 0, seed=9)
-    a = _verify_both(target, tokens, parent, n_tree, D, mode, U)
+    a = _verify_both(target, tokens, parent, n_tree, D, mode, seed=9, cycle=0)
     assert a[0] == 0 and a[1] == D
 
 
@@ -242,9 +241,8 @@ def test_status_token_out_of_range_in_verify():
     ws = E.alloc_workspace(E.eagle_workspace_bytes(cfg))
     i32 = dict(dtype=torch.int32, device="cuda")
     a, sl, tk = torch.empty(1, **i32), torch.empty(1, 3, **i32), torch.empty(1, 3, **i32)
-    U = H.to_dev(synth.words(1, T + 2, 0, seed=1))
-    E.eagle_verify(cfg, ws, E.LOSSLESS, 1.0, H.to_dev(target), H.to_dev(tokens), H.to_dev(parent),
-                   H.to_dev(np.array([T], np.int32)), U, a, sl, tk)
+    E.eagle_verify(cfg, ws, E.LOSSLESS, 1.0, 1, 0, H.to_dev(target), H.to_dev(tokens), H.to_dev(parent),
+                   H.to_dev(np.array([T], np.int32)), a, sl, tk)
     assert E.eagle_status_fetch(ws) == 3
 
 
@@ -265,3 +263,84 @@ def test_status_accept_length_past_limit_leaves_cache():
                        H.to_dev(slots), 20, nl, ws)
     assert E.eagle_status_fetch(ws) == 3
     assert (H.to_host(dc) == cache).all() and int(nl.item()) == -9
+
+
+# --------------------------------------- rows of -inf, short and constant rows ---
+
+def _edge_rows(shape, dtype, seed, k):
+    """Logit rows of four kinds, chosen by the row's flat index mod 4:
+    0 ordinary (2.5 N(0, 1)); 1 mostly -inf (512 finite entries at seeded
+    positions); 2 fewer than k finite entries (k // 3 + 1); 3 constant (every
+    entry equal). No row is entirely -inf (its log-sum-exp would be NaN)."""
+    x = synth.normal4(shape, dtype, 2.5, seed=seed, stream=synth.STREAM_DRAFT)
+    V = shape[-1]
+    rows = x.reshape(-1, V)
+    ninf = np.uint16(0xFF80) if dtype == synth.BF16 else np.float32(-np.inf)
+    rng = np.random.default_rng(seed)
+    for i in range(rows.shape[0]):
+        kind = i % 4
+        if kind in (1, 2):
+            keep = rng.choice(V, 512 if kind == 1 else k // 3 + 1, replace=False)
+            vals = rows[i, keep].copy()
+            rows[i, :] = ninf
+            rows[i, keep] = vals
+        elif kind == 3:
+            rows[i, :] = rows[i, 7]
+    return x
+
+
+@pytest.mark.parametrize("V,dtype", [(128256, synth.BF16), (1024, synth.F32)])
+def test_expand_rows_of_neg_inf_few_finite_and_constant(V, dtype):
+    """Stage 1+2 on rows that are mostly -inf, hold fewer than k finite entries
+    (their last children are -inf entries, lowest ids first) or are constant:
+    the kernel's exact paths for few lanes holding values and for ties at the
+    top, bit-exact against the oracle through stages 2-4."""
+    B, k, D, N = 2, 10, 3, 40
+    logits = _edge_rows((D, B, k, V), dtype, seed=V + 11, k=k)
+    t, tr = _run_tree(logits, B, V, k, D, N, 0.0, dtype)
+    assert np.isneginf(t.logv[t.valid == 1]).any(), "some children should be -inf entries"
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("V,dtype", [(128256, synth.BF16), (1024, synth.F32)])
+def test_verify_rows_of_neg_inf_few_finite_and_constant(V, dtype, mode):
+    """Stage 6 on target rows of the same four kinds (argmax over -inf entries
+    and over ties; integer masses of -inf entries are zero), on a tree built
+    from ordinary draft rows; accepted paths and bonus tokens bit-exact."""
+    B, k, D, N = 2, 4, 3, 12
+    draft = synth.normal4((D, B, k, V), dtype, 2.5, seed=5, stream=synth.STREAM_DRAFT)
+    synth.plant(draft, dtype, float(np.log(9.0 * V)) + 3.0, seed=5, stream=synth.STREAM_DRAFT, frac=0.8)
+    _, tr = _run_tree(draft, B, V, k, D, N, 0.0, dtype)
+    T = N + 1
+    target = _edge_rows((1, B, T, V), dtype, seed=V + 17, k=k)[0]
+    # favour first children on the ordinary rows so that a path is accepted there
+    for b in range(B):
+        for t in range(int(tr["n_tree"][b])):
+            kids = [c for c in range(int(tr["n_tree"][b])) if tr["parent"][b, c] == t]
+            if kids and (b * T + t) % 4 == 0:
+                val = np.float32(40.0)
+                target[b, t, tr["tokens"][b, kids[0]]] = (val.view(np.uint32) >> 16) if dtype == synth.BF16 else val
+    tokens = np.ascontiguousarray(tr["tokens"])
+    parent = np.ascontiguousarray(tr["parent"])
+    for seed in (3, 4):
+        _verify_both(np.ascontiguousarray(target), tokens, parent, tr["n_tree"], D, mode, seed=seed, cycle=seed)
+
+
+def test_status_ring_wait_timeout_then_recovers():
+    """A row-kernel wait that runs out: the expansion's chunk ring receives no
+    copies (test hook), every consumer's bounded wait gives up, the status word
+    reads 2, and the same workspace then serves a normal, oracle-exact draft."""
+    import torch
+    E = _E()
+    B, V, k, D, N = 1, 4096, 2, 2, 4
+    cfg = E.TreeCfg(B, V, k, D, N, 0.0, synth.BF16)
+    ws = E.alloc_workspace(E.eagle_workspace_bytes(cfg))
+    logits = synth.normal4((D, B, k, V), synth.BF16, 2.0, seed=8, stream=synth.STREAM_DRAFT)
+    dl = H.to_dev(logits)
+    row_lse = torch.empty(B, D, k, dtype=torch.float32, device="cuda")
+    ftok, fcnt = torch.empty(B, k, dtype=torch.int32, device="cuda"), torch.empty(B, dtype=torch.int32, device="cuda")
+    E.eagle_tree_init(cfg, ws)
+    E.eagle_test_expand_starved(cfg, ws, 0, dl[0], row_lse, ftok, fcnt)
+    assert E.eagle_status_fetch(ws) == 2
+    assert E.eagle_status_fetch(ws) == 0
+    _run_tree(logits, B, V, k, D, N, 0.0, synth.BF16)
