@@ -12,7 +12,7 @@ is captured once in a CUDA graph and replayed.
 
 The JSON line's headline is the Llama-3.1-8B batch-1 cycle (lossless). The
 same run then measures, with the same K and W, the other configurations of
-the workload table (8B batch 64 greedy, with and without aligned targets,
+the workload table (8B batch 64 greedy, as stated and with planted drafts and aligned targets,
 70B batch 8 lossless, 13B batch 1 lossless, 8B batch 1 greedy) into the
 line's `configs` block (skip with --no-configs). The oracle is timed on the
 host cores: one core, and one process per core on independent cycles.
@@ -47,7 +47,7 @@ POLICIES = {"dynamic": 0, "confidence": 1, "no_rerank": 2, "static": 3}
 # The configurations measured beside the headline: (label, workload, overrides, variant flags).
 EXTRA_CONFIGS = [
     ("llama8b_b64_greedy", "llama8b_b64", {}, {}),
-    ("llama8b_b64_greedy_aligned", "llama8b_b64", {}, {"aligned": True}),
+    ("llama8b_b64_greedy_planted_aligned", "llama8b_b64", {}, {"aligned": True, "planted": True}),
     ("llama70b_b8_lossless", "llama70b_b8", {}, {}),
     ("vicuna13b_b1_lossless", "vicuna13b_b1", {}, {}),
     ("llama8b_b1_greedy", "llama8b_b1", {"verify": "greedy"}, {}),
