@@ -18,9 +18,9 @@
 // Expansion, one pass over the data: per lane a running maximum and a
 // rescaled exp-sum (online normaliser), and the maximum of each lane group
 // (the lane's four vectors of one chunk). After the pass, the admission key
-// tau = the largest over the warps of the warp's k-th largest lane maximum
-// (k distinct elements reach it, so every element of the segment's top-k
-// does, and lies in a group whose maximum reaches it). Only those groups are
+// tau = the k-th largest lane maximum of the CTA's segment (k distinct
+// elements reach it, so every element of the segment's top-k does, and lies
+// in a group whose maximum reaches it). Only those groups are
 // read again (from the stages when the segment stayed resident, else from
 // L2) and their keys >= tau ranked. Keys are (value, -id): unique, so ties go
 // to the lower token id. CTA and cluster results are merged by rank
@@ -185,17 +185,37 @@ __device__ __forceinline__ unsigned lanemask_lt() {
     return m;
 }
 
-// Rank of `key` among n lists of kMaxTopK keys (zeros = empty): how many
-// keys are larger. Every list is read whole (zero padding counts nothing).
+// Rank of `key` among the first n of kMaxChunks lists of kMaxTopK keys
+// (zeros = empty): how many keys are larger. Every list is read whole (zero
+// padding counts nothing); all kMaxChunks lists are read, so that the loads
+// are issued back to back, and the ones past n are not counted.
 __device__ __forceinline__ int rank_in_lists(const uint64_t* lists, int n, uint64_t key) {
     int r = 0;
-    for (int l = 0; l < n; ++l) {
+#pragma unroll
+    for (int l = 0; l < kMaxChunks; ++l) {
         const ulonglong2* p = reinterpret_cast<const ulonglong2*>(lists + l * kMaxTopK);
+        int rl = 0;
 #pragma unroll
         for (int q = 0; q < kMaxTopK / 2; ++q) {
             const ulonglong2 a = p[q];
-            r += (a.x > key) + (a.y > key);
+            rl += (a.x > key) + (a.y > key);
         }
+        r += l < n ? rl : 0;
+    }
+    return r;
+}
+
+// Rank of `key` among n keys (a 16-byte aligned list zero-padded to a
+// multiple of 8): how many are larger. Eight keys per step, loads first.
+__device__ __forceinline__ int rank_in_list(const uint64_t* list, int n, uint64_t key) {
+    const ulonglong2* p = reinterpret_cast<const ulonglong2*>(list);
+    int r = 0;
+    for (int q = 0; q < (n + 7) / 8 * 4; q += 4) {
+        ulonglong2 a[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) a[u] = p[q + u];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) r += (a[u].x > key) + (a[u].y > key);
     }
     return r;
 }
@@ -273,9 +293,12 @@ __device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" 
 
 struct ExpandSmem {
     RowRing ring;
-    unsigned long long tau;                       // segment admission key (atomic maximum)
+    unsigned long long tau;                       // segment admission key
+    alignas(16) uint32_t wtop[kConsumerWarps][kMaxTopK];  // each warp's k largest lane maxima (ordered bits)
     uint32_t gmax[kMaxSegChunks][kConsumers];     // maximum of each lane group (ordered bits; see gmax_put)
     int ngroups, nkeys;
+    int F, parent;                                // this step's frontier count; the row's parent node
+    float plogv;                                  // the parent's log path value
     float wm[kConsumerWarps];
     float ws[kConsumerWarps];
     uint64_t ctop[kMaxTopK];
@@ -308,12 +331,13 @@ __device__ __forceinline__ uint32_t gmax_floor(uint32_t o) { return DT == 1 ? (o
 
 // Top-k keys of a CTA's row segment, after the streaming pass (consumer
 // threads only). A lane group is one lane's four vectors of one chunk, and
-// gmax holds each group's maximum. tau = the largest, over the warps, of the
-// warp's k-th largest lane maximum of the whole segment: k distinct elements
-// reach it, so every element of the segment's top-k does, and lies in a group
-// whose maximum reaches it. Those groups are read again (from L2: the row was
-// just streamed), their elements >= tau collected, and the k largest keys
-// found by rank selection into ctop. When the keys do not fit the scratch
+// gmax holds each group's maximum. tau = the k-th largest lane maximum of the
+// whole segment as a key with zero id bits (0: fewer than k lanes hold
+// elements): k distinct elements reach it, so every element of the segment's
+// top-k does, and lies in a group whose maximum reaches it; and key(x) >= tau
+// exactly when x >= the value of tau. Those groups are read again (from the
+// stages, or from L2: the row was just streamed), their elements >= tau
+// collected, and the k largest keys found by rank selection into ctop. When the keys do not fit the scratch
 // (many equal values at the top), k block-wide rounds over the candidate
 // groups pick the keys one by one instead.
 template <int DT>
@@ -324,7 +348,7 @@ __device__ __forceinline__ void segment_topk(ExpandSmem& sm, const unsigned char
     constexpr int EPV = 16 / ES;
     constexpr int CE = kRowChunkBytes / ES;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const uint64_t tau = sm.tau;
+    const uint64_t tau = sm.tau;  // zero id bits: key(x) >= tau exactly when x >= tv
     const float tv = key_val(tau);
     const bool all = tau == 0ull;
     const uint32_t tau_o = static_cast<uint32_t>(tau >> 32);
@@ -360,20 +384,17 @@ __device__ __forceinline__ void segment_topk(ExpandSmem& sm, const unsigned char
         const uint4 u = resident ? reinterpret_cast<const uint4*>(stages)[(id0 - c0) / EPV]
                                  : __ldcg(reinterpret_cast<const uint4*>(row_base + static_cast<size_t>(id0) * ES));
         unpack16<DT>(u, x);
-        int mine = 0;
+        uint32_t mask = 0;  // bit e: element e is a key >= tau (NaN never is)
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) mask |= static_cast<uint32_t>(all ? x[e] == x[e] : x[e] >= tv) << e;
+        if (mask == 0u) continue;
+        int at = atomicAdd(&sm.nkeys, __popc(mask));
 #pragma unroll
         for (int e = 0; e < EPV; ++e)
-            mine += (all || x[e] >= tv) && x[e] == x[e] && make_key(x[e], static_cast<uint32_t>(id0 + e)) >= tau;
-        if (mine == 0) continue;
-        int at = atomicAdd(&sm.nkeys, mine);
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-            const uint64_t key = make_key(x[e], static_cast<uint32_t>(id0 + e));
-            if ((all || x[e] >= tv) && x[e] == x[e] && key >= tau) {
-                if (at < kcap) keys[at] = key;
+            if ((mask >> e) & 1u) {
+                if (at < kcap) keys[at] = make_key(x[e], static_cast<uint32_t>(id0 + e));
                 ++at;
             }
-        }
     }
     consumer_bar();
     const int nk = sm.nkeys;
@@ -434,38 +455,22 @@ __global__ void __launch_bounds__(kRowThreads, 5) expand_kernel(TreeDims d, Tree
     const int rank = static_cast<int>(cluster.block_rank());
     const int cpr = static_cast<int>(cluster.num_blocks());
     const int row = blockIdx.y;
-    const int b = row / d.k, f = row % d.k;
+    const int rps = step == 0 ? 1 : d.k;  // step 0 expands the root only: one row per sequence
+    const int b = row / rps, f = row % rps;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int ES = DT == 1 ? 2 : 4;
-    pdl_launch_dependents();
-    // the head of the segment into L2 while the previous kernel finishes (rows
-    // of slots that turn out empty are prefetched too: they are inside the input)
-    if (tid == kProducerWarp * 32) {
-        const int cp = rank * seg;
-        const int np = max(0, min(seg, d.V - cp));
-        prefetch_l2_segment(static_cast<const char*>(logits) + (static_cast<size_t>(row) * d.V + cp) * ES, np * ES);
-    }
-    pdl_wait_prior();
-    const int F = w.fcount[step * d.B + b];
     constexpr int EPV = 16 / ES;
     constexpr int CE = kRowChunkBytes / ES;  // elements per chunk
     const int k = d.k;
-
-    if (f >= F) {  // this frontier slot holds no node in this step
-        if (rank == 0 && tid == 0) {
-            row_lse[(static_cast<size_t>(b) * d.D + step) * d.k + f] = __int_as_float(0x7fc00000);
-            if (f == 0) {  // F == 0: nothing to expand, the next frontier is empty
-                fcount_out[b] = 0;
-                for (int j = 0; j < d.k; ++j) ftok_out[b * d.k + j] = -1;
-            }
-        }
-        return;
-    }
-
     const int c0 = rank * seg;
     const int n = max(0, min(seg, d.V - c0));
     const int nch = min(max_seg_chunks<DT>(), (n * ES + kRowChunkBytes - 1) / kRowChunkBytes);  // the launcher keeps within
     const char* row_base = static_cast<const char*>(logits) + static_cast<size_t>(b * d.k + f) * d.V * ES;
+    pdl_launch_dependents();
+    // Before the dependency wait: the head of the segment into L2 (a hint; a
+    // later write by the previous kernel still lands first), and every piece
+    // of state that does not depend on the previous kernel.
+    if (tid == kProducerWarp * 32) prefetch_l2_segment(row_base + static_cast<size_t>(c0) * ES, n * ES);
     if (tid == 0) {
         ring_init(sm.ring, ns);
         sm.tau = 0ull;
@@ -477,11 +482,28 @@ __global__ void __launch_bounds__(kRowThreads, 5) expand_kernel(TreeDims d, Tree
         sm.top[tid] = 0ull;
     }
     __syncthreads();
+    pdl_wait_prior();
 
     if (warp == kProducerWarp) {
-        // (starve: the failure-path test hook, no copy is issued and every ring wait gives up)
-        if (lane == 0 && nch > 0 && !starve)
+        // The copies start before the frontier count is known: a row past the
+        // count is streamed and dropped (all its copies land before the CTA
+        // exits). (starve: the failure-path test hook, no copy is issued and
+        // every ring wait gives up.)
+        if (lane == 0 && nch > 0 && !starve) {
             ring_produce(sm.ring, dyn_smem, row_base + static_cast<size_t>(c0) * ES, n * ES, nch, ns, w.status);
+        } else if (lane == 1) {
+            // the frontier count and this row's parent, read while the row streams
+            const int F = w.fcount[step * d.B + b];
+            int parent = -1;
+            float plogv = 0.0f;
+            if (rank == 0 && f < F) {
+                parent = w.fnode[(step * d.B + b) * d.k + f];
+                if (parent >= 0) plogv = w.cand_logv[static_cast<size_t>(b) * d.C + parent];
+            }
+            sm.F = F;
+            sm.parent = parent;
+            sm.plogv = plogv;
+        }
         __syncwarp();
     } else {
         // ---- one pass: lane maxima, online exp-sum, group maxima ----
@@ -520,11 +542,10 @@ __global__ void __launch_bounds__(kRowThreads, 5) expand_kernel(TreeDims d, Tree
                 s_l += f2_lo(sab) + f2_hi(sab);
             }
         }
-        // tau: the warp's k-th largest lane maximum (0 bits: fewer than k lanes hold elements)
+        // each warp's k largest lane maxima (0 bits: a lane without elements)
         const uint32_t lo = warp_sort_desc_u32(m_l > -INFINITY || (nch > 0 && warp * kVecPerWarp + lane < n / EPV)
                                                    ? f2o(m_l) : 0u);
-        const uint32_t kth = __shfl_sync(0xffffffffu, lo, k - 1);
-        if (lane == 0 && kth != 0u) atomicMax(&sm.tau, static_cast<unsigned long long>(kth) << 32);
+        if (lane < kMaxTopK) sm.wtop[warp][lane] = lane < k ? lo : 0u;
         // the warp's (max, sum)
         float sw = do_sum ? s_l : 0.0f, mw = m_l;
 #pragma unroll
@@ -543,11 +564,40 @@ __global__ void __launch_bounds__(kRowThreads, 5) expand_kernel(TreeDims d, Tree
             sm.ws[warp] = sw;
         }
         consumer_bar();
+        // tau: the k-th largest of the warps' lists (each zero-padded): entry t
+        // ranks by the entries above it (larger, or equal and earlier)
+        if (tid < kConsumerWarps * kMaxTopK) {
+            const uint32_t v = (&sm.wtop[0][0])[tid];
+            if (v != 0u) {
+                const uint4* p = reinterpret_cast<const uint4*>(&sm.wtop[0][0]);
+                int r = 0;
+#pragma unroll
+                for (int q = 0; q < kConsumerWarps * kMaxTopK / 4; ++q) {
+                    const uint4 a = p[q];
+                    r += (a.x > v || (a.x == v && 4 * q + 0 < tid)) + (a.y > v || (a.y == v && 4 * q + 1 < tid)) +
+                         (a.z > v || (a.z == v && 4 * q + 2 < tid)) + (a.w > v || (a.w == v && 4 * q + 3 < tid));
+                }
+                if (r == k - 1) sm.tau = static_cast<unsigned long long>(v) << 32;
+            }
+        }
+        consumer_bar();
         // a segment of at most ns chunks stays in the stages; the scratch then follows them
         const bool resident = nch <= ns;
         const int scratch_off = resident ? ns * kRowChunkBytes : 0;
         segment_topk<DT>(sm, dyn_smem, resident, dyn_smem + scratch_off, smem_bytes - scratch_off, row_base, c0, n,
                          nch, k);
+    }
+    __syncthreads();
+    const int F = sm.F;
+    if (f >= F) {  // this frontier slot holds no node in this step (every CTA of the cluster leaves here)
+        if (rank == 0 && tid == 0) {
+            row_lse[(static_cast<size_t>(b) * d.D + step) * d.k + f] = __int_as_float(0x7fc00000);
+            if (f == 0) {  // F == 0: nothing to expand, the next frontier is empty
+                fcount_out[b] = 0;
+                for (int j = 0; j < d.k; ++j) ftok_out[b * d.k + j] = -1;
+            }
+        }
+        return;
     }
     __syncthreads();
     ExpandSmem* leader = cluster.map_shared_rank(&sm, 0);
@@ -587,8 +637,8 @@ __global__ void __launch_bounds__(kRowThreads, 5) expand_kernel(TreeDims d, Tree
 
     // Children of this frontier node.
     const float lse = lse_in != nullptr ? lse_in[b * d.k + f] : sm.wm[0] + logf(sm.ws[0]);
-    const int parent = w.fnode[(step * d.B + b) * d.k + f];
-    const float plogv = parent < 0 ? 0.0f : w.cand_logv[static_cast<size_t>(b) * d.C + parent];
+    const int parent = sm.parent;
+    const float plogv = sm.plogv;
     const int base = step == 0 ? 0 : d.k + (step - 1) * d.k * d.k;
     if (tid < d.k) {
         const uint64_t key = sm.top[tid];
@@ -609,6 +659,8 @@ __global__ void __launch_bounds__(kRowThreads, 5) expand_kernel(TreeDims d, Tree
         row_lse[(static_cast<size_t>(b) * d.D + step) * d.k + f] = lse;
         if (!isfinite(lse)) raise_status(w.status, kDevNonFinite);
     }
+    if (step == 0 && tid > 0 && tid < d.k)  // rows 1.. of step 0 are not read (not launched)
+        row_lse[static_cast<size_t>(b) * d.D * d.k + tid] = __int_as_float(0x7fc00000);
     __syncthreads();
 
     // Per-sequence ticket: the last row of this sequence picks the next frontier.
@@ -619,7 +671,8 @@ __global__ void __launch_bounds__(kRowThreads, 5) expand_kernel(TreeDims d, Tree
     __syncthreads();
     if (!sm.last) return;
     const int nsel = F * d.k;
-    // the ring is idle now: candidate keys, their tokens, the chosen tokens
+    // the ring is idle now: candidate keys (zero-padded to a multiple of 8),
+    // their tokens, the chosen tokens
     uint64_t* sel = reinterpret_cast<uint64_t*>(dyn_smem);
     int32_t* sel_tok = reinterpret_cast<int32_t*>(dyn_smem + kMaxTopK * kMaxTopK * sizeof(uint64_t));
     int32_t* top_tok = sel_tok + kMaxTopK * kMaxTopK;
@@ -636,18 +689,13 @@ __global__ void __launch_bounds__(kRowThreads, 5) expand_kernel(TreeDims d, Tree
         sel_tok[i] = __ldcg(&w.cand_token[at]);
         sel[i] = (valid && lv >= d.log_thr) ? make_key(rank_by, static_cast<uint32_t>(id)) : 0ull;
     }
-    if (tid == 0 && (nsel & 1)) sel[nsel] = 0ull;  // pad to pairs
+    if (tid >= nsel && tid < (nsel + 7) / 8 * 8) sel[tid] = 0ull;  // padding
     if (tid < kMaxTopK) sm.top[tid] = 0ull;
     __syncthreads();
-    const ulonglong2* sp = reinterpret_cast<const ulonglong2*>(sel);
     for (int i = tid; i < nsel; i += kRowThreads) {
         const uint64_t key = sel[i];
         if (key == 0ull) continue;
-        int r = 0;
-        for (int j = 0; j < (nsel + 1) / 2; ++j) {
-            const ulonglong2 q = sp[j];
-            r += (q.x > key) + (q.y > key);
-        }
+        const int r = rank_in_list(sel, nsel, key);
         if (r < d.k) {
             sm.top[r] = key;
             top_tok[r] = sel_tok[i];
@@ -1230,7 +1278,7 @@ static cudaError_t launch_rows(K kernel, dim3 grid, int cpr, int smem, cudaStrea
 cudaError_t launch_expand(const TreeDims& d, const TreeWs& ws, int step, const void* logits, const float* lse_in,
                           float* row_lse, int32_t* ftok, int32_t* fcount_out, cudaStream_t stream, bool starve_ring) {
     const int esize = d.dtype == 1 ? 2 : 4;
-    const long rows = static_cast<long>(d.B) * d.k;
+    const long rows = static_cast<long>(d.B) * (step == 0 ? 1 : d.k);  // step 0 reads the root rows only
     const int max_seg = esize == 2 ? kMaxSegChunksBf16 : kMaxSegChunks;
     RowPlan p = plan_rows(d.V, esize, rows, false, kExpandStages, kMaxSegChunks);
     // Rows enough to fill every CTA slot once (three to five per SM, five
@@ -1265,7 +1313,7 @@ cudaError_t launch_expand(const TreeDims& d, const TreeWs& ws, int step, const v
         }
     }
     if (p.nch > max_seg) return cudaErrorInvalidValue;
-    dim3 grid(p.cpr, d.B * d.k, 1);
+    dim3 grid(p.cpr, step == 0 ? d.B : d.B * d.k, 1);  // step 0: the root row of each sequence
     TreeDims dd = d;
     TreeWs ww = ws;
     // after the pass the stage memory holds the candidate groups and keys of
