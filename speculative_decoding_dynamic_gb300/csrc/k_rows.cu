@@ -760,14 +760,27 @@ __device__ __forceinline__ uint64_t fixed_mass(float x, float m, float inv_t) {
     return sh >= 0 ? static_cast<uint64_t>(sig) << sh : static_cast<uint64_t>(sig >> (-sh));
 }
 
-// The masses of two elements at once: the same fixed-order exp, its fp32
-// operations done as packed pairs (each lane of a pair rounds exactly as the
-// scalar operation), then per element the significand placed 24 bits up and
-// shifted right by 24 - (exponent + n + 17), i.e. floor(p * 2^(n + 40)); an
-// argument below -32 shifts everything out. Equal to fixed_mass(x0) +
-// fixed_mass(x1).
-__device__ __forceinline__ uint64_t pair_mass(float x0, float x1, uint64_t neg_m2, uint64_t inv_t2) {
-    const uint64_t z = f2_mul(f2_add(f2_pack(x0, x1), neg_m2), inv_t2);
+__device__ __forceinline__ uint64_t f2_add_rz(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// The masses of two elements at once, in two parts. The fixed-order exp's
+// fp32 operations run as packed pairs (each lane of a pair rounds exactly as
+// the scalar operation). Per element the mass is floor(f), f = p * 2^(n + 40)
+// < 2^41: n + 40 added to p's exponent field (exact: a normal float for
+// every argument in [-32, 0]); then hi = rz(f + 2^46) - 2^46 = floor(f / 2^23)
+// 2^23 and b = f - hi (both exact), lo = rz(b + 2^23) - 2^23 = floor(b), so
+// floor(f) = floor(f / 2^23) 2^23 + floor(b). The two parts of both elements
+// are added to *ahi (in units of 2^23, the float bits of rz(f + 2^46)
+// minus those of 2^46) and *alo (the bits of rz(b + 2^23) minus those of
+// 2^23). Arguments below -32 are clamped to -32, whose mass exp(-32) 2^40 < 1
+// is 0 as the definition's is for them. Equal to fixed_mass of each element.
+__device__ __forceinline__ void pair_mass_parts(float x0, float x1, uint64_t neg_m2, uint64_t inv_t2, uint32_t& ahi,
+                                                uint32_t& alo) {
+    uint64_t z = f2_mul(f2_add(f2_pack(x0, x1), neg_m2), inv_t2);
+    z = f2_pack(fmaxf(f2_lo(z), -32.0f), fmaxf(f2_hi(z), -32.0f));
     const uint64_t t = f2_fma(z, f2_pack(0x1.715476p+0f, 0x1.715476p+0f), f2_pack(12582912.0f, 12582912.0f));
     const uint64_t n = f2_add(t, f2_pack(-12582912.0f, -12582912.0f));
     uint64_t r = f2_fma(n, f2_pack(-0x1.62e4p-1f, -0x1.62e4p-1f), z);
@@ -779,23 +792,41 @@ __device__ __forceinline__ uint64_t pair_mass(float x0, float x1, uint64_t neg_m
     p = f2_fma(p, r, f2_pack(0.5f, 0.5f));
     p = f2_fma(p, r, f2_pack(1.0f, 1.0f));
     p = f2_fma(p, r, f2_pack(1.0f, 1.0f));
-    uint64_t s = 0;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const uint32_t pb = static_cast<uint32_t>(p >> (32 * h));
-        const uint32_t tb = static_cast<uint32_t>(t >> (32 * h));
-        const float zh = __uint_as_float(static_cast<uint32_t>(z >> (32 * h)));
-        // 24 - sh with sh = (pb >> 23) - 127 + (tb - 0x4B400000) + 17
-        int shr = 134 - static_cast<int>(pb >> 23) - (static_cast<int>(tb) - 0x4B400000);
-        if (!(zh >= -32.0f)) shr = 63;
-        const uint64_t sig48 = static_cast<uint64_t>((pb & 0x7FFFFFu) | 0x800000u) << 24;
-        s += sig48 >> shr;
-    }
-    return s;
+    // t's low word is n (t = 1.5 * 2^23 + n, exact), so t << 23 = n << 23 modulo 2^32
+    const uint32_t f0 = static_cast<uint32_t>(p) + (static_cast<uint32_t>(t) << 23) + (40u << 23);
+    const uint32_t f1 = static_cast<uint32_t>(p >> 32) + (static_cast<uint32_t>(t >> 32) << 23) + (40u << 23);
+    const uint64_t f = (static_cast<uint64_t>(f1) << 32) | f0;
+    const uint64_t k46 = f2_pack(0x1p46f, 0x1p46f), k23 = f2_pack(0x1p23f, 0x1p23f);
+    const uint64_t x46 = f2_add_rz(f, k46);                                  // 2^46 + floor(f / 2^23) 2^23
+    const uint64_t b = f2_add(f, f2_add(k46, x46 ^ 0x8000000080000000ull));  // f - (x46 - 2^46), exact
+    const uint64_t x23 = f2_add_rz(b, k23);                                  // 2^23 + floor(b)
+    ahi += (static_cast<uint32_t>(x46) - 0x56800000u) + (static_cast<uint32_t>(x46 >> 32) - 0x56800000u);
+    alo += (static_cast<uint32_t>(x23) - 0x4B000000u) + (static_cast<uint32_t>(x23 >> 32) - 0x4B000000u);
+}
+
+// The integer mass of the parts: ahi 2^23 + alo.
+__device__ __forceinline__ uint64_t mass_of_parts(uint32_t ahi, uint32_t alo) {
+    return (static_cast<uint64_t>(ahi) << 23) + alo;
+}
+
+// The masses of two elements, each on its own.
+__device__ __forceinline__ void pair_mass2(float x0, float x1, uint64_t neg_m2, uint64_t inv_t2, uint64_t& m0,
+                                           uint64_t& m1) {
+    uint32_t h0 = 0, l0 = 0, h1 = 0, l1 = 0;
+    pair_mass_parts(x0, -INFINITY, neg_m2, inv_t2, h0, l0);
+    pair_mass_parts(x1, -INFINITY, neg_m2, inv_t2, h1, l1);
+    m0 = mass_of_parts(h0, l0);
+    m1 = mass_of_parts(h1, l1);
 }
 
 struct VerifySmem {
     RowRing ring;
+    // walk inputs that do not depend on other rows, read by every leader
+    // while its row streams (the leader that arrives last walks the tree)
+    int tok[kMaxSlots];
+    int par[kMaxSlots];
+    float xtok[kMaxSlots];       // slot c's token logit in its parent's row (lossless)
+    uint32_t uni[kMaxSlots + 2];  // uniform words (lossless)
     uint64_t wkey[kConsumerWarps];
     unsigned long long wmass[kConsumerWarps];
     uint64_t rkey[kMaxChunks];   // every rank's segment maximum
@@ -806,20 +837,18 @@ struct VerifySmem {
 // Acceptance-walk state of the last-arriving CTA of a sequence; it lives in
 // the (then idle) dynamic shared memory of the chunk ring.
 struct WalkSmem {
-    int tok[kMaxSlots];
-    int par[kMaxSlots];
     int arg[kMaxSlots];
     float rmax[kMaxSlots];
     unsigned long long rowmass[kMaxSlots];
     unsigned long long pmass[kMaxSlots];  // mass of slot c's token in its parent's row
-    uint32_t uni[kMaxSlots + 2];
+    unsigned long long piece[kMaxChunks * kRowStages * kConsumerWarps];  // residual mass of each piece of row cur
     int path[kMaxDepth + 1];
     int child[kMaxTopK];
     int removed_tok[kMaxTopK];
     unsigned long long removed_mass[kMaxTopK];
     unsigned long long scan[4];
     unsigned long long t_in;
-    int n_removed, a, cur, bonus, bad, piece;
+    int n_removed, a, cur, bonus, bad, piece_at;
 };
 
 // Element range [lo, hi) of integer-mass piece q of a row: piece (rank, chunk,
@@ -878,8 +907,39 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
 
     bool failed = false;
     if (warp == kProducerWarp) {
-        if (lane == 0 && nch > 0)
+        if (lane == 0 && nch > 0) {
             ring_produce(sm.ring, dyn_smem, row_base + static_cast<size_t>(c0) * ES, len * ES, nch, ns, w.status);
+        } else if (MODE == 1 && rank == 0 && lane > 0) {
+            // Lossless: the walk's inputs that do not depend on other rows, read
+            // while the row streams (every leader, whose copies are all issued
+            // at once; the leader that arrives last walks).
+            const size_t tb = static_cast<size_t>(b) * d.T;
+            for (int c = lane - 1; c < n; c += 31) {
+                sm.tok[c] = tokens[tb + c];
+                sm.par[c] = parent[tb + c];
+            }
+            {
+                __syncwarp(0xfffffffeu);
+                for (int c = lane - 1; c < n; c += 31) {
+                    const int tk = sm.tok[c], p = sm.par[c];
+                    float x = 0.0f;
+                    if (c > 0 && tk >= 0 && tk < d.V && p >= 0 && p < c) {
+                        const char* prow = static_cast<const char*>(target) + (tb + p) * d.V * ES;
+                        x = DT == 1 ? __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(prow)[tk])
+                                                      << 16)
+                                    : reinterpret_cast<const float*>(prow)[tk];
+                    }
+                    sm.xtok[c] = x;
+                }
+                // uniform word c of sequence b: Philox4x32-10 at counter (c, b, cycle), word 0
+                for (int c = lane - 1; c < d.T + 2; c += 31) {
+                    const uint32_t ctr[4] = {static_cast<uint32_t>(c), static_cast<uint32_t>(b), rng.c2, rng.c3};
+                    uint32_t out[4];
+                    sampling::philox4x32_10(ctr, rng.k0, rng.k1, out);
+                    sm.uni[c] = out[0];
+                }
+            }
+        }
         __syncwarp();
     } else {
         // ---- pass 1: maximum, lowest id among equal values ----
@@ -939,7 +999,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
         const uint64_t neg_m2 = f2_pack(-M, -M), inv_t2 = f2_pack(inv_t, inv_t);
         if (warp < kConsumerWarps) {
             for (int c = 0; c < nch_full; ++c) {
-                unsigned long long s = 0;
+                uint32_t ahi = 0, alo = 0;  // the lane's masses in parts (at most 32 elements: no overflow)
                 if (c < nch && !failed) {
                     const int nvec = min(CE, len - c * CE) / EPV;
                     const uint4* vb = reinterpret_cast<const uint4*>(dyn_smem + c * kRowChunkBytes);
@@ -950,10 +1010,10 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
                         float x[EPV];
                         unpack16<DT>(vb[v], x);
 #pragma unroll
-                        for (int e = 0; e < EPV; e += 2) s += pair_mass(x[e], x[e + 1], neg_m2, inv_t2);
+                        for (int e = 0; e < EPV; e += 2) pair_mass_parts(x[e], x[e + 1], neg_m2, inv_t2, ahi, alo);
                     }
                 }
-                s = warp_sum_u64(s);
+                unsigned long long s = warp_sum_u64(mass_of_parts(ahi, alo));
                 if (lane == 0) w.chunk_mass[rt * nslot + (rank * nch_full + c) * kConsumerWarps + warp] = s;
                 wtot += s;
             }
@@ -987,42 +1047,29 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
     const int T = d.T;
     if (tid == 0) {
         ws.bad = 0;
-        ws.piece = -1;
+        ws.piece_at = -1;
         ws.n_removed = 0;
     }
-    for (int c = tid; c < T; c += kRowThreads) {
-        ws.tok[c] = c < n ? tokens[static_cast<size_t>(b) * T + c] : -1;
-        ws.par[c] = c < n ? parent[static_cast<size_t>(b) * T + c] : -1;
-        if (c < n) {
-            ws.arg[c] = __ldcg(&w.row_arg[static_cast<size_t>(b) * T + c]);
-            ws.rmax[c] = __ldcg(&w.row_max[static_cast<size_t>(b) * T + c]);
-            ws.rowmass[c] = __ldcg(&w.row_mass[static_cast<size_t>(b) * T + c]);
+    // the other rows' statistics (lossless: this CTA's tokens, parents, token
+    // logits and uniforms are already in sm)
+    for (int c = tid; c < n; c += kRowThreads) {
+        if (MODE == 0) {
+            sm.tok[c] = tokens[static_cast<size_t>(b) * T + c];
+            sm.par[c] = parent[static_cast<size_t>(b) * T + c];
         }
+        ws.arg[c] = __ldcg(&w.row_arg[static_cast<size_t>(b) * T + c]);
+        ws.rmax[c] = __ldcg(&w.row_max[static_cast<size_t>(b) * T + c]);
+        ws.rowmass[c] = __ldcg(&w.row_mass[static_cast<size_t>(b) * T + c]);
     }
-    if (MODE == 1)  // uniform word c of sequence b: Philox4x32-10 at counter (c, b, cycle), word 0
-        for (int c = tid; c < T + 2; c += kRowThreads) {
-            const uint32_t ctr[4] = {static_cast<uint32_t>(c), static_cast<uint32_t>(b), rng.c2, rng.c3};
-            uint32_t out[4];
-            sampling::philox4x32_10(ctr, rng.k0, rng.k1, out);
-            ws.uni[c] = out[0];
-        }
     __syncthreads();
     for (int c = 1 + tid; c < n; c += kRowThreads) {
-        const int tk = ws.tok[c], p = ws.par[c];
+        const int tk = sm.tok[c], p = sm.par[c];
         ws.pmass[c] = 0;
         if (tk < 0 || tk >= d.V || p < 0 || p >= c) {
             ws.bad = 1;
             continue;
         }
-        if (MODE == 1) {
-            const char* prow = static_cast<const char*>(target) + (static_cast<size_t>(b) * T + p) * d.V * ES;
-            float x;
-            if (DT == 1)
-                x = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(prow)[tk]) << 16);
-            else
-                x = reinterpret_cast<const float*>(prow)[tk];
-            ws.pmass[c] = fixed_mass(x, ws.rmax[p], inv_t);
-        }
+        if (MODE == 1) ws.pmass[c] = fixed_mass(sm.xtok[c], ws.rmax[p], inv_t);
     }
     __syncthreads();
     const bool bad = ws.bad != 0;
@@ -1038,7 +1085,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
             int nchild = 0;
             for (int c0w = cur + 1; c0w < n; c0w += 32) {
                 const int c = c0w + lane;
-                const bool is = c < n && ws.par[c] == cur;
+                const bool is = c < n && sm.par[c] == cur;
                 const unsigned bal = __ballot_sync(0xffffffffu, is);
                 if (is) {
                     const int pos = nchild + __popc(bal & lanemask_lt());
@@ -1052,7 +1099,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
             const int c = lane < nchild ? ws.child[lane] : -1;
             int next = -1;
             if (MODE == 0) {
-                const unsigned bal = __ballot_sync(0xffffffffu, c >= 0 && ws.tok[c] == ws.arg[cur]);
+                const unsigned bal = __ballot_sync(0xffffffffu, c >= 0 && sm.tok[c] == ws.arg[cur]);
                 if (bal) next = ws.child[__ffs(bal) - 1];
             } else {
                 const unsigned long long P = c >= 0 ? ws.pmass[c] : 0ull;
@@ -1063,7 +1110,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
                     if (lane >= o) incl += y;
                 }
                 const unsigned long long Sj = S - (incl - P);  // after the earlier children's removal
-                const bool acc = c >= 0 && static_cast<unsigned __int128>(ws.uni[c] >> 8) * Sj <
+                const bool acc = c >= 0 && static_cast<unsigned __int128>(sm.uni[c] >> 8) * Sj <
                                                (static_cast<unsigned __int128>(P) << 24);
                 const unsigned bal = __ballot_sync(0xffffffffu, acc);
                 if (bal) {
@@ -1071,7 +1118,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
                 } else {
                     S -= shfl_u64(incl, 31);  // every child rejected: their tokens leave the residual
                     if (c >= 0) {
-                        ws.removed_tok[lane] = ws.tok[c];
+                        ws.removed_tok[lane] = sm.tok[c];
                         ws.removed_mass[lane] = P;
                     }
                     if (lane == 0) ws.n_removed = nchild;
@@ -1088,28 +1135,36 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
             ws.a = a;
             ws.cur = cur;
             ws.bonus = MODE == 0 ? ws.arg[cur] : -1;
+            if (MODE == 1) {  // the draw t = floor(U64 * S / 2^64) on the residual of row cur
+                const uint64_t U64 = (static_cast<uint64_t>(sm.uni[T + 1]) << 32) | sm.uni[T];
+                ws.t_in = static_cast<unsigned long long>((static_cast<unsigned __int128>(U64) * S) >> 64);
+            }
         }
-        if (MODE == 1 && !bad) {
-            // the piece of row `cur` that holds the draw t = floor(U64 * S / 2^64)
-            const uint64_t U64 = (static_cast<uint64_t>(ws.uni[T + 1]) << 32) | ws.uni[T];
-            const unsigned long long tdraw =
-                static_cast<unsigned long long>((static_cast<unsigned __int128>(U64) * S) >> 64);
-            const int nrem = ws.n_removed;
-            const int nch_full = nslot / (cpr * kConsumerWarps);
-            const uint64_t* pm = w.chunk_mass + (static_cast<size_t>(b) * T + cur) * nslot;
+    }
+    __syncthreads();
+
+    if (MODE == 1 && !bad) {
+        const int cur = ws.cur;
+        const int nrem = ws.n_removed;
+        const int nch_full = nslot / (cpr * kConsumerWarps);
+        // the residual mass of every piece of row cur (one piece per thread, one round trip)
+        for (int q = tid; q < nslot; q += kRowThreads) {
+            unsigned long long m = __ldcg(w.chunk_mass + (static_cast<size_t>(b) * T + cur) * nslot + q);
+            int lo, hi;
+            piece_range(q, nch_full, seg, d.V, CE, EPV, lo, hi);
+            for (int r = 0; r < nrem; ++r)
+                if (ws.removed_tok[r] >= lo && ws.removed_tok[r] < hi) m -= ws.removed_mass[r];
+            ws.piece[q] = m;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // the piece that holds the draw: lane l sums pieces [l * per, (l + 1) * per)
             const int per = (nslot + 31) / 32;
-            auto piece_mass = [&](int q) -> unsigned long long {
-                unsigned long long m = __ldcg(pm + q);
-                int lo, hi;
-                piece_range(q, nch_full, seg, d.V, CE, EPV, lo, hi);
-                for (int r = 0; r < nrem; ++r)
-                    if (ws.removed_tok[r] >= lo && ws.removed_tok[r] < hi) m -= ws.removed_mass[r];
-                return m;
-            };
+            const unsigned long long tdraw = ws.t_in;
             unsigned long long loc = 0;
             for (int i = 0; i < per; ++i) {
                 const int q = lane * per + i;
-                if (q < nslot) loc += piece_mass(q);
+                if (q < nslot) loc += ws.piece[q];
             }
             unsigned long long incl = loc;
 #pragma unroll
@@ -1122,9 +1177,9 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
                 for (int i = 0; i < per; ++i) {
                     const int q = lane * per + i;
                     if (q >= nslot) break;
-                    const unsigned long long m = piece_mass(q);
+                    const unsigned long long m = ws.piece[q];
                     if (run + m > tdraw) {
-                        ws.piece = q;
+                        ws.piece_at = q;
                         ws.t_in = tdraw - run;
                         break;
                     }
@@ -1132,20 +1187,14 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
                 }
             }
         }
-    }
-    __syncthreads();
-
-    if (MODE == 1) {
+        __syncthreads();
         // Smallest y of the chosen piece (not removed) whose running mass
         // exceeds the draw: one 16-byte vector per thread, block scan.
-        const int q = ws.piece;
-        const int cur = ws.cur;
-        const int nch_full = nslot / (cpr * kConsumerWarps);
+        const int q = ws.piece_at;
         int lo = 0, hi = 0;
         if (q >= 0) piece_range(q, nch_full, seg, d.V, CE, EPV, lo, hi);
-        const int nrem = ws.n_removed;
         const float m = ws.rmax[cur];
-        unsigned long long em[EPV];
+        uint64_t em[EPV];
         unsigned long long mv = 0;
         const int y0 = lo + tid * EPV;
         if (tid < kVecPerWarp && y0 < hi) {
@@ -1153,9 +1202,11 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
             const uint4 u = __ldcg(reinterpret_cast<const uint4*>(crow + static_cast<size_t>(y0) * ES));
             float x[EPV];
             unpack16<DT>(u, x);
+            const uint64_t neg_m2 = f2_pack(-m, -m), inv_t2 = f2_pack(inv_t, inv_t);
+#pragma unroll
+            for (int e = 0; e < EPV; e += 2) pair_mass2(x[e], x[e + 1], neg_m2, inv_t2, em[e], em[e + 1]);
 #pragma unroll
             for (int e = 0; e < EPV; ++e) {
-                em[e] = fixed_mass(x[e], m, inv_t);
                 for (int r = 0; r < nrem; ++r)
                     if (ws.removed_tok[r] == y0 + e) em[e] = 0;
                 mv += em[e];
@@ -1194,7 +1245,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
         accept_len[b] = a;
         for (int j = 0; j < Dp1; ++j) {
             slots_out[b * Dp1 + j] = j <= a ? ws.path[j] : -1;
-            tokens_out[b * Dp1 + j] = j < a ? ws.tok[ws.path[j + 1]] : (j == a ? ws.bonus : -1);
+            tokens_out[b * Dp1 + j] = j < a ? sm.tok[ws.path[j + 1]] : (j == a ? ws.bonus : -1);
         }
         if (ws.bonus < 0) raise_status(w.status, kDevBadIndex);
         w.verify_ticket[b] = 0;
