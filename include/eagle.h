@@ -282,6 +282,58 @@ int eagle_verify(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int mode,
 int eagle_kv_compact(const eagle_kv_cfg* kv, void* kv_cache, const int32_t* prefix_len, const int32_t* accept_len,
                      const int32_t* accepted_slots, int slots_stride, int32_t* new_len, void* ws, void* stream);
 
+/* ------------------------------------------------- vocabulary shards --- */
+/*
+ * When the LM head is split over several GPUs by vocabulary rows, each GPU
+ * holds a slice [vocab_offset, vocab_offset + shard_vocab) of every logit row
+ * ["EAGLE" notes, EAGLE 方法: the top-k is taken over the whole vocabulary;
+ * how the vocabulary is split is not on the pages]. Stage 1 and the greedy
+ * verify then run on each slice into small partials, one exchange moves the
+ * partials of all slices to every GPU (for example an all-gather: k keys and
+ * two floats per row per slice), and eagle_shard_merge gives the whole row's
+ * results; eagle_expand_topk and eagle_verify_argmax continue from them.
+ *
+ * A key is the 64-bit (order-preserving bits of the logit) << 32 |
+ * (0xFFFFFFFF - token id): a larger key is a larger logit, then a lower token
+ * id; 0 = no key.
+ */
+
+/* Stage-1 partials of `rows` logit rows of one slice.
+ *   logits       [rows, shard_vocab] in cfg->logit_dtype, row starts 16-byte aligned.
+ *   part_max_sum [rows, 2] fp32 out: the slice's maximum M_s and sum of exp(x - M_s).
+ *   part_keys    [rows, 16] out: the slice's k largest keys, best first, 0 padding
+ *                (token ids of the whole vocabulary: vocab_offset + index).
+ * cfg->vocab is the whole vocabulary; vocab_offset + shard_vocab <= cfg->vocab. */
+int eagle_shard_partials(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int rows, int shard_vocab,
+                         int vocab_offset, const void* logits, float* part_max_sum, uint64_t* part_keys,
+                         void* stream);
+
+/* Merge of n_shards (<= 16) slices' partials, [n_shards, rows, ...] each:
+ *   row_lse     [rows] fp32: M + log(sum_s S_s exp(M_s - M)), M = max_s M_s (the
+ *               slices' terms added in slice order).
+ *   topk_ids    [rows, k] int32, topk_logits [rows, k] fp32: the k largest logits
+ *               of the whole row (equal logits: lower id), -1 / -inf padding.
+ *   row_argmax  [rows] int32: the largest logit's token (lowest id on ties).
+ * Equal to stage 1 of the whole row (top-k ids and argmax exactly; lse within
+ * fp32 rounding of the unsplit row's). */
+int eagle_shard_merge(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int n_shards, int rows,
+                      const float* part_max_sum, const uint64_t* part_keys, float* row_lse, int32_t* topk_ids,
+                      float* topk_logits, int32_t* row_argmax, void* stream);
+
+/* Stage 2 of draft step `step` from merged stage-1 results (one CTA per
+ * sequence): topk_ids / topk_logits [B, k, k] (row f = frontier slot f, as
+ * eagle_shard_merge writes for the step's [B * k] rows), row_lse_in [B, k].
+ * Children, values, threshold and next frontier exactly as eagle_expand. */
+int eagle_expand_topk(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int step, const int32_t* topk_ids,
+                      const float* topk_logits, const float* row_lse_in, float* row_lse, int32_t* frontier_tokens,
+                      int32_t* frontier_count, void* stream);
+
+/* Greedy stage 6 from the target's argmax of every slot, row_argmax [B, T]
+ * (merged over the slices): the walk and outputs of eagle_verify GREEDY. */
+int eagle_verify_argmax(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, const int32_t* row_argmax,
+                        const int32_t* tokens, const int32_t* parent, const int32_t* n_tree, int32_t* accept_len,
+                        int32_t* accepted_slots, int32_t* out_tokens, void* stream);
+
 /*
  * eagle_verify without a workspace, for callers that may not allocate device
  * memory (for example a plugin whose host engine plans all GPU memory up

@@ -239,6 +239,70 @@ int eagle_verify(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int mode,
                                        static_cast<cudaStream_t>(stream)));
 }
 
+int eagle_shard_partials(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int rows, int shard_vocab,
+                         int vocab_offset, const void* logits, float* part_max_sum, uint64_t* part_keys,
+                         void* stream) {
+    TreeDims d;
+    TreeWs w;
+    int rc = resolve(cfg, &d);
+    if (rc == EAGLE_OK) rc = bind_ws(d, ws, ws_bytes, &w);
+    if (rc != EAGLE_OK) return rc;
+    if (!logits || !part_max_sum || !part_keys || rows < 1 || rows > 65535 || shard_vocab < 1 || vocab_offset < 0 ||
+        static_cast<long>(vocab_offset) + shard_vocab > d.V)
+        return EAGLE_ERR_INVALID_ARG;
+    const int esize = d.dtype == EAGLE_BF16 ? 2 : 4;
+    if ((static_cast<long>(shard_vocab) * esize) % 16 != 0 || !aligned16(logits)) return EAGLE_ERR_UNSUPPORTED;
+    return launch_result(launch_shard_partials(shard_vocab, d.k, rows, d.dtype, logits, vocab_offset,
+                                               reinterpret_cast<float2*>(part_max_sum), part_keys, w.status,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
+int eagle_shard_merge(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int n_shards, int rows,
+                      const float* part_max_sum, const uint64_t* part_keys, float* row_lse, int32_t* topk_ids,
+                      float* topk_logits, int32_t* row_argmax, void* stream) {
+    TreeDims d;
+    TreeWs w;
+    int rc = resolve(cfg, &d);
+    if (rc == EAGLE_OK) rc = bind_ws(d, ws, ws_bytes, &w);
+    if (rc != EAGLE_OK) return rc;
+    if (!part_max_sum || !part_keys || !row_lse || !topk_ids || !topk_logits || !row_argmax || rows < 1 ||
+        n_shards < 1)
+        return EAGLE_ERR_INVALID_ARG;
+    if (n_shards > kShardMax) return EAGLE_ERR_UNSUPPORTED;
+    return launch_result(launch_shard_merge(n_shards, rows, d.k, reinterpret_cast<const float2*>(part_max_sum),
+                                            part_keys, row_lse, topk_ids, topk_logits, row_argmax, w.status,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+int eagle_expand_topk(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int step, const int32_t* topk_ids,
+                      const float* topk_logits, const float* row_lse_in, float* row_lse, int32_t* frontier_tokens,
+                      int32_t* frontier_count, void* stream) {
+    TreeDims d;
+    TreeWs w;
+    int rc = resolve(cfg, &d);
+    if (rc == EAGLE_OK) rc = bind_ws(d, ws, ws_bytes, &w);
+    if (rc != EAGLE_OK) return rc;
+    if (step < 0 || step >= d.D) return EAGLE_ERR_INVALID_ARG;
+    if (!topk_ids || !topk_logits || !row_lse_in || !row_lse || !frontier_tokens || !frontier_count)
+        return EAGLE_ERR_INVALID_ARG;
+    return launch_result(launch_expand_topk(d, w, step, topk_ids, topk_logits, row_lse_in, row_lse, frontier_tokens,
+                                            frontier_count, static_cast<cudaStream_t>(stream)));
+}
+
+int eagle_verify_argmax(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, const int32_t* row_argmax,
+                        const int32_t* tokens, const int32_t* parent, const int32_t* n_tree, int32_t* accept_len,
+                        int32_t* accepted_slots, int32_t* out_tokens, void* stream) {
+    TreeDims d;
+    TreeWs w;
+    int rc = resolve(cfg, &d);
+    if (rc == EAGLE_OK) rc = bind_ws(d, ws, ws_bytes, &w);
+    if (rc != EAGLE_OK) return rc;
+    if (!row_argmax || !tokens || !parent || !n_tree || !accept_len || !accepted_slots || !out_tokens)
+        return EAGLE_ERR_INVALID_ARG;
+    return launch_result(launch_verify_argmax(d, w, row_argmax, tokens, parent, n_tree, accept_len, accepted_slots,
+                                              out_tokens, static_cast<cudaStream_t>(stream)));
+}
+
 int eagle_kv_compact(const eagle_kv_cfg* kv, void* kv_cache, const int32_t* prefix_len, const int32_t* accept_len,
                      const int32_t* accepted_slots, int slots_stride, int32_t* new_len, void* ws, void* stream) {
     KvDims k;

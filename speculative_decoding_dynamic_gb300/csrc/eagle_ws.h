@@ -145,6 +145,21 @@ cudaError_t launch_verify(const TreeDims& d, const TreeWs& ws, int mode, float i
                           const int32_t* tokens, const int32_t* parent, const int32_t* n_tree, VerifyRng rng,
                           int32_t* accept_len, int32_t* slots, int32_t* out_tokens, cudaStream_t stream);
 
+// Vocabulary slices: stage-1 partials of `rows` rows of a slice [rows, Vs]
+// (keys carry token id id_base + index), their merge over S slices, stage 2
+// from merged top-k, and the greedy walk from merged argmax.
+constexpr int kShardMax = 16;
+cudaError_t launch_shard_partials(int Vs, int k, int rows, int dtype, const void* logits, int id_base, float2* part_ms,
+                                  uint64_t* part_keys, int* status, cudaStream_t stream);
+cudaError_t launch_shard_merge(int S, int rows, int k, const float2* part_ms, const uint64_t* part_keys, float* lse,
+                               int32_t* topk_id, float* topk_val, int32_t* argmax, int* status, cudaStream_t stream);
+cudaError_t launch_expand_topk(const TreeDims& d, const TreeWs& ws, int step, const int32_t* topk_id,
+                               const float* topk_val, const float* lse_in, float* row_lse, int32_t* ftok,
+                               int32_t* fcount_out, cudaStream_t stream);
+cudaError_t launch_verify_argmax(const TreeDims& d, const TreeWs& ws, const int32_t* row_argmax, const int32_t* tokens,
+                                 const int32_t* parent, const int32_t* n_tree, int32_t* accept_len, int32_t* slots,
+                                 int32_t* out_tokens, cudaStream_t stream);
+
 struct KvDims {
     int B, Hq, Hkv, d, layers, max_len, dtype;
     int64_t seq_stride, layer_stride, kv_stride, pos_stride;

@@ -343,7 +343,7 @@ __device__ __forceinline__ uint32_t gmax_floor(uint32_t o) { return DT == 1 ? (o
 template <int DT>
 __device__ __forceinline__ void segment_topk(ExpandSmem& sm, const unsigned char* stages, bool resident,
                                              unsigned char* scratch, int scratch_bytes, const char* row_base, int c0,
-                                             int n, int nch, int k) {
+                                             int n, int nch, int k, int id_base) {
     constexpr int ES = DT == 1 ? 2 : 4;
     constexpr int EPV = 16 / ES;
     constexpr int CE = kRowChunkBytes / ES;
@@ -392,7 +392,7 @@ __device__ __forceinline__ void segment_topk(ExpandSmem& sm, const unsigned char
 #pragma unroll
         for (int e = 0; e < EPV; ++e)
             if ((mask >> e) & 1u) {
-                if (at < kcap) keys[at] = make_key(x[e], static_cast<uint32_t>(id0 + e));
+                if (at < kcap) keys[at] = make_key(x[e], static_cast<uint32_t>(id_base + id0 + e));
                 ++at;
             }
     }
@@ -426,7 +426,7 @@ __device__ __forceinline__ void segment_topk(ExpandSmem& sm, const unsigned char
 #pragma unroll
             for (int e = 0; e < EPV; ++e) {
                 if (x[e] != x[e]) continue;
-                const uint64_t key = make_key(x[e], static_cast<uint32_t>(id0 + e));
+                const uint64_t key = make_key(x[e], static_cast<uint32_t>(id_base + id0 + e));
                 if (key < prev && key > best) best = key;
             }
         }
@@ -440,6 +440,141 @@ __device__ __forceinline__ void segment_topk(ExpandSmem& sm, const unsigned char
         prev = best;
         if (best == 0) break;
     }
+}
+
+// The consumer warps' part of one CTA's row segment (expansion and vocabulary
+// shards): one pass over the streamed chunks for the lane maxima, the online
+// exp-sum (when do_sum) and the group maxima; then tau and the segment's top-k
+// keys into sm.ctop (token ids id_base + element index in the row), and the
+// warps' (max, sum) into sm.wm / sm.ws.
+template <int DT>
+__device__ __forceinline__ void segment_consume(ExpandSmem& sm, unsigned char* dyn_smem, int smem_bytes, int ns,
+                                                const char* row_base, int c0, int n, int nch, int k, bool do_sum,
+                                                int id_base, int* status) {
+    constexpr int ES = DT == 1 ? 2 : 4;
+    constexpr int EPV = 16 / ES;
+    constexpr int CE = kRowChunkBytes / ES;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // ---- one pass: lane maxima, online exp-sum, group maxima ----
+    float m_l = -INFINITY, s_l = 0.0f;  // lane: running max and sum of exp(x - m_l)
+    bool failed = false;
+    for (int c = 0; c < nch; ++c) {
+        const bool ok = ring_wait(sm.ring, c, ns, failed, status);
+        const int nvec = ok ? min(CE, n - c * CE) / EPV : 0;
+        uint4 u[kVecPerLane];
+        load_lane<DT>(dyn_smem + (c % ns) * kRowChunkBytes, nvec, warp, lane, u);
+        ring_release(sm.ring, c, ns);
+        const float cm = lane_max4<DT>(u);
+        gmax_put<DT>(sm, c, tid, warp * kVecPerWarp + lane < nvec ? f2o(cm) : 0u);
+        if (cm > m_l) {
+            s_l = (do_sum && m_l > -INFINITY) ? s_l * ex2_approx((m_l - cm) * kLog2e) : 0.0f;
+            m_l = cm;
+        }
+        if (do_sum && m_l > -INFINITY) {
+            // even and odd elements summed apart, as packed fp32 pairs (one
+            // multiply-add and one add per two elements, each lane's result
+            // the scalar operation's)
+            const float mb = m_l * kLog2e;
+            const uint64_t l2 = f2_pack(kLog2e, kLog2e), nmb = f2_pack(-mb, -mb);
+            uint64_t sab = 0ull;  // (even sum, odd sum)
+#pragma unroll
+            for (int j = 0; j < kVecPerLane; ++j) {
+                float x[EPV];
+                unpack16<DT>(u[j], x);
+#pragma unroll
+                for (int e = 0; e < EPV; e += 2) {
+                    const uint64_t z = f2_fma(f2_pack(x[e], x[e + 1]), l2, nmb);
+                    sab = f2_add(sab, f2_pack(ex2_approx(f2_lo(z)), ex2_approx(f2_hi(z))));
+                }
+            }
+            s_l += f2_lo(sab) + f2_hi(sab);
+        }
+    }
+    // each warp's k largest lane maxima (0 bits: a lane without elements)
+    const uint32_t lo = warp_sort_desc_u32(m_l > -INFINITY || (nch > 0 && warp * kVecPerWarp + lane < n / EPV)
+                                               ? f2o(m_l) : 0u);
+    if (lane < kMaxTopK) sm.wtop[warp][lane] = lane < k ? lo : 0u;
+    // the warp's (max, sum)
+    float sw = do_sum ? s_l : 0.0f, mw = m_l;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float mo = __shfl_xor_sync(0xffffffffu, mw, o);
+        const float so = __shfl_xor_sync(0xffffffffu, sw, o);
+        const float M = fmaxf(mw, mo);
+        float sum = 0.0f;
+        if (mw > -INFINITY) sum += sw * ex2_approx((mw - M) * kLog2e);
+        if (mo > -INFINITY) sum += so * ex2_approx((mo - M) * kLog2e);
+        mw = M;
+        sw = sum;
+    }
+    if (lane == 0) {
+        sm.wm[warp] = mw;
+        sm.ws[warp] = sw;
+    }
+    consumer_bar();
+    // tau: the k-th largest of the warps' lists (each zero-padded): entry t
+    // ranks by the entries above it (larger, or equal and earlier)
+    if (tid < kConsumerWarps * kMaxTopK) {
+        const uint32_t v = (&sm.wtop[0][0])[tid];
+        if (v != 0u) {
+            const uint4* p = reinterpret_cast<const uint4*>(&sm.wtop[0][0]);
+            int r = 0;
+#pragma unroll
+            for (int q = 0; q < kConsumerWarps * kMaxTopK / 4; ++q) {
+                const uint4 a = p[q];
+                r += (a.x > v || (a.x == v && 4 * q + 0 < tid)) + (a.y > v || (a.y == v && 4 * q + 1 < tid)) +
+                     (a.z > v || (a.z == v && 4 * q + 2 < tid)) + (a.w > v || (a.w == v && 4 * q + 3 < tid));
+            }
+            if (r == k - 1) sm.tau = static_cast<unsigned long long>(v) << 32;
+        }
+    }
+    consumer_bar();
+    // a segment of at most ns chunks stays in the stages; the scratch then follows them
+    const bool resident = nch <= ns;
+    const int scratch_off = resident ? ns * kRowChunkBytes : 0;
+    segment_topk<DT>(sm, dyn_smem, resident, dyn_smem + scratch_off, smem_bytes - scratch_off, row_base, c0, n, nch,
+                     k, id_base);
+}
+
+// Merge of the CTAs of one row's cluster: every CTA pushes its top-k keys and
+// (max, sum) into the leader's shared memory, then the leader (rank 0) ranks
+// the keys into sm.top and combines (max, sum) into (sm.wm[0], sm.ws[0]).
+// Returns true in the leader, after a block barrier.
+__device__ __forceinline__ bool cluster_row_merge(ExpandSmem& sm, cg::cluster_group& cluster, int rank, int cpr, int k) {
+    const int tid = threadIdx.x;
+    ExpandSmem* leader = cluster.map_shared_rank(&sm, 0);
+    if (tid < kMaxTopK) leader->rtop[rank * kMaxTopK + tid] = sm.ctop[tid];
+    if (tid == 0) {
+        float M = -INFINITY;
+        for (int i = 0; i < kConsumerWarps; ++i) M = fmaxf(M, sm.wm[i]);
+        float S = 0.0f;
+        if (M > -INFINITY)
+            for (int i = 0; i < kConsumerWarps; ++i)
+                if (sm.wm[i] > -INFINITY) S += sm.ws[i] * ex2_approx((sm.wm[i] - M) * kLog2e);
+        leader->rm[rank] = M;
+        leader->rs[rank] = S;
+    }
+    cluster.sync();
+    if (rank != 0) return false;
+    if (tid < cpr * k) {
+        const uint64_t key = sm.rtop[(tid / k) * kMaxTopK + tid % k];
+        if (key != 0ull) {
+            const int r = rank_in_lists(sm.rtop, cpr, key);
+            if (r < k) sm.top[r] = key;
+        }
+    }
+    if (tid == kRowThreads - 1) {
+        float M = -INFINITY;
+        for (int r = 0; r < cpr; ++r) M = fmaxf(M, sm.rm[r]);
+        float S = 0.0f;
+        if (M > -INFINITY)
+            for (int r = 0; r < cpr; ++r)
+                if (sm.rm[r] > -INFINITY) S += sm.rs[r] * ex2_approx((sm.rm[r] - M) * kLog2e);
+        sm.wm[0] = M;
+        sm.ws[0] = S;
+    }
+    __syncthreads();
+    return true;
 }
 
 template <int DT>
@@ -459,8 +594,6 @@ __global__ void __launch_bounds__(kRowThreads, 5) expand_kernel(TreeDims d, Tree
     const int b = row / rps, f = row % rps;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int ES = DT == 1 ? 2 : 4;
-    constexpr int EPV = 16 / ES;
-    constexpr int CE = kRowChunkBytes / ES;  // elements per chunk
     const int k = d.k;
     const int c0 = rank * seg;
     const int n = max(0, min(seg, d.V - c0));
@@ -506,86 +639,7 @@ __global__ void __launch_bounds__(kRowThreads, 5) expand_kernel(TreeDims d, Tree
         }
         __syncwarp();
     } else {
-        // ---- one pass: lane maxima, online exp-sum, group maxima ----
-        const bool do_sum = lse_in == nullptr;
-        float m_l = -INFINITY, s_l = 0.0f;  // lane: running max and sum of exp(x - m_l)
-        bool failed = false;
-        for (int c = 0; c < nch; ++c) {
-            const bool ok = ring_wait(sm.ring, c, ns, failed, w.status);
-            const int nvec = ok ? min(CE, n - c * CE) / EPV : 0;
-            uint4 u[kVecPerLane];
-            load_lane<DT>(dyn_smem + (c % ns) * kRowChunkBytes, nvec, warp, lane, u);
-            ring_release(sm.ring, c, ns);
-            const float cm = lane_max4<DT>(u);
-            gmax_put<DT>(sm, c, tid, warp * kVecPerWarp + lane < nvec ? f2o(cm) : 0u);
-            if (cm > m_l) {
-                s_l = (do_sum && m_l > -INFINITY) ? s_l * ex2_approx((m_l - cm) * kLog2e) : 0.0f;
-                m_l = cm;
-            }
-            if (do_sum && m_l > -INFINITY) {
-                // even and odd elements summed apart, as packed fp32 pairs (one
-                // multiply-add and one add per two elements, each lane's result
-                // the scalar operation's)
-                const float mb = m_l * kLog2e;
-                const uint64_t l2 = f2_pack(kLog2e, kLog2e), nmb = f2_pack(-mb, -mb);
-                uint64_t sab = 0ull;  // (even sum, odd sum)
-#pragma unroll
-                for (int j = 0; j < kVecPerLane; ++j) {
-                    float x[EPV];
-                    unpack16<DT>(u[j], x);
-#pragma unroll
-                    for (int e = 0; e < EPV; e += 2) {
-                        const uint64_t z = f2_fma(f2_pack(x[e], x[e + 1]), l2, nmb);
-                        sab = f2_add(sab, f2_pack(ex2_approx(f2_lo(z)), ex2_approx(f2_hi(z))));
-                    }
-                }
-                s_l += f2_lo(sab) + f2_hi(sab);
-            }
-        }
-        // each warp's k largest lane maxima (0 bits: a lane without elements)
-        const uint32_t lo = warp_sort_desc_u32(m_l > -INFINITY || (nch > 0 && warp * kVecPerWarp + lane < n / EPV)
-                                                   ? f2o(m_l) : 0u);
-        if (lane < kMaxTopK) sm.wtop[warp][lane] = lane < k ? lo : 0u;
-        // the warp's (max, sum)
-        float sw = do_sum ? s_l : 0.0f, mw = m_l;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float mo = __shfl_xor_sync(0xffffffffu, mw, o);
-            const float so = __shfl_xor_sync(0xffffffffu, sw, o);
-            const float M = fmaxf(mw, mo);
-            float sum = 0.0f;
-            if (mw > -INFINITY) sum += sw * ex2_approx((mw - M) * kLog2e);
-            if (mo > -INFINITY) sum += so * ex2_approx((mo - M) * kLog2e);
-            mw = M;
-            sw = sum;
-        }
-        if (lane == 0) {
-            sm.wm[warp] = mw;
-            sm.ws[warp] = sw;
-        }
-        consumer_bar();
-        // tau: the k-th largest of the warps' lists (each zero-padded): entry t
-        // ranks by the entries above it (larger, or equal and earlier)
-        if (tid < kConsumerWarps * kMaxTopK) {
-            const uint32_t v = (&sm.wtop[0][0])[tid];
-            if (v != 0u) {
-                const uint4* p = reinterpret_cast<const uint4*>(&sm.wtop[0][0]);
-                int r = 0;
-#pragma unroll
-                for (int q = 0; q < kConsumerWarps * kMaxTopK / 4; ++q) {
-                    const uint4 a = p[q];
-                    r += (a.x > v || (a.x == v && 4 * q + 0 < tid)) + (a.y > v || (a.y == v && 4 * q + 1 < tid)) +
-                         (a.z > v || (a.z == v && 4 * q + 2 < tid)) + (a.w > v || (a.w == v && 4 * q + 3 < tid));
-                }
-                if (r == k - 1) sm.tau = static_cast<unsigned long long>(v) << 32;
-            }
-        }
-        consumer_bar();
-        // a segment of at most ns chunks stays in the stages; the scratch then follows them
-        const bool resident = nch <= ns;
-        const int scratch_off = resident ? ns * kRowChunkBytes : 0;
-        segment_topk<DT>(sm, dyn_smem, resident, dyn_smem + scratch_off, smem_bytes - scratch_off, row_base, c0, n,
-                         nch, k);
+        segment_consume<DT>(sm, dyn_smem, smem_bytes, ns, row_base, c0, n, nch, k, lse_in == nullptr, 0, w.status);
     }
     __syncthreads();
     const int F = sm.F;
@@ -600,40 +654,7 @@ __global__ void __launch_bounds__(kRowThreads, 5) expand_kernel(TreeDims d, Tree
         return;
     }
     __syncthreads();
-    ExpandSmem* leader = cluster.map_shared_rank(&sm, 0);
-    if (tid < kMaxTopK) leader->rtop[rank * kMaxTopK + tid] = sm.ctop[tid];
-    if (tid == 0) {
-        float M = -INFINITY;
-        for (int i = 0; i < kConsumerWarps; ++i) M = fmaxf(M, sm.wm[i]);
-        float S = 0.0f;
-        if (M > -INFINITY)
-            for (int i = 0; i < kConsumerWarps; ++i)
-                if (sm.wm[i] > -INFINITY) S += sm.ws[i] * ex2_approx((sm.wm[i] - M) * kLog2e);
-        leader->rm[rank] = M;
-        leader->rs[rank] = S;
-    }
-    cluster.sync();
-    if (rank != 0) return;
-
-    // ---- leader: row top-k and lse ----
-    if (tid < cpr * k) {
-        const uint64_t key = sm.rtop[(tid / k) * kMaxTopK + tid % k];
-        if (key != 0ull) {
-            const int r = rank_in_lists(sm.rtop, cpr, key);
-            if (r < k) sm.top[r] = key;
-        }
-    }
-    if (tid == kRowThreads - 1) {
-        float M = -INFINITY;
-        for (int r = 0; r < cpr; ++r) M = fmaxf(M, sm.rm[r]);
-        float S = 0.0f;
-        if (M > -INFINITY)
-            for (int r = 0; r < cpr; ++r)
-                if (sm.rm[r] > -INFINITY) S += sm.rs[r] * ex2_approx((sm.rm[r] - M) * kLog2e);
-        sm.wm[0] = M;
-        sm.ws[0] = S;
-    }
-    __syncthreads();
+    if (!cluster_row_merge(sm, cluster, rank, cpr, k)) return;
 
     // Children of this frontier node.
     const float lse = lse_in != nullptr ? lse_in[b * d.k + f] : sm.wm[0] + logf(sm.ws[0]);
@@ -1252,6 +1273,259 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
     }
 }
 
+// ------------------------------------------------------ vocabulary shards ---
+//
+// When the LM head is split over GPUs by vocabulary rows, each GPU holds a
+// slice [offset, offset + Vs) of every logit row. Stage 1 and the greedy
+// verify then run per slice into small partials, the partials of all slices
+// meet in one exchange (k keys and two floats per row), and a merge gives the
+// results of the whole row ["EAGLE" notes, EAGLE 方法: TopK over the
+// vocabulary; the split itself is not on the pages]. Partials: (max, sum of
+// exp(x - max)) in fp32 and the slice's top-k keys (value desc, then lower
+// token id, ids of the whole vocabulary); the top-1 key is the slice's argmax.
+
+// Stage-1 partials of one vocabulary slice: grid (cpr, rows), a cluster per row.
+template <int DT>
+__global__ void __launch_bounds__(kRowThreads, 5) shard_partial_kernel(int Vs, int k, int seg, int ns, int smem_bytes,
+                                                                        const void* __restrict__ logits, int id_base,
+                                                                        float2* __restrict__ part_ms,
+                                                                        uint64_t* __restrict__ part_keys,
+                                                                        int* status) {
+    extern __shared__ __align__(128) unsigned char dyn_smem[];
+    __shared__ ExpandSmem sm;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int cpr = static_cast<int>(cluster.num_blocks());
+    const int row = blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int ES = DT == 1 ? 2 : 4;
+    const int c0 = rank * seg;
+    const int n = max(0, min(seg, Vs - c0));
+    const int nch = min(max_seg_chunks<DT>(), (n * ES + kRowChunkBytes - 1) / kRowChunkBytes);
+    const char* row_base = static_cast<const char*>(logits) + static_cast<size_t>(row) * Vs * ES;
+    pdl_launch_dependents();
+    if (tid == kProducerWarp * 32) prefetch_l2_segment(row_base + static_cast<size_t>(c0) * ES, n * ES);
+    if (tid == 0) {
+        ring_init(sm.ring, ns);
+        sm.tau = 0ull;
+        sm.ngroups = 0;
+        sm.nkeys = 0;
+    }
+    if (tid < kMaxTopK) {
+        sm.ctop[tid] = 0ull;
+        sm.top[tid] = 0ull;
+    }
+    __syncthreads();
+    pdl_wait_prior();
+    if (warp == kProducerWarp) {
+        if (lane == 0 && nch > 0)
+            ring_produce(sm.ring, dyn_smem, row_base + static_cast<size_t>(c0) * ES, n * ES, nch, ns, status);
+        __syncwarp();
+    } else {
+        segment_consume<DT>(sm, dyn_smem, smem_bytes, ns, row_base, c0, n, nch, k, true, id_base, status);
+    }
+    __syncthreads();
+    if (!cluster_row_merge(sm, cluster, rank, cpr, k)) return;
+    if (tid < kMaxTopK) part_keys[static_cast<size_t>(row) * kMaxTopK + tid] = tid < k ? sm.top[tid] : 0ull;
+    if (tid == 0) part_ms[row] = make_float2(sm.wm[0], sm.ws[0]);
+}
+
+// Merge of S slices' partials, one warp per row: lse = M + log(sum S_s
+// 2^((M_s - M) log2 e)), M = max M_s; the top-k of the union of the slices'
+// top-k (rank among them); the argmax = the largest key.
+constexpr int kMaxShards = 16;
+constexpr int kMergeWarps = 8;
+__global__ void __launch_bounds__(kMergeWarps * 32) shard_merge_kernel(int S, int rows, int k,
+                                                                       const float2* __restrict__ part_ms,
+                                                                       const uint64_t* __restrict__ part_keys,
+                                                                       float* __restrict__ lse_out,
+                                                                       int32_t* __restrict__ topk_id,
+                                                                       float* __restrict__ topk_val,
+                                                                       int32_t* __restrict__ argmax_out, int* status) {
+    __shared__ alignas(16) uint64_t keys[kMergeWarps][kMaxShards * kMaxTopK];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int row = blockIdx.x * kMergeWarps + warp;
+    pdl_launch_dependents();
+    pdl_wait_prior();
+    if (row >= rows) return;
+    uint64_t* kl = keys[warp];
+    for (int i = lane; i < S * kMaxTopK; i += 32)
+        kl[i] = part_keys[(static_cast<size_t>(i / kMaxTopK) * rows + row) * kMaxTopK + i % kMaxTopK];
+    float m = -INFINITY, s = 0.0f;
+    if (lane < S) {
+        const float2 ms = part_ms[static_cast<size_t>(lane) * rows + row];
+        m = ms.x;
+        s = ms.y;
+    }
+    float M = m;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float t = (lane < S && m > -INFINITY) ? s * ex2_approx((m - M) * kLog2e) : 0.0f;
+    // the slices' terms in slice order (one fixed order: lane 0 first)
+    float sum = 0.0f;
+    for (int i = 0; i < S; ++i) sum += __shfl_sync(0xffffffffu, t, i);
+    __syncwarp();
+    for (int i = lane; i < S * kMaxTopK; i += 32) {
+        const uint64_t key = kl[i];
+        if (key == 0ull || i % kMaxTopK >= k) continue;
+        int r = 0;
+        for (int j = 0; j < S * kMaxTopK; ++j) r += (j % kMaxTopK < k) && kl[j] > key;
+        if (r < k) {
+            topk_id[static_cast<size_t>(row) * k + r] = static_cast<int32_t>(key_id(key));
+            topk_val[static_cast<size_t>(row) * k + r] = key_val(key);
+        }
+        if (r == 0) argmax_out[row] = static_cast<int32_t>(key_id(key));
+    }
+    // ranks past the union's key count: none
+    int have = 0;
+    for (int j = lane; j < S * kMaxTopK; j += 32) have += (j % kMaxTopK < k) && kl[j] != 0ull;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) have += __shfl_xor_sync(0xffffffffu, have, o);
+    if (lane >= have && lane < k) {
+        topk_id[static_cast<size_t>(row) * k + lane] = -1;
+        topk_val[static_cast<size_t>(row) * k + lane] = -INFINITY;
+    }
+    if (lane == 0) {
+        const float lse = M + logf(sum);
+        lse_out[row] = lse;
+        if (!isfinite(lse)) raise_status(status, kDevNonFinite);
+        if (have == 0) argmax_out[row] = -1;
+    }
+}
+
+// Stage 2 from merged top-k, one CTA per sequence: the children of the F
+// frontier rows of step `step` (row f's top-k ids and logits, its lse) and
+// the next frontier, exactly as the expansion's last CTA does.
+__global__ void __launch_bounds__(kRowThreads) expand_topk_kernel(TreeDims d, TreeWs w, int step,
+                                                                  const int32_t* __restrict__ topk_id,
+                                                                  const float* __restrict__ topk_val,
+                                                                  const float* __restrict__ lse_in,
+                                                                  float* __restrict__ row_lse,
+                                                                  int32_t* __restrict__ ftok_out,
+                                                                  int32_t* __restrict__ fcount_out) {
+    __shared__ alignas(16) uint64_t sel[kMaxTopK * kMaxTopK];
+    __shared__ int32_t sel_tok[kMaxTopK * kMaxTopK];
+    __shared__ uint64_t top[kMaxTopK];
+    __shared__ int32_t top_tok[kMaxTopK];
+    const int b = blockIdx.x, tid = threadIdx.x;
+    pdl_launch_dependents();
+    pdl_wait_prior();
+    const int F = w.fcount[step * d.B + b];
+    const int base = step == 0 ? 0 : d.k + (step - 1) * d.k * d.k;
+    const int nsel = F * d.k;
+    for (int i = tid; i < d.k; i += kRowThreads)
+        row_lse[(static_cast<size_t>(b) * d.D + step) * d.k + i] =
+            i < F ? lse_in[b * d.k + i] : __int_as_float(0x7fc00000);
+    for (int i = tid; i < nsel; i += kRowThreads) {
+        const int fr = i / d.k, r = i % d.k;
+        const size_t src = (static_cast<size_t>(b) * d.k + fr) * d.k + r;
+        const int tok = topk_id[src];
+        uint64_t sk = 0ull;
+        if (tok >= 0 && tok < d.V) {
+            const int parent = w.fnode[(step * d.B + b) * d.k + fr];
+            const float plogv = parent < 0 ? 0.0f : __ldcg(&w.cand_logv[static_cast<size_t>(b) * d.C + parent]);
+            const float lse = lse_in[b * d.k + fr];
+            const float lp = __fsub_rn(topk_val[src], lse);
+            const float lv = __fadd_rn(plogv, lp);
+            const int id = base + i;
+            const size_t at = static_cast<size_t>(b) * d.C + id;
+            w.cand_token[at] = tok;
+            w.cand_parent[at] = parent;
+            w.cand_depth[at] = step + 1;
+            w.cand_logv[at] = lv;
+            w.cand_lp[at] = lp;
+            w.cand_valid[at] = 1;
+            if (!isfinite(lse)) raise_status(w.status, kDevNonFinite);
+            const float rank_by = d.policy == 1 ? lp : d.policy == 3 ? -static_cast<float>(fr + r) : lv;
+            if (lv >= d.log_thr) sk = make_key(rank_by, static_cast<uint32_t>(id));
+        } else if (tok >= d.V) {
+            raise_status(w.status, kDevBadIndex);
+        }
+        sel[i] = sk;
+        sel_tok[i] = tok;
+    }
+    if (tid >= nsel && tid < (nsel + 7) / 8 * 8) sel[tid] = 0ull;
+    if (tid < kMaxTopK) top[tid] = 0ull;
+    __syncthreads();
+    for (int i = tid; i < nsel; i += kRowThreads) {
+        const uint64_t key = sel[i];
+        if (key == 0ull) continue;
+        const int r = rank_in_list(sel, nsel, key);
+        if (r < d.k) {
+            top[r] = key;
+            top_tok[r] = sel_tok[i];
+        }
+    }
+    __syncthreads();
+    if (tid < d.k) {
+        const uint64_t key = top[tid];
+        const int id = key ? static_cast<int>(key_id(key)) : -1;
+        w.fnode[((step + 1) * d.B + b) * d.k + tid] = id;
+        ftok_out[b * d.k + tid] = id >= 0 ? top_tok[tid] : -1;
+    }
+    if (tid == 0) {
+        int cnt = 0;
+        for (int j = 0; j < d.k; ++j) cnt += top[j] != 0ull;
+        w.fcount[(step + 1) * d.B + b] = cnt;
+        fcount_out[b] = cnt;
+    }
+}
+
+// Greedy verification from the target's argmax of every slot (merged over the
+// vocabulary slices), one warp per sequence: the walk of verify_kernel.
+__global__ void __launch_bounds__(32) verify_argmax_kernel(TreeDims d, TreeWs w, const int32_t* __restrict__ row_argmax,
+                                                          const int32_t* __restrict__ tokens,
+                                                          const int32_t* __restrict__ parent,
+                                                          const int32_t* __restrict__ n_tree,
+                                                          int32_t* __restrict__ accept_len,
+                                                          int32_t* __restrict__ slots_out,
+                                                          int32_t* __restrict__ tokens_out) {
+    __shared__ int par[kMaxSlots], tok[kMaxSlots], path[kMaxDepth + 1];
+    const int b = blockIdx.x, lane = threadIdx.x;
+    pdl_launch_dependents();
+    pdl_wait_prior();
+    const int n = n_tree[b];
+    const int T = d.T;
+    if (n < 1 || n > T) {
+        if (lane == 0) raise_status(w.status, kDevBadIndex);
+        return;
+    }
+    bool bad = false;
+    for (int c = lane; c < n; c += 32) {
+        par[c] = parent[static_cast<size_t>(b) * T + c];
+        tok[c] = tokens[static_cast<size_t>(b) * T + c];
+        if (c > 0 && (par[c] < 0 || par[c] >= c || tok[c] < 0 || tok[c] >= d.V)) bad = true;
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    __syncwarp();
+    int cur = 0, a = 0;
+    path[0] = 0;
+    while (a < d.D && !bad) {
+        const int want = row_argmax[static_cast<size_t>(b) * T + cur];
+        int next = -1;
+        for (int c0 = cur + 1; c0 < n && next < 0; c0 += 32) {
+            const int c = c0 + lane;
+            const unsigned bal = __ballot_sync(0xffffffffu, c < n && par[c] == cur && tok[c] == want);
+            if (bal) next = c0 + __ffs(bal) - 1;
+        }
+        if (next < 0) break;
+        ++a;
+        if (lane == 0) path[a] = next;
+        cur = next;
+    }
+    __syncwarp();
+    if (lane == 0) {
+        const int bonus = bad ? -1 : row_argmax[static_cast<size_t>(b) * T + cur];
+        if (bad || bonus < 0 || bonus >= d.V) raise_status(w.status, kDevBadIndex);
+        const int Dp1 = d.D + 1;
+        accept_len[b] = a;
+        for (int j = 0; j < Dp1; ++j) {
+            slots_out[b * Dp1 + j] = j <= a ? path[j] : -1;
+            tokens_out[b * Dp1 + j] = j < a ? tok[path[j + 1]] : (j == a ? bonus : -1);
+        }
+    }
+}
+
 // -------------------------------------------------------------- launchers ---
 
 static int sm_count() {
@@ -1421,6 +1695,43 @@ cudaError_t launch_verify(const TreeDims& d, const TreeWs& ws, int mode, float i
                          : launch_rows(verify_kernel<1, 0>, grid, p.cpr, smem, stream, args);
     return mode == 1 ? launch_rows(verify_kernel<0, 1>, grid, p.cpr, smem, stream, args)
                      : launch_rows(verify_kernel<0, 0>, grid, p.cpr, smem, stream, args);
+}
+
+cudaError_t launch_shard_partials(int Vs, int k, int rows, int dtype, const void* logits, int id_base, float2* part_ms,
+                                  uint64_t* part_keys, int* status, cudaStream_t stream) {
+    const int esize = dtype == 1 ? 2 : 4;
+    const int max_seg = esize == 2 ? kMaxSegChunksBf16 : kMaxSegChunks;
+    const RowPlan p = plan_rows(Vs, esize, rows, false, kExpandStages, kMaxSegChunks);
+    if (p.nch > max_seg) return cudaErrorInvalidValue;
+    const int scratch = p.nch * kConsumers * 4 + 512 * 8;
+    const int smem = p.nch <= p.stages ? p.stages * kRowChunkBytes + scratch : std::max(p.smem, scratch);
+    dim3 grid(p.cpr, rows, 1);
+    int seg = p.seg, ns = p.stages, smem_bytes = smem;
+    void* args[] = {&Vs, &k, &seg, &ns, &smem_bytes, const_cast<void**>(&logits), &id_base, &part_ms, &part_keys,
+                    &status};
+    return dtype == 1 ? launch_rows(shard_partial_kernel<1>, grid, p.cpr, smem, stream, args)
+                      : launch_rows(shard_partial_kernel<0>, grid, p.cpr, smem, stream, args);
+}
+
+cudaError_t launch_shard_merge(int S, int rows, int k, const float2* part_ms, const uint64_t* part_keys, float* lse,
+                               int32_t* topk_id, float* topk_val, int32_t* argmax, int* status, cudaStream_t stream) {
+    const int blocks = (rows + kMergeWarps - 1) / kMergeWarps;
+    return launch_pdl(shard_merge_kernel, dim3(blocks), dim3(kMergeWarps * 32), 0, stream, S, rows, k, part_ms,
+                      part_keys, lse, topk_id, topk_val, argmax, status);
+}
+
+cudaError_t launch_expand_topk(const TreeDims& d, const TreeWs& ws, int step, const int32_t* topk_id,
+                               const float* topk_val, const float* lse_in, float* row_lse, int32_t* ftok,
+                               int32_t* fcount_out, cudaStream_t stream) {
+    return launch_pdl(expand_topk_kernel, dim3(d.B), dim3(kRowThreads), 0, stream, d, ws, step, topk_id, topk_val,
+                      lse_in, row_lse, ftok, fcount_out);
+}
+
+cudaError_t launch_verify_argmax(const TreeDims& d, const TreeWs& ws, const int32_t* row_argmax, const int32_t* tokens,
+                                 const int32_t* parent, const int32_t* n_tree, int32_t* accept_len, int32_t* slots,
+                                 int32_t* out_tokens, cudaStream_t stream) {
+    return launch_pdl(verify_argmax_kernel, dim3(d.B), dim3(32), 0, stream, d, ws, row_argmax, tokens, parent, n_tree,
+                      accept_len, slots, out_tokens);
 }
 
 }  // namespace eagle

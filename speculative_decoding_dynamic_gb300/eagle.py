@@ -83,6 +83,10 @@ _lib.eagle_attention_workspace_bytes.restype = _sz
 _lib.eagle_tree_attention.argtypes = [_KP, _i, _p, _p, _i, _p, _p, _p, _p, _p, _sz, _p]
 _u64 = ctypes.c_uint64
 _lib.eagle_verify.argtypes = [_TP, _p, _sz, _i, ctypes.c_float, _u64, _u64, _p, _p, _p, _p, _p, _p, _p, _p, _p]
+_lib.eagle_shard_partials.argtypes = [_TP, _p, _sz, _i, _i, _i, _p, _p, _p, _p]
+_lib.eagle_shard_merge.argtypes = [_TP, _p, _sz, _i, _i, _p, _p, _p, _p, _p, _p, _p]
+_lib.eagle_expand_topk.argtypes = [_TP, _p, _sz, _i, _p, _p, _p, _p, _p, _p, _p]
+_lib.eagle_verify_argmax.argtypes = [_TP, _p, _sz, _p, _p, _p, _p, _p, _p, _p, _p]
 _lib.eagle_kv_compact.argtypes = [_KP, _p, _p, _p, _p, _i, _p, _p, _p]
 _lib.eagle_verify_static.argtypes = [_TP, _i, ctypes.c_float, _u64, _u64, _p, _p, _p, _p, _p, _p, _p, _p]
 _lib.eagle_status_fetch.argtypes = [_p, ctypes.POINTER(ctypes.c_int), _p]
@@ -193,6 +197,35 @@ def eagle_verify_static(cfg, mode, temperature, seed, cycle, target_logits, toke
                                                            int(cycle), _ptr(target_logits), _ptr(tokens),
                                                            _ptr(parent), _ptr(n_tree), _ptr(accept_len),
                                                            _ptr(accepted_slots), _ptr(out_tokens), _stream(stream)))
+
+
+def eagle_shard_partials(cfg, ws, rows, shard_vocab, vocab_offset, logits, part_max_sum, part_keys, stream=None):
+    _check("eagle_shard_partials", _lib.eagle_shard_partials(ctypes.byref(cfg), *_ws(ws), rows, shard_vocab,
+                                                             vocab_offset, _ptr(logits), _ptr(part_max_sum),
+                                                             _ptr(part_keys), _stream(stream)))
+
+
+def eagle_shard_merge(cfg, ws, n_shards, rows, part_max_sum, part_keys, row_lse, topk_ids, topk_logits, row_argmax,
+                      stream=None):
+    _check("eagle_shard_merge", _lib.eagle_shard_merge(ctypes.byref(cfg), *_ws(ws), n_shards, rows,
+                                                       _ptr(part_max_sum), _ptr(part_keys), _ptr(row_lse),
+                                                       _ptr(topk_ids), _ptr(topk_logits), _ptr(row_argmax),
+                                                       _stream(stream)))
+
+
+def eagle_expand_topk(cfg, ws, step, topk_ids, topk_logits, row_lse_in, row_lse, frontier_tokens, frontier_count,
+                      stream=None):
+    _check("eagle_expand_topk", _lib.eagle_expand_topk(ctypes.byref(cfg), *_ws(ws), step, _ptr(topk_ids),
+                                                       _ptr(topk_logits), _ptr(row_lse_in), _ptr(row_lse),
+                                                       _ptr(frontier_tokens), _ptr(frontier_count), _stream(stream)))
+
+
+def eagle_verify_argmax(cfg, ws, row_argmax, tokens, parent, n_tree, accept_len, accepted_slots, out_tokens,
+                        stream=None):
+    _check("eagle_verify_argmax", _lib.eagle_verify_argmax(ctypes.byref(cfg), *_ws(ws), _ptr(row_argmax),
+                                                           _ptr(tokens), _ptr(parent), _ptr(n_tree),
+                                                           _ptr(accept_len), _ptr(accepted_slots), _ptr(out_tokens),
+                                                           _stream(stream)))
 
 
 def eagle_kv_compact(kv, kv_cache, prefix_len, accept_len, accepted_slots, slots_stride, new_len, ws=None,
