@@ -66,7 +66,7 @@ typedef enum {
 
 typedef enum { EAGLE_F32 = 0, EAGLE_BF16 = 1 } eagle_dtype;
 
-typedef enum { EAGLE_VERIFY_GREEDY = 0, EAGLE_VERIFY_LOSSLESS = 1 } eagle_verify_mode;
+typedef enum { EAGLE_VERIFY_GREEDY = 0, EAGLE_VERIFY_LOSSLESS = 1, EAGLE_VERIFY_DRAFT = 2 } eagle_verify_mode;
 
 /* Tree policy [summary 5.2.1, 5.2.2: the ablations of value-based expansion
  * and of reranking; tutorial "Watch the Budget Being Spent": the EAGLE-1
@@ -153,6 +153,26 @@ int eagle_tree_init(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, void* 
 int eagle_expand(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int step, const void* draft_logits,
                  const float* row_lse_in, float* row_lse, int32_t* frontier_tokens, int32_t* frontier_count,
                  void* stream);
+
+/*
+ * Stages 1+2 with sampled drafting ["EAGLE-2: Faster Inference ..." summary,
+ * 2.1 Speculative Sampling: the draft proposes tokens drawn from its
+ * distribution]: the k children of frontier row f are drawn from the row's
+ * softmax without replacement instead of being its k largest logits, by the
+ * Gumbel-top-k identity: keys fl(x + g), g = -ln(-ln u) through a fixed-order
+ * logarithm (atanh series, correctly rounded fp32 steps), u = ((word >> 9) +
+ * 1/2) 2^-23; the children are the k largest keys in drawing order (equal
+ * keys: lower id). The word of element x of row f of sequence b is word x % 4
+ * of Philox4x32-10 at counter (x / 4, b * k + f, step, cycle & 0xffffffff)
+ * under key (seed & 0xffffffff ^ 10, seed >> 32). Everything else (lse,
+ * values from the unperturbed logits, threshold, frontier, outputs) is as
+ * eagle_expand. With eagle_verify in EAGLE_VERIFY_DRAFT mode and a tree
+ * shape that does not depend on the drawn tokens (EAGLE_POLICY_STATIC) the
+ * cycle's output distribution is the target's.
+ */
+int eagle_expand_sampled(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int step, const void* draft_logits,
+                         const float* row_lse_in, uint64_t seed, uint64_t cycle, float* row_lse,
+                         int32_t* frontier_tokens, int32_t* frontier_count, void* stream);
 
 /*
  * LM head of a draft step, the projection whose rows stages 1+2 read
@@ -243,7 +263,10 @@ int eagle_tree_attention(const eagle_kv_cfg* kv, int T, const void* q, const voi
  *                   and T+1 form U64 = w[T+1] * 2^32 + w[T] for the final
  *                   draw. Use a new cycle number per cycle. Unused by GREEDY.
  *   target_logits [B, T, V] in: the target's distribution at each slot.
- *   draft_logits    reserved for the draft-probability rule; may be NULL.
+ *   draft_logits  [D, B, k, V] in (DRAFT only, else may be NULL): the draft
+ *                 rows of every step of the cycle, as passed to
+ *                 eagle_expand_sampled; the workspace's frontiers map each
+ *                 kept node to the row its children were drawn from.
  *   tokens, parent [B, T], n_tree [B] in: the tree from eagle_build_tree.
  *   accept_len [B] out: accepted draft tokens a_b (0..D).
  *   accepted_slots [B, D+1] out: slots of the accepted path, root first, -1 pad.
@@ -258,6 +281,16 @@ int eagle_tree_attention(const eagle_kv_cfg* kv, int T, const void* q, const voi
  *   U24 * S < 2^24 * P_u[x] (S = remaining mass); a rejection removes x. With
  *   no child accepted the bonus is the smallest token y (not removed) whose
  *   running mass exceeds floor(U64 * S / 2^64).
+ * DRAFT (temperature > 0; children drawn by eagle_expand_sampled): at node u
+ *   with target residual A (initially P_u) and the remaining draft masses Q
+ *   of u's draft row (integer masses as above, at the same temperature), the
+ *   kept children are tested in slot (drawing) order and child x is accepted
+ *   iff U24 * Q[x] * SA < 2^24 * A[x] * SQ (SA, SQ the sums); a rejection sets
+ *   A[y] = floor(max(0, A[y] SQ - Q[y] SA) / 2^s) with s the smallest shift
+ *   that brings the largest value to 2^40 or below (A is kept when all are 0),
+ *   then removes x from Q. The bonus is the smallest y whose running sum of A
+ *   exceeds floor(U64 * SA / 2^64). The walk runs in one cluster of CTAs per
+ *   sequence; the residual is kept in the workspace.
  */
 int eagle_verify(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int mode, float temperature, uint64_t seed,
                  uint64_t cycle, const void* target_logits, const void* draft_logits, const int32_t* tokens,
@@ -395,6 +428,13 @@ int eagle_verify_export(const eagle_tree_cfg* cfg, const void* ws, size_t ws_byt
 int eagle_test_expand_starved(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int step,
                               const void* draft_logits, float* row_lse, int32_t* frontier_tokens,
                               int32_t* frontier_count, void* stream);
+
+/* The device arithmetic of sampled drafting, element by element: for i < n,
+ * gumbel_out[i] = the Gumbel noise of words[i] and log_out[i] = the
+ * fixed-order natural logarithm of ys[i] (positive normal floats), as
+ * eagle_expand_sampled computes them. Either input may be NULL. */
+int eagle_test_sampling(const uint32_t* words, const float* ys, int n, float* gumbel_out, float* log_out,
+                        void* stream);
 
 /* Kernels launched by this library since it was loaded (host-side count). */
 uint64_t eagle_kernel_launches(void);

@@ -120,7 +120,7 @@ int eagle_tree_init(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, void* 
 
 static int expand_call(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int step, const void* draft_logits,
                        const float* row_lse_in, float* row_lse, int32_t* frontier_tokens, int32_t* frontier_count,
-                       void* stream, bool starve) {
+                       void* stream, bool starve, const uint64_t* sample_seed_cycle = nullptr) {
     TreeDims d;
     TreeWs w;
     int rc = resolve(cfg, &d);
@@ -130,7 +130,7 @@ static int expand_call(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int
     if (!draft_logits || !row_lse || !frontier_tokens || !frontier_count) return EAGLE_ERR_INVALID_ARG;
     if (!aligned16(draft_logits)) return EAGLE_ERR_UNSUPPORTED;
     return launch_result(launch_expand(d, w, step, draft_logits, row_lse_in, row_lse, frontier_tokens,
-                                       frontier_count, static_cast<cudaStream_t>(stream), starve));
+                                       frontier_count, static_cast<cudaStream_t>(stream), starve, sample_seed_cycle));
 }
 
 int eagle_expand(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int step, const void* draft_logits,
@@ -138,6 +138,14 @@ int eagle_expand(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int step,
                  void* stream) {
     return expand_call(cfg, ws, ws_bytes, step, draft_logits, row_lse_in, row_lse, frontier_tokens, frontier_count,
                        stream, false);
+}
+
+int eagle_expand_sampled(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int step, const void* draft_logits,
+                         const float* row_lse_in, uint64_t seed, uint64_t cycle, float* row_lse,
+                         int32_t* frontier_tokens, int32_t* frontier_count, void* stream) {
+    const uint64_t sc[2] = {seed, cycle};
+    return expand_call(cfg, ws, ws_bytes, step, draft_logits, row_lse_in, row_lse, frontier_tokens, frontier_count,
+                       stream, false, sc);
 }
 
 int eagle_test_expand_starved(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int step,
@@ -224,16 +232,21 @@ int eagle_verify(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int mode,
     int rc = resolve(cfg, &d);
     if (rc == EAGLE_OK) rc = bind_ws(d, ws, ws_bytes, &w);
     if (rc != EAGLE_OK) return rc;
-    if (mode != EAGLE_VERIFY_GREEDY && mode != EAGLE_VERIFY_LOSSLESS) return EAGLE_ERR_INVALID_ARG;
+    if (mode != EAGLE_VERIFY_GREEDY && mode != EAGLE_VERIFY_LOSSLESS && mode != EAGLE_VERIFY_DRAFT)
+        return EAGLE_ERR_INVALID_ARG;
     if (!target_logits || !tokens || !parent || !n_tree || !accept_len || !accepted_slots || !out_tokens)
         return EAGLE_ERR_INVALID_ARG;
-    (void)draft_logits;  // read by the draft-probability rule only
+    if (mode == EAGLE_VERIFY_DRAFT && draft_logits == nullptr) return EAGLE_ERR_INVALID_ARG;
     float inv_t = 1.0f;
-    if (mode == EAGLE_VERIFY_LOSSLESS) {
+    if (mode != EAGLE_VERIFY_GREEDY) {
         if (!(temperature > 0.0f) || !std::isfinite(temperature)) return EAGLE_ERR_INVALID_ARG;
         inv_t = static_cast<float>(1.0 / static_cast<double>(temperature));
     }
     if (!aligned16(target_logits)) return EAGLE_ERR_UNSUPPORTED;
+    if (mode == EAGLE_VERIFY_DRAFT)
+        return launch_result(launch_verify_draft(d, w, inv_t, verify_rng(seed, cycle), target_logits, draft_logits,
+                                                 tokens, parent, n_tree, accept_len, accepted_slots, out_tokens,
+                                                 static_cast<cudaStream_t>(stream)));
     return launch_result(launch_verify(d, w, mode, inv_t, target_logits, tokens, parent, n_tree,
                                        verify_rng(seed, cycle), accept_len, accepted_slots, out_tokens,
                                        static_cast<cudaStream_t>(stream)));
@@ -374,6 +387,13 @@ int eagle_verify_export(const eagle_tree_cfg* cfg, const void* ws, size_t ws_byt
     cp(row_argmax, w.row_arg, BT * 4);
     cp(row_mass, w.row_mass, BT * 8);
     return launch_result(e);
+}
+
+int eagle_test_sampling(const uint32_t* words, const float* ys, int n, float* gumbel_out, float* log_out,
+                        void* stream) {
+    if (n < 0 || (words && !gumbel_out) || (ys && !log_out)) return EAGLE_ERR_INVALID_ARG;
+    if (n == 0) return EAGLE_OK;
+    return launch_result(launch_sampling_probe(words, ys, n, gumbel_out, log_out, static_cast<cudaStream_t>(stream)));
 }
 
 uint64_t eagle_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }

@@ -66,6 +66,7 @@ struct TreeWs {
     int32_t* row_arg;       // [B, T] verify row argmax
     uint64_t* row_mass;     // [B, T] verify integer mass
     uint64_t* chunk_mass;   // [B, T, verify_mass_slots] verify integer mass per row piece
+    uint64_t* resid;        // [B, V] target residual of the draft-probability rule
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -100,6 +101,7 @@ inline size_t ws_layout(const TreeDims& d, void* base, TreeWs* ws) {
     w.row_arg = static_cast<int32_t*>(take(B * T * 4));
     w.row_mass = static_cast<uint64_t*>(take(B * T * 8));
     w.chunk_mass = static_cast<uint64_t*>(take(B * T * verify_mass_slots(d.V, d.dtype == 1 ? 2 : 4) * 8));
+    w.resid = static_cast<uint64_t*>(take(B * static_cast<size_t>(d.V) * 8));
     if (ws) *ws = w;
     return align_up(off, 256);
 }
@@ -122,9 +124,11 @@ RowPlan plan_rows(int V, int esize, long rows, bool resident, int max_stages, in
 cudaError_t launch_tree_init(const TreeDims& d, const TreeWs& ws, cudaStream_t stream);
 // starve_ring: the failure-path test hook (the row ring's producer issues no
 // copies, so the consumers' bounded waits give up and raise status 2).
+// sample_seed_cycle: {seed, cycle} for sampled drafting (children drawn from
+// the row's softmax without replacement), NULL for the top-k children.
 cudaError_t launch_expand(const TreeDims& d, const TreeWs& ws, int step, const void* logits, const float* lse_in,
                           float* row_lse, int32_t* ftok, int32_t* fcount_out, cudaStream_t stream,
-                          bool starve_ring = false);
+                          bool starve_ring = false, const uint64_t* sample_seed_cycle = nullptr);
 cudaError_t launch_rerank(const TreeDims& d, const TreeWs& ws, cudaStream_t stream);
 cudaError_t launch_tree_value(const TreeDims& d, const TreeWs& ws, float* value_sum, cudaStream_t stream);
 cudaError_t launch_build_tree(const TreeDims& d, const TreeWs& ws, const int32_t* prefix_len,
@@ -159,6 +163,13 @@ cudaError_t launch_expand_topk(const TreeDims& d, const TreeWs& ws, int step, co
 cudaError_t launch_verify_argmax(const TreeDims& d, const TreeWs& ws, const int32_t* row_argmax, const int32_t* tokens,
                                  const int32_t* parent, const int32_t* n_tree, int32_t* accept_len, int32_t* slots,
                                  int32_t* out_tokens, cudaStream_t stream);
+
+cudaError_t launch_verify_draft(const TreeDims& d, const TreeWs& ws, float inv_temp, VerifyRng rng,
+                                const void* target, const void* draft, const int32_t* tokens, const int32_t* parent,
+                                const int32_t* n_tree, int32_t* accept_len, int32_t* slots, int32_t* out_tokens,
+                                cudaStream_t stream);
+cudaError_t launch_sampling_probe(const uint32_t* words, const float* ys, int n, float* gumbel_out, float* log_out,
+                                  cudaStream_t stream);
 
 struct KvDims {
     int B, Hq, Hkv, d, layers, max_len, dtype;

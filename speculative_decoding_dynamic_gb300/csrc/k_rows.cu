@@ -46,6 +46,7 @@
 
 #include "eagle_internal.cuh"
 #include "eagle_ws.h"
+#include "mass.cuh"
 #include "sampling.cuh"
 
 namespace eagle {
@@ -329,6 +330,34 @@ __device__ __forceinline__ uint32_t gmax_get(const ExpandSmem& sm, int c, int t)
 template <int DT>
 __device__ __forceinline__ uint32_t gmax_floor(uint32_t o) { return DT == 1 ? (o & 0xFFFF0000u) : o; }
 
+// Sampled drafting: the children of a row are drawn from its softmax without
+// replacement by the Gumbel-top-k identity, keys kappa = fl(x + g), g the
+// Gumbel noise of one uniform word per element ("EAGLE-2: Faster Inference
+// ..." summary, 2.1 Speculative Sampling: the draft proposes tokens sampled
+// from its distribution; the perturbed-key form of the draw is the reading
+// taken here). The words of row r (= b * k + f) of a step come from
+// Philox4x32-10 at counter (x / 4, r, step, cycle), word x % 4.
+struct GumbelRng {
+    uint32_t k0, k1;  // key (seed_lo ^ 10, seed_hi)
+    uint32_t c2, c3;  // step, cycle
+};
+
+// The perturbed keys of one 16-byte vector whose first element is element id0
+// (a multiple of 4) of row `row`.
+template <int DT>
+__device__ __forceinline__ void gumbel_keys(const float (&x)[16 / (DT == 1 ? 2 : 4)], int id0, uint32_t row,
+                                            const GumbelRng& g, float (&kap)[16 / (DT == 1 ? 2 : 4)]) {
+    constexpr int EPV = 16 / (DT == 1 ? 2 : 4);
+#pragma unroll
+    for (int q = 0; q < EPV; q += 4) {
+        const uint32_t ctr[4] = {static_cast<uint32_t>((id0 + q) >> 2), row, g.c2, g.c3};
+        uint32_t wd[4];
+        sampling::philox4x32_10(ctr, g.k0, g.k1, wd);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) kap[q + i] = __fadd_rn(x[q + i], sampling::gumbel_of_word(wd[i]));
+    }
+}
+
 // Top-k keys of a CTA's row segment, after the streaming pass (consumer
 // threads only). A lane group is one lane's four vectors of one chunk, and
 // gmax holds each group's maximum. tau = the k-th largest lane maximum of the
@@ -340,10 +369,10 @@ __device__ __forceinline__ uint32_t gmax_floor(uint32_t o) { return DT == 1 ? (o
 // collected, and the k largest keys found by rank selection into ctop. When the keys do not fit the scratch
 // (many equal values at the top), k block-wide rounds over the candidate
 // groups pick the keys one by one instead.
-template <int DT>
+template <int DT, bool SAMP>
 __device__ __forceinline__ void segment_topk(ExpandSmem& sm, const unsigned char* stages, bool resident,
                                              unsigned char* scratch, int scratch_bytes, const char* row_base, int c0,
-                                             int n, int nch, int k, int id_base) {
+                                             int n, int nch, int k, int id_base, uint32_t grow, const GumbelRng& g) {
     constexpr int ES = DT == 1 ? 2 : 4;
     constexpr int EPV = 16 / ES;
     constexpr int CE = kRowChunkBytes / ES;
@@ -384,6 +413,12 @@ __device__ __forceinline__ void segment_topk(ExpandSmem& sm, const unsigned char
         const uint4 u = resident ? reinterpret_cast<const uint4*>(stages)[(id0 - c0) / EPV]
                                  : __ldcg(reinterpret_cast<const uint4*>(row_base + static_cast<size_t>(id0) * ES));
         unpack16<DT>(u, x);
+        if (SAMP) {  // the keys are the perturbed values
+            float kap[EPV];
+            gumbel_keys<DT>(x, id0, grow, g, kap);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) x[e] = kap[e];
+        }
         uint32_t mask = 0;  // bit e: element e is a key >= tau (NaN never is)
 #pragma unroll
         for (int e = 0; e < EPV; ++e) mask |= static_cast<uint32_t>(all ? x[e] == x[e] : x[e] >= tv) << e;
@@ -423,6 +458,12 @@ __device__ __forceinline__ void segment_topk(ExpandSmem& sm, const unsigned char
             if (id0 >= c0 + n) continue;
             float x[EPV];
             unpack16<DT>(__ldcg(reinterpret_cast<const uint4*>(row_base + static_cast<size_t>(id0) * ES)), x);
+            if (SAMP) {
+                float kap[EPV];
+                gumbel_keys<DT>(x, id0, grow, g, kap);
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) x[e] = kap[e];
+            }
 #pragma unroll
             for (int e = 0; e < EPV; ++e) {
                 if (x[e] != x[e]) continue;
@@ -447,16 +488,19 @@ __device__ __forceinline__ void segment_topk(ExpandSmem& sm, const unsigned char
 // exp-sum (when do_sum) and the group maxima; then tau and the segment's top-k
 // keys into sm.ctop (token ids id_base + element index in the row), and the
 // warps' (max, sum) into sm.wm / sm.ws.
-template <int DT>
+template <int DT, bool SAMP>
 __device__ __forceinline__ void segment_consume(ExpandSmem& sm, unsigned char* dyn_smem, int smem_bytes, int ns,
                                                 const char* row_base, int c0, int n, int nch, int k, bool do_sum,
-                                                int id_base, int* status) {
+                                                int id_base, int* status, uint32_t grow, const GumbelRng& g) {
     constexpr int ES = DT == 1 ? 2 : 4;
     constexpr int EPV = 16 / ES;
     constexpr int CE = kRowChunkBytes / ES;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // ---- one pass: lane maxima, online exp-sum, group maxima ----
+    // (sampled drafting: the lane and group maxima are those of the perturbed
+    // keys, kappa_l; the exp-sum stays that of the logits)
     float m_l = -INFINITY, s_l = 0.0f;  // lane: running max and sum of exp(x - m_l)
+    float kappa_l = -INFINITY;
     bool failed = false;
     for (int c = 0; c < nch; ++c) {
         const bool ok = ring_wait(sm.ring, c, ns, failed, status);
@@ -465,7 +509,21 @@ __device__ __forceinline__ void segment_consume(ExpandSmem& sm, unsigned char* d
         load_lane<DT>(dyn_smem + (c % ns) * kRowChunkBytes, nvec, warp, lane, u);
         ring_release(sm.ring, c, ns);
         const float cm = lane_max4<DT>(u);
-        gmax_put<DT>(sm, c, tid, warp * kVecPerWarp + lane < nvec ? f2o(cm) : 0u);
+        if (SAMP) {
+            float km = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < kVecPerLane; ++j) {
+                float x[EPV], kap[EPV];
+                unpack16<DT>(u[j], x);
+                gumbel_keys<DT>(x, c0 + c * CE + (warp * kVecPerWarp + j * 32 + lane) * EPV, grow, g, kap);
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) km = fmaxf(km, kap[e]);
+            }
+            gmax_put<DT>(sm, c, tid, warp * kVecPerWarp + lane < nvec ? f2o(km) : 0u);
+            kappa_l = fmaxf(kappa_l, km);
+        } else {
+            gmax_put<DT>(sm, c, tid, warp * kVecPerWarp + lane < nvec ? f2o(cm) : 0u);
+        }
         if (cm > m_l) {
             s_l = (do_sum && m_l > -INFINITY) ? s_l * ex2_approx((m_l - cm) * kLog2e) : 0.0f;
             m_l = cm;
@@ -491,8 +549,9 @@ __device__ __forceinline__ void segment_consume(ExpandSmem& sm, unsigned char* d
         }
     }
     // each warp's k largest lane maxima (0 bits: a lane without elements)
-    const uint32_t lo = warp_sort_desc_u32(m_l > -INFINITY || (nch > 0 && warp * kVecPerWarp + lane < n / EPV)
-                                               ? f2o(m_l) : 0u);
+    const float lane_key = SAMP ? kappa_l : m_l;
+    const uint32_t lo = warp_sort_desc_u32(lane_key > -INFINITY || (nch > 0 && warp * kVecPerWarp + lane < n / EPV)
+                                               ? f2o(lane_key) : 0u);
     if (lane < kMaxTopK) sm.wtop[warp][lane] = lane < k ? lo : 0u;
     // the warp's (max, sum)
     float sw = do_sum ? s_l : 0.0f, mw = m_l;
@@ -532,8 +591,8 @@ __device__ __forceinline__ void segment_consume(ExpandSmem& sm, unsigned char* d
     // a segment of at most ns chunks stays in the stages; the scratch then follows them
     const bool resident = nch <= ns;
     const int scratch_off = resident ? ns * kRowChunkBytes : 0;
-    segment_topk<DT>(sm, dyn_smem, resident, dyn_smem + scratch_off, smem_bytes - scratch_off, row_base, c0, n, nch,
-                     k, id_base);
+    segment_topk<DT, SAMP>(sm, dyn_smem, resident, dyn_smem + scratch_off, smem_bytes - scratch_off, row_base, c0, n,
+                           nch, k, id_base, grow, g);
 }
 
 // Merge of the CTAs of one row's cluster: every CTA pushes its top-k keys and
@@ -577,13 +636,14 @@ __device__ __forceinline__ bool cluster_row_merge(ExpandSmem& sm, cg::cluster_gr
     return true;
 }
 
-template <int DT>
-__global__ void __launch_bounds__(kRowThreads, 5) expand_kernel(TreeDims d, TreeWs w, int step, int seg, int ns,
+template <int DT, bool SAMP>
+__global__ void __launch_bounds__(kRowThreads, SAMP ? 3 : 5) expand_kernel(TreeDims d, TreeWs w, int step, int seg, int ns,
                                                                  int smem_bytes, const void* __restrict__ logits,
                                                                  const float* __restrict__ lse_in,
                                                                  float* __restrict__ row_lse,
                                                                  int32_t* __restrict__ ftok_out,
-                                                                 int32_t* __restrict__ fcount_out, int starve) {
+                                                                 int32_t* __restrict__ fcount_out, int starve,
+                                                                 GumbelRng grng) {
     extern __shared__ __align__(128) unsigned char dyn_smem[];
     __shared__ ExpandSmem sm;
     cg::cluster_group cluster = cg::this_cluster();
@@ -639,7 +699,8 @@ __global__ void __launch_bounds__(kRowThreads, 5) expand_kernel(TreeDims d, Tree
         }
         __syncwarp();
     } else {
-        segment_consume<DT>(sm, dyn_smem, smem_bytes, ns, row_base, c0, n, nch, k, lse_in == nullptr, 0, w.status);
+        segment_consume<DT, SAMP>(sm, dyn_smem, smem_bytes, ns, row_base, c0, n, nch, k, lse_in == nullptr, 0, w.status,
+                                  static_cast<uint32_t>(b * d.k + f), grng);
     }
     __syncthreads();
     const int F = sm.F;
@@ -666,7 +727,11 @@ __global__ void __launch_bounds__(kRowThreads, 5) expand_kernel(TreeDims d, Tree
         const int id = base + f * d.k + tid;
         const size_t at = static_cast<size_t>(b) * d.C + id;
         if (key != 0) {
-            const float x = key_val(key);
+            // the child's logit (sampled drafting: the key holds the perturbed value)
+            const float x = SAMP ? (DT == 1 ? __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(
+                                                                   row_base)[key_id(key)]) << 16)
+                                            : reinterpret_cast<const float*>(row_base)[key_id(key)])
+                                 : key_val(key);
             const float lp = __fsub_rn(x, lse);
             w.cand_token[at] = static_cast<int32_t>(key_id(key));
             w.cand_parent[at] = parent;
@@ -739,106 +804,6 @@ __global__ void __launch_bounds__(kRowThreads, 5) expand_kernel(TreeDims d, Tree
 }
 
 // ------------------------------------------------------------ verify kernel ---
-
-// Fixed-order exp for lossless verification (contract in eagle.h): Cody-Waite
-// reduction with ln2 = 0x1.62e4p-1 + 0x1.7f7d1cp-20, degree-7 Taylor series of
-// exp(r) in Horner form, exact scaling by 2^n. Every step is one correctly
-// rounded fp32 operation: n = z log2(e) rounded to nearest-even by one fused
-// multiply-add with 1.5 * 2^23, then fused multiply-adds for the reduction and
-// each Horner step. z <= 0. Returns p and the exponent n (value p * 2^n),
-// p = 0 below -32.
-__device__ __forceinline__ float dexp_parts(float z, int& n_out) {
-    if (!(z >= -32.0f)) {
-        n_out = 0;
-        return 0.0f;
-    }
-    const float t = __fmaf_rn(z, 0x1.715476p+0f, 12582912.0f);  // 1.5 * 2^23 + nearest integer
-    const float n = __fsub_rn(t, 12582912.0f);
-    n_out = __float_as_int(t) - 0x4B400000;
-    float r = __fmaf_rn(-n, 0x1.62e4p-1f, z);
-    r = __fmaf_rn(-n, 0x1.7f7d1cp-20f, r);
-    float p = 0x1.a01a02p-13f;              // 1/7!
-    p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);  // 1/6!
-    p = __fmaf_rn(p, r, 0x1.111112p-7f);   // 1/5!
-    p = __fmaf_rn(p, r, 0x1.555556p-5f);   // 1/4!
-    p = __fmaf_rn(p, r, 0x1.555556p-3f);   // 1/3!
-    p = __fmaf_rn(p, r, 0.5f);             // 1/2!
-    p = __fmaf_rn(p, r, 1.0f);             // 1/1!
-    p = __fmaf_rn(p, r, 1.0f);             // 1/0!
-    return p;
-}
-
-// Integer mass floor(dexp((x - m) * inv_t) * 2^40) = floor(p * 2^(n + 40)):
-// p's 24-bit significand shifted by (its exponent + n + 17), an exact
-// integer operation (the float product would be exact as well).
-__device__ __forceinline__ uint64_t fixed_mass(float x, float m, float inv_t) {
-    int n;
-    const float p = dexp_parts(__fmul_rn(__fsub_rn(x, m), inv_t), n);
-    const uint32_t bits = __float_as_uint(p);
-    const uint32_t sig = (bits & 0x7FFFFFu) | 0x800000u;
-    const int sh = static_cast<int>(bits >> 23) - 127 + n + 17;
-    if (p == 0.0f || sh <= -24) return 0ull;
-    return sh >= 0 ? static_cast<uint64_t>(sig) << sh : static_cast<uint64_t>(sig >> (-sh));
-}
-
-__device__ __forceinline__ uint64_t f2_add_rz(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("add.rz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
-// The masses of two elements at once, in two parts. The fixed-order exp's
-// fp32 operations run as packed pairs (each lane of a pair rounds exactly as
-// the scalar operation). Per element the mass is floor(f), f = p * 2^(n + 40)
-// < 2^41: n + 40 added to p's exponent field (exact: a normal float for
-// every argument in [-32, 0]); then hi = rz(f + 2^46) - 2^46 = floor(f / 2^23)
-// 2^23 and b = f - hi (both exact), lo = rz(b + 2^23) - 2^23 = floor(b), so
-// floor(f) = floor(f / 2^23) 2^23 + floor(b). The two parts of both elements
-// are added to *ahi (in units of 2^23, the float bits of rz(f + 2^46)
-// minus those of 2^46) and *alo (the bits of rz(b + 2^23) minus those of
-// 2^23). Arguments below -32 are clamped to -32, whose mass exp(-32) 2^40 < 1
-// is 0 as the definition's is for them. Equal to fixed_mass of each element.
-__device__ __forceinline__ void pair_mass_parts(float x0, float x1, uint64_t neg_m2, uint64_t inv_t2, uint32_t& ahi,
-                                                uint32_t& alo) {
-    uint64_t z = f2_mul(f2_add(f2_pack(x0, x1), neg_m2), inv_t2);
-    z = f2_pack(fmaxf(f2_lo(z), -32.0f), fmaxf(f2_hi(z), -32.0f));
-    const uint64_t t = f2_fma(z, f2_pack(0x1.715476p+0f, 0x1.715476p+0f), f2_pack(12582912.0f, 12582912.0f));
-    const uint64_t n = f2_add(t, f2_pack(-12582912.0f, -12582912.0f));
-    uint64_t r = f2_fma(n, f2_pack(-0x1.62e4p-1f, -0x1.62e4p-1f), z);
-    r = f2_fma(n, f2_pack(-0x1.7f7d1cp-20f, -0x1.7f7d1cp-20f), r);
-    uint64_t p = f2_fma(f2_pack(0x1.a01a02p-13f, 0x1.a01a02p-13f), r, f2_pack(0x1.6c16c2p-10f, 0x1.6c16c2p-10f));
-    p = f2_fma(p, r, f2_pack(0x1.111112p-7f, 0x1.111112p-7f));
-    p = f2_fma(p, r, f2_pack(0x1.555556p-5f, 0x1.555556p-5f));
-    p = f2_fma(p, r, f2_pack(0x1.555556p-3f, 0x1.555556p-3f));
-    p = f2_fma(p, r, f2_pack(0.5f, 0.5f));
-    p = f2_fma(p, r, f2_pack(1.0f, 1.0f));
-    p = f2_fma(p, r, f2_pack(1.0f, 1.0f));
-    // t's low word is n (t = 1.5 * 2^23 + n, exact), so t << 23 = n << 23 modulo 2^32
-    const uint32_t f0 = static_cast<uint32_t>(p) + (static_cast<uint32_t>(t) << 23) + (40u << 23);
-    const uint32_t f1 = static_cast<uint32_t>(p >> 32) + (static_cast<uint32_t>(t >> 32) << 23) + (40u << 23);
-    const uint64_t f = (static_cast<uint64_t>(f1) << 32) | f0;
-    const uint64_t k46 = f2_pack(0x1p46f, 0x1p46f), k23 = f2_pack(0x1p23f, 0x1p23f);
-    const uint64_t x46 = f2_add_rz(f, k46);                                  // 2^46 + floor(f / 2^23) 2^23
-    const uint64_t b = f2_add(f, f2_add(k46, x46 ^ 0x8000000080000000ull));  // f - (x46 - 2^46), exact
-    const uint64_t x23 = f2_add_rz(b, k23);                                  // 2^23 + floor(b)
-    ahi += (static_cast<uint32_t>(x46) - 0x56800000u) + (static_cast<uint32_t>(x46 >> 32) - 0x56800000u);
-    alo += (static_cast<uint32_t>(x23) - 0x4B000000u) + (static_cast<uint32_t>(x23 >> 32) - 0x4B000000u);
-}
-
-// The integer mass of the parts: ahi 2^23 + alo.
-__device__ __forceinline__ uint64_t mass_of_parts(uint32_t ahi, uint32_t alo) {
-    return (static_cast<uint64_t>(ahi) << 23) + alo;
-}
-
-// The masses of two elements, each on its own.
-__device__ __forceinline__ void pair_mass2(float x0, float x1, uint64_t neg_m2, uint64_t inv_t2, uint64_t& m0,
-                                           uint64_t& m1) {
-    uint32_t h0 = 0, l0 = 0, h1 = 0, l1 = 0;
-    pair_mass_parts(x0, -INFINITY, neg_m2, inv_t2, h0, l0);
-    pair_mass_parts(x1, -INFINITY, neg_m2, inv_t2, h1, l1);
-    m0 = mass_of_parts(h0, l0);
-    m1 = mass_of_parts(h1, l1);
-}
 
 struct VerifySmem {
     RowRing ring;
@@ -1322,7 +1287,8 @@ __global__ void __launch_bounds__(kRowThreads, 5) shard_partial_kernel(int Vs, i
             ring_produce(sm.ring, dyn_smem, row_base + static_cast<size_t>(c0) * ES, n * ES, nch, ns, status);
         __syncwarp();
     } else {
-        segment_consume<DT>(sm, dyn_smem, smem_bytes, ns, row_base, c0, n, nch, k, true, id_base, status);
+        segment_consume<DT, false>(sm, dyn_smem, smem_bytes, ns, row_base, c0, n, nch, k, true, id_base, status, 0u,
+                                   GumbelRng{});
     }
     __syncthreads();
     if (!cluster_row_merge(sm, cluster, rank, cpr, k)) return;
@@ -1526,6 +1492,16 @@ __global__ void __launch_bounds__(32) verify_argmax_kernel(TreeDims d, TreeWs w,
     }
 }
 
+// Inspection: the device's Gumbel noise of words and fixed-order logarithm of
+// values, element by element (checked bit for bit against the oracle's).
+__global__ void sampling_probe_kernel(const uint32_t* __restrict__ words, const float* __restrict__ ys, int n,
+                                      float* __restrict__ gumbel_out, float* __restrict__ log_out) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    if (words != nullptr) gumbel_out[i] = sampling::gumbel_of_word(words[i]);
+    if (ys != nullptr) log_out[i] = sampling::fixed_log(ys[i]);
+}
+
 // -------------------------------------------------------------- launchers ---
 
 static int sm_count() {
@@ -1601,7 +1577,8 @@ static cudaError_t launch_rows(K kernel, dim3 grid, int cpr, int smem, cudaStrea
 }
 
 cudaError_t launch_expand(const TreeDims& d, const TreeWs& ws, int step, const void* logits, const float* lse_in,
-                          float* row_lse, int32_t* ftok, int32_t* fcount_out, cudaStream_t stream, bool starve_ring) {
+                          float* row_lse, int32_t* ftok, int32_t* fcount_out, cudaStream_t stream, bool starve_ring,
+                          const uint64_t* sample_seed_cycle) {
     const int esize = d.dtype == 1 ? 2 : 4;
     const long rows = static_cast<long>(d.B) * (step == 0 ? 1 : d.k);  // step 0 reads the root rows only
     const int max_seg = esize == 2 ? kMaxSegChunksBf16 : kMaxSegChunks;
@@ -1648,6 +1625,12 @@ cudaError_t launch_expand(const TreeDims& d, const TreeWs& ws, int step, const v
     const int pick = kMaxTopK * kMaxTopK * (8 + 4) + kMaxTopK * 4 + 16;
     const int smem = std::max(pick, p.nch <= p.stages ? p.stages * kRowChunkBytes + scratch : std::max(p.smem, scratch));
     int seg = p.seg, ns = p.stages, smem_bytes = smem, starve = starve_ring ? 1 : 0;
+    GumbelRng grng{};
+    if (sample_seed_cycle != nullptr) {
+        const uint64_t seed = sample_seed_cycle[0], cycle = sample_seed_cycle[1];
+        grng = GumbelRng{static_cast<uint32_t>(seed) ^ 10u, static_cast<uint32_t>(seed >> 32),
+                         static_cast<uint32_t>(step), static_cast<uint32_t>(cycle)};
+    }
     void* args[] = {&dd,
                     &ww,
                     &step,
@@ -1659,9 +1642,13 @@ cudaError_t launch_expand(const TreeDims& d, const TreeWs& ws, int step, const v
                     &row_lse,
                     &ftok,
                     &fcount_out,
-                    &starve};
-    return d.dtype == 1 ? launch_rows(expand_kernel<1>, grid, p.cpr, smem, stream, args)
-                        : launch_rows(expand_kernel<0>, grid, p.cpr, smem, stream, args);
+                    &starve,
+                    &grng};
+    if (sample_seed_cycle != nullptr)
+        return d.dtype == 1 ? launch_rows(expand_kernel<1, true>, grid, p.cpr, smem, stream, args)
+                            : launch_rows(expand_kernel<0, true>, grid, p.cpr, smem, stream, args);
+    return d.dtype == 1 ? launch_rows(expand_kernel<1, false>, grid, p.cpr, smem, stream, args)
+                        : launch_rows(expand_kernel<0, false>, grid, p.cpr, smem, stream, args);
 }
 
 cudaError_t launch_verify(const TreeDims& d, const TreeWs& ws, int mode, float inv_temp, const void* target,
@@ -1732,6 +1719,13 @@ cudaError_t launch_verify_argmax(const TreeDims& d, const TreeWs& ws, const int3
                                  int32_t* out_tokens, cudaStream_t stream) {
     return launch_pdl(verify_argmax_kernel, dim3(d.B), dim3(32), 0, stream, d, ws, row_argmax, tokens, parent, n_tree,
                       accept_len, slots, out_tokens);
+}
+
+cudaError_t launch_sampling_probe(const uint32_t* words, const float* ys, int n, float* gumbel_out, float* log_out,
+                                  cudaStream_t stream) {
+    count_launch();
+    sampling_probe_kernel<<<(n + 255) / 256, 256, 0, stream>>>(words, ys, n, gumbel_out, log_out);
+    return cudaGetLastError();
 }
 
 }  // namespace eagle

@@ -21,7 +21,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 EAGLE_OK = 0
 EAGLE_F32, EAGLE_BF16 = 0, 1
-GREEDY, LOSSLESS = 0, 1
+GREEDY, LOSSLESS, DRAFT = 0, 1, 2
 MAX_TOPK, MAX_DEPTH, MAX_SLOTS, MAX_CANDIDATES = 16, 16, 256, 1024
 
 
@@ -73,6 +73,7 @@ _lib.eagle_workspace_bytes.argtypes = [_TP]
 _lib.eagle_workspace_bytes.restype = _sz
 _lib.eagle_tree_init.argtypes = [_TP, _p, _sz, _p]
 _lib.eagle_expand.argtypes = [_TP, _p, _sz, _i, _p, _p, _p, _p, _p, _p]
+_lib.eagle_expand_sampled.argtypes = [_TP, _p, _sz, _i, _p, _p, ctypes.c_uint64, ctypes.c_uint64, _p, _p, _p, _p]
 _lib.eagle_test_expand_starved.argtypes = [_TP, _p, _sz, _i, _p, _p, _p, _p, _p]
 _lib.eagle_lmhead.argtypes = [_TP, _p, _sz, _i, _p, _p, _p, _p]
 _lib.eagle_rerank.argtypes = [_TP, _p, _sz, _p]
@@ -92,6 +93,7 @@ _lib.eagle_verify_static.argtypes = [_TP, _i, ctypes.c_float, _u64, _u64, _p, _p
 _lib.eagle_status_fetch.argtypes = [_p, ctypes.POINTER(ctypes.c_int), _p]
 _lib.eagle_tree_export.argtypes = [_TP, _p, _sz, _p, _p, _p, _p, _p, _p, _p, _p]
 _lib.eagle_verify_export.argtypes = [_TP, _p, _sz, _p, _p, _p, _p]
+_lib.eagle_test_sampling.argtypes = [_p, _p, _i, _p, _p, _p]
 _lib.eagle_kernel_launches.restype = ctypes.c_uint64
 _lib.eagle_last_cuda_error.argtypes = [ctypes.POINTER(ctypes.c_char_p)]
 _lib.eagle_last_cuda_error.restype = _i
@@ -147,6 +149,15 @@ def eagle_expand(cfg, ws, step, draft_logits, row_lse_in, row_lse, frontier_toke
     _check("eagle_expand", _lib.eagle_expand(ctypes.byref(cfg), *_ws(ws), step, _ptr(draft_logits),
                                              _ptr(row_lse_in), _ptr(row_lse), _ptr(frontier_tokens),
                                              _ptr(frontier_count), _stream(stream)))
+
+
+def eagle_expand_sampled(cfg, ws, step, draft_logits, row_lse_in, seed, cycle, row_lse, frontier_tokens,
+                         frontier_count, stream=None):
+    """Stages 1+2 with the children drawn from each row's softmax without replacement (Gumbel-top-k)."""
+    _check("eagle_expand_sampled", _lib.eagle_expand_sampled(ctypes.byref(cfg), *_ws(ws), step, _ptr(draft_logits),
+                                                             _ptr(row_lse_in), int(seed), int(cycle), _ptr(row_lse),
+                                                             _ptr(frontier_tokens), _ptr(frontier_count),
+                                                             _stream(stream)))
 
 
 def eagle_test_expand_starved(cfg, ws, step, draft_logits, row_lse, frontier_tokens, frontier_count, stream=None):
@@ -252,6 +263,11 @@ def eagle_tree_export(cfg, ws, cand_token=None, cand_parent=None, cand_depth=Non
 def eagle_verify_export(cfg, ws, row_max=None, row_argmax=None, row_mass=None, stream=None):
     _check("eagle_verify_export", _lib.eagle_verify_export(ctypes.byref(cfg), *_ws(ws), _ptr(row_max),
                                                            _ptr(row_argmax), _ptr(row_mass), _stream(stream)))
+
+
+def eagle_test_sampling(words, ys, n, gumbel_out, log_out, stream=None):
+    _check("eagle_test_sampling", _lib.eagle_test_sampling(_ptr(words), _ptr(ys), n, _ptr(gumbel_out), _ptr(log_out),
+                                                           _stream(stream)))
 
 
 def eagle_kernel_launches() -> int:

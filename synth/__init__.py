@@ -51,6 +51,7 @@ def _load():
         lib.synth_words.argtypes = [p, i64, i64, u32, u64, u32]
         lib.synth_seq_params.argtypes = [i32, i32, i32, f64, f64, u64, p, p]
         lib.synth_threads.restype = i32
+        lib.synth_gumbel_words.argtypes = [p, i32, i32, i32, u32, u32, u64]
         _lib = lib
     return _lib
 
@@ -105,6 +106,15 @@ def kv_region(base: np.ndarray, dtype: int, offset: int, pos_stride: int, hkv: i
 def words(n1: int, n0: int, c2: int, seed: int, stream: int = STREAM_VERIFY) -> np.ndarray:
     out = np.empty((n1, n0), dtype=np.uint32)
     _load().synth_words(_ptr(out), n0, n1, c2, seed, stream)
+    return out
+
+
+def gumbel_words(B: int, k: int, V: int, step: int, cycle: int, seed: int) -> np.ndarray:
+    """[B, k, V] uniform words of sampled drafting for one draft step: element
+    (b, f, x) is word x & 3 of Philox4x32-10 at counter (x >> 2, b * k + f,
+    step, cycle), key (seed_lo ^ 10, seed_hi)."""
+    out = np.empty((B, k, V), dtype=np.uint32)
+    _load().synth_gumbel_words(_ptr(out), B, k, V, step, cycle, seed)
     return out
 
 

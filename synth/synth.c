@@ -171,3 +171,18 @@ int synth_threads(void) {
     return 1;
 #endif
 }
+
+/* Uniform words of sampled drafting, one Philox call per four elements:
+ * out[(b * k + f) * V + x] = word (x & 3) of Philox4x32-10 at counter
+ * (x >> 2, b * k + f, step, cycle), key (seed_lo ^ 10, seed_hi). */
+void synth_gumbel_words(uint32_t* out, int B, int k, int V, uint32_t step, uint32_t cycle, uint64_t seed) {
+    const int rows = B * k;
+#pragma omp parallel for schedule(static)
+    for (int r = 0; r < rows; ++r) {
+        for (int q = 0; 4 * q < V; ++q) {
+            uint32_t w[4];
+            draw(seed, 10, (uint32_t)q, (uint32_t)r, step, cycle, w);
+            for (int i = 0; i < 4 && 4 * q + i < V; ++i) out[(int64_t)r * V + 4 * q + i] = w[i];
+        }
+    }
+}
