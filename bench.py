@@ -204,9 +204,11 @@ def stop_clocks(h) -> dict | None:
 
 
 CSRC = os.path.join(ROOT, "speculative_decoding_dynamic_gb300", "csrc")
-# translation unit of each profiled kernel
-KERNEL_TU = {"expand_kernel": "k_rows.cu", "verify_kernel": "k_rows.cu", "attention": "k_attn_tc.cu",
-             "lmhead_kernel": "k_lmhead.cu", "kv_compact_kernel": "k_compact.cu"}
+# translation unit(s) of each profiled kernel (attention: the per-item kernel
+# and the persistent pipeline, either may run depending on the shape)
+KERNEL_TU = {"expand_kernel": "k_rows.cu", "verify_kernel": "k_rows.cu",
+             "attention": ("k_attn_tc.cu", "k_attn_pipe.cu"), "lmhead_kernel": "k_lmhead.cu",
+             "kv_compact_kernel": "k_compact.cu"}
 
 
 def _toolchain_id() -> bytes:
@@ -250,7 +252,8 @@ def kernel_src_hash() -> str:
 def tu_src_hash(kernel: str) -> str:
     """Hash of the sources one profiled kernel is compiled from (its .cu file
     and the headers it includes, with the toolchain)."""
-    return _src_hash([KERNEL_TU[kernel]])
+    tu = KERNEL_TU[kernel]
+    return _src_hash([tu] if isinstance(tu, str) else list(tu))
 
 
 def ncu_traffic(kernel: str, workload_name: str):

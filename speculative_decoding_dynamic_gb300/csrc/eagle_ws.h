@@ -180,6 +180,12 @@ cudaError_t launch_kv_compact(const KvDims& kv, void* cache, const int32_t* pref
                               cudaStream_t stream);
 
 size_t attention_ws_bytes(const KvDims& kv, int T);
+// The persistent two-CTA-per-SM attention pipeline (k_attn_pipe.cu) serves
+// shapes whose unsplit items fill two CTAs on every SM.
+bool attention_pipe_fits(const KvDims& kv, int T);
+cudaError_t launch_attention_pipe(const KvDims& kv, int T, const void* q, const void* cache, int layer,
+                                  const int32_t* prefix_len, const uint32_t* mask, const int32_t* n_tree, void* out,
+                                  int* status, cudaStream_t stream);
 // LM-head logits [M, V] (fp32, or bf16 when out_dtype is 1) of hidden [M, H]
 // and weight [V, H] (bf16), on the tensor cores.
 cudaError_t launch_lmhead(int M, int V, int H, const void* hidden, const void* weight, int out_dtype, void* out,

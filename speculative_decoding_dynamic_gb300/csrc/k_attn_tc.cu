@@ -38,6 +38,7 @@
 #include <cmath>
 #include <mutex>
 
+#include "attn_common.cuh"
 #include "eagle_internal.cuh"
 #include "eagle_ws.h"
 #include "tc_ptx.cuh"
@@ -82,27 +83,6 @@ struct TcParams {
 
 // ---------------------------------------------------------------- PTX ---
 // TMA, tcgen05 MMA and tensor-memory helpers: tc_ptx.cuh.
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-// Three-input maximum (NaN operands are dropped, like fmaxf).
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-    float d;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
-
-// Largest of 32 values: a tree of three-input maxima (depth 4).
-__device__ __forceinline__ float max32(const float (&v)[32]) {
-    float t[11];
-#pragma unroll
-    for (int q = 0; q < 10; ++q) t[q] = fmax3(v[3 * q], v[3 * q + 1], v[3 * q + 2]);
-    t[10] = fmaxf(v[30], v[31]);
-    return fmaxf(fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmax3(t[6], t[7], t[8])), fmaxf(t[9], t[10]));
-}
 
 __device__ __forceinline__ void named_sync_softmax() { asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory"); }
 // The two warps of softmax group g that serve one TMEM lane quarter (the
@@ -576,6 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 struct Plan {
     int G, n_rb, nsplit, tps, units;
+    double cost;  // the cost model's estimate, in 128-key tile times of one SM
     size_t off_tickets, off_ml, off_o, bytes;
 };
 
@@ -605,6 +586,7 @@ Plan make_plan(const KvDims& kv, int T) {
     }
     pl.tps = (max_tiles + nsplit - 1) / nsplit;
     pl.nsplit = (max_tiles + pl.tps - 1) / pl.tps;
+    pl.cost = best;
     pl.off_tickets = 256;
     pl.off_ml = align_up(pl.off_tickets + static_cast<size_t>(pl.units) * sizeof(int), 256);
     const size_t slots = pl.nsplit > 1 ? static_cast<size_t>(pl.units) * pl.nsplit : 0;
@@ -620,14 +602,17 @@ bool tc_supported(const KvDims& kv, int T) {
            (kv.kv_stride * 2) % 16 == 0;
 }
 
-bool make_map(CUtensorMap* m, const void* base, const cuuint64_t dims[4], const cuuint64_t strides_bytes[3],
-              const cuuint32_t box[4]) {
-    auto fn = tensor_map_encode_fn();
-    if (!fn) return false;
-    const cuuint32_t estride[4] = {1, 1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides_bytes, box, estride,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+// The persistent pipeline (k_attn_pipe.cu) when its estimated time is the
+// lower one. Both estimates take every unit at the longest length; measured
+// on GB300 at 8B b64: about 1.15 us per 128-key tile of a CTA here, 1.1 us
+// per 64-key tile of each of the pipeline's two CTAs per SM, whose items are
+// never split (so a few very long ones leave SMs idle: 70B b8).
+bool use_pipeline(const KvDims& kv, int T) {
+    if (!attention_pipe_fits(kv, T)) return false;
+    const Plan pl = make_plan(kv, T);
+    const int tiles64 = (kv.max_len + 63) / 64;
+    const double pipe_us = std::ceil(static_cast<double>(pl.units) / (2.0 * 152)) * (tiles64 + 4.0) * 1.1;
+    return pipe_us < pl.cost * 1.15;
 }
 
 }  // namespace
@@ -647,7 +632,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encode_fn() {
 }
 
 size_t attention_ws_bytes(const KvDims& kv, int T) {
-    if (!tc_supported(kv, T)) return 256;
+    if (!tc_supported(kv, T) || use_pipeline(kv, T)) return 256;
     return make_plan(kv, T).bytes;
 }
 
@@ -656,6 +641,11 @@ cudaError_t launch_attention(const KvDims& kv, int T, const void* q, const void*
                              void* ws, size_t ws_bytes, int* status, cudaStream_t stream) {
     if (!tc_supported(kv, T))
         return launch_attention_simt(kv, T, q, cache, layer, prefix_len, mask, n_tree, out, status, stream);
+    // many (sequence, KV head, row block) items of moderate length: the
+    // persistent pipeline (k_attn_pipe.cu); else one CTA per item and key
+    // split, two softmax groups each
+    if (use_pipeline(kv, T))
+        return launch_attention_pipe(kv, T, q, cache, layer, prefix_len, mask, n_tree, out, status, stream);
     const Plan pl = make_plan(kv, T);
     if (ws_bytes < pl.bytes) return cudaErrorInvalidValue;
     char* w = static_cast<char*>(ws);
@@ -668,7 +658,7 @@ cudaError_t launch_attention(const KvDims& kv, int T, const void* q, const void*
         const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kHD) * 2, static_cast<cuuint64_t>(kv.Hq) * kHD * 2,
                                        static_cast<cuuint64_t>(T) * kv.Hq * kHD * 2};
         const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(pl.G), static_cast<cuuint32_t>(kBM / pl.G), 1};
-        if (!make_map(&tq, q, dims, strides, box)) return cudaErrorInvalidValue;
+        if (!make_map_bf16_4d(&tq, q, dims, strides, box)) return cudaErrorInvalidValue;
     }
     {
         const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHD), static_cast<cuuint64_t>(kv.Hkv),
@@ -676,8 +666,8 @@ cudaError_t launch_attention(const KvDims& kv, int T, const void* q, const void*
         const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kHD) * 2, static_cast<cuuint64_t>(kv.pos_stride) * 2,
                                        static_cast<cuuint64_t>(kv.seq_stride) * 2};
         const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kBN), 1};
-        if (!make_map(&tk, kbase, dims, strides, box)) return cudaErrorInvalidValue;
-        if (!make_map(&tv, vbase, dims, strides, box)) return cudaErrorInvalidValue;
+        if (!make_map_bf16_4d(&tk, kbase, dims, strides, box)) return cudaErrorInvalidValue;
+        if (!make_map_bf16_4d(&tv, vbase, dims, strides, box)) return cudaErrorInvalidValue;
     }
     TcParams prm{};
     prm.B = kv.B;

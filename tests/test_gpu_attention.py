@@ -16,7 +16,7 @@ import harness as H
 pytestmark = pytest.mark.gpu
 
 
-def _case(B, Hq, Hkv, d, k, D, N, L, max_len, dtype, seed, nan_tail=True, threshold=0.0):
+def _case(B, Hq, Hkv, d, k, D, N, L, max_len, dtype, seed, nan_tail=True, threshold=0.0, with_vmax=False):
     import torch
     from speculative_decoding_dynamic_gb300 import eagle as E
 
@@ -59,6 +59,8 @@ def _case(B, Hq, Hkv, d, k, D, N, L, max_len, dtype, seed, nan_tail=True, thresh
     torch.cuda.synchronize()
     assert E.eagle_status_fetch(ws) == 0
     got = H.f32(H.to_host(out))
+    if with_vmax:
+        return got, want, tr, float(np.nanmax(np.abs(H.f32(vh))))  # (tails past the keys hold NaN)
     return got, want, tr
 
 
@@ -90,3 +92,31 @@ def test_tensor_core_attention_with_threshold_padding():
 def test_fp32_attention_matches_oracle(d):
     got, want, _ = _case(2, 4, 2, d, 2, 3, 8, [32, 7], 64, synth.F32, seed=3, nan_tail=False)
     assert np.abs(got - want).max() <= 1e-4
+
+
+# Shapes whose (sequence, KV head, row block) items fill two CTAs on every SM
+# run on the persistent pipeline kernel (64-key tiles, two CTAs per SM,
+# sequences longest first). Bound, element by element, from the arithmetic:
+# each weight p_k enters PV as bf16 (relative error <= 2^-9), which moves
+# sum_k p_k v_k / l by at most 2^-9 max|V|; the row sum l is taken from the
+# unrounded p and the output is rounded to bf16, each <= 2^-9 |o|; 1e-4
+# covers the fp32 sums. Rows that see only a few keys (prefix 0 or 1) reach
+# |o| > 2, where a bf16 step is 2^-6, so a flat 1e-2 would not follow.
+@pytest.mark.parametrize("B,Hq,Hkv,N,k,D,lmax,seed,threshold", [
+    (20, 32, 8, 60, 10, 6, 700, 21, 0.0),   # G=4, two row blocks: 320 items
+    (40, 8, 8, 60, 10, 6, 400, 22, 0.0),    # G=1, one row block of 61 rows: 320 items
+    (24, 32, 8, 40, 4, 4, 300, 23, 0.2),    # threshold-pruned trees: padded slots
+])
+def test_persistent_pipeline_matches_oracle(B, Hq, Hkv, N, k, D, lmax, seed, threshold):
+    rng = np.random.default_rng(seed)
+    L = rng.integers(0, lmax, B)
+    L[:4] = [0, 1, 63, 64]  # empty prefix, tile edges
+    max_len = int((L.max() + N + 1 + 63) // 64 * 64)
+    got, want, tr, vmax = _case(B, Hq, Hkv, 128, k, D, N, list(L), max_len, synth.BF16, seed=seed,
+                                threshold=threshold, with_vmax=True)
+    assert np.isfinite(got).all()
+    bound = 2.0 ** -8 * np.abs(want) + 2.0 ** -9 * vmax + 1e-4
+    excess = np.abs(got - want) - bound
+    assert excess.max() <= 0.0, (float(excess.max()), float(np.abs(got - want).max()))
+    for b in range(B):
+        assert (got[b, tr["n_tree"][b]:] == 0).all()
