@@ -280,7 +280,9 @@ int eagle_tree_attention(const eagle_kv_cfg* kv, int T, const void* q, const voi
  *   kept children are tested in slot order and child x is accepted iff
  *   U24 * S < 2^24 * P_u[x] (S = remaining mass); a rejection removes x. With
  *   no child accepted the bonus is the smallest token y (not removed) whose
- *   running mass exceeds floor(U64 * S / 2^64).
+ *   running mass exceeds floor(U64 * S / 2^64). Every row's maximum is taken
+ *   in one pass over all rows; the masses of a row are summed only when the
+ *   walk reaches its node (one cluster of CTAs per sequence).
  * DRAFT (temperature > 0; children drawn by eagle_expand_sampled): at node u
  *   with target residual A (initially P_u) and the remaining draft masses Q
  *   of u's draft row (integer masses as above, at the same temperature), the
@@ -374,12 +376,9 @@ int eagle_verify_argmax(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, co
  * on the allocator). No counterpart on the pages: it is the same stage 6 as
  * eagle_verify, with the same arguments and results, minus ws/ws_bytes.
  *   - Its per-row scratch is one fixed device array inside the library
- *     (about 4.3 MB, present on every GPU that loads the library until the
- *     process exits). It supports batch <= 1024, batch * (node_budget + 1)
- *     <= 4096 rows and, in LOSSLESS mode, rows * mass pieces <= 4096 * 128 (a
- *     row has 128 pieces at a 128256-entry bf16 vocabulary, 64 * ceil(vocab *
- *     element size / 131072) in general) and returns EAGLE_ERR_UNSUPPORTED
- *     beyond.
+ *     (about 70 KB, present on every GPU that loads the library until the
+ *     process exits). It supports batch <= 1024 and batch * (node_budget + 1)
+ *     <= 4096 rows in either mode and returns EAGLE_ERR_UNSUPPORTED beyond.
  *   - The first call on a device looks up that array's device address; make
  *     that first call before any stream capture. The address is kept per
  *     device for the life of the process: do not call this after
@@ -415,7 +414,8 @@ int eagle_tree_export(const eagle_tree_cfg* cfg, const void* ws, size_t ws_bytes
 
 /* Copy the per-row target statistics of the last eagle_verify: row maximum
  * [B, T] fp32, argmax [B, T] int32, integer mass sum_x P_t[x] [B, T] uint64
- * (lossless only). Rows t >= n_tree are unspecified. */
+ * (lossless only: the rows of the nodes the walk visited, 0 for the others).
+ * Rows t >= n_tree are unspecified. */
 int eagle_verify_export(const eagle_tree_cfg* cfg, const void* ws, size_t ws_bytes, float* row_max,
                         int32_t* row_argmax, uint64_t* row_mass, void* stream);
 

@@ -68,6 +68,13 @@ __device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
     }
     return v;
 }
+// Bits of the lanes below this one.
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
 __device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
 #pragma unroll
     for (int m = 16; m > 0; m >>= 1) v += shfl_xor_u64(v, m);

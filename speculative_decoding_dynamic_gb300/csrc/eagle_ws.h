@@ -31,11 +31,6 @@ inline int row_seg_elems(int V, int esize, int cpr) {
     return (seg + epv - 1) / epv * epv;
 }
 inline int row_chunks(int seg, int esize) { return (seg * esize + kRowChunkBytes - 1) / kRowChunkBytes; }
-// Lossless verification keeps a row's segments resident (cpr = kMaxChunks) and
-// records one integer mass per (chunk, warp) piece of the row.
-inline int verify_mass_slots(int V, int esize) {
-    return kMaxChunks * row_chunks(row_seg_elems(V, esize, kMaxChunks), esize) * kRowWarpsPerCta;
-}
 
 // Resolved problem description passed by value to kernels.
 struct TreeDims {
@@ -65,7 +60,6 @@ struct TreeWs {
     float* row_max;         // [B, T] verify row maximum
     int32_t* row_arg;       // [B, T] verify row argmax
     uint64_t* row_mass;     // [B, T] verify integer mass
-    uint64_t* chunk_mass;   // [B, T, verify_mass_slots] verify integer mass per row piece
     uint64_t* resid;        // [B, V] target residual of the draft-probability rule
 };
 
@@ -100,7 +94,6 @@ inline size_t ws_layout(const TreeDims& d, void* base, TreeWs* ws) {
     w.row_max = static_cast<float*>(take(B * T * 4));
     w.row_arg = static_cast<int32_t*>(take(B * T * 4));
     w.row_mass = static_cast<uint64_t*>(take(B * T * 8));
-    w.chunk_mass = static_cast<uint64_t*>(take(B * T * verify_mass_slots(d.V, d.dtype == 1 ? 2 : 4) * 8));
     w.resid = static_cast<uint64_t*>(take(B * static_cast<size_t>(d.V) * 8));
     if (ws) *ws = w;
     return align_up(off, 256);
@@ -113,11 +106,9 @@ struct RowPlan {
     int nch;     // chunks per full segment
     int stages;  // shared-memory stages (all nch when the segment stays resident)
     int smem;    // dynamic shared memory per CTA
-    int slots;   // integer-mass pieces per row (resident plans)
 };
-// rows = logit rows of the launch; resident = the whole segment stays in
-// shared memory (needed by the second pass of lossless verification).
-RowPlan plan_rows(int V, int esize, long rows, bool resident, int max_stages, int max_seg_chunks);
+// rows = logit rows of the launch.
+RowPlan plan_rows(int V, int esize, long rows, int max_stages, int max_seg_chunks);
 
 // ----------------------------------------------------------- launchers ---
 // Each returns cudaSuccess or the launch error. All enqueue on `stream`.
@@ -148,6 +139,11 @@ inline VerifyRng verify_rng(uint64_t seed, uint64_t cycle) {
 cudaError_t launch_verify(const TreeDims& d, const TreeWs& ws, int mode, float inv_temp, const void* target,
                           const int32_t* tokens, const int32_t* parent, const int32_t* n_tree, VerifyRng rng,
                           int32_t* accept_len, int32_t* slots, int32_t* out_tokens, cudaStream_t stream);
+// Lossless acceptance walk (after launch_verify's row statistics): one
+// cluster per sequence; the integer masses of the rows it visits only.
+cudaError_t launch_verify_walk(const TreeDims& d, const TreeWs& ws, float inv_temp, VerifyRng rng, const void* target,
+                               const int32_t* tokens, const int32_t* parent, const int32_t* n_tree,
+                               int32_t* accept_len, int32_t* slots, int32_t* out_tokens, cudaStream_t stream);
 
 // Vocabulary slices: stage-1 partials of `rows` rows of a slice [rows, Vs]
 // (keys carry token id id_base + index), their merge over S slices, stage 2

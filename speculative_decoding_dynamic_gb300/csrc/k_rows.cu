@@ -180,11 +180,6 @@ __device__ __forceinline__ void warp_sort_desc(K (&v)[E]) {
     }
 }
 
-__device__ __forceinline__ unsigned lanemask_lt() {
-    unsigned m;
-    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-    return m;
-}
 
 // Rank of `key` among the first n of kMaxChunks lists of kMaxTopK keys
 // (zeros = empty): how many keys are larger. Every list is read whole (zero
@@ -807,55 +802,32 @@ __global__ void __launch_bounds__(kRowThreads, SAMP ? 3 : 5) expand_kernel(TreeD
 
 struct VerifySmem {
     RowRing ring;
-    // walk inputs that do not depend on other rows, read by every leader
-    // while its row streams (the leader that arrives last walks the tree)
     int tok[kMaxSlots];
     int par[kMaxSlots];
-    float xtok[kMaxSlots];       // slot c's token logit in its parent's row (lossless)
-    uint32_t uni[kMaxSlots + 2];  // uniform words (lossless)
     uint64_t wkey[kConsumerWarps];
-    unsigned long long wmass[kConsumerWarps];
-    uint64_t rkey[kMaxChunks];   // every rank's segment maximum
-    uint64_t rmass[kMaxChunks];  // every rank's segment mass (pushed to the leader)
+    uint64_t rkey[kMaxChunks];  // every rank's segment maximum (pushed to the leader)
     int last;
 };
 
-// Acceptance-walk state of the last-arriving CTA of a sequence; it lives in
-// the (then idle) dynamic shared memory of the chunk ring.
+// Greedy-walk state of the last-arriving CTA of a sequence; it lives in the
+// (then idle) dynamic shared memory of the chunk ring.
 struct WalkSmem {
     int arg[kMaxSlots];
-    float rmax[kMaxSlots];
-    unsigned long long rowmass[kMaxSlots];
-    unsigned long long pmass[kMaxSlots];  // mass of slot c's token in its parent's row
-    unsigned long long piece[kMaxChunks * kRowStages * kConsumerWarps];  // residual mass of each piece of row cur
     int path[kMaxDepth + 1];
     int child[kMaxTopK];
-    int removed_tok[kMaxTopK];
-    unsigned long long removed_mass[kMaxTopK];
-    unsigned long long scan[4];
-    unsigned long long t_in;
-    int n_removed, a, cur, bonus, bad, piece_at;
+    int a, bonus, bad;
 };
 
-// Element range [lo, hi) of integer-mass piece q of a row: piece (rank, chunk,
-// warp) of a resident plan with `nch` chunks per segment of `seg` elements.
-__device__ __forceinline__ void piece_range(int q, int nch, int seg, int V, int CE, int EPV, int& lo, int& hi) {
-    const int r = q / (nch * kConsumerWarps);
-    const int c = (q / kConsumerWarps) % nch;
-    const int wq = q % kConsumerWarps;
-    const int s_end = min(V, (r + 1) * seg);
-    const int cs = r * seg + c * CE;
-    const int ce = min(cs + CE, s_end);
-    lo = cs + wq * kVecPerWarp * EPV;
-    hi = max(lo, min(lo + kVecPerWarp * EPV, ce));
-}
-
+// Stage 6 over the target rows: every row's maximum and argmax (lowest id
+// among equal values). MODE 0 (greedy): the last row of a sequence to finish
+// walks its tree. MODE 1 (lossless): the statistics only, the walk is
+// verify_lossless_walk_kernel.
 template <int DT, int MODE>
-__global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs w, float inv_t, int seg, int ns,
-                                                              int nslot, const void* __restrict__ target,
+__global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs w, int seg, int ns,
+                                                              const void* __restrict__ target,
                                                               const int32_t* __restrict__ tokens,
                                                               const int32_t* __restrict__ parent,
-                                                              const int32_t* __restrict__ n_tree, VerifyRng rng,
+                                                              const int32_t* __restrict__ n_tree,
                                                               int32_t* __restrict__ accept_len,
                                                               int32_t* __restrict__ slots_out,
                                                               int32_t* __restrict__ tokens_out) {
@@ -895,36 +867,6 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
     if (warp == kProducerWarp) {
         if (lane == 0 && nch > 0) {
             ring_produce(sm.ring, dyn_smem, row_base + static_cast<size_t>(c0) * ES, len * ES, nch, ns, w.status);
-        } else if (MODE == 1 && rank == 0 && lane > 0) {
-            // Lossless: the walk's inputs that do not depend on other rows, read
-            // while the row streams (every leader, whose copies are all issued
-            // at once; the leader that arrives last walks).
-            const size_t tb = static_cast<size_t>(b) * d.T;
-            for (int c = lane - 1; c < n; c += 31) {
-                sm.tok[c] = tokens[tb + c];
-                sm.par[c] = parent[tb + c];
-            }
-            {
-                __syncwarp(0xfffffffeu);
-                for (int c = lane - 1; c < n; c += 31) {
-                    const int tk = sm.tok[c], p = sm.par[c];
-                    float x = 0.0f;
-                    if (c > 0 && tk >= 0 && tk < d.V && p >= 0 && p < c) {
-                        const char* prow = static_cast<const char*>(target) + (tb + p) * d.V * ES;
-                        x = DT == 1 ? __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(prow)[tk])
-                                                      << 16)
-                                    : reinterpret_cast<const float*>(prow)[tk];
-                    }
-                    sm.xtok[c] = x;
-                }
-                // uniform word c of sequence b: Philox4x32-10 at counter (c, b, cycle), word 0
-                for (int c = lane - 1; c < d.T + 2; c += 31) {
-                    const uint32_t ctr[4] = {static_cast<uint32_t>(c), static_cast<uint32_t>(b), rng.c2, rng.c3};
-                    uint32_t out[4];
-                    sampling::philox4x32_10(ctr, rng.k0, rng.k1, out);
-                    sm.uni[c] = out[0];
-                }
-            }
         }
         __syncwarp();
     } else {
@@ -966,96 +908,42 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
     if (warp == 0) {
         uint64_t m = lane < kConsumerWarps ? sm.wkey[lane] : 0ull;
         m = warp_max_u64(m);
-        if (MODE == 1) {
-            if (lane < cpr) cluster.map_shared_rank(&sm, lane)->rkey[rank] = m;  // to every rank
-        } else if (lane == 0) {
-            cluster.map_shared_rank(&sm, 0)->rkey[rank] = m;
-        }
+        if (lane == 0) cluster.map_shared_rank(&sm, 0)->rkey[rank] = m;
     }
     cluster.sync();
-    if (MODE == 0 && rank != 0) return;
+    if (rank != 0) return;
     uint64_t gkey = 0;
     for (int r = 0; r < cpr; ++r) gkey = sm.rkey[r] > gkey ? sm.rkey[r] : gkey;
     const float M = key_val(gkey);
     const size_t rt = static_cast<size_t>(b) * d.T + t;
-    if (MODE == 1) {
-        // ---- pass 2: integer masses of the resident segment, one per (chunk, warp) ----
-        const int nch_full = nslot / (cpr * kConsumerWarps);
-        unsigned long long wtot = 0;
-        const uint64_t neg_m2 = f2_pack(-M, -M), inv_t2 = f2_pack(inv_t, inv_t);
-        if (warp < kConsumerWarps) {
-            for (int c = 0; c < nch_full; ++c) {
-                uint32_t ahi = 0, alo = 0;  // the lane's masses in parts (at most 32 elements: no overflow)
-                if (c < nch && !failed) {
-                    const int nvec = min(CE, len - c * CE) / EPV;
-                    const uint4* vb = reinterpret_cast<const uint4*>(dyn_smem + c * kRowChunkBytes);
-#pragma unroll
-                    for (int j = 0; j < kVecPerLane; ++j) {
-                        const int v = warp * kVecPerWarp + j * 32 + lane;
-                        if (v >= nvec) continue;
-                        float x[EPV];
-                        unpack16<DT>(vb[v], x);
-#pragma unroll
-                        for (int e = 0; e < EPV; e += 2) pair_mass_parts(x[e], x[e + 1], neg_m2, inv_t2, ahi, alo);
-                    }
-                }
-                unsigned long long s = warp_sum_u64(mass_of_parts(ahi, alo));
-                if (lane == 0) w.chunk_mass[rt * nslot + (rank * nch_full + c) * kConsumerWarps + warp] = s;
-                wtot += s;
-            }
-            if (lane == 0) sm.wmass[warp] = wtot;
-        }
-        __syncthreads();
-        if (tid == 0) {
-            unsigned long long tot = 0;
-            for (int i = 0; i < kConsumerWarps; ++i) tot += sm.wmass[i];
-            cluster.map_shared_rank(&sm, 0)->rmass[rank] = tot;
-        }
-        cluster.sync();
-        if (rank != 0) return;
-    }
     if (tid == 0) {
-        uint64_t mass = 0;
-        if (MODE == 1)
-            for (int r = 0; r < cpr; ++r) mass += sm.rmass[r];
         w.row_max[rt] = M;
         w.row_arg[rt] = static_cast<int32_t>(key_id(gkey));
-        w.row_mass[rt] = mass;
+        w.row_mass[rt] = 0;  // lossless: written by the walk for the rows it visits
         if (!isfinite(M)) raise_status(w.status, kDevNonFinite);
-        const int prev = ticket_add(&w.verify_ticket[b]);
-        sm.last = (prev == n - 1);
+        if (MODE == 0) {
+            const int prev = ticket_add(&w.verify_ticket[b]);
+            sm.last = (prev == n - 1);
+        }
     }
+    // lossless: the walk is its own kernel (verify_lossless_walk_kernel)
+    if (MODE == 1) return;
     __syncthreads();
     if (!sm.last) return;
 
-    // ---- acceptance walk for sequence b (one CTA) ----
+    // ---- greedy acceptance walk for sequence b (one CTA) ----
     WalkSmem& ws = *reinterpret_cast<WalkSmem*>(dyn_smem);
     const int T = d.T;
-    if (tid == 0) {
-        ws.bad = 0;
-        ws.piece_at = -1;
-        ws.n_removed = 0;
-    }
-    // the other rows' statistics (lossless: this CTA's tokens, parents, token
-    // logits and uniforms are already in sm)
+    if (tid == 0) ws.bad = 0;
     for (int c = tid; c < n; c += kRowThreads) {
-        if (MODE == 0) {
-            sm.tok[c] = tokens[static_cast<size_t>(b) * T + c];
-            sm.par[c] = parent[static_cast<size_t>(b) * T + c];
-        }
+        sm.tok[c] = tokens[static_cast<size_t>(b) * T + c];
+        sm.par[c] = parent[static_cast<size_t>(b) * T + c];
         ws.arg[c] = __ldcg(&w.row_arg[static_cast<size_t>(b) * T + c]);
-        ws.rmax[c] = __ldcg(&w.row_max[static_cast<size_t>(b) * T + c]);
-        ws.rowmass[c] = __ldcg(&w.row_mass[static_cast<size_t>(b) * T + c]);
     }
     __syncthreads();
     for (int c = 1 + tid; c < n; c += kRowThreads) {
         const int tk = sm.tok[c], p = sm.par[c];
-        ws.pmass[c] = 0;
-        if (tk < 0 || tk >= d.V || p < 0 || p >= c) {
-            ws.bad = 1;
-            continue;
-        }
-        if (MODE == 1) ws.pmass[c] = fixed_mass(sm.xtok[c], ws.rmax[p], inv_t);
+        if (tk < 0 || tk >= d.V || p < 0 || p >= c) ws.bad = 1;
     }
     __syncthreads();
     const bool bad = ws.bad != 0;
@@ -1065,7 +953,6 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
         // One warp walks the tree; at each node its children (contiguous in
         // slot order) are tested together, lane j on child j.
         int cur = 0, a = 0;
-        unsigned long long S = MODE == 1 ? ws.rowmass[0] : 0ull;
         if (lane == 0) ws.path[0] = 0;
         while (a < d.D && !bad) {
             int nchild = 0;
@@ -1084,146 +971,20 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
             if (nchild == 0) break;
             const int c = lane < nchild ? ws.child[lane] : -1;
             int next = -1;
-            if (MODE == 0) {
-                const unsigned bal = __ballot_sync(0xffffffffu, c >= 0 && sm.tok[c] == ws.arg[cur]);
-                if (bal) next = ws.child[__ffs(bal) - 1];
-            } else {
-                const unsigned long long P = c >= 0 ? ws.pmass[c] : 0ull;
-                unsigned long long incl = P;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const unsigned long long y = shfl_u64(incl, max(lane - o, 0));
-                    if (lane >= o) incl += y;
-                }
-                const unsigned long long Sj = S - (incl - P);  // after the earlier children's removal
-                const bool acc = c >= 0 && static_cast<unsigned __int128>(sm.uni[c] >> 8) * Sj <
-                                               (static_cast<unsigned __int128>(P) << 24);
-                const unsigned bal = __ballot_sync(0xffffffffu, acc);
-                if (bal) {
-                    next = ws.child[__ffs(bal) - 1];
-                } else {
-                    S -= shfl_u64(incl, 31);  // every child rejected: their tokens leave the residual
-                    if (c >= 0) {
-                        ws.removed_tok[lane] = sm.tok[c];
-                        ws.removed_mass[lane] = P;
-                    }
-                    if (lane == 0) ws.n_removed = nchild;
-                }
-            }
+            const unsigned bal = __ballot_sync(0xffffffffu, c >= 0 && sm.tok[c] == ws.arg[cur]);
+            if (bal) next = ws.child[__ffs(bal) - 1];
             if (next < 0) break;
             ++a;
             if (lane == 0) ws.path[a] = next;
             cur = next;
-            if (MODE == 1) S = ws.rowmass[cur];
         }
         __syncwarp();
         if (lane == 0) {
             ws.a = a;
-            ws.cur = cur;
-            ws.bonus = MODE == 0 ? ws.arg[cur] : -1;
-            if (MODE == 1) {  // the draw t = floor(U64 * S / 2^64) on the residual of row cur
-                const uint64_t U64 = (static_cast<uint64_t>(sm.uni[T + 1]) << 32) | sm.uni[T];
-                ws.t_in = static_cast<unsigned long long>((static_cast<unsigned __int128>(U64) * S) >> 64);
-            }
+            ws.bonus = ws.arg[cur];
         }
     }
     __syncthreads();
-
-    if (MODE == 1 && !bad) {
-        const int cur = ws.cur;
-        const int nrem = ws.n_removed;
-        const int nch_full = nslot / (cpr * kConsumerWarps);
-        // the residual mass of every piece of row cur (one piece per thread, one round trip)
-        for (int q = tid; q < nslot; q += kRowThreads) {
-            unsigned long long m = __ldcg(w.chunk_mass + (static_cast<size_t>(b) * T + cur) * nslot + q);
-            int lo, hi;
-            piece_range(q, nch_full, seg, d.V, CE, EPV, lo, hi);
-            for (int r = 0; r < nrem; ++r)
-                if (ws.removed_tok[r] >= lo && ws.removed_tok[r] < hi) m -= ws.removed_mass[r];
-            ws.piece[q] = m;
-        }
-        __syncthreads();
-        if (warp == 0) {
-            // the piece that holds the draw: lane l sums pieces [l * per, (l + 1) * per)
-            const int per = (nslot + 31) / 32;
-            const unsigned long long tdraw = ws.t_in;
-            unsigned long long loc = 0;
-            for (int i = 0; i < per; ++i) {
-                const int q = lane * per + i;
-                if (q < nslot) loc += ws.piece[q];
-            }
-            unsigned long long incl = loc;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const unsigned long long y = shfl_u64(incl, max(lane - o, 0));
-                if (lane >= o) incl += y;
-            }
-            unsigned long long run = incl - loc;
-            if (loc > 0 && run <= tdraw && tdraw < run + loc) {
-                for (int i = 0; i < per; ++i) {
-                    const int q = lane * per + i;
-                    if (q >= nslot) break;
-                    const unsigned long long m = ws.piece[q];
-                    if (run + m > tdraw) {
-                        ws.piece_at = q;
-                        ws.t_in = tdraw - run;
-                        break;
-                    }
-                    run += m;
-                }
-            }
-        }
-        __syncthreads();
-        // Smallest y of the chosen piece (not removed) whose running mass
-        // exceeds the draw: one 16-byte vector per thread, block scan.
-        const int q = ws.piece_at;
-        int lo = 0, hi = 0;
-        if (q >= 0) piece_range(q, nch_full, seg, d.V, CE, EPV, lo, hi);
-        const float m = ws.rmax[cur];
-        uint64_t em[EPV];
-        unsigned long long mv = 0;
-        const int y0 = lo + tid * EPV;
-        if (tid < kVecPerWarp && y0 < hi) {
-            const char* crow = static_cast<const char*>(target) + (static_cast<size_t>(b) * T + cur) * d.V * ES;
-            const uint4 u = __ldcg(reinterpret_cast<const uint4*>(crow + static_cast<size_t>(y0) * ES));
-            float x[EPV];
-            unpack16<DT>(u, x);
-            const uint64_t neg_m2 = f2_pack(-m, -m), inv_t2 = f2_pack(inv_t, inv_t);
-#pragma unroll
-            for (int e = 0; e < EPV; e += 2) pair_mass2(x[e], x[e + 1], neg_m2, inv_t2, em[e], em[e + 1]);
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) {
-                for (int r = 0; r < nrem; ++r)
-                    if (ws.removed_tok[r] == y0 + e) em[e] = 0;
-                mv += em[e];
-            }
-        }
-        unsigned long long incl = mv;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const unsigned long long y = shfl_u64(incl, max(lane - o, 0));
-            if (lane >= o) incl += y;
-        }
-        if (warp < 4 && lane == 31) ws.scan[warp] = incl;
-        __syncthreads();
-        if (tid < kVecPerWarp && q >= 0) {
-            unsigned long long ex = incl - mv;
-            for (int i = 0; i < warp; ++i) ex += ws.scan[i];
-            const unsigned long long tin = ws.t_in;
-            if (mv > 0 && ex <= tin && tin < ex + mv) {
-                unsigned long long run = ex;
-#pragma unroll
-                for (int e = 0; e < EPV; ++e) {
-                    run += em[e];
-                    if (run > tin) {
-                        ws.bonus = y0 + e;
-                        break;
-                    }
-                }
-            }
-        }
-        __syncthreads();
-    }
 
     if (tid == 0) {
         const int a = ws.a;
@@ -1518,24 +1279,20 @@ static int sm_count() {
     return n;
 }
 
-RowPlan plan_rows(int V, int esize, long rows, bool resident, int max_stages, int max_seg_chunks) {
-    int cpr = kMaxChunks;
-    if (!resident) {
-        // about two waves of CTAs (three to five resident per SM)
-        const long target = 2L * 3 * sm_count();
-        cpr = 1;
-        while (cpr < kMaxChunks &&
-               (rows * cpr < target || row_chunks(row_seg_elems(V, esize, cpr), esize) > max_seg_chunks))
-            cpr *= 2;
-    }
+RowPlan plan_rows(int V, int esize, long rows, int max_stages, int max_seg_chunks) {
+    // about two waves of CTAs (three to five resident per SM)
+    const long target = 2L * 3 * sm_count();
+    int cpr = 1;
+    while (cpr < kMaxChunks &&
+           (rows * cpr < target || row_chunks(row_seg_elems(V, esize, cpr), esize) > max_seg_chunks))
+        cpr *= 2;
     RowPlan p;
     p.cpr = cpr;
     p.seg = row_seg_elems(V, esize, cpr);
     p.nch = row_chunks(p.seg, esize);
-    p.stages = resident ? p.nch : std::min(p.nch, max_stages);
+    p.stages = std::min(p.nch, max_stages);
     p.smem = p.nch <= 1 ? static_cast<int>(align_up(static_cast<size_t>(p.seg) * esize, 128))
                         : p.stages * kRowChunkBytes;
-    p.slots = cpr * p.nch * kConsumerWarps;
     return p;
 }
 
@@ -1582,7 +1339,7 @@ cudaError_t launch_expand(const TreeDims& d, const TreeWs& ws, int step, const v
     const int esize = d.dtype == 1 ? 2 : 4;
     const long rows = static_cast<long>(d.B) * (step == 0 ? 1 : d.k);  // step 0 reads the root rows only
     const int max_seg = esize == 2 ? kMaxSegChunksBf16 : kMaxSegChunks;
-    RowPlan p = plan_rows(d.V, esize, rows, false, kExpandStages, kMaxSegChunks);
+    RowPlan p = plan_rows(d.V, esize, rows, kExpandStages, kMaxSegChunks);
     // Rows enough to fill every CTA slot once (three to five per SM, five
     // resident): one CTA per row in a single wave, no cluster merge, instead
     // of about two waves of half rows whose per-CTA tails leave HBM idle.
@@ -1596,7 +1353,6 @@ cudaError_t launch_expand(const TreeDims& d, const TreeWs& ws, int step, const v
             p.stages = std::min(nch1, kExpandStages);
             p.smem = nch1 <= 1 ? static_cast<int>(align_up(static_cast<size_t>(seg1) * esize, 128))
                                : p.stages * kRowChunkBytes;
-            p.slots = nch1 * kConsumerWarps;
         }
     }
     // With enough rows to fill the SMs at four CTAs per row, four larger
@@ -1611,7 +1367,6 @@ cudaError_t launch_expand(const TreeDims& d, const TreeWs& ws, int step, const v
             p.nch = nch4;
             p.stages = nch4;
             p.smem = nch4 * kRowChunkBytes;
-            p.slots = 4 * nch4 * kConsumerWarps;
         }
     }
     if (p.nch > max_seg) return cudaErrorInvalidValue;
@@ -1655,40 +1410,54 @@ cudaError_t launch_verify(const TreeDims& d, const TreeWs& ws, int mode, float i
                           const int32_t* tokens, const int32_t* parent, const int32_t* n_tree, VerifyRng rng,
                           int32_t* accept_len, int32_t* slots, int32_t* out_tokens, cudaStream_t stream) {
     const int esize = d.dtype == 1 ? 2 : 4;
-    const RowPlan p = plan_rows(d.V, esize, static_cast<long>(d.B) * d.T, mode == 1, kRowStages, 1 << 20);
-    if (mode == 1 && p.stages > kRowStages) return cudaErrorInvalidValue;
+    const long rows = static_cast<long>(d.B) * d.T;
+    RowPlan p = plan_rows(d.V, esize, rows, kRowStages, 1 << 20);
+    // Rows enough to fill three to five CTA slots per SM: one CTA per row in
+    // a single wave (no cluster merge, no second wave of tails), as expansion;
+    // a two-stage ring keeps five CTAs resident per SM.
+    if (p.cpr > 1 && rows >= 3L * sm_count() && rows <= 5L * sm_count()) {
+        p.cpr = 1;
+        p.seg = row_seg_elems(d.V, esize, 1);
+        p.nch = row_chunks(p.seg, esize);
+        p.stages = std::min(p.nch, 2);
+        p.smem = p.nch <= 1 ? static_cast<int>(align_up(static_cast<size_t>(p.seg) * esize, 128))
+                            : p.stages * kRowChunkBytes;
+    }
     dim3 grid(p.cpr, d.B * d.T, 1);
-    // the acceptance walk keeps its state in the (then idle) stage memory
+    // the greedy walk keeps its state in the (then idle) stage memory
     const int smem = static_cast<int>(std::max<size_t>(p.smem, align_up(sizeof(WalkSmem), 128)));
     TreeDims dd = d;
     TreeWs ww = ws;
-    int seg = p.seg, ns = p.stages, nslot = mode == 1 ? p.slots : 0;
+    int seg = p.seg, ns = p.stages;
     void* args[] = {&dd,
                     &ww,
-                    &inv_temp,
                     &seg,
                     &ns,
-                    &nslot,
                     const_cast<void**>(&target),
                     const_cast<int32_t**>(&tokens),
                     const_cast<int32_t**>(&parent),
                     const_cast<int32_t**>(&n_tree),
-                    &rng,
                     &accept_len,
                     &slots,
                     &out_tokens};
+    cudaError_t e;
     if (d.dtype == 1)
-        return mode == 1 ? launch_rows(verify_kernel<1, 1>, grid, p.cpr, smem, stream, args)
-                         : launch_rows(verify_kernel<1, 0>, grid, p.cpr, smem, stream, args);
-    return mode == 1 ? launch_rows(verify_kernel<0, 1>, grid, p.cpr, smem, stream, args)
-                     : launch_rows(verify_kernel<0, 0>, grid, p.cpr, smem, stream, args);
+        e = mode == 1 ? launch_rows(verify_kernel<1, 1>, grid, p.cpr, smem, stream, args)
+                      : launch_rows(verify_kernel<1, 0>, grid, p.cpr, smem, stream, args);
+    else
+        e = mode == 1 ? launch_rows(verify_kernel<0, 1>, grid, p.cpr, smem, stream, args)
+                      : launch_rows(verify_kernel<0, 0>, grid, p.cpr, smem, stream, args);
+    if (e != cudaSuccess || mode != 1) return e;
+    // lossless: one cluster per sequence walks the tree, summing only the rows it visits
+    return launch_verify_walk(d, ws, inv_temp, rng, target, tokens, parent, n_tree, accept_len, slots, out_tokens,
+                              stream);
 }
 
 cudaError_t launch_shard_partials(int Vs, int k, int rows, int dtype, const void* logits, int id_base, float2* part_ms,
                                   uint64_t* part_keys, int* status, cudaStream_t stream) {
     const int esize = dtype == 1 ? 2 : 4;
     const int max_seg = esize == 2 ? kMaxSegChunksBf16 : kMaxSegChunks;
-    const RowPlan p = plan_rows(Vs, esize, rows, false, kExpandStages, kMaxSegChunks);
+    const RowPlan p = plan_rows(Vs, esize, rows, kExpandStages, kMaxSegChunks);
     if (p.nch > max_seg) return cudaErrorInvalidValue;
     const int scratch = p.nch * kConsumers * 4 + 512 * 8;
     const int smem = p.nch <= p.stages ? p.stages * kRowChunkBytes + scratch : std::max(p.smem, scratch);

@@ -27,9 +27,6 @@ namespace {
 
 constexpr int kMaxRows = 4096;  // batch * T
 constexpr int kMaxSeqs = 1024;  // batch
-// integer-mass pieces of lossless verification: rows * verify_mass_slots(V)
-// (128 per row at a 128256-entry bf16 vocabulary)
-constexpr size_t kMaxPieces = static_cast<size_t>(kMaxRows) * 128;
 
 // Byte offsets inside the fixed scratch array.
 constexpr size_t kOffStatus = 0;
@@ -37,8 +34,7 @@ constexpr size_t kOffTicket = 256;
 constexpr size_t kOffRowMax = kOffTicket + kMaxSeqs * sizeof(int);
 constexpr size_t kOffRowArg = kOffRowMax + kMaxRows * sizeof(float);
 constexpr size_t kOffRowMass = kOffRowArg + kMaxRows * sizeof(int32_t);
-constexpr size_t kOffChunkMass = kOffRowMass + kMaxRows * sizeof(uint64_t);
-constexpr size_t kScratchBytes = kOffChunkMass + kMaxPieces * sizeof(uint64_t);
+constexpr size_t kScratchBytes = kOffRowMass + kMaxRows * sizeof(uint64_t);
 
 static __device__ __align__(256) unsigned char g_verify_scratch[kScratchBytes];
 
@@ -80,11 +76,6 @@ extern "C" int eagle_verify_static(const eagle_tree_cfg* cfg, int mode, float te
     if (mode != EAGLE_VERIFY_GREEDY && mode != EAGLE_VERIFY_LOSSLESS) return EAGLE_ERR_INVALID_ARG;
     const long rows = static_cast<long>(cfg->batch) * (cfg->node_budget + 1);
     if (cfg->batch > kMaxSeqs || rows > kMaxRows) return EAGLE_ERR_UNSUPPORTED;  // beyond the fixed scratch
-    // integer-mass pieces are written by lossless verification only
-    const int esize = cfg->logit_dtype == EAGLE_BF16 ? 2 : 4;
-    if (mode == EAGLE_VERIFY_LOSSLESS &&
-        static_cast<size_t>(rows) * verify_mass_slots(cfg->vocab, esize) > kMaxPieces)
-        return EAGLE_ERR_UNSUPPORTED;
     if (!target_logits || !tokens || !parent || !n_tree || !accept_len || !accepted_slots || !out_tokens)
         return EAGLE_ERR_INVALID_ARG;
     float inv_t = 1.0f;
@@ -115,7 +106,6 @@ extern "C" int eagle_verify_static(const eagle_tree_cfg* cfg, int mode, float te
     w.row_max = reinterpret_cast<float*>(base + kOffRowMax);
     w.row_arg = reinterpret_cast<int32_t*>(base + kOffRowArg);
     w.row_mass = reinterpret_cast<uint64_t*>(base + kOffRowMass);
-    w.chunk_mass = reinterpret_cast<uint64_t*>(base + kOffChunkMass);
     // The arrival counters and the status word must start at zero; the rest
     // is fully written by the kernels before it is read.
     cudaStream_t s = static_cast<cudaStream_t>(stream);

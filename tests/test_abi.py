@@ -124,8 +124,7 @@ def test_static_verify_rejects_what_its_fixed_scratch_cannot_hold(E):
 
     assert call(E.TreeCfg(80, 1024, 4, 3, 60, 0.0, E.EAGLE_F32), 0) == -2  # 80 * 61 rows > 4096
     assert call(E.TreeCfg(1025, 1024, 4, 3, 1, 0.0, E.EAGLE_F32), 0) == -2  # batch > 1024
-    # fp32 at a 128256-entry vocabulary: 256 mass pieces per row, so at most 2048 lossless rows
-    assert call(E.TreeCfg(34, 128256, 4, 3, 60, 0.0, E.EAGLE_F32), 1) == -2  # 2074 rows
+    assert call(E.TreeCfg(80, 128256, 4, 3, 60, 0.0, E.EAGLE_BF16), 1) == -2  # lossless: the same row limit
     assert call(E.TreeCfg(2, 1024, 4, 3, 10, 0.0, E.EAGLE_F32), 7) == -1  # unknown mode
     assert call(E.TreeCfg(2, 1024, 0, 3, 10, 0.0, E.EAGLE_F32), 0) == -1  # invalid tree
     assert E.raw_call("eagle_verify_static", ctypes.byref(E.TreeCfg(2, 1024, 4, 3, 10, 0.0, E.EAGLE_F32)), 1,

@@ -6,10 +6,9 @@ the allocator. eagle_verify_static keeps its scratch in a fixed array inside
 the library instead. These tests call it through the C ABI on real device
 buffers only and check its results against eagle_verify (the workspace
 version) on the same inputs, for two calls in a row, in greedy and lossless
-mode, and against the oracle on the small cases; one case sits near the
-array's row and mass-piece limits, one uses greedy mode beyond the lossless
-piece limit. (Its size checks, which reject a call before any CUDA work, are
-tested without a GPU in test_abi.py.) The file is collected last so that a run
+mode, and against the oracle on the small cases; the large cases sit near the
+array's row limit, in bf16 and fp32 and both modes. (Its size checks, which
+reject a call before any CUDA work, are tested without a GPU in test_abi.py.) The file is collected last so that a run
 stopping at the first failure has already run the rest.
 """
 import numpy as np
@@ -65,8 +64,9 @@ def test_static_scratch_verify_matches_workspace_verify(name, batch):
 
 
 @pytest.mark.parametrize("mode,B,N,esize", [
-    (1, 64, 60, 2),   # lossless: 3904 rows x 128 pieces, near the 4096-row and 524288-piece limits
-    (0, 34, 60, 4),   # greedy fp32: 2074 rows, beyond what the pieces allow a lossless call
+    (1, 64, 60, 2),   # lossless bf16: 3904 rows, near the 4096-row limit
+    (1, 34, 60, 4),   # lossless fp32: 2074 rows of 128256 entries
+    (0, 34, 60, 4),   # greedy fp32
 ])
 def test_static_scratch_verify_near_its_limits(mode, B, N, esize):
     import torch
