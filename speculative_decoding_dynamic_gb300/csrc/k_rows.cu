@@ -1414,12 +1414,12 @@ cudaError_t launch_verify(const TreeDims& d, const TreeWs& ws, int mode, float i
     RowPlan p = plan_rows(d.V, esize, rows, kRowStages, 1 << 20);
     // Rows enough to fill three to five CTA slots per SM: one CTA per row in
     // a single wave (no cluster merge, no second wave of tails), as expansion;
-    // a two-stage ring keeps five CTAs resident per SM.
+    // a three-stage ring keeps four CTAs resident per SM.
     if (p.cpr > 1 && rows >= 3L * sm_count() && rows <= 5L * sm_count()) {
         p.cpr = 1;
         p.seg = row_seg_elems(d.V, esize, 1);
         p.nch = row_chunks(p.seg, esize);
-        p.stages = std::min(p.nch, 2);
+        p.stages = std::min(p.nch, 3);
         p.smem = p.nch <= 1 ? static_cast<int>(align_up(static_cast<size_t>(p.seg) * esize, 128))
                             : p.stages * kRowChunkBytes;
     }
