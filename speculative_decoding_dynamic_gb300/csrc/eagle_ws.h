@@ -60,6 +60,7 @@ struct TreeWs {
     float* row_max;         // [B, T] verify row maximum
     int32_t* row_arg;       // [B, T] verify row argmax
     uint64_t* row_mass;     // [B, T] verify integer mass
+    uint64_t* pmass;        // [B, T] lossless: integer mass of slot c's token in its parent's row
     uint64_t* resid;        // [B, V] target residual of the draft-probability rule
 };
 
@@ -94,6 +95,7 @@ inline size_t ws_layout(const TreeDims& d, void* base, TreeWs* ws) {
     w.row_max = static_cast<float*>(take(B * T * 4));
     w.row_arg = static_cast<int32_t*>(take(B * T * 4));
     w.row_mass = static_cast<uint64_t*>(take(B * T * 8));
+    w.pmass = static_cast<uint64_t*>(take(B * T * 8));
     w.resid = static_cast<uint64_t*>(take(B * static_cast<size_t>(d.V) * 8));
     if (ws) *ws = w;
     return align_up(off, 256);

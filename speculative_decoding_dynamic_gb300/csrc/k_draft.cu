@@ -425,7 +425,7 @@ struct LosslessSmem {
     int child[kMaxTopK];
     unsigned long long s_left;
     int next, nrem;
-    int bad, bonus;
+    int bad, bonus, holder;
 };
 
 // u24 * S < P * 2^24 for u24 < 2^24, S < 2^64, P < 2^41, in 64-bit halves.
@@ -492,6 +492,8 @@ __global__ void __launch_bounds__(kWalkThreads) verify_lossless_walk_kernel(Tree
         sm.tok[c] = tokens[tb + c];
         sm.par[c] = parent[tb + c];
         sm.rmax[c] = __ldcg(&w.row_max[tb + c]);
+        // the mass of slot c's token in its parent's row, from the row kernel (which had the parent row streaming)
+        sm.pmass[c] = c > 0 ? __ldcg(&w.pmass[tb + c]) : 0ull;
     }
     // uniform word c of sequence b: Philox4x32-10 at counter (c, b, cycle), word 0
     for (int c = tid; c < T + 2; c += kWalkThreads) {
@@ -503,13 +505,7 @@ __global__ void __launch_bounds__(kWalkThreads) verify_lossless_walk_kernel(Tree
     __syncthreads();
     for (int c = 1 + tid; c < nn; c += kWalkThreads) {
         const int tk = sm.tok[c], p = sm.par[c];
-        sm.pmass[c] = 0;
-        if (tk < 0 || tk >= V || p < 0 || p >= c) {
-            sm.bad = 1;
-            continue;
-        }
-        const char* prow = static_cast<const char*>(target) + (tb + p) * V * ES;
-        sm.pmass[c] = fixed_mass(load_logit(prow, DT, tk), sm.rmax[p], inv_t);
+        if (tk < 0 || tk >= V || p < 0 || p >= c) sm.bad = 1;
     }
     __syncthreads();
     const bool bad = sm.bad != 0;
@@ -562,7 +558,7 @@ __global__ void __launch_bounds__(kWalkThreads) verify_lossless_walk_kernel(Tree
         // 0, lane j on child j: accepted iff u24 S_j < P 2^24, S_j the mass
         // left after the earlier children's removal
         if (warp == 0) {
-            int nchild = 0, next = -1;
+            int nchild = 0;
             if (a < d.D) {
                 for (int c0w = cur + 1; c0w < n && nchild < kMaxTopK; c0w += 32) {
                     const int c = c0w + lane;
@@ -629,10 +625,17 @@ __global__ void __launch_bounds__(kWalkThreads) verify_lossless_walk_kernel(Tree
         };
         const uint64_t U64 = (static_cast<uint64_t>(sm.uni[T + 1]) << 32) | sm.uni[T];
         const unsigned long long tdraw = __umul64hi(U64, S);
-        unsigned long long before = 0;
-        for (int r = 0; r < rank; ++r) before += sm.part[r] - removed_in(min(V, r * seg), min(V, r * seg + seg));
-        const unsigned long long mine = sm.part[rank] - removed_in(lo, hi);
-        if (mine > 0 && tdraw >= before && tdraw < before + mine) {
+        // every CTA knows which slice holds the draw (the same shares everywhere)
+        int holder = -1;
+        unsigned long long before = 0, upto = 0;  // this CTA's prefix; the running prefix over all CTAs
+        for (int r = 0; r < kWalkCtas; ++r) {
+            const unsigned long long share = sm.part[r] - removed_in(min(V, r * seg), min(V, r * seg + seg));
+            if (holder < 0 && share > 0 && tdraw >= upto && tdraw < upto + share) holder = r;
+            if (r < rank) before += share;
+            upto += share;
+        }
+        if (tid == 0) sm.holder = holder;
+        if (holder == rank) {
             // the piece: (round, warp) ranges in element order
             int pq = -1;
             unsigned long long run = before;
@@ -695,21 +698,20 @@ __global__ void __launch_bounds__(kWalkThreads) verify_lossless_walk_kernel(Tree
             }
         }
     }
-    cluster.sync();  // the bonus is in the shared memory of the CTA that found it
-    if (tid == 0) {
-        int bonus = sm.bonus;
-        for (int r = 0; r < kWalkCtas && bonus < 0; ++r) bonus = cluster.map_shared_rank(&sm, r)->bonus;
-        if (rank == 0) {
-            const int Dp1 = d.D + 1;
-            accept_len[b] = a;
-            for (int j = 0; j < Dp1; ++j) {
-                slots_out[b * Dp1 + j] = j <= a ? sm.path[j] : -1;
-                tokens_out[b * Dp1 + j] = j < a ? sm.tok[sm.path[j + 1]] : (j == a ? bonus : -1);
-            }
-            if (bad || bonus < 0) raise_status(w.status, kDevBadIndex);
+    // The outputs: written by the CTA that holds the draw (rank 0 when none
+    // does). After the last cluster barrier of the walk no CTA touches
+    // another's shared memory, so the CTAs leave without a final barrier.
+    __syncthreads();
+    if (tid == 0 && (bad ? rank == 0 : (sm.holder == rank || (sm.holder < 0 && rank == 0)))) {
+        const int bonus = sm.bonus;
+        const int Dp1 = d.D + 1;
+        accept_len[b] = a;
+        for (int j = 0; j < Dp1; ++j) {
+            slots_out[b * Dp1 + j] = j <= a ? sm.path[j] : -1;
+            tokens_out[b * Dp1 + j] = j < a ? sm.tok[sm.path[j + 1]] : (j == a ? bonus : -1);
         }
+        if (bad || bonus < 0) raise_status(w.status, kDevBadIndex);
     }
-    cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
 
 }  // namespace

@@ -804,6 +804,10 @@ struct VerifySmem {
     RowRing ring;
     int tok[kMaxSlots];
     int par[kMaxSlots];
+    // lossless: this row's children (slot, token logit in this row), read while the row streams
+    int kid_c[kMaxTopK];
+    float kid_x[kMaxTopK];
+    int kid_n;
     uint64_t wkey[kConsumerWarps];
     uint64_t rkey[kMaxChunks];  // every rank's segment maximum (pushed to the leader)
     int last;
@@ -823,7 +827,7 @@ struct WalkSmem {
 // walks its tree. MODE 1 (lossless): the statistics only, the walk is
 // verify_lossless_walk_kernel.
 template <int DT, int MODE>
-__global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs w, int seg, int ns,
+__global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs w, float inv_t, int seg, int ns,
                                                               const void* __restrict__ target,
                                                               const int32_t* __restrict__ tokens,
                                                               const int32_t* __restrict__ parent,
@@ -860,13 +864,30 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
     const int len = max(0, min(seg, d.V - c0));
     const int nch = (len * ES + kRowChunkBytes - 1) / kRowChunkBytes;
     const char* row_base = static_cast<const char*>(target) + static_cast<size_t>(b * d.T + t) * d.V * ES;
-    if (tid == 0) ring_init(sm.ring, ns);
+    if (tid == 0) {
+        ring_init(sm.ring, ns);
+        sm.kid_n = 0;
+    }
     __syncthreads();
 
     bool failed = false;
     if (warp == kProducerWarp) {
         if (lane == 0 && nch > 0) {
             ring_produce(sm.ring, dyn_smem, row_base + static_cast<size_t>(c0) * ES, len * ES, nch, ns, w.status);
+        } else if (MODE == 1 && rank == 0 && lane > 0) {
+            // lossless: the token logits of this row's children, read while the
+            // row streams (their masses need the row maximum, known at the end)
+            for (int c = t + lane; c < n; c += 31) {
+                if (parent[static_cast<size_t>(b) * d.T + c] != t) continue;
+                const int tk = tokens[static_cast<size_t>(b) * d.T + c];
+                if (tk < 0 || tk >= d.V) continue;  // the walk flags it
+                const int at = atomicAdd(&sm.kid_n, 1);
+                if (at >= kMaxTopK) continue;
+                sm.kid_c[at] = c;
+                sm.kid_x[at] = DT == 1 ? __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(
+                                                             row_base)[tk]) << 16)
+                                       : reinterpret_cast<const float*>(row_base)[tk];
+            }
         }
         __syncwarp();
     } else {
@@ -916,6 +937,8 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
     for (int r = 0; r < cpr; ++r) gkey = sm.rkey[r] > gkey ? sm.rkey[r] : gkey;
     const float M = key_val(gkey);
     const size_t rt = static_cast<size_t>(b) * d.T + t;
+    if (MODE == 1 && tid < min(sm.kid_n, kMaxTopK))  // the children's masses in this row
+        w.pmass[static_cast<size_t>(b) * d.T + sm.kid_c[tid]] = fixed_mass(sm.kid_x[tid], M, inv_t);
     if (tid == 0) {
         w.row_max[rt] = M;
         w.row_arg[rt] = static_cast<int32_t>(key_id(gkey));
@@ -1431,6 +1454,7 @@ cudaError_t launch_verify(const TreeDims& d, const TreeWs& ws, int mode, float i
     int seg = p.seg, ns = p.stages;
     void* args[] = {&dd,
                     &ww,
+                    &inv_temp,
                     &seg,
                     &ns,
                     const_cast<void**>(&target),

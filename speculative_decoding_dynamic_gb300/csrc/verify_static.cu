@@ -34,7 +34,8 @@ constexpr size_t kOffTicket = 256;
 constexpr size_t kOffRowMax = kOffTicket + kMaxSeqs * sizeof(int);
 constexpr size_t kOffRowArg = kOffRowMax + kMaxRows * sizeof(float);
 constexpr size_t kOffRowMass = kOffRowArg + kMaxRows * sizeof(int32_t);
-constexpr size_t kScratchBytes = kOffRowMass + kMaxRows * sizeof(uint64_t);
+constexpr size_t kOffPMass = kOffRowMass + kMaxRows * sizeof(uint64_t);
+constexpr size_t kScratchBytes = kOffPMass + kMaxRows * sizeof(uint64_t);
 
 static __device__ __align__(256) unsigned char g_verify_scratch[kScratchBytes];
 
@@ -106,6 +107,7 @@ extern "C" int eagle_verify_static(const eagle_tree_cfg* cfg, int mode, float te
     w.row_max = reinterpret_cast<float*>(base + kOffRowMax);
     w.row_arg = reinterpret_cast<int32_t*>(base + kOffRowArg);
     w.row_mass = reinterpret_cast<uint64_t*>(base + kOffRowMass);
+    w.pmass = reinterpret_cast<uint64_t*>(base + kOffPMass);
     // The arrival counters and the status word must start at zero; the rest
     // is fully written by the kernels before it is read.
     cudaStream_t s = static_cast<cudaStream_t>(stream);
