@@ -77,9 +77,15 @@ def parse(argv=None):
     ap.add_argument("--lmhead", action="store_true",
                     help="each draft step's rows come from the LM head (bf16 tensor-core GEMM of synthetic hidden "
                          "states against a resident random [V, H] weight)")
+    ap.add_argument("--fused-head", action="store_true",
+                    help="with the LM head: stage 1 in its epilogue (eagle_lmhead_topk, then eagle_expand_topk); "
+                         "the logits are never written")
     ap.add_argument("--policy", default="dynamic", choices=list(POLICIES),
                     help="tree policy: EAGLE-2, confidence-ranked frontier, no rerank or static shape (ablations)")
-    return ap.parse_args(argv)
+    a = ap.parse_args(argv)
+    if a.fused_head:
+        a.lmhead = True
+    return a
 
 
 # ------------------------------------------------------------- helpers ---
@@ -338,7 +344,7 @@ def config_of(w, args, variant: dict, R: int, per_set: int, attn_bytes: int) -> 
             "sharpness": list(w.sharpness) if isinstance(w.sharpness, tuple) else w.sharpness,
             "verify": w.verify, "compact_layers": w.layers, "planted": bool(variant.get("planted", False)),
             "aligned": bool(variant.get("aligned", False)), "policy": args.policy, "lmhead": args.lmhead,
-            "hidden_size": w.hidden_size if args.lmhead else None,
+            "fused_head": args.fused_head, "hidden_size": w.hidden_size if args.lmhead else None,
             "l2": f"{R} rotating input set(s), {round(R * (per_set + attn_bytes) / 2**20)} MiB > 129 MB L2",
             "graph": "one CUDA graph per input set, replayed"}
 
@@ -578,9 +584,9 @@ def run_workload(args, w, variant: dict, seed: int, ws_: int, rank: int, local: 
                     POLICIES[args.policy])
     kv = E.KvCfg(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.layers, geo["max_len"], w.dtype,
                  geo["seq_stride"], geo["layer_stride"], geo["kv_stride"], geo["pos_stride"])
-    dc = C.DeviceCycle(cfg, kv)
+    dc = C.DeviceCycle(cfg, kv, fused_head=args.fused_head)
     mode = E.GREEDY if w.verify == "greedy" else E.LOSSLESS
-    if args.lmhead:  # the draft rows are an intermediate written by the LM head every step
+    if args.lmhead and not args.fused_head:  # the draft rows are an intermediate written by the LM head every step
         lm_out = torch.empty(w.depth, w.batch, w.top_k, w.vocab, dtype=C.torch_dtype(w.dtype), device="cuda")
 
     def cycle(r, stream=None):
@@ -710,12 +716,19 @@ def run_workload(args, w, variant: dict, seed: int, ws_: int, rank: int, local: 
     cycle(0)
     torch.cuda.synchronize()
     kt = {}
-    if args.lmhead:
-        kt["lmhead"] = time_call(lambda r: E.eagle_lmhead(cfg, dc.ws, w.hidden_size, dev_sets[r]["hidden"][1],
-                                                          weight_d, lm_out[1]), reps)
+    if args.fused_head:
+        kt["lmhead"] = time_call(lambda r: dc.head_topk(weight_d, dev_sets[r]["hidden"][1]), reps)
         cycle(0)
-    kt["expand_step"] = time_call(lambda r: E.eagle_expand(cfg, dc.ws, min(1, w.depth - 1), dev_sets[r]["draft"][
-        min(1, w.depth - 1)], None, dc.row_lse, dc.ftok, dc.fcount), reps)
+        kt["expand_step"] = time_call(lambda r: E.eagle_expand_topk(cfg, dc.ws, min(1, w.depth - 1), dc.lm_ids,
+                                                                    dc.lm_vals, dc.lm_lse, dc.row_lse, dc.ftok,
+                                                                    dc.fcount), reps)
+    else:
+        if args.lmhead:
+            kt["lmhead"] = time_call(lambda r: E.eagle_lmhead(cfg, dc.ws, w.hidden_size, dev_sets[r]["hidden"][1],
+                                                              weight_d, lm_out[1]), reps)
+            cycle(0)
+        kt["expand_step"] = time_call(lambda r: E.eagle_expand(cfg, dc.ws, min(1, w.depth - 1), dev_sets[r]["draft"][
+            min(1, w.depth - 1)], None, dc.row_lse, dc.ftok, dc.fcount), reps)
     cycle(0)
     kt["rerank"] = time_call(lambda r: E.eagle_rerank(cfg, dc.ws), reps)
     kt["build_tree"] = time_call(lambda r: dc.build(prefix_d, root_d), reps)
@@ -736,8 +749,13 @@ def run_workload(args, w, variant: dict, seed: int, ws_: int, rank: int, local: 
     peak_src = "measured" if peak else "fallback"
     tensor_peak = peak["bf16_tflops"] if peak else 1900.0
     # LM head of one step: the weight, the hidden rows, the logits written
+    # (fused: the merged lse and top-k ids and logits instead of the logits)
     lm_flop = 2 * w.batch * w.top_k * w.vocab * w.hidden_size
-    lm_bytes = (w.vocab + w.batch * w.top_k) * w.hidden_size * 2 + w.batch * w.top_k * w.vocab * w.esize
+    rows_ = w.batch * w.top_k
+    lm_bytes = (w.vocab + rows_) * w.hidden_size * 2 + (
+        rows_ * (4 + 8 * w.top_k) if args.fused_head else rows_ * w.vocab * w.esize)
+    if args.fused_head:  # stage 2 from the merged top-k: ids, logits and lse of the step's rows
+        alg = dict(alg, expand_step=rows_ * (4 + 8 * w.top_k))
     per_kernel = {}
     for name, ms_k in kt.items():
         byt = {"expand_step": alg["expand_step"], "attention": alg["attention"], "verify": alg["verify"],

@@ -196,6 +196,31 @@ int eagle_lmhead(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int hidde
                  const void* weight, void* draft_logits, void* stream);
 
 /*
+ * LM head of a draft step with stage 1 in its epilogue [notes EAGLE 方法: the
+ * draft model reuses the target's LM head, and TopK drafting reads its
+ * distribution]: the logits of eagle_lmhead (fp32 tensor-core sums rounded to
+ * cfg->logit_dtype) are reduced on chip and never written.
+ *   hidden_dim, hidden, weight  as eagle_lmhead (B*k rows, bf16).
+ *   scratch       device memory of eagle_lmhead_topk_scratch_bytes(cfg)
+ *                 bytes, 256-byte aligned, owned by the caller: per-CTA
+ *                 partials (max, sum of exp, top-k keys of each row);
+ *                 contents undefined after the call.
+ *   row_lse       [B*k] fp32 out: M + log(sum of exp(x - M)) over the row's
+ *                 logits, fp32 (within 1e-5 of the exact value at V = 128K).
+ *   topk_ids      [B*k, k] int32 out, topk_logits [B*k, k] fp32 out: the k
+ *                 largest logits of each row as eagle_lmhead would store them
+ *                 (equal logits: lower id), best first; -1 / -inf padding.
+ * The outputs are those of eagle_shard_merge on the whole row and feed
+ * eagle_expand_topk (topk_ids as [B, k, k], row_lse as [B, k]). Needs
+ * B*k <= 4096 (EAGLE_ERR_UNSUPPORTED beyond). A non-finite lse raises
+ * device status 1; a timed-out wait status 2.
+ */
+size_t eagle_lmhead_topk_scratch_bytes(const eagle_tree_cfg* cfg);
+int eagle_lmhead_topk(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int hidden_dim, const void* hidden,
+                      const void* weight, void* scratch, size_t scratch_bytes, float* row_lse, int32_t* topk_ids,
+                      float* topk_logits, void* stream);
+
+/*
  * Stage 3 [summary 4.2; tutorial "Value of a Node"; notes EAGLE 2 方法,
  * ReRank]: keep the min(N, #candidates) candidates with the largest value;
  * equal values keep the shallower node, then the lower node id. The kept set

@@ -169,6 +169,32 @@ int eagle_lmhead(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int hidde
                                        static_cast<cudaStream_t>(stream)));
 }
 
+size_t eagle_lmhead_topk_scratch_bytes(const eagle_tree_cfg* cfg) {
+    TreeDims d;
+    if (resolve(cfg, &d) != EAGLE_OK) return 0;
+    return lmhead_topk_scratch_bytes(static_cast<long>(d.B) * d.k, d.k);
+}
+
+int eagle_lmhead_topk(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int hidden_dim, const void* hidden,
+                      const void* weight, void* scratch, size_t scratch_bytes, float* row_lse, int32_t* topk_ids,
+                      float* topk_logits, void* stream) {
+    TreeDims d;
+    TreeWs w;
+    int rc = resolve(cfg, &d);
+    if (rc == EAGLE_OK) rc = bind_ws(d, ws, ws_bytes, &w);
+    if (rc != EAGLE_OK) return rc;
+    if (!hidden || !weight || !row_lse || !topk_ids || !topk_logits || hidden_dim < 8) return EAGLE_ERR_INVALID_ARG;
+    if (hidden_dim % 8 != 0 || !aligned16(hidden) || !aligned16(weight)) return EAGLE_ERR_UNSUPPORTED;
+    const long M = static_cast<long>(d.B) * d.k;
+    if (M > 4096) return EAGLE_ERR_UNSUPPORTED;
+    if (scratch == nullptr || (reinterpret_cast<uintptr_t>(scratch) & 255u) != 0 ||
+        scratch_bytes < lmhead_topk_scratch_bytes(M, d.k))
+        return EAGLE_ERR_WORKSPACE;
+    return launch_result(launch_lmhead_topk(static_cast<int>(M), d.V, hidden_dim, d.k, hidden, weight, d.dtype,
+                                            scratch, row_lse, topk_ids, topk_logits, w.status,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
 int eagle_rerank(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, void* stream) {
     TreeDims d;
     TreeWs w;

@@ -188,6 +188,17 @@ cudaError_t launch_attention_pipe(const KvDims& kv, int T, const void* q, const 
 // and weight [V, H] (bf16), on the tensor cores.
 cudaError_t launch_lmhead(int M, int V, int H, const void* hidden, const void* weight, int out_dtype, void* out,
                           int* status, cudaStream_t stream);
+// The same product with stage 1 in the epilogue: the logits are rounded to
+// out_dtype as launch_lmhead would store them but never leave the SM; each
+// epilogue thread keeps a running (max, sum of exp, top-k keys) of one row
+// over its CTA's vocabulary tiles, writes it to `scratch` once, and a merge
+// gives the row's lse and top-k. scratch holds lmhead_topk_scratch_bytes(M, k)
+// bytes (256-byte aligned); M <= 4096.
+constexpr int kLmShards = 160;  // most CTAs of the fused launch (>= SMs of the GPU)
+size_t lmhead_topk_scratch_bytes(long M, int k);
+cudaError_t launch_lmhead_topk(int M, int V, int H, int k, const void* hidden, const void* weight, int out_dtype,
+                               void* scratch, float* row_lse, int32_t* topk_id, float* topk_val, int* status,
+                               cudaStream_t stream);
 cudaError_t launch_attention(const KvDims& kv, int T, const void* q, const void* cache, int layer,
                              const int32_t* prefix_len, const uint32_t* mask, const int32_t* n_tree, void* out,
                              void* ws, size_t ws_bytes, int* status, cudaStream_t stream);

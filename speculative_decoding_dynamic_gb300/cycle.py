@@ -19,8 +19,9 @@ def torch_dtype(code: int) -> torch.dtype:
 class DeviceCycle:
     """Buffers for one cycle of a (TreeCfg, KvCfg) problem on one device."""
 
-    def __init__(self, cfg: E.TreeCfg, kv: E.KvCfg, device="cuda"):
+    def __init__(self, cfg: E.TreeCfg, kv: E.KvCfg, device="cuda", fused_head: bool = False):
         self.cfg, self.kv = cfg, kv
+        self.fused_head = fused_head
         dev = torch.device(device)
         B, D, k, T, W = cfg.batch, cfg.depth, cfg.top_k, cfg.T, cfg.W
         i32 = dict(dtype=torch.int32, device=dev)
@@ -40,16 +41,29 @@ class DeviceCycle:
         self.slots = torch.empty(B, D + 1, **i32)
         self.out_tokens = torch.empty(B, D + 1, **i32)
         self.new_len = torch.empty(B, **i32)
+        if fused_head:  # stage 1 in the LM head's epilogue: per-CTA partials and the merged top-k
+            self.lm_scratch = E.alloc_workspace(E.eagle_lmhead_topk_scratch_bytes(cfg), dev)
+            self.lm_lse = torch.empty(B * k, dtype=torch.float32, device=dev)
+            self.lm_ids = torch.empty(B * k, k, **i32)
+            self.lm_vals = torch.empty(B * k, k, dtype=torch.float32, device=dev)
 
     # ---- stages -----------------------------------------------------------
     def draft(self, draft_logits: torch.Tensor, stream=None, steps=None, lse_in=None, head=None):
         """Stages 1-3. draft_logits: [D, B, k, V] (one contiguous block per step);
         lse_in: optional [D, B, k] row log-sum-exp supplied from upstream.
         head: optional (weight [V, H], hidden [D, B*k, H]), both bf16: each
-        step's rows are then first written into draft_logits[s] by the LM head."""
+        step's rows are then first written into draft_logits[s] by the LM head,
+        or, with fused_head, reduced to their lse and top-k in the LM head's
+        epilogue and expanded from those (draft_logits unused)."""
         cfg = self.cfg
         E.eagle_tree_init(cfg, self.ws, stream)
         for s in range(cfg.depth if steps is None else steps):
+            if head is not None and self.fused_head:
+                weight, hidden = head
+                self.head_topk(weight, hidden[s], stream)
+                E.eagle_expand_topk(cfg, self.ws, s, self.lm_ids, self.lm_vals, self.lm_lse, self.row_lse, self.ftok,
+                                    self.fcount, stream)
+                continue
             if head is not None:
                 weight, hidden = head
                 E.eagle_lmhead(cfg, self.ws, hidden.shape[-1], hidden[s], weight, draft_logits[s], stream)
@@ -57,6 +71,11 @@ class DeviceCycle:
                            self.ftok, self.fcount, stream)
         if steps is None:
             E.eagle_rerank(cfg, self.ws, stream)
+
+    def head_topk(self, weight, hidden_s, stream=None):
+        """LM head of one step with stage 1 in its epilogue (fused_head)."""
+        E.eagle_lmhead_topk(self.cfg, self.ws, hidden_s.shape[-1], hidden_s, weight, self.lm_scratch, self.lm_lse,
+                            self.lm_ids, self.lm_vals, stream)
 
     def build(self, prefix_len, root_token, stream=None):
         E.eagle_build_tree(self.cfg, self.ws, prefix_len, root_token, self.tokens, self.parent, self.depth, self.pos,

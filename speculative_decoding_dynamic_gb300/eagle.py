@@ -76,6 +76,9 @@ _lib.eagle_expand.argtypes = [_TP, _p, _sz, _i, _p, _p, _p, _p, _p, _p]
 _lib.eagle_expand_sampled.argtypes = [_TP, _p, _sz, _i, _p, _p, ctypes.c_uint64, ctypes.c_uint64, _p, _p, _p, _p]
 _lib.eagle_test_expand_starved.argtypes = [_TP, _p, _sz, _i, _p, _p, _p, _p, _p]
 _lib.eagle_lmhead.argtypes = [_TP, _p, _sz, _i, _p, _p, _p, _p]
+_lib.eagle_lmhead_topk_scratch_bytes.argtypes = [_TP]
+_lib.eagle_lmhead_topk_scratch_bytes.restype = _sz
+_lib.eagle_lmhead_topk.argtypes = [_TP, _p, _sz, _i, _p, _p, _p, _sz, _p, _p, _p, _p]
 _lib.eagle_rerank.argtypes = [_TP, _p, _sz, _p]
 _lib.eagle_tree_value.argtypes = [_TP, _p, _sz, _p, _p]
 _lib.eagle_build_tree.argtypes = [_TP, _p, _sz, _p, _p, _p, _p, _p, _p, _p, _p, _p]
@@ -171,6 +174,16 @@ def eagle_test_expand_starved(cfg, ws, step, draft_logits, row_lse, frontier_tok
 def eagle_lmhead(cfg, ws, hidden_dim, hidden, weight, draft_logits, stream=None):
     _check("eagle_lmhead", _lib.eagle_lmhead(ctypes.byref(cfg), *_ws(ws), hidden_dim, _ptr(hidden), _ptr(weight),
                                              _ptr(draft_logits), _stream(stream)))
+
+
+def eagle_lmhead_topk_scratch_bytes(cfg: TreeCfg) -> int:
+    return int(_lib.eagle_lmhead_topk_scratch_bytes(ctypes.byref(cfg)))
+
+
+def eagle_lmhead_topk(cfg, ws, hidden_dim, hidden, weight, scratch, row_lse, topk_ids, topk_logits, stream=None):
+    _check("eagle_lmhead_topk", _lib.eagle_lmhead_topk(ctypes.byref(cfg), *_ws(ws), hidden_dim, _ptr(hidden),
+                                                       _ptr(weight), *_ws(scratch), _ptr(row_lse), _ptr(topk_ids),
+                                                       _ptr(topk_logits), _stream(stream)))
 
 
 def eagle_rerank(cfg, ws, stream=None):

@@ -94,6 +94,22 @@ def test_calls_reject_bad_arguments_before_launch(E):
     assert r("eagle_lmhead", ctypes.byref(cfg), fake_ws, ws_bytes, 4100, ptr, ptr, ptr, None) == -2  # H % 8
     assert r("eagle_lmhead", ctypes.byref(cfg), fake_ws, ws_bytes, 4096, ptr, P((1 << 21) + 8), ptr, None) == -2
     assert r("eagle_lmhead", ctypes.byref(cfg), None, ws_bytes, 4096, ptr, ptr, ptr, None) == -4
+    sb = E.eagle_lmhead_topk_scratch_bytes(cfg)
+    assert sb > 0
+    fake_sc = P(1 << 22)
+    lm = lambda ws_, H_, hid, sc, sbytes: r("eagle_lmhead_topk", ctypes.byref(cfg), ws_, ws_bytes, H_, hid, ptr, sc,
+                                            sbytes, ptr, ptr, ptr, None)
+    assert lm(fake_ws, 4096, None, fake_sc, sb) == -1
+    assert lm(fake_ws, 0, ptr, fake_sc, sb) == -1
+    assert lm(fake_ws, 4100, ptr, fake_sc, sb) == -2  # H % 8
+    assert lm(fake_ws, 4096, P((1 << 21) + 8), fake_sc, sb) == -2
+    assert lm(fake_ws, 4096, ptr, None, sb) == -4
+    assert lm(fake_ws, 4096, ptr, P((1 << 22) + 128), sb) == -4
+    assert lm(fake_ws, 4096, ptr, fake_sc, sb - 1) == -4
+    assert lm(None, 4096, ptr, fake_sc, sb) == -4
+    big = E.TreeCfg(2048, 32000, 16, 4, 60, 0.0, E.EAGLE_BF16, 0)  # B*k = 32768 rows
+    assert r("eagle_lmhead_topk", ctypes.byref(big), fake_ws, E.eagle_workspace_bytes(big), 4096, ptr, ptr, fake_sc,
+             E.eagle_lmhead_topk_scratch_bytes(big), ptr, ptr, ptr, None) == -2
     kv = E.KvCfg(2, 8, 3, 64, 4, 100, E.EAGLE_BF16, 0, 0, 0, 192)  # 8 % 3 != 0
     assert r("eagle_tree_attention", ctypes.byref(kv), 9, ptr, ptr, 0, ptr, ptr, ptr, ptr, fake_ws, 4096, None) == -1
     kv = E.KvCfg(2, 8, 2, 64, 4, 100, E.EAGLE_BF16, 4 * 2 * 100 * 128, 2 * 100 * 128, 100 * 128, 128)
