@@ -1,6 +1,12 @@
 """Build libeagle.so in place: nvcc for sm_103a, one object per .cu, in parallel.
 
-    python -m speculative_decoding_dynamic_gb300.build [--force] [--verbose-ptxas]
+    python -m speculative_decoding_dynamic_gb300.build [--force] [--verbose-ptxas] [--debug]
+
+--debug builds the checked library libeagle_debug.so (-DEAGLE_DEBUG): every
+launching call waits for its work and returns the device status of its own
+kernels, and internal indices the release kernels trust are range-checked
+(out of range: status word, no access). The binding loads it when the
+environment sets EAGLE_DEBUG=1.
 """
 from __future__ import annotations
 
@@ -16,6 +22,8 @@ ROOT = os.path.dirname(PKG)
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libeagle.so")
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "libeagle_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
               "--expt-relaxed-constexpr"]
@@ -44,15 +52,17 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
+def build(force: bool = False, verbose_ptxas: bool = False, debug: bool = False) -> str:
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    bdir, lib = (BUILD_DEBUG, LIB_DEBUG) if debug else (BUILD, LIB)
+    flags = NVCC_FLAGS + (["-DEAGLE_DEBUG"] if debug else [])
+    os.makedirs(bdir, exist_ok=True)
     hdrs = _headers()
     jobs = []
     for src in _sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
         if force or _stale(obj, [src] + hdrs):
-            cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+            cmd = [nvcc, *ARCH, *flags, "-c", src, "-o", obj]
             if verbose_ptxas:
                 cmd += ["-Xptxas", "-v"]
             jobs.append((src, cmd))
@@ -65,16 +75,16 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
                     raise RuntimeError(f"nvcc failed for {futs[fut]}:\n{r.stderr}")
                 if verbose_ptxas and r.stderr:
                     sys.stderr.write(r.stderr)
-    objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in _sources()]
-    if force or _stale(LIB, objs):
-        tmp = LIB + ".tmp"
+    objs = [os.path.join(bdir, os.path.basename(s)[:-3] + ".o") for s in _sources()]
+    if force or _stale(lib, objs):
+        tmp = lib + ".tmp"
         r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"], capture_output=True,
                            text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose_ptxas="--verbose-ptxas" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose_ptxas="--verbose-ptxas" in sys.argv, debug="--debug" in sys.argv))

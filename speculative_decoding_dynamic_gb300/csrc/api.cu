@@ -6,6 +6,8 @@
 #include <cstdint>
 #include <cstring>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/eagle.h"
 #include "eagle_ws.h"
 
@@ -93,10 +95,45 @@ int resolve_kv(const eagle_kv_cfg* kv, KvDims* k) {
 // The CUDA error of the calling thread's last failed call (0 = none).
 thread_local int g_last_cuda_error = 0;
 
+// One C-ABI call: an NVTX range named after the call (for profilers; a null
+// check when no tool is attached), and the stream and workspace that a
+// checked build waits on.
+thread_local cudaStream_t g_call_stream = nullptr;
+thread_local const void* g_call_ws = nullptr;
+struct CallScope {
+    CallScope(const char* name, void* stream, const void* ws) {
+        nvtxRangePushA(name);
+        g_call_stream = static_cast<cudaStream_t>(stream);
+        g_call_ws = ws;
+    }
+    ~CallScope() { nvtxRangePop(); }
+};
+#define EAGLE_CALL(stream, ws) CallScope eagle_call_scope_(__func__, (stream), (ws))
+
 int launch_result(cudaError_t e) {
-    if (e == cudaSuccess) return EAGLE_OK;
-    g_last_cuda_error = static_cast<int>(e);
-    return EAGLE_ERR_LAUNCH;
+    if (e != cudaSuccess) {
+        g_last_cuda_error = static_cast<int>(e);
+        return EAGLE_ERR_LAUNCH;
+    }
+#ifdef EAGLE_DEBUG
+    // Checked builds: the call waits for its work (outside stream capture) and
+    // reports a fault of its own kernels: a failed execution, or the
+    // workspace's status word (left set for eagle_status_fetch).
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(g_call_stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+        return EAGLE_OK;
+    cudaError_t se = cudaStreamSynchronize(g_call_stream);
+    if (se != cudaSuccess) {
+        g_last_cuda_error = static_cast<int>(se);
+        return EAGLE_ERR_LAUNCH;
+    }
+    if (g_call_ws != nullptr) {
+        int v = 0;
+        if (cudaMemcpy(&v, g_call_ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return EAGLE_ERR_LAUNCH;
+        if (v != 0) return v == 2 ? EAGLE_ERR_TIMEOUT : EAGLE_ERR_DEVICE;
+    }
+#endif
+    return EAGLE_OK;
 }
 
 }  // namespace
@@ -110,6 +147,7 @@ size_t eagle_workspace_bytes(const eagle_tree_cfg* cfg) {
 }
 
 int eagle_tree_init(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, void* stream) {
+    EAGLE_CALL(stream, ws);
     TreeDims d;
     TreeWs w;
     int rc = resolve(cfg, &d);
@@ -136,6 +174,7 @@ static int expand_call(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int
 int eagle_expand(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int step, const void* draft_logits,
                  const float* row_lse_in, float* row_lse, int32_t* frontier_tokens, int32_t* frontier_count,
                  void* stream) {
+    EAGLE_CALL(stream, ws);
     return expand_call(cfg, ws, ws_bytes, step, draft_logits, row_lse_in, row_lse, frontier_tokens, frontier_count,
                        stream, false);
 }
@@ -143,6 +182,7 @@ int eagle_expand(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int step,
 int eagle_expand_sampled(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int step, const void* draft_logits,
                          const float* row_lse_in, uint64_t seed, uint64_t cycle, float* row_lse,
                          int32_t* frontier_tokens, int32_t* frontier_count, void* stream) {
+    EAGLE_CALL(stream, ws);
     const uint64_t sc[2] = {seed, cycle};
     return expand_call(cfg, ws, ws_bytes, step, draft_logits, row_lse_in, row_lse, frontier_tokens, frontier_count,
                        stream, false, sc);
@@ -151,12 +191,14 @@ int eagle_expand_sampled(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, i
 int eagle_test_expand_starved(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int step,
                               const void* draft_logits, float* row_lse, int32_t* frontier_tokens,
                               int32_t* frontier_count, void* stream) {
+    EAGLE_CALL(stream, ws);
     return expand_call(cfg, ws, ws_bytes, step, draft_logits, nullptr, row_lse, frontier_tokens, frontier_count,
                        stream, true);
 }
 
 int eagle_lmhead(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int hidden_dim, const void* hidden,
                  const void* weight, void* draft_logits, void* stream) {
+    EAGLE_CALL(stream, ws);
     TreeDims d;
     TreeWs w;
     int rc = resolve(cfg, &d);
@@ -178,6 +220,7 @@ size_t eagle_lmhead_topk_scratch_bytes(const eagle_tree_cfg* cfg) {
 int eagle_lmhead_topk(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int hidden_dim, const void* hidden,
                       const void* weight, void* scratch, size_t scratch_bytes, float* row_lse, int32_t* topk_ids,
                       float* topk_logits, void* stream) {
+    EAGLE_CALL(stream, ws);
     TreeDims d;
     TreeWs w;
     int rc = resolve(cfg, &d);
@@ -196,6 +239,7 @@ int eagle_lmhead_topk(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int 
 }
 
 int eagle_rerank(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, void* stream) {
+    EAGLE_CALL(stream, ws);
     TreeDims d;
     TreeWs w;
     int rc = resolve(cfg, &d);
@@ -205,6 +249,7 @@ int eagle_rerank(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, void* str
 }
 
 int eagle_tree_value(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, float* value_sum, void* stream) {
+    EAGLE_CALL(stream, ws);
     TreeDims d;
     TreeWs w;
     int rc = resolve(cfg, &d);
@@ -217,6 +262,7 @@ int eagle_tree_value(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, float
 int eagle_build_tree(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, const int32_t* prefix_len,
                      const int32_t* root_token, int32_t* tokens, int32_t* parent, int32_t* depth, int32_t* pos_ids,
                      uint32_t* mask, int32_t* n_tree, void* stream) {
+    EAGLE_CALL(stream, ws);
     TreeDims d;
     TreeWs w;
     int rc = resolve(cfg, &d);
@@ -237,6 +283,7 @@ size_t eagle_attention_workspace_bytes(const eagle_kv_cfg* kv, int T) {
 int eagle_tree_attention(const eagle_kv_cfg* kv, int T, const void* q, const void* kv_cache, int layer,
                          const int32_t* prefix_len, const uint32_t* mask, const int32_t* n_tree, void* out, void* ws,
                          size_t ws_bytes, void* stream) {
+    EAGLE_CALL(stream, ws);
     KvDims k;
     int rc = resolve_kv(kv, &k);
     if (rc != EAGLE_OK) return rc;
@@ -253,6 +300,7 @@ int eagle_verify(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int mode,
                  uint64_t cycle, const void* target_logits, const void* draft_logits, const int32_t* tokens,
                  const int32_t* parent, const int32_t* n_tree, int32_t* accept_len, int32_t* accepted_slots,
                  int32_t* out_tokens, void* stream) {
+    EAGLE_CALL(stream, ws);
     TreeDims d;
     TreeWs w;
     int rc = resolve(cfg, &d);
@@ -281,6 +329,7 @@ int eagle_verify(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int mode,
 int eagle_shard_partials(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int rows, int shard_vocab,
                          int vocab_offset, const void* logits, float* part_max_sum, uint64_t* part_keys,
                          void* stream) {
+    EAGLE_CALL(stream, ws);
     TreeDims d;
     TreeWs w;
     int rc = resolve(cfg, &d);
@@ -299,6 +348,7 @@ int eagle_shard_partials(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, i
 int eagle_shard_merge(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int n_shards, int rows,
                       const float* part_max_sum, const uint64_t* part_keys, float* row_lse, int32_t* topk_ids,
                       float* topk_logits, int32_t* row_argmax, void* stream) {
+    EAGLE_CALL(stream, ws);
     TreeDims d;
     TreeWs w;
     int rc = resolve(cfg, &d);
@@ -316,6 +366,7 @@ int eagle_shard_merge(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int 
 int eagle_expand_topk(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int step, const int32_t* topk_ids,
                       const float* topk_logits, const float* row_lse_in, float* row_lse, int32_t* frontier_tokens,
                       int32_t* frontier_count, void* stream) {
+    EAGLE_CALL(stream, ws);
     TreeDims d;
     TreeWs w;
     int rc = resolve(cfg, &d);
@@ -331,6 +382,7 @@ int eagle_expand_topk(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, int 
 int eagle_verify_argmax(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, const int32_t* row_argmax,
                         const int32_t* tokens, const int32_t* parent, const int32_t* n_tree, int32_t* accept_len,
                         int32_t* accepted_slots, int32_t* out_tokens, void* stream) {
+    EAGLE_CALL(stream, ws);
     TreeDims d;
     TreeWs w;
     int rc = resolve(cfg, &d);
@@ -344,6 +396,7 @@ int eagle_verify_argmax(const eagle_tree_cfg* cfg, void* ws, size_t ws_bytes, co
 
 int eagle_kv_compact(const eagle_kv_cfg* kv, void* kv_cache, const int32_t* prefix_len, const int32_t* accept_len,
                      const int32_t* accepted_slots, int slots_stride, int32_t* new_len, void* ws, void* stream) {
+    EAGLE_CALL(stream, ws);
     KvDims k;
     int rc = resolve_kv(kv, &k);
     if (rc != EAGLE_OK) return rc;
@@ -375,6 +428,7 @@ int eagle_status_fetch(void* ws, int* device_status, void* stream) {
 int eagle_tree_export(const eagle_tree_cfg* cfg, const void* ws, size_t ws_bytes, int32_t* cand_token,
                       int32_t* cand_parent, int32_t* cand_depth, float* cand_logv, uint8_t* cand_valid, uint8_t* kept,
                       int32_t* n_kept, void* stream) {
+    EAGLE_CALL(stream, ws);
     TreeDims d;
     TreeWs w;
     int rc = resolve(cfg, &d);
@@ -398,6 +452,7 @@ int eagle_tree_export(const eagle_tree_cfg* cfg, const void* ws, size_t ws_bytes
 
 int eagle_verify_export(const eagle_tree_cfg* cfg, const void* ws, size_t ws_bytes, float* row_max,
                         int32_t* row_argmax, uint64_t* row_mass, void* stream) {
+    EAGLE_CALL(stream, ws);
     TreeDims d;
     TreeWs w;
     int rc = resolve(cfg, &d);
@@ -417,6 +472,7 @@ int eagle_verify_export(const eagle_tree_cfg* cfg, const void* ws, size_t ws_byt
 
 int eagle_test_sampling(const uint32_t* words, const float* ys, int n, float* gumbel_out, float* log_out,
                         void* stream) {
+    EAGLE_CALL(stream, nullptr);
     if (n < 0 || (words && !gumbel_out) || (ys && !log_out)) return EAGLE_ERR_INVALID_ARG;
     if (n == 0) return EAGLE_OK;
     return launch_result(launch_sampling_probe(words, ys, n, gumbel_out, log_out, static_cast<cudaStream_t>(stream)));

@@ -31,6 +31,20 @@ __device__ __forceinline__ void raise_status(int* status, int code) {
     if (status != nullptr) atomicCAS(status, 0, code);
 }
 
+// Checked builds (EAGLE_DEBUG): an index that the release kernels take on
+// trust from an earlier kernel (a node id read from the workspace, a slot
+// from a scan) is tested before use; out of range, the status word gets
+// kDevBadIndex and the caller skips the access. Release builds: always true.
+__device__ __forceinline__ bool checked_index(bool ok, int* status) {
+    if (!ok) raise_status(status, kDevBadIndex);
+    return ok;
+}
+#ifdef EAGLE_DEBUG
+#define EAGLE_CHECKED(cond, status) (::eagle::checked_index((cond), (status)))
+#else
+#define EAGLE_CHECKED(cond, status) (true)
+#endif
+
 // --------------------------------------------------------------- sort keys ---
 // Float -> unsigned with the same order (-0 and +0 are one value).
 __device__ __forceinline__ uint32_t f2o(float f) {

@@ -686,7 +686,8 @@ __global__ void __launch_bounds__(kRowThreads, SAMP ? 3 : 5) expand_kernel(TreeD
             float plogv = 0.0f;
             if (rank == 0 && f < F) {
                 parent = w.fnode[(step * d.B + b) * d.k + f];
-                if (parent >= 0) plogv = w.cand_logv[static_cast<size_t>(b) * d.C + parent];
+                if (parent >= 0 && EAGLE_CHECKED(parent < d.C, w.status))
+                    plogv = w.cand_logv[static_cast<size_t>(b) * d.C + parent];
             }
             sm.F = F;
             sm.parent = parent;
@@ -721,7 +722,7 @@ __global__ void __launch_bounds__(kRowThreads, SAMP ? 3 : 5) expand_kernel(TreeD
         const uint64_t key = sm.top[tid];
         const int id = base + f * d.k + tid;
         const size_t at = static_cast<size_t>(b) * d.C + id;
-        if (key != 0) {
+        if (key != 0 && EAGLE_CHECKED(id < d.C && key_id(key) < static_cast<uint32_t>(d.V), w.status)) {
             // the child's logit (sampled drafting: the key holds the perturbed value)
             const float x = SAMP ? (DT == 1 ? __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(
                                                                    row_base)[key_id(key)]) << 16)
@@ -1171,8 +1172,8 @@ __global__ void __launch_bounds__(kRowThreads) expand_topk_kernel(TreeDims d, Tr
         const size_t src = (static_cast<size_t>(b) * d.k + fr) * d.k + r;
         const int tok = topk_id[src];
         uint64_t sk = 0ull;
-        if (tok >= 0 && tok < d.V) {
-            const int parent = w.fnode[(step * d.B + b) * d.k + fr];
+        const int parent = w.fnode[(step * d.B + b) * d.k + fr];
+        if (tok >= 0 && tok < d.V && EAGLE_CHECKED(parent < d.C && base + i < d.C, w.status)) {
             const float plogv = parent < 0 ? 0.0f : __ldcg(&w.cand_logv[static_cast<size_t>(b) * d.C + parent]);
             const float lse = lse_in[b * d.k + fr];
             const float lp = __fsub_rn(topk_val[src], lse);

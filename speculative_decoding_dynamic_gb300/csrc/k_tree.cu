@@ -115,7 +115,8 @@ __global__ void __launch_bounds__(kSortThreads) rerank_kernel(TreeDims d, TreeWs
             }
         }
         const int keep = min(d.N, n_valid);
-        if (tid < keep) w.kept[static_cast<size_t>(b) * d.C + key_id(v)] = 1;
+        if (tid < keep && EAGLE_CHECKED(key_id(v) < static_cast<uint32_t>(d.C), w.status))
+            w.kept[static_cast<size_t>(b) * d.C + key_id(v)] = 1;
         if (tid == 0) w.n_kept[b] = keep;
         return;
     }
@@ -139,7 +140,7 @@ __global__ void __launch_bounds__(kSortThreads) rerank_kernel(TreeDims d, TreeWs
     const int keep = min(d.N, n_valid);
     for (int r = tid; r < keep; r += kSortThreads) {
         const uint32_t id = key_id(keys[r]);
-        w.kept[static_cast<size_t>(b) * d.C + id] = 1;
+        if (EAGLE_CHECKED(id < static_cast<uint32_t>(d.C), w.status)) w.kept[static_cast<size_t>(b) * d.C + id] = 1;
     }
     if (tid == 0) w.n_kept[b] = keep;
 }
@@ -170,6 +171,10 @@ __global__ void __launch_bounds__(kBuildThreads) build_tree_kernel(TreeDims d, T
     pdl_wait_prior();
     const int L = prefix_len[b];
     if (tid == 0 && L < 0) raise_status(w.status, kDevBadIndex);
+#ifdef EAGLE_DEBUG
+    for (int i = tid; i < kMaxSlots; i += kBuildThreads) node_at[i] = -1;  // slots no kept node fills stay -1
+    __syncthreads();
+#endif
 
     // Exclusive scan of the kept flags in node-id order gives each kept node its slot.
     const size_t base = static_cast<size_t>(b) * d.C;
@@ -224,7 +229,9 @@ __global__ void __launch_bounds__(kBuildThreads) build_tree_kernel(TreeDims d, T
             pos[r] = L;
         } else {
             const int id = node_at[i];
+            if (!EAGLE_CHECKED(id >= 0 && id < d.C, w.status)) continue;
             const int pn = par_node[id];
+            if (!EAGLE_CHECKED(pn >= -1 && pn < d.C, w.status)) continue;
             const int ps = pn < 0 ? 0 : slot_of[pn];
             if (ps < 0) raise_status(w.status, kDevOverflow);  // parent not kept: cannot happen
             const int dep = dep_of[id];
@@ -242,6 +249,7 @@ __global__ void __launch_bounds__(kBuildThreads) build_tree_kernel(TreeDims d, T
                     mrow[sl / 32] |= 1u << (sl % 32);
                 const int p = par_node[cur];
                 if (p < 0) break;
+                if (!EAGLE_CHECKED(p < d.C && slot_of[p] >= 0 && slot_of[p] < sl, w.status)) break;
                 cur = p;
                 sl = slot_of[p];
             }

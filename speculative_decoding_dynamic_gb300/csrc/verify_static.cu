@@ -16,6 +16,7 @@
 // The kernels are the ones eagle_verify launches; only the place of the
 // scratch differs.
 
+#include <nvtx3/nvToolsExt.h>
 #include <mutex>
 
 #include "../../include/eagle.h"
@@ -71,6 +72,10 @@ extern "C" int eagle_verify_static(const eagle_tree_cfg* cfg, int mode, float te
                                    uint64_t cycle, const void* target_logits, const int32_t* tokens,
                                    const int32_t* parent, const int32_t* n_tree, int32_t* accept_len,
                                    int32_t* accepted_slots, int32_t* out_tokens, void* stream) {
+    struct Range {  // NVTX range over the call
+        Range() { nvtxRangePushA("eagle_verify_static"); }
+        ~Range() { nvtxRangePop(); }
+    } range;
     if (cfg == nullptr) return EAGLE_ERR_INVALID_ARG;
     // Same checks as eagle_verify, through its public size query.
     if (eagle_workspace_bytes(cfg) == 0) return EAGLE_ERR_INVALID_ARG;
@@ -114,5 +119,16 @@ extern "C" int eagle_verify_static(const eagle_tree_cfg* cfg, int mode, float te
     if (cudaMemsetAsync(base, 0, kOffTicket + d.B * sizeof(int), s) != cudaSuccess) return EAGLE_ERR_LAUNCH;
     const cudaError_t e = launch_verify(d, w, mode, inv_t, target_logits, tokens, parent, n_tree,
                                         verify_rng(seed, cycle), accept_len, accepted_slots, out_tokens, s);
-    return e == cudaSuccess ? EAGLE_OK : EAGLE_ERR_LAUNCH;
+    if (e != cudaSuccess) return EAGLE_ERR_LAUNCH;
+#ifdef EAGLE_DEBUG
+    // checked builds: wait (outside stream capture) and report the call's own device fault
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusNone) {
+        if (cudaStreamSynchronize(s) != cudaSuccess) return EAGLE_ERR_LAUNCH;
+        int v = 0;
+        if (cudaMemcpy(&v, w.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return EAGLE_ERR_LAUNCH;
+        if (v != 0) return v == 2 ? EAGLE_ERR_TIMEOUT : EAGLE_ERR_DEVICE;
+    }
+#endif
+    return EAGLE_OK;
 }

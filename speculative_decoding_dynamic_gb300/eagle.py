@@ -13,10 +13,14 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libeagle.so")
+# EAGLE_DEBUG=1: the checked library (each launching call waits and returns
+# its own kernels' device status; internal indices range-checked)
+DEBUG = os.environ.get("EAGLE_DEBUG", "0") not in ("", "0")
+LIB_PATH = os.path.join(_HERE, "libeagle_debug.so" if DEBUG else "libeagle.so")
 if not os.path.exists(LIB_PATH):
-    raise ImportError(f"libeagle.so is missing ({LIB_PATH}); build it with "
-                      "`python -m speculative_decoding_dynamic_gb300.build` (nvcc, sm_103a)")
+    raise ImportError(f"{os.path.basename(LIB_PATH)} is missing ({LIB_PATH}); build it with "
+                      "`python -m speculative_decoding_dynamic_gb300.build" + (" --debug" if DEBUG else "") +
+                      "` (nvcc, sm_103a)")
 _lib = ctypes.CDLL(LIB_PATH)
 
 EAGLE_OK = 0
