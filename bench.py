@@ -212,9 +212,9 @@ def stop_clocks(h) -> dict | None:
 CSRC = os.path.join(ROOT, "speculative_decoding_dynamic_gb300", "csrc")
 # translation unit(s) of each profiled kernel (attention: the per-item kernel
 # and the persistent pipeline, either may run depending on the shape)
-KERNEL_TU = {"expand_kernel": "k_rows.cu", "verify_kernel": "k_rows.cu",
+KERNEL_TU = {"expand_kernel": "k_rows.cu", "verify_kernel": ("k_rows.cu", "k_draft.cu"),
              "attention": ("k_attn_tc.cu", "k_attn_pipe.cu"), "lmhead_kernel": "k_lmhead.cu",
-             "kv_compact_kernel": "k_compact.cu"}
+             "lmhead_topk_kernel": "k_lmhead.cu", "kv_compact_kernel": "k_compact.cu"}
 
 
 def _toolchain_id() -> bytes:
@@ -782,7 +782,7 @@ def run_workload(args, w, variant: dict, seed: int, ws_: int, rank: int, local: 
                  "lmhead": lm_bytes}[dom]
     achieved = dom_bytes / (kt[dom] * 1e-3) / 1e9
     kname = {"expand_step": "expand_kernel", "attention": "attention", "verify": "verify_kernel",
-             "lmhead": "lmhead_kernel"}[dom]
+             "lmhead": "lmhead_topk_kernel" if args.fused_head else "lmhead_kernel"}[dom]
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(achieved / hbm_peak, 4), "traffic": ncu_traffic(kname, w.name), "kernel": kname,
                 "peak_source": f"{peak_src} hbm_gbs (burst copy)",
