@@ -424,21 +424,9 @@ struct LosslessSmem {
     unsigned long long removed_mass[kMaxTopK];
     int child[kMaxTopK];
     unsigned long long s_left;
-    unsigned long long prun;  // mass before the bonus piece
     int next, nrem;
-    int bad, bonus, holder, pq;
+    int bad, bonus, holder;
 };
-
-// Inclusive prefix sum over the lanes of a warp.
-__device__ __forceinline__ unsigned long long warp_incl_u64(unsigned long long v) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long y = shfl_u64(v, max(lane - o, 0));
-        if (lane >= o) v += y;
-    }
-    return v;
-}
 
 // u24 * S < P * 2^24 for u24 < 2^24, S < 2^64, P < 2^41, in 64-bit halves.
 __device__ __forceinline__ bool accept_u24(uint32_t u24, unsigned long long S, unsigned long long P) {
@@ -490,14 +478,6 @@ __global__ void __launch_bounds__(kWalkThreads) verify_lossless_walk_kernel(Tree
     // rounds of kWalkVec vectors per thread, the same in every CTA (their control flow must agree)
     const int rounds = (seg / EPV + kWalkThreads * kWalkVec - 1) / (kWalkThreads * kWalkVec);
     pdl_launch_dependents();
-    // uniform word c of sequence b: Philox4x32-10 at counter (c, b, cycle),
-    // word 0 (kernel arguments only: drawn before the dependency wait)
-    for (int c = tid; c < T + 2; c += kWalkThreads) {
-        const uint32_t ctr[4] = {static_cast<uint32_t>(c), static_cast<uint32_t>(b), rng.c2, rng.c3};
-        uint32_t out[4];
-        sampling::philox4x32_10(ctr, rng.k0, rng.k1, out);
-        sm.uni[c] = out[0];
-    }
     pdl_wait_prior();
 
     const int n = n_tree[b];
@@ -515,6 +495,13 @@ __global__ void __launch_bounds__(kWalkThreads) verify_lossless_walk_kernel(Tree
         // the mass of slot c's token in its parent's row, from the row kernel (which had the parent row streaming)
         sm.pmass[c] = c > 0 ? __ldcg(&w.pmass[tb + c]) : 0ull;
     }
+    // uniform word c of sequence b: Philox4x32-10 at counter (c, b, cycle), word 0
+    for (int c = tid; c < T + 2; c += kWalkThreads) {
+        const uint32_t ctr[4] = {static_cast<uint32_t>(c), static_cast<uint32_t>(b), rng.c2, rng.c3};
+        uint32_t out[4];
+        sampling::philox4x32_10(ctr, rng.k0, rng.k1, out);
+        sm.uni[c] = out[0];
+    }
     __syncthreads();
     for (int c = 1 + tid; c < nn; c += kWalkThreads) {
         const int tk = sm.tok[c], p = sm.par[c];
@@ -523,10 +510,6 @@ __global__ void __launch_bounds__(kWalkThreads) verify_lossless_walk_kernel(Tree
     __syncthreads();
     const bool bad = sm.bad != 0;
     int parity = 0;
-    // the last row's vectors of this thread and their masses (a one-round
-    // slice: the bonus draw then needs no second read)
-    uint4 ru[kWalkVec];
-    unsigned long long rvm[kWalkVec];
     // Integer mass of row `cur` summed over the cluster: every CTA returns the
     // total and keeps its pieces (sm.piece) and every CTA's share (sm.part).
     auto row_mass = [&](int cur) -> unsigned long long {
@@ -535,24 +518,21 @@ __global__ void __launch_bounds__(kWalkThreads) verify_lossless_walk_kernel(Tree
         const uint64_t neg_m2 = f2_pack(-M, -M), inv_t2 = f2_pack(inv_t, inv_t);
         for (int rd = 0; rd < rounds; ++rd) {
             const int vb = rd * kWalkThreads * kWalkVec + warp * 32 * kWalkVec + lane;
+            uint4 u[kWalkVec];
 #pragma unroll
             for (int j = 0; j < kWalkVec; ++j)
                 if (vb + j * 32 < nvec)
-                    ru[j] = __ldcg(reinterpret_cast<const uint4*>(row + (static_cast<size_t>(lo) + (vb + j * 32) * EPV) * ES));
-            unsigned long long tm = 0;
+                    u[j] = __ldcg(reinterpret_cast<const uint4*>(row + (static_cast<size_t>(lo) + (vb + j * 32) * EPV) * ES));
+            uint32_t ahi = 0, alo = 0;  // at most 64 elements: no overflow
 #pragma unroll
             for (int j = 0; j < kWalkVec; ++j) {
-                uint32_t ahi = 0, alo = 0;  // 16 bytes: at most 8 elements
-                if (vb + j * 32 < nvec) {
-                    float x[EPV];
-                    unpack_vec<DT>(ru[j], x);
+                if (vb + j * 32 >= nvec) continue;
+                float x[EPV];
+                unpack_vec<DT>(u[j], x);
 #pragma unroll
-                    for (int e = 0; e < EPV; e += 2) pair_mass_parts(x[e], x[e + 1], neg_m2, inv_t2, ahi, alo);
-                }
-                rvm[j] = mass_of_parts(ahi, alo);
-                tm += rvm[j];
+                for (int e = 0; e < EPV; e += 2) pair_mass_parts(x[e], x[e + 1], neg_m2, inv_t2, ahi, alo);
             }
-            const unsigned long long ws = warp_sum_u64(tm);
+            const unsigned long long ws = warp_sum_u64(mass_of_parts(ahi, alo));
             if (lane == 0) sm.piece[rd * kWalkWarps + warp] = ws;
         }
         __syncthreads();
@@ -629,155 +609,90 @@ __global__ void __launch_bounds__(kWalkThreads) verify_lossless_walk_kernel(Tree
         // running mass exceeds t = floor(U64 S / 2^64). The CTA whose slice
         // holds the draw finds its piece, then the element (one vector per
         // thread, block scan).
-        // the removed tokens (cur's rejected children, in shared memory): their mass in [y0, y1)
+        int rtok[kMaxTopK];
+        unsigned long long rmass[kMaxTopK];
+#pragma unroll
+        for (int i = 0; i < kMaxTopK; ++i) {
+            rtok[i] = i < nrem ? sm.removed_tok[i] : -1;
+            rmass[i] = i < nrem ? sm.removed_mass[i] : 0ull;
+        }
         auto removed_in = [&](int y0, int y1) -> unsigned long long {
             unsigned long long m = 0;
-            for (int i = 0; i < nrem; ++i) {
-                const int t = sm.removed_tok[i];
-                if (t >= y0 && t < y1) m += sm.removed_mass[i];
-            }
+#pragma unroll
+            for (int i = 0; i < kMaxTopK; ++i)
+                if (rtok[i] >= y0 && rtok[i] < y1) m += rmass[i];
             return m;
-        };
-        auto is_removed = [&](int y) -> bool {
-            bool r = false;
-            for (int i = 0; i < nrem; ++i) r |= sm.removed_tok[i] == y;
-            return r;
         };
         const uint64_t U64 = (static_cast<uint64_t>(sm.uni[T + 1]) << 32) | sm.uni[T];
         const unsigned long long tdraw = __umul64hi(U64, S);
-        if (rounds == 1) {
-            // One-round slices: prefix sums over the CTAs' shares give the
-            // holder, over its warps' pieces the piece; the piece is one
-            // warp's vectors, still in its registers with their masses.
-            if (warp == 0) {
-                const unsigned long long sh =
-                    lane < kWalkCtas ? sm.part[lane] - removed_in(min(V, lane * seg), min(V, lane * seg + seg)) : 0ull;
-                const unsigned long long inc = warp_incl_u64(sh);
-                const unsigned hb = __ballot_sync(0xffffffffu, lane < kWalkCtas && tdraw < inc);
-                const int holder = hb ? __ffs(hb) - 1 : -1;
-                unsigned long long run = holder >= 0 ? shfl_u64(inc - sh, holder) : 0ull;
-                int pq = -1;
-                if (holder == rank) {
-                    const int y0 = lo + lane * 32 * kWalkVec * EPV, y1 = min(hi, y0 + 32 * kWalkVec * EPV);
-                    const unsigned long long m =
-                        lane < kWalkWarps && y0 < hi ? sm.piece[lane] - removed_in(y0, y1) : 0ull;
-                    const unsigned long long pin = warp_incl_u64(m);
-                    const unsigned pb = __ballot_sync(0xffffffffu, lane < kWalkWarps && tdraw < run + pin);
-                    pq = pb ? __ffs(pb) - 1 : -1;
-                    if (pq >= 0) run += shfl_u64(pin - m, pq);
+        // every CTA knows which slice holds the draw (the same shares everywhere)
+        int holder = -1;
+        unsigned long long before = 0, upto = 0;  // this CTA's prefix; the running prefix over all CTAs
+        for (int r = 0; r < kWalkCtas; ++r) {
+            const unsigned long long share = sm.part[r] - removed_in(min(V, r * seg), min(V, r * seg + seg));
+            if (holder < 0 && share > 0 && tdraw >= upto && tdraw < upto + share) holder = r;
+            if (r < rank) before += share;
+            upto += share;
+        }
+        if (tid == 0) sm.holder = holder;
+        if (holder == rank) {
+            // the piece: (round, warp) ranges in element order
+            int pq = -1;
+            unsigned long long run = before;
+            for (int q = 0; q < rounds * kWalkWarps; ++q) {
+                const int v0 = (q / kWalkWarps) * kWalkThreads * kWalkVec + (q % kWalkWarps) * 32 * kWalkVec;
+                const int y0 = lo + v0 * EPV, y1 = min(hi, y0 + 32 * kWalkVec * EPV);
+                const unsigned long long m = y0 < hi ? sm.piece[q] - removed_in(y0, y1) : 0ull;
+                if (m > 0 && tdraw < run + m) {
+                    pq = q;
+                    break;
                 }
-                if (lane == 0) {
-                    sm.holder = holder;
-                    sm.pq = pq;
-                    sm.prun = run;
-                }
+                run += m;
             }
+            // thread (warp j < kWalkVec, lane l) takes vector v0 + 32 j + l of the piece (element order)
+            const int v0 = pq < 0 ? 0 : (pq / kWalkWarps) * kWalkThreads * kWalkVec + (pq % kWalkWarps) * 32 * kWalkVec;
+            const int v = v0 + warp * 32 + lane;
+            const int y0 = lo + v * EPV;
+            uint64_t em[EPV];
+            unsigned long long vm = 0;
+            if (pq >= 0 && warp < kWalkVec && v < nvec) {
+                const char* row = static_cast<const char*>(target) + (tb + cur) * V * ES;
+                const uint4 u = __ldcg(reinterpret_cast<const uint4*>(row + static_cast<size_t>(y0) * ES));
+                const float M = sm.rmax[cur];
+                const uint64_t neg_m2 = f2_pack(-M, -M), inv_t2 = f2_pack(inv_t, inv_t);
+                float x[EPV];
+                unpack_vec<DT>(u, x);
+#pragma unroll
+                for (int e = 0; e < EPV; e += 2) pair_mass2(x[e], x[e + 1], neg_m2, inv_t2, em[e], em[e + 1]);
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) {
+#pragma unroll
+                    for (int i = 0; i < kMaxTopK; ++i)
+                        if (rtok[i] == y0 + e) em[e] = 0;
+                    vm += em[e];
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) em[e] = 0;
+            }
+            unsigned long long incl = vm;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long y = shfl_u64(incl, max(lane - o, 0));
+                if (lane >= o) incl += y;
+            }
+            if (lane == 31) sm.wsum[warp] = incl;
             __syncthreads();
-            if (sm.holder == rank && warp == sm.pq) {
-                // vector j of lane l is vector 32 j + l of the piece: element order is (j, l)
-                const int pv0 = warp * 32 * kWalkVec;
-                const bool adj = removed_in(lo + pv0 * EPV, min(hi, lo + (pv0 + 32 * kWalkVec) * EPV)) != 0ull;
-                unsigned long long base = sm.prun;
-                bool found = false;  // (flags, not breaks: the loops stay unrolled, the arrays in registers)
+            unsigned long long ex = run + incl - vm;
+            for (int i = 0; i < warp; ++i) ex += sm.wsum[i];
+            if (vm > 0 && tdraw >= ex && tdraw < ex + vm) {
+                unsigned long long rr = ex;
 #pragma unroll
-                for (int j = 0; j < kWalkVec; ++j) {
-                    if (found) continue;
-                    const int v = pv0 + j * 32 + lane;
-                    const int y0 = lo + v * EPV;
-                    unsigned long long m = v < nvec ? rvm[j] : 0ull;
-                    if (adj && v < nvec) m -= removed_in(y0, y0 + EPV);
-                    const unsigned long long inc = warp_incl_u64(m);
-                    const unsigned hit = __ballot_sync(0xffffffffu, tdraw < base + inc);
-                    if (hit && lane == __ffs(hit) - 1) {
-                        const float M = sm.rmax[cur];
-                        const uint64_t neg_m2 = f2_pack(-M, -M), inv_t2 = f2_pack(inv_t, inv_t);
-                        float x[EPV];
-                        unpack_vec<DT>(ru[j], x);
-                        uint64_t em[EPV];
-#pragma unroll
-                        for (int e = 0; e < EPV; e += 2) pair_mass2(x[e], x[e + 1], neg_m2, inv_t2, em[e], em[e + 1]);
-                        unsigned long long rr = base + inc - m;
-                        int y = -1;
-#pragma unroll
-                        for (int e = 0; e < EPV; ++e) {
-                            if (is_removed(y0 + e)) em[e] = 0;
-                            rr += em[e];
-                            if (y < 0 && rr > tdraw) y = y0 + e;
-                        }
-                        sm.bonus = y;
-                    }
-                    found = hit != 0u;
-                    base += shfl_u64(inc, 31);
-                }
-            }
-        } else {
-            // every CTA knows which slice holds the draw (the same shares everywhere)
-            int holder = -1;
-            unsigned long long before = 0, upto = 0;  // this CTA's prefix; the running prefix over all CTAs
-            for (int r = 0; r < kWalkCtas; ++r) {
-                const unsigned long long share = sm.part[r] - removed_in(min(V, r * seg), min(V, r * seg + seg));
-                if (holder < 0 && share > 0 && tdraw >= upto && tdraw < upto + share) holder = r;
-                if (r < rank) before += share;
-                upto += share;
-            }
-            if (tid == 0) sm.holder = holder;
-            if (holder == rank) {
-                // the piece: (round, warp) ranges in element order
-                int pq = -1;
-                unsigned long long run = before;
-                for (int q = 0; q < rounds * kWalkWarps; ++q) {
-                    const int v0 = (q / kWalkWarps) * kWalkThreads * kWalkVec + (q % kWalkWarps) * 32 * kWalkVec;
-                    const int y0 = lo + v0 * EPV, y1 = min(hi, y0 + 32 * kWalkVec * EPV);
-                    const unsigned long long m = y0 < hi ? sm.piece[q] - removed_in(y0, y1) : 0ull;
-                    if (m > 0 && tdraw < run + m) {
-                        pq = q;
+                for (int e = 0; e < EPV; ++e) {
+                    rr += em[e];
+                    if (rr > tdraw) {
+                        sm.bonus = y0 + e;
                         break;
-                    }
-                    run += m;
-                }
-                // thread (warp j < kWalkVec, lane l) takes vector v0 + 32 j + l of the piece (element order)
-                const int v0 = pq < 0 ? 0 : (pq / kWalkWarps) * kWalkThreads * kWalkVec + (pq % kWalkWarps) * 32 * kWalkVec;
-                const int v = v0 + warp * 32 + lane;
-                const int y0 = lo + v * EPV;
-                uint64_t em[EPV];
-                unsigned long long vm = 0;
-                if (pq >= 0 && warp < kWalkVec && v < nvec) {
-                    const char* row = static_cast<const char*>(target) + (tb + cur) * V * ES;
-                    const uint4 u = __ldcg(reinterpret_cast<const uint4*>(row + static_cast<size_t>(y0) * ES));
-                    const float M = sm.rmax[cur];
-                    const uint64_t neg_m2 = f2_pack(-M, -M), inv_t2 = f2_pack(inv_t, inv_t);
-                    float x[EPV];
-                    unpack_vec<DT>(u, x);
-#pragma unroll
-                    for (int e = 0; e < EPV; e += 2) pair_mass2(x[e], x[e + 1], neg_m2, inv_t2, em[e], em[e + 1]);
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e) {
-                        if (is_removed(y0 + e)) em[e] = 0;
-                        vm += em[e];
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e) em[e] = 0;
-                }
-                unsigned long long incl = vm;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const unsigned long long y = shfl_u64(incl, max(lane - o, 0));
-                    if (lane >= o) incl += y;
-                }
-                if (lane == 31) sm.wsum[warp] = incl;
-                __syncthreads();
-                unsigned long long ex = run + incl - vm;
-                for (int i = 0; i < warp; ++i) ex += sm.wsum[i];
-                if (vm > 0 && tdraw >= ex && tdraw < ex + vm) {
-                    unsigned long long rr = ex;
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e) {
-                        rr += em[e];
-                        if (rr > tdraw) {
-                            sm.bonus = y0 + e;
-                            break;
-                        }
                     }
                 }
             }

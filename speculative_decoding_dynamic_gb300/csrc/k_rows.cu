@@ -847,10 +847,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
     constexpr int ES = DT == 1 ? 2 : 4;
     constexpr int EPV = 16 / ES;
     constexpr int CE = kRowChunkBytes / ES;
-    // Greedy: the next kernel may start at once. Lossless: the walk kernel
-    // follows, and its CTAs (waiting for this grid) would sit beside the
-    // streaming CTAs; they are let in only once this CTA's pass is done.
-    if (MODE == 0) pdl_launch_dependents();
+    pdl_launch_dependents();
     if (tid == kProducerWarp * 32) {  // the segment's head into L2 while the previous kernel finishes
         const int cp = rank * seg;
         const int np = max(0, min(seg, d.V - cp));
@@ -930,7 +927,6 @@ __global__ void __launch_bounds__(kRowThreads) verify_kernel(TreeDims d, TreeWs 
         if (lane == 0) sm.wkey[warp] = key;
     }
     __syncthreads();
-    if (MODE == 1) pdl_launch_dependents();
     if (warp == 0) {
         uint64_t m = lane < kConsumerWarps ? sm.wkey[lane] : 0ull;
         m = warp_max_u64(m);
