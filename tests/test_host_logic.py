@@ -7,7 +7,9 @@ maximum), and for bf16 rows it keeps just the top 16 order bits of each group
 maximum. This models that rule on the kernel's data layout and checks that
 the admitted keys always contain the exact top-k (value descending, equal
 values by lower id), on random rows, heavy ties, negative rows, -inf entries
-and a ragged tail. It does not run or import any CUDA code.
+and a ragged tail. It does not run or import any CUDA code. The end of the
+file models two rules of the LM head with stage 1 in its epilogue (its
+32-bit list keys and its merge's candidate bound).
 """
 import numpy as np
 import pytest
@@ -155,3 +157,75 @@ def test_sampling_philox_matches_the_input_generator(sampling_host):
         sampling_host.t_philox(c.ctypes.data_as(ctypes.c_void_p), k.ctypes.data_as(ctypes.c_void_p),
                                o.ctypes.data_as(ctypes.c_void_p))
         assert np.array_equal(o, synth.philox(c, k))
+
+
+# ----------------------------------------------- LM head with stage 1 ---
+#
+# Models of two rules of eagle_lmhead_topk. (1) An epilogue thread keeps its
+# row's best keys as 32-bit words for bf16 logits: the top 16 order bits of
+# the value, then 0xFFFF minus the entry's position in the CTA's scan (which
+# grows with the token id), so a larger word is a larger value, then a lower
+# id, and the value decodes exactly. (2) The merge keeps, among the CTAs'
+# sorted k-key lists, the keys at or above max(largest k-th key, k-th largest
+# first key); that set must hold the row's whole top-k.
+
+def _list_key(bits16, pos):
+    o = _f2o(synth.bf16_to_f32(bits16))
+    return (o & np.uint32(0xFFFF0000)) | (np.uint32(0xFFFF) - pos.astype(np.uint32))
+
+
+def _list_val(word):
+    hi = word & np.uint32(0xFFFF0000)
+    o = hi | np.where((hi & np.uint32(0x80000000)) != 0, np.uint32(0), np.uint32(0xFFFF))
+    b = np.where((o & np.uint32(0x80000000)) != 0, o & np.uint32(0x7FFFFFFF), ~o).astype(np.uint32)
+    return b.view(np.float32)
+
+
+def test_bf16_list_keys_order_like_value_then_lower_id_and_decode_exactly():
+    rng = np.random.default_rng(3)
+    special = np.array([0x0000, 0x8000, 0x7F80, 0xFF80, 0x3F80, 0xBF80, 0x0001, 0x8001, 0x7F7F, 0xFF7F],
+                       np.uint16)  # +0, -0, +inf, -inf, +1, -1, denormals, max finite
+    bits = np.concatenate([special, rng.integers(0, 1 << 16, 3000).astype(np.uint16),
+                           np.repeat(np.uint16(0x4100), 40)])  # runs of equal values
+    bits = bits[((bits & 0x7F80) != 0x7F80) | ((bits & 0x007F) == 0)]  # no NaN patterns
+    pos = rng.permutation(bits.size).astype(np.int64)  # distinct scan positions < 2^16
+    words = _list_key(bits, pos)
+    x = synth.bf16_to_f32(bits).astype(np.float64)
+    x[x == 0] = 0.0  # -0 and +0 are one value
+    order_words = np.argsort(-words.astype(np.int64), kind="stable")
+    order_ref = np.lexsort((pos, -x))  # value descending, then lower position
+    assert (order_words == order_ref).all()
+    dec = _list_val(words)
+    same = (dec == synth.bf16_to_f32(bits)) | ((dec == 0) & (synth.bf16_to_f32(bits) == 0))
+    assert same.all()
+
+
+def _merge_candidates(lists, k):
+    """Keys the merge kernel ranks: >= max(largest k-th key, k-th largest first key)."""
+    kth = max(int(l[k - 1]) for l in lists)
+    firsts = sorted((int(l[0]) for l in lists), reverse=True)
+    kth_first = firsts[k - 1] if len(firsts) >= k and firsts[k - 1] != 0 else 0
+    th = max(kth, kth_first)
+    return [int(x) for l in lists for x in l if x != 0 and x >= th]
+
+
+@pytest.mark.parametrize("case", ["random", "one_partial_holds_all", "identical_partials", "sparse", "few_keys"])
+@pytest.mark.parametrize("S,k", [(152, 10), (30, 16), (4, 8), (3, 1)])
+def test_merge_bound_keeps_the_whole_topk(case, S, k):
+    rng = np.random.default_rng(S * 100 + k)
+    n_per = 200
+    vals = rng.normal(size=(S, n_per)).astype(np.float32)
+    if case == "one_partial_holds_all":
+        vals[0] += 10.0
+    elif case == "identical_partials":
+        vals[:] = vals[0]
+    elif case == "sparse":
+        vals[rng.random(vals.shape) < 0.97] = -np.inf
+    ids = np.arange(S * n_per).reshape(S, n_per)
+    keys = _keys(_f2o(vals.reshape(-1)), ids.reshape(-1)).reshape(S, n_per)
+    if case == "few_keys":  # partials with fewer than k entries (zero padding)
+        keys[:, max(1, k // 2):] = 0
+    lists = [np.concatenate([np.sort(r[r != 0])[::-1], np.zeros(k, np.uint64)])[:k] for r in keys]
+    everything = np.sort(keys[keys != 0].reshape(-1))[::-1][:k]
+    cand = np.sort(np.array(_merge_candidates(lists, k), np.uint64))[::-1][:k]
+    assert np.array_equal(cand, everything)
