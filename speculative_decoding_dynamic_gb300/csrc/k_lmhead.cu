@@ -273,6 +273,7 @@ struct TkParams {
     int nkc;    // hidden stages per tile
     int stages, stage_bytes;
     int a_bytes;  // hidden box of a stage (the W box follows it)
+    int cb_warps; // epilogue warps with live rows: each has a candidate buffer after the ring
     int bf16;   // logits rounded to bf16 (else fp32)
     uint32_t tmem_cols;
     float2* part_ms;      // [cpb, M]
@@ -420,6 +421,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         const bool warp_live = rb * kTkRows + q4 * 32 < p.M;
         const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
         float m = -INFINITY, s = 0.0f;
+        // this lane's candidate buffer: slot t at cb[t * 32] (32 slots, one chunk)
+        KeyT* const cb = reinterpret_cast<KeyT*>(smem + p.stages * p.stage_bytes) + q4 * 32 * 32 + lane;
         KeyT top[KL];  // the KL >= k largest keys so far, best first (0 = none)
 #pragma unroll
         for (int i = 0; i < KL; ++i) top[i] = KeyT(0);
@@ -470,18 +473,29 @@ __global__ void __launch_bounds__(kLmThreads, 1)
                 // keys of the chunk that may enter the list
                 const uint32_t pos0 = static_cast<uint32_t>(ts * p.Nv + c);
                 // (a group's best possible key: its maximum at its first position)
-                const bool cand = live && (list_key<KeyT>(cm, pos0) > top[KL - 1] || cm != cm);
+                // Candidates: each lane first stages the keys of its groups
+                // that may enter its list (against the list's last key before
+                // the chunk), then inserts its own; the warp runs the
+                // insertion network for the largest count among its lanes,
+                // not for every entry any lane has.
+                const KeyT thr = top[KL - 1];
+                const bool cand = live && (list_key<KeyT>(cm, pos0) > thr || cm != cm);
                 if (__any_sync(0xffffffffu, cand)) {
+                    int nc = 0;
 #pragma unroll
                     for (int g = 0; g < 8; ++g) {
-                        const bool gc = live && (list_key<KeyT>(gm[g], pos0 + 4 * g) > top[KL - 1] || gm[g] != gm[g]);
-                        if (!__any_sync(0xffffffffu, gc)) continue;
+                        if (cand && (list_key<KeyT>(gm[g], pos0 + 4 * g) > thr || gm[g] != gm[g])) {
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int i = 4 * g + j;
-                            const KeyT key = (live && i < nv) ? list_key<KeyT>(x[i], pos0 + i) : KeyT(0);
-                            if (key > top[KL - 1]) list_insert(top, key);
+                            for (int j = 0; j < 4; ++j) {
+                                const int i = 4 * g + j;
+                                const KeyT key = i < nv ? list_key<KeyT>(x[i], pos0 + i) : KeyT(0);
+                                if (key > thr) cb[(nc++) * 32] = key;
+                            }
                         }
+                    }
+                    for (int t = 0; t < nc; ++t) {
+                        const KeyT key = cb[t * 32];
+                        if (key > top[KL - 1]) list_insert(top, key);
                     }
                 }
             }
@@ -615,7 +629,7 @@ __global__ void __launch_bounds__(kLmMergeThreads) lm_merge_kernel(int S, int M,
 
 template <typename KeyT, int KL>
 cudaError_t launch_topk_gemm(const TkParams& p, const CUtensorMap& tw, const CUtensorMap& th, cudaStream_t stream) {
-    const int smem = p.stages * p.stage_bytes + 1024;
+    const int smem = p.stages * p.stage_bytes + p.cb_warps * 32 * 32 * static_cast<int>(sizeof(KeyT)) + 1024;
     cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(lmhead_topk_kernel<KeyT, KL>), smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(lmhead_topk_kernel<KeyT, KL>, dim3(p.nrb * p.cpb), dim3(kLmThreads), static_cast<size_t>(smem),
@@ -694,7 +708,10 @@ cudaError_t launch_lmhead_topk(int M, int V, int H, int k, const void* hidden, c
     const int hbox = p.nrb == 1 ? (M + 15) & ~15 : kTkRows;
     p.a_bytes = hbox * kKC * 2;
     p.stage_bytes = p.a_bytes + p.Nv * kKC * 2;
-    p.stages = (kSmemBudget - 1024) / p.stage_bytes;  // (1 KB left for the static barriers)
+    // candidate buffers (32 keys per lane) for the epilogue warps with live rows
+    p.cb_warps = p.nrb > 1 ? 4 : (M + 31) / 32;
+    const int cb_bytes = p.cb_warps * 32 * 32 * (p.bf16 ? 4 : 8);
+    p.stages = (kSmemBudget - 1024 - cb_bytes) / p.stage_bytes;  // (1 KB left for the static barriers)
     if (p.stages > kTkMaxStages) p.stages = kTkMaxStages;
     if (p.stages > p.nkc) p.stages = p.nkc < 2 ? 2 : p.nkc;
     p.tmem_cols = 2 * static_cast<uint32_t>(p.Nv);
